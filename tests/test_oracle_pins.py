@@ -1,0 +1,349 @@
+"""Pins for the fp64 oracle: checks against what the pages and mathematics fix,
+none of which re-runs the oracle's own loop.
+
+  * hand-worked values (tests/golden/scalar_recurrence.txt);
+  * brute-force expansion of the recurrence as explicit matrix products in the
+    state form `state <- state @ W + U` of the SANA `fused_cam_gdn.py` page
+    (`_torch_cam_scan_single_chunk`), T <= 8;
+  * closed forms: beta = 0 and g = 0 leave the state unchanged; full reset;
+    a single token; exact key-value retrieval with orthonormal keys;
+    mutually orthogonal keys turn the delta rule into gated linear attention
+    (forward, reverse, per-key gate, denominator), computed as a masked
+    matrix product;
+  * invariants: split/resume equivalence (SANA `fused_cam_gdn.py` page,
+    `_cam_scan_kernel` init/final state contract), reverse == flip-and-shift
+    (same page, `_torch_cam_scan_reference`), varlen packing == separate
+    sequences.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "scalar_recurrence.txt")
+
+
+def _golden():
+    d = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, vals = line.split(":", 1)
+        d[key.strip()] = np.array([float(x) for x in vals.split()])
+    return d
+
+
+def _one(x):
+    """(T, ...) single-sequence single-head arrays -> (1, T, 1, ...)."""
+    return x[None, :, None]
+
+
+def _run1(q, k, v, beta, g=None, gk=None, h0=None, reverse=False):
+    out, hf = oracle.scan(_one(q), _one(k), _one(v), _one(beta),
+                          g=None if g is None else _one(g),
+                          gk=None if gk is None else _one(gk),
+                          h0=None if h0 is None else h0[None, None],
+                          reverse=reverse, threads=1)
+    return out[0, :, 0], hf[0, 0]
+
+
+# ----------------------------------------------------------------- golden ---
+
+def test_golden_scalar_cases():
+    G = _golden()
+    for case, K in (("A", 1), ("C", 1), ("D", 2)):
+        T = len(G[f"{case}.v"])
+        q = G[f"{case}.q"].reshape(T, K)
+        k = G[f"{case}.k"].reshape(T, K)
+        v = G[f"{case}.v"].reshape(T, 1)
+        beta = G[f"{case}.beta"]
+        h0 = G[f"{case}.h0"].reshape(K, 1)
+        dec = G[f"{case}.decay"]
+        if dec.size == T:
+            out, hf = _run1(q, k, v, beta, g=np.log(dec), h0=h0)
+        else:
+            out, hf = _run1(q, k, v, beta, gk=np.log(dec.reshape(T, K)), h0=h0)
+        np.testing.assert_allclose(out[:, 0], G[f"{case}.out"], rtol=1e-14, atol=1e-14)
+        np.testing.assert_allclose(hf[:, 0], G[f"{case}.h_final"], rtol=1e-14, atol=1e-14)
+    T = 3
+    out, _ = _run1(G["A.q"].reshape(T, 1), G["A.k"].reshape(T, 1),
+                   G["A.v"].reshape(T, 1), G["A.beta"], g=np.log(G["A.decay"]),
+                   reverse=True)
+    np.testing.assert_allclose(out[:, 0], G["A.rev_out"], rtol=1e-14, atol=1e-14)
+
+
+def test_golden_prep():
+    G = _golden()
+    y = oracle.l2norm(G["P.l2_in"][None], eps=0.0)
+    np.testing.assert_allclose(y[0], G["P.l2_out"], rtol=1e-15)
+    x = G["P.rms_in"].reshape(1, 1, 2, 2)
+    y, inv = oracle.rmsnorm_channels(x, eps=0.0, relu=True, scale=2.0)
+    np.testing.assert_allclose(inv.ravel(), G["P.rms_inv"], rtol=1e-15)
+    np.testing.assert_allclose(y.ravel(), G["P.rms_out"], rtol=1e-15, atol=0)
+
+
+# ------------------------------------------------------------ brute force ---
+
+def _brute(q, k, v, beta, g=None, gk=None, h0=None):
+    """M = S^T (V x K). Each token's map is M <- M W_t + U_t with
+    W_t = D_t (I - beta_t k_t k_t^T), U_t = beta_t v_t k_t^T, D_t the decay.
+    M_t is expanded as M_0 W_1..W_t + sum_s U_s W_{s+1}..W_t with every
+    product formed explicitly."""
+    T, K = k.shape
+    V = v.shape[1]
+    I = np.eye(K)
+    W, U = [], []
+    for t in range(T):
+        D = np.diag(np.exp(gk[t])) if gk is not None else np.exp(g[t]) * I
+        W.append(D @ (I - beta[t] * np.outer(k[t], k[t])))
+        U.append(beta[t] * np.outer(v[t], k[t]))
+
+    def chain(a, b):  # W_a W_{a+1} ... W_b  (identity if a > b)
+        P = I.copy()
+        for i in range(a, b + 1):
+            P = P @ W[i]
+        return P
+
+    M0 = np.zeros((V, K)) if h0 is None else h0.T
+    outs = []
+    M = M0
+    for t in range(T):
+        M = M0 @ chain(0, t)
+        for s in range(t + 1):
+            M = M + U[s] @ chain(s + 1, t)
+        outs.append(M @ q[t])
+    return np.array(outs), M.T
+
+
+@pytest.mark.parametrize("T,K,V,perkey", [(1, 3, 2, False), (5, 4, 3, False),
+                                          (8, 3, 5, False), (7, 4, 2, True),
+                                          (8, 6, 6, True)])
+def test_brute_force_expansion(T, K, V, perkey):
+    rng = np.random.default_rng(100 + T * 10 + K)
+    q, k = rng.standard_normal((T, K)), rng.standard_normal((T, K)) * 0.6
+    v = rng.standard_normal((T, V))
+    beta = rng.uniform(0.1, 1.0, T)
+    h0 = rng.standard_normal((K, V))
+    if perkey:
+        gk = -rng.uniform(0.0, 1.0, (T, K))
+        got = _run1(q, k, v, beta, gk=gk, h0=h0)
+        ref = _brute(q, k, v, beta, gk=gk, h0=h0)
+    else:
+        g = -rng.uniform(0.0, 1.0, T)
+        got = _run1(q, k, v, beta, g=g, h0=h0)
+        ref = _brute(q, k, v, beta, g=g, h0=h0)
+    np.testing.assert_allclose(got[0], ref[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got[1], ref[1], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ closed forms ---
+
+def test_beta0_g0_state_unchanged():
+    rng = np.random.default_rng(1)
+    T, K, V = 13, 5, 4
+    q, k, v = rng.standard_normal((T, K)), rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    h0 = rng.standard_normal((K, V))
+    out, hf = _run1(q, k, v, np.zeros(T), g=np.zeros(T), h0=h0)
+    assert np.array_equal(hf, h0)
+    np.testing.assert_allclose(out, q @ h0, rtol=1e-14, atol=1e-14)
+
+
+def test_full_reset():
+    """g = -inf: exp(g) = 0 wipes the state before each write, so
+    o_t = beta_t (q_t . k_t) v_t whatever h0 was."""
+    rng = np.random.default_rng(2)
+    T, K, V = 9, 4, 3
+    q, k, v = rng.standard_normal((T, K)), rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    beta = rng.uniform(0, 1, T)
+    out, hf = _run1(q, k, v, beta, g=np.full(T, -np.inf), h0=rng.standard_normal((K, V)))
+    ref = (beta * np.sum(q * k, axis=1))[:, None] * v
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(hf, beta[-1] * np.outer(k[-1], v[-1]), rtol=1e-13)
+
+
+def test_single_token_closed_form():
+    """T = 1: S = a h0 + beta k (v - a h0^T k)^T, o = S^T q, with a = e^g."""
+    rng = np.random.default_rng(3)
+    K, V = 6, 5
+    q, k, v = rng.standard_normal((1, K)), rng.standard_normal((1, K)), rng.standard_normal((1, V))
+    h0 = rng.standard_normal((K, V))
+    b, g = np.array([0.7]), np.array([-0.4])
+    a = np.exp(g[0])
+    S = a * h0 + b[0] * np.outer(k[0], v[0] - a * h0.T @ k[0])
+    out, hf = _run1(q, k, v, b, g=g, h0=h0)
+    np.testing.assert_allclose(hf, S, rtol=1e-13)
+    np.testing.assert_allclose(out[0], S.T @ q[0], rtol=1e-13)
+
+
+def test_orthonormal_key_value_retrieval():
+    """beta = 1, g = 0, orthonormal keys: after writing (k_i, v_i) the memory
+    returns v_i for k_i exactly, and later orthogonal writes leave it."""
+    rng = np.random.default_rng(4)
+    T, K, V = 6, 8, 5
+    Qm, _ = np.linalg.qr(rng.standard_normal((K, K)))
+    k = Qm[:, :T].T
+    v = rng.standard_normal((T, V))
+    idx = np.array([rng.integers(0, t + 1) for t in range(T)])  # i(t) <= t
+    q = k[idx]
+    out, hf = _run1(q, k, v, np.ones(T), g=np.zeros(T))
+    np.testing.assert_allclose(out, v[idx], atol=1e-13)
+    np.testing.assert_allclose(k @ hf, v, atol=1e-13)
+
+
+def _orth_keys(rng, T, K, scale=True):
+    Qm, _ = np.linalg.qr(rng.standard_normal((K, K)))
+    k = Qm[:, :T].T
+    if scale:
+        k = k * rng.uniform(0.5, 2.0, (T, 1))
+    return k
+
+
+def test_orthogonal_keys_is_gated_linear_attention():
+    """Mutually orthogonal keys and h0 = 0: the prediction S^T k_t is always 0,
+    so delta_t = beta_t v_t and
+      o_t = sum_{j<=t} exp(G_t - G_j) beta_j (q_t . k_j) v_j,  G = cumsum g."""
+    rng = np.random.default_rng(5)
+    T, K, V = 10, 12, 4
+    k = _orth_keys(rng, T, K)
+    q, v = rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    beta, g = rng.uniform(0.1, 1, T), -rng.uniform(0, 0.7, T)
+    G = np.cumsum(g)
+    L = np.tril(np.exp(G[:, None] - G[None, :]))
+    ref = ((q @ k.T) * L * beta[None, :]) @ v
+    out, _ = _run1(q, k, v, beta, g=g)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    # the denominator: the same with v = 1
+    d = oracle.den(_one(q), _one(k), _one(beta), g=_one(g))[0, 0]
+    np.testing.assert_allclose(d, ((q @ k.T) * L * beta[None, :]).sum(1), rtol=1e-12, atol=1e-12)
+
+
+def test_orthogonal_keys_reverse_closed_form():
+    """Reverse scan, orthogonal keys: token p reads tokens j > p,
+      o_p = sum_{j>p} beta_j (q_p . k_j) v_j exp(g_{p+1} + ... + g_{j-1}),
+    i.e. no self term and a token's own gate does not decay its own write."""
+    rng = np.random.default_rng(6)
+    T, K, V = 9, 10, 3
+    k = _orth_keys(rng, T, K)
+    q, v = rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    beta, g = rng.uniform(0.1, 1, T), -rng.uniform(0, 0.7, T)
+    ref = np.zeros((T, V))
+    for p in range(T):
+        for j in range(p + 1, T):
+            ref[p] += beta[j] * (q[p] @ k[j]) * v[j] * np.exp(g[p + 1:j].sum())
+    out, _ = _run1(q, k, v, beta, g=g, reverse=True)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_disjoint_keys_per_key_gate_closed_form():
+    """Keys on distinct coordinate axes stay orthogonal under any per-key
+    decay, so o_t = sum_{j<=t} beta_j (sum_d q_td k_jd e^{Gk_td - Gk_jd}) v_j."""
+    rng = np.random.default_rng(7)
+    T, K, V = 7, 9, 4
+    perm = rng.permutation(K)[:T]
+    k = np.zeros((T, K))
+    k[np.arange(T), perm] = rng.uniform(0.5, 2.0, T)
+    q, v = rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    beta, gk = rng.uniform(0.1, 1, T), -rng.uniform(0, 0.7, (T, K))
+    Gk = np.cumsum(gk, axis=0)
+    ref = np.zeros((T, V))
+    for t in range(T):
+        for j in range(t + 1):
+            a = np.sum(q[t] * k[j] * np.exp(Gk[t] - Gk[j]))
+            ref[t] += beta[j] * a * v[j]
+    out, _ = _run1(q, k, v, beta, gk=gk)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+# -------------------------------------------------------------- invariants ---
+
+def test_split_resume_equivalence():
+    rng = np.random.default_rng(8)
+    T, K, V, t0 = 40, 6, 5, 17
+    q, k, v = rng.standard_normal((T, K)), rng.standard_normal((T, K)) * 0.4, rng.standard_normal((T, V))
+    beta, gk = rng.uniform(0, 1, T), -rng.uniform(0, 0.3, (T, K))
+    full_o, full_h = _run1(q, k, v, beta, gk=gk)
+    pre_o, pre_h = _run1(q[:t0], k[:t0], v[:t0], beta[:t0], gk=gk[:t0])
+    suf_o, suf_h = _run1(q[t0:], k[t0:], v[t0:], beta[t0:], gk=gk[t0:], h0=pre_h)
+    assert np.array_equal(full_o, np.concatenate([pre_o, suf_o]))
+    assert np.array_equal(full_h, suf_h)
+
+
+def _flip_shift(x, pad):
+    y = np.flip(x, 0)
+    return np.concatenate([np.full((1,) + x.shape[1:], pad), y[:-1]], 0)
+
+
+def test_reverse_equals_flip_and_shift():
+    """Reverse scan == forward scan on q flipped, k, v, beta flipped and
+    shifted (pad 0), gate flipped and shifted (pad log 1 = 0), flipped back."""
+    rng = np.random.default_rng(9)
+    T, K, V = 23, 5, 4
+    q, k, v = rng.standard_normal((T, K)), rng.standard_normal((T, K)) * 0.5, rng.standard_normal((T, V))
+    beta, g = rng.uniform(0, 1, T), -rng.uniform(0, 0.5, T)
+    rev, _ = _run1(q, k, v, beta, g=g, reverse=True)
+    fwd, _ = _run1(np.flip(q, 0), _flip_shift(k, 0.0), _flip_shift(v, 0.0),
+                   _flip_shift(beta, 0.0), g=_flip_shift(g, 0.0))
+    np.testing.assert_allclose(rev, np.flip(fwd, 0), rtol=1e-13, atol=1e-13)
+    assert np.all(rev[-1] == 0.0)
+
+
+def test_varlen_packing_equals_separate_sequences():
+    rng = np.random.default_rng(10)
+    lens = [5, 1, 12, 0, 7]
+    T, H, K, V = sum(lens), 3, 4, 3
+    q, k = rng.standard_normal((1, T, H, K)), rng.standard_normal((1, T, H, K)) * 0.5
+    v = rng.standard_normal((1, T, H, V))
+    beta, g = rng.uniform(0, 1, (1, T, H)), -rng.uniform(0, 0.5, (1, T, H))
+    h0 = rng.standard_normal((len(lens), H, K, V))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    out, hf = oracle.scan(q, k, v, beta, g=g, h0=h0, cu_seqlens=cu)
+    for s in range(len(lens)):
+        a, b = cu[s], cu[s + 1]
+        o_s, h_s = oracle.scan(q[:, a:b], k[:, a:b], v[:, a:b], beta[:, a:b],
+                               g=g[:, a:b], h0=h0[s:s + 1])
+        assert np.array_equal(out[:, a:b], o_s)
+        assert np.array_equal(hf[s], h_s[0])
+    assert np.array_equal(hf[3], h0[3])  # empty sequence passes h0 through
+
+
+def test_threads_do_not_change_results():
+    rng = np.random.default_rng(11)
+    B, T, H, K, V = 2, 30, 5, 4, 3
+    args = [rng.standard_normal((B, T, H, K)), rng.standard_normal((B, T, H, K)),
+            rng.standard_normal((B, T, H, V)), rng.uniform(0, 1, (B, T, H))]
+    g = -rng.uniform(0, 1, (B, T, H))
+    o1, h1 = oracle.scan(*args, g=g, threads=1)
+    o7, h7 = oracle.scan(*args, g=g, threads=7)
+    assert np.array_equal(o1, o7) and np.array_equal(h1, h7)
+
+
+# -------------------------------------------------------------------- prep ---
+
+def test_l2norm_invariants():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((50, 64)) * rng.uniform(0.1, 10, (50, 1))
+    y = oracle.l2norm(x, eps=1e-6)
+    n2 = (x * x).sum(1)
+    # y = c x with c > 0, and |y|^2 = n2 / (n2 + eps)
+    c = (y * x).sum(1) / n2
+    np.testing.assert_allclose(y, c[:, None] * x, rtol=1e-14)
+    np.testing.assert_allclose((y * y).sum(1), n2 / (n2 + 1e-6), rtol=1e-13)
+    # scale invariance when eps = 0
+    np.testing.assert_allclose(oracle.l2norm(3.5 * x, eps=0.0), oracle.l2norm(x, eps=0.0), rtol=1e-14)
+
+
+def test_rmsnorm_channels_invariants():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((2, 7, 4, 6)) * rng.uniform(0.2, 5, (2, 7, 1, 1))
+    y, inv = oracle.rmsnorm_channels(x, eps=0.0)
+    np.testing.assert_allclose((y ** 2).mean(axis=(2, 3)), 1.0, rtol=1e-13)
+    yr, _ = oracle.rmsnorm_channels(x, eps=0.0, relu=True, scale=0.25)
+    np.testing.assert_allclose(yr, 0.25 * np.maximum(y, 0.0), rtol=1e-15)
+    # channels of other heads matter: the norm is over all H*D channels
+    x2 = x.copy()
+    x2[:, :, 1] *= 3.0
+    y2, _ = oracle.rmsnorm_channels(x2, eps=0.0)
+    assert not np.allclose(y2[:, :, 0], y[:, :, 0])

@@ -1,0 +1,237 @@
+"""Seeded synthetic inputs for the gated delta rule forward scan.
+
+This module is shared by the tests, the benchmark and the smoke check. It
+draws random numbers and encodes them into storage types; it holds none of
+the scan's arithmetic (no normalisation, no recurrence, no gating maths), so
+that the fp64 oracle and the CUDA path both consume identical stored values
+without sharing any computation.
+
+Recipe (every workload, seed 0 unless stated):
+  * q, k, v ~ N(0, 1), drawn in float32 and rounded to the storage dtype
+    (bf16 by round-to-nearest-even, or kept in fp32).
+  * beta = sigmoid(N(0, 1)) per (token, head), stored fp32.
+  * g = log(sigmoid(N(mu, 1))) per (token, head), stored fp32 (mu = 3, or 4
+    for the video workload); for the per-key workload gk has the same law per
+    (token, head, key channel) with mu = 4.
+  * varlen lengths: integers uniform on [128, 8192] inclusive; initial states
+    h0 ~ N(0, 0.02^2) per sequence.
+Each tensor gets its own generator seeded by (seed, tensor id, block index)
+so that tensors are independent of one another and of the thread count used
+to fill them; numpy's PCG64 is platform independent, so the Arm GPU host and
+the x86 build host draw identical values.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import dataclasses
+import os
+
+import numpy as np
+
+BLOCK = 1 << 22  # elements per independently seeded block
+
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "g": 5, "gk": 6, "h0": 7,
+               "lens": 8, "qkv": 9}
+
+
+def _normal_f32(seed: int, name: str, n: int, mu: float = 0.0,
+                sigma: float = 1.0) -> np.ndarray:
+    """n draws of N(mu, sigma^2) as float32, filled block by block."""
+    out = np.empty(n, dtype=np.float32)
+    tid = _TENSOR_IDS[name]
+    nblk = (n + BLOCK - 1) // BLOCK
+
+    def fill(b: int) -> None:
+        lo, hi = b * BLOCK, min(n, (b + 1) * BLOCK)
+        rng = np.random.default_rng([seed, tid, b])
+        x = rng.standard_normal(hi - lo, dtype=np.float32)
+        if sigma != 1.0:
+            x *= np.float32(sigma)
+        if mu != 0.0:
+            x += np.float32(mu)
+        out[lo:hi] = x
+
+    if nblk <= 1:
+        for b in range(nblk):
+            fill(b)
+    else:
+        workers = min(nblk, os.cpu_count() or 1, 16)
+        with _cf.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, range(nblk)))
+    return out
+
+
+def bf16_round_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest even.
+
+    Inputs here are finite; NaN handling is not needed."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclasses.dataclass
+class Stored:
+    """A tensor as stored: `values` (float32, exact) plus its storage dtype.
+
+    For bf16 `bits` holds the uint16 patterns; `values` is their exact
+    float32 upcast."""
+    values: np.ndarray
+    dtype: str  # "f32" | "bf16"
+    bits: np.ndarray | None = None
+
+    @property
+    def shape(self):
+        return self.values.shape
+
+
+def stored_normal(seed: int, name: str, shape, dtype: str, mu=0.0,
+                  sigma=1.0) -> Stored:
+    n = int(np.prod(shape))
+    x = _normal_f32(seed, name, n, mu, sigma).reshape(shape)
+    if dtype == "bf16":
+        bits = bf16_round_bits(x)
+        return Stored(bf16_bits_to_f32(bits).reshape(shape), "bf16", bits.reshape(shape))
+    if dtype == "f32":
+        return Stored(x, "f32")
+    raise ValueError(dtype)
+
+
+def sigmoid_normal(seed: int, name: str, shape, mu: float) -> np.ndarray:
+    """sigmoid(N(mu,1)) as float32 (computed in float64 then rounded)."""
+    x = _normal_f32(seed, name, int(np.prod(shape)), mu).astype(np.float64)
+    return (1.0 / (1.0 + np.exp(-x))).astype(np.float32).reshape(shape)
+
+
+def log_sigmoid_normal(seed: int, name: str, shape, mu: float) -> np.ndarray:
+    """log(sigmoid(N(mu,1))) = -log1p(exp(-x)) as float32."""
+    x = _normal_f32(seed, name, int(np.prod(shape)), mu).astype(np.float64)
+    y = np.where(x > 0, -np.log1p(np.exp(-x)), x - np.log1p(np.exp(x)))
+    return y.astype(np.float32).reshape(shape)
+
+
+@dataclasses.dataclass
+class Workload:
+    """One forward problem. Layouts (row-major):
+    q, k: (B, T, H, K) raw (un-normalised) values; v: (B, T, H, V);
+    beta, g: (B, T, H); gk: (B, T, H, K); h0: (n_seq, H, K, V);
+    cu_seqlens: (n_seq + 1,) int32 when varlen (then B == 1).
+    For the video workload `qkv` (B, T, 3, H, D) holds q, k, v interleaved and
+    q, k, v are views into it."""
+    name: str
+    B: int
+    T: int
+    H: int
+    K: int
+    V: int
+    dtype: str
+    q: Stored
+    k: Stored
+    v: Stored
+    beta: np.ndarray
+    g: np.ndarray | None = None
+    gk: np.ndarray | None = None
+    h0: np.ndarray | None = None
+    cu_seqlens: np.ndarray | None = None
+    qkv: Stored | None = None
+    prep: str = "l2"          # "l2" | "rms_relu"
+    bidirectional: bool = False
+    chunk: int = 64
+
+    @property
+    def n_seq(self) -> int:
+        return self.B if self.cu_seqlens is None else len(self.cu_seqlens) - 1
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.T
+
+
+def _vary_lengths(seed: int, n_seq: int, lo: int, hi: int) -> np.ndarray:
+    rng = np.random.default_rng([seed, _TENSOR_IDS["lens"], 0])
+    return rng.integers(lo, hi + 1, size=n_seq)
+
+
+def make(B: int, T: int, H: int, K: int, V: int, dtype: str = "bf16", *,
+         seed: int = 0, g_mu: float | None = 3.0, gk_mu: float | None = None,
+         h0_std: float | None = None, lengths=None, name: str = "custom",
+         chunk: int = 64) -> Workload:
+    """A causal workload with q, k, v ~ N(0,1), beta = sigmoid(N(0,1)) and a
+    scalar gate (g_mu) or a per-key gate (gk_mu). `lengths` (list of ints)
+    makes it varlen: B must be 1 and T == sum(lengths)."""
+    cu = None
+    n_seq = B
+    if lengths is not None:
+        lengths = [int(x) for x in lengths]
+        assert B == 1 and T == sum(lengths)
+        cu = np.zeros(len(lengths) + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(lengths)
+        n_seq = len(lengths)
+    q = stored_normal(seed, "q", (B, T, H, K), dtype)
+    k = stored_normal(seed, "k", (B, T, H, K), dtype)
+    v = stored_normal(seed, "v", (B, T, H, V), dtype)
+    beta = sigmoid_normal(seed, "beta", (B, T, H), 0.0)
+    g = log_sigmoid_normal(seed, "g", (B, T, H), g_mu) if g_mu is not None else None
+    gk = log_sigmoid_normal(seed, "gk", (B, T, H, K), gk_mu) if gk_mu is not None else None
+    h0 = None
+    if h0_std is not None:
+        h0 = _normal_f32(seed, "h0", n_seq * H * K * V, 0.0, h0_std).reshape(n_seq, H, K, V)
+    return Workload(name, B, T, H, K, V, dtype, q, k, v, beta, g, gk, h0, cu,
+                    chunk=chunk)
+
+
+def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
+               g_mu: float = 4.0, name: str = "video") -> Workload:
+    """Interleaved qkv (B, N, 3, H, D) ~ N(0,1) bf16, bidirectional, with the
+    full-channel RMSNorm + ReLU + k-scale prep."""
+    qkv = stored_normal(seed, "qkv", (B, N, 3, H, D), "bf16")
+    beta = sigmoid_normal(seed, "beta", (B, N, H), 0.0)
+    g = log_sigmoid_normal(seed, "g", (B, N, H), g_mu)
+
+    def part(i):
+        return Stored(qkv.values[:, :, i], "bf16", qkv.bits[:, :, i])
+    return Workload(name, B, N, H, D, D, "bf16", part(0), part(1), part(2),
+                    beta, g, qkv=qkv, prep="rms_relu", bidirectional=True)
+
+
+# The five workloads, named by what they are.
+WORKLOADS = {
+    "causal_f32_b1h2t256d64": dict(kind="dense", B=1, T=256, H=2, K=64, V=64,
+                                   dtype="f32", g_mu=3.0),
+    "causal_bf16_b4h16t4096d128": dict(kind="dense", B=4, T=4096, H=16, K=128,
+                                       V=128, dtype="bf16", g_mu=3.0),
+    "bidir_video_b2h16n8192d112": dict(kind="video", B=2, N=8192, H=16, D=112),
+    "varlen_bf16_64seq_h32d128": dict(kind="varlen", n_seq=64, lo=128, hi=8192,
+                                      H=32, K=128, V=128, h0_std=0.02),
+    "gk_bf16_b1h32t65536k128v256": dict(kind="dense", B=1, T=65536, H=32,
+                                        K=128, V=256, dtype="bf16", g_mu=None,
+                                        gk_mu=4.0),
+}
+
+
+def varlen_lengths(seed: int = 0, n_seq: int = 64, lo: int = 128,
+                   hi: int = 8192) -> list[int]:
+    return [int(x) for x in _vary_lengths(seed, n_seq, lo, hi)]
+
+
+def build(name: str, seed: int = 0) -> Workload:
+    spec = dict(WORKLOADS[name])
+    kind = spec.pop("kind")
+    if kind == "dense":
+        return make(spec["B"], spec["T"], spec["H"], spec["K"], spec["V"],
+                    spec["dtype"], seed=seed, g_mu=spec.get("g_mu"),
+                    gk_mu=spec.get("gk_mu"), name=name)
+    if kind == "video":
+        return make_video(spec["B"], spec["N"], spec["H"], spec["D"], seed=seed,
+                          name=name)
+    if kind == "varlen":
+        lens = varlen_lengths(seed, spec["n_seq"], spec["lo"], spec["hi"])
+        return make(1, sum(lens), spec["H"], spec["K"], spec["V"], "bf16",
+                    seed=seed, g_mu=3.0, h0_std=spec["h0_std"], lengths=lens,
+                    name=name)
+    raise ValueError(kind)
