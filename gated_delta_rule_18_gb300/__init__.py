@@ -1,0 +1,263 @@
+"""GB300 (sm_103a) chunked gated delta rule forward scan.
+
+A thin ctypes binding over libgdn.so (include/gdn.h). PyTorch supplies
+device memory and the current stream; every step of the computation runs in
+the library's CUDA kernels. There is no CPU fallback: if the library is not
+built, or no GPU is present, calls fail loudly.
+
+Entry points mirror the C ABI:
+  gdn_prep, gdn_chunk_fwd, gdn_workspace_size, gdn_status_string,
+  gdn_last_device_error, and gdn_forward (prep + one or both scan directions).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+__all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_workspace_size",
+           "gdn_status_string", "gdn_last_device_error", "gdn_forward", "lib",
+           "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect",
+           "launch_count", "kernel_names"]
+
+F32, BF16 = 0, 1
+PREP_L2, PREP_RMS, PREP_RELU = 0x0, 0x1, 0x10
+ACCUMULATE, QK_L2NORM = 0x1, 0x2
+_STATUS = {0: "GDN_OK", 1: "GDN_ERR_NULL", 2: "GDN_ERR_SHAPE", 3: "GDN_ERR_DTYPE",
+           4: "GDN_ERR_LAYOUT", 5: "GDN_ERR_UNSUPPORTED", 6: "GDN_ERR_CUDA",
+           7: "GDN_ERR_TIMEOUT", 8: "GDN_ERR_WORKSPACE", 9: "GDN_ERR_DEVICE"}
+
+
+class TensorDesc(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("stride_b", ctypes.c_int64), ("stride_t", ctypes.c_int64),
+                ("stride_h", ctypes.c_int64)]
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = _STATUS.get(status, str(status))
+        super().__init__(f"{where}: {self.name} ({gdn_status_string(status)})")
+
+
+_lib = None
+
+
+def lib():
+    """Load libgdn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(f"libgdn.so is not built ({LIB}); run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB)
+    P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    L.gdn_status_string.restype = ctypes.c_char_p
+    L.gdn_status_string.argtypes = [I]
+    L.gdn_workspace_size.restype = ctypes.c_size_t
+    L.gdn_workspace_size.argtypes = [I] * 9
+    L.gdn_prep.restype = I
+    L.gdn_prep.argtypes = [P, TensorDesc, P, TensorDesc, I, I, I, I, I, F, F, P, P]
+    L.gdn_chunk_fwd.restype = I
+    L.gdn_chunk_fwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P,
+                                TensorDesc, P, P, I, I, I, I, I, I, I, I, P,
+                                ctypes.c_size_t, P]
+    L.gdn_last_device_error.restype = I
+    L.gdn_last_device_error.argtypes = [P, P, ctypes.POINTER(I)]
+    L.gdn_kernel_kinds.restype = I
+    L.gdn_kernel_kinds.argtypes = []
+    L.gdn_kernel_name.restype = ctypes.c_char_p
+    L.gdn_kernel_name.argtypes = [I]
+    L.gdn_profile_enable.restype = None
+    L.gdn_profile_enable.argtypes = [I]
+    L.gdn_profile_collect.restype = I
+    L.gdn_profile_collect.argtypes = [ctypes.POINTER(F), ctypes.POINTER(I), I]
+    L.gdn_launch_count.restype = ctypes.c_longlong
+    L.gdn_launch_count.argtypes = []
+    _lib = L
+    return L
+
+
+def gdn_status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise GDNError(3, f"unsupported dtype {t.dtype}")
+
+
+def _desc(t) -> TensorDesc:
+    """Descriptor of a 4-D (B, T, H, D) view with a contiguous last dim."""
+    if t.dim() != 4:
+        raise GDNError(2, f"expected a 4-D (B, T, H, D) tensor, got shape {tuple(t.shape)}")
+    if t.stride(3) != 1:
+        raise GDNError(4, "the last dimension must be contiguous")
+    return TensorDesc(_dtype_code(t), 0, t.stride(0), t.stride(1), t.stride(2))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _f32(t, name):
+    torch = _torch()
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise GDNError(3 if t.dtype != torch.float32 else 4,
+                       f"{name} must be a contiguous float32 tensor")
+    return t
+
+
+def gdn_workspace_size(B, T, H, K, V, n_seq, varlen, dtype, with_den) -> int:
+    return int(lib().gdn_workspace_size(B, T, H, K, V, n_seq, int(bool(varlen)),
+                                        dtype, int(bool(with_den))))
+
+
+def gdn_prep(x, y=None, mode=PREP_L2, scale=1.0, eps=1e-6, inv_rms=None, stream=None):
+    """q/k preparation on the GPU (see include/gdn.h). x: (B, T, H, D).
+    Returns y (allocated like x when not given)."""
+    torch = _torch()
+    B, T, H, D = x.shape
+    if y is None:
+        y = torch.empty((B, T, H, D), dtype=x.dtype, device=x.device)
+    if inv_rms is not None:
+        _f32(inv_rms, "inv_rms")
+    st = lib().gdn_prep(_ptr(x), _desc(x), _ptr(y), _desc(y), B, T, H, D, int(mode),
+                        float(scale), float(eps), _ptr(inv_rms), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_prep")
+    return y
+
+
+def gdn_chunk_fwd(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None, out=None,
+                  h_final=None, den=None, reverse=False, accumulate=False,
+                  qk_l2norm=False, workspace=None, stream=None, out_dtype=None):
+    """One direction of the chunked scan (see include/gdn.h).
+
+    q, k: (B, T, H, K); v: (B, T, H, V); beta, g: (B, T, H) fp32;
+    gk: (B, T, H, K) fp32; h0/h_final: (n_seq, H, K, V) fp32;
+    cu_seqlens: int32 device tensor (n_seq + 1) with B == 1;
+    den: (B, H, T) fp32. Missing `out` / `workspace` are allocated with
+    torch. Returns out."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_contiguous()):
+        raise GDNError(3, "cu_seqlens must be a contiguous int32 tensor")
+    for name, t in (("beta", beta), ("g", g), ("gk", gk), ("h0", h0), ("h_final", h_final),
+                    ("den", den)):
+        _f32(t, name)
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=out_dtype or q.dtype, device=q.device)
+    dt = _dtype_code(q)
+    need = gdn_workspace_size(B, T, H, K, V, n_seq, cu_seqlens is not None, dt, den is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    flags = (ACCUMULATE if accumulate else 0) | (QK_L2NORM if qk_l2norm else 0)
+    st = lib().gdn_chunk_fwd(
+        _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta),
+        _ptr(h0), _ptr(cu_seqlens), n_seq, _ptr(out), _desc(out), _ptr(h_final), _ptr(den),
+        B, T, H, K, V, 64, int(bool(reverse)), flags, _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_chunk_fwd")
+    return out
+
+
+def gdn_last_device_error(workspace, stream=None) -> int:
+    """Synchronise, read and clear the device error word; returns it."""
+    w = ctypes.c_int(0)
+    st = lib().gdn_last_device_error(_ptr(workspace), _stream(stream), ctypes.byref(w))
+    if st not in (0, 9):
+        raise GDNError(st, "gdn_last_device_error")
+    return w.value
+
+
+def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
+                prep="l2", bidirectional=False, with_final_state=False, workspace=None,
+                stream=None):
+    """The whole forward: q/k prep, then the causal scan, or the causal plus
+    the reverse scan summed with the denominator (bidirectional).
+
+    prep: "l2" (per-(token, head) L2 norm fused into the scan), "rms_relu"
+    (full-channel RMSNorm, ReLU, and k scaled by K^-0.5, via gdn_prep), or
+    None (q, k used as given). Returns a dict with "out" and, as requested,
+    "h_final" / "den" / "q_inv_rms" / "k_inv_rms"."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    res = {}
+    fuse = prep == "l2"
+    if prep == "rms_relu":
+        res["q_inv_rms"] = torch.empty((B, T), dtype=torch.float32, device=q.device)
+        res["k_inv_rms"] = torch.empty((B, T), dtype=torch.float32, device=q.device)
+        q = gdn_prep(q, mode=PREP_RMS | PREP_RELU, scale=1.0, eps=1e-5,
+                     inv_rms=res["q_inv_rms"], stream=stream)
+        k = gdn_prep(k, mode=PREP_RMS | PREP_RELU, scale=K ** -0.5, eps=1e-5,
+                     inv_rms=res["k_inv_rms"], stream=stream)
+    elif prep not in ("l2", None):
+        raise ValueError(f"unknown prep {prep!r}")
+    if not bidirectional:
+        hf = (torch.empty((n_seq, H, K, v.shape[3]), dtype=torch.float32, device=q.device)
+              if with_final_state else None)
+        res["out"] = gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, h0=h0, cu_seqlens=cu_seqlens,
+                                   h_final=hf, qk_l2norm=fuse, workspace=workspace,
+                                   stream=stream)
+        if hf is not None:
+            res["h_final"] = hf
+        return res
+    den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    out = gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, cu_seqlens=cu_seqlens, den=den,
+                        qk_l2norm=fuse, workspace=workspace, stream=stream)
+    gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, cu_seqlens=cu_seqlens, den=den, out=out,
+                  reverse=True, accumulate=True, qk_l2norm=fuse, workspace=workspace,
+                  stream=stream)
+    res["out"], res["den"] = out, den
+    return res
+
+
+def kernel_names() -> list[str]:
+    L = lib()
+    return [L.gdn_kernel_name(i).decode() for i in range(L.gdn_kernel_kinds())]
+
+
+def profile_enable(on: bool = True) -> None:
+    lib().gdn_profile_enable(int(bool(on)))
+
+
+def profile_collect() -> dict:
+    """{kernel name: (total device ms, launches)} since the last collect."""
+    L = lib()
+    n = L.gdn_kernel_kinds()
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int * n)()
+    st = L.gdn_profile_collect(ms, cnt, n)
+    if st != 0:
+        raise GDNError(st, "gdn_profile_collect")
+    names = kernel_names()
+    return {names[i]: (float(ms[i]), int(cnt[i])) for i in range(n) if cnt[i]}
+
+
+def launch_count() -> int:
+    return int(lib().gdn_launch_count())

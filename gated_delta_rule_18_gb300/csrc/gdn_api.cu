@@ -1,0 +1,341 @@
+// gdn_api.cu -- the C ABI declared in include/gdn.h: host-side argument
+// checks (everything is validated before the first launch), workspace
+// layout, kernel dispatch and optional per-kernel CUDA-event timing.
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_common.cuh"
+
+namespace {
+
+using gdn::FwdParams;
+
+// ------------------------------------------------------------ profiling ----
+
+enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KNumKinds };
+const char *kKindNames[KNumKinds] = {"prep_l2", "prep_rms", "chunk_table",
+                                     "intra_bf16", "state_bf16", "fused_f32"};
+
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    std::vector<cudaEvent_t> pool;
+    struct Rec {
+        int kind;
+        cudaEvent_t a, b;
+    };
+    std::vector<Rec> recs;
+};
+Profiler &prof() {
+    static Profiler *p = new Profiler();  // never destroyed: safe at exit
+    return *p;
+}
+std::atomic<long long> g_launches{0};
+
+cudaEvent_t take_event(Profiler &P) {
+    if (!P.pool.empty()) {
+        cudaEvent_t e = P.pool.back();
+        P.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+template <class F>
+cudaError_t launch(int kind, cudaStream_t st, F &&f) {
+    Profiler &P = prof();
+    cudaEvent_t a = nullptr, b = nullptr;
+    {
+        std::lock_guard<std::mutex> g(P.mu);
+        if (P.on) {
+            a = take_event(P);
+            b = take_event(P);
+        }
+    }
+    if (a && b) cudaEventRecord(a, st);
+    cudaError_t e = f();
+    if (e == cudaSuccess) g_launches.fetch_add(1);
+    if (a && b) {
+        cudaEventRecord(b, st);
+        std::lock_guard<std::mutex> g(P.mu);
+        P.recs.push_back({kind, a, b});
+    }
+    return e;
+}
+
+// ------------------------------------------------------------- workspace ---
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Ws {
+    size_t err, tab, seq0, w, u, qg, kg, aqk, dec, total;
+    int max_chunks, KP, UW, Vt;
+    int64_t rows;
+};
+
+bool ws_layout(int B, int T, int H, int K, int V, int n_seq, int varlen, int dtype,
+               int with_den, Ws &L) {
+    if (B < 1 || T < 0 || H < 1 || K < 1 || K > 128 || V < 1 || n_seq < 0) return false;
+    if (varlen && (B != 1 || n_seq < 1)) return false;
+    if (!varlen && n_seq != B) return false;
+    if (dtype != GDN_F32 && dtype != GDN_BF16) return false;
+    L.Vt = V + (with_den ? 1 : 0);
+    if (L.Vt > 256) return false;
+    L.rows = (int64_t)B * T;
+    L.KP = K <= 64 ? 64 : 128;
+    L.UW = (L.Vt + 7) / 8 * 8;
+    const int64_t nts = ((int64_t)T + gdn::kChunk - 1) / gdn::kChunk;
+    const int64_t mc = varlen ? nts + n_seq : (int64_t)B * nts;
+    if (mc > (1 << 30) || L.rows > ((int64_t)1 << 40)) return false;
+    L.max_chunks = (int)mc;
+    size_t off = 0;
+    L.err = off;
+    off += kAlign;
+    L.tab = off;
+    off = align_up(off + (varlen ? sizeof(int2) * (size_t)mc : 0));
+    L.seq0 = off;
+    off = align_up(off + (varlen ? sizeof(int) * (size_t)(n_seq + 1) : 0));
+    L.w = L.u = L.qg = L.kg = L.aqk = L.dec = off;
+    if (dtype == GDN_BF16) {
+        const size_t hr = (size_t)H * (size_t)L.rows;
+        L.w = off;
+        off = align_up(off + 2 * hr * L.KP);
+        L.qg = off;
+        off = align_up(off + 2 * hr * L.KP);
+        L.kg = off;
+        off = align_up(off + 2 * hr * L.KP);
+        L.u = off;
+        off = align_up(off + 2 * hr * L.UW);
+        L.aqk = off;
+        off = align_up(off + 2 * hr * gdn::kChunk);
+        L.dec = off;
+        off = align_up(off + 4 * (size_t)H * mc * L.KP);
+    }
+    L.total = off;
+    return true;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+int elem_size(int dtype) { return dtype == GDN_BF16 ? 2 : 4; }
+// strides must keep every row start 16-byte aligned
+bool strides_ok(const gdn_tensor_desc &d) {
+    const int64_t vec = 16 / elem_size(d.dtype);
+    return d.stride_b % vec == 0 && d.stride_t % vec == 0 && d.stride_h % vec == 0 &&
+           d.stride_b >= 0 && d.stride_t >= 0 && d.stride_h >= 0;
+}
+bool dtype_ok(int t) { return t == GDN_F32 || t == GDN_BF16; }
+
+gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL: return "a required pointer is NULL";
+        case GDN_ERR_SHAPE: return "sizes out of range or inconsistent";
+        case GDN_ERR_DTYPE: return "unsupported or mismatched element type";
+        case GDN_ERR_LAYOUT: return "stride, alignment or contiguity not supported";
+        case GDN_ERR_UNSUPPORTED: return "unsupported combination of arguments";
+        case GDN_ERR_CUDA: return "a CUDA call failed";
+        case GDN_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+        case GDN_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+        case GDN_ERR_DEVICE: return "a device-side argument check failed";
+    }
+    return "unknown status";
+}
+
+size_t gdn_workspace_size(int B, int T, int H, int K, int V, int n_seq, int varlen, int dtype,
+                          int with_den) {
+    Ws L;
+    if (!ws_layout(B, T, H, K, V, n_seq, varlen, dtype, with_den, L)) return 0;
+    return L.total;
+}
+
+gdn_status gdn_prep(const void *x, gdn_tensor_desc xd, void *y, gdn_tensor_desc yd, int B,
+                    int T, int H, int D, int mode, float scale, float eps, float *inv_rms,
+                    cudaStream_t stream) {
+    if (!x || !y) return GDN_ERR_NULL;
+    if (B < 1 || T < 0 || H < 1 || D < 1) return GDN_ERR_SHAPE;
+    if (!dtype_ok(xd.dtype) || xd.dtype != yd.dtype) return GDN_ERR_DTYPE;
+    const int base = mode & 0xF;
+    if ((mode & ~0x1F) != 0 || (base != GDN_PREP_L2 && base != GDN_PREP_RMS))
+        return GDN_ERR_UNSUPPORTED;
+    const int vec = 16 / elem_size(xd.dtype);
+    if (D % vec != 0) return GDN_ERR_SHAPE;
+    if (base == GDN_PREP_L2 && D > 256) return GDN_ERR_SHAPE;
+    if (base == GDN_PREP_RMS && (int64_t)H * D > 16384) return GDN_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(y) || !strides_ok(xd) || !strides_ok(yd))
+        return GDN_ERR_LAYOUT;
+    if (inv_rms && (reinterpret_cast<uintptr_t>(inv_rms) & 3)) return GDN_ERR_LAYOUT;
+    if (T == 0) return GDN_OK;
+    const int kind = base == GDN_PREP_RMS ? KPrepRms : KPrepL2;
+    return cuda_status(launch(kind, stream, [&] {
+        return gdn::launch_prep(x, xd.stride_b, xd.stride_t, xd.stride_h, y, yd.stride_b,
+                                yd.stride_t, yd.stride_h, B, T, H, D, xd.dtype == GDN_BF16, mode,
+                                scale, eps, base == GDN_PREP_RMS ? inv_rms : nullptr, stream);
+    }));
+}
+
+gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                         gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
+                         const float *h0, const int32_t *cu_seqlens, int n_seq, void *out,
+                         gdn_tensor_desc od, float *h_final, float *den_out, int B, int T,
+                         int H, int K, int V, int chunk, int reverse, int flags,
+                         void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    // With no tokens the per-token tensors may be empty (NULL); only the
+    // state pass-through h0 -> h_final runs.
+    const bool empty = T == 0;
+    if (!empty && (!q || !k || !v || !beta || !out)) return GDN_ERR_NULL;
+    if (g && gk) return GDN_ERR_UNSUPPORTED;
+    if (!empty && !g && !gk) return GDN_ERR_NULL;
+    if (!workspace) return GDN_ERR_WORKSPACE;
+    if (chunk != gdn::kChunk) return GDN_ERR_SHAPE;
+    if ((flags & ~(GDN_ACCUMULATE | GDN_QK_L2NORM)) != 0) return GDN_ERR_UNSUPPORTED;
+    if (!dtype_ok(qkd.dtype) || !dtype_ok(vd.dtype) || !dtype_ok(od.dtype))
+        return GDN_ERR_DTYPE;
+    if (qkd.dtype != vd.dtype) return GDN_ERR_DTYPE;
+    if (B < 1 || T < 0 || H < 1 || K < 1 || K > 128 || V < 1) return GDN_ERR_SHAPE;
+    if (K % 8 != 0 || V % 8 != 0) return GDN_ERR_SHAPE;
+    if (V + (den_out ? 1 : 0) > 256) return GDN_ERR_SHAPE;
+    const int varlen = cu_seqlens != nullptr;
+    if (varlen && (B != 1 || n_seq < 1)) return GDN_ERR_SHAPE;
+    if (!varlen && n_seq != B) return GDN_ERR_SHAPE;
+    if (reverse != 0 && reverse != 1) return GDN_ERR_SHAPE;
+    if (reverse && (h0 || h_final)) return GDN_ERR_UNSUPPORTED;
+    if (den_out && (h0 || h_final)) return GDN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return GDN_ERR_LAYOUT;  // (NULL counts as aligned)
+    if (!strides_ok(qkd) || !strides_ok(vd) || !strides_ok(od)) return GDN_ERR_LAYOUT;
+    for (const void *f : {(const void *)g, (const void *)gk, (const void *)beta,
+                          (const void *)h0, (const void *)h_final, (const void *)den_out,
+                          (const void *)cu_seqlens})
+        if (f && (reinterpret_cast<uintptr_t>(f) & 3)) return GDN_ERR_LAYOUT;
+    Ws L;
+    if (!ws_layout(B, T, H, K, V, n_seq, varlen, qkd.dtype, den_out != nullptr, L))
+        return GDN_ERR_SHAPE;
+    if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+        return GDN_ERR_WORKSPACE;
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    FwdParams p{};
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.qk_sb = qkd.stride_b;
+    p.qk_st = qkd.stride_t;
+    p.qk_sh = qkd.stride_h;
+    p.v_sb = vd.stride_b;
+    p.v_st = vd.stride_t;
+    p.v_sh = vd.stride_h;
+    p.g = g;
+    p.gk = gk;
+    p.beta = beta;
+    p.h0 = h0;
+    p.cu_seqlens = cu_seqlens;
+    p.out = out;
+    p.o_sb = od.stride_b;
+    p.o_st = od.stride_t;
+    p.o_sh = od.stride_h;
+    p.out_f32 = od.dtype == GDN_F32;
+    p.h_final = h_final;
+    p.den = den_out;
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.K = K;
+    p.V = V;
+    p.n_seq = n_seq;
+    p.reverse = reverse;
+    p.accumulate = (flags & GDN_ACCUMULATE) ? 1 : 0;
+    p.l2norm = (flags & GDN_QK_L2NORM) ? 1 : 0;
+    p.has_den = den_out != nullptr;
+    p.Vt = L.Vt;
+    p.err = reinterpret_cast<int *>(ws + L.err);
+    p.n_chunks = reinterpret_cast<int *>(ws + L.err) + 1;
+    p.chunk_tab = reinterpret_cast<int2 *>(ws + L.tab);
+    p.seq_chunk0 = reinterpret_cast<int *>(ws + L.seq0);
+    p.max_chunks = L.max_chunks;
+    p.rows = L.rows;
+    p.w = reinterpret_cast<__nv_bfloat16 *>(ws + L.w);
+    p.u = reinterpret_cast<__nv_bfloat16 *>(ws + L.u);
+    p.qg = reinterpret_cast<__nv_bfloat16 *>(ws + L.qg);
+    p.kg = reinterpret_cast<__nv_bfloat16 *>(ws + L.kg);
+    p.aqk = reinterpret_cast<__nv_bfloat16 *>(ws + L.aqk);
+    p.dec = reinterpret_cast<float *>(ws + L.dec);
+    p.UW = L.UW;
+    const int perkey = gk != nullptr;
+
+    cudaError_t e = cudaSuccess;
+    if (varlen) e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    if (qkd.dtype == GDN_F32) {
+        e = launch(KFusedF32, stream, [&] { return gdn::launch_fused_f32(p, L.KP, perkey, stream); });
+        return cuda_status(e);
+    }
+    if (L.max_chunks > 0) {
+        e = launch(KIntra, stream,
+                   [&] { return gdn::launch_intra_bf16(p, L.KP, perkey, stream); });
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    e = launch(KState, stream, [&] { return gdn::launch_state_bf16(p, L.KP, stream); });
+    return cuda_status(e);
+}
+
+gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream, int *word) {
+    if (!workspace) return GDN_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+    int w = 0;
+    if (cudaMemcpy(&w, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
+    if (word) *word = w;
+    return w ? GDN_ERR_DEVICE : GDN_OK;
+}
+
+int gdn_kernel_kinds(void) { return KNumKinds; }
+
+const char *gdn_kernel_name(int kind) {
+    return (kind >= 0 && kind < KNumKinds) ? kKindNames[kind] : "unknown";
+}
+
+void gdn_profile_enable(int on) {
+    Profiler &P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    P.on = on != 0;
+}
+
+gdn_status gdn_profile_collect(float *ms, int *launches, int n) {
+    Profiler &P = prof();
+    std::lock_guard<std::mutex> g(P.mu);
+    for (int i = 0; i < n; ++i) {
+        if (ms) ms[i] = 0.f;
+        if (launches) launches[i] = 0;
+    }
+    gdn_status st = GDN_OK;
+    for (auto &r : P.recs) {
+        float t = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess ||
+            cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+            st = GDN_ERR_CUDA;
+        if (r.kind < n) {
+            if (ms) ms[r.kind] += t;
+            if (launches) launches[r.kind] += 1;
+        }
+        P.pool.push_back(r.a);
+        P.pool.push_back(r.b);
+    }
+    P.recs.clear();
+    return st;
+}
+
+long long gdn_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

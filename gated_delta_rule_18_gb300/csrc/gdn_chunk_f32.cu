@@ -1,0 +1,293 @@
+// gdn_chunk_f32.cu -- the fp32 path: one fused CUDA-core kernel per
+// (sequence, head, 32-column value tile) that walks the sequence chunk by
+// chunk with IEEE fp32 products throughout (no tensor cores, no TF32).
+//
+// Per chunk of L <= 64 tokens (logical positions; the reverse scan remaps
+// rows, see gdn_common.cuh), with G the in-chunk cumulative log gate
+// (per key for gk) and h the state entering the chunk:
+//   A_ij = beta_i sum_d k_id k_jd e^{G_id - G_jd}      (j < i)
+//   T    = (I + A)^{-1}                               forward substitution
+//   Y    = beta . (V - (e^{G} . K) h)
+//   v_new = T Y                                        (= u - w h)
+//   o    = (e^{G} . Q) h + P v_new,  P_ij = sum_d q_id k_jd e^{G_id - G_jd} (j <= i)
+//   h   <- e^{G_last} . h + (e^{G_last - G} . K)^T v_new
+// This is the chunked WY form of the token recurrence of the SANA
+// `fused_gdn.py` page (`_fused_gdn_kernel`); v_new = u - w h and the
+// h update follow the hyper-parallel coverage_diff page
+// (`chunk_gated_delta_rule_fwd_kernel_h_blockdim64`), with the state kept in
+// shared memory for the whole sequence. Per-key gate factors are evaluated
+// element by element (exp of differences of cumulative gates, all <= 0), so
+// nothing overflows for any gate magnitude.
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kBVf = 32;  // value columns per CTA
+constexpr int kThreadsF = 256;
+
+template <int KP, bool PERKEY>
+struct F32Smem {
+    static constexpr int QS = KP + 1;    // row stride of q/k/gk tiles
+    static constexpr int VS = kBVf + 1;  // row stride of value tiles
+    static constexpr int AS = kChunk + 1;
+    static constexpr int q = 0;
+    static constexpr int k = q + kChunk * QS;
+    static constexpr int gk = k + kChunk * QS;
+    static constexpr int g = gk + (PERKEY ? kChunk * QS : 0);
+    static constexpr int beta = g + kChunk;
+    static constexpr int h = beta + kChunk;
+    static constexpr int v = h + KP * VS;
+    static constexpr int x = v + kChunk * VS;
+    static constexpr int a = x + kChunk * VS;
+    static constexpr int t = a + kChunk * AS;
+    static constexpr int pm = t + kChunk * AS;
+    static constexpr int total = pm + kChunk * AS;  // floats
+    static constexpr size_t bytes = sizeof(float) * total;
+};
+
+template <int KP, bool PERKEY>
+__global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p) {
+    using L = F32Smem<KP, PERKEY>;
+    extern __shared__ float sm[];
+    float *sQ = sm + L::q, *sK = sm + L::k, *sGk = sm + L::gk, *sG = sm + L::g;
+    float *sB = sm + L::beta, *sH = sm + L::h, *sV = sm + L::v, *sX = sm + L::x;
+    float *sA = sm + L::a, *sT = sm + L::t, *sP = sm + L::pm;
+    constexpr int QS = L::QS, VS = L::VS, AS = L::AS;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int s = blockIdx.x / p.H, hh = blockIdx.x % p.H;
+    const int v0 = blockIdx.y * kBVf;
+    const int K = p.K, V = p.V, H = p.H;
+    if (!p.cu_seqlens && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *p.err = 0;
+    if (p.cu_seqlens && *p.n_chunks < 0) return;  // cu_seqlens rejected on the device
+    SeqInfo si;
+    if (!seq_info(p, s, si)) return;
+    const float *q = (const float *)p.q, *k = (const float *)p.k, *v = (const float *)p.v;
+
+    // state tile h[d][n], d < KP, n < 32 (value column v0 + n)
+    for (int e = tid; e < KP * kBVf; e += kThreadsF) {
+        const int d = e / kBVf, n = e % kBVf, col = v0 + n;
+        float x = 0.f;
+        if (p.h0 && d < K && col < V) x = p.h0[(((int64_t)s * H + hh) * K + d) * V + col];
+        sH[d * VS + n] = x;
+    }
+
+    const int nchunks = (si.len + kChunk - 1) / kChunk;
+    for (int c = 0; c < nchunks; ++c) {
+        const int pos0 = c * kChunk;
+        const int Lc = min(kChunk, si.len - pos0);
+        __syncthreads();  // previous chunk fully consumed
+        // ---- load q, k (zero padded), v, beta, gates
+        for (int e = tid; e < kChunk * KP; e += kThreadsF) {
+            const int i = e / KP, d = e % KP;
+            float xq = 0.f, xk = 0.f, xg = 0.f;
+            if (i < Lc && d < K) {
+                const int tq = q_token(p.reverse, si.len, pos0 + i);
+                const int tk = kv_token(p.reverse, si.len, pos0 + i);
+                xq = q[si.b * p.qk_sb + (int64_t)(si.tstart + tq) * p.qk_st + hh * p.qk_sh + d];
+                if (tk >= 0) {
+                    xk = k[si.b * p.qk_sb + (int64_t)(si.tstart + tk) * p.qk_st + hh * p.qk_sh + d];
+                    if (PERKEY) xg = fmaxf(p.gk[((si.row0 + tk) * H + hh) * (int64_t)K + d], kLogGateMin);
+                }
+            }
+            sQ[i * QS + d] = xq;
+            sK[i * QS + d] = xk;
+            if (PERKEY) sGk[i * QS + d] = xg;
+        }
+        for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
+            const int i = e / kBVf, n = e % kBVf, col = v0 + n;
+            float xv = 0.f;
+            if (i < Lc) {
+                const int tk = kv_token(p.reverse, si.len, pos0 + i);
+                if (tk >= 0) {
+                    if (col < V)
+                        xv = v[si.b * p.v_sb + (int64_t)(si.tstart + tk) * p.v_st + hh * p.v_sh + col];
+                    else if (p.has_den && col == V)
+                        xv = 1.f;
+                }
+            }
+            sV[i * VS + n] = xv;
+        }
+        if (tid < kChunk) {
+            const int i = tid;
+            float b = 0.f, gg = 0.f;
+            if (i < Lc) {
+                const int tk = kv_token(p.reverse, si.len, pos0 + i);
+                if (tk >= 0) {
+                    b = p.beta[(si.row0 + tk) * H + hh];
+                    if (!PERKEY) gg = fmaxf(p.g[(si.row0 + tk) * H + hh], kLogGateMin);
+                }
+            }
+            sB[i] = b;
+            sG[i] = gg;
+        }
+        __syncthreads();
+        // ---- optional L2 normalisation of q and k rows; gate cumsums
+        if (p.l2norm) {
+            for (int i = warp; i < 2 * kChunk; i += kThreadsF / 32) {
+                float *row = (i < kChunk) ? (sQ + i * QS) : (sK + (i - kChunk) * QS);
+                float ss = 0.f;
+                for (int d = lane; d < KP; d += 32) ss += row[d] * row[d];
+                ss = warp_sum(ss);
+                const float inv = rsqrtf(ss + 1e-6f);
+                for (int d = lane; d < KP; d += 32) row[d] *= inv;
+            }
+        }
+        if (PERKEY) {
+            for (int d = tid; d < KP; d += kThreadsF) {
+                float acc = 0.f;
+                for (int i = 0; i < kChunk; ++i) {
+                    acc += sGk[i * QS + d];
+                    sGk[i * QS + d] = acc;
+                }
+            }
+        } else if (tid == 0) {
+            float acc = 0.f;
+            for (int i = 0; i < kChunk; ++i) {
+                acc += sG[i];
+                sG[i] = acc;
+            }
+        }
+        __syncthreads();
+        // ---- A (strict lower, beta-scaled) and P (lower incl. diagonal)
+        for (int e = tid; e < kChunk * kChunk; e += kThreadsF) {
+            const int i = e / kChunk, j = e % kChunk;
+            float a = 0.f, pm = 0.f;
+            if (j <= i) {
+                float sa = 0.f, sp = 0.f;
+                if (PERKEY) {
+                    for (int d = 0; d < KP; ++d) {
+                        const float gam = __expf(sGk[i * QS + d] - sGk[j * QS + d]);
+                        const float kj = sK[j * QS + d] * gam;
+                        sa = fmaf(sK[i * QS + d], kj, sa);
+                        sp = fmaf(sQ[i * QS + d], kj, sp);
+                    }
+                } else {
+                    for (int d = 0; d < KP; ++d) {
+                        sa = fmaf(sK[i * QS + d], sK[j * QS + d], sa);
+                        sp = fmaf(sQ[i * QS + d], sK[j * QS + d], sp);
+                    }
+                    const float gam = __expf(sG[i] - sG[j]);
+                    sa *= gam;
+                    sp *= gam;
+                }
+                pm = sp;
+                if (j < i) a = sB[i] * sa;
+            }
+            sA[i * AS + j] = a;
+            sP[i * AS + j] = pm;
+            sT[i * AS + j] = (i == j) ? 1.f : 0.f;
+        }
+        __syncthreads();
+        // ---- T = (I + A)^{-1}: row i = e_i - sum_{j<i} A_ij T_j
+        for (int i = 1; i < kChunk; ++i) {
+            if (tid < i) {
+                const int cc = tid;
+                float acc = 0.f;
+                for (int j = cc; j < i; ++j) acc = fmaf(sA[i * AS + j], sT[j * AS + cc], acc);
+                sT[i * AS + cc] = -acc;
+            }
+            __syncthreads();
+        }
+        // ---- Y = beta (V - (e^G . K) h) into sX
+        for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
+            const int i = e / kBVf, n = e % kBVf;
+            float acc = 0.f;
+            if (PERKEY) {
+                for (int d = 0; d < KP; ++d)
+                    acc = fmaf(sK[i * QS + d] * __expf(sGk[i * QS + d]), sH[d * VS + n], acc);
+            } else {
+                for (int d = 0; d < KP; ++d) acc = fmaf(sK[i * QS + d], sH[d * VS + n], acc);
+                acc *= __expf(sG[i]);
+            }
+            sX[i * VS + n] = sB[i] * (sV[i * VS + n] - acc);
+        }
+        __syncthreads();
+        // ---- v_new = T Y into sV
+        for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
+            const int i = e / kBVf, n = e % kBVf;
+            float acc = 0.f;
+            for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * AS + j], sX[j * VS + n], acc);
+            sV[i * VS + n] = acc;
+        }
+        __syncthreads();
+        // ---- o = (e^G . Q) h + P v_new
+        for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
+            const int i = e / kBVf, n = e % kBVf, col = v0 + n;
+            if (i >= Lc) continue;
+            float acc = 0.f;
+            if (PERKEY) {
+                for (int d = 0; d < KP; ++d)
+                    acc = fmaf(sQ[i * QS + d] * __expf(sGk[i * QS + d]), sH[d * VS + n], acc);
+            } else {
+                for (int d = 0; d < KP; ++d) acc = fmaf(sQ[i * QS + d], sH[d * VS + n], acc);
+                acc *= __expf(sG[i]);
+            }
+            for (int j = 0; j <= i; ++j) acc = fmaf(sP[i * AS + j], sV[j * VS + n], acc);
+            const int tq = q_token(p.reverse, si.len, pos0 + i);
+            if (col < V) {
+                const int64_t off =
+                    si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + col;
+                if (p.out_f32) {
+                    float *o = (float *)p.out + off;
+                    *o = p.accumulate ? *o + acc : acc;
+                } else {
+                    __nv_bfloat16 *o = (__nv_bfloat16 *)p.out + off;
+                    *o = __float2bfloat16_rn(p.accumulate ? __bfloat162float(*o) + acc : acc);
+                }
+            } else if (p.has_den && col == V) {
+                float *o = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
+                *o = p.accumulate ? *o + acc : acc;
+            }
+        }
+        __syncthreads();
+        // ---- h <- e^{G_last} h + (e^{G_last - G} . K)^T v_new
+        const int last = Lc - 1;
+        for (int e = tid; e < KP * kBVf; e += kThreadsF) {
+            const int d = e / kBVf, n = e % kBVf;
+            float acc;
+            if (PERKEY) {
+                const float gl = sGk[last * QS + d];
+                acc = __expf(gl) * sH[d * VS + n];
+                for (int i = 0; i < Lc; ++i)
+                    acc = fmaf(sK[i * QS + d] * __expf(gl - sGk[i * QS + d]), sV[i * VS + n], acc);
+            } else {
+                const float gl = sG[last];
+                acc = __expf(gl) * sH[d * VS + n];
+                for (int i = 0; i < Lc; ++i)
+                    acc = fmaf(sK[i * QS + d] * __expf(gl - sG[i]), sV[i * VS + n], acc);
+            }
+            sH[d * VS + n] = acc;
+        }
+    }
+    __syncthreads();
+    if (p.h_final) {
+        for (int e = tid; e < KP * kBVf; e += kThreadsF) {
+            const int d = e / kBVf, n = e % kBVf, col = v0 + n;
+            if (d < K && col < V)
+                p.h_final[(((int64_t)s * H + hh) * K + d) * V + col] = sH[d * VS + n];
+        }
+    }
+}
+
+template <int KP, bool PERKEY>
+cudaError_t launch_f32_t(const FwdParams &p, cudaStream_t st) {
+    using L = F32Smem<KP, PERKEY>;
+    auto kern = fused_f32_kernel<KP, PERKEY>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L::bytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.n_seq * p.H, (p.Vt + kBVf - 1) / kBVf);
+    kern<<<grid, kThreadsF, L::bytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st) {
+    if (KP == 64) return perkey ? launch_f32_t<64, true>(p, st) : launch_f32_t<64, false>(p, st);
+    return perkey ? launch_f32_t<128, true>(p, st) : launch_f32_t<128, false>(p, st);
+}
+
+}  // namespace gdn

@@ -1,0 +1,162 @@
+// gdn_common.cuh -- shared definitions of the sm_103a kernels behind gdn.h:
+// the launch parameter block, sequence/token addressing (including the
+// flip-and-shift reverse scan done by index remapping), and thin inline-PTX
+// wrappers (cp.async, ldmatrix, bf16 mma).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kChunk = 64;  // tokens per chunk
+
+// Floors applied to log gates on load. A decay below e^-30 (~1e-13) is
+// indistinguishable from 0 in fp32 next to O(1) terms, and the floor keeps
+// exp(G_i - G_j) of cumulative gates finite for g = -inf (a full reset).
+// The bf16 per-key path splits e^{G_i - G_j} into two factors about a point
+// at most 8 tokens away (see gdn_chunk_bf16.cu); a floor of -10 per token
+// bounds each factor by e^80, below the fp32/bf16 overflow at e^88. It
+// changes the result only for per-key decays below e^-10 = 4.5e-5 per token,
+// by less than that relative amount.
+constexpr float kLogGateMin = -30.f;
+constexpr float kLogGateMinPerKeyTC = -10.f;
+
+// Everything a forward launch needs. Strides are in elements.
+struct FwdParams {
+    const void *q, *k, *v;
+    int64_t qk_sb, qk_st, qk_sh;
+    int64_t v_sb, v_st, v_sh;
+    const float *g, *gk, *beta, *h0;
+    const int32_t *cu_seqlens;
+    void *out;
+    int64_t o_sb, o_st, o_sh;
+    int out_f32;
+    float *h_final, *den;
+    int B, T, H, K, V, n_seq;
+    int reverse, accumulate, l2norm, has_den;
+    int Vt;  // V + has_den: value columns carried by the scan
+    // workspace
+    int *err;         // device error word
+    int *n_chunks;    // number of valid chunk-table entries (varlen)
+    int2 *chunk_tab;  // (seq, chunk index within seq) per global chunk
+    int *seq_chunk0;  // first global chunk of each sequence
+    int max_chunks;
+    int64_t rows;     // token rows of the intermediates (B*T)
+    __nv_bfloat16 *w, *u, *qg, *kg, *aqk;  // head-major [H][rows][width]
+    float *dec;       // [H][max_chunks][KP] chunk decay e^{G_last}
+    int UW;           // row width of u (elements, multiple of 8)
+};
+
+// Sequence s: first flat token row, length, batch index, first token in
+// its batch row.
+struct SeqInfo {
+    int64_t row0;  // flat token index b*T + tstart
+    int len;
+    int b;
+    int tstart;
+};
+
+__device__ __forceinline__ bool seq_info(const FwdParams &p, int s, SeqInfo &si) {
+    if (p.cu_seqlens) {
+        int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
+        if (a < 0 || e < a || e > p.T) return false;
+        si.b = 0;
+        si.tstart = a;
+        si.len = e - a;
+        si.row0 = a;
+    } else {
+        si.b = s;
+        si.tstart = 0;
+        si.len = p.T;
+        si.row0 = (int64_t)s * p.T;
+    }
+    return true;
+}
+
+// Physical token (within the sequence) that feeds logical position `pos`.
+// Query rows and output rows: the reverse scan flips. Key/value/beta/gate
+// rows: the reverse scan flips and shifts by one; position 0 reads nothing
+// (returns -1: zero key/value/beta and a zero log-gate).
+__device__ __forceinline__ int q_token(int reverse, int len, int pos) {
+    return reverse ? len - 1 - pos : pos;
+}
+__device__ __forceinline__ int kv_token(int reverse, int len, int pos) {
+    return reverse ? (pos == 0 ? -1 : len - pos) : pos;
+}
+
+// ---------------------------------------------------------------- PTX ------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+// 16-byte async copy global -> shared; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
+                 "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *smem) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(smem)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *smem) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(smem)));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Load a value of the storage type as float.
+template <typename T>
+__device__ __forceinline__ float ldf(const T *p);
+template <>
+__device__ __forceinline__ float ldf<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16 *p) {
+    return __bfloat162float(*p);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace gdn
+
+// Host-side launchers, defined in the .cu files and called by gdn_api.cu.
+namespace gdn {
+cudaError_t launch_chunk_table(const FwdParams &p, cudaStream_t st);
+cudaError_t launch_intra_bf16(const FwdParams &p, int KP, int perkey, cudaStream_t st);
+cudaError_t launch_state_bf16(const FwdParams &p, int KP, cudaStream_t st);
+cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);
+cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, void *y,
+                        int64_t ysb, int64_t yst, int64_t ysh, int B, int T, int H, int D,
+                        int bf16, int mode, float scale, float eps, float *inv_rms,
+                        cudaStream_t st);
+}  // namespace gdn

@@ -1,0 +1,179 @@
+/*
+ * gdn.h -- C ABI of libgdn.so, the GB300 (sm_103a) chunked gated delta rule
+ * forward scan.
+ *
+ * The operation (per sequence and head, state S of K x V, fp32):
+ *   S_t = (I - beta_t k_t k_t^T) e^{g_t} S_{t-1} + beta_t k_t v_t^T,
+ *   o_t = S_t^T q_t, i.e. token by token
+ *     S <- diag(e^{gk_t}) S            (scalar gate: e^{g_t} S)
+ *     d  = beta_t (v_t - S^T k_t)
+ *     S <- S + k_t d^T
+ *     o_t = S^T q_t                    (inclusive: reads the updated state)
+ * as defined by the SANA `fused_gdn.py` page (`_fused_gdn_kernel`, "Pass 1 --
+ * State Accumulation" and "Pass 2 -- Output (reads state_curr, inclusive)")
+ * and the SANA `fused_cam_gdn.py` page (`_cam_scan_kernel`, with its
+ * init/final state contract). It is computed in chunks of 64 tokens with a
+ * WY representation: per chunk, T = (I + strictly_lower(diag(beta)
+ * (K K^T . Gamma)))^{-1}, w = T (beta e^{G} . K), u = T (beta . V), then
+ * v_new = u - w h and h <- e^{G_last} h + (e^{G_last - G} . K)^T v_new, the
+ * state-passing step of the hyper-parallel coverage_diff page
+ * (`chunk_gated_delta_rule_fwd_kernel_h_blockdim64`).
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated. The caller owns every
+ *     buffer; the library never allocates device memory. Scratch space is a
+ *     caller-provided workspace of gdn_workspace_size() bytes.
+ *   - Calls are asynchronous on `stream`. All argument checks run on the host
+ *     before any launch; a call that returns an error launched nothing.
+ *   - Tensor layouts are row-major with the last dimension contiguous; the
+ *     other strides are given in ELEMENTS by gdn_tensor_desc. Base pointers
+ *     and strides must give 16-byte aligned rows (GDN_ERR_LAYOUT otherwise).
+ *   - Errors mirror the pages' contract (SANA `fused_gdn.py` page,
+ *     `fused_gdn_func`): bad shapes, dtypes, strides -> GDN_ERR_SHAPE /
+ *     GDN_ERR_DTYPE / GDN_ERR_LAYOUT (the pages' ValueError); a reverse scan
+ *     combined with initial/final state -> GDN_ERR_UNSUPPORTED (the pages'
+ *     NotImplementedError); launch failures -> GDN_ERR_CUDA (RuntimeError).
+ *     Problems only the device can see (a malformed cu_seqlens) set an error
+ *     word in the workspace, skip the affected work, and are reported by
+ *     gdn_last_device_error(). No kernel traps.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = 2,       /* sizes out of range or inconsistent */
+    GDN_ERR_DTYPE = 3,       /* unsupported or mismatched element type */
+    GDN_ERR_LAYOUT = 4,      /* stride / alignment / contiguity */
+    GDN_ERR_UNSUPPORTED = 5, /* e.g. reverse scan with state input/output */
+    GDN_ERR_CUDA = 6,        /* a CUDA call failed */
+    GDN_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up */
+    GDN_ERR_WORKSPACE = 8,   /* workspace missing, too small or misaligned */
+    GDN_ERR_DEVICE = 9       /* a device-side argument check failed */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Element strides of a (B, T, H, D) view; D is contiguous (stride 1). */
+typedef struct {
+    int32_t dtype; /* gdn_dtype */
+    int32_t reserved;
+    int64_t stride_b;
+    int64_t stride_t;
+    int64_t stride_h;
+} gdn_tensor_desc;
+
+/* gdn_prep modes */
+#define GDN_PREP_L2 0x0   /* per (token, head): y = x / sqrt(sum_d x^2 + eps) */
+#define GDN_PREP_RMS 0x1  /* per token over all H*D channels:
+                             inv = 1/sqrt(sum_{h,d} x^2 / (H*D) + eps), y = x*inv */
+#define GDN_PREP_RELU 0x10 /* then y = max(y, 0) */
+
+/* gdn_chunk_fwd flags */
+#define GDN_ACCUMULATE 0x1 /* add into out (and den_out) instead of storing */
+#define GDN_QK_L2NORM 0x2  /* L2-normalise q and k per (token, head) on load
+                              (eps 1e-6), fusing GDN_PREP_L2 into the scan */
+
+/* device error word bits (gdn_last_device_error) */
+#define GDN_DEVERR_SEQLENS 0x1 /* cu_seqlens not 0 = c0 <= c1 <= ... = T */
+
+/*
+ * gdn_prep -- q/k preparation (SANA `fused_gdn.py` page: `_precompute_inv_rms`,
+ * `_fused_qk_inv_rms_kernel`, and the ReLU / k_scale of `_fused_gdn_kernel`;
+ * the per-(token, head) L2 form is the one the workload statement asks for).
+ *   x, y: (B, T, H, D) with descriptors xd, yd (same dtype; may alias when
+ *         the strides are equal). y = relu?(normalised x) * scale.
+ *   mode: GDN_PREP_L2 or GDN_PREP_RMS, optionally | GDN_PREP_RELU.
+ *   inv_rms: (B, T) fp32 output for GDN_PREP_RMS, or NULL.
+ *   D <= 256 (L2) and H*D <= 16384 (RMS); D a multiple of 8 (bf16) or 4 (fp32).
+ */
+gdn_status gdn_prep(const void *x, gdn_tensor_desc xd, void *y,
+                    gdn_tensor_desc yd, int B, int T, int H, int D, int mode,
+                    float scale, float eps, float *inv_rms,
+                    cudaStream_t stream);
+
+/*
+ * gdn_workspace_size -- bytes of scratch gdn_chunk_fwd needs for this shape.
+ *   varlen != 0: B must be 1 and T is the packed token count.
+ *   with_den != 0: the call will also compute the denominator.
+ * Returns 0 for sizes gdn_chunk_fwd would reject.
+ */
+size_t gdn_workspace_size(int B, int T, int H, int K, int V, int n_seq,
+                          int varlen, int dtype, int with_den);
+
+/*
+ * gdn_chunk_fwd -- one direction of the chunked gated delta rule.
+ *   q, k: (B, T, H, K), descriptor qkd (shared); v: (B, T, H, V), vd.
+ *         All three have the same dtype: GDN_F32 runs the fp32 CUDA-core path
+ *         (IEEE fp32 products), GDN_BF16 the bf16 tensor-core path with an
+ *         fp32 state.
+ *   g:    (B, T, H) fp32 natural-log gate, or NULL when gk is given.
+ *   gk:   (B, T, H, K) fp32 per-key natural-log gate, or NULL.
+ *   beta: (B, T, H) fp32.
+ *   h0:   (n_seq, H, K, V) fp32 initial state (state at the end of a prefix,
+ *         decayed by this call's first gate), or NULL for zero.
+ *   cu_seqlens: device int32 (n_seq + 1) offsets of packed sequences, or NULL
+ *         for B dense sequences of length T (n_seq must then equal B).
+ *         With cu_seqlens, B must be 1; chunks never cross sequences.
+ *   out:  (B, T, H, V), descriptor od, dtype GDN_F32 or GDN_BF16.
+ *   h_final: (n_seq, H, K, V) fp32 state after the last token, or NULL.
+ *   den_out: (B, H, T) fp32 denominator (the same scan with v = 1, SANA
+ *         `fused_gdn.py` page, z state), or NULL.
+ *   chunk: must be 64. K <= 128 (a multiple of 8), V (+1 with den_out) <= 256.
+ *   reverse: 0 causal; 1 anti-causal flip-and-shift scan (SANA
+ *         `fused_cam_gdn.py` page, `_flip_and_shift` and
+ *         `_torch_cam_scan_reference`): o_t reads tokens t+1 .. end, token
+ *         t+1's gate decays the state before its write, and no token reads
+ *         itself. reverse with h0 or h_final -> GDN_ERR_UNSUPPORTED, as on
+ *         the pages; den_out with h0 or h_final -> GDN_ERR_UNSUPPORTED.
+ *   flags: GDN_ACCUMULATE, GDN_QK_L2NORM.
+ *   workspace: >= gdn_workspace_size() bytes, 256-byte aligned.
+ */
+gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd,
+                         const void *v, gdn_tensor_desc vd, const float *g,
+                         const float *gk, const float *beta, const float *h0,
+                         const int32_t *cu_seqlens, int n_seq, void *out,
+                         gdn_tensor_desc od, float *h_final, float *den_out,
+                         int B, int T, int H, int K, int V, int chunk,
+                         int reverse, int flags, void *workspace,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *gdn_status_string(gdn_status s);
+
+/*
+ * gdn_last_device_error -- synchronise `stream`, read the device error word
+ * that gdn_chunk_fwd keeps in `workspace`, store it in *word (GDN_DEVERR_*
+ * bits, may be NULL) and clear it. Returns GDN_ERR_DEVICE if it was set,
+ * GDN_ERR_CUDA on a CUDA failure, else GDN_OK.
+ */
+gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream,
+                                 int *word);
+
+/*
+ * Launch accounting and per-kernel timing, for benchmarks.
+ *   gdn_profile_enable(1) makes every later launch record a CUDA event pair
+ *   on its own stream; gdn_profile_collect() synchronises those events and
+ *   returns, per kernel kind (0 .. gdn_kernel_kinds()-1), the summed device
+ *   milliseconds and launch counts, then clears them.
+ *   gdn_launch_count() counts every kernel this library launched.
+ */
+int gdn_kernel_kinds(void);
+const char *gdn_kernel_name(int kind);
+void gdn_profile_enable(int on);
+gdn_status gdn_profile_collect(float *ms, int *launches, int n);
+long long gdn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_H_ */

@@ -1,0 +1,136 @@
+"""The C ABI library loads, exports every declared entry point, and rejects
+bad arguments on the host before any launch (no GPU needed).
+
+Error contract (SANA `fused_gdn.py` page, `fused_gdn_func`): bad shapes,
+dtypes and layouts are value errors; a reverse scan with state input/output
+is "not implemented"."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_18_gb300 as gdn
+from gated_delta_rule_18_gb300 import TensorDesc
+from gated_delta_rule_18_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+OK, NULL, SHAPE, DTYPE, LAYOUT, UNSUP, CUDA, TIMEOUT, WS, DEVICE = range(10)
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return gdn.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("gdn_prep", "gdn_chunk_fwd", "gdn_workspace_size", "gdn_status_string",
+              "gdn_last_device_error"):
+        assert s in syms
+
+
+def test_every_declared_symbol_is_exported(L):
+    for s in declared_symbols():
+        assert hasattr(L, s), f"{s} declared in gdn.h but not exported"
+
+
+def test_status_strings(L):
+    for code in range(10):
+        assert gdn.gdn_status_string(code)
+    assert gdn.gdn_status_string(99) == "unknown status"
+
+
+def test_workspace_size(L):
+    f32 = gdn.gdn_workspace_size(1, 256, 2, 64, 64, 1, 0, gdn.F32, 0)
+    b16 = gdn.gdn_workspace_size(4, 4096, 16, 128, 128, 4, 0, gdn.BF16, 0)
+    assert 0 < f32 < b16
+    # varlen adds the chunk table; the denominator widens u
+    assert gdn.gdn_workspace_size(1, 4096, 16, 128, 128, 64, 1, gdn.BF16, 0) > \
+        gdn.gdn_workspace_size(1, 4096, 16, 128, 128, 1, 0, gdn.BF16, 0)
+    assert gdn.gdn_workspace_size(1, 4096, 16, 112, 112, 1, 0, gdn.BF16, 1) >= \
+        gdn.gdn_workspace_size(1, 4096, 16, 112, 112, 1, 0, gdn.BF16, 0)
+    # rejected shapes report 0
+    assert gdn.gdn_workspace_size(1, 10, 1, 256, 64, 1, 0, gdn.BF16, 0) == 0   # K > 128
+    assert gdn.gdn_workspace_size(2, 10, 1, 64, 64, 2, 1, gdn.BF16, 0) == 0    # varlen B != 1
+    assert gdn.gdn_workspace_size(1, 10, 1, 64, 256, 1, 0, gdn.BF16, 1) == 0   # V + den > 256
+
+
+# Fake, never-dereferenced, well-aligned device addresses: every call below
+# must be rejected by host-side checks before anything touches them.
+A = 1 << 20
+
+
+def P(i):
+    return ctypes.c_void_p(A * (i + 1))
+
+
+def desc(dtype, B, T, H, D):
+    return TensorDesc(dtype, 0, T * H * D, H * D, D)
+
+
+def fwd(L, **kw):
+    a = dict(q=P(0), k=P(1), qkd=desc(gdn.BF16, 1, 128, 2, 64), v=P(2),
+             vd=desc(gdn.BF16, 1, 128, 2, 64), g=P(3), gk=None, beta=P(4), h0=None, cu=None,
+             n_seq=1, out=P(5), od=desc(gdn.BF16, 1, 128, 2, 64), hf=None, den=None, B=1,
+             T=128, H=2, K=64, V=64, chunk=64, reverse=0, flags=0, ws=P(6), wsb=1 << 30,
+             stream=None)
+    a.update(kw)
+    return L.gdn_chunk_fwd(a["q"], a["k"], a["qkd"], a["v"], a["vd"], a["g"], a["gk"],
+                           a["beta"], a["h0"], a["cu"], a["n_seq"], a["out"], a["od"],
+                           a["hf"], a["den"], a["B"], a["T"], a["H"], a["K"], a["V"],
+                           a["chunk"], a["reverse"], a["flags"], a["ws"], a["wsb"],
+                           a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), NULL), (dict(beta=None), NULL), (dict(out=None), NULL),
+    (dict(g=None), NULL),                       # neither gate
+    (dict(gk=P(7)), UNSUP),                     # both gates
+    (dict(ws=None), WS), (dict(wsb=1024), WS), (dict(ws=ctypes.c_void_p(A + 16)), WS),
+    (dict(chunk=32), SHAPE), (dict(K=136), SHAPE), (dict(K=60), SHAPE), (dict(V=60), SHAPE),
+    (dict(V=256, den=P(8)), SHAPE), (dict(H=0), SHAPE), (dict(T=-1), SHAPE),
+    (dict(n_seq=2), SHAPE),                      # dense needs n_seq == B
+    (dict(cu=P(9), B=2, n_seq=2), SHAPE),        # varlen needs B == 1
+    (dict(cu=P(9), n_seq=0), SHAPE),
+    (dict(qkd=desc(7, 1, 128, 2, 64)), DTYPE),
+    (dict(qkd=desc(gdn.F32, 1, 128, 2, 64)), DTYPE),   # q/k and v dtypes differ
+    (dict(q=ctypes.c_void_p(A + 2)), LAYOUT),
+    (dict(qkd=TensorDesc(gdn.BF16, 0, 128 * 2 * 64, 2 * 64 + 4, 64)), LAYOUT),
+    (dict(g=ctypes.c_void_p(A + 2)), LAYOUT),
+    (dict(reverse=1, h0=P(10)), UNSUP), (dict(reverse=1, hf=P(10)), UNSUP),
+    (dict(den=P(8), h0=P(10)), UNSUP),
+    (dict(flags=0x80), UNSUP),
+])
+def test_chunk_fwd_rejects_on_host(L, kw, code):
+    assert fwd(L, **kw) == code
+
+
+def test_prep_rejects_on_host(L):
+    d = desc(gdn.BF16, 1, 16, 2, 64)
+    assert L.gdn_prep(None, d, P(1), d, 1, 16, 2, 64, 0, 1.0, 1e-6, None, None) == NULL
+    assert L.gdn_prep(P(0), d, P(1), desc(gdn.F32, 1, 16, 2, 64), 1, 16, 2, 64, 0, 1.0,
+                      1e-6, None, None) == DTYPE
+    assert L.gdn_prep(P(0), d, P(1), d, 1, 16, 2, 60, 0, 1.0, 1e-6, None, None) == SHAPE
+    assert L.gdn_prep(P(0), d, P(1), d, 1, 16, 2, 512, 0, 1.0, 1e-6, None, None) == SHAPE
+    assert L.gdn_prep(P(0), d, P(1), d, 1, 16, 2, 64, 0x7, 1.0, 1e-6, None, None) == UNSUP
+    assert L.gdn_prep(ctypes.c_void_p(A + 8), d, P(1), d, 1, 16, 2, 64, 0, 1.0, 1e-6, None,
+                      None) == LAYOUT
+    # zero tokens: nothing to do, nothing launched
+    assert L.gdn_prep(P(0), d, P(1), d, 1, 0, 2, 64, 0, 1.0, 1e-6, None, None) == OK
+
+
+def test_python_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(gdn, "_lib", None)
+    monkeypatch.setattr(gdn, "LIB", "/nonexistent/libgdn.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        gdn.lib()

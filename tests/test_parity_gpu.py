@@ -1,0 +1,229 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element.
+
+Bound (per output: o, h_final, den): max|gpu - ref| / max|ref| <= 1e-4 on the
+fp32 path and <= 2e-2 on the bf16 tensor-core path (fp32 state).
+
+Small cases span several 64-token chunks plus a ragged tail; the full-size
+workloads run exactly as the benchmark launches them and are compared on
+sampled (sequence, head) pairs the oracle computes directly."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import TOL, f32_dev, i32_dev, rel_err, run_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    from gated_delta_rule_18_gb300.build import build
+    build()
+    oracle.build()
+
+
+def _compare(w, keys=None):
+    ref = oracle.forward(w)
+    got = run_gpu(w)
+    keys = keys or [k for k in ("out", "h_final", "den") if k in ref and k in got]
+    errs = {k: rel_err(got[k], ref[k]) for k in keys}
+    tol = TOL[w.dtype]
+    assert all(e <= tol for e in errs.values()), (w.name, errs, tol)
+    return errs
+
+
+VL = [1, 64, 65, 0, 130, 7, 200]
+
+SMALL = {
+    "f32_dense_k64": dict(B=2, T=200, H=2, K=64, V=64, dtype="f32"),
+    "f32_k128_v256_gk": dict(B=1, T=150, H=2, K=128, V=256, dtype="f32", g_mu=None, gk_mu=4.0),
+    "f32_varlen_h0": dict(B=1, T=sum(VL), H=2, K=64, V=64, dtype="f32", lengths=VL, h0_std=0.5),
+    "f32_k32_v96": dict(B=1, T=97, H=3, K=32, V=96, dtype="f32"),
+    "bf16_dense_k64": dict(B=2, T=200, H=3, K=64, V=64),
+    "bf16_k128_h0": dict(B=1, T=333, H=2, K=128, V=128, h0_std=0.5),
+    "bf16_gk_v256": dict(B=1, T=190, H=2, K=128, V=256, g_mu=None, gk_mu=4.0),
+    "bf16_gk_k64_strong": dict(B=2, T=150, H=2, K=64, V=64, g_mu=None, gk_mu=-1.0),
+    "bf16_varlen_h0": dict(B=1, T=sum(VL), H=2, K=128, V=128, lengths=VL, h0_std=0.5),
+    "bf16_k32_v96": dict(B=1, T=97, H=3, K=32, V=96),
+    "bf16_k112_v112": dict(B=1, T=129, H=2, K=112, V=112),
+    "bf16_t1": dict(B=3, T=1, H=2, K=64, V=64, h0_std=0.5),
+    "bf16_t64": dict(B=1, T=64, H=2, K=128, V=128),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_causal(name):
+    spec = dict(SMALL[name])
+    B, T, H, K, V = (spec.pop(x) for x in ("B", "T", "H", "K", "V"))
+    dtype = spec.pop("dtype", "bf16")
+    w = workloads.make(B, T, H, K, V, dtype, seed=1, name=name, **spec)
+    _compare(w)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_bidirectional_l2(dtype):
+    w = workloads.make(2, 170, 2, 64, 64, dtype, seed=2, name="bidir_small")
+    w = dataclasses.replace(w, bidirectional=True)
+    _compare(w, ["out", "den"])
+
+
+def test_small_video_rms_bidirectional():
+    w = workloads.make_video(1, 300, 4, 112, seed=3, name="video_small")
+    _compare(w, ["out", "den"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reverse_only_varlen_gk(dtype):
+    """A single reverse (anti-causal) scan over packed sequences with a
+    per-key gate, against the oracle's literal reverse recurrence."""
+    import gated_delta_rule_18_gb300 as gdn
+    lens = [70, 1, 0, 129]
+    w = workloads.make(1, sum(lens), 2, 64, 64, dtype, seed=4, g_mu=None, gk_mu=3.0,
+                       lengths=lens)
+    qn, kn = oracle.l2norm(w.q.values), oracle.l2norm(w.k.values)
+    ref, _ = oracle.scan(qn, kn, w.v.values, w.beta, gk=w.gk, cu_seqlens=w.cu_seqlens,
+                         reverse=True)
+    out = gdn.gdn_chunk_fwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta),
+                            gk=f32_dev(w.gk), cu_seqlens=i32_dev(w.cu_seqlens), reverse=True,
+                            qk_l2norm=True)
+    assert rel_err(out.double().cpu().numpy(), ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_full_reset_and_frozen_state(dtype):
+    """g = -inf (full reset) and beta = 0, g = 0 (state frozen at h0)."""
+    w = workloads.make(1, 150, 2, 64, 64, dtype, seed=5, h0_std=0.5)
+    w.g[:] = -np.inf
+    _compare(w)
+    w2 = workloads.make(1, 150, 2, 64, 64, dtype, seed=6, h0_std=0.5)
+    w2.g[:] = 0.0
+    w2.beta[:] = 0.0
+    _compare(w2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_tokens_pass_state_through(dtype):
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(2, 0, 2, 64, 64, dtype, seed=7, h0_std=0.5)
+    hf = torch.full((2, 2, 64, 64), float("nan"), device="cuda")
+    gdn.gdn_chunk_fwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), g=f32_dev(w.g),
+                      h0=f32_dev(w.h0), h_final=hf)
+    torch.cuda.synchronize()
+    assert np.array_equal(hf.cpu().numpy(), w.h0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_resume_bit_exact(dtype):
+    """Resuming from h_final at a chunk boundary reproduces the one-call
+    trajectory bit for bit (SANA `fused_cam_gdn.py` page, `_cam_scan_kernel`
+    init/final state contract)."""
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(1, 320, 2, 64, 64, dtype, seed=8)
+    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    beta, g = f32_dev(w.beta), f32_dev(w.g)
+    hf = torch.empty((1, 2, 64, 64), device="cuda")
+    full = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h_final=hf, qk_l2norm=True)
+    t0 = 128
+    h1 = torch.empty_like(hf)
+    a = gdn.gdn_chunk_fwd(q[:, :t0], k[:, :t0], v[:, :t0], beta[:, :t0].contiguous(),
+                          g=g[:, :t0].contiguous(), h_final=h1, qk_l2norm=True)
+    h2 = torch.empty_like(hf)
+    b = gdn.gdn_chunk_fwd(q[:, t0:], k[:, t0:], v[:, t0:], beta[:, t0:].contiguous(),
+                          g=g[:, t0:].contiguous(), h0=h1, h_final=h2, qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([a, b], 1), full)
+    assert torch.equal(h2, hf)
+
+
+def test_malformed_cu_seqlens_sets_device_error():
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(1, 100, 2, 64, 64, "bf16", seed=9, lengths=[30, 20, 50])
+    bad = i32_dev(np.array([0, 50, 30, 100], dtype=np.int32))  # not monotone
+    ws = torch.zeros(gdn.gdn_workspace_size(1, 100, 2, 64, 64, 3, 1, gdn.BF16, 0),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.zeros((1, 100, 2, 64), dtype=torch.bfloat16, device="cuda")
+    gdn.gdn_chunk_fwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta),
+                      g=f32_dev(w.g), cu_seqlens=bad, out=out, workspace=ws)
+    assert gdn.gdn_last_device_error(ws) == 1
+    assert torch.count_nonzero(out) == 0  # nothing was computed
+    good = i32_dev(w.cu_seqlens)
+    gdn.gdn_chunk_fwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta),
+                      g=f32_dev(w.g), cu_seqlens=good, out=out, workspace=ws)
+    assert gdn.gdn_last_device_error(ws) == 0
+
+
+# ------------------------------------------------------- full-size, sampled ---
+
+def _sub(w, b_idx, heads):
+    """The workload restricted to batch rows b_idx and heads (l2 prep is per
+    (token, head), so slicing heads does not change it)."""
+    ix = (slice(b_idx, b_idx + 1), slice(None), heads)
+    return dataclasses.replace(
+        w, B=1, H=len(heads), q=w.q.take(ix), k=w.k.take(ix), v=w.v.take(ix),
+        beta=np.ascontiguousarray(w.beta[ix]),
+        g=None if w.g is None else np.ascontiguousarray(w.g[ix]),
+        gk=None if w.gk is None else np.ascontiguousarray(w.gk[ix]),
+        h0=None if w.h0 is None else np.ascontiguousarray(w.h0[b_idx:b_idx + 1][:, heads]))
+
+
+def _sub_varlen(w, seqs, heads):
+    cu = w.cu_seqlens
+    rows = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in seqs])
+    lens = [int(cu[s + 1] - cu[s]) for s in seqs]
+    ncu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ix = (slice(None), rows[:, None], np.asarray(heads)[None, :])
+    return dataclasses.replace(
+        w, T=int(ncu[-1]), H=len(heads), q=w.q.take(ix), k=w.k.take(ix), v=w.v.take(ix),
+        beta=np.ascontiguousarray(w.beta[ix]), g=np.ascontiguousarray(w.g[ix]),
+        h0=np.ascontiguousarray(w.h0[seqs][:, heads]), cu_seqlens=ncu), rows
+
+
+@pytest.mark.parametrize("name", ["causal_f32_b1h2t256d64", "causal_bf16_b4h16t4096d128",
+                                  "gk_bf16_b1h32t65536k128v256"])
+def test_full_size_dense(name):
+    w = workloads.build(name)
+    got = run_gpu(w)
+    picks = {0: [0, w.H - 1]} if w.B == 1 else {0: [0, 5], w.B - 1: [w.H - 1]}
+    tol = TOL[w.dtype]
+    for b, heads in picks.items():
+        ref = oracle.forward(_sub(w, b, heads))
+        e_o = rel_err(got["out"][b:b + 1, :, heads], ref["out"])
+        e_h = rel_err(got["h_final"][b:b + 1][:, heads], ref["h_final"])
+        assert e_o <= tol and e_h <= tol, (name, b, heads, e_o, e_h)
+
+
+def test_full_size_varlen():
+    w = workloads.build("varlen_bf16_64seq_h32d128")
+    got = run_gpu(w)
+    seqs, heads = [0, 17, 63], [3, 31]
+    sw, rows = _sub_varlen(w, seqs, heads)
+    ref = oracle.forward(sw)
+    e_o = rel_err(got["out"][:, rows][:, :, heads], ref["out"])
+    e_h = rel_err(got["h_final"][seqs][:, heads], ref["h_final"])
+    assert e_o <= 2e-2 and e_h <= 2e-2, (e_o, e_h)
+
+
+def test_full_size_video_bidirectional():
+    w = workloads.build("bidir_video_b2h16n8192d112")
+    got = run_gpu(w)
+    b, heads = 1, [0, 9]
+    # full-channel RMS prep needs every head of the token; scan two heads
+    qkv = w.qkv.take((slice(b, b + 1),)).values.astype(np.float64)
+    qn, _ = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
+    kn, _ = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    qn, kn, vv = qn[:, :, heads], kn[:, :, heads], qkv[:, :, 2][:, :, heads]
+    beta, g = w.beta[b:b + 1][:, :, heads], w.g[b:b + 1][:, :, heads]
+    of, _ = oracle.scan(qn, kn, vv, beta, g=g)
+    orv, _ = oracle.scan(qn, kn, vv, beta, g=g, reverse=True)
+    den = oracle.den(qn, kn, beta, g=g) + oracle.den(qn, kn, beta, g=g, reverse=True)
+    assert rel_err(got["out"][b:b + 1][:, :, heads], of + orv) <= 2e-2
+    assert rel_err(got["den"][b:b + 1][:, heads], den) <= 2e-2

@@ -34,10 +34,10 @@ _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "g": 5, "gk": 6, "h0": 7,
                "lens": 8, "qkv": 9}
 
 
-def _normal_f32(seed: int, name: str, n: int, mu: float = 0.0,
-                sigma: float = 1.0) -> np.ndarray:
-    """n draws of N(mu, sigma^2) as float32, filled block by block."""
-    out = np.empty(n, dtype=np.float32)
+def _normal_fill(seed: int, name: str, n: int, mu: float, sigma: float,
+                 out: np.ndarray, encode) -> np.ndarray:
+    """Fill `out` (length n) with encode(N(mu, sigma^2) float32 draws), block
+    by block; each block has its own generator seeded (seed, tensor, block)."""
     tid = _TENSOR_IDS[name]
     nblk = (n + BLOCK - 1) // BLOCK
 
@@ -49,7 +49,7 @@ def _normal_f32(seed: int, name: str, n: int, mu: float = 0.0,
             x *= np.float32(sigma)
         if mu != 0.0:
             x += np.float32(mu)
-        out[lo:hi] = x
+        out[lo:hi] = encode(x)
 
     if nblk <= 1:
         for b in range(nblk):
@@ -59,6 +59,13 @@ def _normal_f32(seed: int, name: str, n: int, mu: float = 0.0,
         with _cf.ThreadPoolExecutor(workers) as ex:
             list(ex.map(fill, range(nblk)))
     return out
+
+
+def _normal_f32(seed: int, name: str, n: int, mu: float = 0.0,
+                sigma: float = 1.0) -> np.ndarray:
+    """n draws of N(mu, sigma^2) as float32."""
+    return _normal_fill(seed, name, n, mu, sigma, np.empty(n, dtype=np.float32),
+                        lambda x: x)
 
 
 def bf16_round_bits(x: np.ndarray) -> np.ndarray:
@@ -72,47 +79,76 @@ def bf16_round_bits(x: np.ndarray) -> np.ndarray:
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
-    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return (np.asarray(bits).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-@dataclasses.dataclass
 class Stored:
-    """A tensor as stored: `values` (float32, exact) plus its storage dtype.
+    """A tensor as stored: fp32 data, or bf16 bit patterns (uint16).
 
-    For bf16 `bits` holds the uint16 patterns; `values` is their exact
-    float32 upcast."""
-    values: np.ndarray
-    dtype: str  # "f32" | "bf16"
-    bits: np.ndarray | None = None
+    `values` is the exact float32 view of what is stored (computed on demand
+    for bf16, so huge tensors can be sliced before upcasting)."""
+
+    def __init__(self, dtype: str, data: np.ndarray):
+        assert dtype in ("f32", "bf16")
+        self.dtype = dtype
+        self._data = data
+
+    @property
+    def bits(self) -> np.ndarray:
+        assert self.dtype == "bf16"
+        return self._data
+
+    @property
+    def values(self) -> np.ndarray:
+        if self.dtype == "bf16":
+            return bf16_bits_to_f32(self._data)
+        return self._data
 
     @property
     def shape(self):
-        return self.values.shape
+        return self._data.shape
+
+    def take(self, index) -> "Stored":
+        """The stored tensor restricted by a numpy index (no upcast)."""
+        return Stored(self.dtype, np.ascontiguousarray(self._data[index]))
 
 
 def stored_normal(seed: int, name: str, shape, dtype: str, mu=0.0,
                   sigma=1.0) -> Stored:
     n = int(np.prod(shape))
-    x = _normal_f32(seed, name, n, mu, sigma).reshape(shape)
     if dtype == "bf16":
-        bits = bf16_round_bits(x)
-        return Stored(bf16_bits_to_f32(bits).reshape(shape), "bf16", bits.reshape(shape))
+        out = _normal_fill(seed, name, n, mu, sigma, np.empty(n, dtype=np.uint16),
+                           bf16_round_bits)
+        return Stored("bf16", out.reshape(shape))
     if dtype == "f32":
-        return Stored(x, "f32")
+        return Stored("f32", _normal_f32(seed, name, n, mu, sigma).reshape(shape))
     raise ValueError(dtype)
+
+
+def _sigmoid(x: np.ndarray) -> np.ndarray:
+    xd = x.astype(np.float64)
+    return (1.0 / (1.0 + np.exp(-xd))).astype(np.float32)
+
+
+def _log_sigmoid(x: np.ndarray) -> np.ndarray:
+    xd = x.astype(np.float64)
+    with np.errstate(over="ignore"):
+        y = np.where(xd > 0, -np.log1p(np.exp(-xd)), xd - np.log1p(np.exp(xd)))
+    return y.astype(np.float32)
 
 
 def sigmoid_normal(seed: int, name: str, shape, mu: float) -> np.ndarray:
     """sigmoid(N(mu,1)) as float32 (computed in float64 then rounded)."""
-    x = _normal_f32(seed, name, int(np.prod(shape)), mu).astype(np.float64)
-    return (1.0 / (1.0 + np.exp(-x))).astype(np.float32).reshape(shape)
+    n = int(np.prod(shape))
+    return _normal_fill(seed, name, n, mu, 1.0, np.empty(n, dtype=np.float32),
+                        _sigmoid).reshape(shape)
 
 
 def log_sigmoid_normal(seed: int, name: str, shape, mu: float) -> np.ndarray:
     """log(sigmoid(N(mu,1))) = -log1p(exp(-x)) as float32."""
-    x = _normal_f32(seed, name, int(np.prod(shape)), mu).astype(np.float64)
-    y = np.where(x > 0, -np.log1p(np.exp(-x)), x - np.log1p(np.exp(x)))
-    return y.astype(np.float32).reshape(shape)
+    n = int(np.prod(shape))
+    return _normal_fill(seed, name, n, mu, 1.0, np.empty(n, dtype=np.float32),
+                        _log_sigmoid).reshape(shape)
 
 
 @dataclasses.dataclass
@@ -194,7 +230,7 @@ def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
     g = log_sigmoid_normal(seed, "g", (B, N, H), g_mu)
 
     def part(i):
-        return Stored(qkv.values[:, :, i], "bf16", qkv.bits[:, :, i])
+        return qkv.take((slice(None), slice(None), i))
     return Workload(name, B, N, H, D, D, "bf16", part(0), part(1), part(2),
                     beta, g, qkv=qkv, prep="rms_relu", bidirectional=True)
 
