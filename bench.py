@@ -1,0 +1,467 @@
+"""Benchmark of the chunked gated delta rule forward on GB300.
+
+One step = the whole forward of one batch of the workload: q/k prep, the
+intra-chunk WY kernel and the chunk-serial state/output kernel (both scan
+directions and the denominator for the bidirectional workload), on inputs
+already resident in HBM. Default workload: causal, bf16 q/k/v with fp32
+state and gates, B=4, H=16, T=4096, K=V=128, chunk 64 (inputs ~275 MB, larger
+than the 129 MB L2, so no flush is needed between steps).
+
+Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle
+(the reference arm) on a bounded sample of the same workload instead.
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
+workload with its own seed (weak scaling, no collective on the data path);
+the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "GDN chunked fwd tokens/s & TFLOP/s at 1 GB300; % of roofline; vs CPU oracle"
+DEFAULT_WORKLOAD = "causal_bf16_b4h16t4096d128"
+C = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ work model ---
+
+def flops_per_token_head(K, V, C=C):
+    """Algorithmic FLOPs per (token, head) of one scan direction: w h, the
+    state update and q h (2KV each), strictly lower K K^T, T X and T Y (half
+    triangles), the intra-chunk output pair, and the forward substitution
+    (C^3/3 per chunk)."""
+    return 6.0 * K * V + 3.0 * C * K + 2.0 * C * V + C * C / 3.0
+
+
+def path_work(w):
+    """(algorithmic FLOPs, minimum HBM bytes) of one step of workload w:
+    inputs read once, outputs written once, h0/h_final once."""
+    th = w.B * w.T * w.H
+    e = 2 if w.dtype == "bf16" else 4
+    if w.bidirectional:
+        fl = th * (flops_per_token_head(w.K, w.V) + flops_per_token_head(w.K, w.V + 1))
+        by = th * (3 * w.K * e + 4 + 4 + w.V * e + 4)       # qkv, beta, g, num, den
+    else:
+        fl = th * flops_per_token_head(w.K, w.V)
+        by = th * ((2 * w.K + w.V) * e + 4 + (4 * w.K if w.gk is not None else 4) + w.V * e)
+        if w.h0 is not None:
+            by += w.n_seq * w.H * w.K * w.V * 4
+        by += w.n_seq * w.H * w.K * w.V * 4                 # h_final
+    return fl, by
+
+
+def kernel_bytes(w, name):
+    """Algorithmic bytes one launch of kernel `name` must move for workload
+    w: its own inputs read once and outputs written once (shared tiles counted
+    once, padding not counted)."""
+    th = w.B * w.T * w.H
+    e = 2 if w.dtype == "bf16" else 4
+    K, V = w.K, w.V + (1 if w.bidirectional else 0)
+    gate = 4 * w.K if w.gk is not None else 4
+    chunks = th / C
+    if name == "intra_bf16":
+        return th * ((2 * K + w.V) * e + 4 + gate + (3 * K + V + C) * 2) + chunks * K * 4
+    if name == "state_bf16":
+        hs = (2 if w.h0 is not None else 1) * w.n_seq * w.H * w.K * w.V * 4
+        return th * ((3 * K + V + C) * 2 + w.V * e + (4 if w.bidirectional else 0)) \
+            + chunks * K * 4 + (0 if w.bidirectional else hs)
+    if name == "fused_f32":
+        return th * ((2 * K + w.V) * e + 4 + gate + w.V * e) + w.n_seq * w.H * w.K * w.V * 4
+    if name == "prep_rms":
+        return w.B * w.T * w.H * w.K * e * 2 + w.B * w.T * 4
+    if name == "prep_l2":
+        return th * w.K * e * 2
+    return None
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------- device side ---
+
+def device_inputs(w, dev):
+    import torch
+
+    def to_dev(st):
+        if st.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(st.bits).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(st.values)).to(dev)
+
+    def f32(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+
+    d = {}
+    if w.qkv is not None:
+        qkv = to_dev(w.qkv)
+        d["qkv"] = qkv
+        d["q"], d["k"], d["v"] = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    else:
+        d["q"], d["k"], d["v"] = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    d["beta"], d["g"], d["gk"], d["h0"] = f32(w.beta), f32(w.g), f32(w.gk), f32(w.h0)
+    d["cu_seqlens"] = None if w.cu_seqlens is None else torch.from_numpy(
+        w.cu_seqlens.astype(np.int32)).to(dev)
+    return d
+
+
+def run_step(gdn, w, d, ws):
+    return gdn.gdn_forward(d["q"], d["k"], d["v"], d["beta"], g=d["g"], gk=d["gk"],
+                           h0=d["h0"], cu_seqlens=d["cu_seqlens"], prep=w.prep,
+                           bidirectional=w.bidirectional,
+                           with_final_state=not w.bidirectional, workspace=ws)
+
+
+def workspace_for(gdn, w, dev):
+    import torch
+    dt = gdn.BF16 if w.dtype == "bf16" else gdn.F32
+    n = gdn.gdn_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq, w.cu_seqlens is not None, dt,
+                               w.bidirectional)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+
+
+def e2e_measure(gdn, w, d, ws, steps, dev):
+    """The same forward through the public API with pinned host buffers:
+    each step copies the inputs host->device, runs, and copies the output back."""
+    import torch
+    host = {}
+    for key in ("qkv", "q", "k", "v", "beta", "g", "gk", "h0", "cu_seqlens"):
+        t = d.get(key)
+        if t is None or (key in ("q", "k", "v") and "qkv" in d):
+            continue
+        host[key] = t.detach().to("cpu").contiguous().pin_memory() if t.is_contiguous() else None
+    if "qkv" not in d:
+        for key in ("q", "k", "v"):
+            host[key] = d[key].to("cpu").pin_memory()
+    dev_bufs = {k2: torch.empty_like(v2, device=dev) for k2, v2 in host.items() if v2 is not None}
+    out_shape = (w.B, w.T, w.H, w.V)
+    out_host = torch.empty(out_shape, dtype=d["v"].dtype).pin_memory()
+    h2d = sum(v2.numel() * v2.element_size() for v2 in host.values() if v2 is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k2, v2 in host.items():
+            if v2 is not None:
+                dev_bufs[k2].copy_(v2, non_blocking=True)
+        dd = dict(d)
+        dd.update({k2: dev_bufs[k2] for k2 in dev_bufs})
+        if "qkv" in dev_bufs:
+            qkv = dev_bufs["qkv"]
+            dd["q"], dd["k"], dd["v"] = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+        res = run_step(gdn, w, dd, ws)
+        out_host.copy_(res["out"], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    b.synchronize()
+    sec = a.elapsed_time(b) / 1e3 / steps
+    return sec, h2d, d2h
+
+
+# ------------------------------------------------------------- CPU side ----
+
+ORACLE_S_PER_TOKEN_HEAD_KV = 7e-9   # rough fp64 oracle cost per token-head per K*V
+CPU_TARGET_CORE_SECONDS = 20.0
+
+
+def oracle_sample(w):
+    """Time the fp64 oracle (as it stands, all host cores) on a bounded sample
+    of workload w: leading batch rows / sequences and heads, sized to about
+    CPU_TARGET_CORE_SECONDS of single-core work. Returns (tokens/s of the full
+    workload equivalent, seconds, threads used, description)."""
+    import dataclasses
+
+    import oracle
+    threads = os.cpu_count() or 1
+    target = CPU_TARGET_CORE_SECONDS / (ORACLE_S_PER_TOKEN_HEAD_KV * w.K * w.V)
+    if w.qkv is not None:
+        # full-channel RMS prep needs every head of a token: whole batch rows
+        ix = (slice(0, 1),)
+        sw = dataclasses.replace(w, B=1, qkv=w.qkv.take(ix), q=w.q.take(ix), k=w.k.take(ix),
+                                 v=w.v.take(ix), beta=w.beta[ix], g=w.g[ix])
+        desc = f"batch row 0 of {w.B}: {w.T} tokens x {w.H} heads, both directions + den"
+        units = w.H
+    elif w.cu_seqlens is not None:
+        cu = w.cu_seqlens
+        nh = w.H
+        ns = 1
+        while ns < w.n_seq and cu[ns] * nh < target:
+            ns += 1
+        if cu[ns] * nh > 2 * target:
+            nh = max(1, int(target // max(1, cu[ns])))
+        ix = (slice(None), slice(0, int(cu[ns])), slice(0, nh))
+        sw = dataclasses.replace(w, T=int(cu[ns]), H=nh, q=w.q.take(ix), k=w.k.take(ix),
+                                 v=w.v.take(ix), beta=w.beta[ix], g=w.g[ix],
+                                 h0=w.h0[:ns, :nh], cu_seqlens=cu[:ns + 1])
+        desc = f"sequences 0..{ns - 1} ({int(cu[ns])} tokens) x heads 0..{nh - 1} of {w.H}"
+        units = ns * nh
+    else:
+        n_units = int(max(1, min(w.B * w.H, round(target / max(1, w.T)))))
+        nb = min(w.B, -(-n_units // w.H))
+        nh = w.H if nb > 1 else n_units
+        ix = (slice(0, nb), slice(None), slice(0, nh))
+        sw = dataclasses.replace(w, B=nb, H=nh, q=w.q.take(ix), k=w.k.take(ix),
+                                 v=w.v.take(ix), beta=w.beta[ix],
+                                 g=None if w.g is None else w.g[ix],
+                                 gk=None if w.gk is None else w.gk[ix],
+                                 h0=None if w.h0 is None else w.h0[:nb, :nh])
+        desc = f"batch rows 0..{nb - 1} of {w.B} x heads 0..{nh - 1} of {w.H}, {w.T} tokens"
+        units = nb * nh
+    t0 = time.perf_counter()
+    oracle.forward(sw, threads=threads)
+    sec = time.perf_counter() - t0
+    token_heads = sw.B * sw.T * sw.H
+    return token_heads / w.H / sec, sec, min(threads, units), desc
+
+
+# ------------------------------------------------------------------ main ---
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return main_reference(args, warmup, rank, world)
+
+    import torch
+    import gated_delta_rule_18_gb300 as gdn
+    from gated_delta_rule_18_gb300.build import build as build_lib
+    build_lib()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = workloads.build(args.workload, seed=rank)  # each replica its own data
+    d = device_inputs(w, dev)
+    ws = workspace_for(gdn, w, dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(warmup):
+        run_step(gdn, w, d, ws)
+    torch.cuda.synchronize()
+    gdn.profile_collect()
+
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = gdn.launch_count()
+    gdn.profile_enable(True)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        run_step(gdn, w, d, ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    gdn.profile_enable(False)
+    if dist:
+        dist.barrier()
+    launches = gdn.launch_count() - launches0
+    clocks = sampler.stop()
+    sec = a.elapsed_time(b) / 1e3
+    per_kernel = gdn.profile_collect()
+    if dist:
+        t = torch.tensor([sec], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    ms_per_step = sec / args.steps * 1e3
+    tokens = w.B * w.T
+    value = tokens * world * args.steps / sec
+
+    fl, by = path_work(w)
+    peaks, peak_src = load_peaks()
+    step_s = sec / args.steps
+    roof_t = max(fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
+
+    # dominant kernel: largest total device time in the timed region
+    dom = max(per_kernel.items(), key=lambda kv: kv[1][0]) if per_kernel else None
+    roofline = None
+    if dom:
+        name, (ms_tot, n) = dom
+        avg_s = ms_tot / 1e3 / n
+        kb = kernel_bytes(w, name)
+        ach = kb / avg_s / 1e9 if kb else None
+        roofline = {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": (ach / peaks["hbm_gbs"]) if ach else None,
+                    "traffic": None, "avg_launch_us": avg_s * 1e6,
+                    "peak_source": f"{peak_src} hbm_gbs"}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "K": w.K,
+                   "V": w.V, "chunk": C, "tokens_per_step_per_gpu": tokens,
+                   "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "tflops": fl * world / step_s / 1e12,
+        "path_roofline": {"bound": "hbm" if by / peaks["hbm_gbs"] > fl / peaks["bf16_tflops"] / 1e3
+                          else "tensor", "min_bytes": by, "flops": fl,
+                          "roofline_ms": roof_t * 1e3, "frac": roof_t / step_s,
+                          "peak_source": peak_src},
+        "roofline": roofline,
+        "kernels": {k2: {"avg_us": v2[0] / v2[1] * 1e3, "launches": v2[1],
+                         "share": v2[0] / max(1e-9, sum(x[0] for x in per_kernel.values()))}
+                    for k2, v2 in per_kernel.items()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "impl": "ours",
+    }
+    if not args.no_e2e:
+        e2e_s, h2d, d2h = e2e_measure(gdn, w, d, ws, max(3, min(args.steps, 10)), dev)
+        if dist:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        result["e2e"] = {"value": tokens * world / e2e_s, "unit": "tokens/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok_s, csec, cores, desc = oracle_sample(w)
+        result["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": cores,
+                                  "kind": "oracle", "sample": desc, "seconds": csec}
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def main_reference(args, warmup, rank, world):
+    """The reference arm: the fp64 CPU oracle as it stands, timed on the
+    host cores, each step a bounded sample of the workload (rank 0 only)."""
+    if rank != 0:
+        return
+    w = workloads.build(args.workload, seed=0)
+    for _ in range(warmup):
+        oracle_sample(w)
+    secs, vals = [], []
+    desc, cores = "", 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, s, cores, desc = oracle_sample(w)
+        vals.append(v)
+        secs.append(s)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    print(json.dumps({
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": wall / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload},
+        "impl": "reference",
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": desc, "value": value},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()
