@@ -16,7 +16,8 @@ import os
 
 from .build import LIB
 
-__all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_workspace_size",
+__all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
+           "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_forward", "lib",
            "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect",
            "launch_count", "kernel_names"]
@@ -65,6 +66,9 @@ def lib():
     L.gdn_chunk_fwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P,
                                 TensorDesc, P, P, I, I, I, I, I, I, I, I, P,
                                 ctypes.c_size_t, P]
+    L.gdn_chunk_fwd_noalloc.restype = I
+    L.gdn_chunk_fwd_noalloc.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P,
+                                        TensorDesc, P, P, I, I, I, I, I, I, I, I, P]
     L.gdn_last_device_error.restype = I
     L.gdn_last_device_error.argtypes = [P, P, ctypes.POINTER(I)]
     L.gdn_kernel_kinds.restype = I
@@ -182,6 +186,27 @@ def gdn_chunk_fwd(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None, out=
         workspace.numel(), _stream(stream))
     if st != 0:
         raise GDNError(st, "gdn_chunk_fwd")
+    return out
+
+
+def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqlens=None,
+                          h_final=None, den=None, reverse=False, accumulate=False,
+                          qk_l2norm=False, stream=None):
+    """gdn_chunk_fwd without a workspace, for callers that cannot allocate
+    device memory: the library's built-in scratch buffer is used, and this
+    wrapper allocates nothing either (`out`, and h_final / den when wanted,
+    must be given). Problems larger than the buffer raise GDN_ERR_WORKSPACE.
+    Calls that overlap on the GPU race on the shared buffer."""
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    flags = (ACCUMULATE if accumulate else 0) | (QK_L2NORM if qk_l2norm else 0)
+    st = lib().gdn_chunk_fwd_noalloc(
+        _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta),
+        _ptr(h0), _ptr(cu_seqlens), n_seq, _ptr(out), _desc(out), _ptr(h_final), _ptr(den),
+        B, T, H, K, V, 64, int(bool(reverse)), flags, _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_chunk_fwd_noalloc")
     return out
 
 

@@ -147,6 +147,47 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd,
                          int reverse, int flags, void *workspace,
                          size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * gdn_chunk_fwd_noalloc -- gdn_chunk_fwd for callers that cannot allocate
+ * device memory. The pages have no counterpart; this is a library service.
+ *
+ * Who needs it: code running inside a host that forbids cudaMalloc once it
+ * is up (allocation would break its memory accounting or synchronise other
+ * streams), runtimes whose device memory belongs to someone else, and
+ * plug-ins that are handed only input and output pointers. Such callers
+ * cannot provide gdn_chunk_fwd's workspace.
+ *
+ * Same arguments and results as gdn_chunk_fwd, minus the workspace: scratch
+ * comes from a buffer of GDN_NOALLOC_SCRATCH_BYTES built into the library
+ * (a file-scope device array; every GPU that loads the library holds it
+ * until the process exits). Nothing is allocated: no cudaMalloc/cudaFree and
+ * no allocating library routine is called (leave gdn_profile_enable off,
+ * since profiling creates CUDA events).
+ *   - Problems whose gdn_workspace_size() exceeds GDN_NOALLOC_SCRATCH_BYTES
+ *     are rejected with GDN_ERR_WORKSPACE before anything runs.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one buffer, which keeps the last call's contents;
+ *     the kernels write every scratch word they read, so nothing has to be
+ *     cleared between calls. Calls that overlap on the GPU (different
+ *     streams, or different host threads on the same device) race on the
+ *     buffer: serialise them.
+ *   - The device error word of gdn_last_device_error() lives in the buffer
+ *     too; it is not reachable from outside, so device-side argument errors
+ *     of this entry point are not reported.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k,
+                                 gdn_tensor_desc qkd, const void *v,
+                                 gdn_tensor_desc vd, const float *g,
+                                 const float *gk, const float *beta,
+                                 const float *h0, const int32_t *cu_seqlens,
+                                 int n_seq, void *out, gdn_tensor_desc od,
+                                 float *h_final, float *den_out, int B, int T,
+                                 int H, int K, int V, int chunk, int reverse,
+                                 int flags, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gdn_status_string(gdn_status s);
 
