@@ -214,6 +214,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return GDN_ERR_LAYOUT;  // (NULL counts as aligned)
     if (!strides_ok(qkd) || !strides_ok(vd) || !strides_ok(od)) return GDN_ERR_LAYOUT;
+    if (!aligned16(gk)) return GDN_ERR_LAYOUT;  // gk tiles are copied in 16-byte pieces
     for (const void *f : {(const void *)g, (const void *)gk, (const void *)beta,
                           (const void *)h0, (const void *)h_final, (const void *)den_out,
                           (const void *)cu_seqlens})
