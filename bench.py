@@ -75,7 +75,7 @@ def kernel_bytes(w, name):
     chunks = th / C
     if name == "intra_bf16":
         return th * ((2 * K + w.V) * e + 4 + gate + (3 * K + V + C) * 2) + chunks * K * 4
-    if name == "state_bf16":
+    if name == "state_tc":
         hs = (2 if w.h0 is not None else 1) * w.n_seq * w.H * w.K * w.V * 4
         return th * ((3 * K + V + C) * 2 + w.V * e + (4 if w.bidirectional else 0)) \
             + chunks * K * 4 + (0 if w.bidirectional else hs)
@@ -313,6 +313,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--T", type=int, default=None,
+                    help="override the token count of a dense workload (smaller profiling captures)")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -334,7 +336,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    w = workloads.build(args.workload, seed=rank)  # each replica its own data
+    w = workloads.build(args.workload, seed=rank, T=args.T)  # each replica its own data
     d = device_inputs(w, dev)
     ws = workspace_for(gdn, w, dev)
     stream = torch.cuda.current_stream()

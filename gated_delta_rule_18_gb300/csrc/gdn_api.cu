@@ -16,7 +16,7 @@ using gdn::FwdParams;
 
 enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KNumKinds };
 const char *kKindNames[KNumKinds] = {"prep_l2", "prep_rms", "chunk_table",
-                                     "intra_bf16", "state_bf16", "fused_f32"};
+                                     "intra_bf16", "state_tc", "fused_f32"};
 
 struct Profiler {
     std::mutex mu;
@@ -73,9 +73,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Ws {
-    size_t err, tab, seq0, w, u, qg, kg, aqk, dec, total;
-    int max_chunks, KP, UW, Vt;
-    int64_t rows;
+    size_t err, tab, seq0, w, qg, kg, pm, u, dec, total;
+    int max_chunks, KP, Vt, n_vt;
 };
 
 bool ws_layout(int B, int T, int H, int K, int V, int n_seq, int varlen, int dtype,
@@ -86,12 +85,11 @@ bool ws_layout(int B, int T, int H, int K, int V, int n_seq, int varlen, int dty
     if (dtype != GDN_F32 && dtype != GDN_BF16) return false;
     L.Vt = V + (with_den ? 1 : 0);
     if (L.Vt > 256) return false;
-    L.rows = (int64_t)B * T;
-    L.KP = K <= 64 ? 64 : 128;
-    L.UW = (L.Vt + 7) / 8 * 8;
+    L.KP = (dtype == GDN_BF16 || K > 64) ? 128 : 64;  // the bf16 path always pads keys to 128
+    L.n_vt = (L.Vt + 63) / 64;
     const int64_t nts = ((int64_t)T + gdn::kChunk - 1) / gdn::kChunk;
     const int64_t mc = varlen ? nts + n_seq : (int64_t)B * nts;
-    if (mc > (1 << 30) || L.rows > ((int64_t)1 << 40)) return false;
+    if (mc > (1 << 30)) return false;
     L.max_chunks = (int)mc;
     size_t off = 0;
     L.err = off;
@@ -100,21 +98,21 @@ bool ws_layout(int B, int T, int H, int K, int V, int n_seq, int varlen, int dty
     off = align_up(off + (varlen ? sizeof(int2) * (size_t)mc : 0));
     L.seq0 = off;
     off = align_up(off + (varlen ? sizeof(int) * (size_t)(n_seq + 1) : 0));
-    L.w = L.u = L.qg = L.kg = L.aqk = L.dec = off;
-    if (dtype == GDN_BF16) {
-        const size_t hr = (size_t)H * (size_t)L.rows;
+    L.w = L.qg = L.kg = L.pm = L.u = L.dec = off;
+    if (dtype == GDN_BF16) {  // per-(head, chunk) operand images
+        const size_t hmc = (size_t)H * (size_t)mc;
         L.w = off;
-        off = align_up(off + 2 * hr * L.KP);
+        off = align_up(off + hmc * gdn::kImgW);
         L.qg = off;
-        off = align_up(off + 2 * hr * L.KP);
+        off = align_up(off + hmc * gdn::kImgW);
         L.kg = off;
-        off = align_up(off + 2 * hr * L.KP);
+        off = align_up(off + hmc * gdn::kImgW);
+        L.pm = off;
+        off = align_up(off + hmc * gdn::kImgP);
         L.u = off;
-        off = align_up(off + 2 * hr * L.UW);
-        L.aqk = off;
-        off = align_up(off + 2 * hr * gdn::kChunk);
+        off = align_up(off + hmc * L.n_vt * gdn::kImgU);
         L.dec = off;
-        off = align_up(off + 4 * (size_t)H * mc * L.KP);
+        off = align_up(off + hmc * gdn::kDecB);
     }
     L.total = off;
     return true;
@@ -264,14 +262,13 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     p.chunk_tab = reinterpret_cast<int2 *>(ws + L.tab);
     p.seq_chunk0 = reinterpret_cast<int *>(ws + L.seq0);
     p.max_chunks = L.max_chunks;
-    p.rows = L.rows;
-    p.w = reinterpret_cast<__nv_bfloat16 *>(ws + L.w);
-    p.u = reinterpret_cast<__nv_bfloat16 *>(ws + L.u);
-    p.qg = reinterpret_cast<__nv_bfloat16 *>(ws + L.qg);
-    p.kg = reinterpret_cast<__nv_bfloat16 *>(ws + L.kg);
-    p.aqk = reinterpret_cast<__nv_bfloat16 *>(ws + L.aqk);
+    p.w_img = ws + L.w;
+    p.qg_img = ws + L.qg;
+    p.kg_img = ws + L.kg;
+    p.p_img = ws + L.pm;
+    p.u_img = ws + L.u;
     p.dec = reinterpret_cast<float *>(ws + L.dec);
-    p.UW = L.UW;
+    p.n_vt = L.n_vt;
     const int perkey = gk != nullptr;
 
     cudaError_t e = cudaSuccess;
@@ -282,11 +279,10 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
         return cuda_status(e);
     }
     if (L.max_chunks > 0) {
-        e = launch(KIntra, stream,
-                   [&] { return gdn::launch_intra_bf16(p, L.KP, perkey, stream); });
+        e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, perkey, stream); });
         if (e != cudaSuccess) return GDN_ERR_CUDA;
     }
-    e = launch(KState, stream, [&] { return gdn::launch_state_bf16(p, L.KP, stream); });
+    e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
     return cuda_status(e);
 }
 
@@ -298,6 +294,7 @@ gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream, int *word
         return GDN_ERR_CUDA;
     if (cudaMemset(workspace, 0, sizeof(int)) != cudaSuccess) return GDN_ERR_CUDA;
     if (word) *word = w;
+    if (w & GDN_DEVERR_TIMEOUT) return GDN_ERR_TIMEOUT;
     return w ? GDN_ERR_DEVICE : GDN_OK;
 }
 

@@ -43,11 +43,39 @@ struct FwdParams {
     int2 *chunk_tab;  // (seq, chunk index within seq) per global chunk
     int *seq_chunk0;  // first global chunk of each sequence
     int max_chunks;
-    int64_t rows;     // token rows of the intermediates (B*T)
-    __nv_bfloat16 *w, *u, *qg, *kg, *aqk;  // head-major [H][rows][width]
-    float *dec;       // [H][max_chunks][KP] chunk decay e^{G_last}
-    int UW;           // row width of u (elements, multiple of 8)
+    // Per-chunk operand images, indexed [head][global chunk], each laid out
+    // exactly as the state kernel's shared-memory MMA operand (see the
+    // image layout helpers below) so that one bulk copy stages it.
+    unsigned char *w_img, *qg_img, *kg_img, *p_img, *u_img;
+    float *dec;       // [H][max_chunks][kKP] chunk decay e^{G_last}
+    int n_vt;         // 64-column value tiles (ceil(Vt / 64))
 };
+
+// ----------------------------------------------------- operand images -------
+// The tensor-core MMAs read bf16 operands from shared memory in the
+// no-swizzle canonical layout: 8 x 16-byte "core" blocks, addressed by a
+// descriptor (start, LBO = byte stride between cores along K, SBO = byte
+// stride between cores along M/N). The images below use LBO = 128 bytes,
+// i.e. the cores along K are adjacent.
+constexpr int kKP = 128;                 // keys per image (zero padded)
+constexpr uint32_t kImgW = 64 * kKP * 2;  // w, qg (64 tokens x 128 keys), kg^T
+constexpr uint32_t kImgP = 64 * 64 * 2;   // P (64 x 64)
+constexpr uint32_t kUS = 72;              // padded row (elements) of a u tile
+constexpr uint32_t kImgU = 64 * kUS * 2;  // one 64-column u tile
+constexpr uint32_t kDecB = kKP * 4;       // chunk decay vector
+
+// w / qg: K-major A operand, M = token i, K = key d: core (i/8, d/8).
+__host__ __device__ __forceinline__ uint32_t img_w_off(int i, int d) {
+    return (uint32_t)((i >> 3) * 2048 + (d >> 3) * 128 + (i & 7) * 16 + (d & 7) * 2);
+}
+// kg^T: MN-major A operand, M = key d, K = token i: core (d/8, i/8).
+__host__ __device__ __forceinline__ uint32_t img_kt_off(int i, int d) {
+    return (uint32_t)((d >> 3) * 1024 + i * 16 + (d & 7) * 2);
+}
+// P: K-major A operand, M = token i, K = token j.
+__host__ __device__ __forceinline__ uint32_t img_p_off(int i, int j) {
+    return (uint32_t)((i >> 3) * 1024 + (j >> 3) * 128 + (i & 7) * 16 + (j & 7) * 2);
+}
 
 // Sequence s: first flat token row, length, batch index, first token in
 // its batch row.
@@ -152,8 +180,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 // Host-side launchers, defined in the .cu files and called by gdn_api.cu.
 namespace gdn {
 cudaError_t launch_chunk_table(const FwdParams &p, cudaStream_t st);
-cudaError_t launch_intra_bf16(const FwdParams &p, int KP, int perkey, cudaStream_t st);
-cudaError_t launch_state_bf16(const FwdParams &p, int KP, cudaStream_t st);
+cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
+cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);
 cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, void *y,
                         int64_t ysb, int64_t yst, int64_t ysh, int B, int T, int H, int D,

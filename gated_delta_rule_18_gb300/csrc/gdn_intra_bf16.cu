@@ -19,14 +19,18 @@
 //     raw); in-chunk cumulative gates.
 //  3. K K^T and Q K^T on tensor cores (mma.sync bf16 -> fp32), scaled by the
 //     norms, beta and Gamma: A's diagonal 16x16 blocks in fp32, its other
-//     blocks in bf16, P straight to global.
+//     blocks in bf16, P straight to its global image.
 //  4. Each warp inverts one diagonal block, T_II = (I + A_II)^{-1}, by
 //     forward substitution in registers (lane = column).
 //  5. (I + A) W = X is solved by block forward substitution,
 //     W_I = T_II (X_I - sum_{M<I} A_IM W_M), for X = [beta e^G k^ | beta V].
 //     Every warp owns 64-column slices of W, so the four block steps need no
 //     block-wide barrier; W overwrites X in shared memory.
-//  6. Coalesced 16-byte stores of w and u.
+//  6. 16-byte stores of w and u.
+// Every output is written as a per-chunk image in the shared-memory operand
+// layout the state kernel's tensor-core MMAs read (gdn_common.cuh), all 64
+// rows included (zeros past the chunk's end), so the state kernel stages each
+// one with a single bulk copy.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -39,8 +43,9 @@ constexpr int kAbS = 72;  // bf16 row stride of A (MMA operand) and of warp scra
 constexpr int kAdS = 17;  // fp32 row stride of A's diagonal blocks
 constexpr int kTdS = 24;  // bf16 row stride of T's diagonal blocks
 
-template <int KP, bool PERKEY>
+template <bool PERKEY>
 struct Lay {
+    static constexpr int KP = kKP;
     static constexpr int KS = KP + 8;
     static constexpr size_t q = 0;
     static constexpr size_t k = q + 2 * kChunk * KS;
@@ -82,9 +87,10 @@ __device__ __forceinline__ float2 ld_bf2(const bf16 *p) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
 }
 
-template <int KP, bool PERKEY>
+template <bool PERKEY>
 __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int VP) {
-    using L = Lay<KP, PERKEY>;
+    using L = Lay<PERKEY>;
+    constexpr int KP = kKP;
     constexpr int KS = L::KS;
     constexpr int VPR = KP / 8;  // 16-byte vectors per q/k row
     extern __shared__ __align__(16) unsigned char sm[];
@@ -121,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
     const int Lc = min(kChunk, si.len - pos0);
     if (Lc <= 0) return;
     const int K = p.K, H = p.H, V = p.V;
-    const int64_t hrow = (int64_t)hh * p.rows + si.row0 + pos0;
+    const size_t gch = (size_t)hh * p.max_chunks + gid;  // this chunk's image slot
     const bf16 *q = (const bf16 *)p.q, *k = (const bf16 *)p.k, *v = (const bf16 *)p.v;
     const int64_t qk_base = si.b * p.qk_sb + hh * p.qk_sh;
     const int64_t v_base = si.b * p.v_sb + hh * p.v_sh;
@@ -213,7 +219,10 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
     __syncthreads();
 
     // ---- 3. A (strictly lower, beta-scaled) and P (lower incl. diagonal)
-    bf16 *gP = p.aqk + hrow * kChunk;
+    unsigned char *gP = p.p_img + gch * kImgP;
+    auto put_p = [&](int i, int j, float v0f, float v1f) {
+        *reinterpret_cast<uint32_t *>(gP + img_p_off(i, j)) = pack_bf16(v0f, v1f);
+    };
     // store one A entry: diagonal block -> fp32, below -> bf16 operand
     auto put_a = [&](int i, int j, float a) {
         const int I = i >> 4;
@@ -262,9 +271,11 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
                         if (jj < i) put_a(i, jj, bi * rki * ak[n][2 * hf + e] * gam);
                         pv[e] = rqi * ap[n][2 * hf + e] * gam;
                     }
-                    if (i < Lc)
-                        *reinterpret_cast<uint32_t *>(gP + (int64_t)i * kChunk + j) = pack_bf16(pv[0], pv[1]);
+                    put_p(i, j, pv[0], pv[1]);
                 }
+            } else {  // right of the diagonal block: the image must hold zeros
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) put_p(16 * warp + g8 + 8 * hf, 8 * n + 2 * t4, 0.f, 0.f);
             }
         }
     } else {
@@ -322,10 +333,14 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
                             if (jj < i) put_a(i, jj, sB[i] * ak[n][2 * hf + e]);
                             pv[e] = (jj <= i) ? ap[n][2 * hf + e] : 0.f;
                         }
-                        if (i < Lc)
-                            *reinterpret_cast<uint32_t *>(gP + (int64_t)i * kChunk + j) = pack_bf16(pv[0], pv[1]);
+                        put_p(i, j, pv[0], pv[1]);
                     }
                 }
+            } else {  // column block right of this warp's diagonal: zeros
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) put_p(16 * warp + g8 + 8 * hf, r0 + 8 * n + 2 * t4, 0.f, 0.f);
             }
         }
     }
@@ -358,9 +373,9 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
 
     //         qg, kg and the chunk decay to global
     const int last = Lc - 1;
-    bf16 *gQg = p.qg + hrow * KP;
-    bf16 *gKg = p.kg + hrow * KP;
-    for (int e = tid; e < Lc * VPR; e += kThreads) {
+    unsigned char *gQg = p.qg_img + gch * kImgW;
+    unsigned char *gKg = p.kg_img + gch * kImgW;
+    for (int e = tid; e < kChunk * VPR; e += kThreads) {
         const int i = e / VPR, d0 = (e % VPR) * 8;
         float fq[8], fk[8];
         unpack8(*reinterpret_cast<const uint4 *>(sQ + i * KS + d0), fq);
@@ -381,11 +396,11 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
                 fk[x] *= ek;
             }
         }
-        *reinterpret_cast<uint4 *>(gQg + (int64_t)i * KP + d0) = pack8(fq);
-        *reinterpret_cast<uint4 *>(gKg + (int64_t)i * KP + d0) = pack8(fk);
+        *reinterpret_cast<uint4 *>(gQg + img_w_off(i, d0)) = pack8(fq);
+        *reinterpret_cast<uint4 *>(gKg + img_kt_off(i, d0)) = pack8(fk);
     }
     for (int d = tid; d < KP; d += kThreads)
-        p.dec[((int64_t)hh * p.max_chunks + gid) * KP + d] =
+        p.dec[gch * KP + d] =
             PERKEY ? __expf(sG[last * KP + d]) : __expf(sG[last]);
     if (PERKEY) cp_async_wait<0>();
     __syncthreads();
@@ -471,26 +486,27 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
     }
     __syncthreads();
 
-    // ---- 6. w and u rows to global (16-byte stores)
-    bf16 *gW = p.w + hrow * KP;
-    for (int e = tid; e < Lc * VPR; e += kThreads) {
+    // ---- 6. w and u images (all 64 rows; rows past the chunk are zero)
+    unsigned char *gW = p.w_img + gch * kImgW;
+    for (int e = tid; e < kChunk * VPR; e += kThreads) {
         const int i = e / VPR, d = (e % VPR) * 8;
-        *reinterpret_cast<uint4 *>(gW + (int64_t)i * KP + d) = *reinterpret_cast<const uint4 *>(sK + i * KS + d);
+        *reinterpret_cast<uint4 *>(gW + img_w_off(i, d)) = *reinterpret_cast<const uint4 *>(sK + i * KS + d);
     }
-    bf16 *gU = p.u + hrow * p.UW;
-    const int UWv = p.UW / 8;
-    for (int e = tid; e < Lc * UWv; e += kThreads) {
-        const int i = e / UWv, d = (e % UWv) * 8;
-        *reinterpret_cast<uint4 *>(gU + (int64_t)i * p.UW + d) = *reinterpret_cast<const uint4 *>(sV + i * VS + d);
+    unsigned char *gU = p.u_img + gch * p.n_vt * kImgU;
+    const int VPRv = VP / 8;
+    for (int e = tid; e < kChunk * VPRv; e += kThreads) {
+        const int i = e / VPRv, c = (e % VPRv) * 8;
+        *reinterpret_cast<uint4 *>(gU + (c >> 6) * kImgU + i * (kUS * 2) + (c & 63) * 2) =
+            *reinterpret_cast<const uint4 *>(sV + i * VS + c);
     }
 }
 
-template <int KP, bool PERKEY>
+template <bool PERKEY>
 cudaError_t launch_t(const FwdParams &p, cudaStream_t st) {
-    using L = Lay<KP, PERKEY>;
-    const int VP = (p.Vt + 63) / 64 * 64;
+    using L = Lay<PERKEY>;
+    const int VP = p.n_vt * 64;
     const size_t bytes = L::bytes(VP);
-    auto kern = intra_kernel<KP, PERKEY>;
+    auto kern = intra_kernel<PERKEY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.max_chunks, p.H);
@@ -500,10 +516,9 @@ cudaError_t launch_t(const FwdParams &p, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_intra_bf16(const FwdParams &p, int KP, int perkey, cudaStream_t st) {
+cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st) {
     if (p.max_chunks == 0) return cudaSuccess;
-    if (KP == 64) return perkey ? launch_t<64, true>(p, st) : launch_t<64, false>(p, st);
-    return perkey ? launch_t<128, true>(p, st) : launch_t<128, false>(p, st);
+    return perkey ? launch_t<true>(p, st) : launch_t<false>(p, st);
 }
 
 }  // namespace gdn

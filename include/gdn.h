@@ -85,6 +85,7 @@ typedef struct {
 
 /* device error word bits (gdn_last_device_error) */
 #define GDN_DEVERR_SEQLENS 0x1 /* cu_seqlens not 0 = c0 <= c1 <= ... = T */
+#define GDN_DEVERR_TIMEOUT 0x2 /* a bounded wait inside a kernel gave up */
 
 /*
  * gdn_prep -- q/k preparation (SANA `fused_gdn.py` page: `_precompute_inv_rms`,
@@ -194,8 +195,9 @@ const char *gdn_status_string(gdn_status s);
 /*
  * gdn_last_device_error -- synchronise `stream`, read the device error word
  * that gdn_chunk_fwd keeps in `workspace`, store it in *word (GDN_DEVERR_*
- * bits, may be NULL) and clear it. Returns GDN_ERR_DEVICE if it was set,
- * GDN_ERR_CUDA on a CUDA failure, else GDN_OK.
+ * bits, may be NULL) and clear it. Returns GDN_ERR_TIMEOUT if a bounded
+ * wait gave up, GDN_ERR_DEVICE for other set bits, GDN_ERR_CUDA on a CUDA
+ * failure, else GDN_OK.
  */
 gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream,
                                  int *word);

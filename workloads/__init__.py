@@ -255,9 +255,18 @@ def varlen_lengths(seed: int = 0, n_seq: int = 64, lo: int = 128,
     return [int(x) for x in _vary_lengths(seed, n_seq, lo, hi)]
 
 
-def build(name: str, seed: int = 0) -> Workload:
+def build(name: str, seed: int = 0, T: int | None = None) -> Workload:
+    """The named workload; `T` overrides the token count of the dense and
+    video workloads (same recipe, fewer tokens)."""
     spec = dict(WORKLOADS[name])
     kind = spec.pop("kind")
+    if T is not None:
+        if kind == "dense":
+            spec["T"] = T
+        elif kind == "video":
+            spec["N"] = T
+        else:
+            raise ValueError("T override applies to dense and video workloads")
     if kind == "dense":
         return make(spec["B"], spec["T"], spec["H"], spec["K"], spec["V"],
                     spec["dtype"], seed=seed, g_mu=spec.get("g_mu"),
