@@ -9,20 +9,22 @@
 // in-chunk term and reads the state after each token's own write, as the
 // SANA `fused_gdn.py` page's Pass 2 does):
 //
-//   Xw    = w  h            (MMA, M=64 tokens, N=64, K=128 keys)
-//   O     = qg h            (MMA)
-//   v_new = u - Xw          (threads; bf16 operand for the next two MMAs)
-//   dh    = kg^T v_new      (MMA, M=128 keys, N=64, K=64 tokens)
-//   O    += P v_new         (MMA, M=64, K=64)
-//   h     = dec . h + dh    (threads, fp32)
+//   [Xw; O] = [w; qg] h      one MMA chain, M=128 (w and qg stacked), K=128
+//   v_new   = u - Xw         threads of warps 0-1 (bf16 operand below)
+//   dh      = kg^T v_new     MMA, M=128 keys, K=64 tokens
+//   h       = dec . h + dh   every thread, fp32
+//   [.; O] += [0; P] v_new   MMA, M=128 (a zero block stacked over P)
 //
-// The intra-chunk kernel stores w, qg, kg^T, P, u and dec as per-chunk images
-// already in the shared-memory operand layouts, so each chunk's operands
-// arrive by six 1-D bulk async copies (cp.async.bulk, completion counted in
-// bytes on an mbarrier), double-buffered one chunk ahead. One thread issues
-// the MMAs (tcgen05.mma, operands read from shared memory through matrix
-// descriptors) and tcgen05.commit signals completion on an mbarrier; all
-// threads then read their accumulator rows with tcgen05.ld.
+// Only the recurrence (the first product, v_new, dh, the h update) is on the
+// critical path. Its MMAs are issued by thread 0; the output of chunk c
+// (P v_new, then storing O) runs one chunk later on warps 2-3 while warps 0-1
+// compute chunk c+1's v_new, so the [Xw; O] accumulator and v_new are double
+// buffered. Copies are issued by a thread of warp 1; each MMA group completes
+// on its own mbarrier. The intra-chunk kernel stores w, qg, kg^T, P, u and dec
+// as per-chunk images already in the shared-memory operand layouts, so a
+// chunk's operands arrive by six 1-D bulk async copies (cp.async.bulk,
+// completion counted in bytes on an mbarrier), double-buffered one chunk
+// ahead; w and qg land back to back, so one descriptor spans both.
 //
 // Every wait is bounded: on a timeout the kernel records GDN_DEVERR_TIMEOUT in
 // the workspace error word, drains what it issued (again bounded), frees its
@@ -38,30 +40,34 @@ constexpr int kThreads = 128;
 constexpr int kBVt = 64;  // value columns per CTA
 
 struct Lay {
+    // one stage: w | qg | kg^T | zero block | P | u | dec
     static constexpr uint32_t w = 0;
-    static constexpr uint32_t qg = w + kImgW;
+    static constexpr uint32_t qg = w + kImgW;  // directly after w: [w; qg] is one M=128 operand
     static constexpr uint32_t kg = qg + kImgW;
-    static constexpr uint32_t pm = kg + kImgW;
+    static constexpr uint32_t z = kg + kImgW;  // 64 zero rows stacked over P
+    static constexpr uint32_t pm = z + kImgP;
     static constexpr uint32_t u = pm + kImgP;
     static constexpr uint32_t dec = u + kImgU;
     static constexpr uint32_t stage = dec + kDecB;
-    static constexpr uint32_t stage_bytes = stage;  // bytes one stage receives
-    static constexpr uint32_t h = 2 * stage;         // h as the MMA B operand (MN-major)
-    static constexpr uint32_t vn = h + 64 * kKP * 2;  // v_new as the MMA B operand (MN-major)
-    static constexpr uint32_t bytes = vn + 64 * 64 * 2;
+    static constexpr uint32_t copy_bytes = stage - kImgP;  // everything but the zero block
+    static constexpr uint32_t h = 2 * stage;               // h as the MMA B operand (MN-major)
+    static constexpr uint32_t vn = h + 64 * kKP * 2;       // 2 x v_new as the MMA B operand (MN-major)
+    static constexpr uint32_t vn_bytes = 64 * 64 * 2;
+    static constexpr uint32_t bytes = vn + 2 * vn_bytes;
 };
 
-// TMEM columns: Xw [0,64), O [64,128), dh [128,192)
+// TMEM columns: [Xw; O] of even / odd chunks [0,64) / [64,128) (lane = row:
+// 0-63 Xw, 64-127 O), dh [128,192)
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColXw = 0, kColO = 64, kColDh = 128;
+constexpr uint32_t kColD = 0, kColDh = 128;
 
 // instruction descriptors (kind::f16: bf16 inputs, fp32 accumulate)
 constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-constexpr uint32_t kIdescTok = idesc(64, 64, 0, 1);   // A K-major (w, qg, P), B MN-major (h, v_new)
-constexpr uint32_t kIdescKey = idesc(128, 64, 1, 1);  // A = kg^T MN-major, B = v_new MN-major
+constexpr uint32_t kIdescK = idesc(128, 64, 0, 1);   // A K-major ([w;qg], [0;P]), B MN-major
+constexpr uint32_t kIdescMN = idesc(128, 64, 1, 1);  // A = kg^T MN-major, B = v_new MN-major
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
@@ -137,7 +143,7 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
 __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p) {
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ __align__(8) uint64_t bar_stage[2];
-    __shared__ __align__(8) uint64_t bar_mma;
+    __shared__ __align__(8) uint64_t bar_a, bar_dh, bar_o;
     __shared__ uint32_t tmem_base_s;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const int gc0 = p.cu_seqlens ? p.seq_chunk0[s] : s * ((p.T + kChunk - 1) / kChunk);
     const uint32_t sbase = smem_u32(sm);
     const uint32_t bar_st0 = smem_u32(&bar_stage[0]), bar_st1 = smem_u32(&bar_stage[1]);
-    const uint32_t bar_m = smem_u32(&bar_mma);
+    const uint32_t b_a = smem_u32(&bar_a), b_dh = smem_u32(&bar_dh), b_o = smem_u32(&bar_o);
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -163,9 +169,17 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_st0));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_st1));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_m));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_a));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_dh));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_o));
         asm volatile("fence.mbarrier_init.release.cluster;");
     }
+    // the zero blocks stacked over P (never overwritten by the copies)
+    for (int e = tid; e < (int)(kImgP / 16); e += kThreads) {
+        *reinterpret_cast<uint4 *>(sm + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + Lay::stage + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
+    }
+    fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
@@ -179,41 +193,115 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     for (int c = 0; c < 64; ++c)
         h[c] = (p.h0 && r < K && v0 + c < V) ? p.h0[(((int64_t)s * H + hh) * K + r) * V + v0 + c] : 0.f;
 
-    auto issue_stage = [&](int c) {  // thread 0 only
+    // chunk c's operands: part 0 = w, qg, kg^T, u, dec; part 1 = P (P of the
+    // stage's previous chunk is read by the deferred output MMA, so it is
+    // copied later). Both parts complete on the stage's mbarrier.
+    auto issue_stage = [&](int c, int part) {  // one thread
         const int st = c & 1;
         const uint32_t dst = sbase + st * Lay::stage;
         const uint32_t bar = st ? bar_st1 : bar_st0;
         const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                     "r"(Lay::stage_bytes)
-                     : "memory");
-        const void *src[6] = {p.w_img + gch * kImgW, p.qg_img + gch * kImgW, p.kg_img + gch * kImgW,
-                              p.p_img + gch * kImgP, p.u_img + (gch * p.n_vt + vt) * kImgU,
-                              p.dec + gch * kKP};
-        const uint32_t off[6] = {Lay::w, Lay::qg, Lay::kg, Lay::pm, Lay::u, Lay::dec};
-        const uint32_t len[6] = {kImgW, kImgW, kImgW, kImgP, kImgU, kDecB};
+        if (part == 0) {
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                         "r"(Lay::copy_bytes)
+                         : "memory");
+            const void *src[5] = {p.w_img + gch * kImgW, p.qg_img + gch * kImgW, p.kg_img + gch * kImgW,
+                                  p.u_img + (gch * p.n_vt + vt) * kImgU, p.dec + gch * kKP};
+            const uint32_t off[5] = {Lay::w, Lay::qg, Lay::kg, Lay::u, Lay::dec};
+            const uint32_t len[5] = {kImgW, kImgW, kImgW, kImgU, kDecB};
 #pragma unroll
-        for (int x = 0; x < 6; ++x)
+            for (int x = 0; x < 5; ++x)
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        dst + off[x]),
+                    "l"(src[x]), "r"(len[x]), "r"(bar)
+                    : "memory");
+        } else {
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    dst + off[x]),
-                "l"(src[x]), "r"(len[x]), "r"(bar)
+                    dst + Lay::pm),
+                "l"(p.p_img + gch * kImgP), "r"(kImgP), "r"(bar)
                 : "memory");
+        }
+    };
+    // output of chunk c (warps 2-3): O += P v_new, then store O's rows
+    auto output = [&](int c, bool &okc) {
+        const int st = c & 1;
+        const uint32_t dcol = kColD + (uint32_t)(c & 1) * 64;
+        if (tid == 64) {
+            const uint32_t vb = sbase + Lay::vn + (uint32_t)(c & 1) * Lay::vn_bytes;
+            const uint32_t stg = sbase + st * Lay::stage;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma(tmem + dcol, sdesc(stg + Lay::z + ks * 256, 128, 1024), sdesc(vb + ks * 256, 128, 1024),
+                    kIdescK, 1);
+            commit(b_o);
+        }
+        okc = wait_bar(b_o, c & 1) && okc;
+        fence_after();
+        float t[64];
+        tmem_ld64(tmem + lane_base + dcol, t);
+        const int i = tid - 64;
+        const int pos0 = c * kChunk;
+        const int Lc = min(kChunk, si.len - pos0);
+        if (i < Lc && okc) {
+            const int tq = q_token(p.reverse, si.len, pos0 + i);
+            const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int col = v0 + 8 * j;
+                if (col + 8 <= V) {
+                    if (p.out_f32) {
+                        float4 *op = reinterpret_cast<float4 *>((float *)p.out + off + 8 * j);
+                        float4 a = make_float4(t[8 * j], t[8 * j + 1], t[8 * j + 2], t[8 * j + 3]);
+                        float4 b = make_float4(t[8 * j + 4], t[8 * j + 5], t[8 * j + 6], t[8 * j + 7]);
+                        if (p.accumulate) {
+                            const float4 y0 = op[0], y1 = op[1];
+                            a.x += y0.x; a.y += y0.y; a.z += y0.z; a.w += y0.w;
+                            b.x += y1.x; b.y += y1.y; b.z += y1.z; b.w += y1.w;
+                        }
+                        op[0] = a;
+                        op[1] = b;
+                    } else {
+                        uint4 *op = reinterpret_cast<uint4 *>((bf16 *)p.out + off + 8 * j);
+                        float f[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) f[x] = t[8 * j + x];
+                        if (p.accumulate) {
+                            const uint4 y = *op;
+                            const __nv_bfloat162 *y2 = reinterpret_cast<const __nv_bfloat162 *>(&y);
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const float2 fy = __bfloat1622float2(y2[x]);
+                                f[2 * x] += fy.x;
+                                f[2 * x + 1] += fy.y;
+                            }
+                        }
+                        *op = pack8(f);
+                    }
+                } else if (p.has_den && col == V) {
+                    float *dp = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
+                    *dp = p.accumulate ? *dp + t[8 * j] : t[8 * j];
+                }
+            }
+        }
     };
 
-    int timed_out = 0;  // 1: stage copy wait, 2: MMA wait
-    uint32_t mma_phase = 0;
-    if (nchunks > 0 && tid == 0) issue_stage(0);
+    int timed_out = 0;
+    if (nchunks > 0 && tid == 32) {
+        issue_stage(0, 0);
+        issue_stage(0, 1);
+    }
     int c = 0;
     for (; c < nchunks; ++c) {
         const int st = c & 1;
+        const uint32_t par = c & 1;  // phase of the per-chunk barriers
         const uint32_t stg = sbase + st * Lay::stage;
         const int pos0 = c * kChunk;
         const int Lc = min(kChunk, si.len - pos0);
 
-        // S1: operands of chunk c have landed
+        // operands of chunk c have landed; h (bf16) -> MN-major B operand
         const bool ok_stage = wait_bar(st ? bar_st1 : bar_st0, (c >> 1) & 1);
-        // S2: h (bf16) -> shared memory, MN-major B operand: (col/8)*2048 + r*16
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = pack8(&h[8 * j]);
@@ -224,133 +312,95 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             break;
         }
         fence_after();
-        if (tid == 0) {
-            if (c + 1 < nchunks) issue_stage(c + 1);
-            // S3: Xw = w h, O = qg h  (K = 128 keys, 8 steps of 16)
+        const uint32_t dcol = kColD + par * 64;  // this chunk's [Xw; O] columns
+        if (tid == 0) {  // [Xw; O] = [w; qg] h, K = 128 keys in 8 steps
             const uint32_t hb = sbase + Lay::h;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t b = sdesc(hb + ks * 256, 128, 2048);
-                mma(tmem + kColXw, sdesc(stg + Lay::w + ks * 256, 128, 2048), b, kIdescTok, ks > 0);
-                mma(tmem + kColO, sdesc(stg + Lay::qg + ks * 256, 128, 2048), b, kIdescTok, ks > 0);
-            }
-            commit(bar_m);
+            for (int ks = 0; ks < 8; ++ks)
+                mma(tmem + dcol, sdesc(stg + Lay::w + ks * 256, 128, 2048), sdesc(hb + ks * 256, 128, 2048),
+                    kIdescK, ks > 0);
+            commit(b_a);
+        } else if (tid == 32 && c + 1 < nchunks) {
+            issue_stage(c + 1, 0);
         }
-        const bool ok1 = wait_bar(bar_m, mma_phase);
-        mma_phase ^= 1;
-        fence_after();
-        // S4: v_new = u - Xw for token row i = 16*warp + lane (lanes 0..15)
-        {
+        bool ok = true;
+        if (warp >= 2 && c > 0) output(c - 1, ok);  // the previous chunk's output, off the critical path
+        if (warp < 2) {  // v_new = u - Xw for token row i = tid
+            ok = wait_bar(b_a, par);
+            fence_after();
             float xw[64];
-            tmem_ld64(tmem + lane_base + kColXw, xw);
-            if (lane < 16) {
-                const int i = 16 * warp + lane;
-                const unsigned char *urow = sm + st * Lay::stage + Lay::u + i * (kUS * 2);
+            tmem_ld64(tmem + lane_base + dcol, xw);
+            const int i = tid;
+            const unsigned char *urow = sm + st * Lay::stage + Lay::u + i * (kUS * 2);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 uv = *reinterpret_cast<const uint4 *>(urow + 16 * j);
-                    const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
-                    float f[8];
+            for (int j = 0; j < 8; ++j) {
+                const uint4 uv = *reinterpret_cast<const uint4 *>(urow + 16 * j);
+                const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
+                float f[8];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const float2 t = __bfloat1622float2(u2[x]);
-                        f[2 * x] = t.x - xw[8 * j + 2 * x];
-                        f[2 * x + 1] = t.y - xw[8 * j + 2 * x + 1];
-                    }
-                    // MN-major B operand (N = column, K = token): (col/8)*1024 + i*16
-                    *reinterpret_cast<uint4 *>(sm + Lay::vn + j * 1024 + i * 16) = pack8(f);
+                for (int x = 0; x < 4; ++x) {
+                    const float2 t = __bfloat1622float2(u2[x]);
+                    f[2 * x] = t.x - xw[8 * j + 2 * x];
+                    f[2 * x + 1] = t.y - xw[8 * j + 2 * x + 1];
                 }
+                // MN-major B operand (N = column, K = token): (col/8)*1024 + i*16
+                *reinterpret_cast<uint4 *>(sm + Lay::vn + par * Lay::vn_bytes + j * 1024 + i * 16) = pack8(f);
             }
+            fence_async_smem();
         }
-        fence_async_smem();
         fence_before();
-        if (__syncthreads_or(!ok1)) {
+        if (__syncthreads_or(!ok)) {
             timed_out = 2;
             break;
         }
         fence_after();
-        if (tid == 0) {
-            // S5: dh = kg^T v_new (M = 128 keys), O += P v_new (K = 64 tokens)
-            const uint32_t vb = sbase + Lay::vn;
+        const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
+        if (tid == 0) {  // dh = kg^T v_new (M = 128 keys, K = 64 tokens)
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t b = sdesc(vb + ks * 256, 128, 1024);
-                mma(tmem + kColDh, sdesc(stg + Lay::kg + ks * 256, 128, 1024), b, kIdescKey, ks > 0);
-                mma(tmem + kColO, sdesc(stg + Lay::pm + ks * 256, 128, 1024), b, kIdescTok, 1);
-            }
-            commit(bar_m);
+            for (int ks = 0; ks < 4; ++ks)
+                mma(tmem + kColDh, sdesc(stg + Lay::kg + ks * 256, 128, 1024), sdesc(vb + ks * 256, 128, 1024),
+                    kIdescMN, ks > 0);
+            commit(b_dh);
+        } else if (tid == 32 && c + 1 < nchunks) {
+            issue_stage(c + 1, 1);  // the previous chunk's output MMA no longer reads this stage's P
         }
-        const bool ok2 = wait_bar(bar_m, mma_phase);
-        mma_phase ^= 1;
+        // h = dec . h + dh (row r)
+        bool ok2 = wait_bar(b_dh, par);
         fence_after();
-        // S6: h = dec . h + dh (row r); output row i
         {
             float t[64];
             tmem_ld64(tmem + lane_base + kColDh, t);
             const float d = reinterpret_cast<const float *>(sm + st * Lay::stage + Lay::dec)[r];
 #pragma unroll
             for (int x = 0; x < 64; ++x) h[x] = fmaf(d, h[x], t[x]);
-            tmem_ld64(tmem + lane_base + kColO, t);
-            const int i = 16 * warp + lane;
-            if (lane < 16 && i < Lc && ok2) {
-                const int tq = q_token(p.reverse, si.len, pos0 + i);
-                const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int col = v0 + 8 * j;
-                    if (col + 8 <= V) {
-                        if (p.out_f32) {
-                            float4 *op = reinterpret_cast<float4 *>((float *)p.out + off + 8 * j);
-                            float4 a = make_float4(t[8 * j], t[8 * j + 1], t[8 * j + 2], t[8 * j + 3]);
-                            float4 b = make_float4(t[8 * j + 4], t[8 * j + 5], t[8 * j + 6], t[8 * j + 7]);
-                            if (p.accumulate) {
-                                const float4 y0 = op[0], y1 = op[1];
-                                a.x += y0.x; a.y += y0.y; a.z += y0.z; a.w += y0.w;
-                                b.x += y1.x; b.y += y1.y; b.z += y1.z; b.w += y1.w;
-                            }
-                            op[0] = a;
-                            op[1] = b;
-                        } else {
-                            uint4 *op = reinterpret_cast<uint4 *>((bf16 *)p.out + off + 8 * j);
-                            float f[8];
-#pragma unroll
-                            for (int x = 0; x < 8; ++x) f[x] = t[8 * j + x];
-                            if (p.accumulate) {
-                                const uint4 y = *op;
-                                const __nv_bfloat162 *y2 = reinterpret_cast<const __nv_bfloat162 *>(&y);
-#pragma unroll
-                                for (int x = 0; x < 4; ++x) {
-                                    const float2 fy = __bfloat1622float2(y2[x]);
-                                    f[2 * x] += fy.x;
-                                    f[2 * x + 1] += fy.y;
-                                }
-                            }
-                            *op = pack8(f);
-                        }
-                    } else if (p.has_den && col == V) {
-                        float *dp = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
-                        *dp = p.accumulate ? *dp + t[8 * j] : t[8 * j];
-                    }
-                }
-            }
         }
         fence_before();
         if (__syncthreads_or(!ok2)) {
-            timed_out = 2;
+            timed_out = 3;
             break;
         }
     }
+    if (!timed_out && nchunks > 0) {  // the last chunk's output
+        fence_after();
+        bool ok = true;
+        if (warp >= 2) output(nchunks - 1, ok);
+        fence_before();
+        if (__syncthreads_or(!ok)) timed_out = 4;
+    }
 
     if (timed_out) {
-        // record, then drain what this CTA issued (bounded) before freeing TMEM:
-        // a stage wait failed -> chunk c's copies; an MMA wait failed -> the
-        // last committed MMA group and chunk c+1's copies.
+        // record, then drain what this CTA issued (bounded) before freeing TMEM
         if (tid == 0) {
             atomicOr(p.err, 2);
+            const uint32_t par = c & 1;
             if (timed_out == 1) {
                 wait_bar((c & 1) ? bar_st1 : bar_st0, (c >> 1) & 1);
+            } else if (timed_out == 4) {
+                wait_bar(b_o, (nchunks - 1) & 1);
             } else {
-                wait_bar(bar_m, mma_phase ^ 1);
+                wait_bar(b_a, par);
+                if (c > 0) wait_bar(b_o, (c - 1) & 1);
+                if (timed_out == 3) wait_bar(b_dh, par);
                 if (c + 1 < nchunks) wait_bar(((c + 1) & 1) ? bar_st1 : bar_st0, ((c + 1) >> 1) & 1);
             }
         }
