@@ -1,32 +1,42 @@
 // gdn_state_tc.cu -- chunk-serial state passing and output of the bf16 path
 // on the fifth-generation tensor cores (tcgen05, accumulators in TMEM).
 //
-// One CTA (4 warps) per (sequence, head, 64-column value tile), walking the
-// sequence's 64-token chunks in order. Thread r keeps row r of the fp32 state
-// h (128 keys x 64 columns) in registers. Per chunk (hyper-parallel
-// coverage_diff page, `chunk_gated_delta_rule_fwd_kernel_h_blockdim64`:
-// b_v = u - w h, h *= exp(g_last), h += k^T v_new; the output adds the
-// in-chunk term and reads the state after each token's own write, as the
-// SANA `fused_gdn.py` page's Pass 2 does):
+// One CTA per (sequence, head, 64-column value tile), walking the sequence's
+// 64-token chunks in order, warp-specialised (8 warps):
 //
-//   [Xw; O] = [w; qg] h      one MMA chain, M=128 (w and qg stacked), K=128
-//   v_new   = u - Xw         threads of warps 0-1 (bf16 operand below)
+//   warps 0-3  the recurrence. Thread r keeps row r of the fp32 state h
+//              (128 keys x 64 columns) in registers; per chunk it writes h as
+//              the bf16 B operand and applies h = dec . h + dh.
+//   warps 0,1  with warps 4,5 (same TMEM lanes 0-63): v_new = u - Xw, each
+//   + 4,5      warp pair splitting a row's 64 columns in halves.
+//   warps 6-7  the output: read O for TMEM lanes 64-127 and store it; one of
+//              their threads also copies the next chunk's MMA operands.
+//   warp 4     lane 0 also issues every tcgen05.mma and the u / dec copies:
+//              the first product of a chunk must finish before warp 4's
+//              v_new work anyway, and its later products follow that work.
+//
+// Per chunk (hyper-parallel coverage_diff page,
+// `chunk_gated_delta_rule_fwd_kernel_h_blockdim64`: b_v = u - w h,
+// h *= exp(g_last), h += k^T v_new; the output adds the in-chunk term and
+// reads the state after each token's own write, as the SANA `fused_gdn.py`
+// page's Pass 2 does):
+//
+//   [Xw; O] = [w; qg] h      MMA chain, M=128 (w and qg stacked), K=128 keys
+//   v_new   = u - Xw         warps 0-1 (bf16 MN-major operand)
 //   dh      = kg^T v_new     MMA, M=128 keys, K=64 tokens
-//   h       = dec . h + dh   every thread, fp32
+//   h       = dec . h + dh   warps 0-3, fp32
 //   [.; O] += [0; P] v_new   MMA, M=128 (a zero block stacked over P)
 //
-// Only the recurrence (the first product, v_new, dh, the h update) is on the
-// critical path. Its MMAs are issued by thread 0; the output of chunk c
-// (P v_new, then storing O) runs one chunk later on warps 2-3 while warps 0-1
-// compute chunk c+1's v_new, so the [Xw; O] accumulator and v_new are double
-// buffered. Copies are issued by a thread of warp 1; each MMA group completes
-// on its own mbarrier. The intra-chunk kernel stores w, qg, kg^T, P, u and dec
-// as per-chunk images already in the shared-memory operand layouts, so a
-// chunk's operands arrive by six 1-D bulk async copies (cp.async.bulk,
-// completion counted in bytes on an mbarrier), double-buffered one chunk
-// ahead; w and qg land back to back, so one descriptor spans both.
+// Roles hand over through mbarriers only (thread arrivals for "operand
+// written", tcgen05.commit for "MMA done", transaction bytes for copies), so
+// only the recurrence is on the critical path; the output of a chunk overlaps
+// the next chunk. [Xw; O] and v_new are double buffered. The intra-chunk
+// kernel stores w, qg, kg^T, P, u and dec as per-chunk images in the
+// shared-memory operand layouts, so a chunk's operands arrive by six 1-D bulk
+// async copies (cp.async.bulk), double-buffered one chunk ahead.
 //
-// Every wait is bounded: on a timeout the kernel records GDN_DEVERR_TIMEOUT in
+// Every wait is bounded: a wait that gives up raises a shared abort flag that
+// makes every role leave its loop, the kernel records GDN_DEVERR_TIMEOUT in
 // the workspace error word, drains what it issued (again bounded), frees its
 // tensor memory and returns.
 #include "gdn_common.cuh"
@@ -36,7 +46,7 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps, see the role map above
 constexpr int kBVt = 64;  // value columns per CTA
 
 struct Lay {
@@ -49,7 +59,6 @@ struct Lay {
     static constexpr uint32_t u = pm + kImgP;
     static constexpr uint32_t dec = u + kImgU;
     static constexpr uint32_t stage = dec + kDecB;
-    static constexpr uint32_t copy_bytes = stage - kImgP;  // everything but the zero block
     static constexpr uint32_t h = 2 * stage;               // h as the MMA B operand (MN-major)
     static constexpr uint32_t vn = h + 64 * kKP * 2;       // 2 x v_new as the MMA B operand (MN-major)
     static constexpr uint32_t vn_bytes = 64 * 64 * 2;
@@ -93,8 +102,9 @@ __device__ __forceinline__ uint64_t now_ns() {
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
     return t;
 }
-// Wait for the mbarrier phase `parity`; false after ~0.5 s (no hang).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
+// Wait for the mbarrier phase `parity`; false after ~0.5 s or once *abort is
+// set by another role (no hang either way).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         uint32_t ok;
@@ -106,11 +116,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
             : "memory");
         if (ok) return true;
         if ((it & 255) == 0) {
+            if (abort && *abort) return false;
             const uint64_t t = now_ns();
             if (t0 == 0) t0 = t;
-            else if (t - t0 > 500000000ull) return false;
+            else if (t - t0 > 500000000ull) {
+                if (abort) *abort = 1;
+                return false;
+            }
         }
     }
+}
+// a flag every lane of the warp agrees on (warp-collective tcgen05 ops need
+// the whole warp)
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+__device__ __forceinline__ void arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // 64 consecutive TMEM columns of this warp's 32 lanes -> 64 registers
@@ -142,11 +163,12 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
 
 __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ __align__(8) uint64_t bar_stage[2];
-    __shared__ __align__(8) uint64_t bar_a, bar_dh, bar_o;
+    __shared__ __align__(8) uint64_t bar_stage[2], bar_ofree[2];
+    __shared__ __align__(8) uint64_t bar_h, bar_vn, bar_a, bar_dh, bar_o;
     __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int H = p.H, K = p.K, V = p.V;
     const int s = blockIdx.x / H, hh = blockIdx.x % H;
     const int vt = blockIdx.y, v0 = vt * kBVt;
@@ -157,8 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const int nchunks = (si.len + kChunk - 1) / kChunk;
     const int gc0 = p.cu_seqlens ? p.seq_chunk0[s] : s * ((p.T + kChunk - 1) / kChunk);
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t bar_st0 = smem_u32(&bar_stage[0]), bar_st1 = smem_u32(&bar_stage[1]);
-    const uint32_t b_a = smem_u32(&bar_a), b_dh = smem_u32(&bar_dh), b_o = smem_u32(&bar_o);
+    const uint32_t b_st[2] = {smem_u32(&bar_stage[0]), smem_u32(&bar_stage[1])};
+    const uint32_t b_of[2] = {smem_u32(&bar_ofree[0]), smem_u32(&bar_ofree[1])};
+    const uint32_t b_h = smem_u32(&bar_h), b_vn = smem_u32(&bar_vn), b_a = smem_u32(&bar_a);
+    const uint32_t b_dh = smem_u32(&bar_dh), b_o = smem_u32(&bar_o);
+    volatile int *abort = &abort_s;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -167,8 +192,13 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_st0));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_st1));
+        abort_s = 0;
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(b_st[0]));  // two copy parts
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(b_st[1]));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[0]));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[1]));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(b_h));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(b_vn));  // warps 0, 1, 4, 5
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_a));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_dh));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_o));
@@ -184,67 +214,212 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     __syncthreads();
     fence_after();
     const uint32_t tmem = tmem_base_s;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // state row r = tid (TMEM lane of the M=128 accumulator), columns v0..v0+63
-    const int r = tid;
-    float h[64];
-#pragma unroll
-    for (int c = 0; c < 64; ++c)
-        h[c] = (p.h0 && r < K && v0 + c < V) ? p.h0[(((int64_t)s * H + hh) * K + r) * V + v0 + c] : 0.f;
-
-    // chunk c's operands: part 0 = w, qg, kg^T, u, dec; part 1 = P (P of the
-    // stage's previous chunk is read by the deferred output MMA, so it is
-    // copied later). Both parts complete on the stage's mbarrier.
-    auto issue_stage = [&](int c, int part) {  // one thread
+    // chunk c's operands into stage c&1: part 0 = the MMA-only operands
+    // (w, qg, kg^T, P), part 1 = what threads read (u, dec). Each part is one
+    // arrival with its byte count on the stage's barrier.
+    auto issue_stage = [&](int c, int part) {
         const int st = c & 1;
         const uint32_t dst = sbase + st * Lay::stage;
-        const uint32_t bar = st ? bar_st1 : bar_st0;
         const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
+        const uint32_t bytes = part == 0 ? 3 * kImgW + kImgP : kImgU + kDecB;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b_st[st]), "r"(bytes)
+                     : "memory");
+        const void *src[4];
+        uint32_t off[4], len[4];
+        int n;
         if (part == 0) {
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                         "r"(Lay::copy_bytes)
-                         : "memory");
-            const void *src[5] = {p.w_img + gch * kImgW, p.qg_img + gch * kImgW, p.kg_img + gch * kImgW,
-                                  p.u_img + (gch * p.n_vt + vt) * kImgU, p.dec + gch * kKP};
-            const uint32_t off[5] = {Lay::w, Lay::qg, Lay::kg, Lay::u, Lay::dec};
-            const uint32_t len[5] = {kImgW, kImgW, kImgW, kImgU, kDecB};
-#pragma unroll
-            for (int x = 0; x < 5; ++x)
-                asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                        dst + off[x]),
-                    "l"(src[x]), "r"(len[x]), "r"(bar)
-                    : "memory");
+            src[0] = p.w_img + gch * kImgW;
+            src[1] = p.qg_img + gch * kImgW;
+            src[2] = p.kg_img + gch * kImgW;
+            src[3] = p.p_img + gch * kImgP;
+            off[0] = Lay::w; off[1] = Lay::qg; off[2] = Lay::kg; off[3] = Lay::pm;
+            len[0] = len[1] = len[2] = kImgW; len[3] = kImgP;
+            n = 4;
         } else {
+            src[0] = p.u_img + (gch * p.n_vt + vt) * kImgU;
+            src[1] = p.dec + gch * kKP;
+            off[0] = Lay::u; off[1] = Lay::dec;
+            len[0] = kImgU; len[1] = kDecB;
+            n = 2;
+        }
+        for (int x = 0; x < n; ++x)
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    dst + Lay::pm),
-                "l"(p.p_img + gch * kImgP), "r"(kImgP), "r"(bar)
+                    dst + off[x]),
+                "l"(src[x]), "r"(len[x]), "r"(b_st[st])
                 : "memory");
+    };
+    // v_new = u - Xw for token row i, columns c0 .. c0+31 (warps 0,1 / 4,5)
+    auto vnew_half = [&](int c, int i, int c0) {
+        const int st = c & 1;
+        const uint32_t par = c & 1;
+        uint32_t rr[32];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(rr[0]), "=r"(rr[1]), "=r"(rr[2]), "=r"(rr[3]), "=r"(rr[4]), "=r"(rr[5]), "=r"(rr[6]),
+              "=r"(rr[7]), "=r"(rr[8]), "=r"(rr[9]), "=r"(rr[10]), "=r"(rr[11]), "=r"(rr[12]), "=r"(rr[13]),
+              "=r"(rr[14]), "=r"(rr[15]), "=r"(rr[16]), "=r"(rr[17]), "=r"(rr[18]), "=r"(rr[19]),
+              "=r"(rr[20]), "=r"(rr[21]), "=r"(rr[22]), "=r"(rr[23]), "=r"(rr[24]), "=r"(rr[25]),
+              "=r"(rr[26]), "=r"(rr[27]), "=r"(rr[28]), "=r"(rr[29]), "=r"(rr[30]), "=r"(rr[31])
+            : "r"(tmem + lane_base + kColD + par * 64 + c0));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const unsigned char *urow = sm + st * Lay::stage + Lay::u + i * (kUS * 2) + c0 * 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 uv = *reinterpret_cast<const uint4 *>(urow + 16 * j);
+            const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
+            float f[8];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float2 t = __bfloat1622float2(u2[x]);
+                f[2 * x] = t.x - __uint_as_float(rr[8 * j + 2 * x]);
+                f[2 * x + 1] = t.y - __uint_as_float(rr[8 * j + 2 * x + 1]);
+            }
+            // MN-major B operand (N = column, K = token): (col/8)*1024 + i*16
+            *reinterpret_cast<uint4 *>(sm + Lay::vn + par * Lay::vn_bytes + (c0 / 8 + j) * 1024 + i * 16) =
+                pack8(f);
         }
     };
-    // output of chunk c (warps 2-3): O += P v_new, then store O's rows
-    auto output = [&](int c, bool &okc) {
-        const int st = c & 1;
-        const uint32_t dcol = kColD + (uint32_t)(c & 1) * 64;
-        if (tid == 64) {
-            const uint32_t vb = sbase + Lay::vn + (uint32_t)(c & 1) * Lay::vn_bytes;
-            const uint32_t stg = sbase + st * Lay::stage;
+
+    if (warp < 4) {
+        // ------------------------------------------------ recurrence warps
+        const int r = tid;
+        float h[64];
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma(tmem + dcol, sdesc(stg + Lay::z + ks * 256, 128, 1024), sdesc(vb + ks * 256, 128, 1024),
-                    kIdescK, 1);
-            commit(b_o);
+        for (int c = 0; c < 64; ++c)
+            h[c] = (p.h0 && r < K && v0 + c < V) ? p.h0[(((int64_t)s * H + hh) * K + r) * V + v0 + c] : 0.f;
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            const uint32_t par = c & 1;
+            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
+            // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = pack8(&h[8 * j]);
+            fence_async_smem();
+            arrive(b_h);
+            if (!ok) break;
+            if (warp < 2) {  // v_new for token row i = tid, columns 0..31
+                ok = warp_all(wait_bar(b_a, par, abort));
+                fence_after();
+                vnew_half(c, tid, 0);
+                fence_async_smem();
+                fence_before();
+                arrive(b_vn);
+                if (!ok) break;
+            }
+            ok = warp_all(wait_bar(b_dh, par, abort));
+            fence_after();
+            float t[64];
+            tmem_ld64(tmem + lane_base + kColDh, t);
+            const float d = reinterpret_cast<const float *>(sm + st * Lay::stage + Lay::dec)[r];
+#pragma unroll
+            for (int x = 0; x < 64; ++x) h[x] = fmaf(d, h[x], t[x]);
+            fence_before();
         }
-        okc = wait_bar(b_o, c & 1) && okc;
-        fence_after();
-        float t[64];
-        tmem_ld64(tmem + lane_base + dcol, t);
-        const int i = tid - 64;
-        const int pos0 = c * kChunk;
-        const int Lc = min(kChunk, si.len - pos0);
-        if (i < Lc && okc) {
+        if (ok && p.h_final && r < K) {
+#pragma unroll
+            for (int x = 0; x < 64; ++x)
+                if (v0 + x < V) p.h_final[(((int64_t)s * H + hh) * K + r) * V + v0 + x] = h[x];
+        }
+    } else if (warp == 4 || warp == 5) {
+        // ---------------------- v_new helpers (columns 32..63); lane 0 of warp 4 issues
+        const bool issuer = tid == 128;
+        if (issuer && nchunks > 0) issue_stage(0, 1);  // part 0 of chunks 0, 1: output warp
+        bool ok = true;
+        int c = 0;
+        for (; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            const uint32_t par = c & 1;
+            const uint32_t stg = sbase + st * Lay::stage;
+            const uint32_t dcol = kColD + par * 64;
+            if (issuer) {
+                // h of chunk c written and its operands landed (this accumulator
+                // set's previous user, chunk c-2, was read out before P v_new of
+                // chunk c-1 was issued, below)
+                ok = wait_bar(b_h, par, abort);
+                if (ok) ok = wait_bar(b_st[st], (c >> 1) & 1, abort);
+                if (ok) {
+                    fence_after();
+                    const uint32_t hb = sbase + Lay::h;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma(tmem + dcol, sdesc(stg + Lay::w + ks * 256, 128, 2048), sdesc(hb + ks * 256, 128, 2048),
+                            kIdescK, ks > 0);
+                    commit(b_a);
+                    // u and dec of chunk c+1: every thread read chunk c-1's before
+                    // arriving on b_h for chunk c
+                    if (c + 1 < nchunks) issue_stage(c + 1, 1);
+                }
+            }
+            ok = warp_all(ok);
+            if (ok) ok = wait_bar(b_st[st], (c >> 1) & 1, abort);  // u of chunk c
+            if (ok) ok = wait_bar(b_a, par, abort);
+            ok = warp_all(ok);
+            fence_after();
+            if (ok) vnew_half(c, tid - 128, 32);
+            fence_async_smem();
+            fence_before();
+            arrive(b_vn);
+            if (issuer && ok) {
+                ok = wait_bar(b_vn, par, abort);
+                if (ok) {
+                    fence_after();
+                    const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma(tmem + kColDh, sdesc(stg + Lay::kg + ks * 256, 128, 1024), sdesc(vb + ks * 256, 128, 1024),
+                            kIdescMN, ks > 0);
+                    commit(b_dh);
+                    // b_o must not run two phases ahead of the output warps: chunk
+                    // c-1's output has to be read out before chunk c's is committed
+                    if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
+                    if (ok) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            mma(tmem + dcol, sdesc(stg + Lay::z + ks * 256, 128, 1024),
+                                sdesc(vb + ks * 256, 128, 1024), kIdescK, 1);
+                        commit(b_o);
+                    }
+                }
+            }
+            ok = warp_all(ok);  // the warp leaves together
+        }
+        if (issuer && !ok) {
+            // drain what was issued: the last MMA groups and outstanding copies
+            *abort = 1;
+            wait_bar(b_a, (uint32_t)c & 1, nullptr);
+            wait_bar(b_o, (uint32_t)(c - 1) & 1, nullptr);
+            wait_bar(b_st[c & 1], (c >> 1) & 1, nullptr);
+            if (c + 1 < nchunks) wait_bar(b_st[(c + 1) & 1], ((c + 1) >> 1) & 1, nullptr);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------ output warps (lanes 64-127)
+        const int i = tid - 192;  // token row within the chunk
+        if (tid == 192) {
+            if (nchunks > 0) issue_stage(0, 0);
+            if (nchunks > 1) issue_stage(1, 0);
+        }
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const uint32_t par = c & 1;
+            ok = warp_all(wait_bar(b_o, par, abort));
+            fence_after();
+            // chunk c's last MMA is done: its stage's MMA operands may be
+            // replaced by chunk c+2's
+            if (tid == 192 && ok && c + 2 < nchunks) issue_stage(c + 2, 0);
+            float t[64];
+            tmem_ld64(tmem + lane_base + kColD + par * 64, t);
+            fence_before();
+            arrive(b_of[c & 1]);
+            const int pos0 = c * kChunk;
+            const int Lc = min(kChunk, si.len - pos0);
+            if (!ok || i >= Lc) continue;
             const int tq = q_token(p.reverse, si.len, pos0 + i);
             const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
 #pragma unroll
@@ -285,133 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 }
             }
         }
-    };
-
-    int timed_out = 0;
-    if (nchunks > 0 && tid == 32) {
-        issue_stage(0, 0);
-        issue_stage(0, 1);
-    }
-    int c = 0;
-    for (; c < nchunks; ++c) {
-        const int st = c & 1;
-        const uint32_t par = c & 1;  // phase of the per-chunk barriers
-        const uint32_t stg = sbase + st * Lay::stage;
-        const int pos0 = c * kChunk;
-        const int Lc = min(kChunk, si.len - pos0);
-
-        // operands of chunk c have landed; h (bf16) -> MN-major B operand
-        const bool ok_stage = wait_bar(st ? bar_st1 : bar_st0, (c >> 1) & 1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = pack8(&h[8 * j]);
-        fence_async_smem();
-        fence_before();
-        if (__syncthreads_or(!ok_stage)) {
-            timed_out = 1;
-            break;
-        }
-        fence_after();
-        const uint32_t dcol = kColD + par * 64;  // this chunk's [Xw; O] columns
-        if (tid == 0) {  // [Xw; O] = [w; qg] h, K = 128 keys in 8 steps
-            const uint32_t hb = sbase + Lay::h;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma(tmem + dcol, sdesc(stg + Lay::w + ks * 256, 128, 2048), sdesc(hb + ks * 256, 128, 2048),
-                    kIdescK, ks > 0);
-            commit(b_a);
-        } else if (tid == 32 && c + 1 < nchunks) {
-            issue_stage(c + 1, 0);
-        }
-        bool ok = true;
-        if (warp >= 2 && c > 0) output(c - 1, ok);  // the previous chunk's output, off the critical path
-        if (warp < 2) {  // v_new = u - Xw for token row i = tid
-            ok = wait_bar(b_a, par);
-            fence_after();
-            float xw[64];
-            tmem_ld64(tmem + lane_base + dcol, xw);
-            const int i = tid;
-            const unsigned char *urow = sm + st * Lay::stage + Lay::u + i * (kUS * 2);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 uv = *reinterpret_cast<const uint4 *>(urow + 16 * j);
-                const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
-                float f[8];
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const float2 t = __bfloat1622float2(u2[x]);
-                    f[2 * x] = t.x - xw[8 * j + 2 * x];
-                    f[2 * x + 1] = t.y - xw[8 * j + 2 * x + 1];
-                }
-                // MN-major B operand (N = column, K = token): (col/8)*1024 + i*16
-                *reinterpret_cast<uint4 *>(sm + Lay::vn + par * Lay::vn_bytes + j * 1024 + i * 16) = pack8(f);
-            }
-            fence_async_smem();
-        }
-        fence_before();
-        if (__syncthreads_or(!ok)) {
-            timed_out = 2;
-            break;
-        }
-        fence_after();
-        const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
-        if (tid == 0) {  // dh = kg^T v_new (M = 128 keys, K = 64 tokens)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma(tmem + kColDh, sdesc(stg + Lay::kg + ks * 256, 128, 1024), sdesc(vb + ks * 256, 128, 1024),
-                    kIdescMN, ks > 0);
-            commit(b_dh);
-        } else if (tid == 32 && c + 1 < nchunks) {
-            issue_stage(c + 1, 1);  // the previous chunk's output MMA no longer reads this stage's P
-        }
-        // h = dec . h + dh (row r)
-        bool ok2 = wait_bar(b_dh, par);
-        fence_after();
-        {
-            float t[64];
-            tmem_ld64(tmem + lane_base + kColDh, t);
-            const float d = reinterpret_cast<const float *>(sm + st * Lay::stage + Lay::dec)[r];
-#pragma unroll
-            for (int x = 0; x < 64; ++x) h[x] = fmaf(d, h[x], t[x]);
-        }
-        fence_before();
-        if (__syncthreads_or(!ok2)) {
-            timed_out = 3;
-            break;
-        }
-    }
-    if (!timed_out && nchunks > 0) {  // the last chunk's output
-        fence_after();
-        bool ok = true;
-        if (warp >= 2) output(nchunks - 1, ok);
-        fence_before();
-        if (__syncthreads_or(!ok)) timed_out = 4;
     }
 
-    if (timed_out) {
-        // record, then drain what this CTA issued (bounded) before freeing TMEM
-        if (tid == 0) {
-            atomicOr(p.err, 2);
-            const uint32_t par = c & 1;
-            if (timed_out == 1) {
-                wait_bar((c & 1) ? bar_st1 : bar_st0, (c >> 1) & 1);
-            } else if (timed_out == 4) {
-                wait_bar(b_o, (nchunks - 1) & 1);
-            } else {
-                wait_bar(b_a, par);
-                if (c > 0) wait_bar(b_o, (c - 1) & 1);
-                if (timed_out == 3) wait_bar(b_dh, par);
-                if (c + 1 < nchunks) wait_bar(((c + 1) & 1) ? bar_st1 : bar_st0, ((c + 1) >> 1) & 1);
-            }
-        }
-    } else if (p.h_final && r < K) {
-#pragma unroll
-        for (int x = 0; x < 64; ++x)
-            if (v0 + x < V) p.h_final[(((int64_t)s * H + hh) * K + r) * V + v0 + x] = h[x];
-    }
     fence_before();
     __syncthreads();
     fence_after();
+    if (tid == 0 && *abort) atomicOr(p.err, 2);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
