@@ -10,8 +10,9 @@
 //   warps 0,1  with warps 4,5 (same TMEM lanes 0-63): v_new = u - Xw, each
 //   + 4,5      warp pair splitting a row's 64 columns in halves.
 //   warps 6-7  the output: read O for TMEM lanes 64-127 and store it; one of
-//              their threads also copies the next chunk's MMA operands.
-//   warp 4     lane 0 also issues every tcgen05.mma and the u / dec copies:
+//              their threads also copies chunk c+2's operands once chunk
+//              c's last MMA is done.
+//   warp 4     lane 0 also issues every tcgen05.mma:
 //              the first product of a chunk must finish before warp 4's
 //              v_new work anyway, and its later products follow that work.
 //
@@ -33,7 +34,9 @@
 // the next chunk. [Xw; O] and v_new are double buffered. The intra-chunk
 // kernel stores w, qg, kg^T, P, u and dec as per-chunk images in the
 // shared-memory operand layouts, so a chunk's operands arrive by six 1-D bulk
-// async copies (cp.async.bulk), double-buffered one chunk ahead.
+// async copies (cp.async.bulk), two chunks ahead (the MMA operands in two
+// stages, u in a ring of three and dec in a ring of four, so that every buffer
+// a copy overwrites was released before the copy is issued).
 //
 // Every wait is bounded: a wait that gives up raises a shared abort flag that
 // makes every role leave its loop, the kernel records GDN_DEVERR_TIMEOUT in
@@ -50,19 +53,20 @@ constexpr int kThreads = 256;  // 8 warps, see the role map above
 constexpr int kBVt = 64;  // value columns per CTA
 
 struct Lay {
-    // one stage: w | qg | kg^T | zero block | P | u | dec
+    // one stage of MMA operands: w | qg | kg^T | zero block | P
     static constexpr uint32_t w = 0;
     static constexpr uint32_t qg = w + kImgW;  // directly after w: [w; qg] is one M=128 operand
     static constexpr uint32_t kg = qg + kImgW;
     static constexpr uint32_t z = kg + kImgW;  // 64 zero rows stacked over P
     static constexpr uint32_t pm = z + kImgP;
-    static constexpr uint32_t u = pm + kImgP;
-    static constexpr uint32_t dec = u + kImgU;
-    static constexpr uint32_t stage = dec + kDecB;
-    static constexpr uint32_t h = 2 * stage;               // h as the MMA B operand (MN-major)
+    static constexpr uint32_t stage = pm + kImgP;
+    static constexpr uint32_t u = 2 * stage;               // ring of 3 u tiles
+    static constexpr uint32_t dec = u + 3 * kImgU;         // ring of 4 decay vectors
+    static constexpr uint32_t h = dec + 4 * kDecB;          // h as the MMA B operand (MN-major)
     static constexpr uint32_t vn = h + 64 * kKP * 2;       // 2 x v_new as the MMA B operand (MN-major)
     static constexpr uint32_t vn_bytes = 64 * 64 * 2;
     static constexpr uint32_t bytes = vn + 2 * vn_bytes;
+    static constexpr uint32_t copy_bytes = 3 * kImgW + kImgP + kImgU + kDecB;
 };
 
 // TMEM columns: [Xw; O] of even / odd chunks [0,64) / [64,128) (lane = row:
@@ -193,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     }
     if (tid == 0) {
         abort_s = 0;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(b_st[0]));  // two copy parts
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(b_st[1]));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_st[0]));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_st[1]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[0]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[1]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(b_h));
@@ -216,44 +220,29 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const uint32_t tmem = tmem_base_s;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // chunk c's operands into stage c&1: part 0 = the MMA-only operands
-    // (w, qg, kg^T, P), part 1 = what threads read (u, dec). Each part is one
-    // arrival with its byte count on the stage's barrier.
-    auto issue_stage = [&](int c, int part) {
+    // chunk c's operands: MMA operands into stage c&1, u into ring slot c%3,
+    // dec into ring slot c%4, all counted on the stage's barrier.
+    auto issue_stage = [&](int c) {
         const int st = c & 1;
         const uint32_t dst = sbase + st * Lay::stage;
         const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
-        const uint32_t bytes = part == 0 ? 3 * kImgW + kImgP : kImgU + kDecB;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b_st[st]), "r"(bytes)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b_st[st]), "r"(Lay::copy_bytes)
                      : "memory");
-        const void *src[4];
-        uint32_t off[4], len[4];
-        int n;
-        if (part == 0) {
-            src[0] = p.w_img + gch * kImgW;
-            src[1] = p.qg_img + gch * kImgW;
-            src[2] = p.kg_img + gch * kImgW;
-            src[3] = p.p_img + gch * kImgP;
-            off[0] = Lay::w; off[1] = Lay::qg; off[2] = Lay::kg; off[3] = Lay::pm;
-            len[0] = len[1] = len[2] = kImgW; len[3] = kImgP;
-            n = 4;
-        } else {
-            src[0] = p.u_img + (gch * p.n_vt + vt) * kImgU;
-            src[1] = p.dec + gch * kKP;
-            off[0] = Lay::u; off[1] = Lay::dec;
-            len[0] = kImgU; len[1] = kDecB;
-            n = 2;
-        }
-        for (int x = 0; x < n; ++x)
+        const void *src[6] = {p.w_img + gch * kImgW, p.qg_img + gch * kImgW, p.kg_img + gch * kImgW,
+                              p.p_img + gch * kImgP, p.u_img + (gch * p.n_vt + vt) * kImgU, p.dec + gch * kKP};
+        const uint32_t dsts[6] = {dst + Lay::w, dst + Lay::qg, dst + Lay::kg, dst + Lay::pm,
+                                  sbase + Lay::u + (uint32_t)(c % 3) * kImgU, sbase + Lay::dec + (uint32_t)(c % 4) * kDecB};
+        const uint32_t len[6] = {kImgW, kImgW, kImgW, kImgP, kImgU, kDecB};
+#pragma unroll
+        for (int x = 0; x < 6; ++x)
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    dst + off[x]),
+                    dsts[x]),
                 "l"(src[x]), "r"(len[x]), "r"(b_st[st])
                 : "memory");
     };
     // v_new = u - Xw for token row i, columns c0 .. c0+31 (warps 0,1 / 4,5)
     auto vnew_half = [&](int c, int i, int c0) {
-        const int st = c & 1;
         const uint32_t par = c & 1;
         uint32_t rr[32];
         asm volatile(
@@ -267,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
               "=r"(rr[26]), "=r"(rr[27]), "=r"(rr[28]), "=r"(rr[29]), "=r"(rr[30]), "=r"(rr[31])
             : "r"(tmem + lane_base + kColD + par * 64 + c0));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        const unsigned char *urow = sm + st * Lay::stage + Lay::u + i * (kUS * 2) + c0 * 2;
+        const unsigned char *urow = sm + Lay::u + (c % 3) * kImgU + i * (kUS * 2) + c0 * 2;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint4 uv = *reinterpret_cast<const uint4 *>(urow + 16 * j);
@@ -317,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             fence_after();
             float t[64];
             tmem_ld64(tmem + lane_base + kColDh, t);
-            const float d = reinterpret_cast<const float *>(sm + st * Lay::stage + Lay::dec)[r];
+            const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
 #pragma unroll
             for (int x = 0; x < 64; ++x) h[x] = fmaf(d, h[x], t[x]);
             fence_before();
@@ -330,7 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     } else if (warp == 4 || warp == 5) {
         // ---------------------- v_new helpers (columns 32..63); lane 0 of warp 4 issues
         const bool issuer = tid == 128;
-        if (issuer && nchunks > 0) issue_stage(0, 1);  // part 0 of chunks 0, 1: output warp
         bool ok = true;
         int c = 0;
         for (; c < nchunks && ok; ++c) {
@@ -342,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 // h of chunk c written and its operands landed (this accumulator
                 // set's previous user, chunk c-2, was read out before P v_new of
                 // chunk c-1 was issued, below)
+                // (b_h also means the recurrence warps saw chunk c's operands land)
                 ok = wait_bar(b_h, par, abort);
-                if (ok) ok = wait_bar(b_st[st], (c >> 1) & 1, abort);
                 if (ok) {
                     fence_after();
                     const uint32_t hb = sbase + Lay::h;
@@ -352,9 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                         mma(tmem + dcol, sdesc(stg + Lay::w + ks * 256, 128, 2048), sdesc(hb + ks * 256, 128, 2048),
                             kIdescK, ks > 0);
                     commit(b_a);
-                    // u and dec of chunk c+1: every thread read chunk c-1's before
-                    // arriving on b_h for chunk c
-                    if (c + 1 < nchunks) issue_stage(c + 1, 1);
                 }
             }
             ok = warp_all(ok);
@@ -397,22 +382,24 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             wait_bar(b_o, (uint32_t)(c - 1) & 1, nullptr);
             wait_bar(b_st[c & 1], (c >> 1) & 1, nullptr);
             if (c + 1 < nchunks) wait_bar(b_st[(c + 1) & 1], ((c + 1) >> 1) & 1, nullptr);
+            if (c + 2 < nchunks) wait_bar(b_st[c & 1], ((c + 2) >> 1) & 1, nullptr);
         }
     } else if (warp >= 6) {
         // ------------------------------------------------ output warps (lanes 64-127)
         const int i = tid - 192;  // token row within the chunk
         if (tid == 192) {
-            if (nchunks > 0) issue_stage(0, 0);
-            if (nchunks > 1) issue_stage(1, 0);
+            if (nchunks > 0) issue_stage(0);
+            if (nchunks > 1) issue_stage(1);
         }
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const uint32_t par = c & 1;
             ok = warp_all(wait_bar(b_o, par, abort));
             fence_after();
-            // chunk c's last MMA is done: its stage's MMA operands may be
-            // replaced by chunk c+2's
-            if (tid == 192 && ok && c + 2 < nchunks) issue_stage(c + 2, 0);
+            // chunk c's last MMA is done: stage c&1 may take chunk c+2's MMA
+            // operands; u slot (c+2)%3 was last read by chunk c-1's v_new and
+            // dec slot (c+2)%4 by chunk c-2's h update, both long finished
+            if (tid == 192 && ok && c + 2 < nchunks) issue_stage(c + 2);
             float t[64];
             tmem_ld64(tmem + lane_base + kColD + par * 64, t);
             fence_before();
