@@ -88,6 +88,32 @@ def kernel_bytes(w, name):
     return None
 
 
+KERNEL_SOURCES = {"intra_bf16": ["gdn_intra_bf16.cu", "gdn_common.cuh"],
+                  "state_tc": ["gdn_state_tc.cu", "gdn_common.cuh"]}
+
+
+def measured_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when no
+    capture exists for this kernel and workload or the kernel's sources have
+    changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if kernel not in KERNEL_SOURCES or not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "gated_delta_rule_18_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) == 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[3] == digest:
+                return int(parts[2])
+    return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -95,6 +121,25 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------- multi-rank ----
+
+def max_over_ranks(x, dist=None, device=None):
+    """The largest value of x over all ranks (the job takes as long as its
+    slowest replica); identity without a process group."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, steps, seconds):
+    """Whole-job throughput: every rank processed its own replica of the
+    workload (weak scaling), so the job processed world x tokens per step."""
+    return tokens_per_rank * world * steps / seconds
 
 
 # --------------------------------------------------------------- clocks ----
@@ -369,13 +414,10 @@ def main():
     clocks = sampler.stop()
     sec = a.elapsed_time(b) / 1e3
     per_kernel = gdn.profile_collect()
-    if dist:
-        t = torch.tensor([sec], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = max_over_ranks(sec, dist, dev)
     ms_per_step = sec / args.steps * 1e3
     tokens = w.B * w.T
-    value = tokens * world * args.steps / sec
+    value = job_tokens_per_s(tokens, world, args.steps, sec)
 
     fl, by = path_work(w)
     peaks, peak_src = load_peaks()
@@ -392,7 +434,8 @@ def main():
         ach = kb / avg_s / 1e9 if kb else None
         roofline = {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": (ach / peaks["hbm_gbs"]) if ach else None,
-                    "traffic": None, "avg_launch_us": avg_s * 1e6,
+                    "traffic": measured_traffic(name, args.workload) if args.T is None else None,
+                    "algorithmic_bytes": kb, "avg_launch_us": avg_s * 1e6,
                     "peak_source": f"{peak_src} hbm_gbs"}
 
     result = {
@@ -419,10 +462,7 @@ def main():
     }
     if not args.no_e2e:
         e2e_s, h2d, d2h = e2e_measure(gdn, w, d, ws, max(3, min(args.steps, 10)), dev)
-        if dist:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks(e2e_s, dist, dev)
         result["e2e"] = {"value": tokens * world / e2e_s, "unit": "tokens/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
