@@ -1,7 +1,8 @@
 // gdn_common.cuh -- shared definitions of the sm_103a kernels behind gdn.h:
 // the launch parameter block, sequence/token addressing (including the
 // flip-and-shift reverse scan done by index remapping), and thin inline-PTX
-// wrappers (cp.async, ldmatrix, bf16 mma).
+// wrappers (cp.async, bulk async copies, mbarriers, ldmatrix, movmatrix,
+// bf16 mma).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -16,7 +17,7 @@ constexpr int kChunk = 64;  // tokens per chunk
 // indistinguishable from 0 in fp32 next to O(1) terms, and the floor keeps
 // exp(G_i - G_j) of cumulative gates finite for g = -inf (a full reset).
 // The bf16 per-key path splits e^{G_i - G_j} into two factors about a point
-// at most 8 tokens away (see gdn_chunk_bf16.cu); a floor of -10 per token
+// at most 8 tokens away (see gdn_intra_bf16.cu); a floor of -10 per token
 // bounds each factor by e^80, below the fp32/bf16 overflow at e^88. It
 // changes the result only for per-key decays below e^-10 = 4.5e-5 per token,
 // by less than that relative amount.
@@ -131,6 +132,60 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
+// ---- mbarriers and 1-D bulk async copies (global -> shared)
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// order this thread's generic-proxy shared-memory accesses before later
+// async-proxy ones (bulk copies, tensor-core operand reads)
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// one arrival that also announces `bytes` of copies counted on the barrier
+__device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// bytes: a multiple of 16; both addresses 16-byte aligned
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for the mbarrier phase `parity`; false after ~0.5 s or once *abort is
+// set by another role (no hang either way). abort may be null.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 255) == 0) {
+            if (abort && *abort) return false;
+            const uint64_t t = now_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > 500000000ull) {
+                if (abort) *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *smem) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -140,6 +195,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *smem) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(smem_u32(smem)));
+}
+
+// 8x8 b16 transpose across the warp: in and out in the mma fragment layout
+// (lane holds row lane/4, columns 2*(lane%4) and 2*(lane%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
 }
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.

@@ -13,24 +13,34 @@
 // (SANA `fused_gdn.py` page, `_fused_gdn_kernel` Pass 1).
 //
 // Steps:
-//  1. cp.async every tile (q, k, v rows -- remapped for the reverse scan --
-//     and the gk tile); scalars (beta, g) load meanwhile.
-//  2. Row norms r = 1/sqrt(|x|^2 + 1e-6) as per-row scalars (the tiles stay
-//     raw); in-chunk cumulative gates.
-//  3. K K^T and Q K^T on tensor cores (mma.sync bf16 -> fp32), scaled by the
-//     norms, beta and Gamma: A's diagonal 16x16 blocks in fp32, its other
-//     blocks in bf16, P straight to its global image.
-//  4. Each warp inverts one diagonal block, T_II = (I + A_II)^{-1}, by
-//     forward substitution in registers (lane = column).
+//  1. One bulk async copy per q / k row (and gk row), remapped for the
+//     reverse scan, counted on an mbarrier; rows with no token are zeroed.
+//  2. K K^T and Q K^T on tensor cores (mma.sync bf16 -> fp32). Scalar gate:
+//     the squared row norms come from the diagonals of K K^T and of an extra
+//     Q Q^T diagonal block, and the in-chunk gate cumsum runs meanwhile.
+//     Per-key gate: norms and per-channel cumsums first, then the split
+//     products (below).
+//  3. Scaling by the norms, beta and Gamma: A's diagonal 16x16 blocks in fp32,
+//     its six blocks below the diagonal in bf16, P straight to its image.
+//  4. qg / kg images and the chunk decay. The value tile is then copied in
+//     (scalar gate: into the q tile's space, now free) while each warp
+//     inverts one diagonal block, T_II = (I + A_II)^{-1}, by forward
+//     substitution in registers (lane = column).
 //  5. (I + A) W = X is solved by block forward substitution,
 //     W_I = T_II (X_I - sum_{M<I} A_IM W_M), for X = [beta e^G k^ | beta V].
-//     Every warp owns 64-column slices of W, so the four block steps need no
-//     block-wide barrier; W overwrites X in shared memory.
-//  6. 16-byte stores of w and u.
+//     The row scales of X are folded into T's columns and B_IM = -T_II A_IM
+//     is formed once per block, so W_I = T_II diag(s_I) X~_I + sum B_IM W_M
+//     with X~ the raw tile. Every warp owns 64-column slices of W, writes each
+//     solved W_I over X~_I in shared memory (the operand of later blocks) and
+//     straight to its global image; the solve needs no block-wide barrier.
 // Every output is written as a per-chunk image in the shared-memory operand
 // layout the state kernel's tensor-core MMAs read (gdn_common.cuh), all 64
 // rows included (zeros past the chunk's end), so the state kernel stages each
 // one with a single bulk copy.
+//
+// Every wait on a copy is bounded (about 0.5 s); a wait that gives up sets
+// GDN_DEVERR_TIMEOUT in the error word and the CTA leaves after a second
+// bounded wait for its copies in flight.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -39,32 +49,42 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kThreads = 128;
-constexpr int kAbS = 72;  // bf16 row stride of A (MMA operand) and of warp scratch
+constexpr int kBS = 24;   // bf16 row stride of a 16x16 block (A below the diagonal, T)
+constexpr int kTSet = 4 * 16 * kBS;  // one set of T's four diagonal blocks
 constexpr int kAdS = 17;  // fp32 row stride of A's diagonal blocks
-constexpr int kTdS = 24;  // bf16 row stride of T's diagonal blocks
+constexpr int kDevErrTimeout = 2;
 
+// Shared memory. The scalar-gate kernel copies the value tile into the q
+// tile's space once qg is written; the per-key kernel keeps it apart (its
+// space first holds the three split operands of step 2).
 template <bool PERKEY>
 struct Lay {
     static constexpr int KP = kKP;
     static constexpr int KS = KP + 8;
-    static constexpr size_t q = 0;
-    static constexpr size_t k = q + 2 * kChunk * KS;
-    static constexpr size_t gates = k + 2 * kChunk * KS;
+    static constexpr size_t tile = (size_t)2 * kChunk * KS;
+    static constexpr size_t k = 0;
+    static constexpr size_t gates = k + tile;
     static constexpr size_t beta = gates + 4 * (PERKEY ? kChunk * KP : kChunk);
     static constexpr size_t rq = beta + 4 * kChunk;
     static constexpr size_t rk = rq + 4 * kChunk;
     static constexpr size_t ab = rk + 4 * kChunk;
-    static constexpr size_t ad = ab + 2 * kChunk * kAbS;
+    static constexpr size_t ad = ab + 2 * 6 * 16 * kBS;
     static constexpr size_t td = ad + 4 * 4 * 16 * kAdS;
-    static constexpr size_t v = td + 2 * 4 * 16 * kTdS;
-    // the value tile shares its space with the per-key operand scratch
-    static size_t v_bytes(int VP) {
-        const size_t a = (size_t)2 * kChunk * (VP + 8);
-        const size_t b = PERKEY ? (size_t)3 * 2 * kChunk * KS : 0;
-        return a > b ? a : b;
+    static constexpr size_t q = td + 3 * 2 * kTSet;
+    static size_t vtile(int VP) { return (size_t)2 * kChunk * (VP + 8); }
+    static constexpr size_t v = PERKEY ? q + tile : q;
+    static size_t bytes(int VP) {
+        if (PERKEY) {
+            const size_t a = vtile(VP), b = 3 * tile;
+            return q + tile + (a > b ? a : b);
+        }
+        const size_t a = vtile(VP);
+        return q + (a > tile ? a : tile);
     }
-    static size_t bytes(int VP) { return v + v_bytes(VP); }
 };
+
+// index of A's block (I, M), M < I, among the six below the diagonal
+__device__ __forceinline__ int blk(int I, int M) { return I * (I - 1) / 2 + M; }
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -86,14 +106,26 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
 __device__ __forceinline__ float2 ld_bf2(const bf16 *p) {
     return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
 }
+__device__ __forceinline__ void zero_row(bf16 *row, int from, int to) {  // 8-aligned bounds
+    for (int d = from; d < to; d += 8) *reinterpret_cast<uint4 *>(row + d) = make_uint4(0, 0, 0, 0);
+}
+// a bounded wait for a copy barrier; on time-out the error word is marked and
+// the copies in flight get a second bounded window before the caller leaves
+__device__ __forceinline__ bool wait_copies(uint32_t bar, int *err) {
+    if (wait_bar(bar, 0, nullptr)) return true;
+    atomicOr(err, kDevErrTimeout);
+    wait_bar(bar, 0, nullptr);
+    return false;
+}
 
 template <bool PERKEY>
-__global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int VP) {
+__global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const FwdParams p, int VP) {
     using L = Lay<PERKEY>;
     constexpr int KP = kKP;
     constexpr int KS = L::KS;
     constexpr int VPR = KP / 8;  // 16-byte vectors per q/k row
     extern __shared__ __align__(16) unsigned char sm[];
+    __shared__ __align__(8) uint64_t bar_qk, bar_v;
     bf16 *sQ = reinterpret_cast<bf16 *>(sm + L::q);
     bf16 *sK = reinterpret_cast<bf16 *>(sm + L::k);
     float *sG = reinterpret_cast<float *>(sm + L::gates);  // [64] or [64][KP]
@@ -102,13 +134,17 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
     float *sRk = reinterpret_cast<float *>(sm + L::rk);
     bf16 *sAb = reinterpret_cast<bf16 *>(sm + L::ab);
     float *sAd = reinterpret_cast<float *>(sm + L::ad);
-    bf16 *sTd = reinterpret_cast<bf16 *>(sm + L::td);
+    bf16 *sTd = reinterpret_cast<bf16 *>(sm + L::td);  // T_II, then T_II diag(s_w), T_II diag(beta)
     bf16 *sV = reinterpret_cast<bf16 *>(sm + L::v);
     const int VS = VP + 8;
+    const uint32_t b_qk = smem_u32(&bar_qk), b_v = smem_u32(&bar_v);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
     const int gid = blockIdx.x, hh = blockIdx.y;
+    // the first kernel of a fixed-length launch clears the error word (the
+    // chunk-table kernel does it for variable-length batches)
+    if (!p.cu_seqlens && gid == 0 && hh == 0 && tid == 0) *p.err = 0;
     int s, c;
     if (p.cu_seqlens) {
         if (gid >= *p.n_chunks) return;
@@ -132,129 +168,125 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
     const int64_t qk_base = si.b * p.qk_sb + hh * p.qk_sh;
     const int64_t v_base = si.b * p.v_sb + hh * p.v_sh;
 
-    // ---- 1. asynchronous tile loads (zero fill outside the chunk / K / V)
-    for (int e = tid; e < kChunk * VPR; e += kThreads) {
-        const int i = e / VPR, d = (e % VPR) * 8;
-        const int tq = i < Lc ? q_token(p.reverse, si.len, pos0 + i) : -1;
-        const int tk = i < Lc ? kv_token(p.reverse, si.len, pos0 + i) : -1;
-        const bool okq = tq >= 0 && d < K, okk = tk >= 0 && d < K;
-        cp_async16(sQ + i * KS + d, okq ? (const void *)(q + qk_base + (int64_t)(si.tstart + tq) * p.qk_st + d) : (const void *)q,
-                   okq ? 16 : 0);
-        cp_async16(sK + i * KS + d, okk ? (const void *)(k + qk_base + (int64_t)(si.tstart + tk) * p.qk_st + d) : (const void *)k,
-                   okk ? 16 : 0);
+    if (tid == 0) {
+        mbar_init(b_qk, kChunk);
+        mbar_init(b_v, kChunk);
+        fence_mbar_init();
     }
-    if (PERKEY) {
-        for (int e = tid; e < kChunk * (KP / 4); e += kThreads) {
-            const int i = e / (KP / 4), d = (e % (KP / 4)) * 4;
-            const int tk = i < Lc ? kv_token(p.reverse, si.len, pos0 + i) : -1;
-            const bool ok = tk >= 0 && d < K;
-            cp_async16(sG + i * KP + d,
-                       ok ? (const void *)(p.gk + ((si.row0 + tk) * H + hh) * (int64_t)K + d) : (const void *)p.gk,
-                       ok ? 16 : 0);
-        }
-    }
-    auto load_v = [&]() {
-        const int VPRv = VP / 8;
-        for (int e = tid; e < kChunk * VPRv; e += kThreads) {
-            const int i = e / VPRv, c0 = (e % VPRv) * 8;
-            const int tk = i < Lc ? kv_token(p.reverse, si.len, pos0 + i) : -1;
-            const bool ok = tk >= 0 && c0 + 8 <= V;
-            cp_async16(sV + i * VS + c0,
-                       ok ? (const void *)(v + v_base + (int64_t)(si.tstart + tk) * p.v_st + c0) : (const void *)v,
-                       ok ? 16 : 0);
-        }
-    };
-    if (!PERKEY) load_v();
-    cp_async_commit();
+    __syncthreads();
+
+    // ---- 1. row copies: thread i < 64 owns row i (its token, beta, gate)
+    int tk_row = -1;
     if (tid < kChunk) {
         const int i = tid;
+        const int tq = i < Lc ? q_token(p.reverse, si.len, pos0 + i) : -1;
+        const int tk = i < Lc ? kv_token(p.reverse, si.len, pos0 + i) : -1;
+        tk_row = tk;
+        const uint32_t rowb = (uint32_t)K * 2;
+        uint32_t bytes = (tq >= 0 ? rowb : 0) + (tk >= 0 ? rowb : 0);
+        if (PERKEY && tk >= 0) bytes += (uint32_t)K * 4;
+        arrive_expect_tx(b_qk, bytes);
+        if (tq >= 0) bulk_g2s(smem_u32(sQ + i * KS), q + qk_base + (int64_t)(si.tstart + tq) * p.qk_st, rowb, b_qk);
+        else zero_row(sQ + i * KS, 0, K);
+        if (tk >= 0) {
+            bulk_g2s(smem_u32(sK + i * KS), k + qk_base + (int64_t)(si.tstart + tk) * p.qk_st, rowb, b_qk);
+            if (PERKEY) bulk_g2s(smem_u32(sG + i * KP), p.gk + ((si.row0 + tk) * H + hh) * (int64_t)K, K * 4, b_qk);
+        } else {
+            zero_row(sK + i * KS, 0, K);
+            if (PERKEY)
+                for (int d = 0; d < K; d += 4) *reinterpret_cast<float4 *>(sG + i * KP + d) = make_float4(0, 0, 0, 0);
+        }
+        if (K < KP) {  // padding keys
+            zero_row(sQ + i * KS, K, KP);
+            zero_row(sK + i * KS, K, KP);
+            if (PERKEY)
+                for (int d = K; d < KP; d += 4) *reinterpret_cast<float4 *>(sG + i * KP + d) = make_float4(0, 0, 0, 0);
+        }
         float b = 0.f, gg = 0.f;
-        if (i < Lc) {
-            const int tk = kv_token(p.reverse, si.len, pos0 + i);
-            if (tk >= 0) {
-                b = p.beta[(si.row0 + tk) * H + hh];
-                if (!PERKEY) gg = fmaxf(p.g[(si.row0 + tk) * H + hh], kLogGateMin);
-            }
+        if (tk >= 0) {
+            b = p.beta[(si.row0 + tk) * H + hh];
+            if (!PERKEY) gg = fmaxf(p.g[(si.row0 + tk) * H + hh], kLogGateMin);
         }
         sB[i] = b;
         if (!PERKEY) sG[i] = gg;
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    const bool copied = wait_copies(b_qk, p.err);
+    if (__syncthreads_or(!copied)) return;
 
-    // ---- 2. row norms (as scalars) and in-chunk cumulative gates
-    {
-        const int r = tid & 63;
-        const bf16 *row = (tid < 64 ? sQ : sK) + r * KS;
-        float ss = 0.f;
-#pragma unroll
-        for (int d = 0; d < KP; d += 8) {
-            float f[8];
-            unpack8(*reinterpret_cast<const uint4 *>(row + d), f);
-#pragma unroll
-            for (int x = 0; x < 8; ++x) ss = fmaf(f[x], f[x], ss);
-        }
-        (tid < 64 ? sRq : sRk)[r] = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
-    }
-    if (PERKEY) {
-        for (int d = tid; d < KP; d += kThreads) {
-            float acc = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < kChunk; ++i) {
-                acc += fmaxf(sG[i * KP + d], kLogGateMinPerKeyTC);
-                sG[i * KP + d] = acc;
-            }
-        }
-    } else if (warp == 0) {
-        const float a0 = sG[2 * lane], a1 = sG[2 * lane + 1];
-        float incl = a0 + a1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        sG[2 * lane] = incl - a1;
-        sG[2 * lane + 1] = incl;
-    }
-    __syncthreads();
-
-    // ---- 3. A (strictly lower, beta-scaled) and P (lower incl. diagonal)
+    // ---- 2./3. A (strictly lower, beta-scaled) and P (lower incl. diagonal)
     unsigned char *gP = p.p_img + gch * kImgP;
     auto put_p = [&](int i, int j, float v0f, float v1f) {
         *reinterpret_cast<uint32_t *>(gP + img_p_off(i, j)) = pack_bf16(v0f, v1f);
     };
-    // store one A entry: diagonal block -> fp32, below -> bf16 operand
+    // store one A entry: diagonal block -> fp32, below -> bf16 operand block
     auto put_a = [&](int i, int j, float a) {
-        const int I = i >> 4;
-        if (j >= 16 * I)
+        const int I = i >> 4, M = j >> 4;
+        if (M == I)
             sAd[(I * 16 + (i & 15)) * kAdS + (j & 15)] = a;
         else
-            sAb[i * kAbS + j] = __float2bfloat16_rn(a);
+            sAb[(blk(I, M) * 16 + (i & 15)) * kBS + (j & 15)] = __float2bfloat16_rn(a);
     };
     if (!PERKEY) {
-        float ak[8][4], ap[8][4];
+        if (warp == 0) {  // in-chunk cumulative gates (exclusive of nothing: G_i includes g_i)
+            const float a0 = sG[2 * lane], a1 = sG[2 * lane + 1];
+            float incl = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            sG[2 * lane] = incl - a1;
+            sG[2 * lane + 1] = incl;
+        }
+        float ak[8][4], ap[8][4], aq[2][4];
 #pragma unroll
         for (int n = 0; n < 8; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) ak[n][e] = ap[n][e] = 0.f;
 #pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) aq[n][e] = 0.f;
+#pragma unroll
         for (int kk = 0; kk < KP / 16; ++kk) {
             uint32_t aK[4], aQ[4];
             ldsm_x4(aK, sK + (16 * warp + (lane & 15)) * KS + kk * 16 + (lane >> 4) * 8);
             ldsm_x4(aQ, sQ + (16 * warp + (lane & 15)) * KS + kk * 16 + (lane >> 4) * 8);
+            const int brow = (lane & 7) + ((lane >> 4) << 3), bcol = kk * 16 + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 if (np <= warp) {
                     uint32_t b[4];
-                    ldsm_x4(b, sK + (16 * np + (lane & 7) + ((lane >> 4) << 3)) * KS + kk * 16 +
-                                   ((lane >> 3) & 1) * 8);
+                    ldsm_x4(b, sK + (16 * np + brow) * KS + bcol);
                     mma_bf16(ak[2 * np], aK, b[0], b[1]);
                     mma_bf16(ak[2 * np + 1], aK, b[2], b[3]);
                     mma_bf16(ap[2 * np], aQ, b[0], b[1]);
                     mma_bf16(ap[2 * np + 1], aQ, b[2], b[3]);
                 }
             }
+            uint32_t bq[4];  // Q Q^T, diagonal block only (the q norms)
+            ldsm_x4(bq, sQ + (16 * warp + brow) * KS + bcol);
+            mma_bf16(aq[0], aQ, bq[0], bq[1]);
+            mma_bf16(aq[1], aQ, bq[2], bq[3]);
         }
+        // row i = 16 warp + g8 + 8 hf sits on the diagonal in lane t4 = g8/2,
+        // element 2 hf + (g8 & 1) of column group 2 warp + hf
+        if (t4 == (g8 >> 1)) {
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                if (np == warp) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int i = 16 * warp + g8 + 8 * hf;
+                        const float kk2 = (g8 & 1) ? ak[2 * np + hf][2 * hf + 1] : ak[2 * np + hf][2 * hf];
+                        const float qq2 = (g8 & 1) ? aq[hf][2 * hf + 1] : aq[hf][2 * hf];
+                        sRk[i] = p.l2norm ? rsqrtf(kk2 + 1e-6f) : 1.f;
+                        sRq[i] = p.l2norm ? rsqrtf(qq2 + 1e-6f) : 1.f;
+                    }
+                }
+            }
+        }
+        __syncthreads();
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
             if (n < 2 * (warp + 1)) {
@@ -279,6 +311,27 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
             }
         }
     } else {
+        {  // row norms as scalars (the tiles stay raw)
+            const int r = tid & 63;
+            const bf16 *row = (tid < 64 ? sQ : sK) + r * KS;
+            float ss = 0.f;
+#pragma unroll
+            for (int d = 0; d < KP; d += 8) {
+                float f[8];
+                unpack8(*reinterpret_cast<const uint4 *>(row + d), f);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) ss = fmaf(f[x], f[x], ss);
+            }
+            (tid < 64 ? sRq : sRk)[r] = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
+        }
+        for (int d = tid; d < KP; d += kThreads) {  // per-channel cumsums
+            float acc = 0.f;
+#pragma unroll 8
+            for (int i = 0; i < kChunk; ++i) {
+                acc += fmaxf(sG[i * KP + d], kLogGateMinPerKeyTC);
+                sG[i * KP + d] = acc;
+            }
+        }
         // Per-key gate: for column block J split e^{G_i - G_j} about the
         // block's middle row r = 16J + 8: left x_i^ . e^{G_i - G_r} (rows
         // i >= 16J), right k_j^ . e^{G_r - G_j} (rows of block J). Each factor
@@ -287,6 +340,7 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
         bf16 *sR = sV;
         bf16 *sLq = sR + kChunk * KS;
         bf16 *sLk = sLq + kChunk * KS;
+        __syncthreads();
         for (int e = tid; e < kChunk * KP; e += kThreads) {
             const int i = e / KP, d = e % KP, r = (i & ~15) + 8;
             const float f = __expf(sG[r * KP + d] - sG[i * KP + d]) * sRk[i];
@@ -345,12 +399,57 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
         }
     }
     __syncthreads();
-    if (PERKEY) {  // the operand scratch is free: bring in the value tile now
-        load_v();
-        cp_async_commit();
+
+    // ---- 4. qg, kg and the chunk decay to global
+    const int last = Lc - 1;
+    unsigned char *gQg = p.qg_img + gch * kImgW;
+    unsigned char *gKg = p.kg_img + gch * kImgW;
+    for (int e = tid; e < kChunk * VPR; e += kThreads) {
+        const int i = e / VPR, d0 = (e % VPR) * 8;
+        float fq[8], fk[8], fx[8];
+        unpack8(*reinterpret_cast<const uint4 *>(sQ + i * KS + d0), fq);
+        unpack8(*reinterpret_cast<const uint4 *>(sK + i * KS + d0), fk);
+        const float rq = sRq[i], rk = sRk[i];
+        if (PERKEY) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float Gi = sG[i * KP + d0 + x];
+                const float eg = __expf(Gi);
+                fx[x] = fk[x] * eg;  // e^{G} . k (raw k: the norm goes into T's columns)
+                fq[x] *= eg * rq;
+                fk[x] *= __expf(sG[last * KP + d0 + x] - Gi) * rk;
+            }
+            *reinterpret_cast<uint4 *>(sK + i * KS + d0) = pack8(fx);
+        } else {
+            const float eq = __expf(sG[i]) * rq, ek = __expf(sG[last] - sG[i]) * rk;
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                fq[x] *= eq;
+                fk[x] *= ek;
+            }
+        }
+        *reinterpret_cast<uint4 *>(gQg + img_w_off(i, d0)) = pack8(fq);
+        *reinterpret_cast<uint4 *>(gKg + img_kt_off(i, d0)) = pack8(fk);
+    }
+    for (int d = tid; d < KP; d += kThreads)
+        p.dec[gch * KP + d] = PERKEY ? __expf(sG[last * KP + d]) : __expf(sG[last]);
+    fence_async_smem();  // these generic accesses come before the copies that reuse the space
+    __syncthreads();     // the q tile (scalar gate) and the split operands (per key) are free
+
+    //         the value tile, one bulk copy per row, into the freed space
+    if (tid < kChunk) {
+        const int i = tid;
+        const uint32_t rowb = (uint32_t)V * 2;
+        arrive_expect_tx(b_v, tk_row >= 0 ? rowb : 0);
+        if (tk_row >= 0)
+            bulk_g2s(smem_u32(sV + i * VS), v + v_base + (int64_t)(si.tstart + tk_row) * p.v_st, rowb, b_v);
+        else
+            zero_row(sV + i * VS, 0, V);
+        if (V < VP) zero_row(sV + i * VS, V, VP);
+        if (p.has_den) sV[i * VS + V] = __float2bfloat16_rn(1.f);  // the denominator's ones column
     }
 
-    // ---- 4. T_II = (I + A_II)^{-1} for the diagonal block of this warp;
+    //         T_II = (I + A_II)^{-1} for the diagonal block of this warp;
     //         lane c < 16 holds column c: t = e_c, t_r = -sum_{j<r} A_rj t_j
     {
         const int I = warp, cc = lane & 15;
@@ -365,140 +464,113 @@ __global__ void __launch_bounds__(kThreads) intra_kernel(const FwdParams p, int 
             for (int j = 0; j < r; ++j) acc = fmaf(Ad[r * kAdS + j], t[j], acc);
             if (r > cc) t[r] = -acc;
         }
-        if (lane < 16) {
+        if (lane < 16) {  // T_II and its column-scaled copies for the w and u right-hand sides
+            const int j = 16 * I + cc;
+            const float bj = sB[j];
+            const float sw = PERKEY ? bj * sRk[j] : bj * sRk[j] * __expf(sG[j]);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sTd[(I * 16 + r) * kTdS + cc] = __float2bfloat16_rn(t[r]);
-        }
-    }
-
-    //         qg, kg and the chunk decay to global
-    const int last = Lc - 1;
-    unsigned char *gQg = p.qg_img + gch * kImgW;
-    unsigned char *gKg = p.kg_img + gch * kImgW;
-    for (int e = tid; e < kChunk * VPR; e += kThreads) {
-        const int i = e / VPR, d0 = (e % VPR) * 8;
-        float fq[8], fk[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sQ + i * KS + d0), fq);
-        unpack8(*reinterpret_cast<const uint4 *>(sK + i * KS + d0), fk);
-        const float rq = sRq[i], rk = sRk[i];
-        if (PERKEY) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const float Gi = sG[i * KP + d0 + x];
-                fq[x] *= __expf(Gi) * rq;
-                fk[x] *= __expf(sG[last * KP + d0 + x] - Gi) * rk;
-            }
-        } else {
-            const float eq = __expf(sG[i]) * rq, ek = __expf(sG[last] - sG[i]) * rk;
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                fq[x] *= eq;
-                fk[x] *= ek;
+            for (int r = 0; r < 16; ++r) {
+                const int o = (I * 16 + r) * kBS + cc;
+                sTd[o] = __float2bfloat16_rn(t[r]);
+                sTd[kTSet + o] = __float2bfloat16_rn(t[r] * sw);
+                sTd[2 * kTSet + o] = __float2bfloat16_rn(t[r] * bj);
             }
         }
-        *reinterpret_cast<uint4 *>(gQg + img_w_off(i, d0)) = pack8(fq);
-        *reinterpret_cast<uint4 *>(gKg + img_kt_off(i, d0)) = pack8(fk);
+        __syncwarp();
+        //     B_IM = -T_II A_IM for the blocks left of this warp's diagonal
+        //     block, in place of A_IM
+        if (I > 0) {
+            uint32_t a[4];
+            ldsm_x4(a, sTd + (16 * I + (lane & 15)) * kBS + (lane >> 4) * 8);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) a[x] ^= 0x80008000u;  // -T_II
+            for (int M = 0; M < I; ++M) {
+                bf16 *blkp = sAb + blk(I, M) * 16 * kBS;
+                uint32_t b[4];
+                ldsm_x4_t(b, blkp + (lane & 15) * kBS + (lane >> 4) * 8);
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_bf16(c0, a, b[0], b[1]);
+                mma_bf16(c1, a, b[2], b[3]);
+                __syncwarp();  // every lane has read A_IM before it is overwritten
+                *reinterpret_cast<uint32_t *>(blkp + g8 * kBS + 2 * t4) = pack_bf16(c0[0], c0[1]);
+                *reinterpret_cast<uint32_t *>(blkp + (g8 + 8) * kBS + 2 * t4) = pack_bf16(c0[2], c0[3]);
+                *reinterpret_cast<uint32_t *>(blkp + g8 * kBS + 8 + 2 * t4) = pack_bf16(c1[0], c1[1]);
+                *reinterpret_cast<uint32_t *>(blkp + (g8 + 8) * kBS + 8 + 2 * t4) = pack_bf16(c1[2], c1[3]);
+            }
+        }
     }
-    for (int d = tid; d < KP; d += kThreads)
-        p.dec[gch * KP + d] =
-            PERKEY ? __expf(sG[last * KP + d]) : __expf(sG[last]);
-    if (PERKEY) cp_async_wait<0>();
     __syncthreads();
 
-    // ---- 5. W_I = T_II (X_I - sum_{M<I} A_IM W_M), per 64-column slice
-    bf16 *scratch = sQ + warp * 16 * kAbS;  // q tile is no longer needed
+    // ---- 5. W_I = T_II diag(s_I) X~_I + sum_{M<I} B_IM W_M per 64-column
+    //         slice, straight to the w / u images. X = diag(s) X~ with X~ the
+    //         tile in shared memory (k, or e^{G} . k per key; V) and s the row
+    //         scales, folded into T's columns.
+    unsigned char *gW = p.w_img + gch * kImgW;
+    unsigned char *gU = p.u_img + gch * p.n_vt * kImgU;
     const int nsw = KP / 64, nsu = VP / 64;
+    bool v_ready = false;
     for (int sl = warp; sl < nsw + nsu; sl += kThreads / 32) {
         const bool isw = sl < nsw;
-        bf16 *tile = isw ? sK : sV;
+        if (!isw && !v_ready) {
+            if (!wait_copies(b_v, p.err)) return;
+            v_ready = true;
+        }
+        bf16 *tile = isw ? sK : sV;  // rows of X~_I, then of W_I once solved
+        const bf16 *sTs = sTd + (isw ? kTSet : 2 * kTSet);
         const int ts = isw ? KS : VS;
         const int c0 = isw ? 64 * sl : 64 * (sl - nsw);
-#pragma unroll 1
+#pragma unroll
         for (int I = 0; I < 4; ++I) {
-            float acc[8][4];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int i = 16 * I + g8 + 8 * hf;
-                const float bi = sB[i];
-                const float srow = isw ? (PERKEY ? bi * sRk[i] : bi * sRk[i] * __expf(sG[i])) : bi;
-#pragma unroll
-                for (int n = 0; n < 8; ++n) {
-                    const int col = c0 + 8 * n + 2 * t4;
-                    float2 x = ld_bf2(tile + i * ts + col);
-                    if (!isw && p.has_den) {
-                        if (col == V) x.x = 1.f;
-                        if (col + 1 == V) x.y = 1.f;
-                    }
-                    float s0 = srow, s1 = srow;
-                    if (isw && PERKEY) {
-                        s0 *= __expf(sG[i * KP + col]);
-                        s1 *= __expf(sG[i * KP + col + 1]);
-                    }
-                    acc[n][2 * hf] = x.x * s0;
-                    acc[n][2 * hf + 1] = x.y * s1;
-                }
-            }
-#pragma unroll
-            for (int M = 0; M < 3; ++M) {
-                if (M < I) {
-                    uint32_t a[4];
-                    ldsm_x4(a, sAb + (16 * I + (lane & 15)) * kAbS + 16 * M + (lane >> 4) * 8);
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) a[x] ^= 0x80008000u;  // -A
-#pragma unroll
-                    for (int np = 0; np < 4; ++np) {
-                        uint32_t b[4];
-                        ldsm_x4_t(b, tile + (16 * M + (lane & 15)) * ts + c0 + 16 * np + (lane >> 4) * 8);
-                        mma_bf16(acc[2 * np], a, b[0], b[1]);
-                        mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    *reinterpret_cast<uint32_t *>(scratch + (g8 + 8 * hf) * kAbS + 8 * n + 2 * t4) =
-                        pack_bf16(acc[n][2 * hf], acc[n][2 * hf + 1]);
-            __syncwarp();
             float wa[8][4];
 #pragma unroll
             for (int n = 0; n < 8; ++n)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) wa[n][e] = 0.f;
-            uint32_t a[4];
-            ldsm_x4(a, sTd + (16 * I + (lane & 15)) * kTdS + (lane >> 4) * 8);
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b[4];
-                ldsm_x4_t(b, scratch + (lane & 15) * kAbS + 16 * np + (lane >> 4) * 8);
-                mma_bf16(wa[2 * np], a, b[0], b[1]);
-                mma_bf16(wa[2 * np + 1], a, b[2], b[3]);
+            for (int M = 0; M < I; ++M) {
+                uint32_t a[4];
+                ldsm_x4(a, sAb + (blk(I, M) * 16 + (lane & 15)) * kBS + (lane >> 4) * 8);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b[4];
+                    ldsm_x4_t(b, tile + (16 * M + (lane & 15)) * ts + c0 + 16 * np + (lane >> 4) * 8);
+                    mma_bf16(wa[2 * np], a, b[0], b[1]);
+                    mma_bf16(wa[2 * np + 1], a, b[2], b[3]);
+                }
+            }
+            {
+                uint32_t a[4];
+                ldsm_x4(a, sTs + (16 * I + (lane & 15)) * kBS + (lane >> 4) * 8);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b[4];
+                    ldsm_x4_t(b, tile + (16 * I + (lane & 15)) * ts + c0 + 16 * np + (lane >> 4) * 8);
+                    mma_bf16(wa[2 * np], a, b[0], b[1]);
+                    mma_bf16(wa[2 * np + 1], a, b[2], b[3]);
+                }
             }
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    *reinterpret_cast<uint32_t *>(tile + (16 * I + g8 + 8 * hf) * ts + c0 + 8 * n + 2 * t4) =
-                        pack_bf16(wa[n][2 * hf], wa[n][2 * hf + 1]);
+            for (int n = 0; n < 8; ++n) {
+                const uint32_t lo = pack_bf16(wa[n][0], wa[n][1]), hi = pack_bf16(wa[n][2], wa[n][3]);
+                const int i = 16 * I + g8, cl = 8 * n + 2 * t4;
+                if (isw) {
+                    *reinterpret_cast<uint32_t *>(gW + img_w_off(i, c0 + cl)) = lo;
+                    *reinterpret_cast<uint32_t *>(gW + img_w_off(i + 8, c0 + cl)) = hi;
+                } else {
+                    unsigned char *u = gU + (c0 >> 6) * kImgU + cl * 2;
+                    *reinterpret_cast<uint32_t *>(u + i * (kUS * 2)) = lo;
+                    *reinterpret_cast<uint32_t *>(u + (i + 8) * (kUS * 2)) = hi;
+                }
+                if (I < 3) {
+                    *reinterpret_cast<uint32_t *>(tile + i * ts + c0 + cl) = lo;
+                    *reinterpret_cast<uint32_t *>(tile + (i + 8) * ts + c0 + cl) = hi;
+                }
+            }
             __syncwarp();
         }
     }
-    __syncthreads();
-
-    // ---- 6. w and u images (all 64 rows; rows past the chunk are zero)
-    unsigned char *gW = p.w_img + gch * kImgW;
-    for (int e = tid; e < kChunk * VPR; e += kThreads) {
-        const int i = e / VPR, d = (e % VPR) * 8;
-        *reinterpret_cast<uint4 *>(gW + img_w_off(i, d)) = *reinterpret_cast<const uint4 *>(sK + i * KS + d);
-    }
-    unsigned char *gU = p.u_img + gch * p.n_vt * kImgU;
-    const int VPRv = VP / 8;
-    for (int e = tid; e < kChunk * VPRv; e += kThreads) {
-        const int i = e / VPRv, c = (e % VPRv) * 8;
-        *reinterpret_cast<uint4 *>(gU + (c >> 6) * kImgU + i * (kUS * 2) + (c & 63) * 2) =
-            *reinterpret_cast<const uint4 *>(sV + i * VS + c);
-    }
+    // (every value-tile copy was waited for by the warp owning a u slice, so
+    // none outlives the CTA)
 }
 
 template <bool PERKEY>

@@ -99,44 +99,9 @@ __device__ __forceinline__ void commit(uint32_t bar) {
 }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ uint64_t now_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-// Wait for the mbarrier phase `parity`; false after ~0.5 s or once *abort is
-// set by another role (no hang either way).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        uint32_t ok;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-            " selp.u32 %0, 1, 0, p;\n}"
-            : "=r"(ok)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (ok) return true;
-        if ((it & 255) == 0) {
-            if (abort && *abort) return false;
-            const uint64_t t = now_ns();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > 500000000ull) {
-                if (abort) *abort = 1;
-                return false;
-            }
-        }
-    }
-}
 // a flag every lane of the warp agrees on (warp-collective tcgen05 ops need
 // the whole warp)
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
-
-__device__ __forceinline__ void arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 // 64 consecutive TMEM columns of this warp's 32 lanes -> 64 registers
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
@@ -176,7 +141,6 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const int H = p.H, K = p.K, V = p.V;
     const int s = blockIdx.x / H, hh = blockIdx.x % H;
     const int vt = blockIdx.y, v0 = vt * kBVt;
-    if (!p.cu_seqlens && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *p.err = 0;
     if (p.cu_seqlens && *p.n_chunks < 0) return;
     SeqInfo si;
     if (!seq_info(p, s, si)) return;
