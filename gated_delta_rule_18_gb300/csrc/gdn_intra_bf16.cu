@@ -103,9 +103,6 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
     u.w = pack_bf16(f[6], f[7]);
     return u;
 }
-__device__ __forceinline__ float2 ld_bf2(const bf16 *p) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(p));
-}
 __device__ __forceinline__ void zero_row(bf16 *row, int from, int to) {  // 8-aligned bounds
     for (int d = from; d < to; d += 8) *reinterpret_cast<uint4 *>(row + d) = make_uint4(0, 0, 0, 0);
 }
@@ -141,7 +138,9 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const F
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int gid = blockIdx.x, hh = blockIdx.y;
+    // heads vary fastest across the grid, so CTAs resident together read the
+    // same tokens of all heads (whole DRAM pages) rather than one head's rows
+    const int hh = blockIdx.x % p.H, gid = blockIdx.x / p.H;
     // the first kernel of a fixed-length launch clears the error word (the
     // chunk-table kernel does it for variable-length batches)
     if (!p.cu_seqlens && gid == 0 && hh == 0 && tid == 0) *p.err = 0;
@@ -287,27 +286,50 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const F
             }
         }
         __syncthreads();
+        // every scale factor first, then the stores (shared loads cannot be
+        // moved across stores the compiler must assume may alias them)
+        float Gi[2], ai[2], rqi[2];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int i = 16 * warp + g8 + 8 * hf;
+            Gi[hf] = sG[i];
+            ai[hf] = sB[i] * sRk[i];
+            rqi[hf] = sRq[i];
+        }
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
             if (n < 2 * (warp + 1)) {
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int i = 16 * warp + g8 + 8 * hf;
-                    const int j = 8 * n + 2 * t4;
-                    const float Gi = sG[i], bi = sB[i], rki = sRk[i], rqi = sRq[i];
-                    float pv[2];
+                for (int e = 0; e < 2; ++e) {
+                    const int jj = 8 * n + 2 * t4 + e;
+                    const float Gj = sG[jj], rkj = sRk[jj];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int jj = j + e;
-                        const float gam = (jj <= i) ? __expf(Gi - sG[jj]) * sRk[jj] : 0.f;
-                        if (jj < i) put_a(i, jj, bi * rki * ak[n][2 * hf + e] * gam);
-                        pv[e] = rqi * ap[n][2 * hf + e] * gam;
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int i = 16 * warp + g8 + 8 * hf;
+                        const float gam = (jj <= i) ? __expf(Gi[hf] - Gj) * rkj : 0.f;
+                        ak[n][2 * hf + e] = (jj < i) ? ai[hf] * ak[n][2 * hf + e] * gam : 0.f;
+                        ap[n][2 * hf + e] = rqi[hf] * ap[n][2 * hf + e] * gam;
                     }
-                    put_p(i, j, pv[0], pv[1]);
                 }
-            } else {  // right of the diagonal block: the image must hold zeros
+            }
+        }
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) put_p(16 * warp + g8 + 8 * hf, 8 * n + 2 * t4, 0.f, 0.f);
+        for (int n = 0; n < 8; ++n) {
+            const bool on = n < 2 * (warp + 1);  // else right of the diagonal block: zeros
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int i = 16 * warp + g8 + 8 * hf, j = 8 * n + 2 * t4;
+                put_p(i, j, on ? ap[n][2 * hf] : 0.f, on ? ap[n][2 * hf + 1] : 0.f);
+                if (on) {
+                    if ((n >> 1) == warp) {  // diagonal block, fp32 (entries j >= i are zero, unread)
+                        float *d = sAd + (16 * warp + (i & 15)) * kAdS + (j & 15);
+                        d[0] = ak[n][2 * hf];
+                        d[1] = ak[n][2 * hf + 1];
+                    } else {
+                        *reinterpret_cast<uint32_t *>(sAb + (blk(warp, n >> 1) * 16 + (i & 15)) * kBS + (j & 15)) =
+                            pack_bf16(ak[n][2 * hf], ak[n][2 * hf + 1]);
+                    }
+                }
             }
         }
     } else {
@@ -404,32 +426,49 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const F
     const int last = Lc - 1;
     unsigned char *gQg = p.qg_img + gch * kImgW;
     unsigned char *gKg = p.kg_img + gch * kImgW;
-    for (int e = tid; e < kChunk * VPR; e += kThreads) {
-        const int i = e / VPR, d0 = (e % VPR) * 8;
-        float fq[8], fk[8], fx[8];
-        unpack8(*reinterpret_cast<const uint4 *>(sQ + i * KS + d0), fq);
-        unpack8(*reinterpret_cast<const uint4 *>(sK + i * KS + d0), fk);
-        const float rq = sRq[i], rk = sRk[i];
-        if (PERKEY) {
+    constexpr int kQgBatch = 4;  // items loaded before any is stored
+    static_assert((kChunk * VPR) % (kQgBatch * kThreads) == 0, "qg batches");
+    for (int e0 = tid; e0 < kChunk * VPR; e0 += kQgBatch * kThreads) {
+        uint4 xq[kQgBatch], xk[kQgBatch];
+        float sq[kQgBatch], sk[kQgBatch], gi[kQgBatch];
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const float Gi = sG[i * KP + d0 + x];
-                const float eg = __expf(Gi);
-                fx[x] = fk[x] * eg;  // e^{G} . k (raw k: the norm goes into T's columns)
-                fq[x] *= eg * rq;
-                fk[x] *= __expf(sG[last * KP + d0 + x] - Gi) * rk;
-            }
-            *reinterpret_cast<uint4 *>(sK + i * KS + d0) = pack8(fx);
-        } else {
-            const float eq = __expf(sG[i]) * rq, ek = __expf(sG[last] - sG[i]) * rk;
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                fq[x] *= eq;
-                fk[x] *= ek;
-            }
+        for (int u = 0; u < kQgBatch; ++u) {
+            const int e = e0 + u * kThreads, i = e / VPR, d0 = (e % VPR) * 8;
+            xq[u] = *reinterpret_cast<const uint4 *>(sQ + i * KS + d0);
+            xk[u] = *reinterpret_cast<const uint4 *>(sK + i * KS + d0);
+            sq[u] = sRq[i];
+            sk[u] = sRk[i];
+            gi[u] = PERKEY ? 0.f : sG[i];
         }
-        *reinterpret_cast<uint4 *>(gQg + img_w_off(i, d0)) = pack8(fq);
-        *reinterpret_cast<uint4 *>(gKg + img_kt_off(i, d0)) = pack8(fk);
+        const float glast = PERKEY ? 0.f : sG[last];
+#pragma unroll
+        for (int u = 0; u < kQgBatch; ++u) {
+            const int e = e0 + u * kThreads, i = e / VPR, d0 = (e % VPR) * 8;
+            float fq[8], fk[8];
+            unpack8(xq[u], fq);
+            unpack8(xk[u], fk);
+            if (PERKEY) {
+                float fx[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const float Gi = sG[i * KP + d0 + x];
+                    const float eg = __expf(Gi);
+                    fx[x] = fk[x] * eg;  // e^{G} . k (raw k: the norm goes into T's columns)
+                    fq[x] *= eg * sq[u];
+                    fk[x] *= __expf(sG[last * KP + d0 + x] - Gi) * sk[u];
+                }
+                *reinterpret_cast<uint4 *>(sK + i * KS + d0) = pack8(fx);
+            } else {
+                const float eq = __expf(gi[u]) * sq[u], ek = __expf(glast - gi[u]) * sk[u];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    fq[x] *= eq;
+                    fk[x] *= ek;
+                }
+            }
+            *reinterpret_cast<uint4 *>(gQg + img_w_off(i, d0)) = pack8(fq);
+            *reinterpret_cast<uint4 *>(gKg + img_kt_off(i, d0)) = pack8(fk);
+        }
     }
     for (int d = tid; d < KP; d += kThreads)
         p.dec[gch * KP + d] = PERKEY ? __expf(sG[last * KP + d]) : __expf(sG[last]);
@@ -581,7 +620,7 @@ cudaError_t launch_t(const FwdParams &p, cudaStream_t st) {
     auto kern = intra_kernel<PERKEY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.max_chunks, p.H);
+    const dim3 grid((unsigned)p.max_chunks * (unsigned)p.H);
     kern<<<grid, kThreads, bytes, st>>>(p, VP);
     return cudaGetLastError();
 }
