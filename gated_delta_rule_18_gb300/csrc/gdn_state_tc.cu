@@ -42,7 +42,7 @@
 // makes every role leave its loop, the kernel records GDN_DEVERR_TIMEOUT in
 // the workspace error word, drains what it issued (again bounded), frees its
 // tensor memory and returns.
-#include "gdn_common.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
@@ -74,52 +74,8 @@ struct Lay {
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColD = 0, kColDh = 128;
 
-// instruction descriptors (kind::f16: bf16 inputs, fp32 accumulate)
-constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-constexpr uint32_t kIdescK = idesc(128, 64, 0, 1);   // A K-major ([w;qg], [0;P]), B MN-major
-constexpr uint32_t kIdescMN = idesc(128, 64, 1, 1);  // A = kg^T MN-major, B = v_new MN-major
-
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
-}
-
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(id), "r"(acc));
-}
-__device__ __forceinline__ void commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// a flag every lane of the warp agrees on (warp-collective tcgen05 ops need
-// the whole warp)
-__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
-
-// 64 consecutive TMEM columns of this warp's 32 lanes -> 64 registers
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
-    uint32_t r[64];
-#define GDN_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-        : GDN_R8(0), GDN_R8(8), GDN_R8(16), GDN_R8(24), GDN_R8(32), GDN_R8(40), GDN_R8(48), GDN_R8(56)
-        : "r"(taddr));
-#undef GDN_R8
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
-}
+constexpr uint32_t kIdescK = tc_idesc(128, 64, 0, 1);   // A K-major ([w;qg], [0;P]), B MN-major
+constexpr uint32_t kIdescMN = tc_idesc(128, 64, 1, 1);  // A = kg^T MN-major, B = v_new MN-major
 
 __device__ __forceinline__ uint4 pack8(const float *f) {
     uint4 u;
@@ -178,9 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         *reinterpret_cast<uint4 *>(sm + Lay::stage + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
     }
     fence_async_smem();
-    fence_before();
+    tc_fence_before();
     __syncthreads();
-    fence_after();
+    tc_fence_after();
     const uint32_t tmem = tmem_base_s;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
@@ -259,21 +215,21 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             if (!ok) break;
             if (warp < 2) {  // v_new for token row i = tid, columns 0..31
                 ok = warp_all(wait_bar(b_a, par, abort));
-                fence_after();
+                tc_fence_after();
                 vnew_half(c, tid, 0);
                 fence_async_smem();
-                fence_before();
+                tc_fence_before();
                 arrive(b_vn);
                 if (!ok) break;
             }
             ok = warp_all(wait_bar(b_dh, par, abort));
-            fence_after();
+            tc_fence_after();
             float t[64];
-            tmem_ld64(tmem + lane_base + kColDh, t);
+            tc_ld64(tmem + lane_base + kColDh, t);
             const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
 #pragma unroll
             for (int x = 0; x < 64; ++x) h[x] = fmaf(d, h[x], t[x]);
-            fence_before();
+            tc_fence_before();
         }
         if (ok && p.h_final && r < K) {
 #pragma unroll
@@ -297,43 +253,43 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 // (b_h also means the recurrence warps saw chunk c's operands land)
                 ok = wait_bar(b_h, par, abort);
                 if (ok) {
-                    fence_after();
+                    tc_fence_after();
                     const uint32_t hb = sbase + Lay::h;
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        mma(tmem + dcol, sdesc(stg + Lay::w + ks * 256, 128, 2048), sdesc(hb + ks * 256, 128, 2048),
+                        tc_mma(tmem + dcol, tc_sdesc(stg + Lay::w + ks * 256, 128, 2048), tc_sdesc(hb + ks * 256, 128, 2048),
                             kIdescK, ks > 0);
-                    commit(b_a);
+                    tc_commit(b_a);
                 }
             }
             ok = warp_all(ok);
             if (ok) ok = wait_bar(b_st[st], (c >> 1) & 1, abort);  // u of chunk c
             if (ok) ok = wait_bar(b_a, par, abort);
             ok = warp_all(ok);
-            fence_after();
+            tc_fence_after();
             if (ok) vnew_half(c, tid - 128, 32);
             fence_async_smem();
-            fence_before();
+            tc_fence_before();
             arrive(b_vn);
             if (issuer && ok) {
                 ok = wait_bar(b_vn, par, abort);
                 if (ok) {
-                    fence_after();
+                    tc_fence_after();
                     const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        mma(tmem + kColDh, sdesc(stg + Lay::kg + ks * 256, 128, 1024), sdesc(vb + ks * 256, 128, 1024),
+                        tc_mma(tmem + kColDh, tc_sdesc(stg + Lay::kg + ks * 256, 128, 1024), tc_sdesc(vb + ks * 256, 128, 1024),
                             kIdescMN, ks > 0);
-                    commit(b_dh);
+                    tc_commit(b_dh);
                     // b_o must not run two phases ahead of the output warps: chunk
                     // c-1's output has to be read out before chunk c's is committed
                     if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
                     if (ok) {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-                            mma(tmem + dcol, sdesc(stg + Lay::z + ks * 256, 128, 1024),
-                                sdesc(vb + ks * 256, 128, 1024), kIdescK, 1);
-                        commit(b_o);
+                            tc_mma(tmem + dcol, tc_sdesc(stg + Lay::z + ks * 256, 128, 1024),
+                                tc_sdesc(vb + ks * 256, 128, 1024), kIdescK, 1);
+                        tc_commit(b_o);
                     }
                 }
             }
@@ -359,14 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         for (int c = 0; c < nchunks && ok; ++c) {
             const uint32_t par = c & 1;
             ok = warp_all(wait_bar(b_o, par, abort));
-            fence_after();
+            tc_fence_after();
             // chunk c's last MMA is done: stage c&1 may take chunk c+2's MMA
             // operands; u slot (c+2)%3 was last read by chunk c-1's v_new and
             // dec slot (c+2)%4 by chunk c-2's h update, both long finished
             if (tid == 192 && ok && c + 2 < nchunks) issue_stage(c + 2);
             float t[64];
-            tmem_ld64(tmem + lane_base + kColD + par * 64, t);
-            fence_before();
+            tc_ld64(tmem + lane_base + kColD + par * 64, t);
+            tc_fence_before();
             arrive(b_of[c & 1]);
             const int pos0 = c * kChunk;
             const int Lc = min(kChunk, si.len - pos0);
@@ -413,9 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         }
     }
 
-    fence_before();
+    tc_fence_before();
     __syncthreads();
-    fence_after();
+    tc_fence_after();
     if (tid == 0 && *abort) atomicOr(p.err, 2);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
