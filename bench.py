@@ -89,7 +89,7 @@ def kernel_bytes(w, name):
 
 
 KERNEL_SOURCES = {"intra_bf16": ["gdn_intra_bf16.cu", "gdn_common.cuh"],
-                  "state_tc": ["gdn_state_tc.cu", "gdn_common.cuh"]}
+                  "state_tc": ["gdn_state_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"]}
 
 
 def measured_traffic(kernel, workload):
