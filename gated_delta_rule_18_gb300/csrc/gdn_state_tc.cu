@@ -2,7 +2,7 @@
 // on the fifth-generation tensor cores (tcgen05, accumulators in TMEM).
 //
 // One CTA per (sequence, head, 64-column value tile), walking the sequence's
-// 64-token chunks in order, warp-specialised (8 warps):
+// 64-token chunks in order, warp-specialised (9 warps):
 //
 //   warps 0-3  the recurrence. Thread r keeps row r of the fp32 state h
 //              (128 keys x 64 columns) in registers; per chunk it writes h as
@@ -12,9 +12,9 @@
 //   warps 6-7  the output: read O for TMEM lanes 64-127 and store it; one of
 //              their threads also copies chunk c+2's operands once chunk
 //              c's last MMA is done.
-//   warp 4     lane 0 also issues every tcgen05.mma:
-//              the first product of a chunk must finish before warp 4's
-//              v_new work anyway, and its later products follow that work.
+//   warp 8     lane 0 issues every tcgen05.mma and does nothing else, so it
+//              answers each hand-over at once and no v_new warp waits on
+//              its issuing.
 //
 // Per chunk (hyper-parallel coverage_diff page,
 // `chunk_gated_delta_rule_fwd_kernel_h_blockdim64`: b_v = u - w h,
@@ -49,7 +49,7 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kThreads = 256;  // 8 warps, see the role map above
+constexpr int kThreads = 288;  // 9 warps, see the role map above
 constexpr int kBVt = 64;  // value columns per CTA
 
 struct Lay {
@@ -224,11 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             }
             ok = warp_all(wait_bar(b_dh, par, abort));
             tc_fence_after();
-            float t[64];
-            tc_ld64(tmem + lane_base + kColDh, t);
             const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
 #pragma unroll
-            for (int x = 0; x < 64; ++x) h[x] = fmaf(d, h[x], t[x]);
+            for (int half = 0; half < 2; ++half) {
+                float t[32];
+                tc_ld32(tmem + lane_base + kColDh + 32 * half, t);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) h[32 * half + x] = fmaf(d, h[32 * half + x], t[x]);
+            }
             tc_fence_before();
         }
         if (ok && p.h_final && r < K) {
@@ -237,8 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 if (v0 + x < V) p.h_final[(((int64_t)s * H + hh) * K + r) * V + v0 + x] = h[x];
         }
     } else if (warp == 4 || warp == 5) {
-        // ---------------------- v_new helpers (columns 32..63); lane 0 of warp 4 issues
-        const bool issuer = tid == 128;
+        // ------------------------------------- v_new helpers (columns 32..63)
+        bool ok = true;
+        for (int c = 0; c < nchunks && ok; ++c) {
+            const int st = c & 1;
+            const uint32_t par = c & 1;
+            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort) && wait_bar(b_a, par, abort));
+            tc_fence_after();
+            if (ok) vnew_half(c, tid - 128, 32);
+            fence_async_smem();
+            tc_fence_before();
+            arrive(b_vn);
+        }
+    } else if (tid == 8 * 32) {
+        // ------------------------------------------------------ the MMA issuer
         bool ok = true;
         int c = 0;
         for (; c < nchunks && ok; ++c) {
@@ -246,56 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             const uint32_t par = c & 1;
             const uint32_t stg = sbase + st * Lay::stage;
             const uint32_t dcol = kColD + par * 64;
-            if (issuer) {
-                // h of chunk c written and its operands landed (this accumulator
-                // set's previous user, chunk c-2, was read out before P v_new of
-                // chunk c-1 was issued, below)
-                // (b_h also means the recurrence warps saw chunk c's operands land)
-                ok = wait_bar(b_h, par, abort);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t hb = sbase + Lay::h;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc_mma(tmem + dcol, tc_sdesc(stg + Lay::w + ks * 256, 128, 2048), tc_sdesc(hb + ks * 256, 128, 2048),
-                            kIdescK, ks > 0);
-                    tc_commit(b_a);
-                }
-            }
-            ok = warp_all(ok);
-            if (ok) ok = wait_bar(b_st[st], (c >> 1) & 1, abort);  // u of chunk c
-            if (ok) ok = wait_bar(b_a, par, abort);
-            ok = warp_all(ok);
+            // [Xw; O] = [w; qg] h once h_c is written and chunk c's operands
+            // landed (this accumulator set's previous user, chunk c-2, was read
+            // out before P v_new of chunk c-1 was issued, below)
+            ok = wait_bar(b_st[st], (c >> 1) & 1, abort) && wait_bar(b_h, par, abort);
+            if (!ok) break;
             tc_fence_after();
-            if (ok) vnew_half(c, tid - 128, 32);
-            fence_async_smem();
-            tc_fence_before();
-            arrive(b_vn);
-            if (issuer && ok) {
-                ok = wait_bar(b_vn, par, abort);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
+            const uint32_t hb = sbase + Lay::h;
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc_mma(tmem + kColDh, tc_sdesc(stg + Lay::kg + ks * 256, 128, 1024), tc_sdesc(vb + ks * 256, 128, 1024),
-                            kIdescMN, ks > 0);
-                    tc_commit(b_dh);
-                    // b_o must not run two phases ahead of the output warps: chunk
-                    // c-1's output has to be read out before chunk c's is committed
-                    if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
-                    if (ok) {
+            for (int ks = 0; ks < 8; ++ks)
+                tc_mma(tmem + dcol, tc_sdesc(stg + Lay::w + ks * 256, 128, 2048), tc_sdesc(hb + ks * 256, 128, 2048),
+                       kIdescK, ks > 0);
+            tc_commit(b_a);
+            // dh = kg^T v_new, then [.; O] += [0; P] v_new
+            ok = wait_bar(b_vn, par, abort);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            tc_mma(tmem + dcol, tc_sdesc(stg + Lay::z + ks * 256, 128, 1024),
-                                tc_sdesc(vb + ks * 256, 128, 1024), kIdescK, 1);
-                        tc_commit(b_o);
-                    }
-                }
-            }
-            ok = warp_all(ok);  // the warp leaves together
+            for (int ks = 0; ks < 4; ++ks)
+                tc_mma(tmem + kColDh, tc_sdesc(stg + Lay::kg + ks * 256, 128, 1024), tc_sdesc(vb + ks * 256, 128, 1024),
+                       kIdescMN, ks > 0);
+            tc_commit(b_dh);
+            // b_o must not run two phases ahead of the output warps: chunk
+            // c-1's output has to be read out before chunk c's is committed
+            if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
+            if (!ok) break;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                tc_mma(tmem + dcol, tc_sdesc(stg + Lay::z + ks * 256, 128, 1024), tc_sdesc(vb + ks * 256, 128, 1024),
+                       kIdescK, 1);
+            tc_commit(b_o);
         }
-        if (issuer && !ok) {
+        if (!ok) {
             // drain what was issued: the last MMA groups and outstanding copies
             *abort = 1;
             wait_bar(b_a, (uint32_t)c & 1, nullptr);
@@ -304,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             if (c + 1 < nchunks) wait_bar(b_st[(c + 1) & 1], ((c + 1) >> 1) & 1, nullptr);
             if (c + 2 < nchunks) wait_bar(b_st[c & 1], ((c + 2) >> 1) & 1, nullptr);
         }
-    } else if (warp >= 6) {
+    } else if (warp == 6 || warp == 7) {
         // ------------------------------------------------ output warps (lanes 64-127)
         const int i = tid - 192;  // token row within the chunk
         if (tid == 192) {
