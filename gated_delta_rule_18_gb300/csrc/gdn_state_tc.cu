@@ -162,7 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 : "memory");
     };
     // v_new = u - Xw for token row i, columns c0 .. c0+31 (warps 0,1 / 4,5)
-    auto vnew_half = [&](int c, int i, int c0) {
+    // token row i, columns c0 .. c0+31 of chunk c's u, read ahead of the
+    // product it is combined with
+    auto load_u = [&](int c, int i, int c0, uint4 (&uv)[4]) {
+        const unsigned char *urow = sm + Lay::u + (c % 3) * kImgU + i * (kUS * 2) + c0 * 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) uv[j] = *reinterpret_cast<const uint4 *>(urow + 16 * j);
+    };
+    auto vnew_half = [&](int c, int i, int c0, const uint4 (&uvs)[4]) {
         const uint32_t par = c & 1;
         uint32_t rr[32];
         asm volatile(
@@ -176,10 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
               "=r"(rr[26]), "=r"(rr[27]), "=r"(rr[28]), "=r"(rr[29]), "=r"(rr[30]), "=r"(rr[31])
             : "r"(tmem + lane_base + kColD + par * 64 + c0));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        const unsigned char *urow = sm + Lay::u + (c % 3) * kImgU + i * (kUS * 2) + c0 * 2;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint4 uv = *reinterpret_cast<const uint4 *>(urow + 16 * j);
+            const uint4 uv = uvs[j];
             const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&uv);
             float f[8];
 #pragma unroll
@@ -214,17 +220,19 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             arrive(b_h);
             if (!ok) break;
             if (warp < 2) {  // v_new for token row i = tid, columns 0..31
+                uint4 uv[4];
+                load_u(c, tid, 0, uv);
                 ok = warp_all(wait_bar(b_a, par, abort));
                 tc_fence_after();
-                vnew_half(c, tid, 0);
+                vnew_half(c, tid, 0, uv);
                 fence_async_smem();
                 tc_fence_before();
                 arrive(b_vn);
                 if (!ok) break;
             }
+            const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
             ok = warp_all(wait_bar(b_dh, par, abort));
             tc_fence_after();
-            const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 float t[32];
@@ -245,9 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1;
             const uint32_t par = c & 1;
-            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort) && wait_bar(b_a, par, abort));
+            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));
+            uint4 uv[4];
+            if (ok) load_u(c, tid - 128, 32, uv);
+            ok = ok && warp_all(wait_bar(b_a, par, abort));
             tc_fence_after();
-            if (ok) vnew_half(c, tid - 128, 32);
+            if (ok) vnew_half(c, tid - 128, 32, uv);
             fence_async_smem();
             tc_fence_before();
             arrive(b_vn);
