@@ -211,13 +211,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1;
             const uint32_t par = c & 1;
-            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
-            // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16
+            // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16; its last
+            // reader, chunk c-1's first product, finished before that chunk's dh
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = pack8(&h[8 * j]);
             fence_async_smem();
             arrive(b_h);
+            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
             if (!ok) break;
             if (warp < 2) {  // v_new for token row i = tid, columns 0..31
                 uint4 uv[4];
