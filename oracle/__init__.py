@@ -142,6 +142,21 @@ def rmsnorm_channels(x, eps=1e-5, relu=False, scale=1.0):
     return y, inv
 
 
+def merge(num, den_, gate=None, eps=1e-6):
+    """The bidirectional merge (SANA `fused_gdn.py` page, `fused_bigdn_func`
+    and `_fused_bidi_merge_kernel` with its optional gate):
+    out = num / (den + eps) * silu(gate), silu(x) = x / (1 + e^{-x}).
+    num, gate: (B, T, H, V); den: (B, H, T). Returns float64 (B, T, H, V)."""
+    num = _f64(num)
+    d = np.asarray(den_, dtype=np.float64).transpose(0, 2, 1)[..., None]
+    out = num / (d + eps)
+    if gate is not None:
+        x = _f64(gate)
+        with np.errstate(over="ignore"):
+            out = out * (x / (1.0 + np.exp(-x)))
+    return out
+
+
 def forward(w, threads=None):
     """The whole forward of a `workloads.Workload`: prep, then the causal
     scan, or (bidirectional) the causal plus the reverse scan summed, with
@@ -161,13 +176,20 @@ def forward(w, threads=None):
                        cu_seqlens=w.cu_seqlens, threads=threads)
         res["out"], res["h_final"] = out, hf
         return res
+    # the backward direction takes its own gates / beta when given (the
+    # chunk-causal form of the SANA `fused_gdn.py` page: decay_bwd, beta_bwd)
+    gb = w.g if getattr(w, "g_bwd", None) is None else w.g_bwd
+    bb = w.beta if getattr(w, "beta_bwd", None) is None else w.beta_bwd
     of, _ = scan(qn, kn, vv, w.beta, g=w.g, gk=w.gk, cu_seqlens=w.cu_seqlens,
                  threads=threads)
-    orv, _ = scan(qn, kn, vv, w.beta, g=w.g, gk=w.gk, cu_seqlens=w.cu_seqlens,
+    orv, _ = scan(qn, kn, vv, bb, g=gb, gk=w.gk, cu_seqlens=w.cu_seqlens,
                   reverse=True, threads=threads)
     res["out"] = of + orv
     res["den"] = (den(qn, kn, w.beta, g=w.g, gk=w.gk, cu_seqlens=w.cu_seqlens,
                       threads=threads)
-                  + den(qn, kn, w.beta, g=w.g, gk=w.gk,
+                  + den(qn, kn, bb, g=gb, gk=w.gk,
                         cu_seqlens=w.cu_seqlens, reverse=True, threads=threads))
+    if getattr(w, "merge", False):
+        gate = None if w.gate is None else w.gate.values
+        res["merged"] = merge(res["out"], res["den"], gate=gate, eps=w.eps)
     return res

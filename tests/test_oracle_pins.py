@@ -347,3 +347,50 @@ def test_rmsnorm_channels_invariants():
     x2[:, :, 1] *= 3.0
     y2, _ = oracle.rmsnorm_channels(x2, eps=0.0)
     assert not np.allclose(y2[:, :, 0], y[:, :, 0])
+
+
+def test_merge_closed_form():
+    # out = num / (den + eps) * silu(gate) (SANA `fused_gdn.py` page,
+    # `fused_bigdn_func` and `_fused_bidi_merge_kernel`): worked values
+    num = np.array([3.0, -3.0, 6.0, 0.0]).reshape(1, 1, 1, 4)
+    den = np.array([1.0]).reshape(1, 1, 1)
+    np.testing.assert_allclose(oracle.merge(num, den, eps=0.5), [[[[2.0, -2.0, 4.0, 0.0]]]],
+                               rtol=0, atol=1e-15)
+    # silu(ln 3) = ln 3 / (1 + 1/3) = 0.75 ln 3; silu(0) = 0; silu(-ln 3) = -0.25 ln 3
+    gate = np.array([np.log(3.0), np.log(3.0), 0.0, -np.log(3.0)]).reshape(1, 1, 1, 4)
+    want = np.array([2.0 * 0.75, -2.0 * 0.75, 0.0, 0.0]) * np.log(3.0)
+    np.testing.assert_allclose(oracle.merge(num, den, gate=gate, eps=0.5)[0, 0, 0], want,
+                               rtol=1e-15, atol=1e-15)
+    # den is indexed (B, H, T): a transposed den must move to the right rows
+    num2 = np.ones((1, 2, 3, 4))
+    den2 = np.arange(6, dtype=np.float64).reshape(1, 3, 2)  # (B, H, T)
+    got = oracle.merge(num2, den2, eps=1.0)
+    for t in range(2):
+        for h in range(3):
+            np.testing.assert_allclose(got[0, t, h], 1.0 / (den2[0, h, t] + 1.0), rtol=1e-15)
+
+
+@pytest.mark.parametrize("b", [1, 5, 10])
+def test_reverse_reset_splits_the_sequence(b):
+    # Chunk-causal backward direction (SANA `fused_gdn.py` page: decay_bwd
+    # zeroed at boundary frames): with the log-gate of token b at -inf, the
+    # reverse scan of the whole sequence equals, for positions p < b, the
+    # reverse scan of tokens 0..b alone and, for p >= b, that of tokens b..T-1
+    # alone (position p reads tokens p+1.. ; token b's decay wipes what came
+    # after it before its own update lands).
+    rng = np.random.default_rng(7)
+    T, K, V = 12, 4, 3
+    q, k = rng.normal(size=(T, K)), rng.normal(size=(T, K))
+    v, beta = rng.normal(size=(T, V)), rng.uniform(0.1, 0.9, size=T)
+    g = np.log(rng.uniform(0.5, 0.99, size=T))
+    g_reset = g.copy()
+    g_reset[b] = -np.inf
+    full, _ = oracle.scan(*map(_one, (q, k, v, beta, g_reset)), reverse=True)
+    pre, _ = oracle.scan(*map(_one, (q[:b + 1], k[:b + 1], v[:b + 1], beta[:b + 1], g[:b + 1])),
+                         reverse=True)
+    suf, _ = oracle.scan(*map(_one, (q[b:], k[b:], v[b:], beta[b:], g[b:])), reverse=True)
+    np.testing.assert_allclose(full[0, :b, 0], pre[0, :b, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(full[0, b:, 0], suf[0, :, 0], rtol=1e-12, atol=1e-12)
+    # without the reset the early positions see the later tokens
+    plain, _ = oracle.scan(*map(_one, (q, k, v, beta, g)), reverse=True)
+    assert np.abs(plain[0, :b, 0] - pre[0, :b, 0]).max() > 1e-3

@@ -31,7 +31,7 @@ import numpy as np
 BLOCK = 1 << 22  # elements per independently seeded block
 
 _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "g": 5, "gk": 6, "h0": 7,
-               "lens": 8, "qkv": 9}
+               "lens": 8, "qkv": 9, "gate": 10}
 
 
 def _normal_fill(seed: int, name: str, n: int, mu: float, sigma: float,
@@ -178,6 +178,14 @@ class Workload:
     prep: str = "l2"          # "l2" | "rms_relu"
     bidirectional: bool = False
     chunk: int = 64
+    # chunk-causal bidirectional form: gates / beta of the backward direction
+    # (None: the forward ones), and the merge out = num / (den + eps) *
+    # silu(gate) with `gate` (B, T, H, V)
+    g_bwd: np.ndarray | None = None
+    beta_bwd: np.ndarray | None = None
+    merge: bool = False
+    gate: Stored | None = None
+    eps: float = 1e-6
 
     @property
     def n_seq(self) -> int:
@@ -222,17 +230,30 @@ def make(B: int, T: int, H: int, K: int, V: int, dtype: str = "bf16", *,
 
 
 def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
-               g_mu: float = 4.0, name: str = "video") -> Workload:
+               g_mu: float = 4.0, name: str = "video", reset_every: int | None = None,
+               merge: bool = False) -> Workload:
     """Interleaved qkv (B, N, 3, H, D) ~ N(0,1) bf16, bidirectional, with the
-    full-channel RMSNorm + ReLU + k-scale prep."""
+    full-channel RMSNorm + ReLU + k-scale prep.
+
+    reset_every = R makes it chunk-causal: the backward direction's log-gate
+    is -inf and its beta 0 at tokens R, 2R, ..., so that a token's backward
+    state holds only the later tokens of its own R-token chunk. merge adds
+    out = num / (den + eps) * silu(gate), gate (B, N, H, D) ~ N(0,1) bf16."""
     qkv = stored_normal(seed, "qkv", (B, N, 3, H, D), "bf16")
     beta = sigmoid_normal(seed, "beta", (B, N, H), 0.0)
     g = log_sigmoid_normal(seed, "g", (B, N, H), g_mu)
+    g_bwd = beta_bwd = None
+    if reset_every:
+        g_bwd, beta_bwd = g.copy(), beta.copy()
+        g_bwd[:, reset_every::reset_every, :] = -np.inf
+        beta_bwd[:, reset_every::reset_every, :] = 0.0
+    gate = stored_normal(seed, "gate", (B, N, H, D), "bf16") if merge else None
 
     def part(i):
         return qkv.take((slice(None), slice(None), i))
     return Workload(name, B, N, H, D, D, "bf16", part(0), part(1), part(2),
-                    beta, g, qkv=qkv, prep="rms_relu", bidirectional=True)
+                    beta, g, qkv=qkv, prep="rms_relu", bidirectional=True,
+                    g_bwd=g_bwd, beta_bwd=beta_bwd, merge=merge, gate=gate)
 
 
 # The five workloads, named by what they are.
@@ -242,6 +263,8 @@ WORKLOADS = {
     "causal_bf16_b4h16t4096d128": dict(kind="dense", B=4, T=4096, H=16, K=128,
                                        V=128, dtype="bf16", g_mu=3.0),
     "bidir_video_b2h16n8192d112": dict(kind="video", B=2, N=8192, H=16, D=112),
+    "chunkcausal_merge_video_b2h16n8192d112": dict(kind="video", B=2, N=8192, H=16,
+                                                   D=112, reset_every=1024, merge=True),
     "varlen_bf16_64seq_h32d128": dict(kind="varlen", n_seq=64, lo=128, hi=8192,
                                       H=32, K=128, V=128, h0_std=0.02),
     "gk_bf16_b1h32t65536k128v256": dict(kind="dense", B=1, T=65536, H=32,
@@ -273,7 +296,8 @@ def build(name: str, seed: int = 0, T: int | None = None) -> Workload:
                     gk_mu=spec.get("gk_mu"), name=name)
     if kind == "video":
         return make_video(spec["B"], spec["N"], spec["H"], spec["D"], seed=seed,
-                          name=name)
+                          name=name, reset_every=spec.get("reset_every"),
+                          merge=spec.get("merge", False))
     if kind == "varlen":
         lens = varlen_lengths(seed, spec["n_seq"], spec["lo"], spec["hi"])
         return make(1, sum(lens), spec["H"], spec["K"], spec["V"], "bf16",
