@@ -55,6 +55,11 @@ def path_work(w):
     if w.bidirectional:
         fl = th * (flops_per_token_head(w.K, w.V) + flops_per_token_head(w.K, w.V + 1))
         by = th * (3 * w.K * e + 4 + 4 + w.V * e + 4)       # qkv, beta, g, num, den
+        if w.g_bwd is not None or w.beta_bwd is not None:
+            by += th * 8                                     # backward gates and beta
+        if w.merge:
+            fl += th * w.V * (6 if w.gate is not None else 2)
+            by += th * w.V * e * (2 if w.gate is not None else 1)  # gate in, merged out
     else:
         fl = th * flops_per_token_head(w.K, w.V)
         by = th * ((2 * w.K + w.V) * e + 4 + (4 * w.K if w.gk is not None else 4) + w.V * e)
@@ -85,6 +90,8 @@ def kernel_bytes(w, name):
         return w.B * w.T * w.H * w.K * e * 2 + w.B * w.T * 4
     if name == "prep_l2":
         return th * w.K * e * 2
+    if name == "merge":
+        return th * w.V * e * (3 if w.gate is not None else 2) + th * 4
     return None
 
 
@@ -225,16 +232,22 @@ def device_inputs(w, dev):
     else:
         d["q"], d["k"], d["v"] = to_dev(w.q), to_dev(w.k), to_dev(w.v)
     d["beta"], d["g"], d["gk"], d["h0"] = f32(w.beta), f32(w.g), f32(w.gk), f32(w.h0)
+    d["g_bwd"], d["beta_bwd"] = f32(w.g_bwd), f32(w.beta_bwd)
+    d["gate"] = None if w.gate is None else to_dev(w.gate)
     d["cu_seqlens"] = None if w.cu_seqlens is None else torch.from_numpy(
         w.cu_seqlens.astype(np.int32)).to(dev)
     return d
 
 
 def run_step(gdn, w, d, ws):
+    extra = {}
+    if w.bidirectional:
+        bw = {k2: d[k2 + "_bwd"] for k2 in ("g", "beta") if d.get(k2 + "_bwd") is not None}
+        extra = dict(backward=bw or None, merge=w.merge, gate=d.get("gate"), eps=w.eps)
     return gdn.gdn_forward(d["q"], d["k"], d["v"], d["beta"], g=d["g"], gk=d["gk"],
                            h0=d["h0"], cu_seqlens=d["cu_seqlens"], prep=w.prep,
                            bidirectional=w.bidirectional,
-                           with_final_state=not w.bidirectional, workspace=ws)
+                           with_final_state=not w.bidirectional, workspace=ws, **extra)
 
 
 def workspace_for(gdn, w, dev):
@@ -250,7 +263,8 @@ def e2e_measure(gdn, w, d, ws, steps, dev):
     each step copies the inputs host->device, runs, and copies the output back."""
     import torch
     host = {}
-    for key in ("qkv", "q", "k", "v", "beta", "g", "gk", "h0", "cu_seqlens"):
+    for key in ("qkv", "q", "k", "v", "beta", "g", "gk", "h0", "cu_seqlens", "g_bwd",
+                "beta_bwd", "gate"):
         t = d.get(key)
         if t is None or (key in ("q", "k", "v") and "qkv" in d):
             continue
@@ -275,7 +289,7 @@ def e2e_measure(gdn, w, d, ws, steps, dev):
             qkv = dev_bufs["qkv"]
             dd["q"], dd["k"], dd["v"] = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
         res = run_step(gdn, w, dd, ws)
-        out_host.copy_(res["out"], non_blocking=True)
+        out_host.copy_(res["merged" if w.merge else "out"], non_blocking=True)
 
     for _ in range(2):
         one()
@@ -311,8 +325,12 @@ def oracle_sample(w):
         # full-channel RMS prep needs every head of a token: whole batch rows
         ix = (slice(0, 1),)
         sw = dataclasses.replace(w, B=1, qkv=w.qkv.take(ix), q=w.q.take(ix), k=w.k.take(ix),
-                                 v=w.v.take(ix), beta=w.beta[ix], g=w.g[ix])
-        desc = f"batch row 0 of {w.B}: {w.T} tokens x {w.H} heads, both directions + den"
+                                 v=w.v.take(ix), beta=w.beta[ix], g=w.g[ix],
+                                 g_bwd=None if w.g_bwd is None else w.g_bwd[ix],
+                                 beta_bwd=None if w.beta_bwd is None else w.beta_bwd[ix],
+                                 gate=None if w.gate is None else w.gate.take(ix))
+        desc = (f"batch row 0 of {w.B}: {w.T} tokens x {w.H} heads, both directions + den"
+                + (" + merge" if w.merge else ""))
         units = w.H
     elif w.cu_seqlens is not None:
         cu = w.cu_seqlens

@@ -6,8 +6,9 @@ the library's CUDA kernels. There is no CPU fallback: if the library is not
 built, or no GPU is present, calls fail loudly.
 
 Entry points mirror the C ABI:
-  gdn_prep, gdn_chunk_fwd, gdn_workspace_size, gdn_status_string,
-  gdn_last_device_error, and gdn_forward (prep + one or both scan directions).
+  gdn_prep, gdn_chunk_fwd, gdn_merge, gdn_workspace_size, gdn_status_string,
+  gdn_last_device_error, and gdn_forward (prep + one or both scan directions,
+  optionally merged).
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ import os
 from .build import LIB
 
 __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
-           "gdn_workspace_size",
+           "gdn_merge", "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_forward", "lib",
            "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect",
            "launch_count", "kernel_names"]
@@ -69,6 +70,8 @@ def lib():
     L.gdn_chunk_fwd_noalloc.restype = I
     L.gdn_chunk_fwd_noalloc.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P,
                                         TensorDesc, P, P, I, I, I, I, I, I, I, I, P]
+    L.gdn_merge.restype = I
+    L.gdn_merge.argtypes = [P, TensorDesc, P, P, TensorDesc, P, TensorDesc, I, I, I, I, F, P]
     L.gdn_last_device_error.restype = I
     L.gdn_last_device_error.argtypes = [P, P, ctypes.POINTER(I)]
     L.gdn_kernel_kinds.restype = I
@@ -210,6 +213,23 @@ def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqle
     return out
 
 
+def gdn_merge(num, den, gate=None, eps=1e-6, out=None, out_dtype=None, stream=None):
+    """out = num / (den + eps) * (silu(gate) if gate is given), see
+    include/gdn.h. num, gate: (B, T, H, V); den: (B, H, T) fp32. Returns out
+    (allocated when not given: num's dtype, or `out_dtype`)."""
+    torch = _torch()
+    B, T, H, V = num.shape
+    _f32(den, "den")
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=out_dtype or num.dtype, device=num.device)
+    gd = _desc(gate) if gate is not None else TensorDesc(_dtype_code(num), 0, 0, 0, 0)
+    st = lib().gdn_merge(_ptr(num), _desc(num), _ptr(den), _ptr(gate), gd, _ptr(out), _desc(out),
+                         B, T, H, V, float(eps), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_merge")
+    return out
+
+
 def gdn_last_device_error(workspace, stream=None) -> int:
     """Synchronise, read and clear the device error word; returns it."""
     w = ctypes.c_int(0)
@@ -221,19 +241,31 @@ def gdn_last_device_error(workspace, stream=None) -> int:
 
 def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                 prep="l2", bidirectional=False, with_final_state=False, workspace=None,
-                stream=None):
+                stream=None, backward=None, merge=False, gate=None, eps=1e-6):
     """The whole forward: q/k prep, then the causal scan, or the causal plus
     the reverse scan summed with the denominator (bidirectional).
 
     prep: "l2" (per-(token, head) L2 norm fused into the scan), "rms_relu"
     (full-channel RMSNorm, ReLU, and k scaled by K^-0.5, via gdn_prep), or
-    None (q, k used as given). Returns a dict with "out" and, as requested,
-    "h_final" / "den" / "q_inv_rms" / "k_inv_rms"."""
+    None (q, k used as given).
+    backward: optional dict of inputs the reverse direction uses instead of
+    the forward ones ("q", "k", "v", "beta", "g", "gk"), e.g. the
+    chunk-causal form's gates with -inf at chunk boundaries (the SANA
+    `fused_gdn.py` page's decay_bwd / beta_bwd / qkv_bwd).
+    merge: also return "merged" = out / (den + eps) * silu(gate) (gdn_merge).
+    Returns a dict with "out" and, as requested, "h_final" / "den" /
+    "merged" / "q_inv_rms" / "k_inv_rms"."""
     torch = _torch()
     B, T, H, K = q.shape
     n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
     res = {}
     fuse = prep == "l2"
+    bw = dict(backward or {})
+    unknown = set(bw) - {"q", "k", "v", "beta", "g", "gk"}
+    if unknown:
+        raise ValueError(f"unknown backward inputs {sorted(unknown)}")
+    if (backward or merge) and not bidirectional:
+        raise ValueError("backward inputs and merge need bidirectional=True")
     if prep == "rms_relu":
         res["q_inv_rms"] = torch.empty((B, T), dtype=torch.float32, device=q.device)
         res["k_inv_rms"] = torch.empty((B, T), dtype=torch.float32, device=q.device)
@@ -241,6 +273,10 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                      inv_rms=res["q_inv_rms"], stream=stream)
         k = gdn_prep(k, mode=PREP_RMS | PREP_RELU, scale=K ** -0.5, eps=1e-5,
                      inv_rms=res["k_inv_rms"], stream=stream)
+        for name, scale in (("q", 1.0), ("k", K ** -0.5)):
+            if name in bw:
+                bw[name] = gdn_prep(bw[name], mode=PREP_RMS | PREP_RELU, scale=scale, eps=1e-5,
+                                    stream=stream)
     elif prep not in ("l2", None):
         raise ValueError(f"unknown prep {prep!r}")
     if not bidirectional:
@@ -255,10 +291,13 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
     den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
     out = gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, cu_seqlens=cu_seqlens, den=den,
                         qk_l2norm=fuse, workspace=workspace, stream=stream)
-    gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, cu_seqlens=cu_seqlens, den=den, out=out,
+    gdn_chunk_fwd(bw.get("q", q), bw.get("k", k), bw.get("v", v), bw.get("beta", beta),
+                  g=bw.get("g", g), gk=bw.get("gk", gk), cu_seqlens=cu_seqlens, den=den, out=out,
                   reverse=True, accumulate=True, qk_l2norm=fuse, workspace=workspace,
                   stream=stream)
     res["out"], res["den"] = out, den
+    if merge:
+        res["merged"] = gdn_merge(out, den, gate=gate, eps=eps, stream=stream)
     return res
 
 

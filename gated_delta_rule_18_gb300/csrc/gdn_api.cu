@@ -14,9 +14,9 @@ using gdn::FwdParams;
 
 // ------------------------------------------------------------ profiling ----
 
-enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KNumKinds };
-const char *kKindNames[KNumKinds] = {"prep_l2", "prep_rms", "chunk_table",
-                                     "intra_bf16", "state_tc", "fused_f32"};
+enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KNumKinds };
+const char *kKindNames[KNumKinds] = {"prep_l2", "prep_rms", "chunk_table", "intra_bf16",
+                                     "state_tc", "fused_f32", "merge"};
 
 struct Profiler {
     std::mutex mu;
@@ -284,6 +284,36 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     }
     e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
     return cuda_status(e);
+}
+
+gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den, const void *gate,
+                     gdn_tensor_desc gd, void *out, gdn_tensor_desc od, int B, int T, int H, int V,
+                     float eps, cudaStream_t stream) {
+    if (B < 1 || T < 0 || H < 1 || V < 1) return GDN_ERR_SHAPE;
+    if (T > 0 && (!num || !den || !out)) return GDN_ERR_NULL;
+    if (!dtype_ok(nd.dtype) || !dtype_ok(od.dtype)) return GDN_ERR_DTYPE;
+    if (nd.dtype == GDN_BF16 && od.dtype != GDN_BF16) return GDN_ERR_DTYPE;
+    if (gate && gd.dtype != nd.dtype) return GDN_ERR_DTYPE;
+    if (V % (16 / elem_size(nd.dtype)) != 0) return GDN_ERR_SHAPE;
+    if (!aligned16(num) || !aligned16(out) || !aligned16(gate) || !strides_ok(nd) || !strides_ok(od) ||
+        (gate && !strides_ok(gd)))
+        return GDN_ERR_LAYOUT;
+    if (den && (reinterpret_cast<uintptr_t>(den) & 3)) return GDN_ERR_LAYOUT;
+    if (!(eps >= 0.f)) return GDN_ERR_SHAPE;
+    if (T == 0) return GDN_OK;
+    gdn::MergeParams m{};
+    m.num = num;
+    m.n_sb = nd.stride_b, m.n_st = nd.stride_t, m.n_sh = nd.stride_h;
+    m.den = den;
+    m.gate = gate;
+    m.g_sb = gd.stride_b, m.g_st = gd.stride_t, m.g_sh = gd.stride_h;
+    m.out = out;
+    m.o_sb = od.stride_b, m.o_st = od.stride_t, m.o_sh = od.stride_h;
+    m.B = B, m.T = T, m.H = H, m.V = V;
+    m.eps = eps;
+    m.num_bf16 = nd.dtype == GDN_BF16;
+    m.out_bf16 = od.dtype == GDN_BF16;
+    return cuda_status(launch(KMerge, stream, [&] { return gdn::launch_merge(m, stream); }));
 }
 
 gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream, int *word) {

@@ -247,6 +247,20 @@ __device__ __forceinline__ float warp_sum(float x) {
 // Host-side launchers, defined in the .cu files and called by gdn_api.cu.
 namespace gdn {
 cudaError_t launch_chunk_table(const FwdParams &p, cudaStream_t st);
+// The bidirectional merge: out = num / (den + eps) * (gate ? silu(gate) : 1).
+struct MergeParams {
+    const void *num;  // (B, T, H, V), fp32 or bf16
+    int64_t n_sb, n_st, n_sh;
+    const float *den;  // (B, H, T) contiguous
+    const void *gate;  // like num, or null
+    int64_t g_sb, g_st, g_sh;
+    void *out;  // (B, T, H, V)
+    int64_t o_sb, o_st, o_sh;
+    int B, T, H, V;
+    float eps;
+    int num_bf16, out_bf16;
+};
+cudaError_t launch_merge(const MergeParams &m, cudaStream_t st);
 cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
 cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);

@@ -190,6 +190,29 @@ gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k,
                                  int flags, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
+/*
+ * gdn_merge -- the bidirectional merge (SANA `fused_gdn.py` page,
+ * `fused_bigdn_func`: out = (num_fwd + num_bwd) / (den_fwd + den_bwd + eps),
+ * and `_fused_bidi_merge_kernel` with APPLY_GATE: times silu(gate) =
+ * gate / (1 + e^{-gate})). The scan has already summed both directions
+ * (gdn_chunk_fwd with GDN_ACCUMULATE on the reverse call), so
+ *   out = num / (den + eps) * (gate ? silu(gate) : 1)
+ * elementwise, in fp32.
+ *   num, gate, out: (B, T, H, V) with descriptors nd, gd, od. num is fp32 or
+ *       bf16; gate (or NULL) has num's dtype; out is bf16, or fp32 when num
+ *       is fp32 (GDN_ERR_DTYPE otherwise). out may alias num when the
+ *       descriptors are equal.
+ *   den: (B, H, T) fp32, contiguous.
+ *   V a multiple of 8 (bf16 num) or 4 (fp32 num); eps >= 0.
+ * The chunk-causal variant of the page (state zeroed at chunk boundaries in
+ * the backward direction only) needs nothing here: the reverse gdn_chunk_fwd
+ * call takes its own gates, with a log-gate of -inf at each boundary token.
+ */
+gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den,
+                     const void *gate, gdn_tensor_desc gd, void *out,
+                     gdn_tensor_desc od, int B, int T, int H, int V, float eps,
+                     cudaStream_t stream);
+
 const char *gdn_status_string(gdn_status s);
 
 /*

@@ -55,9 +55,18 @@ def run_gpu(w, with_final_state=True):
         q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
     else:
         q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    bw = {}
+    if w.g_bwd is not None:
+        bw["g"] = f32_dev(w.g_bwd)
+    if w.beta_bwd is not None:
+        bw["beta"] = f32_dev(w.beta_bwd)
+    extra = {}
+    if w.bidirectional and (bw or w.merge):
+        extra = dict(backward=bw or None, merge=w.merge, eps=w.eps,
+                     gate=None if w.gate is None else to_dev(w.gate))
     res = gdn.gdn_forward(q, k, v, f32_dev(w.beta), g=f32_dev(w.g), gk=f32_dev(w.gk),
                           h0=f32_dev(w.h0), cu_seqlens=i32_dev(w.cu_seqlens), prep=w.prep,
                           bidirectional=w.bidirectional,
-                          with_final_state=with_final_state and not w.bidirectional)
+                          with_final_state=with_final_state and not w.bidirectional, **extra)
     t.cuda.synchronize()
     return {k2: v2.double().cpu().numpy() for k2, v2 in res.items()}

@@ -129,6 +129,20 @@ def test_prep_rejects_on_host(L):
     assert L.gdn_prep(P(0), d, P(1), d, 1, 0, 2, 64, 0, 1.0, 1e-6, None, None) == OK
 
 
+def test_merge_rejects_on_host(L):
+    d16, d32 = desc(gdn.BF16, 1, 16, 2, 64), desc(gdn.F32, 1, 16, 2, 64)
+    m = lambda num=P(0), nd=d16, den=P(4), gate=None, gd=d16, out=P(1), od=d16, V=64, eps=1e-6, T=16: \
+        L.gdn_merge(num, nd, den, gate, gd, out, od, 1, T, 2, V, eps, None)
+    assert m(num=None) == NULL
+    assert m(od=d32) == DTYPE                       # bf16 num, fp32 out: not offered
+    assert m(gate=P(2), gd=d32) == DTYPE            # gate dtype differs from num
+    assert m(V=60) == SHAPE                         # V not a multiple of 8 (bf16)
+    assert m(eps=-1.0) == SHAPE
+    assert m(num=ctypes.c_void_p(A + 8)) == LAYOUT  # misaligned rows
+    assert m(den=ctypes.c_void_p(A + 2)) == LAYOUT
+    assert m(T=0) == OK                             # nothing to do, nothing launched
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(gdn, "_lib", None)
     monkeypatch.setattr(gdn, "LIB", "/nonexistent/libgdn.so")

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_helpers import TOL, f32_dev, i32_dev, rel_err, run_gpu, to_dev
+from gpu_helpers import TOL, dev, f32_dev, i32_dev, rel_err, run_gpu, to_dev, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -76,6 +76,36 @@ def test_small_bidirectional_l2(dtype):
 def test_small_video_rms_bidirectional():
     w = workloads.make_video(1, 300, 4, 112, seed=3, name="video_small")
     _compare(w, ["out", "den"])
+
+
+@pytest.mark.parametrize("reset", [64, 100])
+def test_small_chunkcausal_merge(reset):
+    # chunk-causal bidirectional (backward gates -inf / beta 0 every `reset`
+    # tokens, chunk-aligned or not) and the merge num / (den + eps) * silu(gate)
+    w = workloads.make_video(1, 450, 4, 112, seed=5, name="chunkcausal_small",
+                             reset_every=reset, merge=True)
+    _compare(w, ["out", "den", "merged"])
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
+@pytest.mark.parametrize("with_gate", [False, True])
+def test_merge_kernel(dtype, out_dtype, with_gate):
+    import gated_delta_rule_18_gb300 as gdn
+    t = torch()
+    tdt = {"bf16": t.bfloat16, "f32": t.float32}
+    rng = np.random.default_rng(11)
+    B, T, H, V = 2, 37, 3, 24
+    # num as a strided view (every other head of a wider tensor)
+    wide = t.from_numpy(rng.standard_normal((B, T, 2 * H, V))).to(dev()).to(tdt[dtype])
+    num = wide[:, :, ::2]
+    den = t.from_numpy(rng.uniform(0.05, 3.0, (B, H, T))).float().to(dev())
+    gate = t.from_numpy(rng.standard_normal((B, T, H, V)) * 3).to(dev()).to(tdt[dtype]) if with_gate else None
+    out = gdn.gdn_merge(num, den, gate=gate, eps=1e-3, out_dtype=tdt[out_dtype])
+    t.cuda.synchronize()
+    ref = oracle.merge(num.double().cpu().numpy(), den.double().cpu().numpy(),
+                       gate=None if gate is None else gate.double().cpu().numpy(), eps=1e-3)
+    tol = 8e-3 if out_dtype == "bf16" else 1e-6
+    assert rel_err(out.double().cpu().numpy(), ref) <= tol
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -210,6 +240,25 @@ def test_full_size_varlen():
     e_o = rel_err(got["out"][:, rows][:, :, heads], ref["out"])
     e_h = rel_err(got["h_final"][seqs][:, heads], ref["h_final"])
     assert e_o <= 2e-2 and e_h <= 2e-2, (e_o, e_h)
+
+
+def test_full_size_chunkcausal_merge():
+    w = workloads.build("chunkcausal_merge_video_b2h16n8192d112")
+    got = run_gpu(w)
+    b, heads = 0, [3, 14]
+    qkv = w.qkv.take((slice(b, b + 1),)).values.astype(np.float64)
+    qn, _ = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
+    kn, _ = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    qn, kn, vv = qn[:, :, heads], kn[:, :, heads], qkv[:, :, 2][:, :, heads]
+    sel = lambda a: a[b:b + 1][:, :, heads]
+    beta, g, bb, gb = sel(w.beta), sel(w.g), sel(w.beta_bwd), sel(w.g_bwd)
+    of, _ = oracle.scan(qn, kn, vv, beta, g=g)
+    orv, _ = oracle.scan(qn, kn, vv, bb, g=gb, reverse=True)
+    den = oracle.den(qn, kn, beta, g=g) + oracle.den(qn, kn, bb, g=gb, reverse=True)
+    merged = oracle.merge(of + orv, den, gate=w.gate.values[b:b + 1][:, :, heads], eps=w.eps)
+    assert rel_err(got["out"][b:b + 1][:, :, heads], of + orv) <= 2e-2
+    assert rel_err(got["den"][b:b + 1][:, heads], den) <= 2e-2
+    assert rel_err(got["merged"][b:b + 1][:, :, heads], merged) <= 2e-2
 
 
 def test_full_size_video_bidirectional():
