@@ -294,7 +294,8 @@ gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den, cons
     if (!dtype_ok(nd.dtype) || !dtype_ok(od.dtype)) return GDN_ERR_DTYPE;
     if (nd.dtype == GDN_BF16 && od.dtype != GDN_BF16) return GDN_ERR_DTYPE;
     if (gate && gd.dtype != nd.dtype) return GDN_ERR_DTYPE;
-    if (V % (16 / elem_size(nd.dtype)) != 0) return GDN_ERR_SHAPE;
+    if (V % (16 / elem_size(nd.dtype)) != 0 || V > 1024) return GDN_ERR_SHAPE;
+    if ((int64_t)B * T * H > INT32_MAX) return GDN_ERR_SHAPE;
     if (!aligned16(num) || !aligned16(out) || !aligned16(gate) || !strides_ok(nd) || !strides_ok(od) ||
         (gate && !strides_ok(gd)))
         return GDN_ERR_LAYOUT;

@@ -4,8 +4,8 @@
 // factor silu(gate) = gate / (1 + e^{-gate})). The scan has already summed
 // both directions into num (B, T, H, V) and den (B, H, T).
 //
-// HBM-bound elementwise pass: one 16-byte vector of a (token, head) row per
-// thread and step of a grid-stride loop, fp32 arithmetic.
+// HBM-bound elementwise pass: each block takes whole (token, head) rows, one
+// 16-byte vector per thread, fp32 arithmetic.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -55,54 +55,49 @@ __device__ __forceinline__ void store_vec(T *p, const float *f) {
 }
 
 template <typename TI, typename TO>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams m) {
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams m, int vpr, int rows_per_block) {
     constexpr int N = Vec<TI>::N;
-    const int vpr = m.V / N;  // vectors per (token, head) row
-    const int64_t total = (int64_t)m.B * m.T * m.H * vpr;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total; e += (int64_t)gridDim.x * blockDim.x) {
-        const int c = (int)(e % vpr) * N;
-        int64_t row = e / vpr;
-        const int h = (int)(row % m.H);
-        row /= m.H;
-        const int t = (int)(row % m.T);
-        const int b = (int)(row / m.T);
-        const float inv = 1.f / (m.den[((int64_t)b * m.H + h) * m.T + t] + m.eps);
-        float x[8];
-        load_vec<TI>((const TI *)m.num + b * m.n_sb + (int64_t)t * m.n_st + h * m.n_sh + c, x);
+    // a block covers rows_per_block whole (token, head) rows of vpr vectors
+    const int lr = threadIdx.x / vpr, c = (threadIdx.x - lr * vpr) * N;
+    const int row = blockIdx.x * rows_per_block + lr;
+    if (lr >= rows_per_block || row >= m.B * m.T * m.H) return;
+    const int h = row % m.H, bt = row / m.H;
+    const int t = bt % m.T, b = bt / m.T;
+    const float inv = 1.f / (__ldg(m.den + ((int64_t)b * m.H + h) * m.T + t) + m.eps);
+    float x[8];
+    load_vec<TI>((const TI *)m.num + b * m.n_sb + (int64_t)t * m.n_st + h * m.n_sh + c, x);
 #pragma unroll
-        for (int i = 0; i < N; ++i) x[i] *= inv;
-        if (m.gate) {
-            float gt[8];
-            load_vec<TI>((const TI *)m.gate + b * m.g_sb + (int64_t)t * m.g_st + h * m.g_sh + c, gt);
+    for (int i = 0; i < N; ++i) x[i] *= inv;
+    if (m.gate) {
+        float gt[8];
+        load_vec<TI>((const TI *)m.gate + b * m.g_sb + (int64_t)t * m.g_st + h * m.g_sh + c, gt);
 #pragma unroll
-            for (int i = 0; i < N; ++i) x[i] *= gt[i] / (1.f + __expf(-gt[i]));
-        }
-        if constexpr (sizeof(TO) == sizeof(TI)) {
-            store_vec<TO>((TO *)m.out + b * m.o_sb + (int64_t)t * m.o_st + h * m.o_sh + c, x);
-        } else {  // fp32 in, bf16 out: two 8-byte halves
-            TO *o = (TO *)m.out + b * m.o_sb + (int64_t)t * m.o_st + h * m.o_sh + c;
-            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]));
-        }
+        for (int i = 0; i < N; ++i) x[i] *= gt[i] / (1.f + __expf(-gt[i]));
+    }
+    if constexpr (sizeof(TO) == sizeof(TI)) {
+        store_vec<TO>((TO *)m.out + b * m.o_sb + (int64_t)t * m.o_st + h * m.o_sh + c, x);
+    } else {  // fp32 in, bf16 out: one 8-byte half
+        TO *o = (TO *)m.out + b * m.o_sb + (int64_t)t * m.o_st + h * m.o_sh + c;
+        *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]));
     }
 }
 
 }  // namespace
 
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t st) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
     const int vec = m.num_bf16 ? 8 : 4;
-    const int64_t total = (int64_t)m.B * m.T * m.H * (m.V / vec);
-    const int64_t want = (total + 255) / 256;
-    const int grid = (int)(want < 8LL * sms ? (want > 0 ? want : 1) : 8LL * sms);
+    const int vpr = m.V / vec;  // vectors per row (V <= 1024 keeps it <= 256)
+    const int rows_per_block = vpr <= 256 ? 256 / vpr : 0;
+    if (rows_per_block == 0) return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)m.B * m.T * m.H;
+    if (rows > INT32_MAX) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
     if (m.num_bf16) {
-        if (m.out_bf16) merge_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(m);
+        if (m.out_bf16) merge_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>(m, vpr, rows_per_block);
         else return cudaErrorInvalidValue;  // bf16 in, fp32 out: not offered
     } else {
-        if (m.out_bf16) merge_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(m);
-        else merge_kernel<float, float><<<grid, 256, 0, st>>>(m);
+        if (m.out_bf16) merge_kernel<float, __nv_bfloat16><<<grid, 256, 0, st>>>(m, vpr, rows_per_block);
+        else merge_kernel<float, float><<<grid, 256, 0, st>>>(m, vpr, rows_per_block);
     }
     return cudaGetLastError();
 }

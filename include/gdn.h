@@ -203,7 +203,8 @@ gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k,
  *       is fp32 (GDN_ERR_DTYPE otherwise). out may alias num when the
  *       descriptors are equal.
  *   den: (B, H, T) fp32, contiguous.
- *   V a multiple of 8 (bf16 num) or 4 (fp32 num); eps >= 0.
+ *   V a multiple of 8 (bf16 num) or 4 (fp32 num), at most 1024; B*T*H < 2^31;
+ *   eps >= 0.
  * The chunk-causal variant of the page (state zeroed at chunk boundaries in
  * the backward direction only) needs nothing here: the reverse gdn_chunk_fwd
  * call takes its own gates, with a log-gate of -inf at each boundary token.
