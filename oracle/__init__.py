@@ -53,6 +53,10 @@ def _load():
             lib.oracle_gdn_scan.argtypes = [
                 ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 P, P, P, P, P, P, P, ctypes.c_int, P, P, ctypes.c_int]
+            lib.oracle_gdn_frame_scan.restype = ctypes.c_int
+            lib.oracle_gdn_frame_scan.argtypes = [
+                ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int]
             lib.oracle_l2norm.restype = None
             lib.oracle_l2norm.argtypes = [P, ctypes.c_int64, ctypes.c_int,
                                           ctypes.c_double, P]
@@ -107,6 +111,38 @@ def scan(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
     if rc != 0:
         raise RuntimeError(f"oracle_gdn_scan failed with status {rc}")
     return out, hf
+
+
+def frame_scan(q, k, v, beta, g_frame, frame, h0=None, reverse=False, threads=None):
+    """Frame-causal rule (see `oracle_gdn_frame_scan` in gdn_oracle.c): frames
+    of `frame` tokens share one pre-frame state for their predictions and
+    output from the post-frame state. Dense only: q, k (B, T, H, K); v
+    (B, T, H, V); beta (B, T, H); g_frame (B, T // frame, H) log decays;
+    h0 (B, H, K, V) or None. Returns (out, h_final) in float64."""
+    q, k, v, beta, g_frame, h0 = map(_f64, (q, k, v, beta, g_frame, h0))
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    assert T % frame == 0 and g_frame.shape == (B, T // frame, H)
+    row0 = np.arange(B, dtype=np.int64) * T
+    lens = np.full(B, T, dtype=np.int64)
+    out = np.zeros((B, T, H, V), dtype=np.float64)
+    hf = np.zeros((B, H, K, V), dtype=np.float64)
+    rc = _load().oracle_gdn_frame_scan(
+        B, _ptr(row0), _ptr(lens), H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(g_frame),
+        _ptr(beta), _ptr(h0), int(frame), int(bool(reverse)), _ptr(out), _ptr(hf),
+        int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gdn_frame_scan failed with status {rc}")
+    return out, hf
+
+
+def frame_den(q, k, beta, g_frame, frame, reverse=False, threads=None):
+    """Denominator of the frame-causal rule: the same recurrence with V = 1,
+    v = 1. Returns (B, H, T) float64."""
+    B, T, H, _ = np.shape(q)
+    ones = np.ones((B, T, H, 1), dtype=np.float64)
+    out, _ = frame_scan(q, k, ones, beta, g_frame, frame, reverse=reverse, threads=threads)
+    return np.ascontiguousarray(out[..., 0].transpose(0, 2, 1))
 
 
 def den(q, k, beta, g=None, gk=None, cu_seqlens=None, reverse=False,
@@ -171,6 +207,18 @@ def forward(w, threads=None):
                                                 scale=w.K ** -0.5)
     else:
         raise ValueError(w.prep)
+    if getattr(w, "frame", 1) > 1:
+        # frame-causal form (bidirectional: both directions summed, with den)
+        S, gf = w.frame, w.g_frame
+        of, hf = frame_scan(qn, kn, vv, w.beta, gf, S, h0=w.h0, threads=threads)
+        if not w.bidirectional:
+            res["out"], res["h_final"] = of, hf
+            return res
+        orv, _ = frame_scan(qn, kn, vv, w.beta, gf, S, reverse=True, threads=threads)
+        res["out"] = of + orv
+        res["den"] = (frame_den(qn, kn, w.beta, gf, S, threads=threads)
+                      + frame_den(qn, kn, w.beta, gf, S, reverse=True, threads=threads))
+        return res
     if not w.bidirectional:
         out, hf = scan(qn, kn, vv, w.beta, g=w.g, gk=w.gk, h0=w.h0,
                        cu_seqlens=w.cu_seqlens, threads=threads)

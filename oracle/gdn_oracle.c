@@ -166,6 +166,127 @@ int oracle_gdn_scan(int n_seq, const int64_t *row0, const int64_t *len, int H,
 }
 
 /*
+ * Frame-causal scan (SANA `fused_gdn.py` page, `_fused_gdn_kernel` with S
+ * tokens per frame; SANA `fused_cam_gdn.py` page, `_cam_scan_kernel`): per
+ * (sequence, head), frames of `frame` tokens, one log-decay per frame:
+ *   forward, frame f = 0 .. F-1:
+ *     S <- exp(gf_f) S;  S_pre = S
+ *     for every token t of frame f:  d = beta_t (v_t - S_pre^T k_t);
+ *                                    S <- S + k_t d^T
+ *     (every token predicts from the same pre-frame state S_pre)
+ *     then o_t = S^T q_t for every token of frame f (the post-frame state)
+ *   reverse, step i = 0 .. F-1: the output frame is F-1-i; for i > 0 the
+ *     state first absorbs frame F-i (its decay, then its tokens as above);
+ *     step 0 absorbs nothing. So frame f reads frames f+1 .. F-1.
+ * gf is (n_seq, F, H); h0 / h_final as for oracle_gdn_scan.
+ */
+typedef struct {
+    int n_seq, H, K, V, frame, reverse;
+    const int64_t *row0, *len;
+    const double *q, *k, *v, *gf, *beta, *h0;
+    double *out, *h_final;
+    long next;
+    int status;
+} frame_job;
+
+static void frame_absorb(const frame_job *J, double *S, double *Spre, double *p, int s, int f, int h) {
+    const int K = J->K, V = J->V, H = J->H;
+    const int F = (int)(J->len[s] / J->frame);
+    const double d = exp(J->gf[((int64_t)s * F + f) * H + h]);
+    for (int a = 0; a < K * V; ++a) S[a] *= d;
+    memcpy(Spre, S, sizeof(double) * K * V);
+    for (int t = 0; t < J->frame; ++t) {
+        const int64_t r = J->row0[s] + (int64_t)f * J->frame + t;
+        const double *kt = J->k + (r * H + h) * (int64_t)K;
+        const double *vt = J->v + (r * H + h) * (int64_t)V;
+        const double bt = J->beta[r * H + h];
+        for (int b = 0; b < V; ++b) {
+            double acc = 0.0;
+            for (int a = 0; a < K; ++a) acc += Spre[a * V + b] * kt[a];
+            p[b] = bt * (vt[b] - acc);
+        }
+        for (int a = 0; a < K; ++a)
+            for (int b = 0; b < V; ++b) S[a * V + b] += kt[a] * p[b];
+    }
+}
+
+static void frame_emit(const frame_job *J, const double *S, int s, int f, int h) {
+    const int K = J->K, V = J->V, H = J->H;
+    for (int t = 0; t < J->frame; ++t) {
+        const int64_t r = J->row0[s] + (int64_t)f * J->frame + t;
+        const double *qt = J->q + (r * H + h) * (int64_t)K;
+        double *ot = J->out + (r * H + h) * (int64_t)V;
+        for (int b = 0; b < V; ++b) {
+            double acc = 0.0;
+            for (int a = 0; a < K; ++a) acc += S[a * V + b] * qt[a];
+            ot[b] = acc;
+        }
+    }
+}
+
+static void *frame_worker(void *arg) {
+    frame_job *J = (frame_job *)arg;
+    const int K = J->K, V = J->V, H = J->H;
+    double *S = (double *)malloc(sizeof(double) * (size_t)K * V);
+    double *Spre = (double *)malloc(sizeof(double) * (size_t)K * V);
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!S || !Spre || !p) {
+        __atomic_store_n(&J->status, 1, __ATOMIC_RELAXED);
+        free(S);
+        free(Spre);
+        free(p);
+        return NULL;
+    }
+    const long total = (long)J->n_seq * H;
+    for (;;) {
+        long w = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+        if (w >= total) break;
+        const int s = (int)(w / H), h = (int)(w % H);
+        const int F = (int)(J->len[s] / J->frame);
+        if (J->h0)
+            memcpy(S, J->h0 + ((int64_t)s * H + h) * K * V, sizeof(double) * K * V);
+        else
+            memset(S, 0, sizeof(double) * K * V);
+        for (int i = 0; i < F; ++i) {
+            if (!J->reverse) {
+                frame_absorb(J, S, Spre, p, s, i, h);
+                frame_emit(J, S, s, i, h);
+            } else {
+                if (i > 0) frame_absorb(J, S, Spre, p, s, F - i, h);
+                frame_emit(J, S, s, F - 1 - i, h);
+            }
+        }
+        if (J->h_final) memcpy(J->h_final + ((int64_t)s * H + h) * K * V, S, sizeof(double) * K * V);
+    }
+    free(S);
+    free(Spre);
+    free(p);
+    return NULL;
+}
+
+int oracle_gdn_frame_scan(int n_seq, const int64_t *row0, const int64_t *len, int H, int K, int V,
+                          const double *q, const double *k, const double *v, const double *gf,
+                          const double *beta, const double *h0, int frame, int reverse,
+                          double *out, double *h_final, int n_threads) {
+    if (n_seq < 0 || H <= 0 || K <= 0 || V <= 0 || frame <= 0) return 2;
+    for (int s = 0; s < n_seq; ++s)
+        if (len[s] % frame != 0) return 2;
+    frame_job J = {n_seq, H, K, V, frame, reverse, row0, len, q, k, v, gf, beta, h0, out, h_final, 0, 0};
+    long total = (long)n_seq * H;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > total) n_threads = (int)(total > 0 ? total : 1);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * n_threads);
+    if (!th) return 1;
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i)
+        if (pthread_create(&th[started], NULL, frame_worker, &J) == 0) ++started;
+    frame_worker(&J);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    return J.status;
+}
+
+/*
  * L2 prep: x and y are (rows, D); y_r = x_r / sqrt(|x_r|^2 + eps).
  */
 void oracle_l2norm(const double *x, int64_t rows, int D, double eps, double *y) {

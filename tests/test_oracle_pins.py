@@ -394,3 +394,72 @@ def test_reverse_reset_splits_the_sequence(b):
     # without the reset the early positions see the later tokens
     plain, _ = oracle.scan(*map(_one, (q, k, v, beta, g)), reverse=True)
     assert np.abs(plain[0, :b, 0] - pre[0, :b, 0]).max() > 1e-3
+
+
+# ------------------------------------------------------------ frame-causal ---
+
+def _frame_rand(seed, B, F, S, H, K, V):
+    rng = np.random.default_rng(seed)
+    T = F * S
+    q, k = rng.normal(size=(B, T, H, K)), rng.normal(size=(B, T, H, K)) * 0.5
+    v, beta = rng.normal(size=(B, T, H, V)), rng.uniform(0.1, 0.9, (B, T, H))
+    gf = np.log(rng.uniform(0.5, 0.99, (B, F, H)))
+    return q, k, v, beta, gf
+
+
+@pytest.mark.parametrize("reverse", [False, True])
+def test_frame_of_one_token_is_the_token_rule(reverse):
+    # one token per frame: the SANA kernels' frame rule is exactly the token
+    # rule, with the per-frame decay as the per-token gate
+    q, k, v, beta, gf = _frame_rand(21, 2, 9, 1, 3, 4, 3)
+    h0 = None if reverse else np.random.default_rng(22).normal(size=(2, 3, 4, 3))
+    of, hf = oracle.frame_scan(q, k, v, beta, gf, 1, h0=h0, reverse=reverse)
+    ot, ht = oracle.scan(q, k, v, beta, g=gf, h0=h0, reverse=reverse)
+    np.testing.assert_allclose(of, ot, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(hf, ht, rtol=0, atol=1e-14)
+
+
+def test_frame_rule_matrix_form():
+    # per frame, as matrix products (SANA `fused_gdn.py` page, Pass 1 with a
+    # fixed state_prev): S_pre = e^{g_f} S; S = S_pre + K^T diag(beta)(V - K S_pre);
+    # then O = Q S for the frame's tokens
+    B, F, S, H, K, V = 1, 4, 5, 2, 3, 4
+    q, k, v, beta, gf = _frame_rand(23, B, F, S, H, K, V)
+    h0 = np.random.default_rng(24).normal(size=(B, H, K, V))
+    out, hf = oracle.frame_scan(q, k, v, beta, gf, S, h0=h0)
+    for h in range(H):
+        St = h0[0, h].copy()
+        for f in range(F):
+            rows = slice(f * S, (f + 1) * S)
+            Kf, Vf, Qf = k[0, rows, h], v[0, rows, h], q[0, rows, h]
+            Spre = np.exp(gf[0, f, h]) * St
+            St = Spre + Kf.T @ (beta[0, rows, h][:, None] * (Vf - Kf @ Spre))
+            np.testing.assert_allclose(out[0, rows, h], Qf @ St, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(hf[0, h], St, rtol=1e-12, atol=1e-12)
+
+
+def test_frame_reverse_is_frame_flip_and_shift():
+    # reverse at frame granularity (`_fused_gdn_kernel` REVERSE: q_frame =
+    # F-1-i, kv_frame = F-i, no update and decay 1 at i = 0) == the forward
+    # frame rule on frames taken in reverse order, k / v / beta / decay moved
+    # one frame later (pad 0, decay pad 0 = log 1), outputs put back
+    B, F, S, H, K, V = 2, 5, 3, 2, 4, 3
+    q, k, v, beta, gf = _frame_rand(25, B, F, S, H, K, V)
+    rev, _ = oracle.frame_scan(q, k, v, beta, gf, S, reverse=True)
+
+    def frames(x):
+        return x.reshape(x.shape[0], F, S, *x.shape[2:])
+
+    def flip_shift(x, pad):
+        xf = frames(x)[:, ::-1]
+        y = np.full_like(xf, pad)
+        y[:, 1:] = xf[:, :-1]
+        return y.reshape(x.shape)
+    qf = frames(q)[:, ::-1].reshape(q.shape)
+    g2 = np.zeros_like(gf)
+    g2[:, 1:] = gf[:, ::-1][:, :-1]
+    fwd, _ = oracle.frame_scan(qf, flip_shift(k, 0.0), flip_shift(v, 0.0), flip_shift(beta, 0.0),
+                               g2, S)
+    back = frames(fwd)[:, ::-1].reshape(fwd.shape)
+    np.testing.assert_allclose(rev, back, rtol=1e-13, atol=1e-13)
+    assert np.all(frames(rev)[:, -1] == 0.0)

@@ -31,7 +31,7 @@ import numpy as np
 BLOCK = 1 << 22  # elements per independently seeded block
 
 _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "g": 5, "gk": 6, "h0": 7,
-               "lens": 8, "qkv": 9, "gate": 10}
+               "lens": 8, "qkv": 9, "gate": 10, "g_frame": 11}
 
 
 def _normal_fill(seed: int, name: str, n: int, mu: float, sigma: float,
@@ -186,6 +186,10 @@ class Workload:
     merge: bool = False
     gate: Stored | None = None
     eps: float = 1e-6
+    # frame-causal form: `frame` tokens per frame share the pre-frame state;
+    # one log-decay per frame, g_frame (B, T // frame, H) (then g is None)
+    frame: int = 1
+    g_frame: np.ndarray | None = None
 
     @property
     def n_seq(self) -> int:
@@ -231,14 +235,16 @@ def make(B: int, T: int, H: int, K: int, V: int, dtype: str = "bf16", *,
 
 def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
                g_mu: float = 4.0, name: str = "video", reset_every: int | None = None,
-               merge: bool = False) -> Workload:
+               merge: bool = False, frame: int = 1) -> Workload:
     """Interleaved qkv (B, N, 3, H, D) ~ N(0,1) bf16, bidirectional, with the
     full-channel RMSNorm + ReLU + k-scale prep.
 
     reset_every = R makes it chunk-causal: the backward direction's log-gate
     is -inf and its beta 0 at tokens R, 2R, ..., so that a token's backward
     state holds only the later tokens of its own R-token chunk. merge adds
-    out = num / (den + eps) * silu(gate), gate (B, N, H, D) ~ N(0,1) bf16."""
+    out = num / (den + eps) * silu(gate), gate (B, N, H, D) ~ N(0,1) bf16.
+    frame = S > 1 makes it frame-causal: frames of S tokens, one log-decay per
+    frame and head, log sigmoid(N(g_mu, 1)) (B, N // S, H)."""
     qkv = stored_normal(seed, "qkv", (B, N, 3, H, D), "bf16")
     beta = sigmoid_normal(seed, "beta", (B, N, H), 0.0)
     g = log_sigmoid_normal(seed, "g", (B, N, H), g_mu)
@@ -248,12 +254,17 @@ def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
         g_bwd[:, reset_every::reset_every, :] = -np.inf
         beta_bwd[:, reset_every::reset_every, :] = 0.0
     gate = stored_normal(seed, "gate", (B, N, H, D), "bf16") if merge else None
+    g_frame = None
+    if frame > 1:
+        assert N % frame == 0
+        g, g_frame = None, log_sigmoid_normal(seed, "g_frame", (B, N // frame, H), g_mu)
 
     def part(i):
         return qkv.take((slice(None), slice(None), i))
     return Workload(name, B, N, H, D, D, "bf16", part(0), part(1), part(2),
                     beta, g, qkv=qkv, prep="rms_relu", bidirectional=True,
-                    g_bwd=g_bwd, beta_bwd=beta_bwd, merge=merge, gate=gate)
+                    g_bwd=g_bwd, beta_bwd=beta_bwd, merge=merge, gate=gate,
+                    frame=frame, g_frame=g_frame)
 
 
 # The five workloads, named by what they are.
@@ -265,6 +276,8 @@ WORKLOADS = {
     "bidir_video_b2h16n8192d112": dict(kind="video", B=2, N=8192, H=16, D=112),
     "chunkcausal_merge_video_b2h16n8192d112": dict(kind="video", B=2, N=8192, H=16,
                                                    D=112, reset_every=1024, merge=True),
+    "frame_video_b2h16f8s1024d112": dict(kind="video", B=2, N=8192, H=16, D=112,
+                                         frame=1024),
     "varlen_bf16_64seq_h32d128": dict(kind="varlen", n_seq=64, lo=128, hi=8192,
                                       H=32, K=128, V=128, h0_std=0.02),
     "gk_bf16_b1h32t65536k128v256": dict(kind="dense", B=1, T=65536, H=32,
@@ -297,7 +310,7 @@ def build(name: str, seed: int = 0, T: int | None = None) -> Workload:
     if kind == "video":
         return make_video(spec["B"], spec["N"], spec["H"], spec["D"], seed=seed,
                           name=name, reset_every=spec.get("reset_every"),
-                          merge=spec.get("merge", False))
+                          merge=spec.get("merge", False), frame=spec.get("frame", 1))
     if kind == "varlen":
         lens = varlen_lengths(seed, spec["n_seq"], spec["lo"], spec["hi"])
         return make(1, sum(lens), spec["H"], spec["K"], spec["V"], "bf16",
