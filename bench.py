@@ -52,6 +52,20 @@ def path_work(w):
     inputs read once, outputs written once, h0/h_final once."""
     th = w.B * w.T * w.H
     e = 2 if w.dtype == "bf16" else 4
+    if w.frame > 1:
+        # per token-head: the frame Gram K^T diag(beta)[K | V | 1] and O = Q S (2KVt
+        # each direction summed first); the chain adds 2 K K Vt per frame and direction
+        Vt = w.V + (1 if w.bidirectional else 0)
+        dirs = 2 if w.bidirectional else 1
+        fl = th * (2.0 * w.K * (w.K + Vt) + 2.0 * w.K * Vt) + dirs * w.B * w.H * (w.T // w.frame) \
+            * 2.0 * w.K * w.K * Vt
+        by = th * (3 * w.K * e + 4 + w.V * e + (4 if w.bidirectional else 0)) \
+            + w.B * w.H * (w.T // w.frame) * 4
+        if w.h0 is not None:
+            by += w.n_seq * w.H * w.K * w.V * 4
+        if not w.bidirectional:
+            by += w.n_seq * w.H * w.K * w.V * 4
+        return fl, by
     if w.bidirectional:
         fl = th * (flops_per_token_head(w.K, w.V) + flops_per_token_head(w.K, w.V + 1))
         by = th * (3 * w.K * e + 4 + 4 + w.V * e + 4)       # qkv, beta, g, num, den
@@ -90,6 +104,15 @@ def kernel_bytes(w, name):
         return w.B * w.T * w.H * w.K * e * 2 + w.B * w.T * 4
     if name == "prep_l2":
         return th * w.K * e * 2
+    if name == "frame":
+        # gram reads k (per column block, from L2 after the first) and v once,
+        # writes A_f, B_f; the chain reads them and writes the read states; the
+        # output reads q and the states, writes out (and den)
+        Vt = w.V + (1 if w.bidirectional else 0)
+        nf = w.B * w.H * (w.T // w.frame)
+        mats = nf * w.K * (w.K + Vt) * 4
+        return th * (3 * w.K * e + 4 + w.V * e + (4 if w.bidirectional else 0)) \
+            + 2 * mats + 2 * nf * w.K * Vt * 4
     if name == "merge":
         return th * w.V * e * (3 if w.gate is not None else 2) + th * 4
     return None
@@ -233,6 +256,7 @@ def device_inputs(w, dev):
         d["q"], d["k"], d["v"] = to_dev(w.q), to_dev(w.k), to_dev(w.v)
     d["beta"], d["g"], d["gk"], d["h0"] = f32(w.beta), f32(w.g), f32(w.gk), f32(w.h0)
     d["g_bwd"], d["beta_bwd"] = f32(w.g_bwd), f32(w.beta_bwd)
+    d["g_frame"] = f32(w.g_frame)
     d["gate"] = None if w.gate is None else to_dev(w.gate)
     d["cu_seqlens"] = None if w.cu_seqlens is None else torch.from_numpy(
         w.cu_seqlens.astype(np.int32)).to(dev)
@@ -241,7 +265,9 @@ def device_inputs(w, dev):
 
 def run_step(gdn, w, d, ws):
     extra = {}
-    if w.bidirectional:
+    if w.frame > 1:
+        extra = dict(frame=w.frame, g_frame=d["g_frame"])
+    elif w.bidirectional:
         bw = {k2: d[k2 + "_bwd"] for k2 in ("g", "beta") if d.get(k2 + "_bwd") is not None}
         extra = dict(backward=bw or None, merge=w.merge, gate=d.get("gate"), eps=w.eps)
     return gdn.gdn_forward(d["q"], d["k"], d["v"], d["beta"], g=d["g"], gk=d["gk"],
@@ -264,7 +290,7 @@ def e2e_measure(gdn, w, d, ws, steps, dev):
     import torch
     host = {}
     for key in ("qkv", "q", "k", "v", "beta", "g", "gk", "h0", "cu_seqlens", "g_bwd",
-                "beta_bwd", "gate"):
+                "beta_bwd", "gate", "g_frame"):
         t = d.get(key)
         if t is None or (key in ("q", "k", "v") and "qkv" in d):
             continue
@@ -325,7 +351,9 @@ def oracle_sample(w):
         # full-channel RMS prep needs every head of a token: whole batch rows
         ix = (slice(0, 1),)
         sw = dataclasses.replace(w, B=1, qkv=w.qkv.take(ix), q=w.q.take(ix), k=w.k.take(ix),
-                                 v=w.v.take(ix), beta=w.beta[ix], g=w.g[ix],
+                                 v=w.v.take(ix), beta=w.beta[ix],
+                                 g=None if w.g is None else w.g[ix],
+                                 g_frame=None if w.g_frame is None else w.g_frame[ix],
                                  g_bwd=None if w.g_bwd is None else w.g_bwd[ix],
                                  beta_bwd=None if w.beta_bwd is None else w.beta_bwd[ix],
                                  gate=None if w.gate is None else w.gate.take(ix))

@@ -18,7 +18,7 @@ import os
 from .build import LIB
 
 __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
-           "gdn_merge", "gdn_workspace_size",
+           "gdn_merge", "gdn_frame_fwd", "gdn_frame_workspace_size", "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_forward", "lib",
            "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect",
            "launch_count", "kernel_names"]
@@ -70,6 +70,11 @@ def lib():
     L.gdn_chunk_fwd_noalloc.restype = I
     L.gdn_chunk_fwd_noalloc.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P,
                                         TensorDesc, P, P, I, I, I, I, I, I, I, I, P]
+    L.gdn_frame_workspace_size.restype = ctypes.c_size_t
+    L.gdn_frame_workspace_size.argtypes = [I] * 7
+    L.gdn_frame_fwd.restype = I
+    L.gdn_frame_fwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, TensorDesc, P, P,
+                                I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
     L.gdn_merge.restype = I
     L.gdn_merge.argtypes = [P, TensorDesc, P, P, TensorDesc, P, TensorDesc, I, I, I, I, F, P]
     L.gdn_last_device_error.restype = I
@@ -230,6 +235,37 @@ def gdn_merge(num, den, gate=None, eps=1e-6, out=None, out_dtype=None, stream=No
     return out
 
 
+def gdn_frame_workspace_size(B, T, H, K, V, frame, with_den) -> int:
+    return int(lib().gdn_frame_workspace_size(B, T, H, K, V, frame, int(bool(with_den))))
+
+
+def gdn_frame_fwd(q, k, v, beta, g_frame, frame, out=None, den=None, h0=None, h_final=None,
+                  direction=0, accumulate=False, workspace=None, stream=None, out_dtype=None):
+    """The frame-causal form (see include/gdn.h): frames of `frame` tokens
+    share the pre-frame state. q, k (B, T, H, K), v (B, T, H, V) bf16 (q, k
+    prepared); beta (B, T, H), g_frame (B, T // frame, H) fp32; direction 0
+    forward, 1 reverse, 2 both summed; den (B, H, T) fp32. Returns out."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    for name, t in (("beta", beta), ("g_frame", g_frame), ("h0", h0), ("h_final", h_final),
+                    ("den", den)):
+        _f32(t, name)
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=out_dtype or q.dtype, device=q.device)
+    need = gdn_frame_workspace_size(B, T, H, K, V, frame, den is not None)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().gdn_frame_fwd(
+        _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g_frame), _ptr(beta), _ptr(h0),
+        _ptr(out), _desc(out), _ptr(h_final), _ptr(den), B, T, H, K, V, int(frame),
+        int(direction), ACCUMULATE if accumulate else 0, _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_frame_fwd")
+    return out
+
+
 def gdn_last_device_error(workspace, stream=None) -> int:
     """Synchronise, read and clear the device error word; returns it."""
     w = ctypes.c_int(0)
@@ -241,7 +277,8 @@ def gdn_last_device_error(workspace, stream=None) -> int:
 
 def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                 prep="l2", bidirectional=False, with_final_state=False, workspace=None,
-                stream=None, backward=None, merge=False, gate=None, eps=1e-6):
+                stream=None, backward=None, merge=False, gate=None, eps=1e-6, frame=1,
+                g_frame=None):
     """The whole forward: q/k prep, then the causal scan, or the causal plus
     the reverse scan summed with the denominator (bidirectional).
 
@@ -253,6 +290,8 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
     chunk-causal form's gates with -inf at chunk boundaries (the SANA
     `fused_gdn.py` page's decay_bwd / beta_bwd / qkv_bwd).
     merge: also return "merged" = out / (den + eps) * silu(gate) (gdn_merge).
+    frame > 1: the frame-causal form (gdn_frame_fwd) with per-frame log
+    decays g_frame (B, T // frame, H) in place of g.
     Returns a dict with "out" and, as requested, "h_final" / "den" /
     "merged" / "q_inv_rms" / "k_inv_rms"."""
     torch = _torch()
@@ -279,6 +318,24 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                                     stream=stream)
     elif prep not in ("l2", None):
         raise ValueError(f"unknown prep {prep!r}")
+    if frame > 1:
+        if backward or merge or gk is not None or cu_seqlens is not None:
+            raise ValueError("the frame-causal form takes no backward inputs, merge, gk or varlen")
+        if fuse:
+            q, k = gdn_prep(q, mode=PREP_L2, stream=stream), gdn_prep(k, mode=PREP_L2, stream=stream)
+        if not bidirectional:
+            hf = (torch.empty((B, H, K, v.shape[3]), dtype=torch.float32, device=q.device)
+                  if with_final_state else None)
+            res["out"] = gdn_frame_fwd(q, k, v, beta, g_frame, frame, h0=h0, h_final=hf,
+                                       workspace=workspace, stream=stream)
+            if hf is not None:
+                res["h_final"] = hf
+            return res
+        den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+        res["out"] = gdn_frame_fwd(q, k, v, beta, g_frame, frame, den=den, direction=2,
+                                   workspace=workspace, stream=stream)
+        res["den"] = den
+        return res
     if not bidirectional:
         hf = (torch.empty((n_seq, H, K, v.shape[3]), dtype=torch.float32, device=q.device)
               if with_final_state else None)

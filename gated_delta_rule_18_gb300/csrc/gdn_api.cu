@@ -14,9 +14,9 @@ using gdn::FwdParams;
 
 // ------------------------------------------------------------ profiling ----
 
-enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KNumKinds };
+enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrame, KNumKinds };
 const char *kKindNames[KNumKinds] = {"prep_l2", "prep_rms", "chunk_table", "intra_bf16",
-                                     "state_tc", "fused_f32", "merge"};
+                                     "state_tc", "fused_f32", "merge", "frame"};
 
 struct Profiler {
     std::mutex mu;
@@ -315,6 +315,75 @@ gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den, cons
     m.num_bf16 = nd.dtype == GDN_BF16;
     m.out_bf16 = od.dtype == GDN_BF16;
     return cuda_status(launch(KMerge, stream, [&] { return gdn::launch_merge(m, stream); }));
+}
+
+namespace {
+// frame-causal workspace: A_f, B_f and the read states, fp32, 256-byte sections
+struct FrameWs {
+    size_t amat, bmat, sout, total;
+};
+bool frame_ws(int B, int T, int H, int K, int V, int frame, int with_den, FrameWs &L) {
+    if (B < 1 || T < 0 || H < 1 || K < 1 || K > 128 || V < 1 || V > 256 || frame < gdn::kChunk ||
+        frame % gdn::kChunk != 0 || T % frame != 0)
+        return false;
+    const size_t F = (size_t)(T / frame), bh = (size_t)B * H, Vt = (size_t)V + (with_den ? 1 : 0);
+    size_t off = 0;
+    L.amat = off;
+    off = align_up(off + bh * F * K * K * 4);
+    L.bmat = off;
+    off = align_up(off + bh * F * K * Vt * 4);
+    L.sout = off;
+    off = align_up(off + bh * F * K * Vt * 4);
+    L.total = off > 0 ? off : kAlign;
+    return true;
+}
+}  // namespace
+
+size_t gdn_frame_workspace_size(int B, int T, int H, int K, int V, int frame, int with_den) {
+    FrameWs L;
+    return frame_ws(B, T, H, K, V, frame, with_den, L) ? L.total : 0;
+}
+
+gdn_status gdn_frame_fwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                         gdn_tensor_desc vd, const float *g_frame, const float *beta,
+                         const float *h0, void *out, gdn_tensor_desc od, float *h_final,
+                         float *den_out, int B, int T, int H, int K, int V, int frame,
+                         int direction, int flags, void *workspace, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (B < 1 || T < 0 || H < 1 || K < 1 || V < 1) return GDN_ERR_SHAPE;
+    if (direction < 0 || direction > 2) return GDN_ERR_UNSUPPORTED;
+    if ((flags & ~GDN_ACCUMULATE) != 0) return GDN_ERR_UNSUPPORTED;
+    if ((h0 || h_final) && direction != 0) return GDN_ERR_UNSUPPORTED;
+    if (T > 0 && (!q || !k || !v || !g_frame || !beta || !out)) return GDN_ERR_NULL;
+    if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16) return GDN_ERR_DTYPE;
+    if (!dtype_ok(od.dtype)) return GDN_ERR_DTYPE;
+    if (K % 8 != 0 || V % 8 != 0 || K > 128 || V > 256) return GDN_ERR_SHAPE;
+    if (frame < gdn::kChunk || frame % gdn::kChunk != 0 || T % frame != 0) return GDN_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !strides_ok(qkd) ||
+        !strides_ok(vd) || !strides_ok(od))
+        return GDN_ERR_LAYOUT;
+    FrameWs L;
+    if (!frame_ws(B, T, H, K, V, frame, den_out != nullptr, L)) return GDN_ERR_SHAPE;
+    if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
+    if (T == 0) return GDN_OK;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    gdn::FrameParams p{};
+    p.q = q, p.k = k, p.v = v;
+    p.qk_sb = qkd.stride_b, p.qk_st = qkd.stride_t, p.qk_sh = qkd.stride_h;
+    p.v_sb = vd.stride_b, p.v_st = vd.stride_t, p.v_sh = vd.stride_h;
+    p.beta = beta, p.g_frame = g_frame, p.h0 = h0, p.h_final = h_final;
+    p.out = out, p.o_sb = od.stride_b, p.o_st = od.stride_t, p.o_sh = od.stride_h;
+    p.out_f32 = od.dtype == GDN_F32;
+    p.den = den_out;
+    p.B = B, p.T = T, p.H = H, p.K = K, p.V = V, p.Vt = V + (den_out ? 1 : 0);
+    p.F = T / frame, p.frame = frame;
+    p.has_den = den_out != nullptr;
+    p.accumulate = (flags & GDN_ACCUMULATE) != 0;
+    p.direction = direction;
+    p.amat = reinterpret_cast<float *>(ws + L.amat);
+    p.bmat = reinterpret_cast<float *>(ws + L.bmat);
+    p.sout = reinterpret_cast<float *>(ws + L.sout);
+    return cuda_status(launch(KFrame, stream, [&] { return gdn::launch_frame(p, stream); }));
 }
 
 gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream, int *word) {

@@ -261,6 +261,23 @@ struct MergeParams {
     int num_bf16, out_bf16;
 };
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t st);
+// The frame-causal form (gdn_frame.cu).
+struct FrameParams {
+    const void *q, *k, *v;  // bf16 (B, T, H, D)
+    int64_t qk_sb, qk_st, qk_sh, v_sb, v_st, v_sh;
+    const float *beta;     // (B, T, H)
+    const float *g_frame;  // (B, F, H) log decay per frame
+    const float *h0;       // (B, H, K, V) or null (forward only)
+    float *h_final;        // (B, H, K, V) or null (forward only)
+    void *out;
+    int64_t o_sb, o_st, o_sh;
+    int out_f32;
+    float *den;  // (B, H, T) or null
+    int B, T, H, K, V, Vt, F, frame;
+    int has_den, accumulate, direction;  // direction: 0 forward, 1 reverse, 2 both summed
+    float *amat, *bmat, *sout;           // workspace: A_f (K x K), B_f (K x Vt), read states (K x Vt)
+};
+cudaError_t launch_frame(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
 cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);

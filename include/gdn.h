@@ -214,6 +214,35 @@ gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den,
                      gdn_tensor_desc od, int B, int T, int H, int V, float eps,
                      cudaStream_t stream);
 
+/*
+ * gdn_frame_workspace_size / gdn_frame_fwd -- the frame-causal form of the
+ * rule (SANA `fused_gdn.py` page, `_fused_gdn_kernel` with S tokens per frame;
+ * SANA `fused_cam_gdn.py` page, `_cam_scan_kernel`): per (sequence, head),
+ * frames of `frame` tokens and one log-decay per frame,
+ *   S_pre = e^{g_f} S;  S <- S_pre + sum_{t in frame} k_t beta_t (v_t - S_pre^T k_t)^T
+ *   o_t = S^T q_t for every token t of the frame (the post-frame state)
+ * i.e. every token of a frame predicts from the same pre-frame state. With
+ * direction 1 (reverse) frame f reads frames f+1 .. F-1 (each frame's decay
+ * applied before its tokens); direction 2 sums both directions (the
+ * bidirectional num, and den when den_out is given).
+ *   q, k: (B, T, H, K) bf16 (prepared: gdn_prep); v: (B, T, H, V) bf16;
+ *   g_frame: (B, T / frame, H) fp32 log decays (floored at -30);
+ *   beta: (B, T, H) fp32; out: (B, T, H, V) bf16 or fp32; den_out: (B, H, T)
+ *   fp32 or NULL; h0 / h_final: (B, H, K, V) fp32, direction 0 only.
+ *   frame a multiple of 64 dividing T; K <= 128, V <= 256, both multiples
+ *   of 8. flags: GDN_ACCUMULATE adds into out / den_out.
+ * Workspace: gdn_frame_workspace_size() bytes (with_den as for the call).
+ */
+size_t gdn_frame_workspace_size(int B, int T, int H, int K, int V, int frame,
+                                int with_den);
+gdn_status gdn_frame_fwd(const void *q, const void *k, gdn_tensor_desc qkd,
+                         const void *v, gdn_tensor_desc vd, const float *g_frame,
+                         const float *beta, const float *h0, void *out,
+                         gdn_tensor_desc od, float *h_final, float *den_out,
+                         int B, int T, int H, int K, int V, int frame,
+                         int direction, int flags, void *workspace,
+                         size_t ws_bytes, cudaStream_t stream);
+
 const char *gdn_status_string(gdn_status s);
 
 /*

@@ -61,7 +61,9 @@ def run_gpu(w, with_final_state=True):
     if w.beta_bwd is not None:
         bw["beta"] = f32_dev(w.beta_bwd)
     extra = {}
-    if w.bidirectional and (bw or w.merge):
+    if w.frame > 1:
+        extra = dict(frame=w.frame, g_frame=f32_dev(w.g_frame))
+    elif w.bidirectional and (bw or w.merge):
         extra = dict(backward=bw or None, merge=w.merge, eps=w.eps,
                      gate=None if w.gate is None else to_dev(w.gate))
     res = gdn.gdn_forward(q, k, v, f32_dev(w.beta), g=f32_dev(w.g), gk=f32_dev(w.gk),

@@ -143,6 +143,27 @@ def test_merge_rejects_on_host(L):
     assert m(T=0) == OK                             # nothing to do, nothing launched
 
 
+def test_frame_fwd_rejects_on_host(L):
+    d16, d32 = desc(gdn.BF16, 1, 256, 2, 64), desc(gdn.F32, 1, 256, 2, 64)
+
+    def ff(q=P(0), qkd=d16, vd=d16, gf=P(3), h0=None, hf=None, den=None, T=256, frame=64,
+           direction=0, flags=0, ws=P(9), wsb=1 << 30):
+        return L.gdn_frame_fwd(q, P(1), qkd, P(2), vd, gf, P(4), h0, P(5), d16, hf, den, 1, T, 2,
+                               64, 64, frame, direction, flags, ws, wsb, None)
+    assert ff(q=None) == NULL
+    assert ff(qkd=d32) == DTYPE                    # the frame path takes bf16 q / k / v
+    assert ff(frame=96) == SHAPE                   # not a multiple of 64
+    assert ff(frame=192) == SHAPE                  # does not divide T
+    assert ff(direction=3) == UNSUP
+    assert ff(direction=1, h0=P(6)) == UNSUP       # state I/O is forward only
+    assert ff(flags=0x2) == UNSUP
+    assert ff(q=ctypes.c_void_p(A + 8)) == LAYOUT
+    assert ff(wsb=16) == WS
+    assert ff(T=0) == OK                           # nothing to do, nothing launched
+    assert gdn.gdn_frame_workspace_size(1, 256, 2, 64, 64, 64, True) > 0
+    assert gdn.gdn_frame_workspace_size(1, 256, 2, 64, 64, 96, True) == 0
+
+
 def test_python_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(gdn, "_lib", None)
     monkeypatch.setattr(gdn, "LIB", "/nonexistent/libgdn.so")

@@ -87,6 +87,21 @@ def test_small_chunkcausal_merge(reset):
     _compare(w, ["out", "den", "merged"])
 
 
+@pytest.mark.parametrize("frame", [64, 192])
+def test_small_frame_bidirectional(frame):
+    # frame-causal form: frames share the pre-frame state; both directions + den
+    w = workloads.make_video(1, 576, 4, 112, seed=6, name="frame_small", frame=frame)
+    _compare(w, ["out", "den"])
+
+
+def test_small_frame_forward_state_io():
+    # frame-causal forward with h0 / h_final and L2 prep, K = V = 64
+    w = workloads.make(2, 256, 3, 64, 64, "bf16", seed=7, name="frame_fwd", h0_std=0.1)
+    gf = workloads.log_sigmoid_normal(7, "g_frame", (2, 256 // 128, 3), 3.0)
+    w = dataclasses.replace(w, frame=128, g_frame=gf, g=None)
+    _compare(w, ["out", "h_final"])
+
+
 @pytest.mark.parametrize("dtype,out_dtype", [("bf16", "bf16"), ("f32", "f32"), ("f32", "bf16")])
 @pytest.mark.parametrize("with_gate", [False, True])
 def test_merge_kernel(dtype, out_dtype, with_gate):
@@ -259,6 +274,23 @@ def test_full_size_chunkcausal_merge():
     assert rel_err(got["out"][b:b + 1][:, :, heads], of + orv) <= 2e-2
     assert rel_err(got["den"][b:b + 1][:, heads], den) <= 2e-2
     assert rel_err(got["merged"][b:b + 1][:, :, heads], merged) <= 2e-2
+
+
+def test_full_size_frame_video():
+    w = workloads.build("frame_video_b2h16f8s1024d112")
+    got = run_gpu(w)
+    b, heads = 1, [2, 11]
+    qkv = w.qkv.take((slice(b, b + 1),)).values.astype(np.float64)
+    qn, _ = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
+    kn, _ = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    qn, kn, vv = qn[:, :, heads], kn[:, :, heads], qkv[:, :, 2][:, :, heads]
+    beta, gf = w.beta[b:b + 1][:, :, heads], w.g_frame[b:b + 1][:, :, heads]
+    of, _ = oracle.frame_scan(qn, kn, vv, beta, gf, w.frame)
+    orv, _ = oracle.frame_scan(qn, kn, vv, beta, gf, w.frame, reverse=True)
+    den = oracle.frame_den(qn, kn, beta, gf, w.frame) + oracle.frame_den(qn, kn, beta, gf, w.frame,
+                                                                         reverse=True)
+    assert rel_err(got["out"][b:b + 1][:, :, heads], of + orv) <= 2e-2
+    assert rel_err(got["den"][b:b + 1][:, heads], den) <= 2e-2
 
 
 def test_full_size_video_bidirectional():
