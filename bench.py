@@ -104,15 +104,16 @@ def kernel_bytes(w, name):
         return w.B * w.T * w.H * w.K * e * 2 + w.B * w.T * 4
     if name == "prep_l2":
         return th * w.K * e * 2
-    if name == "frame":
-        # gram reads k (per column block, from L2 after the first) and v once,
-        # writes A_f, B_f; the chain reads them and writes the read states; the
-        # output reads q and the states, writes out (and den)
+    if name in ("frame_gram", "frame_chain", "frame_out"):
         Vt = w.V + (1 if w.bidirectional else 0)
         nf = w.B * w.H * (w.T // w.frame)
-        mats = nf * w.K * (w.K + Vt) * 4
-        return th * (3 * w.K * e + 4 + w.V * e + (4 if w.bidirectional else 0)) \
-            + 2 * mats + 2 * nf * w.K * Vt * 4
+        mats = nf * w.K * (w.K + Vt) * 4          # A_f and B_f, fp32
+        states = nf * w.K * Vt * 4                 # the states the outputs read
+        if name == "frame_gram":                   # k, v, beta in; A_f, B_f out
+            return th * (w.K * e + w.V * e + 4) + mats
+        if name == "frame_chain":                  # A_f, B_f in; states out
+            return mats + states + nf * 4
+        return th * (w.K * e + w.V * e + (4 if w.bidirectional else 0)) + states
     if name == "merge":
         return th * w.V * e * (3 if w.gate is not None else 2) + th * 4
     return None

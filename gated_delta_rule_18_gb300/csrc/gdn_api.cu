@@ -14,9 +14,13 @@ using gdn::FwdParams;
 
 // ------------------------------------------------------------ profiling ----
 
-enum Kind { KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrame, KNumKinds };
-const char *kKindNames[KNumKinds] = {"prep_l2", "prep_rms", "chunk_table", "intra_bf16",
-                                     "state_tc", "fused_f32", "merge", "frame"};
+enum Kind {
+    KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
+    KFrameOut, KNumKinds
+};
+const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
+                                     "state_tc", "fused_f32", "merge",      "frame_gram",
+                                     "frame_chain", "frame_out"};
 
 struct Profiler {
     std::mutex mu;
@@ -383,7 +387,10 @@ gdn_status gdn_frame_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     p.amat = reinterpret_cast<float *>(ws + L.amat);
     p.bmat = reinterpret_cast<float *>(ws + L.bmat);
     p.sout = reinterpret_cast<float *>(ws + L.sout);
-    return cuda_status(launch(KFrame, stream, [&] { return gdn::launch_frame(p, stream); }));
+    cudaError_t e = launch(KFrameGram, stream, [&] { return gdn::launch_frame_gram(p, stream); });
+    if (e == cudaSuccess) e = launch(KFrameChain, stream, [&] { return gdn::launch_frame_chain(p, stream); });
+    if (e == cudaSuccess) e = launch(KFrameOut, stream, [&] { return gdn::launch_frame_out(p, stream); });
+    return cuda_status(e);
 }
 
 gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream, int *word) {

@@ -277,7 +277,9 @@ struct FrameParams {
     int has_den, accumulate, direction;  // direction: 0 forward, 1 reverse, 2 both summed
     float *amat, *bmat, *sout;           // workspace: A_f (K x K), B_f (K x Vt), read states (K x Vt)
 };
-cudaError_t launch_frame(const FrameParams &p, cudaStream_t st);
+cudaError_t launch_frame_gram(const FrameParams &p, cudaStream_t st);
+cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st);
+cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
 cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);

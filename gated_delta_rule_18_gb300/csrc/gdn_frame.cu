@@ -17,8 +17,9 @@
 //                bf16, fp32 accumulate); A_f = I - C_KK, B_f = C_KV to the
 //                workspace (fp32)
 //   frame_chain  per (sequence, head, 16-column tile): the fp32 chains
-//                S_f = A_f (e^{g_f} S_{f-1}) + B_f forward and / or reverse,
-//                the states each frame's outputs read summed over directions
+//                S_f = A_f (e^{g_f} S_{f-1}) + B_f forward and / or reverse
+//                (A_f staged in shared memory per step), the states each
+//                frame's outputs read summed over directions
 //   frame_out    per (sequence, head, 64-token chunk, 64-column block):
 //                O = Q S_f on tensor cores; the ones column gives den
 #include "gdn_common.cuh"
@@ -135,10 +136,16 @@ __global__ void __launch_bounds__(128) frame_gram_kernel(const FrameParams p) {
 }
 
 // --------------------------------------------------------------- chain ---
-constexpr int kCT = 16;  // state columns per chain CTA
+constexpr int kCT = 16;        // state columns per chain CTA
+constexpr int kAS = kKP + 1;   // fp32 row stride of A_f in shared memory (conflict-free rows)
+struct ChainSmem {
+    float a[kKP * kAS];        // A_f, [key][key]
+    float s[kKP * kCT];        // the state tile, [key][column]
+    float n[kKP * kCT];
+};
 __global__ void __launch_bounds__(256) frame_chain_kernel(const FrameParams p) {
-    __shared__ float sS[kKP * kCT];  // the state tile, [key][column]
-    __shared__ float sN[kKP * kCT];
+    extern __shared__ __align__(16) unsigned char smraw[];
+    ChainSmem &sm = *reinterpret_cast<ChainSmem *>(smraw);
     const int tid = threadIdx.x;
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int j0 = blockIdx.y * kCT;
@@ -150,7 +157,7 @@ __global__ void __launch_bounds__(256) frame_chain_kernel(const FrameParams p) {
             const int rr = e / kCT, j = j0 + e % kCT;
             float v0 = 0.f;
             if (!rev && p.h0 && rr < K && j < p.V) v0 = p.h0[(((int64_t)b * p.H + h) * K + rr) * p.V + j];
-            sS[e] = v0;
+            sm.s[e] = v0;
         }
         __syncthreads();
         for (int i = 0; i < F; ++i) {
@@ -159,28 +166,40 @@ __global__ void __launch_bounds__(256) frame_chain_kernel(const FrameParams p) {
             const int af = rev ? F - i : i, of = rev ? F - 1 - i : i;
             if (!rev || i > 0) {
                 const int64_t fi = (int64_t)bh * F + af;
+                const float *amat = p.amat + fi * K * K;
+                for (int e = tid; e < K * K; e += 256) sm.a[(e / K) * kAS + e % K] = amat[e];
                 const float dec = __expf(fmaxf(p.g_frame[((int64_t)b * F + af) * p.H + h], kLogGateMin));
+                __syncthreads();
                 float accv[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x) accv[x] = 0.f;
                 if (r < K) {
-                    const float *arow = p.amat + (fi * K + r) * K;
+                    const float *arow = sm.a + r * kAS;
+#pragma unroll 4
                     for (int a = 0; a < K; ++a) {
                         const float av = arow[a];
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) accv[x] = fmaf(av, sS[a * kCT + cs + x], accv[x]);
+                        const float4 s0 = *reinterpret_cast<const float4 *>(sm.s + a * kCT + cs);
+                        const float4 s1 = *reinterpret_cast<const float4 *>(sm.s + a * kCT + cs + 4);
+                        accv[0] = fmaf(av, s0.x, accv[0]);
+                        accv[1] = fmaf(av, s0.y, accv[1]);
+                        accv[2] = fmaf(av, s0.z, accv[2]);
+                        accv[3] = fmaf(av, s0.w, accv[3]);
+                        accv[4] = fmaf(av, s1.x, accv[4]);
+                        accv[5] = fmaf(av, s1.y, accv[5]);
+                        accv[6] = fmaf(av, s1.z, accv[6]);
+                        accv[7] = fmaf(av, s1.w, accv[7]);
                     }
                 }
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     const int j = j0 + cs + x;
-                    float bv = 0.f;
-                    if (r < K && j < Vt) bv = p.bmat[(fi * K + r) * Vt + j];
-                    sN[r * kCT + cs + x] = (r < K && j < Vt) ? fmaf(dec, accv[x], bv) : 0.f;
+                    const bool in = r < K && j < Vt;
+                    const float bv = in ? p.bmat[(fi * K + r) * Vt + j] : 0.f;
+                    sm.n[r * kCT + cs + x] = in ? fmaf(dec, accv[x], bv) : 0.f;
                 }
                 __syncthreads();
 #pragma unroll
-                for (int x = 0; x < 8; ++x) sS[r * kCT + cs + x] = sN[r * kCT + cs + x];
+                for (int x = 0; x < 8; ++x) sm.s[r * kCT + cs + x] = sm.n[r * kCT + cs + x];
                 __syncthreads();
             }
             // the state frame `of` reads, summed over the directions
@@ -189,7 +208,7 @@ __global__ void __launch_bounds__(256) frame_chain_kernel(const FrameParams p) {
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     const int j = j0 + cs + x;
-                    if (j < Vt) dst[j] = (rev && p.direction == 2) ? dst[j] + sS[r * kCT + cs + x] : sS[r * kCT + cs + x];
+                    if (j < Vt) dst[j] = (rev && p.direction == 2) ? dst[j] + sm.s[r * kCT + cs + x] : sm.s[r * kCT + cs + x];
                 }
             }
         }
@@ -197,7 +216,7 @@ __global__ void __launch_bounds__(256) frame_chain_kernel(const FrameParams p) {
 #pragma unroll
             for (int x = 0; x < 8; ++x) {
                 const int j = j0 + cs + x;
-                if (j < p.V) p.h_final[(((int64_t)b * p.H + h) * K + r) * p.V + j] = sS[r * kCT + cs + x];
+                if (j < p.V) p.h_final[(((int64_t)b * p.H + h) * K + r) * p.V + j] = sm.s[r * kCT + cs + x];
             }
         }
         __syncthreads();
@@ -279,14 +298,19 @@ __global__ void __launch_bounds__(128) frame_out_kernel(const FrameParams p) {
 
 }  // namespace
 
-cudaError_t launch_frame(const FrameParams &p, cudaStream_t st) {
-    const int ncb_gram = (kKP + p.Vt + 63) / 64;
-    frame_gram_kernel<<<dim3(p.B * p.H, p.F, ncb_gram), 128, 0, st>>>(p);
-    cudaError_t e = cudaGetLastError();
+cudaError_t launch_frame_gram(const FrameParams &p, cudaStream_t st) {
+    const int ncb = (kKP + p.Vt + 63) / 64;
+    frame_gram_kernel<<<dim3(p.B * p.H, p.F, ncb), 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st) {
+    const int bytes = (int)sizeof(ChainSmem);
+    cudaError_t e = cudaFuncSetAttribute(frame_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    frame_chain_kernel<<<dim3(p.B * p.H, (p.Vt + kCT - 1) / kCT), 256, 0, st>>>(p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    frame_chain_kernel<<<dim3(p.B * p.H, (p.Vt + kCT - 1) / kCT), 256, bytes, st>>>(p);
+    return cudaGetLastError();
+}
+cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st) {
     frame_out_kernel<<<dim3(p.B * p.H, p.T / kChunk, (p.Vt + 63) / 64), 128, 0, st>>>(p);
     return cudaGetLastError();
 }
