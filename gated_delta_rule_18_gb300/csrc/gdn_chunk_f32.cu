@@ -78,36 +78,69 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
         const int pos0 = c * kChunk;
         const int Lc = min(kChunk, si.len - pos0);
         __syncthreads();  // previous chunk fully consumed
-        // ---- load q, k (zero padded), v, beta, gates
-        for (int e = tid; e < kChunk * KP; e += kThreadsF) {
-            const int i = e / KP, d = e % KP;
-            float xq = 0.f, xk = 0.f, xg = 0.f;
-            if (i < Lc && d < K) {
-                const int tq = q_token(p.reverse, si.len, pos0 + i);
-                const int tk = kv_token(p.reverse, si.len, pos0 + i);
-                xq = q[si.b * p.qk_sb + (int64_t)(si.tstart + tq) * p.qk_st + hh * p.qk_sh + d];
-                if (tk >= 0) {
-                    xk = k[si.b * p.qk_sb + (int64_t)(si.tstart + tk) * p.qk_st + hh * p.qk_sh + d];
-                    if (PERKEY) xg = fmaxf(p.gk[((si.row0 + tk) * H + hh) * (int64_t)K + d], kLogGateMin);
+        // ---- load q, k (zero padded), v, beta, gates: 16-byte pieces, every
+        // load of a thread issued before its stores
+        constexpr int KV4 = KP / 4, NQ = kChunk * KV4 / kThreadsF;
+        {
+            float4 xq[NQ], xk[NQ], xg[NQ];
+#pragma unroll
+            for (int u = 0; u < NQ; ++u) {
+                const int e = tid + u * kThreadsF, i = e / KV4, d = (e % KV4) * 4;
+                xq[u] = xk[u] = xg[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < Lc && d < K) {
+                    const int tq = q_token(p.reverse, si.len, pos0 + i);
+                    const int tk = kv_token(p.reverse, si.len, pos0 + i);
+                    xq[u] = __ldg(reinterpret_cast<const float4 *>(
+                        q + si.b * p.qk_sb + (int64_t)(si.tstart + tq) * p.qk_st + hh * p.qk_sh + d));
+                    if (tk >= 0) {
+                        xk[u] = __ldg(reinterpret_cast<const float4 *>(
+                            k + si.b * p.qk_sb + (int64_t)(si.tstart + tk) * p.qk_st + hh * p.qk_sh + d));
+                        if (PERKEY)
+                            xg[u] = __ldg(reinterpret_cast<const float4 *>(
+                                p.gk + ((si.row0 + tk) * H + hh) * (int64_t)K + d));
+                    }
                 }
             }
-            sQ[i * QS + d] = xq;
-            sK[i * QS + d] = xk;
-            if (PERKEY) sGk[i * QS + d] = xg;
+#pragma unroll
+            for (int u = 0; u < NQ; ++u) {
+                const int e = tid + u * kThreadsF, i = e / KV4, d = (e % KV4) * 4;
+                const float qa[4] = {xq[u].x, xq[u].y, xq[u].z, xq[u].w};
+                const float ka[4] = {xk[u].x, xk[u].y, xk[u].z, xk[u].w};
+                const float ga[4] = {xg[u].x, xg[u].y, xg[u].z, xg[u].w};
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    sQ[i * QS + d + x] = qa[x];
+                    sK[i * QS + d + x] = ka[x];
+                    if (PERKEY) sGk[i * QS + d + x] = (i < Lc && d < K) ? fmaxf(ga[x], kLogGateMin) : 0.f;
+                }
+            }
         }
-        for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
-            const int i = e / kBVf, n = e % kBVf, col = v0 + n;
-            float xv = 0.f;
-            if (i < Lc) {
-                const int tk = kv_token(p.reverse, si.len, pos0 + i);
-                if (tk >= 0) {
-                    if (col < V)
-                        xv = v[si.b * p.v_sb + (int64_t)(si.tstart + tk) * p.v_st + hh * p.v_sh + col];
-                    else if (p.has_den && col == V)
-                        xv = 1.f;
+        {
+            constexpr int NV = kChunk * (kBVf / 4) / kThreadsF;
+            float4 xv[NV];
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const int e = tid + u * kThreadsF, i = e / (kBVf / 4), n = (e % (kBVf / 4)) * 4, col = v0 + n;
+                xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i < Lc) {
+                    const int tk = kv_token(p.reverse, si.len, pos0 + i);
+                    if (tk >= 0) {
+                        if (col < V)  // V is a multiple of 8: a group is wholly inside or at V
+                            xv[u] = __ldg(reinterpret_cast<const float4 *>(
+                                v + si.b * p.v_sb + (int64_t)(si.tstart + tk) * p.v_st + hh * p.v_sh + col));
+                        else if (p.has_den && col == V)
+                            xv[u].x = 1.f;
+                    }
                 }
             }
-            sV[i * VS + n] = xv;
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const int e = tid + u * kThreadsF, i = e / (kBVf / 4), n = (e % (kBVf / 4)) * 4;
+                sV[i * VS + n] = xv[u].x;
+                sV[i * VS + n + 1] = xv[u].y;
+                sV[i * VS + n + 2] = xv[u].z;
+                sV[i * VS + n + 3] = xv[u].w;
+            }
         }
         if (tid < kChunk) {
             const int i = tid;
@@ -177,18 +210,22 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
             }
             sA[i * AS + j] = a;
             sP[i * AS + j] = pm;
-            sT[i * AS + j] = (i == j) ? 1.f : 0.f;
         }
         __syncthreads();
-        // ---- T = (I + A)^{-1}: row i = e_i - sum_{j<i} A_ij T_j
-        for (int i = 1; i < kChunk; ++i) {
-            if (tid < i) {
-                const int cc = tid;
-                float acc = 0.f;
-                for (int j = cc; j < i; ++j) acc = fmaf(sA[i * AS + j], sT[j * AS + cc], acc);
-                sT[i * AS + cc] = -acc;
+        // ---- diagonal blocks T_II = (I + A_II)^{-1}, 16 x 16: one warp per
+        // block, lane = column, forward substitution in registers
+        if (warp < 4 && lane < 16) {
+            const int o = 16 * warp;
+            float t[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = (r == lane) ? 1.f : 0.f;
+#pragma unroll
+                for (int j = 0; j < r; ++j) acc = fmaf(-sA[(o + r) * AS + o + j], t[j], acc);
+                t[r] = acc;
             }
-            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(o + r) * AS + o + lane] = t[r];
         }
         // ---- Y = beta (V - (e^G . K) h) into sX
         for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
@@ -204,14 +241,28 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
             sX[i * VS + n] = sB[i] * (sV[i * VS + n] - acc);
         }
         __syncthreads();
-        // ---- v_new = T Y into sV
-        for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
-            const int i = e / kBVf, n = e % kBVf;
-            float acc = 0.f;
-            for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * AS + j], sX[j * VS + n], acc);
-            sV[i * VS + n] = acc;
+        // ---- v_new = (I + A)^{-1} Y into sV by block forward substitution,
+        // v_new_I = T_II (Y_I - sum_{M<I} A_IM v_new_M), four 16-row blocks
+        for (int I = 0; I < 4; ++I) {
+            const int o = 16 * I;
+            if (I > 0) {
+                for (int e = tid; e < 16 * kBVf; e += kThreadsF) {
+                    const int i = o + e / kBVf, n = e % kBVf;
+                    float acc = sX[i * VS + n];
+                    for (int j = 0; j < o; ++j) acc = fmaf(-sA[i * AS + j], sV[j * VS + n], acc);
+                    sX[i * VS + n] = acc;
+                }
+                __syncthreads();
+            }
+            for (int e = tid; e < 16 * kBVf; e += kThreadsF) {
+                const int i = o + e / kBVf, n = e % kBVf;
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc = fmaf(sT[i * AS + o + j], sX[(o + j) * VS + n], acc);
+                sV[i * VS + n] = acc;
+            }
+            __syncthreads();
         }
-        __syncthreads();
         // ---- o = (e^G . Q) h + P v_new
         for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
             const int i = e / kBVf, n = e % kBVf, col = v0 + n;
@@ -242,8 +293,13 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
             }
         }
         __syncthreads();
-        // ---- h <- e^{G_last} h + (e^{G_last - G} . K)^T v_new
+        // ---- h <- e^{G_last} h + (e^{G_last - G} . K)^T v_new (scalar gate:
+        // beta is no longer needed, its slots take the row factors)
         const int last = Lc - 1;
+        if (!PERKEY) {
+            if (tid < kChunk) sB[tid] = __expf(sG[last] - sG[tid]);
+            __syncthreads();
+        }
         for (int e = tid; e < KP * kBVf; e += kThreadsF) {
             const int d = e / kBVf, n = e % kBVf;
             float acc;
@@ -253,10 +309,8 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
                 for (int i = 0; i < Lc; ++i)
                     acc = fmaf(sK[i * QS + d] * __expf(gl - sGk[i * QS + d]), sV[i * VS + n], acc);
             } else {
-                const float gl = sG[last];
-                acc = __expf(gl) * sH[d * VS + n];
-                for (int i = 0; i < Lc; ++i)
-                    acc = fmaf(sK[i * QS + d] * __expf(gl - sG[i]), sV[i * VS + n], acc);
+                acc = __expf(sG[last]) * sH[d * VS + n];
+                for (int i = 0; i < Lc; ++i) acc = fmaf(sK[i * QS + d] * sB[i], sV[i * VS + n], acc);
             }
             sH[d * VS + n] = acc;
         }
