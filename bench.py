@@ -16,6 +16,7 @@ the time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -83,6 +84,13 @@ def path_work(w):
     return fl, by
 
 
+def seg_count(w):
+    """Segments per sequence of a segment-parallel workload (1 otherwise)."""
+    if not isinstance(w.segment_len, int) or w.segment_len <= 0:
+        return 1
+    return -(-(-(-w.T // C)) // (w.segment_len // C))
+
+
 def kernel_bytes(w, name):
     """Algorithmic bytes one launch of kernel `name` must move for workload
     w: its own inputs read once and outputs written once (shared tiles counted
@@ -94,10 +102,18 @@ def kernel_bytes(w, name):
     chunks = th / C
     if name == "intra_bf16":
         return th * ((2 * K + w.V) * e + 4 + gate + (3 * K + V + C) * 2) + chunks * K * 4
+    n_seg, bh = seg_count(w), w.n_seq * w.H
     if name == "state_tc":
         hs = (2 if w.h0 is not None else 1) * w.n_seq * w.H * w.K * w.V * 4
+        if n_seg > 1:  # each segment reads the state entering it
+            hs += (n_seg - (1 if w.h0 is not None else 0)) * bh * K * V * 4
         return th * ((3 * K + V + C) * 2 + w.V * e + (4 if w.bidirectional else 0)) \
             + chunks * K * 4 + (0 if w.bidirectional else hs)
+    if name == "seg_summary":  # every segment but the last: images in, (E, M) out
+        f = (n_seg - 1) / n_seg
+        return f * (th * ((3 * K + V + C) * 2) + chunks * K * 4) + (n_seg - 1) * bh * K * (V + K) * 4
+    if name == "seg_combine":  # (E, M) in, the entering states out
+        return (n_seg - 1) * bh * K * (V + K) * 4 + n_seg * bh * K * V * 4
     if name == "fused_f32":
         return th * ((2 * K + w.V) * e + 4 + gate + w.V * e) + w.n_seq * w.H * w.K * w.V * 4
     if name == "prep_rms":
@@ -266,6 +282,8 @@ def device_inputs(w, dev):
 
 def run_step(gdn, w, d, ws):
     extra = {}
+    if w.segment_len is not None:
+        extra["segment_len"] = w.segment_len
     if w.frame > 1:
         extra = dict(frame=w.frame, g_frame=d["g_frame"])
     elif w.bidirectional:
@@ -277,9 +295,23 @@ def run_step(gdn, w, d, ws):
                            with_final_state=not w.bidirectional, workspace=ws, **extra)
 
 
+def resolve_segments(gdn, w, dev):
+    """The workload with its segment length fixed for this device (the
+    library's choice for "auto")."""
+    import torch
+    if w.segment_len != "auto":
+        return w
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    return dataclasses.replace(w, segment_len=gdn.gdn_seg_choose(
+        w.B, w.T, w.H, w.K, w.V, w.bidirectional, n_sm))
+
+
 def workspace_for(gdn, w, dev):
     import torch
     dt = gdn.BF16 if w.dtype == "bf16" else gdn.F32
+    if w.segment_len is not None:
+        n = gdn.gdn_seg_workspace_size(w.B, w.T, w.H, w.K, w.V, w.bidirectional, w.segment_len)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
     n = gdn.gdn_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq, w.cu_seqlens is not None, dt,
                                w.bidirectional)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
@@ -407,6 +439,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--T", type=int, default=None,
                     help="override the token count of a dense workload (smaller profiling captures)")
+    ap.add_argument("--segment-len", type=int, default=None,
+                    help="segment-parallel state passing with this many tokens per segment "
+                         "(0: one pass per sequence); default: the workload's own setting")
     args = ap.parse_args()
     warmup = max(3, args.warmup)
 
@@ -429,6 +464,9 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
 
     w = workloads.build(args.workload, seed=rank, T=args.T)  # each replica its own data
+    if args.segment_len is not None:
+        w = dataclasses.replace(w, segment_len=args.segment_len or None)
+    w = resolve_segments(gdn, w, dev)
     d = device_inputs(w, dev)
     ws = workspace_for(gdn, w, dev)
     stream = torch.cuda.current_stream()
@@ -493,7 +531,9 @@ def main():
         "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "K": w.K,
                    "V": w.V, "chunk": C, "tokens_per_step_per_gpu": tokens,
                    "l2": "inputs larger than L2 (no flush)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   **({"segment_len": w.segment_len, "segments": seg_count(w)}
+                      if w.segment_len is not None else {})},
         "tflops": fl * world / step_s / 1e12,
         "path_roofline": {"bound": "hbm" if by / peaks["hbm_gbs"] > fl / peaks["bf16_tflops"] / 1e3
                           else "tensor", "min_bytes": by, "flops": fl,

@@ -75,6 +75,16 @@ def lib():
     L.gdn_frame_fwd.restype = I
     L.gdn_frame_fwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, TensorDesc, P, P,
                                 I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+    L.gdn_seg_workspace_size.restype = ctypes.c_size_t
+    L.gdn_seg_workspace_size.argtypes = [I] * 7
+    L.gdn_chunk_fwd_seg.restype = I
+    L.gdn_chunk_fwd_seg.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, TensorDesc, P,
+                                    P, I, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+    L.gdn_seg_choose.restype = I
+    L.gdn_seg_choose.argtypes = [I] * 7
+    L.gdn_state_summary.restype = I
+    L.gdn_state_summary.argtypes = [P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, I, I, I, I, I,
+                                    I, I, P, ctypes.c_size_t, P]
     L.gdn_merge.restype = I
     L.gdn_merge.argtypes = [P, TensorDesc, P, P, TensorDesc, P, TensorDesc, I, I, I, I, F, P]
     L.gdn_last_device_error.restype = I
@@ -197,6 +207,70 @@ def gdn_chunk_fwd(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None, out=
     return out
 
 
+def gdn_seg_workspace_size(B, T, H, K, V, with_den, segment_len) -> int:
+    return int(lib().gdn_seg_workspace_size(B, T, H, K, V, int(bool(with_den)), int(segment_len)))
+
+
+def gdn_seg_choose(B, T, H, K, V, with_den, n_sm) -> int:
+    """segment_len for gdn_chunk_fwd_seg on a GPU with n_sm SMs (host
+    arithmetic in the library; see include/gdn.h)."""
+    return int(lib().gdn_seg_choose(B, T, H, K, V, int(bool(with_den)), int(n_sm)))
+
+
+def gdn_chunk_fwd_seg(q, k, v, beta, segment_len, g=None, gk=None, h0=None, out=None,
+                      h_final=None, den=None, reverse=False, accumulate=False,
+                      qk_l2norm=False, workspace=None, stream=None, out_dtype=None):
+    """gdn_chunk_fwd with segment-parallel state passing (dense bf16
+    batches; see include/gdn.h). segment_len: tokens per segment, a multiple
+    of 64. Returns out."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    for name, t in (("beta", beta), ("g", g), ("gk", gk), ("h0", h0), ("h_final", h_final),
+                    ("den", den)):
+        _f32(t, name)
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=out_dtype or q.dtype, device=q.device)
+    need = gdn_seg_workspace_size(B, T, H, K, V, den is not None, segment_len)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    flags = (ACCUMULATE if accumulate else 0) | (QK_L2NORM if qk_l2norm else 0)
+    st = lib().gdn_chunk_fwd_seg(
+        _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta),
+        _ptr(h0), _ptr(out), _desc(out), _ptr(h_final), _ptr(den), B, T, H, K, V, 64,
+        int(bool(reverse)), flags, int(segment_len), _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_chunk_fwd_seg")
+    return out
+
+
+def gdn_state_summary(k, v, beta, segment_len, g=None, gk=None, with_transition=True,
+                      qk_l2norm=False, workspace=None, stream=None):
+    """Per-segment affine summaries (see include/gdn.h): returns
+    (state_ext (n_seg, B, H, K, V), transition (n_seg, B, H, K, K) or None),
+    fp32, with h_out = transition @ h_in + state_ext per segment."""
+    torch = _torch()
+    B, T, H, K = k.shape
+    V = v.shape[3]
+    for name, t in (("beta", beta), ("g", g), ("gk", gk)):
+        _f32(t, name)
+    n_seg = -(-T // int(segment_len)) if segment_len > 0 else 0
+    ext = torch.empty((n_seg, B, H, K, V), dtype=torch.float32, device=k.device)
+    tr = (torch.empty((n_seg, B, H, K, K), dtype=torch.float32, device=k.device)
+          if with_transition else None)
+    need = gdn_workspace_size(B, T, H, K, V, B, 0, BF16, 0)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=k.device)
+    st = lib().gdn_state_summary(
+        _ptr(k), _desc(k), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta), _ptr(ext), _ptr(tr),
+        B, T, H, K, V, 64, int(segment_len), QK_L2NORM if qk_l2norm else 0, _ptr(workspace),
+        workspace.numel(), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_state_summary")
+    return ext, tr
+
+
 def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqlens=None,
                           h_final=None, den=None, reverse=False, accumulate=False,
                           qk_l2norm=False, stream=None):
@@ -278,7 +352,7 @@ def gdn_last_device_error(workspace, stream=None) -> int:
 def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                 prep="l2", bidirectional=False, with_final_state=False, workspace=None,
                 stream=None, backward=None, merge=False, gate=None, eps=1e-6, frame=1,
-                g_frame=None):
+                g_frame=None, segment_len=None):
     """The whole forward: q/k prep, then the causal scan, or the causal plus
     the reverse scan summed with the denominator (bidirectional).
 
@@ -292,6 +366,9 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
     merge: also return "merged" = out / (den + eps) * silu(gate) (gdn_merge).
     frame > 1: the frame-causal form (gdn_frame_fwd) with per-frame log
     decays g_frame (B, T // frame, H) in place of g.
+    segment_len: segment-parallel state passing (gdn_chunk_fwd_seg; dense
+    bf16 inputs) with segments of this many tokens, or "auto" for
+    gdn_seg_choose's pick on this device.
     Returns a dict with "out" and, as requested, "h_final" / "den" /
     "merged" / "q_inv_rms" / "k_inv_rms"."""
     torch = _torch()
@@ -336,22 +413,31 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                                    workspace=workspace, stream=stream)
         res["den"] = den
         return res
+    if segment_len is not None:
+        if cu_seqlens is not None or q.dtype != torch.bfloat16:
+            raise ValueError("segment-parallel state passing takes dense bf16 inputs")
+        if segment_len == "auto":
+            n_sm = torch.cuda.get_device_properties(q.device).multi_processor_count
+            segment_len = gdn_seg_choose(B, T, H, K, v.shape[3], bidirectional, n_sm)
+
+    def scan(q, k, v, beta, g, gk, **kw):
+        if segment_len:
+            return gdn_chunk_fwd_seg(q, k, v, beta, segment_len, g=g, gk=gk, qk_l2norm=fuse,
+                                     workspace=workspace, stream=stream, **kw)
+        return gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, cu_seqlens=cu_seqlens, qk_l2norm=fuse,
+                             workspace=workspace, stream=stream, **kw)
+
     if not bidirectional:
         hf = (torch.empty((n_seq, H, K, v.shape[3]), dtype=torch.float32, device=q.device)
               if with_final_state else None)
-        res["out"] = gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, h0=h0, cu_seqlens=cu_seqlens,
-                                   h_final=hf, qk_l2norm=fuse, workspace=workspace,
-                                   stream=stream)
+        res["out"] = scan(q, k, v, beta, g, gk, h0=h0, h_final=hf)
         if hf is not None:
             res["h_final"] = hf
         return res
     den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
-    out = gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, cu_seqlens=cu_seqlens, den=den,
-                        qk_l2norm=fuse, workspace=workspace, stream=stream)
-    gdn_chunk_fwd(bw.get("q", q), bw.get("k", k), bw.get("v", v), bw.get("beta", beta),
-                  g=bw.get("g", g), gk=bw.get("gk", gk), cu_seqlens=cu_seqlens, den=den, out=out,
-                  reverse=True, accumulate=True, qk_l2norm=fuse, workspace=workspace,
-                  stream=stream)
+    out = scan(q, k, v, beta, g, gk, den=den)
+    scan(bw.get("q", q), bw.get("k", k), bw.get("v", v), bw.get("beta", beta), bw.get("g", g),
+         bw.get("gk", gk), den=den, out=out, reverse=True, accumulate=True)
     res["out"], res["den"] = out, den
     if merge:
         res["merged"] = gdn_merge(out, den, gate=gate, eps=eps, stream=stream)

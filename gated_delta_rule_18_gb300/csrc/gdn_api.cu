@@ -16,11 +16,11 @@ using gdn::FwdParams;
 
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
-    KFrameOut, KNumKinds
+    KFrameOut, KSegSummary, KSegCombine, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
-                                     "frame_chain", "frame_out"};
+                                     "frame_chain", "frame_out", "seg_summary", "seg_combine"};
 
 struct Profiler {
     std::mutex mu;
@@ -186,19 +186,25 @@ gdn_status gdn_prep(const void *x, gdn_tensor_desc xd, void *y, gdn_tensor_desc 
     }));
 }
 
-gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
-                         gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
-                         const float *h0, const int32_t *cu_seqlens, int n_seq, void *out,
-                         gdn_tensor_desc od, float *h_final, float *den_out, int B, int T,
-                         int H, int K, int V, int chunk, int reverse, int flags,
-                         void *workspace, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks and the launch parameter block shared by gdn_chunk_fwd,
+// gdn_chunk_fwd_seg and gdn_state_summary; on GDN_OK, L and p describe the
+// problem (workspace pointers are bound by bind_ws). With need_out unset the
+// output may be NULL (summary passes write none).
+gdn_status fwd_setup(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                     gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
+                     const float *h0, const int32_t *cu_seqlens, int n_seq, void *out,
+                     gdn_tensor_desc od, float *h_final, float *den_out, int B, int T, int H,
+                     int K, int V, int chunk, int reverse, int flags, bool need_out, Ws &L,
+                     gdn::FwdParams &p) {
     // With no tokens the per-token tensors may be empty (NULL); only the
     // state pass-through h0 -> h_final runs.
     const bool empty = T == 0;
-    if (!empty && (!q || !k || !v || !beta || !out)) return GDN_ERR_NULL;
+    if (!empty && (!q || !k || !v || !beta || (need_out && !out))) return GDN_ERR_NULL;
     if (g && gk) return GDN_ERR_UNSUPPORTED;
     if (!empty && !g && !gk) return GDN_ERR_NULL;
-    if (!workspace) return GDN_ERR_WORKSPACE;
     if (chunk != gdn::kChunk) return GDN_ERR_SHAPE;
     if ((flags & ~(GDN_ACCUMULATE | GDN_QK_L2NORM)) != 0) return GDN_ERR_UNSUPPORTED;
     if (!dtype_ok(qkd.dtype) || !dtype_ok(vd.dtype) || !dtype_ok(od.dtype))
@@ -221,14 +227,9 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
                           (const void *)h0, (const void *)h_final, (const void *)den_out,
                           (const void *)cu_seqlens})
         if (f && (reinterpret_cast<uintptr_t>(f) & 3)) return GDN_ERR_LAYOUT;
-    Ws L;
     if (!ws_layout(B, T, H, K, V, n_seq, varlen, qkd.dtype, den_out != nullptr, L))
         return GDN_ERR_SHAPE;
-    if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
-        return GDN_ERR_WORKSPACE;
-
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    FwdParams p{};
+    p = gdn::FwdParams{};
     p.q = q;
     p.k = k;
     p.v = v;
@@ -261,19 +262,69 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     p.l2norm = (flags & GDN_QK_L2NORM) ? 1 : 0;
     p.has_den = den_out != nullptr;
     p.Vt = L.Vt;
+    p.max_chunks = L.max_chunks;
+    p.n_vt = L.n_vt;
+    return GDN_OK;
+}
+
+void bind_ws(unsigned char *ws, const Ws &L, gdn::FwdParams &p) {
     p.err = reinterpret_cast<int *>(ws + L.err);
     p.n_chunks = reinterpret_cast<int *>(ws + L.err) + 1;
     p.chunk_tab = reinterpret_cast<int2 *>(ws + L.tab);
     p.seq_chunk0 = reinterpret_cast<int *>(ws + L.seq0);
-    p.max_chunks = L.max_chunks;
     p.w_img = ws + L.w;
     p.qg_img = ws + L.qg;
     p.kg_img = ws + L.kg;
     p.p_img = ws + L.pm;
     p.u_img = ws + L.u;
     p.dec = reinterpret_cast<float *>(ws + L.dec);
-    p.n_vt = L.n_vt;
+}
+
+bool ws_ok(const void *workspace, size_t ws_bytes, size_t need) {
+    return workspace && ws_bytes >= need && (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) == 0;
+}
+
+// segment-parallel sections after the forward workspace: the summaries and
+// the state entering each segment, fp32
+struct SegWs {
+    size_t ext, tr, hin, total;
+    int seg_chunks, n_seg;
+};
+bool seg_layout(const Ws &L, int B, int T, int H, int K, int segment_len, SegWs &S) {
+    if (segment_len < gdn::kChunk || segment_len % gdn::kChunk != 0) return false;
+    S.seg_chunks = segment_len / gdn::kChunk;
+    const int nall = (T + gdn::kChunk - 1) / gdn::kChunk;
+    S.n_seg = (nall + S.seg_chunks - 1) / S.seg_chunks;
+    const size_t per = (size_t)S.n_seg * B * H * K * 4;
+    size_t off = L.total;
+    S.ext = off;
+    off = align_up(off + per * L.Vt);
+    S.tr = off;
+    off = align_up(off + per * K);
+    S.hin = off;
+    off = align_up(off + per * L.Vt);
+    S.total = off;
+    return true;
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                         gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
+                         const float *h0, const int32_t *cu_seqlens, int n_seq, void *out,
+                         gdn_tensor_desc od, float *h_final, float *den_out, int B, int T,
+                         int H, int K, int V, int chunk, int reverse, int flags,
+                         void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    Ws L;
+    gdn::FwdParams p;
+    const gdn_status st = fwd_setup(q, k, qkd, v, vd, g, gk, beta, h0, cu_seqlens, n_seq, out, od,
+                                    h_final, den_out, B, T, H, K, V, chunk, reverse, flags, true, L, p);
+    if (st != GDN_OK) return st;
+    if (!ws_ok(workspace, ws_bytes, L.total)) return GDN_ERR_WORKSPACE;
+    bind_ws(static_cast<unsigned char *>(workspace), L, p);
     const int perkey = gk != nullptr;
+    const int varlen = cu_seqlens != nullptr;
 
     cudaError_t e = cudaSuccess;
     if (varlen) e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
@@ -287,6 +338,121 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
         if (e != cudaSuccess) return GDN_ERR_CUDA;
     }
     e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
+    return cuda_status(e);
+}
+
+size_t gdn_seg_workspace_size(int B, int T, int H, int K, int V, int with_den, int segment_len) {
+    Ws L;
+    SegWs S;
+    if (!ws_layout(B, T, H, K, V, B, 0, GDN_BF16, with_den, L)) return 0;
+    if (!seg_layout(L, B, T, H, K, segment_len, S)) return 0;
+    return S.total;
+}
+
+gdn_status gdn_chunk_fwd_seg(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                             gdn_tensor_desc vd, const float *g, const float *gk,
+                             const float *beta, const float *h0, void *out, gdn_tensor_desc od,
+                             float *h_final, float *den_out, int B, int T, int H, int K, int V,
+                             int chunk, int reverse, int flags, int segment_len, void *workspace,
+                             size_t ws_bytes, cudaStream_t stream) {
+    if (!workspace) return GDN_ERR_WORKSPACE;
+    Ws L;
+    gdn::FwdParams p;
+    gdn_status st = fwd_setup(q, k, qkd, v, vd, g, gk, beta, h0, nullptr, B, out, od, h_final,
+                              den_out, B, T, H, K, V, chunk, reverse, flags, true, L, p);
+    if (st != GDN_OK) return st;
+    if (qkd.dtype != GDN_BF16) return GDN_ERR_DTYPE;  // the fp32 path is one fused kernel
+    SegWs S;
+    if (!seg_layout(L, B, T, H, K, segment_len, S)) return GDN_ERR_SHAPE;
+    if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    bind_ws(ws, L, p);
+    const int perkey = gk != nullptr;
+    cudaError_t e = cudaSuccess;
+    if (L.max_chunks > 0) {
+        e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, perkey, stream); });
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    if (S.n_seg <= 1) {  // one segment: the plain state pass
+        e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
+        return cuda_status(e);
+    }
+    p.seg_chunks = S.seg_chunks;
+    p.sum_ext = reinterpret_cast<float *>(ws + S.ext);
+    p.sum_tr = reinterpret_cast<float *>(ws + S.tr);
+    p.n_kt = (K + 63) / 64;
+    // 1. every segment's summary but the last one's, in parallel
+    gdn::FwdParams ps = p;
+    ps.summary = 2;
+    e = launch(KSegSummary, stream, [&] { return gdn::launch_state_tc(ps, stream); });
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    // 2. the chain over segments
+    gdn::SegParams c{};
+    c.h0 = h0;
+    c.sum_ext = p.sum_ext;
+    c.sum_tr = p.sum_tr;
+    c.h_in = reinterpret_cast<float *>(ws + S.hin);
+    c.n_bh = B * H, c.K = K, c.V = V, c.Vt = L.Vt, c.n_seg = S.n_seg;
+    e = launch(KSegCombine, stream, [&] { return gdn::launch_seg_combine(c, stream); });
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    // 3. every segment again from its entering state, with the outputs
+    p.h_in = c.h_in;
+    e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
+    return cuda_status(e);
+}
+
+int gdn_seg_choose(int B, int T, int H, int K, int V, int with_den, int n_sm) {
+    if (B < 1 || T < 1 || H < 1 || K < 1 || V < 1 || n_sm < 1) return 0;
+    const int64_t nall = (T + gdn::kChunk - 1) / gdn::kChunk;
+    const int64_t bh = (int64_t)B * H, n_vt = (V + (with_den ? 1 : 0) + 63) / 64, n_kt = (K + 63) / 64;
+    // time in chunk steps of one state-kernel CTA (one CTA per SM): the
+    // summary pass, the chain (about one step per segment) and the re-run
+    auto cost = [&](int64_t n_seg, int64_t seg) {
+        if (n_seg == 1) return ((bh * n_vt + n_sm - 1) / n_sm) * nall;
+        return ((bh * (n_vt + n_kt) * (n_seg - 1) + n_sm - 1) / n_sm) * seg + n_seg +
+               ((bh * n_vt * n_seg + n_sm - 1) / n_sm) * seg;
+    };
+    int64_t best_seg = nall, best = cost(1, nall);
+    for (int64_t n = 2; n <= 256 && n <= nall; ++n) {
+        const int64_t seg = (nall + n - 1) / n;
+        const int64_t n_seg = (nall + seg - 1) / seg;
+        const int64_t c = cost(n_seg, seg);
+        if (c < best) best = c, best_seg = seg;
+    }
+    return (int)(best_seg * gdn::kChunk);
+}
+
+gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v, gdn_tensor_desc vd,
+                             const float *g, const float *gk, const float *beta, float *state_ext,
+                             float *transition, int B, int T, int H, int K, int V, int chunk,
+                             int segment_len, int flags, void *workspace, size_t ws_bytes,
+                             cudaStream_t stream) {
+    if (!workspace) return GDN_ERR_WORKSPACE;
+    if (T > 0 && !state_ext) return GDN_ERR_NULL;
+    if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(state_ext) & 3) || (reinterpret_cast<uintptr_t>(transition) & 3))
+        return GDN_ERR_LAYOUT;
+    if (kd.dtype != GDN_BF16) return GDN_ERR_DTYPE;
+    Ws L;
+    gdn::FwdParams p;
+    // the keys stand in for the queries: the summary reads no query
+    gdn_status st = fwd_setup(k, k, kd, v, vd, g, gk, beta, nullptr, nullptr, B, nullptr,
+                              gdn_tensor_desc{GDN_F32, 0, 0, 0, 0}, nullptr, nullptr, B, T, H, K,
+                              V, chunk, 0, flags, false, L, p);
+    if (st != GDN_OK) return st;
+    SegWs S;
+    if (!seg_layout(L, B, T, H, K, segment_len, S)) return GDN_ERR_SHAPE;
+    if (!ws_ok(workspace, ws_bytes, L.total)) return GDN_ERR_WORKSPACE;
+    if (T == 0) return GDN_OK;
+    bind_ws(static_cast<unsigned char *>(workspace), L, p);
+    cudaError_t e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, gk != nullptr, stream); });
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    p.seg_chunks = S.seg_chunks;
+    p.summary = 1;
+    p.sum_ext = state_ext;
+    p.sum_tr = transition;
+    p.n_kt = transition ? (K + 63) / 64 : 0;
+    e = launch(KSegSummary, stream, [&] { return gdn::launch_state_tc(p, stream); });
     return cuda_status(e);
 }
 

@@ -50,6 +50,18 @@ struct FwdParams {
     unsigned char *w_img, *qg_img, *kg_img, *p_img, *u_img;
     float *dec;       // [H][max_chunks][kKP] chunk decay e^{G_last}
     int n_vt;         // 64-column value tiles (ceil(Vt / 64))
+    // Segment-parallel state passing (dense batches): the chunks of every
+    // sequence are cut into segments of seg_chunks chunks (0: one segment),
+    // one state-kernel CTA per segment (grid z). With summary set the kernel
+    // emits each segment's affine summary h_out = M h_in + E instead of
+    // outputs: value tiles run from h = 0 (E), n_kt extra 64-column tiles run
+    // the same recurrence with u = 0 from h = I (the transition M). Otherwise
+    // segment s starts from h_in[s] when h_in is given. summary 1 covers every
+    // segment and stores M; summary 2 all but the last and stores M^T.
+    int seg_chunks, summary, n_kt;
+    float *sum_ext;      // (segments, n_seq * H, K, Vt)
+    float *sum_tr;       // (segments, n_seq * H, K, K)
+    const float *h_in;   // (segments, n_seq * H, K, Vt)
 };
 
 // ----------------------------------------------------- operand images -------
@@ -282,6 +294,17 @@ cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
 cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
+
+// The serial step of segment-parallel state passing: per (sequence x head),
+// h_in[0] = h0 (or 0) and h_in[s+1] = M_s h_in[s] + E_s, fp32.
+struct SegParams {
+    const float *h0;       // (n_bh, K, V) or NULL
+    const float *sum_ext;  // (n_seg, n_bh, K, Vt)
+    const float *sum_tr;   // (n_seg, n_bh, K, K), each M_s transposed
+    float *h_in;           // (n_seg, n_bh, K, Vt)
+    int n_bh, K, V, Vt, n_seg;
+};
+cudaError_t launch_seg_combine(const SegParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);
 cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, void *y,
                         int64_t ysb, int64_t yst, int64_t ysh, int B, int T, int H, int D,

@@ -97,11 +97,19 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const int H = p.H, K = p.K, V = p.V;
     const int s = blockIdx.x / H, hh = blockIdx.x % H;
     const int vt = blockIdx.y, v0 = vt * kBVt;
+    const int seg = blockIdx.z;
+    // a transition tile of a summary pass: columns t0 .. t0+63 of M
+    const bool trt = p.summary && vt >= p.n_vt;
+    const int t0 = trt ? (vt - p.n_vt) * kBVt : 0;
     if (p.cu_seqlens && *p.n_chunks < 0) return;
     SeqInfo si;
     if (!seq_info(p, s, si)) return;
-    const int nchunks = (si.len + kChunk - 1) / kChunk;
-    const int gc0 = p.cu_seqlens ? p.seq_chunk0[s] : s * ((p.T + kChunk - 1) / kChunk);
+    const int nall = (si.len + kChunk - 1) / kChunk;
+    // this CTA's chunks: cb .. cb + nchunks - 1 of the sequence
+    const int cb = p.seg_chunks ? seg * p.seg_chunks : 0;
+    const int nchunks = p.seg_chunks ? max(0, min(p.seg_chunks, nall - cb)) : nall;
+    const int64_t bh = (int64_t)s * H + hh, n_bh = (int64_t)p.n_seq * H;
+    const int gc0 = (p.cu_seqlens ? p.seq_chunk0[s] : s * ((p.T + kChunk - 1) / kChunk)) + cb;
     const uint32_t sbase = smem_u32(sm);
     const uint32_t b_st[2] = {smem_u32(&bar_stage[0]), smem_u32(&bar_stage[1])};
     const uint32_t b_of[2] = {smem_u32(&bar_ofree[0]), smem_u32(&bar_ofree[1])};
@@ -133,6 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         *reinterpret_cast<uint4 *>(sm + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4 *>(sm + Lay::stage + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
     }
+    if (trt)  // u = 0 for the transition columns: the u ring stays zero
+        for (int e = tid; e < (int)(3 * kImgU / 16); e += kThreads)
+            *reinterpret_cast<uint4 *>(sm + Lay::u + 16 * e) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -146,7 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         const int st = c & 1;
         const uint32_t dst = sbase + st * Lay::stage;
         const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b_st[st]), "r"(Lay::copy_bytes)
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b_st[st]),
+                     "r"(Lay::copy_bytes - (trt ? kImgU : 0u))
                      : "memory");
         const void *src[6] = {p.w_img + gch * kImgW, p.qg_img + gch * kImgW, p.kg_img + gch * kImgW,
                               p.p_img + gch * kImgP, p.u_img + (gch * p.n_vt + vt) * kImgU, p.dec + gch * kKP};
@@ -154,12 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                                   sbase + Lay::u + (uint32_t)(c % 3) * kImgU, sbase + Lay::dec + (uint32_t)(c % 4) * kDecB};
         const uint32_t len[6] = {kImgW, kImgW, kImgW, kImgP, kImgU, kDecB};
 #pragma unroll
-        for (int x = 0; x < 6; ++x)
+        for (int x = 0; x < 6; ++x) {
+            if (x == 4 && trt) continue;  // transition tiles read no u
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                     dsts[x]),
                 "l"(src[x]), "r"(len[x]), "r"(b_st[st])
                 : "memory");
+        }
     };
     // v_new = u - Xw for token row i, columns c0 .. c0+31 (warps 0,1 / 4,5)
     // token row i, columns c0 .. c0+31 of chunk c's u, read ahead of the
@@ -204,9 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         // ------------------------------------------------ recurrence warps
         const int r = tid;
         float h[64];
+        if (p.summary) {  // E from h = 0, M from h = I
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-            h[c] = (p.h0 && r < K && v0 + c < V) ? p.h0[(((int64_t)s * H + hh) * K + r) * V + v0 + c] : 0.f;
+            for (int c = 0; c < 64; ++c) h[c] = (trt && r < K && r == t0 + c) ? 1.f : 0.f;
+        } else if (p.h_in) {
+            const float *src = p.h_in + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) h[c] = (r < K && v0 + c < p.Vt) ? src[v0 + c] : 0.f;
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                h[c] = (p.h0 && r < K && v0 + c < V) ? p.h0[(bh * K + r) * V + v0 + c] : 0.f;
+        }
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const int st = c & 1;
@@ -243,10 +266,23 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             }
             tc_fence_before();
         }
-        if (ok && p.h_final && r < K) {
+        if (ok && p.summary && r < K) {
+            if (trt) {  // summary 1: M row-major; summary 2: M^T (the chain's operand)
+                float *dst = p.sum_tr + ((int64_t)seg * n_bh + bh) * K * K;
+                const int64_t rs = p.summary == 2 ? 1 : K, cs = p.summary == 2 ? K : 1;
+#pragma unroll
+                for (int x = 0; x < 64; ++x)
+                    if (t0 + x < K) dst[r * rs + (t0 + x) * cs] = h[x];
+            } else {
+                float *dst = p.sum_ext + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt;
+#pragma unroll
+                for (int x = 0; x < 64; ++x)
+                    if (v0 + x < p.Vt) dst[v0 + x] = h[x];
+            }
+        } else if (ok && p.h_final && r < K && cb + nchunks == nall) {
 #pragma unroll
             for (int x = 0; x < 64; ++x)
-                if (v0 + x < V) p.h_final[(((int64_t)s * H + hh) * K + r) * V + v0 + x] = h[x];
+                if (v0 + x < V) p.h_final[(bh * K + r) * V + v0 + x] = h[x];
         }
     } else if (warp == 4 || warp == 5) {
         // ------------------------------------- v_new helpers (columns 32..63)
@@ -334,9 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             tc_ld64(tmem + lane_base + kColD + par * 64, t);
             tc_fence_before();
             arrive(b_of[c & 1]);
-            const int pos0 = c * kChunk;
+            const int pos0 = (cb + c) * kChunk;
             const int Lc = min(kChunk, si.len - pos0);
-            if (!ok || i >= Lc) continue;
+            if (!ok || i >= Lc || p.summary) continue;
             const int tq = q_token(p.reverse, si.len, pos0 + i);
             const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
 #pragma unroll
@@ -392,7 +428,11 @@ cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_seq * p.H, p.n_vt);
+    const int nall = (p.T + kChunk - 1) / kChunk;
+    // summary 2: every segment but the last (whose summary nothing reads)
+    const int nseg = p.seg_chunks ? max(1, (nall + p.seg_chunks - 1) / p.seg_chunks) - (p.summary == 2 ? 1 : 0) : 1;
+    if (nseg < 1) return cudaSuccess;
+    dim3 grid(p.n_seq * p.H, p.n_vt + (p.summary ? p.n_kt : 0), nseg);
     state_tc_kernel<<<grid, kThreads, Lay::bytes, st>>>(p);
     return cudaGetLastError();
 }

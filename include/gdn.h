@@ -189,6 +189,69 @@ gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k,
                                  int H, int K, int V, int chunk, int reverse,
                                  int flags, cudaStream_t stream);
 
+/*
+ * gdn_seg_workspace_size / gdn_chunk_fwd_seg -- gdn_chunk_fwd for dense
+ * batches with segment-parallel state passing (hyper-parallel coverage_diff
+ * page: `kda_state_summary_forward_from_prepared` forms a piece's summary
+ * (state_ext, transition), the initial state of a piece is the previous
+ * piece's final state transition . h_in + state_ext, and
+ * `chunk_gated_delta_rule_fwd_h` re-runs the piece from it). Each sequence
+ * is cut into segments of segment_len tokens; every segment's summary
+ * (E = the segment's state from h = 0, M = its transition) is formed in
+ * parallel, a short fp32 chain gives the state entering each segment
+ * (h_in[0] = h0, h_in[s+1] = M_s h_in[s] + E_s), and every segment is then
+ * re-run from its h_in in parallel, writing the outputs. The result is the
+ * token recurrence's, as for gdn_chunk_fwd (rounding differs: the states
+ * entering segments are formed in fp32 from fp32 summaries). It pays when
+ * B * H * ceil((V + den) / 64) is small next to the SM count.
+ *   Arguments as gdn_chunk_fwd with cu_seqlens = NULL and n_seq = B; bf16
+ *   q/k/v only (GDN_ERR_DTYPE for fp32). segment_len: a positive multiple of
+ *   64 (GDN_ERR_SHAPE otherwise); a sequence of at most segment_len tokens
+ *   runs as gdn_chunk_fwd does.
+ *   workspace: >= gdn_seg_workspace_size() bytes, 256-byte aligned.
+ */
+size_t gdn_seg_workspace_size(int B, int T, int H, int K, int V, int with_den,
+                              int segment_len);
+gdn_status gdn_chunk_fwd_seg(const void *q, const void *k, gdn_tensor_desc qkd,
+                             const void *v, gdn_tensor_desc vd, const float *g,
+                             const float *gk, const float *beta,
+                             const float *h0, void *out, gdn_tensor_desc od,
+                             float *h_final, float *den_out, int B, int T,
+                             int H, int K, int V, int chunk, int reverse,
+                             int flags, int segment_len, void *workspace,
+                             size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * gdn_seg_choose -- a segment_len for gdn_chunk_fwd_seg on a GPU with n_sm
+ * SMs (host arithmetic only, no CUDA call): the length that minimises the
+ * estimated time of the summary pass, the chain and the re-run, counted in
+ * chunk steps of state-kernel CTAs at one per SM. A result >= T means the
+ * plain one-segment pass is estimated fastest. Returns 0 for bad sizes.
+ */
+int gdn_seg_choose(int B, int T, int H, int K, int V, int with_den, int n_sm);
+
+/*
+ * gdn_state_summary -- the affine summary of each segment of each sequence
+ * (hyper-parallel coverage_diff page, `kda_state_summary_forward_from_prepared`
+ * returning state_ext and transition): for segment s of segment_len tokens
+ * (the last one ragged), the state after the segment is
+ *   h_out = transition_s . h_in + state_ext_s
+ * for any state h_in entering it (h in [K, V] orientation, causal scan).
+ *   k: (B, T, H, K) bf16, kd; v: (B, T, H, V) bf16, vd; g / gk / beta as for
+ *   gdn_chunk_fwd. flags: GDN_QK_L2NORM (normalise k) or 0.
+ *   state_ext: (n_seg, B, H, K, V) fp32 output; transition: (n_seg, B, H, K,
+ *   K) fp32 output or NULL (not formed); n_seg = ceil(T / segment_len).
+ *   segment_len: a positive multiple of 64.
+ *   workspace: >= gdn_workspace_size(B, T, H, K, V, B, 0, GDN_BF16, 0) bytes.
+ */
+gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
+                             gdn_tensor_desc vd, const float *g,
+                             const float *gk, const float *beta,
+                             float *state_ext, float *transition, int B, int T,
+                             int H, int K, int V, int chunk, int segment_len,
+                             int flags, void *workspace, size_t ws_bytes,
+                             cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 /*
  * gdn_merge -- the bidirectional merge (SANA `fused_gdn.py` page,

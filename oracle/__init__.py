@@ -157,6 +157,36 @@ def den(q, k, beta, g=None, gk=None, cu_seqlens=None, reverse=False,
     return np.ascontiguousarray(out[..., 0].transpose(0, 2, 1))
 
 
+def state_summary(k, v, beta, segment_len, g=None, gk=None, threads=None):
+    """Affine summary of every segment of every sequence (hyper-parallel
+    coverage_diff page, `kda_state_summary_forward_from_prepared` returning
+    state_ext and transition): over segment s (tokens s*L .. s*L+L-1, the last
+    one ragged) the causal token recurrence maps the entering state h to
+    M_s h + E_s. The recurrence is linear in the state with v entering only
+    additively, so E_s is the scan's final state from h = 0, and column j of
+    M_s is the final state of the same scan with v = 0 from h = e_j.
+    Dense only: k (B, T, H, K); v (B, T, H, V); beta, g (B, T, H); gk
+    (B, T, H, K). Returns (ext (n_seg, B, H, K, V), tr (n_seg, B, H, K, K))
+    in float64."""
+    k, v, beta, g, gk = map(_f64, (k, v, beta, g, gk))
+    B, T, H, K = k.shape
+    V = v.shape[-1]
+    L = int(segment_len)
+    n_seg = -(-T // L)
+    ext = np.zeros((n_seg, B, H, K, V))
+    tr = np.zeros((n_seg, B, H, K, K))
+    eye = np.ascontiguousarray(np.broadcast_to(np.eye(K), (B, H, K, K)))
+    for s in range(n_seg):
+        sl = slice(s * L, min((s + 1) * L, T))
+        ks, vs, bs = k[:, sl], v[:, sl], beta[:, sl]
+        gs = None if g is None else g[:, sl]
+        gks = None if gk is None else gk[:, sl]
+        _, ext[s] = scan(ks, ks, vs, bs, g=gs, gk=gks, threads=threads)
+        _, tr[s] = scan(ks, ks, np.zeros(ks.shape[:3] + (K,)), bs, g=gs, gk=gks, h0=eye,
+                        threads=threads)
+    return ext, tr
+
+
 def l2norm(x, eps=1e-6):
     """Per-row L2 normalisation over the last dim: x / sqrt(sum x^2 + eps)."""
     x = _f64(x)

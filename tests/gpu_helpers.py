@@ -66,6 +66,8 @@ def run_gpu(w, with_final_state=True):
     elif w.bidirectional and (bw or w.merge):
         extra = dict(backward=bw or None, merge=w.merge, eps=w.eps,
                      gate=None if w.gate is None else to_dev(w.gate))
+    if w.segment_len is not None:
+        extra["segment_len"] = w.segment_len
     res = gdn.gdn_forward(q, k, v, f32_dev(w.beta), g=f32_dev(w.g), gk=f32_dev(w.gk),
                           h0=f32_dev(w.h0), cu_seqlens=i32_dev(w.cu_seqlens), prep=w.prep,
                           bidirectional=w.bidirectional,

@@ -18,6 +18,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
 
 OK, NULL, SHAPE, DTYPE, LAYOUT, UNSUP, CUDA, TIMEOUT, WS, DEVICE = range(10)
+GDN_ACCUMULATE_FLAG = 0x1
 
 
 @pytest.fixture(scope="module")
@@ -162,6 +163,51 @@ def test_frame_fwd_rejects_on_host(L):
     assert ff(T=0) == OK                           # nothing to do, nothing launched
     assert gdn.gdn_frame_workspace_size(1, 256, 2, 64, 64, 64, True) > 0
     assert gdn.gdn_frame_workspace_size(1, 256, 2, 64, 64, 96, True) == 0
+
+
+def test_seg_fwd_and_summary_reject_on_host(L):
+    d16, d32 = desc(gdn.BF16, 1, 256, 2, 64), desc(gdn.F32, 1, 256, 2, 64)
+
+    def sf(q=P(0), qkd=d16, vd=d16, seg=128, T=256, h0=None, reverse=0, flags=0, ws=P(9),
+           wsb=1 << 30):
+        return L.gdn_chunk_fwd_seg(q, P(1), qkd, P(2), vd, P(3), None, P(4), h0, P(5), d16,
+                                   None, None, 1, T, 2, 64, 64, 64, reverse, flags, seg, ws, wsb,
+                                   None)
+    assert sf(q=None) == NULL
+    assert sf(qkd=d32, vd=d32) == DTYPE            # fp32 runs the fused path only
+    assert sf(seg=96) == SHAPE                     # not a multiple of 64
+    assert sf(seg=0) == SHAPE
+    assert sf(reverse=1, h0=P(6)) == UNSUP
+    assert sf(wsb=1024) == WS
+    need = gdn.gdn_seg_workspace_size(1, 256, 2, 64, 64, False, 128)
+    assert need > gdn.gdn_workspace_size(1, 256, 2, 64, 64, 1, 0, gdn.BF16, 0)
+    assert gdn.gdn_seg_workspace_size(1, 256, 2, 64, 64, False, 100) == 0
+
+    def ss(k=P(0), kd=d16, ext=P(5), tr=P(6), seg=128, T=256, flags=0, wsb=1 << 30):
+        return L.gdn_state_summary(k, kd, P(2), d16, P(3), None, P(4), ext, tr, 1, T, 2, 64, 64,
+                                   64, seg, flags, P(9), wsb, None)
+    assert ss(k=None) == NULL
+    assert ss(ext=None) == NULL
+    assert ss(kd=d32) == DTYPE
+    assert ss(seg=32) == SHAPE
+    assert ss(flags=GDN_ACCUMULATE_FLAG) == UNSUP  # summaries are stored, never added
+    assert ss(ext=ctypes.c_void_p(A + 2)) == LAYOUT
+    assert ss(wsb=16) == WS
+    assert ss(T=0) == OK
+
+
+def test_seg_choose_sizes_the_grid():
+    """Host arithmetic only: segments pay when few (sequence, head, value
+    tile) CTAs would walk a long sequence, never when the plain pass already
+    fills the SMs."""
+    choose = gdn.gdn_seg_choose
+    long_few = choose(1, 65536, 4, 128, 128, False, 152)
+    assert 64 <= long_few < 65536 and long_few % 64 == 0
+    assert choose(4, 4096, 16, 128, 128, False, 152) >= 4096    # 128 CTAs already
+    assert choose(1, 256, 2, 64, 64, False, 152) >= 256         # four chunks
+    assert choose(1, 65536, 4, 128, 128, False, 8) >= long_few  # fewer SMs, longer segments
+    assert choose(1, 0, 4, 128, 128, False, 152) == 0
+    assert choose(1, 64, 4, 128, 128, False, 0) == 0
 
 
 def test_python_binding_fails_loudly_without_library(monkeypatch):

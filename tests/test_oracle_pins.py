@@ -463,3 +463,69 @@ def test_frame_reverse_is_frame_flip_and_shift():
     back = frames(fwd)[:, ::-1].reshape(fwd.shape)
     np.testing.assert_allclose(rev, back, rtol=1e-13, atol=1e-13)
     assert np.all(frames(rev)[:, -1] == 0.0)
+
+
+# ------------------------------------------- segment summaries (state_ext, M) ---
+# hyper-parallel coverage_diff page, `kda_state_summary_forward_from_prepared`:
+# a piece's final state is transition . h_in + state_ext.
+
+def test_summary_one_token_segments_closed_form():
+    """segment_len = 1: M_t = (I - beta_t k_t k_t^T) e^{g_t} and
+    E_t = beta_t k_t v_t^T, written out from the update rule (decay, predict,
+    correct); per-key gate: M_t = (I - beta k k^T) diag(e^{gk_t})."""
+    rng = np.random.default_rng(31)
+    T, K, V = 3, 5, 4
+    k, v = rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    beta, g = rng.uniform(0.1, 1, T), -rng.uniform(0, 1, T)
+    gk = -rng.uniform(0, 1, (T, K))
+    ext, tr = oracle.state_summary(_one(k), _one(v), _one(beta), 1, g=_one(g), threads=1)
+    _, trk = oracle.state_summary(_one(k), _one(v), _one(beta), 1, gk=_one(gk), threads=1)
+    for t in range(T):
+        P = np.eye(K) - beta[t] * np.outer(k[t], k[t])
+        np.testing.assert_allclose(tr[t, 0, 0], P * np.exp(g[t]), rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(ext[t, 0, 0], beta[t] * np.outer(k[t], v[t]), rtol=1e-13)
+        np.testing.assert_allclose(trk[t, 0, 0], P @ np.diag(np.exp(gk[t])), rtol=1e-13, atol=1e-15)
+
+
+def test_summary_beta0_is_pure_decay():
+    """beta = 0: nothing is written; M = e^{sum g} I (diag(e^{sum gk})), E = 0."""
+    rng = np.random.default_rng(32)
+    T, K, V = 7, 4, 3
+    k, v = rng.standard_normal((T, K)), rng.standard_normal((T, V))
+    g, gk = -rng.uniform(0, 1, T), -rng.uniform(0, 1, (T, K))
+    ext, tr = oracle.state_summary(_one(k), _one(v), _one(np.zeros(T)), T, g=_one(g), threads=1)
+    np.testing.assert_array_equal(ext, 0.0)
+    np.testing.assert_allclose(tr[0, 0, 0], np.exp(g.sum()) * np.eye(K), rtol=1e-13, atol=1e-16)
+    _, trk = oracle.state_summary(_one(k), _one(v), _one(np.zeros(T)), T, gk=_one(gk), threads=1)
+    np.testing.assert_allclose(trk[0, 0, 0], np.diag(np.exp(gk.sum(0))), rtol=1e-13, atol=1e-16)
+
+
+def test_summary_composes_over_adjacent_segments():
+    """Two halves compose into the whole: M = M2 M1, E = M2 E1 + E2 (a
+    transposed or reversed product fails)."""
+    rng = np.random.default_rng(33)
+    T, K, V = 12, 5, 3
+    k, v = rng.standard_normal((T, K)) / np.sqrt(K), rng.standard_normal((T, V))
+    beta, g = rng.uniform(0, 1, T), -rng.uniform(0, 0.5, T)
+    half, whole = (oracle.state_summary(_one(k), _one(v), _one(beta), L, g=_one(g), threads=1)
+                   for L in (6, 12))
+    (E1, E2), (M1, M2) = half[0][:, 0, 0], half[1][:, 0, 0]
+    np.testing.assert_allclose(whole[1][0, 0, 0], M2 @ M1, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(whole[0][0, 0, 0], M2 @ E1 + E2, rtol=1e-12, atol=1e-14)
+
+
+def test_summary_reproduces_scan_from_any_state():
+    """Ragged last segment: applying the summaries segment by segment from a
+    random h0 gives the scan's final state from h0."""
+    rng = np.random.default_rng(34)
+    B, T, H, K, V = 2, 11, 2, 4, 3
+    k, v = rng.standard_normal((B, T, H, K)) / 2, rng.standard_normal((B, T, H, V))
+    beta, g = rng.uniform(0, 1, (B, T, H)), -rng.uniform(0, 0.5, (B, T, H))
+    h0 = rng.standard_normal((B, H, K, V))
+    ext, tr = oracle.state_summary(k, v, beta, 4, g=g, threads=1)
+    assert ext.shape == (3, B, H, K, V) and tr.shape == (3, B, H, K, K)
+    h = h0.copy()
+    for s in range(3):
+        h = tr[s] @ h + ext[s]
+    _, hf = oracle.scan(k, k, v, beta, g=g, h0=h0, threads=1)
+    np.testing.assert_allclose(h, hf, rtol=1e-12, atol=1e-13)

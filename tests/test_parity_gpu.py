@@ -308,3 +308,62 @@ def test_full_size_video_bidirectional():
     den = oracle.den(qn, kn, beta, g=g) + oracle.den(qn, kn, beta, g=g, reverse=True)
     assert rel_err(got["out"][b:b + 1][:, :, heads], of + orv) <= 2e-2
     assert rel_err(got["den"][b:b + 1][:, heads], den) <= 2e-2
+
+
+# ------------------------------------------- segment-parallel state passing ---
+
+SEG = {
+    # several segments, ragged last chunk and segment, state in and out
+    "k128_h0": (dict(B=2, T=64 * 11 + 17, H=2, K=128, V=128, h0_std=0.5), 128),
+    "k64_seg64": (dict(B=1, T=64 * 7, H=3, K=64, V=64, h0_std=0.5), 64),
+    "k112_v112": (dict(B=1, T=333, H=2, K=112, V=112), 192),
+    "gk_v256": (dict(B=1, T=300, H=2, K=128, V=256, g_mu=None, gk_mu=4.0, h0_std=0.5), 128),
+    "one_segment": (dict(B=1, T=200, H=2, K=64, V=64, h0_std=0.5), 256),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SEG))
+def test_small_segmented(name):
+    spec, seg = SEG[name]
+    w = workloads.make(**spec, seed=11, name="seg_" + name, segment_len=seg)
+    _compare(w)
+
+
+def test_small_segmented_bidirectional_den():
+    """reverse scan and the denominator column through the segment path"""
+    w = dataclasses.replace(workloads.make(1, 64 * 9 + 5, 2, 64, 64, seed=12, name="seg_bidir"),
+                            bidirectional=True, segment_len=128)
+    _compare(w)
+
+
+@pytest.mark.parametrize("perkey", [False, True])
+def test_state_summary(perkey):
+    """(state_ext, transition) per segment against the oracle's summaries"""
+    import gated_delta_rule_18_gb300 as gdn
+    B, T, H, K, V, L = 2, 64 * 5 + 9, 2, 128, 64, 128
+    w = workloads.make(B, T, H, K, V, seed=13, g_mu=None if perkey else 3.0,
+                       gk_mu=4.0 if perkey else None)
+    kn = oracle.l2norm(w.k.values)
+    ext_ref, tr_ref = oracle.state_summary(kn, w.v.values, w.beta, L, g=w.g, gk=w.gk)
+    ext, tr = gdn.gdn_state_summary(to_dev(w.k), to_dev(w.v), f32_dev(w.beta), L, g=f32_dev(w.g),
+                                    gk=f32_dev(w.gk), qk_l2norm=True)
+    torch().cuda.synchronize()
+    e_ext = rel_err(ext.double().cpu().numpy(), ext_ref)
+    e_tr = rel_err(tr.double().cpu().numpy(), tr_ref)
+    assert e_ext <= TOL["bf16"] and e_tr <= TOL["bf16"], (e_ext, e_tr)
+
+
+def test_full_size_segmented_long_sequence():
+    """one 65536-token sequence of 4 heads with h0, segments as the
+    benchmark picks them; two heads checked against the oracle"""
+    import gated_delta_rule_18_gb300 as gdn
+    w = workloads.build("seg_long_bf16_b1h4t65536d128")
+    n_sm = torch().cuda.get_device_properties(0).multi_processor_count
+    seg = gdn.gdn_seg_choose(w.B, w.T, w.H, w.K, w.V, False, n_sm)
+    assert seg < w.T  # really segmented
+    got = run_gpu(dataclasses.replace(w, segment_len=seg))
+    heads = [0, w.H - 1]
+    ref = oracle.forward(_sub(w, 0, heads))
+    e_o = rel_err(got["out"][:, :, heads], ref["out"])
+    e_h = rel_err(got["h_final"][:, heads], ref["h_final"])
+    assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)

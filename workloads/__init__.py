@@ -190,6 +190,10 @@ class Workload:
     # one log-decay per frame, g_frame (B, T // frame, H) (then g is None)
     frame: int = 1
     g_frame: np.ndarray | None = None
+    # how the GPU path walks each sequence (same result): segment-parallel
+    # state passing with segments of this many tokens, "auto" to let the
+    # library pick for the device, or None for one pass per sequence
+    segment_len: int | str | None = None
 
     @property
     def n_seq(self) -> int:
@@ -208,7 +212,7 @@ def _vary_lengths(seed: int, n_seq: int, lo: int, hi: int) -> np.ndarray:
 def make(B: int, T: int, H: int, K: int, V: int, dtype: str = "bf16", *,
          seed: int = 0, g_mu: float | None = 3.0, gk_mu: float | None = None,
          h0_std: float | None = None, lengths=None, name: str = "custom",
-         chunk: int = 64) -> Workload:
+         chunk: int = 64, segment_len: int | str | None = None) -> Workload:
     """A causal workload with q, k, v ~ N(0,1), beta = sigmoid(N(0,1)) and a
     scalar gate (g_mu) or a per-key gate (gk_mu). `lengths` (list of ints)
     makes it varlen: B must be 1 and T == sum(lengths)."""
@@ -230,7 +234,7 @@ def make(B: int, T: int, H: int, K: int, V: int, dtype: str = "bf16", *,
     if h0_std is not None:
         h0 = _normal_f32(seed, "h0", n_seq * H * K * V, 0.0, h0_std).reshape(n_seq, H, K, V)
     return Workload(name, B, T, H, K, V, dtype, q, k, v, beta, g, gk, h0, cu,
-                    chunk=chunk)
+                    chunk=chunk, segment_len=segment_len)
 
 
 def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
@@ -283,6 +287,11 @@ WORKLOADS = {
     "gk_bf16_b1h32t65536k128v256": dict(kind="dense", B=1, T=65536, H=32,
                                         K=128, V=256, dtype="bf16", g_mu=None,
                                         gk_mu=4.0),
+    # one long sequence of few heads, carried in from a prefix (h0) and out
+    # (h_final): segment-parallel state passing
+    "seg_long_bf16_b1h4t65536d128": dict(kind="dense", B=1, T=65536, H=4, K=128,
+                                         V=128, dtype="bf16", g_mu=3.0, h0_std=0.02,
+                                         segment_len="auto"),
 }
 
 
@@ -306,7 +315,8 @@ def build(name: str, seed: int = 0, T: int | None = None) -> Workload:
     if kind == "dense":
         return make(spec["B"], spec["T"], spec["H"], spec["K"], spec["V"],
                     spec["dtype"], seed=seed, g_mu=spec.get("g_mu"),
-                    gk_mu=spec.get("gk_mu"), name=name)
+                    gk_mu=spec.get("gk_mu"), h0_std=spec.get("h0_std"), name=name,
+                    segment_len=spec.get("segment_len"))
     if kind == "video":
         return make_video(spec["B"], spec["N"], spec["H"], spec["D"], seed=seed,
                           name=name, reset_every=spec.get("reset_every"),
