@@ -11,6 +11,9 @@ gcc and marshals numpy arrays. Every function takes the STORED input values
 
 Pins that tie it to the pages and to mathematics, independently of itself,
 are in tests/test_oracle_pins.py; every function here has at least one.
+The gradients of the scan (`oracle.backward`) are the float64 autograd
+derivative of the plain token loop, pinned to central finite differences of
+the C forward above.
 """
 from __future__ import annotations
 

@@ -1,0 +1,93 @@
+"""fp64 CPU oracle for the gradients of the gated delta rule scan.
+
+TEST INFRASTRUCTURE ONLY, like the rest of `oracle/`: the tests, the smoke
+check and the benchmark's CPU leg may use it; the product path never does.
+
+The loss is L = sum(do * o) + sum(dh_final * h_final) for the token-level
+recurrence (SANA `fused_gdn.py` page, `_fused_gdn_kernel`: per token, decay,
+predict, correct, write; the output reads the state after the token's own
+write), with optional per-(token, head) L2 normalisation of q and k (eps
+1e-6) in front. The gradients are the reverse-mode derivative of that plain
+token loop, taken by PyTorch autograd in float64 on the CPU: the loop below
+is the definition, written out step by step, and autograd differentiates it
+exactly (no chunking, no reassociation). The pages' own backward (SANA
+`fused_cam_gdn.py` page, `_cam_scan_bwd_kernel`) walks the same recurrence in
+reverse time with the per-step rules ds_post += q do^T, ddelta = ds_post^T k,
+dv = beta ddelta, ds_pre = ds_post - k (beta ddelta)^T, ds <- e^{g} ds_pre;
+autograd applies the same chain rule.
+
+Pins (tests/test_oracle_pins.py): central finite differences of the C
+oracle's forward, an independent implementation, on every input, and the
+closed form of the beta = 0 case.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _t(x):
+    torch = _torch()
+    return None if x is None else torch.tensor(np.asarray(x, dtype=np.float64), requires_grad=True)
+
+
+def _l2(x, eps):
+    return x / (x * x).sum(-1, keepdim=True).add(eps).sqrt()
+
+
+def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6):
+    """The token recurrence on torch float64 tensors (differentiable).
+    q, k (B, T, H, K); v (B, T, H, V); beta, g (B, T, H); h0 (B, H, K, V).
+    Returns (o (B, T, H, V), h_final (B, H, K, V)); reverse: the
+    flip-and-shift scan (position p reads tokens p+1 .. T-1, R_{T-1} = 0)."""
+    torch = _torch()
+    if l2norm:
+        q, k = _l2(q, eps), _l2(k, eps)
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    S = torch.zeros(B, H, K, V, dtype=torch.float64) if h0 is None else h0
+    outs = [None] * T
+
+    def write(S, t):
+        S = torch.exp(g[:, t])[:, :, None, None] * S                     # decay
+        pred = torch.einsum("bhkv,bhk->bhv", S, k[:, t])                   # S^T k
+        d = beta[:, t][:, :, None] * (v[:, t] - pred)                      # correct
+        return S + k[:, t][:, :, :, None] * d[:, :, None, :]               # write
+
+    if not reverse:
+        for t in range(T):
+            S = write(S, t)
+            outs[t] = torch.einsum("bhkv,bhk->bhv", S, q[:, t])
+    else:
+        for p in range(T - 1, -1, -1):
+            outs[p] = torch.einsum("bhkv,bhk->bhv", S, q[:, p])
+            S = write(S, p)
+    return torch.stack(outs, dim=1), S
+
+
+def scan_grad(q, k, v, beta, g, do, h0=None, dh_final=None, reverse=False, l2norm=False,
+              eps=1e-6):
+    """Gradients of L = sum(do * o) + sum(dh_final * h_final) with respect to
+    q, k, v, beta, g and h0 (raw q, k when l2norm). Returns a dict of float64
+    numpy arrays: dq, dk, dv, dbeta, dg, dh0 (dh0 also when h0 is None: the
+    gradient at a zero initial state), and the forward o, h_final."""
+    torch = _torch()
+    B, T, H, K = np.shape(q)
+    V = np.shape(v)[-1]
+    tq, tk, tv, tb, tg = map(_t, (q, k, v, beta, g))
+    th0 = _t(np.zeros((B, H, K, V)) if h0 is None else h0)
+    o, hf = scan_torch(tq, tk, tv, tb, tg, th0, reverse=reverse, l2norm=l2norm, eps=eps)
+    loss = (o * torch.tensor(np.asarray(do, dtype=np.float64))).sum()
+    if dh_final is not None:
+        loss = loss + (hf * torch.tensor(np.asarray(dh_final, dtype=np.float64))).sum()
+    grads = torch.autograd.grad(loss, (tq, tk, tv, tb, tg, th0), allow_unused=True)
+    names = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
+    shapes = (tq.shape, tk.shape, tv.shape, tb.shape, tg.shape, th0.shape)
+    res = {n: (np.zeros(s) if gr is None else gr.detach().numpy())
+           for n, gr, s in zip(names, grads, shapes)}
+    res["o"], res["h_final"] = o.detach().numpy(), hf.detach().numpy()
+    return res

@@ -529,3 +529,69 @@ def test_summary_reproduces_scan_from_any_state():
         h = tr[s] @ h + ext[s]
     _, hf = oracle.scan(k, k, v, beta, g=g, h0=h0, threads=1)
     np.testing.assert_allclose(h, hf, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------- gradients ---
+# oracle/backward.py differentiates the plain token loop with autograd; it is
+# pinned to central finite differences of the C forward oracle (a separate
+# implementation) and to the beta = 0 closed form.
+
+def _fd_case(seed, B, T, H, K, V):
+    rng = np.random.default_rng(seed)
+    x = dict(q=rng.standard_normal((B, T, H, K)), k=rng.standard_normal((B, T, H, K)) / np.sqrt(K),
+             v=rng.standard_normal((B, T, H, V)), beta=rng.uniform(0.2, 0.9, (B, T, H)),
+             g=-rng.uniform(0.05, 0.6, (B, T, H)), h0=rng.standard_normal((B, H, K, V)))
+    return x, rng.standard_normal((B, T, H, V)), rng.standard_normal((B, H, K, V))
+
+
+def _loss_c(x, do, dhf, reverse, l2norm):
+    """L = sum(do o) + sum(dh_final h_final) through the C forward oracle."""
+    q, k = (oracle.l2norm(x["q"]), oracle.l2norm(x["k"])) if l2norm else (x["q"], x["k"])
+    o, hf = oracle.scan(q, k, x["v"], x["beta"], g=x["g"], h0=None if reverse else x["h0"],
+                        reverse=reverse, threads=1)
+    return float(np.sum(do * o) + (0.0 if reverse else np.sum(dhf * hf)))
+
+
+@pytest.mark.parametrize("reverse,l2norm", [(False, False), (False, True), (True, False)])
+def test_gradients_match_central_differences(reverse, l2norm):
+    from oracle import backward
+    x, do, dhf = _fd_case(41 + 2 * reverse + l2norm, 1, 5, 2, 3, 2)
+    res = backward.scan_grad(x["q"], x["k"], x["v"], x["beta"], x["g"], do,
+                             h0=None if reverse else x["h0"], dh_final=None if reverse else dhf,
+                             reverse=reverse, l2norm=l2norm)
+    eps = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"), ("g", "dg"),
+                        ("h0", "dh0")):
+        if reverse and name == "h0":
+            continue
+        fd = np.zeros_like(x[name])
+        for ix in np.ndindex(x[name].shape):
+            xp = {n: a.copy() for n, a in x.items()}
+            xm = {n: a.copy() for n, a in x.items()}
+            xp[name][ix] += eps
+            xm[name][ix] -= eps
+            fd[ix] = (_loss_c(xp, do, dhf, reverse, l2norm) - _loss_c(xm, do, dhf, reverse, l2norm)) / (2 * eps)
+        np.testing.assert_allclose(res[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
+
+
+def test_gradients_beta0_closed_form():
+    """beta = 0: o_t = e^{G_t} h0^T q_t and h_final = e^{G_T} h0 with G the
+    running sum of g, so dq_t = e^{G_t} h0 do_t, dh0 = sum_t e^{G_t} q_t do_t^T
+    + e^{G_T} dh_final, dk = dv = 0 and dg_t = sum_{s >= t} (the terms of L
+    that G_s multiplies)."""
+    from oracle import backward
+    x, do, dhf = _fd_case(47, 1, 6, 1, 3, 2)
+    q, g, h0 = x["q"][0, :, 0], x["g"][0, :, 0], x["h0"][0, 0]
+    dd = do[0, :, 0]
+    res = backward.scan_grad(x["q"], x["k"], x["v"], np.zeros_like(x["beta"]), x["g"], do,
+                             h0=x["h0"], dh_final=dhf)
+    G = np.cumsum(g)
+    e = np.exp(G)
+    np.testing.assert_allclose(res["dq"][0, :, 0], e[:, None] * (dd @ h0.T), rtol=1e-12)
+    np.testing.assert_allclose(res["dh0"][0, 0], (e[:, None] * q).T @ dd + e[-1] * dhf[0, 0],
+                               rtol=1e-12)
+    np.testing.assert_array_equal(res["dk"], 0.0)
+    np.testing.assert_array_equal(res["dv"], 0.0)
+    terms = e * np.einsum("tk,kv,tv->t", q, h0, dd)
+    terms[-1] += e[-1] * np.sum(dhf[0, 0] * h0)
+    np.testing.assert_allclose(res["dg"][0, :, 0], np.cumsum(terms[::-1])[::-1], rtol=1e-12)
