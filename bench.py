@@ -84,6 +84,9 @@ def path_work(w):
     return fl, by
 
 
+METRIC_BWD = "GDN chunked bwd tokens/s (forward recompute + all input gradients) at 1 GB300"
+
+
 def seg_count(w):
     """Segments per sequence of a segment-parallel workload (1 otherwise)."""
     if not isinstance(w.segment_len, int) or w.segment_len <= 0:
@@ -132,6 +135,15 @@ def kernel_bytes(w, name):
         return th * (w.K * e + w.V * e + (4 if w.bidirectional else 0)) + states
     if name == "merge":
         return th * w.V * e * (3 if w.gate is not None else 2) + th * 4
+    snap_h = w.B * w.H * (-(-w.T // C)) * w.K * w.V * 2  # one bf16 K x V state per chunk
+    snap_v = th * w.V * 2                                 # one bf16 value row per token
+    if name == "bwd_dh":  # images + do in; dh' and dv_new snapshots out
+        return th * ((3 * K + C) * 2 + w.V * 2) + chunks * K * 4 + snap_h + snap_v
+    if name == "bwd_dq":  # q, k, do, v_new, h in; dq, dk and dG partials out
+        return th * (2 * K * 2 + w.V * 2 + 4) + snap_v + snap_h + th * (2 * K * 4 + 4)
+    if name == "bwd_dk":  # k, v, dv_new, v_new, h, dh', partials in; dk, dv, dbeta, dg out
+        return th * (K * 2 + w.V * 2 + 8) + 2 * snap_v + 2 * snap_h + th * (K * 4 + 4) \
+            + th * (K * 4 + w.V * 4 + 8)
     return None
 
 
@@ -439,6 +451,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--T", type=int, default=None,
                     help="override the token count of a dense workload (smaller profiling captures)")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time the gradients (gdn_chunk_bwd, forward recompute included) "
+                         "of a dense causal workload instead of the forward")
     ap.add_argument("--segment-len", type=int, default=None,
                     help="segment-parallel state passing with this many tokens per segment "
                          "(0: one pass per sequence); default: the workload's own setting")
@@ -468,7 +483,22 @@ def main():
         w = dataclasses.replace(w, segment_len=args.segment_len or None)
     w = resolve_segments(gdn, w, dev)
     d = device_inputs(w, dev)
-    ws = workspace_for(gdn, w, dev)
+    if args.pass_ == "bwd":
+        if w.dtype != "bf16" or w.bidirectional or w.gk is not None or w.cu_seqlens is not None \
+                or w.frame > 1:
+            raise SystemExit("--pass bwd takes a dense causal bf16 workload with a scalar gate")
+        d["dout"] = torch.from_numpy(workloads.stored_normal(
+            rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V), dtype=torch.uint8,
+                         device=dev)
+        args.no_e2e = args.no_cpu_baseline = True
+
+        def run_step(gdn, w, d, ws):  # noqa: F811 -- the timed step of this pass
+            return gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dout"],
+                                     h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws)
+    else:
+        ws = workspace_for(gdn, w, dev)
+        run_step = globals()["run_step"]
     stream = torch.cuda.current_stream()
 
     for _ in range(warmup):
@@ -524,7 +554,7 @@ def main():
                     "peak_source": f"{peak_src} hbm_gbs"}
 
     result = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC if args.pass_ == "fwd" else METRIC_BWD, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",

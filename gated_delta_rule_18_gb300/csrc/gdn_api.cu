@@ -16,11 +16,12 @@ using gdn::FwdParams;
 
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
-    KFrameOut, KSegSummary, KSegCombine, KNumKinds
+    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
-                                     "frame_chain", "frame_out", "seg_summary", "seg_combine"};
+                                     "frame_chain", "frame_out", "seg_summary", "seg_combine",
+                                     "bwd_dh", "bwd_dq", "bwd_dk"};
 
 struct Profiler {
     std::mutex mu;
@@ -453,6 +454,99 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v, g
     p.sum_tr = transition;
     p.n_kt = transition ? (K + 63) / 64 : 0;
     e = launch(KSegSummary, stream, [&] { return gdn::launch_state_tc(p, stream); });
+    return cuda_status(e);
+}
+
+}  // extern "C"
+
+namespace {
+// backward sections after the forward workspace: bf16 snapshots of the state
+// entering each chunk, v_new, the state gradient at each chunk's end, dv_new
+struct BwdWs {
+    size_t h, vn, dh, dvn, total;
+};
+bool bwd_layout(const Ws &L, int H, int K, int V, BwdWs &S) {
+    const size_t hc = (size_t)H * L.max_chunks;
+    size_t off = L.total;
+    S.h = off;
+    off = align_up(off + hc * K * V * 2);
+    S.vn = off;
+    off = align_up(off + hc * gdn::kChunk * V * 2);
+    S.dh = off;
+    off = align_up(off + hc * K * V * 2);
+    S.dvn = off;
+    off = align_up(off + hc * gdn::kChunk * V * 2);
+    S.total = off;
+    return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V) {
+    Ws L;
+    BwdWs S;
+    if (V > 128 || !ws_layout(B, T, H, K, V, B, 0, GDN_BF16, 0, L)) return 0;
+    bwd_layout(L, H, K, V, S);
+    return S.total;
+}
+
+gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                         gdn_tensor_desc vd, const float *g, const float *beta, const float *h0,
+                         const void *dout, gdn_tensor_desc dod, const float *dh_final, float *dq,
+                         float *dk, float *dv, float *dbeta, float *dg, float *dh0, int B, int T,
+                         int H, int K, int V, int chunk, int reverse, int flags, void *workspace,
+                         size_t ws_bytes, cudaStream_t stream) {
+    if (T > 0 && (!dout || !dq || !dk || !dv || !dbeta || !dg)) return GDN_ERR_NULL;
+    if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16 || (T > 0 && dod.dtype != GDN_BF16))
+        return GDN_ERR_DTYPE;
+    if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;
+    if (reverse && (h0 || dh_final || dh0)) return GDN_ERR_UNSUPPORTED;
+    if (V > 128) return GDN_ERR_SHAPE;
+    if (!aligned16(dout) || !strides_ok(dod)) return GDN_ERR_LAYOUT;
+    for (const void *f : {(const void *)dq, (const void *)dk, (const void *)dv, (const void *)dbeta,
+                          (const void *)dg, (const void *)dh0, (const void *)dh_final})
+        if (f && (reinterpret_cast<uintptr_t>(f) & 7)) return GDN_ERR_LAYOUT;
+    Ws L;
+    gdn::FwdParams p;
+    // the forward recompute: no outputs, the snapshots instead
+    gdn_status st = fwd_setup(q, k, qkd, v, vd, g, nullptr, beta, h0, nullptr, B, nullptr,
+                              gdn_tensor_desc{GDN_BF16, 0, 0, 0, 0}, nullptr, nullptr, B, T, H, K,
+                              V, chunk, reverse, flags, false, L, p);
+    if (st != GDN_OK) return st;
+    BwdWs S;
+    bwd_layout(L, H, K, V, S);
+    if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
+    if (T == 0) {  // dL/dh0 = dL/dh_final
+        if (!dh0) return GDN_OK;
+        const size_t n = (size_t)B * H * K * V * sizeof(float);
+        cudaError_t e = dh_final ? cudaMemcpyAsync(dh0, dh_final, n, cudaMemcpyDeviceToDevice, stream)
+                                 : cudaMemsetAsync(dh0, 0, n, stream);
+        return cuda_status(e);
+    }
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    bind_ws(ws, L, p);
+    p.h_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.h);
+    p.vn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.vn);
+    cudaError_t e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, 0, stream); });
+    if (e == cudaSuccess) e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    gdn::BwdParams b{};
+    b.q = q, b.k = k, b.v = v, b.dout = dout;
+    b.qk_sb = qkd.stride_b, b.qk_st = qkd.stride_t, b.qk_sh = qkd.stride_h;
+    b.v_sb = vd.stride_b, b.v_st = vd.stride_t, b.v_sh = vd.stride_h;
+    b.do_sb = dod.stride_b, b.do_st = dod.stride_t, b.do_sh = dod.stride_h;
+    b.g = g, b.beta = beta, b.dh_final = dh_final;
+    b.dq = dq, b.dk = dk, b.dv = dv, b.dbeta = dbeta, b.dg = dg, b.dh0 = dh0;
+    b.B = B, b.T = T, b.H = H, b.K = K, b.V = V, b.reverse = reverse, b.l2norm = p.l2norm;
+    b.max_chunks = L.max_chunks;
+    b.w_img = p.w_img, b.qg_img = p.qg_img, b.kg_img = p.kg_img, b.p_img = p.p_img, b.dec = p.dec;
+    b.h_snap = p.h_snap, b.vn_snap = p.vn_snap;
+    b.dh_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dh);
+    b.dvn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dvn);
+    e = launch(KBwdDh, stream, [&] { return gdn::launch_bwd_dh(b, stream); });
+    if (e == cudaSuccess) e = launch(KBwdDq, stream, [&] { return gdn::launch_bwd_dq(b, stream); });
+    if (e == cudaSuccess) e = launch(KBwdDk, stream, [&] { return gdn::launch_bwd_dk(b, stream); });
     return cuda_status(e);
 }
 

@@ -1,0 +1,738 @@
+// gdn_bwd_grad.cu -- the chunk-parallel part of the backward: per (64-token
+// chunk, head), the input gradients from the chunk's inputs, the state h
+// entering it, the state gradient dh' at its end and dL/dv_new (the forward
+// snapshots and the dh pass).
+//
+// Forward per chunk (G the in-chunk cumulative log gate, Gamma_ij =
+// e^{G_i - G_j}, q^ / k^ the normalised rows, S = K^ K^T):
+//   A   = strictly_lower(diag(beta) (S . Gamma)),  T = (I + A)^{-1}
+//   w   = T diag(beta e^{G}) K^,   u = T diag(beta) V,   v_new = u - w h
+//   P   = lower_incl(Q^ K^T . Gamma),  o = diag(e^{G}) Q^ h + P v_new
+//   h'  = e^{G_C} h + (diag(e^{G_C - G}) K^)^T v_new
+// (the WY form of the token rule of the SANA `fused_gdn.py` page; w, u,
+// v_new and the h update as on the hyper-parallel coverage_diff page, whose
+// backward kernels `chunk_bwd_dqkwg` and `prepare_wy_repr_bwd` split the same
+// reverse-mode derivative). With dv_new = dL/dv_new and dh', reverse mode:
+//   dP  = lower_incl(do v_new^T),   M_P = dP . Gamma
+//   dq^ = e^{G} . (do h^T) + M_P K^
+//   dw  = -dv_new h^T,   dB_w = T^T dw,   dB_u = T^T dv_new
+//   dA  = -strictly_lower(T^T (dw (beta e^G . K^)^T + dv_new (beta . V)^T) T^T)
+//   M_A = dA . Gamma . beta_row,   dS = M_A + M_A^T
+//   dk^ = M_P^T Q^ + e^{G_C - G} . (v_new dh'^T) + beta e^{G} . dB_w + dS K^
+//   dv  = beta . dB_u
+//   dbeta_i = sum_c dB_u v + e^{G_i} sum_d dB_w k^ + sum_j dA_ij (S . Gamma)_ij
+//   dG_i   = terms of P, A, qg, kg, B_w and, at the last token, of e^{G_C}
+//   dg_i   = sum_{j >= i} dG_j (G is the running sum of g),
+// then through the L2 normalisation: dx = (dx^ - x^ (x^ . dx^)) / |x|.
+//
+// Two kernels share the work (each within the shared-memory budget):
+//   bwd_dq  dq, the P and qg parts of dG, and M_P^T Q^ (stored into dk as a
+//           partial sum)
+//   bwd_dk  dk (adding that partial), dv, dbeta, dg (adding bwd_dq's dG).
+// Products run on mma.sync (bf16 operands, fp32 accumulate); T = (I + A)^{-1}
+// is formed in fp32 by blocks. 8 warps per CTA.
+#include "gdn_mma.cuh"
+
+namespace gdn {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kThreads = 256;
+constexpr int kLK = kKP + 8;   // row stride of 128-column tiles (keys or values)
+constexpr int kL6 = 64 + 8;    // row stride of 64-column tiles
+constexpr int kPS = kChunk + 1;  // fp32 64 x 64 row stride
+
+__device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
+
+// common per-chunk addressing
+struct ChunkCtx {
+    int s, hh, c, pos0, Lc;
+    int64_t gch;  // [head][global chunk] image / snapshot slot
+};
+__device__ __forceinline__ ChunkCtx chunk_ctx(const BwdParams &p) {
+    ChunkCtx x;
+    const int nts = (p.T + kChunk - 1) / kChunk;
+    x.hh = blockIdx.x % p.H;
+    const int gid = blockIdx.x / p.H;
+    x.s = gid / nts;
+    x.c = gid - x.s * nts;
+    x.pos0 = x.c * kChunk;
+    x.Lc = min(kChunk, p.T - x.pos0);
+    x.gch = (int64_t)x.hh * p.max_chunks + gid;
+    return x;
+}
+
+// 16-byte pieces of a (rows x ncol) bf16 block into a row-major tile; rows
+// or columns outside (nrow_ok, ncol) are zero-filled
+template <class RowPtr>
+__device__ __forceinline__ void load_rows(bf16 *dst, int ld, int rows, int ncol, int ncol_tile, RowPtr row_ptr) {
+    const int pieces = ncol_tile / 8;
+    for (int e = threadIdx.x; e < rows * pieces; e += kThreads) {
+        const int i = e / pieces, c8 = (e % pieces) * 8;
+        const bf16 *src = row_ptr(i);
+        const bool in = src != nullptr && c8 < ncol;
+        cp_async16(dst + i * ld + c8, in ? src + c8 : dst, in ? 16 : 0);
+    }
+}
+
+// L2 norms of 64 rows of a tile (1 when not normalising), then the rows
+// scaled in place (bf16)
+__device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_out, bool l2) {
+    const int tid = threadIdx.x;
+    if (tid < kChunk) {
+        float ss = 0.f;
+        for (int d = 0; d < ncol; d += 8) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(t + tid * ld + d);
+            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float2 f = __bfloat1622float2(h2[x]);
+                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+            }
+        }
+        r_out[tid] = l2 ? rsqrtf(ss + 1e-6f) : 1.f;
+    }
+    __syncthreads();
+    if (!l2) return;
+    for (int e = tid; e < kChunk * (ncol / 8); e += kThreads) {
+        const int i = e / (ncol / 8), d = (e % (ncol / 8)) * 8;
+        uint4 u = *reinterpret_cast<const uint4 *>(t + i * ld + d);
+        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
+        const float r = r_out[i];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const float2 f = __bfloat1622float2(h2[x]);
+            h2[x] = __floats2bfloat162_rn(f.x * r, f.y * r);
+        }
+        *reinterpret_cast<uint4 *>(t + i * ld + d) = u;
+    }
+}
+
+// in-chunk cumulative (floored) log gates of the kv rows, and beta
+__device__ __forceinline__ void gates(const BwdParams &p, const ChunkCtx &x, float *sG, float *sB, float *graw) {
+    const int tid = threadIdx.x;
+    if (tid < kChunk) {
+        const int tk = tid < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + tid) : -1;
+        const int64_t row = ((int64_t)x.s * p.T + tk) * p.H + x.hh;
+        const float g = tk >= 0 ? p.g[row] : 0.f;
+        graw[tid] = g;
+        sG[tid] = tk >= 0 ? fmaxf(g, kLogGateMin) : 0.f;
+        if (sB) sB[tid] = tk >= 0 ? p.beta[row] : 0.f;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const float a0 = sG[2 * tid], a1 = sG[2 * tid + 1];
+        float incl = a0 + a1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += y;
+        }
+        sG[2 * tid] = incl - a1;
+        sG[2 * tid + 1] = incl;
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ dq ---
+struct DqSmem {
+    bf16 q[kChunk * kLK], k[kChunk * kLK], dout[kChunk * kLK], vn[kChunk * kLK];
+    bf16 h[kKP * kLK];
+    bf16 mp[kChunk * kL6];
+    float G[kChunk], graw[kChunk], rq[kChunk], rk[kChunk], dG[kChunk], row[kChunk];
+};
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) {
+    extern __shared__ __align__(16) unsigned char smraw[];
+    DqSmem &sm = *reinterpret_cast<DqSmem *>(smraw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const ChunkCtx x = chunk_ctx(p);
+    if (x.s >= p.B) return;
+    const int K = p.K, V = p.V, kq = round16(K), kv = round16(V);
+    const bf16 *q = (const bf16 *)p.q, *k = (const bf16 *)p.k, *dout = (const bf16 *)p.dout;
+
+    load_rows(sm.q, kLK, kChunk, K, kKP, [&](int i) -> const bf16 * {
+        if (i >= x.Lc) return nullptr;
+        return q + x.s * p.qk_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.qk_st + x.hh * p.qk_sh;
+    });
+    load_rows(sm.k, kLK, kChunk, K, kKP, [&](int i) -> const bf16 * {
+        const int tk = i < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + i) : -1;
+        if (tk < 0) return nullptr;
+        return k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
+    });
+    load_rows(sm.dout, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+        if (i >= x.Lc) return nullptr;
+        return dout + x.s * p.do_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.do_st + x.hh * p.do_sh;
+    });
+    load_rows(sm.vn, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+        return p.vn_snap + (x.gch * kChunk + i) * V;
+    });
+    load_rows(sm.h, kLK, kKP, V, kKP, [&](int r) -> const bf16 * {
+        return r < K ? p.h_snap + (x.gch * K + r) * V : nullptr;
+    });
+    cp_async_commit();
+    if (tid < kChunk) sm.dG[tid] = sm.row[tid] = 0.f;
+    gates(p, x, sm.G, nullptr, sm.graw);
+    cp_async_wait<0>();
+    __syncthreads();
+    norm_rows(sm.q, kLK, kq, sm.rq, p.l2norm);
+    norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
+    __syncthreads();
+
+    // P (kept in registers) and dP = do v_new^T on the same fragments
+    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
+    {
+        float sp[4][4], dp[4][4];
+        acc_zero(sp);
+        acc_zero(dp);
+        warp_gemm(sp, Tile{sm.q, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
+        warp_gemm(dp, Tile{sm.dout, kLK}, false, Tile{sm.vn, kLK}, false, m0, n0, kv, lane);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int i = m0 + g8 + 8 * hf;
+                float mpv[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = n0 + 8 * n + 2 * t4 + e;
+                    const bool on = j <= i && i < x.Lc;
+                    const float gam = on ? __expf(sm.G[i] - sm.G[j]) : 0.f;
+                    const float P = gam * sp[n][2 * hf + e], dP = on ? dp[n][2 * hf + e] : 0.f;
+                    mpv[e] = dP * gam;
+                    const float cterm = dP * P;  // d/dG_i of P_ij is P_ij, d/dG_j is -P_ij
+                    if (on && cterm != 0.f) {
+                        atomicAdd(&sm.dG[i], cterm);
+                        atomicAdd(&sm.dG[j], -cterm);
+                    }
+                }
+                *reinterpret_cast<uint32_t *>(sm.mp + i * kL6 + n0 + 8 * n + 2 * t4) = pack_bf16(mpv[0], mpv[1]);
+            }
+    }
+    __syncthreads();
+
+    // dq^ = e^{G} . (do h^T) + M_P K^   (64 x 128; warp: 16 rows x 64 keys)
+    const int nk0 = 64 * (warp >> 2);
+    float dq[8][4];
+    {
+        acc_zero(dq);
+        warp_gemm(dq, Tile{sm.dout, kLK}, false, Tile{sm.h, kLK}, false, m0, nk0, kv, lane);
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
+                const float eg = __expf(sm.G[i]);
+                // dG_i of qg = e^{G_i} q^_i: sum_d dqg_id qg_id
+                part[hf] += dq[n][e] * eg * __bfloat162float(sm.q[i * kLK + d]);
+                dq[n][e] *= eg;
+            }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float v = part[hf];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (t4 == 0 && m0 + g8 + 8 * hf < x.Lc) atomicAdd(&sm.dG[m0 + g8 + 8 * hf], v);
+        }
+        warp_gemm(dq, Tile{sm.mp, kL6}, false, Tile{sm.k, kLK}, true, m0, nk0, kChunk, lane);
+    }
+    // through the normalisation: dq = (dq^ - q^ (q^ . dq^)) / |q|
+    {
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
+                part[hf] += dq[n][e] * __bfloat162float(sm.q[i * kLK + d]);
+            }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float v = part[hf];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (t4 == 0) atomicAdd(&sm.row[m0 + g8 + 8 * hf], v);
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int i = m0 + g8 + 8 * hf;
+        if (i >= x.Lc) continue;
+        const int tq = q_token(p.reverse, p.T, x.pos0 + i);
+        float *dst = p.dq + (((int64_t)x.s * p.T + tq) * p.H + x.hh) * K;
+        const float r = sm.rq[i], dot = sm.row[i];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            const int d = nk0 + 8 * n + 2 * t4;
+            if (d >= K) continue;
+            float2 o;
+            o.x = p.l2norm ? r * (dq[n][2 * hf] - __bfloat162float(sm.q[i * kLK + d]) * dot) : dq[n][2 * hf];
+            o.y = p.l2norm ? r * (dq[n][2 * hf + 1] - __bfloat162float(sm.q[i * kLK + d + 1]) * dot)
+                           : dq[n][2 * hf + 1];
+            *reinterpret_cast<float2 *>(dst + d) = o;
+        }
+    }
+    // M_P^T Q^: bwd_dk adds it into dk^
+    {
+        float pk[8][4];
+        acc_zero(pk);
+        warp_gemm(pk, Tile{sm.mp, kL6}, true, Tile{sm.q, kLK}, true, m0, nk0, kChunk, lane);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int j = m0 + g8 + 8 * hf;
+            const int tk = j < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + j) : -1;
+            if (tk < 0) continue;
+            float *dst = p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const int d = nk0 + 8 * n + 2 * t4;
+                if (d < K) *reinterpret_cast<float2 *>(dst + d) = make_float2(pk[n][2 * hf], pk[n][2 * hf + 1]);
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < x.Lc) {  // this kernel's share of dG, at the kv rows (bwd_dk adds the rest)
+        const int tk = kv_token(p.reverse, p.T, x.pos0 + tid);
+        if (tk >= 0) p.dg[((int64_t)x.s * p.T + tk) * p.H + x.hh] = sm.dG[tid];
+    }
+}
+
+// ------------------------------------------------------------------ dk ---
+struct DkP1 {  // until the products with h and dh' are done
+    bf16 vn[kChunk * kLK];
+    bf16 h[kKP * kLK];
+    bf16 dh[kKP * kLK];
+};
+struct DkP2 {  // afterwards
+    float t[kChunk * kPS];
+    bf16 tb[kChunk * kL6];
+    bf16 xw[kChunk * kLK];
+    bf16 y[kChunk * kL6];
+    bf16 z[kChunk * kL6];
+    bf16 ms[kChunk * kL6];
+};
+struct DkSmem {
+    bf16 k[kChunk * kLK], v[kChunk * kLK], dvn[kChunk * kLK], dw[kChunk * kLK];
+    union {
+        DkP1 a;
+        DkP2 b;
+    } u;
+    float kkg[kChunk * kPS];  // (K^ K^T . Gamma), strictly lower
+    float G[kChunk], graw[kChunk], beta[kChunk], rk[kChunk], dG[kChunk], dB[kChunk], row[kChunk];
+    float gc;  // dL/dG_C
+};
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) {
+    extern __shared__ __align__(16) unsigned char smraw[];
+    DkSmem &sm = *reinterpret_cast<DkSmem *>(smraw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const ChunkCtx x = chunk_ctx(p);
+    if (x.s >= p.B) return;
+    const int K = p.K, V = p.V, kq = round16(K), kv = round16(V);
+    const bf16 *k = (const bf16 *)p.k, *v = (const bf16 *)p.v;
+    auto kv_row = [&](int i) { return i < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + i) : -1; };
+
+    load_rows(sm.k, kLK, kChunk, K, kKP, [&](int i) -> const bf16 * {
+        const int tk = kv_row(i);
+        return tk < 0 ? nullptr : k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
+    });
+    load_rows(sm.v, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+        const int tk = kv_row(i);
+        return tk < 0 ? nullptr : v + x.s * p.v_sb + (int64_t)tk * p.v_st + x.hh * p.v_sh;
+    });
+    load_rows(sm.dvn, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+        return p.dvn_snap + (x.gch * kChunk + i) * V;
+    });
+    load_rows(sm.u.a.vn, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+        return p.vn_snap + (x.gch * kChunk + i) * V;
+    });
+    load_rows(sm.u.a.h, kLK, kKP, V, kKP, [&](int r) -> const bf16 * {
+        return r < K ? p.h_snap + (x.gch * K + r) * V : nullptr;
+    });
+    load_rows(sm.u.a.dh, kLK, kKP, V, kKP, [&](int r) -> const bf16 * {
+        return r < K ? p.dh_snap + (x.gch * K + r) * V : nullptr;
+    });
+    cp_async_commit();
+    if (tid < kChunk) sm.dG[tid] = sm.dB[tid] = sm.row[tid] = 0.f;
+    if (tid == 0) sm.gc = 0.f;
+    gates(p, x, sm.G, sm.beta, sm.graw);
+    cp_async_wait<0>();
+    __syncthreads();
+    norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
+    const int last = x.Lc - 1;
+    const float GC = sm.G[last];
+    // e^{G_C} h . dh'  (dG_C of the state decay)
+    {
+        float acc = 0.f;
+        for (int e = tid; e < K * (kv / 2); e += kThreads) {
+            const int r = e / (kv / 2), c2 = (e % (kv / 2)) * 2;
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.u.a.h + r * kLK + c2));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.u.a.dh + r * kLK + c2));
+            acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) atomicAdd(&sm.gc, acc * __expf(GC));
+    }
+    __syncthreads();
+
+    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
+    // S . Gamma, strictly lower
+    {
+        float sk[4][4];
+        acc_zero(sk);
+        warp_gemm(sk, Tile{sm.k, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = m0 + g8 + 8 * (e >> 1), j = n0 + 8 * n + 2 * t4 + (e & 1);
+                sm.kkg[i * kPS + j] = (j < i && i < x.Lc) ? __expf(sm.G[i] - sm.G[j]) * sk[n][e] : 0.f;
+            }
+    }
+    // dk^ starts with the kg term: e^{G_C - G} . (v_new dh'^T)
+    float dk[8][4];
+    {
+        acc_zero(dk);
+        warp_gemm(dk, Tile{sm.u.a.vn, kLK}, false, Tile{sm.u.a.dh, kLK}, false, m0, nk0, kv, lane);
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
+                const float f = i < x.Lc ? __expf(GC - sm.G[i]) : 0.f;
+                dk[n][e] *= f;
+                part[hf] += dk[n][e] * __bfloat162float(sm.k[i * kLK + d]);
+            }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float s = part[hf];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (t4 == 0 && s != 0.f) {  // kg_i = e^{G_C - G_i} k^_i
+                atomicAdd(&sm.dG[m0 + g8 + 8 * hf], -s);
+                atomicAdd(&sm.gc, s);
+            }
+        }
+    }
+    // dw = -v_new' ... = -(dv_new h^T)
+    {
+        float dw[8][4];
+        acc_zero(dw);
+        warp_gemm(dw, Tile{sm.dvn, kLK}, false, Tile{sm.u.a.h, kLK}, false, m0, nk0, kv, lane);
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+                *reinterpret_cast<uint32_t *>(sm.dw + (m0 + g8 + 8 * hf) * kLK + nk0 + 8 * n + 2 * t4) =
+                    pack_bf16(-dw[n][2 * hf], -dw[n][2 * hf + 1]);
+    }
+    __syncthreads();  // v_new, h, dh' are done with: their space takes T and the rest
+
+    // T = (I + A)^{-1}, A_ij = beta_i (S . Gamma)_ij (i > j), by 16 x 16 blocks
+    float *sT = sm.u.b.t;
+    for (int e = tid; e < kChunk * kPS; e += kThreads) sT[e] = 0.f;
+    __syncthreads();
+    if (warp < 4 && lane < 16) {  // diagonal blocks: forward substitution, lane = column
+        const int o = 16 * warp;
+        float t[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = (r == lane) ? 1.f : 0.f;
+#pragma unroll
+            for (int j = 0; j < r; ++j) acc = fmaf(-sm.beta[o + r] * sm.kkg[(o + r) * kPS + o + j], t[j], acc);
+            t[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(o + r) * kPS + o + lane] = t[r];
+    }
+    __syncthreads();
+    for (int I = 1; I < 4; ++I) {  // block row I: T_IJ = -T_II sum_{J <= M < I} A_IM T_MJ
+        const int n_el = 16 * 16 * I;  // rows 16I .. 16I+15, columns 0 .. 16I-1
+        float rr[3];
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {  // R_IJ = sum_{J <= M < I} A_IM T_MJ
+            const int e = tid + u * kThreads;
+            rr[u] = 0.f;
+            if (e < n_el) {
+                const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
+                float acc = 0.f;
+                for (int m = cidx & ~15; m < 16 * I; ++m)
+                    acc = fmaf(sm.beta[r] * sm.kkg[r * kPS + m], sT[m * kPS + cidx], acc);
+                rr[u] = acc;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int e = tid + u * kThreads;
+            if (e < n_el) sT[(16 * I + e / (16 * I)) * kPS + e % (16 * I)] = rr[u];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {  // T_IJ = -T_II R_IJ
+            const int e = tid + u * kThreads;
+            rr[u] = 0.f;
+            if (e < n_el) {
+                const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
+                float t = 0.f;
+#pragma unroll 4
+                for (int m = 0; m < 16; ++m) t = fmaf(sT[r * kPS + 16 * I + m], sT[(16 * I + m) * kPS + cidx], t);
+                rr[u] = -t;
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int e = tid + u * kThreads;
+            if (e < n_el) sT[(16 * I + e / (16 * I)) * kPS + e % (16 * I)] = rr[u];
+        }
+        __syncthreads();
+    }
+    // bf16 copies: T, and X_w = beta e^{G} . K^
+    for (int e = tid; e < kChunk * 32; e += kThreads) {
+        const int i = e >> 5, j = (e & 31) * 2;
+        *reinterpret_cast<uint32_t *>(sm.u.b.tb + i * kL6 + j) = pack_bf16(sT[i * kPS + j], sT[i * kPS + j + 1]);
+    }
+    for (int e = tid; e < kChunk * (kKP / 2); e += kThreads) {
+        const int i = e / (kKP / 2), d = (e % (kKP / 2)) * 2;
+        const float f = sm.beta[i] * __expf(sm.G[i]);
+        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.k + i * kLK + d));
+        *reinterpret_cast<uint32_t *>(sm.u.b.xw + i * kLK + d) = pack_bf16(f * kk.x, f * kk.y);
+    }
+    __syncthreads();
+    const Tile tT{sm.u.b.tb, kL6};
+    // Y = dv_new (beta . V)^T + dw X_w^T
+    {
+        float y[4][4];
+        acc_zero(y);
+        warp_gemm(y, Tile{sm.dvn, kLK}, false, Tile{sm.v, kLK}, false, m0, n0, kv, lane);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[n][e] *= sm.beta[n0 + 8 * n + 2 * t4 + (e & 1)];
+        warp_gemm(y, Tile{sm.dw, kLK}, false, Tile{sm.u.b.xw, kLK}, false, m0, n0, kq, lane);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+                *reinterpret_cast<uint32_t *>(sm.u.b.y + (m0 + g8 + 8 * hf) * kL6 + n0 + 8 * n + 2 * t4) =
+                    pack_bf16(y[n][2 * hf], y[n][2 * hf + 1]);
+    }
+    __syncthreads();
+    // Z = Y T^T
+    {
+        float z[4][4];
+        acc_zero(z);
+        warp_gemm(z, Tile{sm.u.b.y, kL6}, false, tT, false, m0, n0, kChunk, lane);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+                *reinterpret_cast<uint32_t *>(sm.u.b.z + (m0 + g8 + 8 * hf) * kL6 + n0 + 8 * n + 2 * t4) =
+                    pack_bf16(z[n][2 * hf], z[n][2 * hf + 1]);
+    }
+    __syncthreads();
+    // dA = -T^T Z (strictly lower): dbeta, dG, and dS = M_A + M_A^T
+    {
+        float a[4][4];
+        acc_zero(a);
+        warp_gemm(a, tT, true, Tile{sm.u.b.z, kL6}, true, m0, n0, kChunk, lane);
+        float pb[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hf = e >> 1, i = m0 + g8 + 8 * hf, j = n0 + 8 * n + 2 * t4 + (e & 1);
+                float ms = 0.f;
+                if (j < i && i < x.Lc) {
+                    const float da = -a[n][e], kk = sm.kkg[i * kPS + j];
+                    pb[hf] += da * kk;
+                    const float Aij = sm.beta[i] * kk, c = da * Aij;
+                    if (c != 0.f) {
+                        atomicAdd(&sm.dG[i], c);
+                        atomicAdd(&sm.dG[j], -c);
+                    }
+                    ms = da * sm.beta[i] * __expf(sm.G[i] - sm.G[j]);
+                }
+                if (j <= i) {  // (i, j) and its mirror; the diagonal stays 0
+                    sm.u.b.ms[i * kL6 + j] = __float2bfloat16_rn(ms);
+                    sm.u.b.ms[j * kL6 + i] = __float2bfloat16_rn(ms);
+                }
+            }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float s = pb[hf];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (t4 == 0 && s != 0.f) atomicAdd(&sm.dB[m0 + g8 + 8 * hf], s);
+        }
+    }
+    __syncthreads();
+    // dk^ += dS K^ + beta e^{G} . (T^T dw)
+    warp_gemm(dk, Tile{sm.u.b.ms, kL6}, false, Tile{sm.k, kLK}, true, m0, nk0, kChunk, lane);
+    {
+        float bw[8][4];
+        acc_zero(bw);
+        warp_gemm(bw, tT, true, Tile{sm.dw, kLK}, true, m0, nk0, kChunk, lane);
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
+                const float eg = __expf(sm.G[i]);
+                part[hf] += bw[n][e] * __bfloat162float(sm.k[i * kLK + d]);
+                dk[n][e] = fmaf(sm.beta[i] * eg, bw[n][e], dk[n][e]);
+            }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float s = part[hf];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            const int i = m0 + g8 + 8 * hf;
+            if (t4 == 0 && i < x.Lc && s != 0.f) {
+                const float eg = __expf(sm.G[i]);
+                atomicAdd(&sm.dB[i], eg * s);
+                atomicAdd(&sm.dG[i], sm.beta[i] * eg * s);
+            }
+        }
+    }
+    // plus bwd_dq's M_P^T Q^, then through the normalisation
+    {
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int i = m0 + g8 + 8 * hf;
+            const int tk = kv_row(i);
+            const float *src = tk >= 0 ? p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K : nullptr;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const int d = nk0 + 8 * n + 2 * t4;
+                if (src && d < K) {
+                    const float2 pp = *reinterpret_cast<const float2 *>(src + d);
+                    dk[n][2 * hf] += pp.x;
+                    dk[n][2 * hf + 1] += pp.y;
+                }
+                part[hf] += dk[n][2 * hf] * __bfloat162float(sm.k[i * kLK + d]) +
+                            dk[n][2 * hf + 1] * __bfloat162float(sm.k[i * kLK + d + 1]);
+            }
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float s = part[hf];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (t4 == 0) atomicAdd(&sm.row[m0 + g8 + 8 * hf], s);
+        }
+    }
+    // dB_u = T^T dv_new: dv and the beta term of u
+    {
+        float bu[8][4];
+        acc_zero(bu);
+        warp_gemm(bu, tT, true, Tile{sm.dvn, kLK}, true, m0, nk0, kChunk, lane);
+        float part[2] = {0.f, 0.f};
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int i = m0 + g8 + 8 * hf;
+            const int tk = kv_row(i);
+            float *dst = tk >= 0 ? p.dv + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * V : nullptr;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                const int c = nk0 + 8 * n + 2 * t4;
+                part[hf] += bu[n][2 * hf] * __bfloat162float(sm.v[i * kLK + c]) +
+                            bu[n][2 * hf + 1] * __bfloat162float(sm.v[i * kLK + c + 1]);
+                if (dst && c < V)
+                    *reinterpret_cast<float2 *>(dst + c) =
+                        make_float2(sm.beta[i] * bu[n][2 * hf], sm.beta[i] * bu[n][2 * hf + 1]);
+            }
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            float s = part[hf];
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            if (t4 == 0 && s != 0.f) atomicAdd(&sm.dB[m0 + g8 + 8 * hf], s);
+        }
+    }
+    __syncthreads();
+    // dk out
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int i = m0 + g8 + 8 * hf;
+        const int tk = kv_row(i);
+        if (tk < 0) continue;
+        float *dst = p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K;
+        const float r = sm.rk[i], dot = sm.row[i];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            const int d = nk0 + 8 * n + 2 * t4;
+            if (d >= K) continue;
+            float2 o;
+            o.x = p.l2norm ? r * (dk[n][2 * hf] - __bfloat162float(sm.k[i * kLK + d]) * dot) : dk[n][2 * hf];
+            o.y = p.l2norm ? r * (dk[n][2 * hf + 1] - __bfloat162float(sm.k[i * kLK + d + 1]) * dot)
+                           : dk[n][2 * hf + 1];
+            *reinterpret_cast<float2 *>(dst + d) = o;
+        }
+    }
+    // the reverse scan never reads token 0's key and value: zero gradients
+    if (p.reverse && x.c == 0) {
+        const int64_t row = (int64_t)x.s * p.T * p.H + x.hh;
+        for (int e = tid; e < K; e += kThreads) p.dk[row * K + e] = 0.f;
+        for (int e = tid; e < V; e += kThreads) p.dv[row * V + e] = 0.f;
+        if (tid == 0) p.dbeta[row] = p.dg[row] = 0.f;
+    }
+    // dbeta, and dg = suffix sums of dG within the chunk (G is the running sum of g)
+    if (warp == 0) {
+        float d0 = 0.f, d1 = 0.f;
+        const int i0 = 2 * lane, i1 = 2 * lane + 1;
+        const int t0 = kv_row(i0), t1 = kv_row(i1);
+        if (t0 >= 0) d0 = sm.dG[i0] + p.dg[((int64_t)x.s * p.T + t0) * p.H + x.hh];
+        if (t1 >= 0) d1 = sm.dG[i1] + p.dg[((int64_t)x.s * p.T + t1) * p.H + x.hh];
+        if (i0 == last) d0 += sm.gc;
+        if (i1 == last) d1 += sm.gc;
+        // suffix sum over lanes of the pair sums
+        float incl = d0 + d1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_down_sync(0xffffffffu, incl, o);
+            if (lane + o < 32) incl += y;
+        }
+        const float s1 = incl - d0, s0 = incl;  // dg at i1 and at i0
+        if (t0 >= 0) {
+            const int64_t row = ((int64_t)x.s * p.T + t0) * p.H + x.hh;
+            p.dg[row] = sm.graw[i0] < kLogGateMin ? 0.f : s0;
+            p.dbeta[row] = sm.dB[i0];
+        }
+        if (t1 >= 0) {
+            const int64_t row = ((int64_t)x.s * p.T + t1) * p.H + x.hh;
+            p.dg[row] = sm.graw[i1] < kLogGateMin ? 0.f : s1;
+            p.dbeta[row] = sm.dB[i1];
+        }
+    }
+}
+
+template <class Kern>
+cudaError_t launch_grid(Kern kern, int bytes, const BwdParams &p, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    const int nts = (p.T + kChunk - 1) / kChunk;
+    kern<<<p.B * nts * p.H, kThreads, bytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq(const BwdParams &p, cudaStream_t st) {
+    return launch_grid(bwd_dq_kernel, (int)sizeof(DqSmem), p, st);
+}
+cudaError_t launch_bwd_dk(const BwdParams &p, cudaStream_t st) {
+    return launch_grid(bwd_dk_kernel, (int)sizeof(DkSmem), p, st);
+}
+
+}  // namespace gdn

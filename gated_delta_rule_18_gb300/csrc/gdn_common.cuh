@@ -62,6 +62,29 @@ struct FwdParams {
     float *sum_ext;      // (segments, n_seq * H, K, Vt)
     float *sum_tr;       // (segments, n_seq * H, K, K)
     const float *h_in;   // (segments, n_seq * H, K, Vt)
+    // Recompute pass of the backward: when set, the state kernel also stores
+    // the state entering every chunk and the chunk's v_new, bf16, indexed
+    // [head][global chunk]: h_snap (K, V) rows, vn_snap (64, V) rows.
+    __nv_bfloat16 *h_snap, *vn_snap;
+};
+
+// Everything the backward kernels need (dense batches, scalar gate). The
+// gradient outputs are fp32 and contiguous: dq, dk (B, T, H, K), dv (B, T,
+// H, V), dbeta, dg (B, T, H), dh0 (B, H, K, V).
+struct BwdParams {
+    const void *q, *k, *v, *dout;
+    int64_t qk_sb, qk_st, qk_sh;
+    int64_t v_sb, v_st, v_sh;
+    int64_t do_sb, do_st, do_sh;
+    const float *g, *beta, *dh_final;
+    float *dq, *dk, *dv, *dbeta, *dg, *dh0;
+    int B, T, H, K, V, reverse, l2norm;
+    int max_chunks;  // chunks per head: B * ceil(T / 64)
+    // the forward's per-chunk operand images and snapshots (workspace)
+    const unsigned char *w_img, *qg_img, *kg_img, *p_img;
+    const float *dec;
+    const __nv_bfloat16 *h_snap, *vn_snap;
+    __nv_bfloat16 *dh_snap, *dvn_snap;  // state gradient at each chunk's end, dL/dv_new
 };
 
 // ----------------------------------------------------- operand images -------
@@ -305,6 +328,9 @@ struct SegParams {
     int n_bh, K, V, Vt, n_seg;
 };
 cudaError_t launch_seg_combine(const SegParams &p, cudaStream_t st);
+cudaError_t launch_bwd_dh(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_dq(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_dk(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);
 cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, void *y,
                         int64_t ysb, int64_t yst, int64_t ysh, int B, int T, int H, int D,

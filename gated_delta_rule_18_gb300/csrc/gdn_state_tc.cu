@@ -209,8 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 f[2 * x + 1] = t.y - __uint_as_float(rr[8 * j + 2 * x + 1]);
             }
             // MN-major B operand (N = column, K = token): (col/8)*1024 + i*16
-            *reinterpret_cast<uint4 *>(sm + Lay::vn + par * Lay::vn_bytes + (c0 / 8 + j) * 1024 + i * 16) =
-                pack8(f);
+            const uint4 pv = pack8(f);
+            *reinterpret_cast<uint4 *>(sm + Lay::vn + par * Lay::vn_bytes + (c0 / 8 + j) * 1024 + i * 16) = pv;
+            if (p.vn_snap && v0 + c0 + 8 * j < V)
+                *reinterpret_cast<uint4 *>(p.vn_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * kChunk + i) * V +
+                                           v0 + c0 + 8 * j) = pv;
         }
     };
 
@@ -236,9 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             const uint32_t par = c & 1;
             // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16; its last
             // reader, chunk c-1's first product, finished before that chunk's dh
+            bf16 *hs = p.h_snap ? p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * V + v0 : nullptr;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = pack8(&h[8 * j]);
+            for (int j = 0; j < 8; ++j) {
+                const uint4 hv = pack8(&h[8 * j]);
+                *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = hv;
+                if (hs && r < K && v0 + 8 * j < V) *reinterpret_cast<uint4 *>(hs + 8 * j) = hv;
+            }
             fence_async_smem();
             arrive(b_h);
             ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             arrive(b_of[c & 1]);
             const int pos0 = (cb + c) * kChunk;
             const int Lc = min(kChunk, si.len - pos0);
-            if (!ok || i >= Lc || p.summary) continue;
+            if (!ok || i >= Lc || p.summary || !p.out) continue;  // no output: summary or recompute pass
             const int tq = q_token(p.reverse, si.len, pos0 + i);
             const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
 #pragma unroll

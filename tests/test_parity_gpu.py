@@ -367,3 +367,64 @@ def test_full_size_segmented_long_sequence():
     e_o = rel_err(got["out"][:, :, heads], ref["out"])
     e_h = rel_err(got["h_final"][:, heads], ref["h_final"])
     assert e_o <= TOL["bf16"] and e_h <= TOL["bf16"], (e_o, e_h)
+
+
+# ------------------------------------------------------------------ backward ---
+
+BWD = {
+    "k64_h0_l2": dict(B=2, T=200, H=2, K=64, V=64, h0_std=0.5),
+    "k128_v128": dict(B=1, T=333, H=2, K=128, V=128, h0_std=0.5),
+    "k112_v112": dict(B=1, T=130, H=2, K=112, V=112),
+    "k32_v96": dict(B=1, T=97, H=3, K=32, V=96),
+    "t64": dict(B=1, T=64, H=2, K=128, V=128, h0_std=0.5),
+    "t1": dict(B=2, T=1, H=2, K=64, V=64, h0_std=0.5),
+}
+
+
+def _bwd_compare(w, reverse=False, seed=21):
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    rng = np.random.default_rng(seed)
+    dout = workloads.stored_normal(seed, "dout", (w.B, w.T, w.H, w.V), "bf16")
+    dhf = None if reverse else rng.standard_normal((w.B, w.H, w.K, w.V)).astype(np.float32)
+    h0 = None if reverse else w.h0
+    ref = backward.scan_grad(w.q.values, w.k.values, w.v.values, w.beta, w.g, dout.values,
+                             h0=h0, dh_final=dhf, reverse=reverse, l2norm=True)
+    got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(dout), h0=f32_dev(h0), dh_final=f32_dev(dhf), reverse=reverse,
+                            qk_l2norm=True)
+    torch().cuda.synchronize()
+    errs = {n: rel_err(got[n].double().cpu().numpy(), ref[n]) for n in got}
+    assert all(e <= 3e-2 for e in errs.values()), (w.name, errs)
+    return errs
+
+
+@pytest.mark.parametrize("name", sorted(BWD))
+def test_small_backward(name):
+    w = workloads.make(**BWD[name], seed=17, name="bwd_" + name)
+    _bwd_compare(w)
+
+
+def test_small_backward_reverse():
+    w = workloads.make(1, 64 * 3 + 9, 2, 64, 64, seed=18, name="bwd_reverse")
+    _bwd_compare(w, reverse=True)
+
+
+def test_full_size_backward():
+    """the 4 x 4096-token, 16-head, K = V = 128 causal workload: gradients of
+    every head on the GPU, two (sequence, head) pairs against the oracle"""
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    w = workloads.build("causal_bf16_b4h16t4096d128")
+    dout = workloads.stored_normal(5, "dout", (w.B, w.T, w.H, w.V), "bf16")
+    got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(dout), qk_l2norm=True)
+    torch().cuda.synchronize()
+    got = {n: t.double().cpu().numpy() for n, t in got.items()}
+    for b, h in ((0, 3), (3, 15)):
+        sel = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        ref = backward.scan_grad(w.q.values[sel], w.k.values[sel], w.v.values[sel], w.beta[sel],
+                                 w.g[sel], dout.values[sel], l2norm=True)
+        errs = {n: rel_err(got[n][sel], ref[n]) for n in ("dq", "dk", "dv", "dbeta", "dg")}
+        errs["dh0"] = rel_err(got["dh0"][b:b + 1, h:h + 1], ref["dh0"])
+        assert all(e <= 3e-2 for e in errs.values()), (b, h, errs)

@@ -31,7 +31,7 @@ import numpy as np
 BLOCK = 1 << 22  # elements per independently seeded block
 
 _TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "g": 5, "gk": 6, "h0": 7,
-               "lens": 8, "qkv": 9, "gate": 10, "g_frame": 11}
+               "lens": 8, "qkv": 9, "gate": 10, "g_frame": 11, "dout": 12}
 
 
 def _normal_fill(seed: int, name: str, n: int, mu: float, sigma: float,
