@@ -56,7 +56,8 @@ constexpr int kDevErrTimeout = 2;
 
 // Shared memory. The scalar-gate kernel copies the value tile into the q
 // tile's space once qg is written; the per-key kernel keeps it apart (its
-// space first holds the three split operands of step 2).
+// space first holds the two split operands of step 2) and puts T's blocks
+// over its gate tile, so that two per-key CTAs fit on an SM.
 template <bool PERKEY>
 struct Lay {
     static constexpr int KP = kKP;
@@ -69,13 +70,14 @@ struct Lay {
     static constexpr size_t rk = rq + 4 * kChunk;
     static constexpr size_t ab = rk + 4 * kChunk;
     static constexpr size_t ad = ab + 2 * 6 * 16 * kBS;
-    static constexpr size_t td = ad + 4 * 4 * 16 * kAdS;
-    static constexpr size_t q = td + 3 * 2 * kTSet;
+    // per key, T's blocks take the gate tile's space once the gates are used up
+    static constexpr size_t td = PERKEY ? gates : ad + 4 * 4 * 16 * kAdS;
+    static constexpr size_t q = PERKEY ? ad + 4 * 4 * 16 * kAdS : td + 3 * 2 * kTSet;
     static size_t vtile(int VP) { return (size_t)2 * kChunk * (VP + 8); }
     static constexpr size_t v = PERKEY ? q + tile : q;
     static size_t bytes(int VP) {
         if (PERKEY) {
-            const size_t a = vtile(VP), b = 3 * tile;
+            const size_t a = vtile(VP), b = 2 * tile;
             return q + tile + (a > b ? a : b);
         }
         const size_t a = vtile(VP);
@@ -103,6 +105,17 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
     u.w = pack_bf16(f[6], f[7]);
     return u;
 }
+constexpr float kLog2e = 1.4426950408889634f;
+// 2^x (the per-key gates are kept in base 2)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void ld8f(const float *p, float *f) {  // 16-byte aligned
+    const float4 a = *reinterpret_cast<const float4 *>(p), b = *reinterpret_cast<const float4 *>(p + 4);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
 __device__ __forceinline__ void zero_row(bf16 *row, int from, int to) {  // 8-aligned bounds
     for (int d = from; d < to; d += 8) *reinterpret_cast<uint4 *>(row + d) = make_uint4(0, 0, 0, 0);
 }
@@ -116,7 +129,7 @@ __device__ __forceinline__ bool wait_copies(uint32_t bar, int *err) {
 }
 
 template <bool PERKEY>
-__global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const FwdParams p, int VP) {
+__global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const FwdParams p, int VP) {
     using L = Lay<PERKEY>;
     constexpr int KP = kKP;
     constexpr int KS = L::KS;
@@ -346,56 +359,89 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const F
             }
             (tid < 64 ? sRq : sRk)[r] = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
         }
-        for (int d = tid; d < KP; d += kThreads) {  // per-channel cumsums
-            float acc = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < kChunk; ++i) {
-                acc += fmaxf(sG[i * KP + d], kLogGateMinPerKeyTC);
-                sG[i * KP + d] = acc;
-            }
+        {  // per-channel cumsums: thread d keeps its channel's 64 gates in registers
+            static_assert(kThreads == KP, "one thread per key channel");
+            const int d = tid;
+            float a[kChunk];
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) a[i] = fmaxf(sG[i * KP + d], kLogGateMinPerKeyTC);
+#pragma unroll
+            for (int i = 1; i < kChunk; ++i) a[i] += a[i - 1];
+            // kept in base 2 (G log2 e): every factor below is then one ex2
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) sG[i * KP + d] = a[i] * kLog2e;
         }
         // Per-key gate: for column block J split e^{G_i - G_j} about the
         // block's middle row r = 16J + 8: left x_i^ . e^{G_i - G_r} (rows
         // i >= 16J), right k_j^ . e^{G_r - G_j} (rows of block J). Each factor
         // spans at most 8 tokens of decay, so with the -10 floor it stays
-        // below e^80; entries with j > i are discarded, never used.
-        bf16 *sR = sV;
-        bf16 *sLq = sR + kChunk * KS;
-        bf16 *sLk = sLq + kChunk * KS;
+        // below e^80; entries with j > i are discarded, never used. Eight
+        // channels per step (16-byte loads and stores).
+        bf16 *sR = sV;                // right factors, all 64 rows
+        bf16 *sL = sR + kChunk * KS;  // left factors of keys, then of queries
         __syncthreads();
-        for (int e = tid; e < kChunk * KP; e += kThreads) {
-            const int i = e / KP, d = e % KP, r = (i & ~15) + 8;
-            const float f = __expf(sG[r * KP + d] - sG[i * KP + d]) * sRk[i];
-            sR[i * KS + d] = __float2bfloat16_rn(__bfloat162float(sK[i * KS + d]) * f);
+        for (int e = tid; e < kChunk * (KP / 8); e += kThreads) {
+            const int i = e / (KP / 8), d = (e % (KP / 8)) * 8, r = (i & ~15) + 8;
+            float gi[8], gr[8], kx[8], o[8];
+            ld8f(sG + i * KP + d, gi);
+            ld8f(sG + r * KP + d, gr);
+            unpack8(*reinterpret_cast<const uint4 *>(sK + i * KS + d), kx);
+            const float rk = sRk[i];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) o[x] = kx[x] * (ex2(gr[x] - gi[x]) * rk);
+            *reinterpret_cast<uint4 *>(sR + i * KS + d) = pack8(o);
         }
         for (int J = 0; J < 4; ++J) {
-            __syncthreads();
             const int r0 = 16 * J, r = r0 + 8;
-            for (int e = tid; e < (kChunk - r0) * KP; e += kThreads) {
-                const int i = r0 + e / KP, d = e % KP;
-                const float f = __expf(sG[i * KP + d] - sG[r * KP + d]);
-                sLq[i * KS + d] = __float2bfloat16_rn(__bfloat162float(sQ[i * KS + d]) * f * sRq[i]);
-                sLk[i * KS + d] = __float2bfloat16_rn(__bfloat162float(sK[i * KS + d]) * f * sRk[i]);
-            }
-            __syncthreads();
-            if (warp >= J) {
-                float ak[2][4], ap[2][4];
+            float ak[2][4], ap[2][4];
 #pragma unroll
-                for (int n = 0; n < 2; ++n)
+            for (int n = 0; n < 2; ++n)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) ak[n][e] = ap[n][e] = 0.f;
+                for (int e = 0; e < 4; ++e) ak[n][e] = ap[n][e] = 0.f;
+            // this thread's items: (64 - r0) rows x 16 eight-channel groups
+            // over the block, at most 8 each; the factors e^{G_i - G_r} of
+            // the key pass stay in registers for the query pass
+            const int n_items = (kChunk - r0) * (KP / 8);
+            float fct[8][8];
 #pragma unroll
-                for (int kk = 0; kk < KP / 16; ++kk) {
-                    uint32_t aK[4], aQ[4], b[4];
-                    ldsm_x4(aK, sLk + (16 * warp + (lane & 15)) * KS + kk * 16 + (lane >> 4) * 8);
-                    ldsm_x4(aQ, sLq + (16 * warp + (lane & 15)) * KS + kk * 16 + (lane >> 4) * 8);
-                    ldsm_x4(b, sR + (r0 + (lane & 7) + ((lane >> 4) << 3)) * KS + kk * 16 +
-                                   ((lane >> 3) & 1) * 8);
-                    mma_bf16(ak[0], aK, b[0], b[1]);
-                    mma_bf16(ak[1], aK, b[2], b[3]);
-                    mma_bf16(ap[0], aQ, b[0], b[1]);
-                    mma_bf16(ap[1], aQ, b[2], b[3]);
+            for (int pass = 0; pass < 2; ++pass) {  // 0: keys (A), 1: queries (P)
+                __syncthreads();  // the previous product has read sL
+                const bf16 *src = pass ? sQ : sK;
+                const float *rs = pass ? sRq : sRk;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int e = tid + u * kThreads;
+                    if (e >= n_items) break;
+                    const int i = r0 + e / (KP / 8), d = (e % (KP / 8)) * 8;
+                    if (pass == 0) {
+                        float gi[8], gr[8];
+                        ld8f(sG + i * KP + d, gi);
+                        ld8f(sG + r * KP + d, gr);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) fct[u][x] = ex2(gi[x] - gr[x]);
+                    }
+                    float xx[8], o[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(src + i * KS + d), xx);
+                    const float rr = rs[i];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) o[x] = xx[x] * fct[u][x] * rr;
+                    *reinterpret_cast<uint4 *>(sL + i * KS + d) = pack8(o);
                 }
+                __syncthreads();
+                if (warp >= J) {
+#pragma unroll
+                    for (int kk = 0; kk < KP / 16; ++kk) {
+                        uint32_t aL[4], b[4];
+                        ldsm_x4(aL, sL + (16 * warp + (lane & 15)) * KS + kk * 16 + (lane >> 4) * 8);
+                        ldsm_x4(b, sR + (r0 + (lane & 7) + ((lane >> 4) << 3)) * KS + kk * 16 +
+                                       ((lane >> 3) & 1) * 8);
+                        float(&acc)[2][4] = pass ? ap : ak;
+                        mma_bf16(acc[0], aL, b[0], b[1]);
+                        mma_bf16(acc[1], aL, b[2], b[3]);
+                    }
+                }
+            }
+            if (warp >= J) {
 #pragma unroll
                 for (int n = 0; n < 2; ++n) {
 #pragma unroll
@@ -448,14 +494,15 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const F
             unpack8(xq[u], fq);
             unpack8(xk[u], fk);
             if (PERKEY) {
-                float fx[8];
+                float fx[8], gi8[8], gl8[8];
+                ld8f(sG + i * KP + d0, gi8);
+                ld8f(sG + last * KP + d0, gl8);
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
-                    const float Gi = sG[i * KP + d0 + x];
-                    const float eg = __expf(Gi);
+                    const float eg = ex2(gi8[x]);
                     fx[x] = fk[x] * eg;  // e^{G} . k (raw k: the norm goes into T's columns)
                     fq[x] *= eg * sq[u];
-                    fk[x] *= __expf(sG[last * KP + d0 + x] - Gi) * sk[u];
+                    fk[x] *= ex2(gl8[x] - gi8[x]) * sk[u];
                 }
                 *reinterpret_cast<uint4 *>(sK + i * KS + d0) = pack8(fx);
             } else {
@@ -471,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 1 : 4) intra_kernel(const F
         }
     }
     for (int d = tid; d < KP; d += kThreads)
-        p.dec[gch * KP + d] = PERKEY ? __expf(sG[last * KP + d]) : __expf(sG[last]);
+        p.dec[gch * KP + d] = PERKEY ? ex2(sG[last * KP + d]) : __expf(sG[last]);
     fence_async_smem();  // these generic accesses come before the copies that reuse the space
     __syncthreads();     // the q tile (scalar gate) and the split operands (per key) are free
 
@@ -619,6 +666,9 @@ cudaError_t launch_t(const FwdParams &p, cudaStream_t st) {
     const size_t bytes = L::bytes(VP);
     auto kern = intra_kernel<PERKEY>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    // the whole shared-memory carveout, so that 4 (scalar) / 2 (per-key) CTAs fit per SM
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)p.max_chunks * (unsigned)p.H);
     kern<<<grid, kThreads, bytes, st>>>(p, VP);
