@@ -597,7 +597,7 @@ bool frame_ws(int B, int T, int H, int K, int V, int frame, int with_den, FrameW
     L.bmat = off;
     off = align_up(off + bh * F * K * Vt * 4);
     L.sout = off;
-    off = align_up(off + bh * F * K * Vt * 4);
+    off = align_up(off + bh * F * K * ((Vt + 7) / 8 * 8) * 4);
     L.total = off > 0 ? off : kAlign;
     return true;
 }
@@ -640,6 +640,7 @@ gdn_status gdn_frame_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     p.out_f32 = od.dtype == GDN_F32;
     p.den = den_out;
     p.B = B, p.T = T, p.H = H, p.K = K, p.V = V, p.Vt = V + (den_out ? 1 : 0);
+    p.Vs = (p.Vt + 7) / 8 * 8;
     p.F = T / frame, p.frame = frame;
     p.has_den = den_out != nullptr;
     p.accumulate = (flags & GDN_ACCUMULATE) != 0;

@@ -309,6 +309,7 @@ struct FrameParams {
     int out_f32;
     float *den;  // (B, H, T) or null
     int B, T, H, K, V, Vt, F, frame;
+    int Vs;  // row stride of sout: Vt rounded up to a multiple of 8
     int has_den, accumulate, direction;  // direction: 0 forward, 1 reverse, 2 both summed
     float *amat, *bmat, *sout;           // workspace: A_f (K x K), B_f (K x Vt), read states (K x Vt)
 };

@@ -12,15 +12,15 @@
 // only the short chain over frames is serial, and the reverse direction
 // (frame f reads frames f+1 .. F-1) runs the same chain backwards over the
 // same A_f, B_f. Three kernels:
-//   frame_gram   per (sequence, head, frame, 64-column block): C = K^T diag(beta)
+//   frame_gram   per (sequence, head, frame, 128-column block): C = K^T diag(beta)
 //                [K | V | 1] over the frame's tokens on tensor cores (mma.sync
-//                bf16, fp32 accumulate); A_f = I - C_KK, B_f = C_KV to the
-//                workspace (fp32)
-//   frame_chain  per (sequence, head, 16-column tile): the fp32 chains
+//                bf16, fp32 accumulate), chunks streamed one ahead; A_f = I -
+//                C_KK, B_f = C_KV to the workspace (fp32)
+//   frame_chain  per (sequence, head, 32-column tile): the fp32 chains
 //                S_f = A_f (e^{g_f} S_{f-1}) + B_f forward and / or reverse
-//                (A_f staged in shared memory per step), the states each
-//                frame's outputs read summed over directions
-//   frame_out    per (sequence, head, 64-token chunk, 64-column block):
+//                (the next A_f copied in while the current one is applied),
+//                the states each frame's outputs read summed over directions
+//   frame_out    per (sequence, head, 64-token chunk, 128-column block):
 //                O = Q S_f on tensor cores; the ones column gives den
 #include "gdn_common.cuh"
 
@@ -38,13 +38,54 @@ __device__ __forceinline__ const bf16 *row_ptr(const void *base, int64_t sb, int
 }
 
 // ---------------------------------------------------------------- gram ---
-__global__ void __launch_bounds__(128) frame_gram_kernel(const FrameParams p) {
-    __shared__ __align__(16) bf16 sKb[kChunk * kKS];  // beta . k, [token][key]
-    __shared__ __align__(16) bf16 sX[kChunk * kXS];   // [K | V | 1] columns of this block
+// One CTA (8 warps) per (sequence x head, frame, 128-column block of
+// [K | V | 1]); warp w owns keys 32 (w & 3) .. + 31 and the block's column
+// half w >> 2. The frame's 64-token chunks stream through two stages
+// (cp.async one chunk ahead): raw k rows and the block's columns, the latter
+// scaled by beta in place once they land, so C = K^T (diag(beta) X).
+constexpr int kXB = 128 + 8;  // bf16 row stride of a 128-column tile
+struct GramStage {
+    bf16 k[kChunk * kKS];  // raw k, [token][key]
+    bf16 x[kChunk * kXB];  // [K | V | 1] columns of this block, [token][column]
+    float beta[kChunk];
+};
+struct GramSmem {
+    GramStage st[2];
+};
+__global__ void __launch_bounds__(256) frame_gram_kernel(const FrameParams p) {
+    extern __shared__ __align__(16) unsigned char smraw[];
+    GramSmem &sm = *reinterpret_cast<GramSmem *>(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H, f = blockIdx.y, cb = blockIdx.z;
     const int K = p.K, V = p.V, Vt = p.Vt;
-    const int col0 = cb * 64;  // columns [0, 128) are keys, [128, 128 + Vt) values (+ ones)
+    const int col0 = cb * 128;  // columns [0, 128) are keys, [128, 128 + Vt) values (+ ones)
+    const int nc = p.frame / kChunk;
+    const bf16 *kp = (const bf16 *)p.k, *vp = (const bf16 *)p.v;
+
+    auto stage = [&](int c) {
+        GramStage &S = sm.st[c & 1];
+        const int64_t t0 = (int64_t)f * p.frame + (int64_t)c * kChunk;
+        for (int e = tid; e < kChunk * (kKP / 8); e += 256) {  // k rows
+            const int i = e / (kKP / 8), d = (e % (kKP / 8)) * 8;
+            const bool in = d < K;
+            const bf16 *src = kp + b * p.qk_sb + (t0 + i) * p.qk_st + h * p.qk_sh + d;
+            cp_async16(S.k + i * kKS + d, in ? src : kp, in ? 16 : 0);
+        }
+        for (int e = tid; e < kChunk * 16; e += 256) {  // the block's 128 columns
+            const int i = e >> 4, cc = (e & 15) * 8, col = col0 + cc;
+            const bf16 *src = kp;
+            int nb = 0;
+            if (col < kKP) {
+                if (col < K) src = kp + b * p.qk_sb + (t0 + i) * p.qk_st + h * p.qk_sh + col, nb = 16;
+            } else if (col - kKP + 8 <= V) {
+                src = vp + b * p.v_sb + (t0 + i) * p.v_st + h * p.v_sh + (col - kKP), nb = 16;
+            }
+            cp_async16(S.x + i * kXB + cc, src, nb);
+        }
+        cp_async_commit();
+        if (tid < kChunk) S.beta[tid] = p.beta[((int64_t)b * p.T + t0 + tid) * p.H + h];
+    };
+
     float acc[2][8][4];
 #pragma unroll
     for (int m = 0; m < 2; ++m)
@@ -52,61 +93,47 @@ __global__ void __launch_bounds__(128) frame_gram_kernel(const FrameParams p) {
         for (int n = 0; n < 8; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.f;
-
-    for (int c = 0; c < p.frame / kChunk; ++c) {
-        const int64_t t0 = (int64_t)f * p.frame + (int64_t)c * kChunk;
-        __syncthreads();  // the previous chunk's tiles are no longer read
-        for (int e = tid; e < kChunk * (kKP / 8); e += 128) {
-            const int i = e / (kKP / 8), d = (e % (kKP / 8)) * 8;
-            const float bt = p.beta[((int64_t)b * p.T + t0 + i) * p.H + h];
-            float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (d < K) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(
-                    row_ptr(p.k, p.qk_sb, p.qk_st, p.qk_sh, b, t0 + i, h) + d);
-                const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 t = __bfloat1622float2(u2[j]);
-                    x[2 * j] = t.x * bt;
-                    x[2 * j + 1] = t.y * bt;
-                }
-            }
-            uint4 o;
-            o.x = pack_bf16(x[0], x[1]);
-            o.y = pack_bf16(x[2], x[3]);
-            o.z = pack_bf16(x[4], x[5]);
-            o.w = pack_bf16(x[6], x[7]);
-            *reinterpret_cast<uint4 *>(sKb + i * kKS + d) = o;
+    const int mw = 32 * (warp & 3), nw = 64 * (warp >> 2);
+    stage(0);
+    for (int c = 0; c < nc; ++c) {
+        GramStage &S = sm.st[c & 1];
+        if (c + 1 < nc) {
+            stage(c + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
-        for (int e = tid; e < kChunk * 8; e += 128) {
-            const int i = e / 8, cc = (e % 8) * 8, col = col0 + cc;
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (col < kKP) {
-                if (col < K) o = *reinterpret_cast<const uint4 *>(row_ptr(p.k, p.qk_sb, p.qk_st, p.qk_sh, b, t0 + i, h) + col);
-            } else {
-                const int vc = col - kKP;
-                if (vc + 8 <= V) {
-                    o = *reinterpret_cast<const uint4 *>(row_ptr(p.v, p.v_sb, p.v_st, p.v_sh, b, t0 + i, h) + vc);
-                } else if (p.has_den && vc <= V && V < vc + 8) {
-                    // the ones column sits at value column V (V is a multiple of 8)
-                    o.x = pack_bf16(1.f, 0.f);
-                }
+        __syncthreads();  // chunk c landed everywhere
+        // beta . X in place (and the ones column of the denominator)
+        for (int e = tid; e < kChunk * 16; e += 256) {
+            const int i = e >> 4, cc = (e & 15) * 8, col = col0 + cc;
+            uint4 u = *reinterpret_cast<const uint4 *>(S.x + i * kXB + cc);
+            if (p.has_den && col >= kKP && col - kKP <= V && V < col - kKP + 8) {
+                // the ones column sits at value column V (V is a multiple of 8)
+                u = make_uint4(pack_bf16(1.f, 0.f), 0, 0, 0);
             }
-            *reinterpret_cast<uint4 *>(sX + i * kXS + cc) = o;
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
+            const float bt = S.beta[i];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float2 t = __bfloat1622float2(h2[x]);
+                h2[x] = __floats2bfloat162_rn(t.x * bt, t.y * bt);
+            }
+            *reinterpret_cast<uint4 *>(S.x + i * kXB + cc) = u;
         }
         __syncthreads();
-        // C[key m][col n] += sum_token Kb[token][m] X[token][n]; warp w: keys 32w..32w+31
+        // C[key m][col n] += sum_token K[token][m] (beta X)[token][n]
 #pragma unroll
         for (int ks = 0; ks < kChunk / 16; ++ks) {
             uint32_t a[2][4];
 #pragma unroll
             for (int m = 0; m < 2; ++m)
-                ldsm_x4_t(a[m], sKb + (ks * 16 + (lane & 7) + ((lane >> 4) << 3)) * kKS + 32 * warp + 16 * m +
+                ldsm_x4_t(a[m], S.k + (ks * 16 + (lane & 7) + ((lane >> 4) << 3)) * kKS + mw + 16 * m +
                                     ((lane >> 3) & 1) * 8);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 uint32_t bb[4];
-                ldsm_x4_t(bb, sX + (ks * 16 + (lane & 15)) * kXS + 16 * np + (lane >> 4) * 8);
+                ldsm_x4_t(bb, S.x + (ks * 16 + (lane & 15)) * kXB + nw + 16 * np + (lane >> 4) * 8);
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     mma_bf16(acc[m][2 * np], a[m], bb[0], bb[1]);
@@ -114,6 +141,7 @@ __global__ void __launch_bounds__(128) frame_gram_kernel(const FrameParams p) {
                 }
             }
         }
+        __syncthreads();  // this stage is refilled next
     }
     // A_f = I - C (key columns), B_f = C (value columns)
     const int64_t fi = ((int64_t)blockIdx.x * p.F + f);
@@ -124,8 +152,8 @@ __global__ void __launch_bounds__(128) frame_gram_kernel(const FrameParams p) {
         for (int n = 0; n < 8; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int row = 32 * warp + 16 * m + g8 + 8 * (e >> 1);
-                const int col = col0 + 8 * n + 2 * t4 + (e & 1);
+                const int row = mw + 16 * m + g8 + 8 * (e >> 1);
+                const int col = col0 + nw + 8 * n + 2 * t4 + (e & 1);
                 if (row >= K) continue;
                 if (col < kKP) {
                     if (col < K) p.amat[(fi * K + row) * K + col] = (row == col ? 1.f : 0.f) - acc[m][n][e];
@@ -136,119 +164,163 @@ __global__ void __launch_bounds__(128) frame_gram_kernel(const FrameParams p) {
 }
 
 // --------------------------------------------------------------- chain ---
-constexpr int kCT = 16;        // state columns per chain CTA
-constexpr int kAS = kKP + 1;   // fp32 row stride of A_f in shared memory (conflict-free rows)
+// Thread (rb, cq) keeps rows 4 rb .. 4 rb + 3 and columns 4 cq .. 4 cq + 3 of
+// the CTA's 32-column state tile (one wave of CTAs for the video shapes);
+// A_f is symmetric (I - K^T diag(beta) K), so row a of A_f holds column a,
+// and a thread's four rows of A_f S come from one 16-byte load of row a per
+// step of the sum. The next frame's A_f is copied in (cp.async) while the
+// current one is applied.
+constexpr int kCT = 32;  // state columns per chain CTA
 struct ChainSmem {
-    float a[kKP * kAS];        // A_f, [key][key]
-    float s[kKP * kCT];        // the state tile, [key][column]
-    float n[kKP * kCT];
+    float a[2][kKP * kKP];  // A_f of this step and of the next
+    float s[kKP * kCT];     // the state tile, [key][column]
 };
-__global__ void __launch_bounds__(256) frame_chain_kernel(const FrameParams p) {
+__device__ __forceinline__ void stage_a(const FrameParams &p, ChainSmem &sm, int buf, int64_t fi) {
+    // thread t copies 16-byte piece t % 32 of rows t / 32, t / 32 + 8, ...
+    const int K = p.K, c = (threadIdx.x & 31) * 4;
+    const float *A = p.amat + fi * K * K;
+    if (c < K)
+        for (int r = threadIdx.x >> 5; r < K; r += 8)
+            cp_async16(sm.a[buf] + r * kKP + c, A + (int64_t)r * K + c, 16);
+    cp_async_commit();
+}
+__global__ void __launch_bounds__(256, 1) frame_chain_kernel(const FrameParams p) {
     extern __shared__ __align__(16) unsigned char smraw[];
     ChainSmem &sm = *reinterpret_cast<ChainSmem *>(smraw);
     const int tid = threadIdx.x;
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int j0 = blockIdx.y * kCT;
     const int K = p.K, Vt = p.Vt, F = p.F;
-    // thread: key row r = tid / 2, columns (tid & 1) * 8 .. + 7
-    const int r = tid >> 1, cs = (tid & 1) * 8;
+    const int rb = tid >> 3, cq = tid & 7, r0 = 4 * rb, c0 = 4 * cq;
+    // columns K .. 127 of A_f are never copied: zero them once
+    if (K < kKP)
+        for (int e = tid; e < 2 * kKP * kKP; e += 256)
+            if (e % kKP >= K) (&sm.a[0][0])[e] = 0.f;
+    __syncthreads();
     auto run = [&](bool rev) {
-        for (int e = tid; e < kKP * kCT; e += 256) {
-            const int rr = e / kCT, j = j0 + e % kCT;
-            float v0 = 0.f;
-            if (!rev && p.h0 && rr < K && j < p.V) v0 = p.h0[(((int64_t)b * p.H + h) * K + rr) * p.V + j];
-            sm.s[e] = v0;
-        }
-        __syncthreads();
+        // step i absorbs frame af(i) (none for the reverse direction's first
+        // step) and gives the state frame of(i) reads
+        auto af = [&](int i) { return rev ? F - i : i; };
+        const int first = rev ? 1 : 0;  // first step that absorbs a frame
+        if (first < F) stage_a(p, sm, first & 1, (int64_t)bh * F + af(first));
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int r = r0 + i, j = j0 + c0 + c;
+                acc[i][c] = (!rev && p.h0 && r < K && j < p.V) ? p.h0[(((int64_t)b * p.H + h) * K + r) * p.V + j] : 0.f;
+            }
         for (int i = 0; i < F; ++i) {
-            // forward: absorb frame i, outputs of frame i read it; reverse:
-            // step i outputs frame F-1-i after absorbing frame F-i (none at i = 0)
-            const int af = rev ? F - i : i, of = rev ? F - 1 - i : i;
-            if (!rev || i > 0) {
-                const int64_t fi = (int64_t)bh * F + af;
-                const float *amat = p.amat + fi * K * K;
-                for (int e = tid; e < K * K; e += 256) sm.a[(e / K) * kAS + e % K] = amat[e];
-                const float dec = __expf(fmaxf(p.g_frame[((int64_t)b * F + af) * p.H + h], kLogGateMin));
-                __syncthreads();
-                float accv[8];
+            const int of = rev ? F - 1 - i : i;
+            if (i >= first) {
+                const int64_t fi = (int64_t)bh * F + af(i);
 #pragma unroll
-                for (int x = 0; x < 8; ++x) accv[x] = 0.f;
-                if (r < K) {
-                    const float *arow = sm.a + r * kAS;
-#pragma unroll 4
-                    for (int a = 0; a < K; ++a) {
-                        const float av = arow[a];
-                        const float4 s0 = *reinterpret_cast<const float4 *>(sm.s + a * kCT + cs);
-                        const float4 s1 = *reinterpret_cast<const float4 *>(sm.s + a * kCT + cs + 4);
-                        accv[0] = fmaf(av, s0.x, accv[0]);
-                        accv[1] = fmaf(av, s0.y, accv[1]);
-                        accv[2] = fmaf(av, s0.z, accv[2]);
-                        accv[3] = fmaf(av, s0.w, accv[3]);
-                        accv[4] = fmaf(av, s1.x, accv[4]);
-                        accv[5] = fmaf(av, s1.y, accv[5]);
-                        accv[6] = fmaf(av, s1.z, accv[6]);
-                        accv[7] = fmaf(av, s1.w, accv[7]);
+                for (int x = 0; x < 4; ++x)
+                    *reinterpret_cast<float4 *>(sm.s + (r0 + x) * kCT + c0) =
+                        make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+                const bool next = i + 1 < F;
+                if (next) stage_a(p, sm, (i + 1) & 1, (int64_t)bh * F + af(i + 1));
+                float bv[4][4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int r = r0 + x, j = j0 + c0 + c;
+                        bv[x][c] = (r < K && j < Vt) ? p.bmat[(fi * K + r) * Vt + j] : 0.f;
                     }
+                const float dec = __expf(fmaxf(p.g_frame[((int64_t)b * F + af(i)) * p.H + h], kLogGateMin));
+                if (next) cp_async_wait<1>();
+                else cp_async_wait<0>();
+                __syncthreads();  // A_f and the tile are complete
+                const float *A = sm.a[i & 1];
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[x][c] = 0.f;
+#pragma unroll 8
+                for (int a = 0; a < K; ++a) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(A + a * kKP + r0);
+                    const float4 s4 = *reinterpret_cast<const float4 *>(sm.s + a * kCT + c0);
+                    const float mv[4] = {m4.x, m4.y, m4.z, m4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) acc[x][c] = fmaf(mv[x], sv[c], acc[x][c]);
                 }
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const int j = j0 + cs + x;
-                    const bool in = r < K && j < Vt;
-                    const float bv = in ? p.bmat[(fi * K + r) * Vt + j] : 0.f;
-                    sm.n[r * kCT + cs + x] = in ? fmaf(dec, accv[x], bv) : 0.f;
-                }
-                __syncthreads();
+                for (int x = 0; x < 4; ++x)
 #pragma unroll
-                for (int x = 0; x < 8; ++x) sm.s[r * kCT + cs + x] = sm.n[r * kCT + cs + x];
-                __syncthreads();
+                    for (int c = 0; c < 4; ++c) acc[x][c] = fmaf(dec, acc[x][c], bv[x][c]);
+                __syncthreads();  // the tile and this buffer are rewritten next
             }
             // the state frame `of` reads, summed over the directions
-            if (r < K) {
-                float *dst = p.sout + (((int64_t)bh * F + of) * K + r) * Vt;
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const int j = j0 + cs + x;
-                    if (j < Vt) dst[j] = (rev && p.direction == 2) ? dst[j] + sm.s[r * kCT + cs + x] : sm.s[r * kCT + cs + x];
+            for (int x = 0; x < 4; ++x) {
+                const int r = r0 + x;
+                if (r >= K) continue;
+                float *dst = p.sout + (((int64_t)bh * F + of) * K + r) * p.Vs;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = j0 + c0 + c;
+                    if (j < Vt) dst[j] = (rev && p.direction == 2) ? dst[j] + acc[x][c] : acc[x][c];
                 }
             }
         }
-        if (!rev && p.h_final && r < K) {
+        if (!rev && p.h_final) {
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const int j = j0 + cs + x;
-                if (j < p.V) p.h_final[(((int64_t)b * p.H + h) * K + r) * p.V + j] = sm.s[r * kCT + cs + x];
-            }
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int r = r0 + x, j = j0 + c0 + c;
+                    if (r < K && j < p.V) p.h_final[(((int64_t)b * p.H + h) * K + r) * p.V + j] = acc[x][c];
+                }
         }
-        __syncthreads();
     };
     if (p.direction != 1) run(false);
     if (p.direction != 0) run(true);
 }
 
 // ----------------------------------------------------------------- out ---
-__global__ void __launch_bounds__(128) frame_out_kernel(const FrameParams p) {
-    __shared__ __align__(16) bf16 sQ[kChunk * kKS];   // [token][key]
-    __shared__ __align__(16) bf16 sSt[kKP * kXS];     // state block, [key][column]
+// One CTA (8 warps) per (sequence x head, 64-token chunk, 128 value columns):
+// the chunk's q rows (cp.async) and its frame's state, converted to bf16
+// from 16-byte fp32 loads; warp w computes tokens 16 (w & 3) .. + 15 of
+// column half w >> 2.
+struct OutSmem {
+    bf16 q[kChunk * kKS];   // [token][key]
+    bf16 st[kKP * kXB];     // state block, [key][column]
+};
+__global__ void __launch_bounds__(256) frame_out_kernel(const FrameParams p) {
+    extern __shared__ __align__(16) unsigned char smraw[];
+    OutSmem &sm = *reinterpret_cast<OutSmem *>(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.x / p.H, h = blockIdx.x % p.H, c = blockIdx.y, cb = blockIdx.z;
     const int K = p.K, V = p.V, Vt = p.Vt;
     const int64_t t0 = (int64_t)c * kChunk;
     const int f = (int)(t0 / p.frame);
-    const int col0 = cb * 64;
-    for (int e = tid; e < kChunk * (kKP / 8); e += 128) {
-        const int i = e / (kKP / 8), d = (e % (kKP / 8)) * 8;
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (d < K) o = *reinterpret_cast<const uint4 *>(row_ptr(p.q, p.qk_sb, p.qk_st, p.qk_sh, b, t0 + i, h) + d);
-        *reinterpret_cast<uint4 *>(sQ + i * kKS + d) = o;
+    const int col0 = cb * 128;
+    const bf16 *qp = (const bf16 *)p.q;
+    for (int e = tid; e < kChunk * (kKP / 8); e += 256) {
+        const int i = e >> 4, d = (e & 15) * 8;
+        const bool in = d < K;
+        cp_async16(sm.q + i * kKS + d, in ? qp + b * p.qk_sb + (t0 + i) * p.qk_st + h * p.qk_sh + d : qp,
+                   in ? 16 : 0);
     }
-    const float *S = p.sout + ((int64_t)blockIdx.x * p.F + f) * K * Vt;
-    for (int e = tid; e < kKP * 32; e += 128) {
-        const int rr = e / 32, cc = (e % 32) * 2, j = col0 + cc;
-        const float s0 = (rr < K && j < Vt) ? S[(int64_t)rr * Vt + j] : 0.f;
-        const float s1 = (rr < K && j + 1 < Vt) ? S[(int64_t)rr * Vt + j + 1] : 0.f;
-        *reinterpret_cast<uint32_t *>(sSt + rr * kXS + cc) = pack_bf16(s0, s1);
+    cp_async_commit();
+    const float *S = p.sout + ((int64_t)blockIdx.x * p.F + f) * K * p.Vs;
+#pragma unroll 4
+    for (int e = tid; e < kKP * 32; e += 256) {  // 4 columns per step
+        const int rr = e >> 5, cc = (e & 31) * 4, j = col0 + cc;
+        float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rr < K && j < Vt) v4 = *reinterpret_cast<const float4 *>(S + (int64_t)rr * p.Vs + j);
+        if (j + 1 >= Vt) v4.y = 0.f;  // padding columns of the state rows
+        if (j + 2 >= Vt) v4.z = 0.f;
+        if (j + 3 >= Vt) v4.w = 0.f;
+        *reinterpret_cast<uint2 *>(sm.st + rr * kXB + cc) = make_uint2(pack_bf16(v4.x, v4.y), pack_bf16(v4.z, v4.w));
     }
+    cp_async_wait<0>();
     __syncthreads();
+    const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
     float acc[8][4];
 #pragma unroll
     for (int n = 0; n < 8; ++n)
@@ -257,11 +329,11 @@ __global__ void __launch_bounds__(128) frame_out_kernel(const FrameParams p) {
 #pragma unroll
     for (int ks = 0; ks < kKP / 16; ++ks) {
         uint32_t a[4];
-        ldsm_x4(a, sQ + (16 * warp + (lane & 15)) * kKS + ks * 16 + (lane >> 4) * 8);
+        ldsm_x4(a, sm.q + (m0 + (lane & 15)) * kKS + ks * 16 + (lane >> 4) * 8);
 #pragma unroll
         for (int np = 0; np < 4; ++np) {
             uint32_t bb[4];
-            ldsm_x4_t(bb, sSt + (ks * 16 + (lane & 15)) * kXS + 16 * np + (lane >> 4) * 8);
+            ldsm_x4_t(bb, sm.st + (ks * 16 + (lane & 15)) * kXB + n0 + 16 * np + (lane >> 4) * 8);
             mma_bf16(acc[2 * np], a, bb[0], bb[1]);
             mma_bf16(acc[2 * np + 1], a, bb[2], bb[3]);
         }
@@ -271,8 +343,8 @@ __global__ void __launch_bounds__(128) frame_out_kernel(const FrameParams p) {
     for (int n = 0; n < 8; ++n)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-            const int64_t t = t0 + 16 * warp + g8 + 8 * hf;
-            const int j = col0 + 8 * n + 2 * t4;
+            const int64_t t = t0 + m0 + g8 + 8 * hf;
+            const int j = col0 + n0 + 8 * n + 2 * t4;
             const float o0 = acc[n][2 * hf], o1 = acc[n][2 * hf + 1];
             if (j + 1 < V) {  // both columns are values (V is a multiple of 8)
                 const int64_t off = b * p.o_sb + t * p.o_st + h * p.o_sh + j;
@@ -299,8 +371,11 @@ __global__ void __launch_bounds__(128) frame_out_kernel(const FrameParams p) {
 }  // namespace
 
 cudaError_t launch_frame_gram(const FrameParams &p, cudaStream_t st) {
-    const int ncb = (kKP + p.Vt + 63) / 64;
-    frame_gram_kernel<<<dim3(p.B * p.H, p.F, ncb), 128, 0, st>>>(p);
+    const int bytes = (int)sizeof(GramSmem);
+    cudaError_t e = cudaFuncSetAttribute(frame_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    const int ncb = (kKP + p.Vt + 127) / 128;
+    frame_gram_kernel<<<dim3(p.B * p.H, p.F, ncb), 256, bytes, st>>>(p);
     return cudaGetLastError();
 }
 cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st) {
@@ -311,7 +386,10 @@ cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st) {
     return cudaGetLastError();
 }
 cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st) {
-    frame_out_kernel<<<dim3(p.B * p.H, p.T / kChunk, (p.Vt + 63) / 64), 128, 0, st>>>(p);
+    const int bytes = (int)sizeof(OutSmem);
+    cudaError_t e = cudaFuncSetAttribute(frame_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    frame_out_kernel<<<dim3(p.B * p.H, p.T / kChunk, (p.Vt + 127) / 128), 256, bytes, st>>>(p);
     return cudaGetLastError();
 }
 

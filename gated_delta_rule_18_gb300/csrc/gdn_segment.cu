@@ -15,8 +15,8 @@
 // and the state kernel then re-runs every segment from its h_in, again in
 // parallel, producing the outputs.
 //
-// One CTA per (sequence x head, 16-column tile); each thread keeps a 4 x 2
-// block of the tile, the tile and M_s^T (stored transposed by the summary
+// One CTA per (sequence x head, 8-column tile: many CTAs for the few
+// sequence-heads this path serves); each thread keeps 4 rows of one column, the tile and M_s^T (stored transposed by the summary
 // pass, so a thread's four rows are one 16-byte load) sit in shared memory,
 // and M_{s+1}^T is copied in (cp.async) while step s computes.
 #include "gdn_common.cuh"
@@ -24,8 +24,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kCT = 16;          // state columns per CTA
-constexpr int kThreads = 256;    // thread: rows 4 rb .. 4 rb + 3, columns 2 cp, 2 cp + 1
+constexpr int kCT = 8;           // state columns per CTA
+constexpr int kThreads = 256;    // thread: rows 4 rb .. 4 rb + 3, column cp
 
 struct CombineSmem {
     float mt[2][kKP * kKP];      // M_s^T and M_{s+1}^T, [a][r] (double buffer)
@@ -34,12 +34,12 @@ struct CombineSmem {
 
 // M_s^T (K x K, rows contiguous) into buffer `buf` by 16-byte async copies
 __device__ __forceinline__ void stage_mt(const SegParams &p, CombineSmem &sm, int buf, int s, int64_t bh) {
-    const int K = p.K, q4 = K / 4;
+    // thread t copies 16-byte piece t % 32 of rows t / 32, t / 32 + 8, ...
+    const int K = p.K, c = (threadIdx.x & 31) * 4;
     const float *Mt = p.sum_tr + ((int64_t)s * p.n_bh + bh) * K * K;
-    for (int e = threadIdx.x; e < K * q4; e += kThreads) {
-        const int a = e / q4, c = (e % q4) * 4;
-        cp_async16(sm.mt[buf] + a * kKP + c, Mt + (int64_t)a * K + c, 16);
-    }
+    if (c < K)
+        for (int a = threadIdx.x >> 5; a < K; a += kThreads / 32)
+            cp_async16(sm.mt[buf] + a * kKP + c, Mt + (int64_t)a * K + c, 16);
     cp_async_commit();
 }
 
@@ -51,71 +51,55 @@ __global__ void __launch_bounds__(kThreads) seg_combine_kernel(const SegParams p
     const int j0 = blockIdx.y * kCT;
     const int K = p.K, Vt = p.Vt;
     const int rb = tid >> 3, cp = tid & 7;
-    const int r0 = 4 * rb, c0 = 2 * cp;  // this thread's rows r0 .. r0+3, tile columns c0, c0+1
+    const int r0 = 4 * rb, jc = j0 + cp;  // this thread's rows r0 .. r0+3 and column jc
     // rows K .. 127 of M^T's columns are never copied: zero them once
     if (K < kKP)
         for (int e = tid; e < 2 * kKP * kKP; e += kThreads)
             if (e % kKP >= K) (&sm.mt[0][0])[e] = 0.f;
     __syncthreads();
     if (p.n_seg > 1) stage_mt(p, sm, 0, 0, bh);
-    float acc[4][2];
+    float acc[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            const int r = r0 + i, j = j0 + c0 + c;
-            acc[i][c] = (p.h0 && r < K && j < p.V) ? p.h0[(bh * K + r) * p.V + j] : 0.f;
-        }
+    for (int i = 0; i < 4; ++i) {
+        const int r = r0 + i;
+        acc[i] = (p.h0 && r < K && jc < p.V) ? p.h0[(bh * K + r) * p.V + jc] : 0.f;
+    }
     for (int s = 0;; ++s) {
         // h_in[s]: to global and to the shared tile
+        if (jc < Vt) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = r0 + i;
-            if (r >= K) continue;
-            float *dst = p.h_in + (((int64_t)s * p.n_bh + bh) * K + r) * Vt + j0 + c0;
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-                if (j0 + c0 + c < Vt) dst[c] = acc[i][c];
+            for (int i = 0; i < 4; ++i)
+                if (r0 + i < K) p.h_in[(((int64_t)s * p.n_bh + bh) * K + r0 + i) * Vt + jc] = acc[i];
         }
         if (s + 1 >= p.n_seg) break;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<float2 *>(sm.s + (r0 + i) * kCT + c0) = make_float2(acc[i][0], acc[i][1]);
+        for (int i = 0; i < 4; ++i) sm.s[(r0 + i) * kCT + cp] = acc[i];
         // M_{s+1}^T streams in while step s computes
         const bool next = s + 2 < p.n_seg;
         if (next) stage_mt(p, sm, (s + 1) & 1, s + 1, bh);
-        float e[4][2];
+        float e[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int r = r0 + i, j = j0 + c0 + c;
-                e[i][c] = (r < K && j < Vt) ? p.sum_ext[(((int64_t)s * p.n_bh + bh) * K + r) * Vt + j] : 0.f;
-            }
+        for (int i = 0; i < 4; ++i) {
+            const int r = r0 + i;
+            e[i] = (r < K && jc < Vt) ? p.sum_ext[(((int64_t)s * p.n_bh + bh) * K + r) * Vt + jc] : 0.f;
+        }
         if (next) cp_async_wait<1>();
         else cp_async_wait<0>();
         __syncthreads();  // M_s^T and the tile are complete
         const float *mt = sm.mt[s & 1];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[i] = 0.f;
 #pragma unroll 8
         for (int a = 0; a < K; ++a) {
             const float4 m4 = *reinterpret_cast<const float4 *>(mt + a * kKP + r0);
-            const float2 s2 = *reinterpret_cast<const float2 *>(sm.s + a * kCT + c0);
-            acc[0][0] = fmaf(m4.x, s2.x, acc[0][0]);
-            acc[0][1] = fmaf(m4.x, s2.y, acc[0][1]);
-            acc[1][0] = fmaf(m4.y, s2.x, acc[1][0]);
-            acc[1][1] = fmaf(m4.y, s2.y, acc[1][1]);
-            acc[2][0] = fmaf(m4.z, s2.x, acc[2][0]);
-            acc[2][1] = fmaf(m4.z, s2.y, acc[2][1]);
-            acc[3][0] = fmaf(m4.w, s2.x, acc[3][0]);
-            acc[3][1] = fmaf(m4.w, s2.y, acc[3][1]);
+            const float sv = sm.s[a * kCT + cp];
+            acc[0] = fmaf(m4.x, sv, acc[0]);
+            acc[1] = fmaf(m4.y, sv, acc[1]);
+            acc[2] = fmaf(m4.z, sv, acc[2]);
+            acc[3] = fmaf(m4.w, sv, acc[3]);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            acc[i][0] += e[i][0];
-            acc[i][1] += e[i][1];
-        }
+        for (int i = 0; i < 4; ++i) acc[i] += e[i];
         __syncthreads();  // the tile and buffer s & 1 are rewritten next
     }
 }
