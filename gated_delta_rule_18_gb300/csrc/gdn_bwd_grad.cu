@@ -63,17 +63,44 @@ __device__ __forceinline__ ChunkCtx chunk_ctx(const BwdParams &p) {
     return x;
 }
 
-// 16-byte pieces of a (rows x ncol) bf16 block into a row-major tile; rows
-// or columns outside (nrow_ok, ncol) are zero-filled
+// 16-byte pieces of a (rows x ncol) bf16 block into a row-major 128-column
+// tile: thread t copies piece t % 16 of rows t / 16, t / 16 + 16, ...; rows
+// with no source (row_ptr NULL) and columns >= ncol are zero-filled
 template <class RowPtr>
-__device__ __forceinline__ void load_rows(bf16 *dst, int ld, int rows, int ncol, int ncol_tile, RowPtr row_ptr) {
-    const int pieces = ncol_tile / 8;
-    for (int e = threadIdx.x; e < rows * pieces; e += kThreads) {
-        const int i = e / pieces, c8 = (e % pieces) * 8;
+__device__ __forceinline__ void load_rows(bf16 *dst, int ld, int rows, int ncol, RowPtr row_ptr) {
+    const int c8 = (threadIdx.x & 15) * 8;
+    for (int i = threadIdx.x >> 4; i < rows; i += kThreads / 16) {
         const bf16 *src = row_ptr(i);
         const bool in = src != nullptr && c8 < ncol;
         cp_async16(dst + i * ld + c8, in ? src + c8 : dst, in ? 16 : 0);
     }
+}
+
+// row sums of a warp's 16 x 32 fragment set c (see gdn_mma.cuh) added into
+// row_dst[m0 ..], and column sums times col_sign into col_dst[n0 ..]: the
+// gate-gradient terms of entries that depend on G_i - G_j
+__device__ __forceinline__ void rowcol_add(const float (&c)[4][4], int m0, int n0, float *row_dst,
+                                           float *col_dst, float col_sign) {
+    const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        float r = 0.f;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) r += c[n][2 * hf] + c[n][2 * hf + 1];
+        r += __shfl_xor_sync(0xffffffffu, r, 1);
+        r += __shfl_xor_sync(0xffffffffu, r, 2);
+        if (t4 == 0 && r != 0.f) atomicAdd(row_dst + m0 + g8 + 8 * hf, r);
+    }
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            float v = c[n][b] + c[n][2 + b];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            if (g8 == 0 && v != 0.f) atomicAdd(col_dst + n0 + 8 * n + 2 * t4 + b, col_sign * v);
+        }
 }
 
 // L2 norms of 64 rows of a tile (1 when not normalising), then the rows
@@ -153,23 +180,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
     const int K = p.K, V = p.V, kq = round16(K), kv = round16(V);
     const bf16 *q = (const bf16 *)p.q, *k = (const bf16 *)p.k, *dout = (const bf16 *)p.dout;
 
-    load_rows(sm.q, kLK, kChunk, K, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.q, kLK, kChunk, K, [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
         return q + x.s * p.qk_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.qk_st + x.hh * p.qk_sh;
     });
-    load_rows(sm.k, kLK, kChunk, K, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.k, kLK, kChunk, K, [&](int i) -> const bf16 * {
         const int tk = i < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + i) : -1;
         if (tk < 0) return nullptr;
         return k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
     });
-    load_rows(sm.dout, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.dout, kLK, kChunk, V, [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
         return dout + x.s * p.do_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.do_st + x.hh * p.do_sh;
     });
-    load_rows(sm.vn, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.vn_snap + (x.gch * kChunk + i) * V;
     });
-    load_rows(sm.h, kLK, kKP, V, kKP, [&](int r) -> const bf16 * {
+    load_rows(sm.h, kLK, kKP, V, [&](int r) -> const bf16 * {
         return r < K ? p.h_snap + (x.gch * K + r) * V : nullptr;
     });
     cp_async_commit();
@@ -189,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
         acc_zero(dp);
         warp_gemm(sp, Tile{sm.q, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
         warp_gemm(dp, Tile{sm.dout, kLK}, false, Tile{sm.vn, kLK}, false, m0, n0, kv, lane);
+        float ct[4][4];  // dP_ij P_ij: d/dG_i of P_ij is P_ij, d/dG_j is -P_ij
 #pragma unroll
         for (int n = 0; n < 4; ++n)
 #pragma unroll
@@ -202,19 +230,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
                     const float gam = on ? __expf(sm.G[i] - sm.G[j]) : 0.f;
                     const float P = gam * sp[n][2 * hf + e], dP = on ? dp[n][2 * hf + e] : 0.f;
                     mpv[e] = dP * gam;
-                    const float cterm = dP * P;  // d/dG_i of P_ij is P_ij, d/dG_j is -P_ij
-                    if (on && cterm != 0.f) {
-                        atomicAdd(&sm.dG[i], cterm);
-                        atomicAdd(&sm.dG[j], -cterm);
-                    }
+                    ct[n][2 * hf + e] = dP * P;
                 }
                 *reinterpret_cast<uint32_t *>(sm.mp + i * kL6 + n0 + 8 * n + 2 * t4) = pack_bf16(mpv[0], mpv[1]);
             }
+        rowcol_add(ct, m0, n0, sm.dG, sm.dG, -1.f);
     }
     __syncthreads();
 
     // dq^ = e^{G} . (do h^T) + M_P K^   (64 x 128; warp: 16 rows x 64 keys)
     const int nk0 = 64 * (warp >> 2);
+    // e^{G_i} of this thread's two fragment rows
+    const float egr[2] = {__expf(sm.G[m0 + g8]), __expf(sm.G[m0 + g8 + 8])};
     float dq[8][4];
     {
         acc_zero(dq);
@@ -225,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                const float eg = __expf(sm.G[i]);
+                const float eg = egr[hf];
                 // dG_i of qg = e^{G_i} q^_i: sum_d dqg_id qg_id
                 part[hf] += dq[n][e] * eg * __bfloat162float(sm.q[i * kLK + d]);
                 dq[n][e] *= eg;
@@ -337,24 +364,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     const bf16 *k = (const bf16 *)p.k, *v = (const bf16 *)p.v;
     auto kv_row = [&](int i) { return i < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + i) : -1; };
 
-    load_rows(sm.k, kLK, kChunk, K, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.k, kLK, kChunk, K, [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
     });
-    load_rows(sm.v, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.v, kLK, kChunk, V, [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : v + x.s * p.v_sb + (int64_t)tk * p.v_st + x.hh * p.v_sh;
     });
-    load_rows(sm.dvn, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.dvn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.dvn_snap + (x.gch * kChunk + i) * V;
     });
-    load_rows(sm.u.a.vn, kLK, kChunk, V, kKP, [&](int i) -> const bf16 * {
+    load_rows(sm.u.a.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.vn_snap + (x.gch * kChunk + i) * V;
     });
-    load_rows(sm.u.a.h, kLK, kKP, V, kKP, [&](int r) -> const bf16 * {
+    load_rows(sm.u.a.h, kLK, kKP, V, [&](int r) -> const bf16 * {
         return r < K ? p.h_snap + (x.gch * K + r) * V : nullptr;
     });
-    load_rows(sm.u.a.dh, kLK, kKP, V, kKP, [&](int r) -> const bf16 * {
+    load_rows(sm.u.a.dh, kLK, kKP, V, [&](int r) -> const bf16 * {
         return r < K ? p.dh_snap + (x.gch * K + r) * V : nullptr;
     });
     cp_async_commit();
@@ -381,6 +408,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     __syncthreads();
 
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
+    // factors of this thread's two fragment rows: e^{G_i}, e^{G_C - G_i} (0
+    // past the chunk's end)
+    float egr[2], ecr[2];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int i = m0 + g8 + 8 * hf;
+        egr[hf] = __expf(sm.G[i]);
+        ecr[hf] = i < x.Lc ? __expf(GC - sm.G[i]) : 0.f;
+    }
     // S . Gamma, strictly lower
     {
         float sk[4][4];
@@ -405,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                const float f = i < x.Lc ? __expf(GC - sm.G[i]) : 0.f;
+                const float f = ecr[hf];
                 dk[n][e] *= f;
                 part[hf] += dk[n][e] * __bfloat162float(sm.k[i * kLK + d]);
             }
@@ -462,9 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             if (e < n_el) {
                 const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
                 float acc = 0.f;
-                for (int m = cidx & ~15; m < 16 * I; ++m)
-                    acc = fmaf(sm.beta[r] * sm.kkg[r * kPS + m], sT[m * kPS + cidx], acc);
-                rr[u] = acc;
+                for (int m = cidx & ~15; m < 16 * I; ++m) acc = fmaf(sm.kkg[r * kPS + m], sT[m * kPS + cidx], acc);
+                rr[u] = sm.beta[r] * acc;
             }
         }
         __syncthreads();
@@ -499,11 +534,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         const int i = e >> 5, j = (e & 31) * 2;
         *reinterpret_cast<uint32_t *>(sm.u.b.tb + i * kL6 + j) = pack_bf16(sT[i * kPS + j], sT[i * kPS + j + 1]);
     }
-    for (int e = tid; e < kChunk * (kKP / 2); e += kThreads) {
-        const int i = e / (kKP / 2), d = (e % (kKP / 2)) * 2;
+    for (int e = tid; e < kChunk * (kKP / 8); e += kThreads) {
+        const int i = e >> 4, d = (e & 15) * 8;
         const float f = sm.beta[i] * __expf(sm.G[i]);
-        const float2 kk = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.k + i * kLK + d));
-        *reinterpret_cast<uint32_t *>(sm.u.b.xw + i * kLK + d) = pack_bf16(f * kk.x, f * kk.y);
+        uint4 u = *reinterpret_cast<const uint4 *>(sm.k + i * kLK + d);
+        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+        for (int x2 = 0; x2 < 4; ++x2) {
+            const float2 kk = __bfloat1622float2(h2[x2]);
+            h2[x2] = __floats2bfloat162_rn(f * kk.x, f * kk.y);
+        }
+        *reinterpret_cast<uint4 *>(sm.u.b.xw + i * kLK + d) = u;
     }
     __syncthreads();
     const Tile tT{sm.u.b.tb, kL6};
@@ -544,20 +585,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         acc_zero(a);
         warp_gemm(a, tT, true, Tile{sm.u.b.z, kL6}, true, m0, n0, kChunk, lane);
         float pb[2] = {0.f, 0.f};
+        float ct[4][4];  // dA_ij A_ij: d/dG_i of A_ij is A_ij, d/dG_j is -A_ij
 #pragma unroll
         for (int n = 0; n < 4; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, j = n0 + 8 * n + 2 * t4 + (e & 1);
                 float ms = 0.f;
+                ct[n][e] = 0.f;
                 if (j < i && i < x.Lc) {
                     const float da = -a[n][e], kk = sm.kkg[i * kPS + j];
                     pb[hf] += da * kk;
-                    const float Aij = sm.beta[i] * kk, c = da * Aij;
-                    if (c != 0.f) {
-                        atomicAdd(&sm.dG[i], c);
-                        atomicAdd(&sm.dG[j], -c);
-                    }
+                    ct[n][e] = da * sm.beta[i] * kk;
                     ms = da * sm.beta[i] * __expf(sm.G[i] - sm.G[j]);
                 }
                 if (j <= i) {  // (i, j) and its mirror; the diagonal stays 0
@@ -572,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             if (t4 == 0 && s != 0.f) atomicAdd(&sm.dB[m0 + g8 + 8 * hf], s);
         }
+        rowcol_add(ct, m0, n0, sm.dG, sm.dG, -1.f);
     }
     __syncthreads();
     // dk^ += dS K^ + beta e^{G} . (T^T dw)
@@ -586,9 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                const float eg = __expf(sm.G[i]);
                 part[hf] += bw[n][e] * __bfloat162float(sm.k[i * kLK + d]);
-                dk[n][e] = fmaf(sm.beta[i] * eg, bw[n][e], dk[n][e]);
+                dk[n][e] = fmaf(sm.beta[i] * egr[hf], bw[n][e], dk[n][e]);
             }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -597,9 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             const int i = m0 + g8 + 8 * hf;
             if (t4 == 0 && i < x.Lc && s != 0.f) {
-                const float eg = __expf(sm.G[i]);
-                atomicAdd(&sm.dB[i], eg * s);
-                atomicAdd(&sm.dG[i], sm.beta[i] * eg * s);
+                atomicAdd(&sm.dB[i], egr[hf] * s);
+                atomicAdd(&sm.dG[i], sm.beta[i] * egr[hf] * s);
             }
         }
     }
