@@ -324,6 +324,10 @@ def workspace_for(gdn, w, dev):
     if w.segment_len is not None:
         n = gdn.gdn_seg_workspace_size(w.B, w.T, w.H, w.K, w.V, w.bidirectional, w.segment_len)
         return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    if w.bidirectional and w.frame == 1:  # both directions at once (two workspaces + staging)
+        n = gdn.gdn_bidir_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq, w.cu_seqlens is not None,
+                                         dt, True)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
     n = gdn.gdn_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq, w.cu_seqlens is not None, dt,
                                w.bidirectional)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=dev)

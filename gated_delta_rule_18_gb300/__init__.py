@@ -90,6 +90,11 @@ def lib():
     L.gdn_chunk_bwd.restype = I
     L.gdn_chunk_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, TensorDesc, P, P, P,
                                 P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+    L.gdn_bidir_workspace_size.restype = ctypes.c_size_t
+    L.gdn_bidir_workspace_size.argtypes = [I] * 9
+    L.gdn_chunk_fwd_bidir.restype = I
+    L.gdn_chunk_fwd_bidir.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, P, I, P,
+                                      TensorDesc, P, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
     L.gdn_merge.restype = I
     L.gdn_merge.argtypes = [P, TensorDesc, P, P, TensorDesc, P, TensorDesc, I, I, I, I, F, P]
     L.gdn_last_device_error.restype = I
@@ -314,6 +319,39 @@ def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
     return res
 
 
+def gdn_bidir_workspace_size(B, T, H, K, V, n_seq, varlen, dtype, with_den) -> int:
+    return int(lib().gdn_bidir_workspace_size(B, T, H, K, V, n_seq, int(bool(varlen)), dtype,
+                                              int(bool(with_den))))
+
+
+def gdn_chunk_fwd_bidir(q, k, v, beta, g=None, gk=None, g_bwd=None, beta_bwd=None,
+                        cu_seqlens=None, out=None, den=None, qk_l2norm=False, workspace=None,
+                        stream=None):
+    """Both directions of the bidirectional scan, run concurrently (see
+    include/gdn.h): out = num_fwd + num_bwd, den = den_fwd + den_bwd.
+    Returns out (allocated in q's dtype when not given)."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    for name, t in (("beta", beta), ("g", g), ("gk", gk), ("g_bwd", g_bwd),
+                    ("beta_bwd", beta_bwd), ("den", den)):
+        _f32(t, name)
+    if out is None:
+        out = torch.empty((B, T, H, V), dtype=q.dtype, device=q.device)
+    need = gdn_bidir_workspace_size(B, T, H, K, V, n_seq, cu_seqlens is not None, _dtype_code(q),
+                                    den is not None)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().gdn_chunk_fwd_bidir(
+        _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta), _ptr(g_bwd),
+        _ptr(beta_bwd), _ptr(cu_seqlens), n_seq, _ptr(out), _desc(out), _ptr(den), B, T, H, K, V,
+        64, QK_L2NORM if qk_l2norm else 0, _ptr(workspace), workspace.numel(), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_chunk_fwd_bidir")
+    return out
+
+
 def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqlens=None,
                           h_final=None, den=None, reverse=False, accumulate=False,
                           qk_l2norm=False, stream=None):
@@ -478,9 +516,19 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
             res["h_final"] = hf
         return res
     den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
-    out = scan(q, k, v, beta, g, gk, den=den)
-    scan(bw.get("q", q), bw.get("k", k), bw.get("v", v), bw.get("beta", beta), bw.get("g", g),
-         bw.get("gk", gk), den=den, out=out, reverse=True, accumulate=True)
+    if not segment_len and not ({"q", "k", "v", "gk"} & set(bw)) and not (gk is not None and "g" in bw):
+        # both directions at once, the reverse on the library's second stream
+        out = gdn_chunk_fwd_bidir(q, k, v, beta, g=g, gk=gk, g_bwd=bw.get("g"),
+                                  beta_bwd=bw.get("beta"), cu_seqlens=cu_seqlens, den=den,
+                                  qk_l2norm=fuse, stream=stream,
+                                  workspace=workspace if workspace is not None and workspace.numel()
+                                  >= gdn_bidir_workspace_size(B, T, H, K, v.shape[3], n_seq,
+                                                              cu_seqlens is not None,
+                                                              _dtype_code(q), True) else None)
+    else:
+        out = scan(q, k, v, beta, g, gk, den=den)
+        scan(bw.get("q", q), bw.get("k", k), bw.get("v", v), bw.get("beta", beta), bw.get("g", g),
+             bw.get("gk", gk), den=den, out=out, reverse=True, accumulate=True)
     res["out"], res["den"] = out, den
     if merge:
         res["merged"] = gdn_merge(out, den, gate=gate, eps=eps, stream=stream)

@@ -16,12 +16,12 @@ using gdn::FwdParams;
 
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
-    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KNumKinds
+    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
-                                     "bwd_dh", "bwd_dq", "bwd_dk"};
+                                     "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum"};
 
 struct Profiler {
     std::mutex mu;
@@ -548,6 +548,129 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     if (e == cudaSuccess) e = launch(KBwdDq, stream, [&] { return gdn::launch_bwd_dq(b, stream); });
     if (e == cudaSuccess) e = launch(KBwdDk, stream, [&] { return gdn::launch_bwd_dk(b, stream); });
     return cuda_status(e);
+}
+
+}  // extern "C"
+
+namespace {
+// A library-owned second stream per device (and the events that fork it
+// from, and join it back to, the caller's stream), for the reverse direction
+// of a concurrent bidirectional scan. Created on first use, never destroyed.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex &side_mutex() {
+    static std::mutex *m = new std::mutex();
+    return *m;
+}
+cudaError_t side_stream(SideStream *&out) {
+    static SideStream *per_dev = new SideStream[64];
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return e;
+    if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+    SideStream &x = per_dev[d];
+    if (!x.s) {
+        if ((e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    out = &x;
+    return cudaSuccess;
+}
+
+struct BidirWs {
+    size_t fwd, rev, out2, den2, total;
+};
+bool bidir_layout(const Ws &L, int B, int T, int H, int V, int dtype, int with_den, BidirWs &S) {
+    S.fwd = 0;
+    S.rev = align_up(L.total);
+    size_t off = S.rev + align_up(L.total);
+    S.out2 = off;
+    off = align_up(off + (size_t)B * T * H * V * (dtype == GDN_BF16 ? 2 : 4));
+    S.den2 = off;
+    off = align_up(off + (with_den ? (size_t)B * H * T * 4 : 0));
+    S.total = off;
+    return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t gdn_bidir_workspace_size(int B, int T, int H, int K, int V, int n_seq, int varlen, int dtype,
+                                int with_den) {
+    Ws L;
+    BidirWs S;
+    if (!ws_layout(B, T, H, K, V, n_seq, varlen, dtype, with_den, L)) return 0;
+    bidir_layout(L, B, T, H, V, dtype, with_den, S);
+    return S.total;
+}
+
+gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                               gdn_tensor_desc vd, const float *g, const float *gk,
+                               const float *beta, const float *g_bwd, const float *beta_bwd,
+                               const int32_t *cu_seqlens, int n_seq, void *out, gdn_tensor_desc od,
+                               float *den_out, int B, int T, int H, int K, int V, int chunk,
+                               int flags, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;
+    if (g_bwd && !g) return GDN_ERR_UNSUPPORTED;  // backward gates replace a scalar gate only
+    if (od.dtype != qkd.dtype) return GDN_ERR_DTYPE;  // the reverse half is staged in out's dtype
+    for (const void *f : {(const void *)g_bwd, (const void *)beta_bwd})
+        if (f && (reinterpret_cast<uintptr_t>(f) & 3)) return GDN_ERR_LAYOUT;
+    Ws L;
+    gdn::FwdParams pf, pr;
+    gdn_status st = fwd_setup(q, k, qkd, v, vd, g, gk, beta, nullptr, cu_seqlens, n_seq, out, od,
+                              nullptr, den_out, B, T, H, K, V, chunk, 0, flags, true, L, pf);
+    if (st != GDN_OK) return st;
+    BidirWs S;
+    bidir_layout(L, B, T, H, V, qkd.dtype, den_out != nullptr, S);
+    if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
+    if (T == 0) return GDN_OK;
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    // the reverse direction writes its own contiguous output, summed in after
+    gdn_tensor_desc od2{};
+    od2.dtype = od.dtype;
+    od2.stride_b = (int64_t)T * H * V;
+    od2.stride_t = (int64_t)H * V;
+    od2.stride_h = V;
+    float *den2 = den_out ? reinterpret_cast<float *>(ws + S.den2) : nullptr;
+    st = fwd_setup(q, k, qkd, v, vd, g_bwd ? g_bwd : g, gk, beta_bwd ? beta_bwd : beta, nullptr,
+                   cu_seqlens, n_seq, ws + S.out2, od2, nullptr, den2, B, T, H, K, V, chunk, 1, flags,
+                   true, L, pr);
+    if (st != GDN_OK) return st;
+    bind_ws(ws + S.fwd, L, pf);
+    bind_ws(ws + S.rev, L, pr);
+    const int perkey = gk != nullptr, varlen = cu_seqlens != nullptr;
+
+    std::lock_guard<std::mutex> lock(side_mutex());
+    SideStream *side = nullptr;
+    if (side_stream(side) != cudaSuccess) return GDN_ERR_CUDA;
+    auto run = [&](gdn::FwdParams &p, cudaStream_t s) -> cudaError_t {
+        cudaError_t e = cudaSuccess;
+        if (varlen) e = launch(KTable, s, [&] { return gdn::launch_chunk_table(p, s); });
+        if (e != cudaSuccess) return e;
+        if (qkd.dtype == GDN_F32)
+            return launch(KFusedF32, s, [&] { return gdn::launch_fused_f32(p, L.KP, perkey, s); });
+        if (L.max_chunks > 0) e = launch(KIntra, s, [&] { return gdn::launch_intra_bf16(p, perkey, s); });
+        if (e != cudaSuccess) return e;
+        return launch(KState, s, [&] { return gdn::launch_state_tc(p, s); });
+    };
+    // fork: the reverse direction on the side stream, the forward on the caller's
+    cudaError_t e = cudaEventRecord(side->fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e == cudaSuccess) e = run(pr, side->s);
+    if (e == cudaSuccess) e = run(pf, stream);
+    // join, then out += the reverse half, den += its denominator
+    if (e == cudaSuccess) e = cudaEventRecord(side->join, side->s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
+    gdn::SumParams a{};
+    a.out = out, a.o_sb = od.stride_b, a.o_st = od.stride_t, a.o_sh = od.stride_h;
+    a.add = ws + S.out2;
+    a.den = den_out, a.den_add = den2;
+    a.B = B, a.T = T, a.H = H, a.V = V, a.bf16 = od.dtype == GDN_BF16;
+    return cuda_status(launch(KSum, stream, [&] { return gdn::launch_sum(a, stream); }));
 }
 
 gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den, const void *gate,

@@ -296,6 +296,18 @@ struct MergeParams {
     int num_bf16, out_bf16;
 };
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t st);
+
+// out += add, den += den_add (the two directions of a concurrent
+// bidirectional scan)
+struct SumParams {
+    void *out;  // (B, T, H, V), fp32 or bf16
+    int64_t o_sb, o_st, o_sh;
+    const void *add;  // contiguous (B, T, H, V), out's dtype
+    float *den;       // (B, H, T) or null
+    const float *den_add;
+    int B, T, H, V, bf16;
+};
+cudaError_t launch_sum(const SumParams &a, cudaStream_t st);
 // The frame-causal form (gdn_frame.cu).
 struct FrameParams {
     const void *q, *k, *v;  // bf16 (B, T, H, D)

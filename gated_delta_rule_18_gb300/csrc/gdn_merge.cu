@@ -82,7 +82,57 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams m, int vpr
     }
 }
 
+// out += add (rows of V, 16-byte vectors; add contiguous (B, T, H, V) in
+// out's dtype) and den += den_add (B * H * T), fp32 arithmetic
+template <class T>
+__global__ void __launch_bounds__(256) sum_kernel(const SumParams a, int vpr, int rows_per_block) {
+    constexpr int kVec = 16 / sizeof(T);
+    const int tid = threadIdx.x;
+    const int64_t row = (int64_t)blockIdx.x * rows_per_block + tid / vpr;
+    const int c = (tid % vpr) * kVec;
+    const int64_t rows = (int64_t)a.B * a.T * a.H;
+    if (tid < rows_per_block * vpr && row < rows) {
+        const int64_t h = row % a.H, t = (row / a.H) % a.T, b = row / ((int64_t)a.H * a.T);
+        T *o = (T *)a.out + b * a.o_sb + t * a.o_st + h * a.o_sh + c;
+        const T *x = (const T *)a.add + row * a.V + c;
+        uint4 uo = *reinterpret_cast<const uint4 *>(o);
+        const uint4 ux = __ldg(reinterpret_cast<const uint4 *>(x));
+        if (sizeof(T) == 2) {
+            __nv_bfloat162 *po = reinterpret_cast<__nv_bfloat162 *>(&uo);
+            const __nv_bfloat162 *px = reinterpret_cast<const __nv_bfloat162 *>(&ux);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 fo = __bfloat1622float2(po[i]), fx = __bfloat1622float2(px[i]);
+                po[i] = __floats2bfloat162_rn(fo.x + fx.x, fo.y + fx.y);
+            }
+        } else {
+            float *po = reinterpret_cast<float *>(&uo);
+            const float *px = reinterpret_cast<const float *>(&ux);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) po[i] += px[i];
+        }
+        *reinterpret_cast<uint4 *>(o) = uo;
+    }
+    if (a.den)
+        for (int64_t i = (int64_t)blockIdx.x * 256 + tid; i < (int64_t)a.B * a.H * a.T; i += (int64_t)gridDim.x * 256)
+            a.den[i] += a.den_add[i];
+}
+
 }  // namespace
+
+cudaError_t launch_sum(const SumParams &a, cudaStream_t st) {
+    const int vec = a.bf16 ? 8 : 4;
+    const int vpr = a.V / vec;
+    const int rows_per_block = vpr <= 256 ? 256 / vpr : 0;
+    if (rows_per_block == 0) return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)a.B * a.T * a.H;
+    if (rows > INT32_MAX) return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+    if (grid == 0) return cudaSuccess;
+    if (a.bf16) sum_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a, vpr, rows_per_block);
+    else sum_kernel<float><<<grid, 256, 0, st>>>(a, vpr, rows_per_block);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeParams &m, cudaStream_t st) {
     const int vec = m.num_bf16 ? 8 : 4;

@@ -367,6 +367,24 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
             const uint32_t par = c & 1;
+            const int pos0 = (cb + c) * kChunk;
+            const int Lc = min(kChunk, si.len - pos0);
+            const bool wr = i < Lc && !p.summary && p.out;  // no output: summary or recompute pass
+            const int tq = wr ? q_token(p.reverse, si.len, pos0 + i) : 0;
+            const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
+            float *dp = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
+            const bool den_here = p.has_den && v0 <= V && V < v0 + 64;
+            // accumulating into bf16 rows: their old contents are loaded while
+            // this chunk's products are still running
+            uint4 prev[8];
+            float dprev = 0.f;
+            if (wr && p.accumulate && !p.out_f32) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    prev[j] = (v0 + 8 * j + 8 <= V) ? *reinterpret_cast<const uint4 *>((const bf16 *)p.out + off + 8 * j)
+                                                    : make_uint4(0, 0, 0, 0);
+            }
+            if (wr && p.accumulate && den_here) dprev = *dp;
             ok = warp_all(wait_bar(b_o, par, abort));
             tc_fence_after();
             // chunk c's last MMA is done: stage c&1 may take chunk c+2's MMA
@@ -377,47 +395,56 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             tc_ld64(tmem + lane_base + kColD + par * 64, t);
             tc_fence_before();
             arrive(b_of[c & 1]);
-            const int pos0 = (cb + c) * kChunk;
-            const int Lc = min(kChunk, si.len - pos0);
-            if (!ok || i >= Lc || p.summary || !p.out) continue;  // no output: summary or recompute pass
-            const int tq = q_token(p.reverse, si.len, pos0 + i);
-            const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
+            if (!ok || !wr) continue;
+            if (p.out_f32) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int col = v0 + 8 * j;
-                if (col + 8 <= V) {
-                    if (p.out_f32) {
-                        float4 *op = reinterpret_cast<float4 *>((float *)p.out + off + 8 * j);
-                        float4 a = make_float4(t[8 * j], t[8 * j + 1], t[8 * j + 2], t[8 * j + 3]);
-                        float4 b = make_float4(t[8 * j + 4], t[8 * j + 5], t[8 * j + 6], t[8 * j + 7]);
-                        if (p.accumulate) {
-                            const float4 y0 = op[0], y1 = op[1];
-                            a.x += y0.x; a.y += y0.y; a.z += y0.z; a.w += y0.w;
-                            b.x += y1.x; b.y += y1.y; b.z += y1.z; b.w += y1.w;
-                        }
-                        op[0] = a;
-                        op[1] = b;
-                    } else {
-                        uint4 *op = reinterpret_cast<uint4 *>((bf16 *)p.out + off + 8 * j);
-                        float f[8];
+                for (int h4 = 0; h4 < 2; ++h4) {  // per half: every load before any store
+                    float4 y[8];
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) f[x] = t[8 * j + x];
-                        if (p.accumulate) {
-                            const uint4 y = *op;
-                            const __nv_bfloat162 *y2 = reinterpret_cast<const __nv_bfloat162 *>(&y);
-#pragma unroll
-                            for (int x = 0; x < 4; ++x) {
-                                const float2 fy = __bfloat1622float2(y2[x]);
-                                f[2 * x] += fy.x;
-                                f[2 * x + 1] += fy.y;
-                            }
-                        }
-                        *op = pack8(f);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = 4 * h4 + jj;
+                        const bool in = p.accumulate && v0 + 8 * j + 8 <= V;
+                        const float4 *op = reinterpret_cast<const float4 *>((const float *)p.out + off + 8 * j);
+                        y[2 * jj] = in ? op[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        y[2 * jj + 1] = in ? op[1] : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                } else if (p.has_den && col == V) {
-                    float *dp = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
-                    *dp = p.accumulate ? *dp + t[8 * j] : t[8 * j];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = 4 * h4 + jj;
+                        if (v0 + 8 * j + 8 > V) continue;
+                        float4 *op = reinterpret_cast<float4 *>((float *)p.out + off + 8 * j);
+                        const float4 y0 = y[2 * jj], y1 = y[2 * jj + 1];
+                        op[0] = make_float4(t[8 * j] + y0.x, t[8 * j + 1] + y0.y, t[8 * j + 2] + y0.z,
+                                            t[8 * j + 3] + y0.w);
+                        op[1] = make_float4(t[8 * j + 4] + y1.x, t[8 * j + 5] + y1.y, t[8 * j + 6] + y1.z,
+                                            t[8 * j + 7] + y1.w);
+                    }
                 }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (v0 + 8 * j + 8 > V) continue;
+                    float f[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) f[x] = t[8 * j + x];
+                    if (p.accumulate) {
+                        const __nv_bfloat162 *y2 = reinterpret_cast<const __nv_bfloat162 *>(&prev[j]);
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const float2 fy = __bfloat1622float2(y2[x]);
+                            f[2 * x] += fy.x;
+                            f[2 * x + 1] += fy.y;
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>((bf16 *)p.out + off + 8 * j) = pack8(f);
+                }
+            }
+            if (den_here) {  // the ones column V sits at the start of an 8-column group
+                float dv = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (v0 + 8 * j == V) dv = t[8 * j];
+                *dp = (p.accumulate ? dprev : 0.f) + dv;
             }
         }
     }

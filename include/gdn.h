@@ -286,6 +286,39 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd,
 
 /* Human-readable name of a status code (static storage). */
 /*
+ * gdn_bidir_workspace_size / gdn_chunk_fwd_bidir -- both directions of the
+ * bidirectional scan in one call (SANA `fused_gdn.py` page, `fused_bigdn_func`
+ * forms num_fwd + num_bwd and den_fwd + den_bwd before any divide), with the
+ * two directions running concurrently: the reverse scan is launched on a
+ * second stream the library owns for the current device (forked from and
+ * joined back to `stream` with events, so the call stays asynchronous and
+ * capturable), writes its half into the workspace, and a last kernel on
+ * `stream` adds it into out (and den_out). The result equals gdn_chunk_fwd
+ * (reverse = 0) followed by gdn_chunk_fwd (reverse = 1, GDN_ACCUMULATE) up to
+ * rounding.
+ *   Arguments as gdn_chunk_fwd (no h0 / h_final, out overwritten); out has
+ *   q's dtype. g_bwd / beta_bwd: the reverse direction's log gates and betas
+ *   (the chunk-causal form's decay_bwd / beta_bwd), or NULL for g / beta;
+ *   g_bwd only with a scalar gate. flags: GDN_QK_L2NORM.
+ *   workspace: >= gdn_bidir_workspace_size() bytes, 256-byte aligned; the
+ *   device error word of gdn_last_device_error() is the forward half's.
+ * Calls on one device serialise their launches on a host lock (the side
+ * stream and its events are shared).
+ */
+size_t gdn_bidir_workspace_size(int B, int T, int H, int K, int V, int n_seq,
+                                int varlen, int dtype, int with_den);
+gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd,
+                               const void *v, gdn_tensor_desc vd,
+                               const float *g, const float *gk,
+                               const float *beta, const float *g_bwd,
+                               const float *beta_bwd,
+                               const int32_t *cu_seqlens, int n_seq,
+                               void *out, gdn_tensor_desc od, float *den_out,
+                               int B, int T, int H, int K, int V, int chunk,
+                               int flags, void *workspace, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/*
  * gdn_merge -- the bidirectional merge (SANA `fused_gdn.py` page,
  * `fused_bigdn_func`: out = (num_fwd + num_bwd) / (den_fwd + den_bwd + eps),
  * and `_fused_bidi_merge_kernel` with APPLY_GATE: times silu(gate) =

@@ -217,6 +217,21 @@ def test_chunk_bwd_rejects_on_host(L):
     assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 256) == 0
 
 
+def test_bidir_rejects_on_host(L):
+    d16, d32 = desc(gdn.BF16, 1, 128, 2, 64), desc(gdn.F32, 1, 128, 2, 64)
+
+    def bd(g=P(3), gk=None, g_bwd=None, od=d16, flags=0, wsb=1 << 30, T=128):
+        return L.gdn_chunk_fwd_bidir(P(0), P(1), d16, P(2), d16, g, gk, P(4), g_bwd, None, None, 1,
+                                     P(5), od, P(6), 1, T, 2, 64, 64, 64, flags, P(9), wsb, None)
+    assert bd(g=None, gk=P(7), g_bwd=P(8)) == UNSUP   # backward gates replace a scalar gate only
+    assert bd(flags=GDN_ACCUMULATE_FLAG) == UNSUP      # out is overwritten
+    assert bd(od=d32) == DTYPE                         # out in q's dtype
+    assert bd(wsb=1024) == WS
+    assert bd(T=0) == OK
+    assert gdn.gdn_bidir_workspace_size(1, 128, 2, 64, 64, 1, 0, gdn.BF16, 1) > \
+        2 * gdn.gdn_workspace_size(1, 128, 2, 64, 64, 1, 0, gdn.BF16, 1)
+
+
 def test_seg_choose_sizes_the_grid():
     """Host arithmetic only: segments pay when few (sequence, head, value
     tile) CTAs would walk a long sequence, never when the plain pass already
