@@ -544,6 +544,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     b.h_snap = p.h_snap, b.vn_snap = p.vn_snap;
     b.dh_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dh);
     b.dvn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dvn);
+    b.err = p.err;
     e = launch(KBwdDh, stream, [&] { return gdn::launch_bwd_dh(b, stream); });
     if (e == cudaSuccess) e = launch(KBwdDq, stream, [&] { return gdn::launch_bwd_dq(b, stream); });
     if (e == cudaSuccess) e = launch(KBwdDk, stream, [&] { return gdn::launch_bwd_dk(b, stream); });

@@ -11,10 +11,14 @@
 //   dh     = e^{G_C} dh' + qg^T do - w^T dv_new (dL/dh, handed to chunk c-1)
 // One CTA (8 warps) per (sequence, head, 64-column value tile) walks the
 // chunks last to first; dh (128 keys x 64 columns, fp32) lives in the warps'
-// mma accumulators, warp w holding keys 16w .. 16w+15. The chunk operands
-// (the forward's P, qg, kg, w images and decay, and the do tile) are copied
-// with cp.async one chunk ahead into row-major tiles. Per chunk it stores
-// dh' and dv_new (bf16) for the chunk-parallel gradient kernels.
+// mma accumulators, warp w holding keys 16w .. 16w+15. The forward's P, qg,
+// kg and w images and decay arrive one chunk ahead by one bulk async copy
+// each onto an mbarrier and are read by ldmatrix in their stored (core
+// block) layout; the do tile comes by cp.async. Per chunk the kernel stores
+// dh' and dv_new (bf16, 16-byte stores from shared memory) for the
+// chunk-parallel gradient kernels. Every wait is bounded (about 0.5 s); a
+// wait that gives up marks the error word and the CTA leaves after its
+// copies in flight have landed (again bounded).
 #include "gdn_mma.cuh"
 
 namespace gdn {
@@ -23,26 +27,28 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kThreads = 256;
-constexpr int kLK = kKP + 8;  // row stride of a 128-column tile
-constexpr int kL6 = 64 + 8;   // row stride of a 64-column tile
+constexpr int kL6 = 64 + 8;  // row stride of a 64-column tile
+constexpr uint32_t kStageBytes = kImgP + 3 * kImgW + kDecB;
+constexpr int kDevErrTimeout = 2;  // the error word's time-out bit
 
 struct DhStage {
-    bf16 p[kChunk * kL6];    // P [i][j]
-    bf16 qg[kChunk * kLK];   // qg [i][d]
-    bf16 kd[kChunk * kLK];   // kg [i][d]
-    bf16 w[kChunk * kLK];    // w [i][d]
-    bf16 dout[kChunk * kL6]; // do [i][col]
+    unsigned char p[kImgP];   // P image
+    unsigned char qg[kImgW];  // qg image
+    unsigned char kd[kImgW];  // kg^T image
+    unsigned char w[kImgW];   // w image
     float dec[kKP];
+    bf16 dout[kChunk * kL6];  // do [i][col]
 };
 struct DhSmem {
     DhStage st[2];
-    bf16 dh[kKP * kL6];      // dh' [d][col] (B operand)
-    bf16 dvn[kChunk * kL6];  // -dv_new [i][col] (B operand)
+    bf16 dh[kKP * kL6];       // dh' [d][col] (B operand)
+    bf16 dvn[kChunk * kL6];   // -dv_new [i][col] (B operand)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) {
-    extern __shared__ __align__(16) unsigned char smraw[];
+    extern __shared__ __align__(128) unsigned char smraw[];
     DhSmem &sm = *reinterpret_cast<DhSmem *>(smraw);
+    __shared__ __align__(8) uint64_t bars[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
     const int s = blockIdx.x / p.H, hh = blockIdx.x % p.H;
@@ -50,27 +56,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
     const int K = p.K, V = p.V, T = p.T;
     const int nts = (T + kChunk - 1) / kChunk;
     const bf16 *dout = (const bf16 *)p.dout;
+    const uint32_t bar[2] = {smem_u32(&bars[0]), smem_u32(&bars[1])};
+    if (tid == 0) {
+        mbar_init(bar[0], 1);
+        mbar_init(bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
 
-    auto stage = [&](int c) {
-        DhStage &S = sm.st[c & 1];
-        const int64_t gch = (int64_t)hh * p.max_chunks + (int64_t)s * nts + c;
+    // step `it` handles chunk nts - 1 - it in stage it & 1
+    auto gch_of = [&](int it) { return (int64_t)hh * p.max_chunks + (int64_t)s * nts + (nts - 1 - it); };
+    auto stage = [&](int it) {
+        DhStage &S = sm.st[it & 1];
+        const int c = nts - 1 - it;
+        const int64_t gch = gch_of(it);
+        if (tid == 0) {
+            fence_async_smem();  // earlier generic reads of this stage come first
+            arrive_expect_tx(bar[it & 1], kStageBytes);
+            bulk_g2s(smem_u32(S.p), p.p_img + gch * kImgP, kImgP, bar[it & 1]);
+            bulk_g2s(smem_u32(S.qg), p.qg_img + gch * kImgW, kImgW, bar[it & 1]);
+            bulk_g2s(smem_u32(S.kd), p.kg_img + gch * kImgW, kImgW, bar[it & 1]);
+            bulk_g2s(smem_u32(S.w), p.w_img + gch * kImgW, kImgW, bar[it & 1]);
+            bulk_g2s(smem_u32(S.dec), p.dec + gch * kKP, kDecB, bar[it & 1]);
+        }
         const int pos0 = c * kChunk, Lc = min(kChunk, T - pos0);
-        for (int e = tid; e < kChunk * 8; e += kThreads) {  // P and do: 64 rows x 8 pieces
-            const int i = e >> 3, j8 = (e & 7) * 8;
-            cp_async16(S.p + i * kL6 + j8, p.p_img + gch * kImgP + img_p_off(i, j8), 16);
-            const int col = v0 + j8;
+        for (int e = tid; e < kChunk * 8; e += kThreads) {  // do: 64 rows x 8 pieces
+            const int i = e >> 3, c8 = (e & 7) * 8, col = v0 + c8;
             const bool in = i < Lc && col < V;
             const int tq = in ? q_token(p.reverse, T, pos0 + i) : 0;
             const bf16 *src = in ? dout + s * p.do_sb + (int64_t)tq * p.do_st + hh * p.do_sh + col : dout;
-            cp_async16(S.dout + i * kL6 + j8, src, in ? 16 : 0);
+            cp_async16(S.dout + i * kL6 + c8, src, in ? 16 : 0);
         }
-        for (int e = tid; e < kChunk * 16; e += kThreads) {  // qg, kg, w: 64 rows x 16 pieces
-            const int i = e >> 4, d8 = (e & 15) * 8;
-            cp_async16(S.qg + i * kLK + d8, p.qg_img + gch * kImgW + img_w_off(i, d8), 16);
-            cp_async16(S.kd + i * kLK + d8, p.kg_img + gch * kImgW + img_kt_off(i, d8), 16);
-            cp_async16(S.w + i * kLK + d8, p.w_img + gch * kImgW + img_w_off(i, d8), 16);
-        }
-        if (tid < kKP / 4) cp_async16(S.dec + 4 * tid, p.dec + gch * kKP + 4 * tid, 16);
         cp_async_commit();
     };
 
@@ -84,47 +100,85 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
             acc[n][e] = (p.dh_final && r < K && col < V) ? p.dh_final[(((int64_t)s * p.H + hh) * K + r) * V + col]
                                                          : 0.f;
         }
-    if (nts > 0) stage(nts - 1);
-    for (int c = nts - 1; c >= 0; --c) {
-        const DhStage &S = sm.st[c & 1];
-        if (c > 0) {
-            stage(c - 1);
+    if (nts > 0) stage(0);
+    bool ok = true;
+    int it = 0;
+    for (; it < nts; ++it) {
+        const DhStage &S = sm.st[it & 1];
+        if (it + 1 < nts) {
+            stage(it + 1);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
-        // dh' to the B-operand tile and to its snapshot
-        const int64_t gch = (int64_t)hh * p.max_chunks + (int64_t)s * nts + c;
-        bf16 *snap = p.dh_snap + gch * K * V;
+        ok = wait_bar(bar[it & 1], (it >> 1) & 1, nullptr);
+        // dh' to the B-operand tile
 #pragma unroll
         for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int r = 16 * warp + g8 + 8 * hf, cl = 8 * n + 2 * t4;
-                const uint32_t pk = pack_bf16(acc[n][2 * hf], acc[n][2 * hf + 1]);
-                *reinterpret_cast<uint32_t *>(sm.dh + r * kL6 + cl) = pk;
-                if (r < K && v0 + cl < V) *reinterpret_cast<uint32_t *>(snap + (int64_t)r * V + v0 + cl) = pk;
+            for (int hf = 0; hf < 2; ++hf)
+                *reinterpret_cast<uint32_t *>(sm.dh + (16 * warp + g8 + 8 * hf) * kL6 + 8 * n + 2 * t4) =
+                    pack_bf16(acc[n][2 * hf], acc[n][2 * hf + 1]);
+        if (__syncthreads_or(!ok)) break;
+        const int64_t gch = gch_of(it);
+        {  // its snapshot, 16-byte pieces
+            bf16 *snap = p.dh_snap + gch * K * V + v0;
+            for (int e = tid; e < kKP * 8; e += kThreads) {
+                const int r = e >> 3, c8 = (e & 7) * 8;
+                if (r < K && v0 + c8 < V)
+                    *reinterpret_cast<uint4 *>(snap + (int64_t)r * V + c8) =
+                        *reinterpret_cast<const uint4 *>(sm.dh + r * kL6 + c8);
             }
-        __syncthreads();
+        }
         // dv_new = P^T do + kg dh'  (64 tokens x 64 columns; warp: 16 rows x 32 columns)
         {
             float a2[4][4];
             acc_zero(a2);
             const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
-            warp_gemm(a2, Tile{S.p, kL6}, true, Tile{S.dout, kL6}, true, m0, n0, kChunk, lane);
-            warp_gemm(a2, Tile{S.kd, kLK}, false, Tile{sm.dh, kL6}, true, m0, n0, kKP, lane);
-            bf16 *vsnap = p.dvn_snap + gch * kChunk * V;
+            const Tile tdo{S.dout, kL6}, tdh{sm.dh, kL6};
+#pragma unroll
+            for (int k0 = 0; k0 < kChunk; k0 += 16) {  // P^T: stored [i][j], read transposed
+                uint32_t a[4];
+                ldsm_x4_t(a, S.p + img_p_off(k0 + (lane & 7) + ((lane >> 4) << 3), m0 + ((lane >> 3) & 1) * 8));
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t b[4];
+                    frag_b2(b, tdo, true, n0 + 16 * np, k0, lane);
+                    mma_bf16(a2[2 * np], a, b[0], b[1]);
+                    mma_bf16(a2[2 * np + 1], a, b[2], b[3]);
+                }
+            }
+#pragma unroll
+            for (int k0 = 0; k0 < kKP; k0 += 16) {  // kg: [j][d] pieces of the kg^T image
+                uint32_t a[4];
+                ldsm_x4(a, S.kd + img_kt_off(m0 + (lane & 15), k0 + (lane >> 4) * 8));
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t b[4];
+                    frag_b2(b, tdh, true, n0 + 16 * np, k0, lane);
+                    mma_bf16(a2[2 * np], a, b[0], b[1]);
+                    mma_bf16(a2[2 * np + 1], a, b[2], b[3]);
+                }
+            }
 #pragma unroll
             for (int n = 0; n < 4; ++n)
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int i = m0 + g8 + 8 * hf, cl = n0 + 8 * n + 2 * t4;
-                    const float x0 = a2[n][2 * hf], x1 = a2[n][2 * hf + 1];
-                    *reinterpret_cast<uint32_t *>(sm.dvn + i * kL6 + cl) = pack_bf16(-x0, -x1);
-                    if (v0 + cl < V) *reinterpret_cast<uint32_t *>(vsnap + (int64_t)i * V + v0 + cl) = pack_bf16(x0, x1);
-                }
+                for (int hf = 0; hf < 2; ++hf)
+                    *reinterpret_cast<uint32_t *>(sm.dvn + (m0 + g8 + 8 * hf) * kL6 + n0 + 8 * n + 2 * t4) =
+                        pack_bf16(-a2[n][2 * hf], -a2[n][2 * hf + 1]);
         }
         __syncthreads();
+        {  // dv_new's snapshot (the tile holds -dv_new: flip the sign bits)
+            bf16 *vsnap = p.dvn_snap + gch * kChunk * V + v0;
+            for (int e = tid; e < kChunk * 8; e += kThreads) {
+                const int i = e >> 3, c8 = (e & 7) * 8;
+                if (v0 + c8 < V) {
+                    uint4 u = *reinterpret_cast<const uint4 *>(sm.dvn + i * kL6 + c8);
+                    u.x ^= 0x80008000u, u.y ^= 0x80008000u, u.z ^= 0x80008000u, u.w ^= 0x80008000u;
+                    *reinterpret_cast<uint4 *>(vsnap + (int64_t)i * V + c8) = u;
+                }
+            }
+        }
         // dh = e^{G_C} dh' + qg^T do - w^T dv_new
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -135,9 +189,35 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
                 acc[n][2 * hf + 1] *= d;
             }
         }
-        warp_gemm(acc, Tile{S.qg, kLK}, true, Tile{S.dout, kL6}, true, 16 * warp, 0, kChunk, lane);
-        warp_gemm(acc, Tile{S.w, kLK}, true, Tile{sm.dvn, kL6}, true, 16 * warp, 0, kChunk, lane);
-        __syncthreads();  // stage c & 1, dh and dvn are rewritten next
+        {
+            const Tile tdo{S.dout, kL6}, tdv{sm.dvn, kL6};
+            const int m0 = 16 * warp;
+#pragma unroll
+            for (int k0 = 0; k0 < kChunk; k0 += 16) {  // qg^T and w^T: stored [i][d], read transposed
+                uint32_t aq[4], aw[4];
+                ldsm_x4_t(aq, S.qg + img_w_off(k0 + (lane & 7) + ((lane >> 4) << 3), m0 + ((lane >> 3) & 1) * 8));
+                ldsm_x4_t(aw, S.w + img_w_off(k0 + (lane & 7) + ((lane >> 4) << 3), m0 + ((lane >> 3) & 1) * 8));
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    uint32_t b[4], bv[4];
+                    frag_b2(b, tdo, true, 16 * np, k0, lane);
+                    frag_b2(bv, tdv, true, 16 * np, k0, lane);
+                    mma_bf16(acc[2 * np], aq, b[0], b[1]);
+                    mma_bf16(acc[2 * np + 1], aq, b[2], b[3]);
+                    mma_bf16(acc[2 * np], aw, bv[0], bv[1]);
+                    mma_bf16(acc[2 * np + 1], aw, bv[2], bv[3]);
+                }
+            }
+        }
+        __syncthreads();  // stage it & 1, dh and dvn are rewritten next
+    }
+    if (!ok) {
+        // a copy wait gave up: record it, let the copies in flight land, leave
+        if (tid == 0) atomicOr(p.err, kDevErrTimeout);
+        cp_async_wait<0>();
+        wait_bar(bar[it & 1], (it >> 1) & 1, nullptr);
+        if (it + 1 < nts) wait_bar(bar[(it + 1) & 1], ((it + 1) >> 1) & 1, nullptr);
+        return;
     }
     if (p.dh0) {
 #pragma unroll

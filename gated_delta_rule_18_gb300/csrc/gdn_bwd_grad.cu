@@ -107,10 +107,11 @@ __device__ __forceinline__ void rowcol_add(const float (&c)[4][4], int m0, int n
 // scaled in place (bf16)
 __device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_out, bool l2) {
     const int tid = threadIdx.x;
-    if (tid < kChunk) {
+    {  // four threads per row, each a quarter of the columns
+        const int row = tid >> 2, q4 = tid & 3;
         float ss = 0.f;
-        for (int d = 0; d < ncol; d += 8) {
-            const uint4 u = *reinterpret_cast<const uint4 *>(t + tid * ld + d);
+        for (int d = 8 * q4; d < ncol; d += 32) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(t + row * ld + d);
             const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
@@ -118,7 +119,9 @@ __device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_ou
                 ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
             }
         }
-        r_out[tid] = l2 ? rsqrtf(ss + 1e-6f) : 1.f;
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (q4 == 0) r_out[row] = l2 ? rsqrtf(ss + 1e-6f) : 1.f;
     }
     __syncthreads();
     if (!l2) return;
@@ -385,6 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         return r < K ? p.dh_snap + (x.gch * K + r) * V : nullptr;
     });
     cp_async_commit();
+    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
+    // bwd_dq's M_P^T Q^ for this thread's dk fragment, loaded now (added at the end)
+    float2 pdk[2][8];
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int tk = kv_row(m0 + g8 + 8 * hf);
+        const float *src = tk >= 0 ? p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K : nullptr;
+#pragma unroll
+        for (int n = 0; n < 8; ++n) {
+            const int d = nk0 + 8 * n + 2 * t4;
+            pdk[hf][n] = (src && d < K) ? *reinterpret_cast<const float2 *>(src + d) : make_float2(0.f, 0.f);
+        }
+    }
     if (tid < kChunk) sm.dG[tid] = sm.dB[tid] = sm.row[tid] = 0.f;
     if (tid == 0) sm.gc = 0.f;
     gates(p, x, sm.G, sm.beta, sm.graw);
@@ -393,21 +409,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
     const int last = x.Lc - 1;
     const float GC = sm.G[last];
-    // e^{G_C} h . dh'  (dG_C of the state decay)
+    // e^{G_C} h . dh'  (dG_C of the state decay), 8 columns per step
     {
         float acc = 0.f;
-        for (int e = tid; e < K * (kv / 2); e += kThreads) {
-            const int r = e / (kv / 2), c2 = (e % (kv / 2)) * 2;
-            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.u.a.h + r * kLK + c2));
-            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(sm.u.a.dh + r * kLK + c2));
-            acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+        for (int e = tid; e < K * (kv / 8); e += kThreads) {
+            const int r = e / (kv / 8), c8 = (e % (kv / 8)) * 8;
+            const uint4 ua = *reinterpret_cast<const uint4 *>(sm.u.a.h + r * kLK + c8);
+            const uint4 ub = *reinterpret_cast<const uint4 *>(sm.u.a.dh + r * kLK + c8);
+            const __nv_bfloat162 *a2 = reinterpret_cast<const __nv_bfloat162 *>(&ua);
+            const __nv_bfloat162 *b2 = reinterpret_cast<const __nv_bfloat162 *>(&ub);
+#pragma unroll
+            for (int x2 = 0; x2 < 4; ++x2) {
+                const float2 a = __bfloat1622float2(a2[x2]), b = __bfloat1622float2(b2[x2]);
+                acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
+            }
         }
         acc = warp_sum(acc);
         if (lane == 0) atomicAdd(&sm.gc, acc * __expf(GC));
     }
     __syncthreads();
 
-    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
     // factors of this thread's two fragment rows: e^{G_i}, e^{G_C - G_i} (0
     // past the chunk's end)
     float egr[2], ecr[2];
@@ -479,10 +500,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         float t[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            float acc = (r == lane) ? 1.f : 0.f;
+            // t_r = e_r - beta_r sum_{j<r} kkg_rj t_j, in two independent halves
+            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < r; ++j) acc = fmaf(-sm.beta[o + r] * sm.kkg[(o + r) * kPS + o + j], t[j], acc);
-            t[r] = acc;
+            for (int j = 0; j < r; ++j) {
+                if (j & 1) a1 = fmaf(sm.kkg[(o + r) * kPS + o + j], t[j], a1);
+                else a0 = fmaf(sm.kkg[(o + r) * kPS + o + j], t[j], a0);
+            }
+            t[r] = ((r == lane) ? 1.f : 0.f) - sm.beta[o + r] * (a0 + a1);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(o + r) * kPS + o + lane] = t[r];
@@ -497,9 +522,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             rr[u] = 0.f;
             if (e < n_el) {
                 const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
-                float acc = 0.f;
-                for (int m = cidx & ~15; m < 16 * I; ++m) acc = fmaf(sm.kkg[r * kPS + m], sT[m * kPS + cidx], acc);
-                rr[u] = sm.beta[r] * acc;
+                // four independent partial sums (the span is a multiple of 16)
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                for (int m = cidx & ~15; m < 16 * I; m += 4) {
+                    a0 = fmaf(sm.kkg[r * kPS + m], sT[m * kPS + cidx], a0);
+                    a1 = fmaf(sm.kkg[r * kPS + m + 1], sT[(m + 1) * kPS + cidx], a1);
+                    a2 = fmaf(sm.kkg[r * kPS + m + 2], sT[(m + 2) * kPS + cidx], a2);
+                    a3 = fmaf(sm.kkg[r * kPS + m + 3], sT[(m + 3) * kPS + cidx], a3);
+                }
+                rr[u] = sm.beta[r] * ((a0 + a1) + (a2 + a3));
             }
         }
         __syncthreads();
@@ -515,10 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             rr[u] = 0.f;
             if (e < n_el) {
                 const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
-                float t = 0.f;
-#pragma unroll 4
-                for (int m = 0; m < 16; ++m) t = fmaf(sT[r * kPS + 16 * I + m], sT[(16 * I + m) * kPS + cidx], t);
-                rr[u] = -t;
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int m = 0; m < 16; ++m)
+                    t[m & 3] = fmaf(sT[r * kPS + 16 * I + m], sT[(16 * I + m) * kPS + cidx], t[m & 3]);
+                rr[u] = -((t[0] + t[1]) + (t[2] + t[3]));
             }
         }
         __syncthreads();
@@ -647,16 +679,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int i = m0 + g8 + 8 * hf;
-            const int tk = kv_row(i);
-            const float *src = tk >= 0 ? p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K : nullptr;
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
                 const int d = nk0 + 8 * n + 2 * t4;
-                if (src && d < K) {
-                    const float2 pp = *reinterpret_cast<const float2 *>(src + d);
-                    dk[n][2 * hf] += pp.x;
-                    dk[n][2 * hf + 1] += pp.y;
-                }
+                dk[n][2 * hf] += pdk[hf][n].x;
+                dk[n][2 * hf + 1] += pdk[hf][n].y;
                 part[hf] += dk[n][2 * hf] * __bfloat162float(sm.k[i * kLK + d]) +
                             dk[n][2 * hf + 1] * __bfloat162float(sm.k[i * kLK + d + 1]);
             }

@@ -85,6 +85,7 @@ struct BwdParams {
     const float *dec;
     const __nv_bfloat16 *h_snap, *vn_snap;
     __nv_bfloat16 *dh_snap, *dvn_snap;  // state gradient at each chunk's end, dL/dv_new
+    int *err;                           // device error word (bounded waits that gave up)
 };
 
 // ----------------------------------------------------- operand images -------
