@@ -30,7 +30,8 @@
 //           partial sum)
 //   bwd_dk  dk (adding that partial), dv, dbeta, dg (adding bwd_dq's dG).
 // Products run on mma.sync (bf16 operands, fp32 accumulate); T = (I + A)^{-1}
-// is formed in fp32 by blocks. 8 warps per CTA.
+// is formed by blocks (fp32 diagonal inverses, bf16 block products). 8 warps
+// per CTA.
 #include "gdn_mma.cuh"
 
 namespace gdn {
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
         if (tk < 0) return nullptr;
         return k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
     });
+    cp_async_commit();  // q and k first: the norms and Q K^T start while the rest lands
     load_rows(sm.dout, kLK, kChunk, V, [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
         return dout + x.s * p.do_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.do_st + x.hh * p.do_sh;
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
     cp_async_commit();
     if (tid < kChunk) sm.dG[tid] = sm.row[tid] = 0.f;
     gates(p, x, sm.G, nullptr, sm.graw);
-    cp_async_wait<0>();
+    cp_async_wait<1>();
     __syncthreads();
     norm_rows(sm.q, kLK, kq, sm.rq, p.l2norm);
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
@@ -218,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
         acc_zero(sp);
         acc_zero(dp);
         warp_gemm(sp, Tile{sm.q, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
+        cp_async_wait<0>();
+        __syncthreads();
         warp_gemm(dp, Tile{sm.dout, kLK}, false, Tile{sm.vn, kLK}, false, m0, n0, kv, lane);
         float ct[4][4];  // dP_ij P_ij: d/dG_i of P_ij is P_ij, d/dG_j is -P_ij
 #pragma unroll
@@ -338,7 +342,6 @@ struct DkP1 {  // until the products with h and dh' are done
     bf16 dh[kKP * kLK];
 };
 struct DkP2 {  // afterwards
-    float t[kChunk * kPS];
     bf16 tb[kChunk * kL6];
     bf16 xw[kChunk * kLK];
     bf16 y[kChunk * kL6];
@@ -371,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
     });
+    cp_async_commit();  // k first: the norms and K K^T start while the rest lands
     load_rows(sm.v, kLK, kChunk, V, [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : v + x.s * p.v_sb + (int64_t)tk * p.v_st + x.hh * p.v_sh;
@@ -404,11 +408,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     if (tid < kChunk) sm.dG[tid] = sm.dB[tid] = sm.row[tid] = 0.f;
     if (tid == 0) sm.gc = 0.f;
     gates(p, x, sm.G, sm.beta, sm.graw);
-    cp_async_wait<0>();
+    cp_async_wait<1>();
     __syncthreads();
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
     const int last = x.Lc - 1;
     const float GC = sm.G[last];
+    __syncthreads();
+    // S . Gamma, strictly lower
+    {
+        float sk[4][4];
+        acc_zero(sk);
+        warp_gemm(sk, Tile{sm.k, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = m0 + g8 + 8 * (e >> 1), j = n0 + 8 * n + 2 * t4 + (e & 1);
+                sm.kkg[i * kPS + j] = (j < i && i < x.Lc) ? __expf(sm.G[i] - sm.G[j]) * sk[n][e] : 0.f;
+            }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
     // e^{G_C} h . dh'  (dG_C of the state decay), 8 columns per step
     {
         float acc = 0.f;
@@ -437,19 +457,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         const int i = m0 + g8 + 8 * hf;
         egr[hf] = __expf(sm.G[i]);
         ecr[hf] = i < x.Lc ? __expf(GC - sm.G[i]) : 0.f;
-    }
-    // S . Gamma, strictly lower
-    {
-        float sk[4][4];
-        acc_zero(sk);
-        warp_gemm(sk, Tile{sm.k, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = m0 + g8 + 8 * (e >> 1), j = n0 + 8 * n + 2 * t4 + (e & 1);
-                sm.kkg[i * kPS + j] = (j < i && i < x.Lc) ? __expf(sm.G[i] - sm.G[j]) * sk[n][e] : 0.f;
-            }
     }
     // dk^ starts with the kg term: e^{G_C - G} . (v_new dh'^T)
     float dk[8][4];
@@ -491,9 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     }
     __syncthreads();  // v_new, h, dh' are done with: their space takes T and the rest
 
-    // T = (I + A)^{-1}, A_ij = beta_i (S . Gamma)_ij (i > j), by 16 x 16 blocks
-    float *sT = sm.u.b.t;
-    for (int e = tid; e < kChunk * kPS; e += kThreads) sT[e] = 0.f;
+    // T = (I + A)^{-1}, A_ij = beta_i (S . Gamma)_ij (i > j), by 16 x 16
+    // blocks as in the forward's solve: diagonal inverses T_II in fp32 by
+    // forward substitution, B_IM = -T_II A_IM, then block row I of T is
+    // sum_{M<I} B_IM (block row M) next to T_II (bf16 products, fp32 sums).
+    // A and the B_IM take the Y and Z tiles' space until those are formed.
+    bf16 *sTb = sm.u.b.tb, *sAb = sm.u.b.y, *sBb = sm.u.b.z;
+    for (int e = tid; e < kChunk * 32; e += kThreads) {
+        const int i = e >> 5, j = (e & 31) * 2;
+        const float a0 = j < i ? sm.beta[i] * sm.kkg[i * kPS + j] : 0.f;
+        const float a1 = j + 1 < i ? sm.beta[i] * sm.kkg[i * kPS + j + 1] : 0.f;
+        *reinterpret_cast<uint32_t *>(sAb + i * kL6 + j) = pack_bf16(a0, a1);
+        *reinterpret_cast<uint32_t *>(sTb + i * kL6 + j) = 0u;
+    }
     __syncthreads();
     if (warp < 4 && lane < 16) {  // diagonal blocks: forward substitution, lane = column
         const int o = 16 * warp;
@@ -510,62 +527,46 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             t[r] = ((r == lane) ? 1.f : 0.f) - sm.beta[o + r] * (a0 + a1);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(o + r) * kPS + o + lane] = t[r];
+        for (int r = 0; r < 16; ++r) sTb[(o + r) * kL6 + o + lane] = __float2bfloat16_rn(t[r]);
     }
     __syncthreads();
-    for (int I = 1; I < 4; ++I) {  // block row I: T_IJ = -T_II sum_{J <= M < I} A_IM T_MJ
-        const int n_el = 16 * 16 * I;  // rows 16I .. 16I+15, columns 0 .. 16I-1
-        float rr[3];
+    if (warp >= 1 && warp < 4) {  // B_IM = -T_II A_IM for M < I = warp
+        const int I = warp;
+        uint32_t a[4];
+        frag_a(a, Tile{sTb, kL6}, false, 16 * I, 16 * I, lane);
 #pragma unroll
-        for (int u = 0; u < 3; ++u) {  // R_IJ = sum_{J <= M < I} A_IM T_MJ
-            const int e = tid + u * kThreads;
-            rr[u] = 0.f;
-            if (e < n_el) {
-                const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
-                // four independent partial sums (the span is a multiple of 16)
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                for (int m = cidx & ~15; m < 16 * I; m += 4) {
-                    a0 = fmaf(sm.kkg[r * kPS + m], sT[m * kPS + cidx], a0);
-                    a1 = fmaf(sm.kkg[r * kPS + m + 1], sT[(m + 1) * kPS + cidx], a1);
-                    a2 = fmaf(sm.kkg[r * kPS + m + 2], sT[(m + 2) * kPS + cidx], a2);
-                    a3 = fmaf(sm.kkg[r * kPS + m + 3], sT[(m + 3) * kPS + cidx], a3);
-                }
-                rr[u] = sm.beta[r] * ((a0 + a1) + (a2 + a3));
+        for (int x2 = 0; x2 < 4; ++x2) a[x2] ^= 0x80008000u;  // -T_II
+        for (int M = 0; M < I; ++M) {
+            uint32_t b[4];
+            ldsm_x4_t(b, sAb + (16 * I + (lane & 15)) * kL6 + 16 * M + (lane >> 4) * 8);
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(c0, a, b[0], b[1]);
+            mma_bf16(c1, a, b[2], b[3]);
+            bf16 *dst = sBb + (16 * I) * kL6 + 16 * M;
+            *reinterpret_cast<uint32_t *>(dst + g8 * kL6 + 2 * t4) = pack_bf16(c0[0], c0[1]);
+            *reinterpret_cast<uint32_t *>(dst + (g8 + 8) * kL6 + 2 * t4) = pack_bf16(c0[2], c0[3]);
+            *reinterpret_cast<uint32_t *>(dst + g8 * kL6 + 8 + 2 * t4) = pack_bf16(c1[0], c1[1]);
+            *reinterpret_cast<uint32_t *>(dst + (g8 + 8) * kL6 + 8 + 2 * t4) = pack_bf16(c1[2], c1[3]);
+        }
+    }
+    __syncthreads();
+    for (int I = 1; I < 4; ++I) {  // block row I left of the diagonal
+        if (warp == I) {
+            float tr[8][4];
+            acc_zero(tr);
+            warp_gemm(tr, Tile{sBb, kL6}, false, Tile{sTb, kL6}, true, 16 * I, 0, 16 * I, lane);
+#pragma unroll
+            for (int n = 0; n < 8; ++n) {
+                if (8 * n >= 16 * I) break;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    *reinterpret_cast<uint32_t *>(sTb + (16 * I + g8 + 8 * hf) * kL6 + 8 * n + 2 * t4) =
+                        pack_bf16(tr[n][2 * hf], tr[n][2 * hf + 1]);
             }
         }
         __syncthreads();
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-            const int e = tid + u * kThreads;
-            if (e < n_el) sT[(16 * I + e / (16 * I)) * kPS + e % (16 * I)] = rr[u];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {  // T_IJ = -T_II R_IJ
-            const int e = tid + u * kThreads;
-            rr[u] = 0.f;
-            if (e < n_el) {
-                const int r = 16 * I + e / (16 * I), cidx = e % (16 * I);
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int m = 0; m < 16; ++m)
-                    t[m & 3] = fmaf(sT[r * kPS + 16 * I + m], sT[(16 * I + m) * kPS + cidx], t[m & 3]);
-                rr[u] = -((t[0] + t[1]) + (t[2] + t[3]));
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-            const int e = tid + u * kThreads;
-            if (e < n_el) sT[(16 * I + e / (16 * I)) * kPS + e % (16 * I)] = rr[u];
-        }
-        __syncthreads();
     }
-    // bf16 copies: T, and X_w = beta e^{G} . K^
-    for (int e = tid; e < kChunk * 32; e += kThreads) {
-        const int i = e >> 5, j = (e & 31) * 2;
-        *reinterpret_cast<uint32_t *>(sm.u.b.tb + i * kL6 + j) = pack_bf16(sT[i * kPS + j], sT[i * kPS + j + 1]);
-    }
+    // X_w = beta e^{G} . K^
     for (int e = tid; e < kChunk * (kKP / 8); e += kThreads) {
         const int i = e >> 4, d = (e & 15) * 8;
         const float f = sm.beta[i] * __expf(sm.G[i]);
