@@ -428,3 +428,43 @@ def test_full_size_backward():
         errs = {n: rel_err(got[n][sel], ref[n]) for n in ("dq", "dk", "dv", "dbeta", "dg")}
         errs["dh0"] = rel_err(got["dh0"][b:b + 1, h:h + 1], ref["dh0"])
         assert all(e <= 1.5e-2 for e in errs.values()), (b, h, errs)
+
+
+# ------------------------------------------------ edge cases of the newer calls ---
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bidirectional_varlen_concurrent(dtype):
+    """both directions at once over packed sequences (one empty, one short)"""
+    lens = [70, 0, 1, 130, 64]
+    w = workloads.make(1, sum(lens), 2, 64, 64, dtype, seed=23, lengths=lens, name="bidir_varlen")
+    _compare(dataclasses.replace(w, bidirectional=True), ["out", "den"])
+
+
+def test_bidirectional_gk_concurrent():
+    """per-key gates through the concurrent bidirectional call"""
+    w = workloads.make(1, 150, 2, 64, 64, seed=24, g_mu=None, gk_mu=4.0, name="bidir_gk")
+    _compare(dataclasses.replace(w, bidirectional=True), ["out", "den"])
+
+
+def test_zero_tokens_segmented_and_backward():
+    """T = 0: the segment call passes h0 through; the backward returns
+    dh0 = dh_final"""
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(2, 0, 2, 64, 64, seed=25, h0_std=0.5)
+    hf = torch.full((2, 2, 64, 64), float("nan"), device="cuda")
+    gdn.gdn_chunk_fwd_seg(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), 128, g=f32_dev(w.g),
+                          h0=f32_dev(w.h0), h_final=hf)
+    dhf = f32_dev(w.h0)
+    res = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(w.v), h0=f32_dev(w.h0), dh_final=dhf)
+    torch.cuda.synchronize()
+    assert np.array_equal(hf.cpu().numpy(), w.h0)
+    assert np.array_equal(res["dh0"].cpu().numpy(), w.h0)
+
+
+def test_segment_shorter_than_sequence_end():
+    """segment length not dividing the chunk count, and one chunk shorter
+    than 64 tokens at the end"""
+    w = workloads.make(2, 64 * 5 + 3, 2, 64, 64, seed=26, h0_std=0.5, segment_len=128)
+    _compare(w)
