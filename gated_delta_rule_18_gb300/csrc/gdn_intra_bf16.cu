@@ -129,8 +129,12 @@ __device__ __forceinline__ bool wait_copies(uint32_t bar, int *err) {
 }
 
 template <bool PERKEY>
-__global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const FwdParams p, int VP) {
+__global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 : 4)
+    intra_kernel(const FwdParams p, int VP) {
     using L = Lay<PERKEY>;
+    // the per-key kernel runs 8 warps: warps 0-3 own the 16-row blocks of the
+    // products, all 8 share the elementwise passes and the solve's slices
+    constexpr int NT = PERKEY ? 2 * kThreads : kThreads;
     constexpr int KP = kKP;
     constexpr int KS = L::KS;
     constexpr int VPR = KP / 8;  // 16-byte vectors per q/k row
@@ -346,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
             }
         }
     } else {
-        {  // row norms as scalars (the tiles stay raw)
+        if (tid < 2 * kChunk) {  // row norms as scalars (the tiles stay raw)
             const int r = tid & 63;
             const bf16 *row = (tid < 64 ? sQ : sK) + r * KS;
             float ss = 0.f;
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
             }
             (tid < 64 ? sRq : sRk)[r] = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
         }
-        {  // per-channel cumsums: thread d keeps its channel's 64 gates in registers
+        if (tid < KP) {  // per-channel cumsums: thread d keeps its channel's 64 gates in registers
             static_assert(kThreads == KP, "one thread per key channel");
             const int d = tid;
             float a[kChunk];
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
         bf16 *sR = sV;                // right factors, all 64 rows
         bf16 *sL = sR + kChunk * KS;  // left factors of keys, then of queries
         __syncthreads();
-        for (int e = tid; e < kChunk * (KP / 8); e += kThreads) {
+        for (int e = tid; e < kChunk * (KP / 8); e += NT) {
             const int i = e / (KP / 8), d = (e % (KP / 8)) * 8, r = (i & ~15) + 8;
             float gi[8], gr[8], kx[8], o[8];
             ld8f(sG + i * KP + d, gi);
@@ -399,18 +403,19 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
 #pragma unroll
                 for (int e = 0; e < 4; ++e) ak[n][e] = ap[n][e] = 0.f;
             // this thread's items: (64 - r0) rows x 16 eight-channel groups
-            // over the block, at most 8 each; the factors e^{G_i - G_r} of
-            // the key pass stay in registers for the query pass
+            // over the block, at most kItems each; the factors e^{G_i - G_r}
+            // of the key pass stay in registers for the query pass
+            constexpr int kItems = kChunk * (KP / 8) / NT;
             const int n_items = (kChunk - r0) * (KP / 8);
-            float fct[8][8];
+            float fct[kItems][8];
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {  // 0: keys (A), 1: queries (P)
                 __syncthreads();  // the previous product has read sL
                 const bf16 *src = pass ? sQ : sK;
                 const float *rs = pass ? sRq : sRk;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int e = tid + u * kThreads;
+                for (int u = 0; u < kItems; ++u) {
+                    const int e = tid + u * NT;
                     if (e >= n_items) break;
                     const int i = r0 + e / (KP / 8), d = (e % (KP / 8)) * 8;
                     if (pass == 0) {
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
                     *reinterpret_cast<uint4 *>(sL + i * KS + d) = pack8(o);
                 }
                 __syncthreads();
-                if (warp >= J) {
+                if (warp < 4 && warp >= J) {
 #pragma unroll
                     for (int kk = 0; kk < KP / 16; ++kk) {
                         uint32_t aL[4], b[4];
@@ -441,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
                     }
                 }
             }
-            if (warp >= J) {
+            if (warp < 4 && warp >= J) {
 #pragma unroll
                 for (int n = 0; n < 2; ++n) {
 #pragma unroll
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
                         put_p(i, j, pv[0], pv[1]);
                     }
                 }
-            } else {  // column block right of this warp's diagonal: zeros
+            } else if (warp < 4) {  // column block right of this warp's diagonal: zeros
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -473,13 +478,13 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
     unsigned char *gQg = p.qg_img + gch * kImgW;
     unsigned char *gKg = p.kg_img + gch * kImgW;
     constexpr int kQgBatch = 4;  // items loaded before any is stored
-    static_assert((kChunk * VPR) % (kQgBatch * kThreads) == 0, "qg batches");
-    for (int e0 = tid; e0 < kChunk * VPR; e0 += kQgBatch * kThreads) {
+    static_assert((kChunk * VPR) % (kQgBatch * NT) == 0, "qg batches");
+    for (int e0 = tid; e0 < kChunk * VPR; e0 += kQgBatch * NT) {
         uint4 xq[kQgBatch], xk[kQgBatch];
         float sq[kQgBatch], sk[kQgBatch], gi[kQgBatch];
 #pragma unroll
         for (int u = 0; u < kQgBatch; ++u) {
-            const int e = e0 + u * kThreads, i = e / VPR, d0 = (e % VPR) * 8;
+            const int e = e0 + u * NT, i = e / VPR, d0 = (e % VPR) * 8;
             xq[u] = *reinterpret_cast<const uint4 *>(sQ + i * KS + d0);
             xk[u] = *reinterpret_cast<const uint4 *>(sK + i * KS + d0);
             sq[u] = sRq[i];
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
         const float glast = PERKEY ? 0.f : sG[last];
 #pragma unroll
         for (int u = 0; u < kQgBatch; ++u) {
-            const int e = e0 + u * kThreads, i = e / VPR, d0 = (e % VPR) * 8;
+            const int e = e0 + u * NT, i = e / VPR, d0 = (e % VPR) * 8;
             float fq[8], fk[8];
             unpack8(xq[u], fq);
             unpack8(xk[u], fk);
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
             *reinterpret_cast<uint4 *>(gKg + img_kt_off(i, d0)) = pack8(fk);
         }
     }
-    for (int d = tid; d < KP; d += kThreads)
+    for (int d = tid; d < KP; d += NT)
         p.dec[gch * KP + d] = PERKEY ? ex2(sG[last * KP + d]) : __expf(sG[last]);
     fence_async_smem();  // these generic accesses come before the copies that reuse the space
     __syncthreads();     // the q tile (scalar gate) and the split operands (per key) are free
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
 
     //         T_II = (I + A_II)^{-1} for the diagonal block of this warp;
     //         lane c < 16 holds column c: t = e_c, t_r = -sum_{j<r} A_rj t_j
-    {
+    if (warp < 4) {
         const int I = warp, cc = lane & 15;
         const float *Ad = sAd + I * 16 * kAdS;
         float t[16];
@@ -595,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, PERKEY ? 2 : 4) intra_kernel(const F
     unsigned char *gU = p.u_img + gch * p.n_vt * kImgU;
     const int nsw = KP / 64, nsu = VP / 64;
     bool v_ready = false;
-    for (int sl = warp; sl < nsw + nsu; sl += kThreads / 32) {
+    for (int sl = warp; sl < nsw + nsu; sl += NT / 32) {
         const bool isw = sl < nsw;
         if (!isw && !v_ready) {
             if (!wait_copies(b_v, p.err)) return;
@@ -671,7 +676,7 @@ cudaError_t launch_t(const FwdParams &p, cudaStream_t st) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)p.max_chunks * (unsigned)p.H);
-    kern<<<grid, kThreads, bytes, st>>>(p, VP);
+    kern<<<grid, PERKEY ? 2 * kThreads : kThreads, bytes, st>>>(p, VP);
     return cudaGetLastError();
 }
 
