@@ -1,8 +1,9 @@
 // gdn_state_tc.cu -- chunk-serial state passing and output of the bf16 path
 // on the fifth-generation tensor cores (tcgen05, accumulators in TMEM).
 //
-// One CTA per (sequence, head, 64-column value tile), walking the sequence's
-// 64-token chunks in order, warp-specialised (9 warps):
+// One CTA per (sequence, head, 64-column value tile), the tiles of a head
+// adjacent in the grid, walking the sequence's 64-token chunks in order,
+// warp-specialised (9 warps):
 //
 //   warps 0-3  the recurrence. Thread r keeps row r of the fp32 state h
 //              (128 keys x 64 columns) in registers; per chunk it writes h as
@@ -95,8 +96,13 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int H = p.H, K = p.K, V = p.V;
-    const int s = blockIdx.x / H, hh = blockIdx.x % H;
-    const int vt = blockIdx.y, v0 = vt * kBVt;
+    // the column tiles of one (sequence, head) are adjacent in launch order,
+    // so they run together and all but the first read the head's operand
+    // images from L2 rather than HBM
+    const int n_tiles = p.n_vt + (p.summary ? p.n_kt : 0);
+    const int bhx = blockIdx.x / n_tiles;
+    const int s = bhx / H, hh = bhx % H;
+    const int vt = blockIdx.x % n_tiles, v0 = vt * kBVt;
     const int seg = blockIdx.z;
     // a transition tile of a summary pass: columns t0 .. t0+63 of M
     const bool trt = p.summary && vt >= p.n_vt;
@@ -466,7 +472,7 @@ cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st) {
     // summary 2: every segment but the last (whose summary nothing reads)
     const int nseg = p.seg_chunks ? max(1, (nall + p.seg_chunks - 1) / p.seg_chunks) - (p.summary == 2 ? 1 : 0) : 1;
     if (nseg < 1) return cudaSuccess;
-    dim3 grid(p.n_seq * p.H, p.n_vt + (p.summary ? p.n_kt : 0), nseg);
+    dim3 grid(p.n_seq * p.H * (p.n_vt + (p.summary ? p.n_kt : 0)), 1, nseg);
     state_tc_kernel<<<grid, kThreads, Lay::bytes, st>>>(p);
     return cudaGetLastError();
 }
