@@ -169,12 +169,11 @@ __device__ __forceinline__ void gates(const BwdParams &p, const ChunkCtx &x, flo
 // ------------------------------------------------------------------ dq ---
 struct DqSmem {
     bf16 q[kChunk * kLK], k[kChunk * kLK], dout[kChunk * kLK], vn[kChunk * kLK];
-    bf16 h[kKP * kLK];
-    bf16 mp[kChunk * kL6];
+    bf16 h[kKP * kLK];  // (M_P takes the v_new tile's space once dP is formed)
     float G[kChunk], graw[kChunk], rq[kChunk], rk[kChunk], dG[kChunk], row[kChunk];
 };
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) {
     extern __shared__ __align__(16) unsigned char smraw[];
     DqSmem &sm = *reinterpret_cast<DqSmem *>(smraw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -223,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
         cp_async_wait<0>();
         __syncthreads();
         warp_gemm(dp, Tile{sm.dout, kLK}, false, Tile{sm.vn, kLK}, false, m0, n0, kv, lane);
+        __syncthreads();  // v_new is read out everywhere: M_P takes its space
         float ct[4][4];  // dP_ij P_ij: d/dG_i of P_ij is P_ij, d/dG_j is -P_ij
 #pragma unroll
         for (int n = 0; n < 4; ++n)
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
                     mpv[e] = dP * gam;
                     ct[n][2 * hf + e] = dP * P;
                 }
-                *reinterpret_cast<uint32_t *>(sm.mp + i * kL6 + n0 + 8 * n + 2 * t4) = pack_bf16(mpv[0], mpv[1]);
+                *reinterpret_cast<uint32_t *>(sm.vn + i * kL6 + n0 + 8 * n + 2 * t4) = pack_bf16(mpv[0], mpv[1]);
             }
         rowcol_add(ct, m0, n0, sm.dG, sm.dG, -1.f);
     }
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
             v += __shfl_xor_sync(0xffffffffu, v, 2);
             if (t4 == 0 && m0 + g8 + 8 * hf < x.Lc) atomicAdd(&sm.dG[m0 + g8 + 8 * hf], v);
         }
-        warp_gemm(dq, Tile{sm.mp, kL6}, false, Tile{sm.k, kLK}, true, m0, nk0, kChunk, lane);
+        warp_gemm(dq, Tile{sm.vn, kL6}, false, Tile{sm.k, kLK}, true, m0, nk0, kChunk, lane);
     }
     // through the normalisation: dq = (dq^ - q^ (q^ . dq^)) / |q|
     {
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const BwdParams p) 
     {
         float pk[8][4];
         acc_zero(pk);
-        warp_gemm(pk, Tile{sm.mp, kL6}, true, Tile{sm.q, kLK}, true, m0, nk0, kChunk, lane);
+        warp_gemm(pk, Tile{sm.vn, kL6}, true, Tile{sm.q, kLK}, true, m0, nk0, kChunk, lane);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int j = m0 + g8 + 8 * hf;
@@ -795,6 +795,9 @@ cudaError_t launch_grid(Kern kern, int bytes, const BwdParams &p, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_bwd_dq(const BwdParams &p, cudaStream_t st) {
+    // two CTAs per SM: ask for the whole shared-memory carveout
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     return launch_grid(bwd_dq_kernel, (int)sizeof(DqSmem), p, st);
 }
 cudaError_t launch_bwd_dk(const BwdParams &p, cudaStream_t st) {
