@@ -157,15 +157,18 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
         }
         __syncthreads();
         // ---- optional L2 normalisation of q and k rows; gate cumsums
-        if (p.l2norm) {
-            for (int i = warp; i < 2 * kChunk; i += kThreadsF / 32) {
-                float *row = (i < kChunk) ? (sQ + i * QS) : (sK + (i - kChunk) * QS);
-                float ss = 0.f;
-                for (int d = lane; d < KP; d += 32) ss += row[d] * row[d];
-                ss = warp_sum(ss);
-                const float inv = rsqrtf(ss + 1e-6f);
-                for (int d = lane; d < KP; d += 32) row[d] *= inv;
+        if (p.l2norm) {  // two threads per row (128 rows: q then k), then the scaling
+            const int row = tid >> 1, half = tid & 1;
+            float *rp = (row < kChunk) ? (sQ + row * QS) : (sK + (row - kChunk) * QS);
+            float s0 = 0.f, s1 = 0.f;
+            for (int d = half; d < KP; d += 4) {
+                s0 = fmaf(rp[d], rp[d], s0);
+                if (d + 2 < KP) s1 = fmaf(rp[d + 2], rp[d + 2], s1);
             }
+            float ss = s0 + s1;
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            const float inv = rsqrtf(ss + 1e-6f);
+            for (int d = half; d < KP; d += 2) rp[d] *= inv;
         }
         if (PERKEY) {
             for (int d = tid; d < KP; d += kThreadsF) {
@@ -175,15 +178,61 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
                     sGk[i * QS + d] = acc;
                 }
             }
-        } else if (tid == 0) {
-            float acc = 0.f;
-            for (int i = 0; i < kChunk; ++i) {
-                acc += sG[i];
-                sG[i] = acc;
+        } else if (warp == 0) {  // scan over the chunk, two gates per lane
+            const float a0 = sG[2 * lane], a1 = sG[2 * lane + 1];
+            float incl = a0 + a1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
             }
+            sG[2 * lane] = incl - a1;
+            sG[2 * lane + 1] = incl;
         }
         __syncthreads();
-        // ---- A (strict lower, beta-scaled) and P (lower incl. diagonal)
+        // ---- A (strict lower, beta-scaled) and P (lower incl. diagonal);
+        // scalar gate: a 4 x 4 block of (i, j) per thread
+        if constexpr (!PERKEY) {
+            const int bi = tid >> 4, bj = tid & 15;
+            float sa[4][4], sp[4][4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) sa[x][y] = sp[x][y] = 0.f;
+            if (bj <= bi) {
+#pragma unroll 4
+                for (int d = 0; d < KP; ++d) {
+                    float ki[4], qi[4], kj[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        ki[x] = sK[(4 * bi + x) * QS + d];
+                        qi[x] = sQ[(4 * bi + x) * QS + d];
+                        kj[x] = sK[(4 * bj + x) * QS + d];
+                    }
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) {
+                            sa[x][y] = fmaf(ki[x], kj[y], sa[x][y]);
+                            sp[x][y] = fmaf(qi[x], kj[y], sp[x][y]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) {
+                    const int i = 4 * bi + x, j = 4 * bj + y;
+                    float a = 0.f, pm = 0.f;
+                    if (j <= i) {
+                        const float gam = __expf(sG[i] - sG[j]);
+                        pm = sp[x][y] * gam;
+                        if (j < i) a = sB[i] * (sa[x][y] * gam);
+                    }
+                    sA[i * AS + j] = a;
+                    sP[i * AS + j] = pm;
+                }
+        } else
         for (int e = tid; e < kChunk * kChunk; e += kThreadsF) {
             const int i = e / kChunk, j = e % kChunk;
             float a = 0.f, pm = 0.f;
@@ -227,7 +276,36 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
 #pragma unroll
             for (int r = 0; r < 16; ++r) sT[(o + r) * AS + o + lane] = t[r];
         }
-        // ---- Y = beta (V - (e^G . K) h) into sX
+        // ---- Y = beta (V - (e^G . K) h) into sX; scalar gate: 2 rows x 4
+        // columns per thread (rows ig, ig + 32; columns 4 nq .. 4 nq + 3)
+        const int nq = tid & 7, ig = tid >> 3;
+        if constexpr (!PERKEY) {
+            float acc[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < KP; ++d) {
+                float hv[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) hv[c4] = sH[d * VS + 4 * nq + c4];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float kv = sK[(ig + 32 * r) * QS + d];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(kv, hv[c4], acc[r][c4]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = ig + 32 * r;
+                const float eg = __expf(sG[i]);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+                    sX[i * VS + 4 * nq + c4] = sB[i] * (sV[i * VS + 4 * nq + c4] - acc[r][c4] * eg);
+            }
+        } else
         for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
             const int i = e / kBVf, n = e % kBVf;
             float acc = 0.f;
@@ -248,22 +326,82 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
             if (I > 0) {
                 for (int e = tid; e < 16 * kBVf; e += kThreadsF) {
                     const int i = o + e / kBVf, n = e % kBVf;
-                    float acc = sX[i * VS + n];
-                    for (int j = 0; j < o; ++j) acc = fmaf(-sA[i * AS + j], sV[j * VS + n], acc);
-                    sX[i * VS + n] = acc;
+                    float a4[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums
+                    for (int j = 0; j < o; j += 4) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) a4[u] = fmaf(sA[i * AS + j + u], sV[(j + u) * VS + n], a4[u]);
+                    }
+                    sX[i * VS + n] -= (a4[0] + a4[1]) + (a4[2] + a4[3]);
                 }
                 __syncthreads();
             }
             for (int e = tid; e < 16 * kBVf; e += kThreadsF) {
                 const int i = o + e / kBVf, n = e % kBVf;
-                float acc = 0.f;
+                float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc = fmaf(sT[i * AS + o + j], sX[(o + j) * VS + n], acc);
-                sV[i * VS + n] = acc;
+                for (int j = 0; j < 16; ++j) a4[j & 3] = fmaf(sT[i * AS + o + j], sX[(o + j) * VS + n], a4[j & 3]);
+                sV[i * VS + n] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
             }
             __syncthreads();
         }
-        // ---- o = (e^G . Q) h + P v_new
+        // ---- o = (e^G . Q) h + P v_new; scalar gate: 2 rows x 4 columns per
+        // thread as for Y (P is zero right of the diagonal)
+        if constexpr (!PERKEY) {
+            float acc[2][4], pv[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = pv[r][c4] = 0.f;
+#pragma unroll 4
+            for (int d = 0; d < KP; ++d) {
+                float hv[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) hv[c4] = sH[d * VS + 4 * nq + c4];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float qv = sQ[(ig + 32 * r) * QS + d];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(qv, hv[c4], acc[r][c4]);
+                }
+            }
+#pragma unroll 4
+            for (int j = 0; j < kChunk; ++j) {
+                float vv[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) vv[c4] = sV[j * VS + 4 * nq + c4];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float pj = sP[(ig + 32 * r) * AS + j];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) pv[r][c4] = fmaf(pj, vv[c4], pv[r][c4]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = ig + 32 * r;
+                if (i >= Lc) continue;
+                const float eg = __expf(sG[i]);
+                const int tq = q_token(p.reverse, si.len, pos0 + i);
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int col = v0 + 4 * nq + c4;
+                    const float val = acc[r][c4] * eg + pv[r][c4];
+                    if (col < V) {
+                        const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + col;
+                        if (p.out_f32) {
+                            float *o = (float *)p.out + off;
+                            *o = p.accumulate ? *o + val : val;
+                        } else {
+                            __nv_bfloat16 *o = (__nv_bfloat16 *)p.out + off;
+                            *o = __float2bfloat16_rn(p.accumulate ? __bfloat162float(*o) + val : val);
+                        }
+                    } else if (p.has_den && col == V) {
+                        float *o = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
+                        *o = p.accumulate ? *o + val : val;
+                    }
+                }
+            }
+        } else
         for (int e = tid; e < kChunk * kBVf; e += kThreadsF) {
             const int i = e / kBVf, n = e % kBVf, col = v0 + n;
             if (i >= Lc) continue;
@@ -300,6 +438,34 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
             if (tid < kChunk) sB[tid] = __expf(sG[last] - sG[tid]);
             __syncthreads();
         }
+        if constexpr (!PERKEY) {  // KP / 32 key rows x 4 columns per thread
+            constexpr int RD = KP / 32;
+            const int dg = tid >> 3;
+            const float el = __expf(sG[last]);
+            float acc[RD][4];
+#pragma unroll
+            for (int r = 0; r < RD; ++r)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = el * sH[(dg + 32 * r) * VS + 4 * nq + c4];
+#pragma unroll 4
+            for (int i = 0; i < Lc; ++i) {
+                const float f = sB[i];
+                float vv[4];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) vv[c4] = sV[i * VS + 4 * nq + c4];
+#pragma unroll
+                for (int r = 0; r < RD; ++r) {
+                    const float kf = sK[i * QS + dg + 32 * r] * f;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(kf, vv[c4], acc[r][c4]);
+                }
+            }
+            __syncthreads();  // every thread has read its h block before any is rewritten
+#pragma unroll
+            for (int r = 0; r < RD; ++r)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) sH[(dg + 32 * r) * VS + 4 * nq + c4] = acc[r][c4];
+        } else
         for (int e = tid; e < KP * kBVf; e += kThreadsF) {
             const int d = e / kBVf, n = e % kBVf;
             float acc;
