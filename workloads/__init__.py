@@ -275,6 +275,9 @@ def make_video(B: int, N: int, H: int, D: int, *, seed: int = 0,
 WORKLOADS = {
     "causal_f32_b1h2t256d64": dict(kind="dense", B=1, T=256, H=2, K=64, V=64,
                                    dtype="f32", g_mu=3.0),
+    # 64 independent problems of the 256-token fp32 shape in one launch
+    "causal_f32_b64h2t256d64": dict(kind="dense", B=64, T=256, H=2, K=64, V=64,
+                                    dtype="f32", g_mu=3.0),
     "causal_bf16_b4h16t4096d128": dict(kind="dense", B=4, T=4096, H=16, K=128,
                                        V=128, dtype="bf16", g_mu=3.0),
     "bidir_video_b2h16n8192d112": dict(kind="video", B=2, N=8192, H=16, D=112),
