@@ -97,8 +97,7 @@ struct BwdParams {
 constexpr int kKP = 128;                 // keys per image (zero padded)
 constexpr uint32_t kImgW = 64 * kKP * 2;  // w, qg (64 tokens x 128 keys), kg^T
 constexpr uint32_t kImgP = 64 * 64 * 2;   // P (64 x 64)
-constexpr uint32_t kUS = 72;              // padded row (elements) of a u tile
-constexpr uint32_t kImgU = 64 * kUS * 2;  // one 64-column u tile
+constexpr uint32_t kImgU = 64 * 64 * 2;   // one 64-column u tile
 constexpr uint32_t kDecB = kKP * 4;       // chunk decay vector
 
 // w / qg: K-major A operand, M = token i, K = key d: core (i/8, d/8).
@@ -108,6 +107,11 @@ __host__ __device__ __forceinline__ uint32_t img_w_off(int i, int d) {
 // kg^T: MN-major A operand, M = key d, K = token i: core (d/8, i/8).
 __host__ __device__ __forceinline__ uint32_t img_kt_off(int i, int d) {
     return (uint32_t)((d >> 3) * 1024 + i * 16 + (d & 7) * 2);
+}
+// u (one 64-column tile): MN-major B operand, N = column j, K = token i:
+// core (j/8, i/8), so a warp's stores of 8 rows x 8 columns fill 128 bytes.
+__host__ __device__ __forceinline__ uint32_t img_u_off(int i, int j) {
+    return (uint32_t)((j >> 3) * 1024 + i * 16 + (j & 7) * 2);
 }
 // P: K-major A operand, M = token i, K = token j.
 __host__ __device__ __forceinline__ uint32_t img_p_off(int i, int j) {

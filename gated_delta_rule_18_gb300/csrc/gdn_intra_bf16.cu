@@ -479,12 +479,18 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
     unsigned char *gKg = p.kg_img + gch * kImgW;
     constexpr int kQgBatch = 4;  // items loaded before any is stored
     static_assert((kChunk * VPR) % (kQgBatch * NT) == 0, "qg batches");
+    static_assert(VPR == 16, "item map below assumes 16 eight-key vectors per row");
+    // item e -> (row i, keys d0 .. d0+7): the 32 items of a warp instruction
+    // are 8 consecutive rows x 4 consecutive 8-key blocks, so each warp store
+    // fills whole 128-byte lines of both images (512 contiguous bytes of qg)
+    auto item_row = [](int e) { return (((e >> 5) & 7) << 3) + (e & 7); };
+    auto item_key = [](int e) { return ((((e >> 5) >> 3) << 2) + ((e & 31) >> 3)) * 8; };
     for (int e0 = tid; e0 < kChunk * VPR; e0 += kQgBatch * NT) {
         uint4 xq[kQgBatch], xk[kQgBatch];
         float sq[kQgBatch], sk[kQgBatch], gi[kQgBatch];
 #pragma unroll
         for (int u = 0; u < kQgBatch; ++u) {
-            const int e = e0 + u * NT, i = e / VPR, d0 = (e % VPR) * 8;
+            const int e = e0 + u * NT, i = item_row(e), d0 = item_key(e);
             xq[u] = *reinterpret_cast<const uint4 *>(sQ + i * KS + d0);
             xk[u] = *reinterpret_cast<const uint4 *>(sK + i * KS + d0);
             sq[u] = sRq[i];
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
         const float glast = PERKEY ? 0.f : sG[last];
 #pragma unroll
         for (int u = 0; u < kQgBatch; ++u) {
-            const int e = e0 + u * NT, i = e / VPR, d0 = (e % VPR) * 8;
+            const int e = e0 + u * NT, i = item_row(e), d0 = item_key(e);
             float fq[8], fk[8];
             unpack8(xq[u], fq);
             unpack8(xk[u], fk);
@@ -648,9 +654,9 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
                     *reinterpret_cast<uint32_t *>(gW + img_w_off(i, c0 + cl)) = lo;
                     *reinterpret_cast<uint32_t *>(gW + img_w_off(i + 8, c0 + cl)) = hi;
                 } else {
-                    unsigned char *u = gU + (c0 >> 6) * kImgU + cl * 2;
-                    *reinterpret_cast<uint32_t *>(u + i * (kUS * 2)) = lo;
-                    *reinterpret_cast<uint32_t *>(u + (i + 8) * (kUS * 2)) = hi;
+                    unsigned char *u = gU + (c0 >> 6) * kImgU;
+                    *reinterpret_cast<uint32_t *>(u + img_u_off(i, cl)) = lo;
+                    *reinterpret_cast<uint32_t *>(u + img_u_off(i + 8, cl)) = hi;
                 }
                 if (I < 3) {
                     *reinterpret_cast<uint32_t *>(tile + i * ts + c0 + cl) = lo;

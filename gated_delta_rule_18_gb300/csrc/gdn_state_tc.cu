@@ -185,9 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     // token row i, columns c0 .. c0+31 of chunk c's u, read ahead of the
     // product it is combined with
     auto load_u = [&](int c, int i, int c0, uint4 (&uv)[4]) {
-        const unsigned char *urow = sm + Lay::u + (c % 3) * kImgU + i * (kUS * 2) + c0 * 2;
+        const unsigned char *urow = sm + Lay::u + (c % 3) * kImgU + img_u_off(i, c0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) uv[j] = *reinterpret_cast<const uint4 *>(urow + 16 * j);
+        for (int j = 0; j < 4; ++j) uv[j] = *reinterpret_cast<const uint4 *>(urow + 1024 * j);
     };
     auto vnew_half = [&](int c, int i, int c0, const uint4 (&uvs)[4]) {
         const uint32_t par = c & 1;
