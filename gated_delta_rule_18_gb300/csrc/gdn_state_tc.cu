@@ -254,9 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             }
             fence_async_smem();
             arrive(b_h);
-            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
-            if (!ok) break;
             if (warp < 2) {  // v_new for token row i = tid, columns 0..31
+                // Only the v_new warps wait for the stage: chunk c+2's copies
+                // into the same slot need this chunk's v_new first, so the
+                // barrier cannot run a phase ahead of them; warps 2-3 take
+                // dec after the dh product, which follows the stage.
+                ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
+                if (!ok) break;
                 uint4 uv[4];
                 load_u(c, tid, 0, uv);
                 ok = warp_all(wait_bar(b_a, par, abort));
@@ -267,8 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 arrive(b_vn);
                 if (!ok) break;
             }
-            const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
             ok = warp_all(wait_bar(b_dh, par, abort));
+            if (!ok) break;
+            const float d = reinterpret_cast<const float *>(sm + Lay::dec + (c % 4) * kDecB)[r];
             tc_fence_after();
 #pragma unroll
             for (int half = 0; half < 2; ++half) {

@@ -468,3 +468,31 @@ def test_segment_shorter_than_sequence_end():
     than 64 tokens at the end"""
     w = workloads.make(2, 64 * 5 + 3, 2, 64, 64, seed=26, h0_std=0.5, segment_len=128)
     _compare(w)
+
+
+@pytest.mark.parametrize("name", ["varlen_bf16_64seq_h32d128", "gk_bf16_b1h32t65536k128v256"])
+def test_repeated_long_runs_clean_and_deterministic(name):
+    """Many CTA waves and long sequences, run repeatedly through the C ABI
+    with one workspace: every run leaves the device error word clear (no
+    bounded wait of the tensor-core state pass gave up, which would also have
+    left wrong outputs) and reproduces the first run's outputs bit for bit."""
+    import gated_delta_rule_18_gb300 as gdn
+    t = torch()
+    w = workloads.build(name)
+    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    beta, g, gk = f32_dev(w.beta), f32_dev(w.g), f32_dev(w.gk)
+    h0, cu = f32_dev(w.h0), i32_dev(w.cu_seqlens)
+    n_seq = w.B if w.cu_seqlens is None else len(w.cu_seqlens) - 1
+    need = gdn.gdn_workspace_size(w.B, w.T, w.H, w.K, w.V, n_seq, cu is not None, gdn.BF16, False)
+    ws = t.empty(max(need, 256), dtype=t.uint8, device=dev())
+    hf = t.empty((n_seq, w.H, w.K, w.V), dtype=t.float32, device=dev())
+    first = None
+    for _ in range(12):
+        out = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, gk=gk, h0=h0, cu_seqlens=cu, h_final=hf,
+                                qk_l2norm=w.prep == "l2", workspace=ws)
+        assert gdn.gdn_last_device_error(ws) == 0
+        cur = (out.clone(), hf.clone())
+        if first is None:
+            first = cur
+        else:
+            assert t.equal(cur[0], first[0]) and t.equal(cur[1], first[1])
