@@ -408,7 +408,7 @@ def e2e_measure(gdn, w, d, ws, steps, dev):
 # ------------------------------------------------------------- CPU side ----
 
 ORACLE_S_PER_TOKEN_HEAD_KV = 7e-9   # rough fp64 oracle cost per token-head per K*V
-CPU_TARGET_CORE_SECONDS = 20.0
+CPU_TARGET_CORE_SECONDS = 40.0
 
 
 def oracle_sample(w):
