@@ -405,6 +405,42 @@ def e2e_measure(gdn, w, d, ws, steps, dev):
     return sec, h2d, d2h
 
 
+PROFILE_EVERY = 4
+
+
+def graph_replay(gdn, w, d, ws, n, fl, by, peaks, reps=20):
+    """N back-to-back calls of the step captured in one CUDA graph and
+    replayed: the per-call time with the launch cost amortised (the CPU
+    enqueues nothing per call). The library's per-launch event pairs are off
+    here (they are on only in the timed region above)."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            run_step(gdn, w, d, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            run_step(gdn, w, d, ws)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    per_call = a.elapsed_time(b) / 1e3 / (reps * n)
+    roof = max(by / (peaks["hbm_gbs"] * 1e9), fl / (peaks["bf16_tflops"] * 1e12))
+    return {"calls_per_graph": n, "replays": reps, "us_per_call": per_call * 1e6,
+            "l2": "warm: no flush between the calls of a replay",
+            "tokens_per_s": w.B * w.T / per_call if w.cu_seqlens is None else int(w.cu_seqlens[-1]) / per_call,
+            "path_roofline_frac": roof / per_call}
+
+
 # ------------------------------------------------------------- CPU side ----
 
 ORACLE_S_PER_TOKEN_HEAD_KV = 7e-9   # rough fp64 oracle cost per token-head per K*V
@@ -483,6 +519,8 @@ def main():
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="bwd: time the gradients (gdn_chunk_bwd, forward recompute included) "
                          "of a dense causal workload instead of the forward")
+    ap.add_argument("--graph-replay", type=int, default=0,
+                    help="also time N back-to-back calls captured in one CUDA graph (forward pass)")
     ap.add_argument("--segment-len", type=int, default=None,
                     help="segment-parallel state passing with this many tokens per segment "
                          "(0: one pass per sequence); default: the workload's own setting")
@@ -530,10 +568,6 @@ def main():
         run_step = globals()["run_step"]
     stream = torch.cuda.current_stream()
 
-    for _ in range(warmup):
-        run_step(gdn, w, d, ws)
-    torch.cuda.synchronize()
-    gdn.profile_collect()
     # L2 hygiene: a workload whose inputs exceed L2 needs no flush between
     # steps; smaller ones get an L2-sized write before every timed step
     in_bytes = sum(t.numel() * t.element_size() for t in d.values() if torch.is_tensor(t))
@@ -545,16 +579,25 @@ def main():
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     sampler.start()
     time.sleep(0.3)
+    # the warm-up steps run right before the timed ones (no idle gap between)
+    for _ in range(warmup):
+        run_step(gdn, w, d, ws)
+    torch.cuda.synchronize()
+    gdn.profile_collect()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = gdn.launch_count()
-    gdn.profile_enable(True)
+    # the library's per-launch event pairs (the per-kernel times) are taken on
+    # every PROFILE_EVERY-th timed step: an event pair waits for the kernel
+    # before it to drain, which costs ~2 us per kernel boundary
+    prof = lambda i: gdn.profile_enable(i % PROFILE_EVERY == 0)
     if not flush:
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            prof(i)
             run_step(gdn, w, d, ws)
         b.record(stream)
         torch.cuda.synchronize()
@@ -564,9 +607,10 @@ def main():
         # step, outside that step's own events
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
-        for ea, eb in evs:
+        for i, (ea, eb) in enumerate(evs):
             scrub.zero_()
             ea.record(stream)
+            prof(i)
             run_step(gdn, w, d, ws)
             eb.record(stream)
         torch.cuda.synchronize()
@@ -620,6 +664,7 @@ def main():
                           "roofline_ms": roof_t * 1e3, "frac": roof_t / step_s,
                           "peak_source": peak_src},
         "roofline": roofline,
+        "kernels_sampled": f"per-launch CUDA event pairs on every {PROFILE_EVERY}th timed step",
         "kernels": {k2: {"avg_us": v2[0] / v2[1] * 1e3, "launches": v2[1],
                          "share": v2[0] / max(1e-9, sum(x[0] for x in per_kernel.values()))}
                     for k2, v2 in per_kernel.items()},
@@ -627,6 +672,8 @@ def main():
         "clocks": clocks,
         "impl": "ours",
     }
+    if args.graph_replay > 0 and args.pass_ == "fwd":
+        result["graph_replay"] = graph_replay(gdn, w, d, ws, args.graph_replay, fl, by, peaks)
     if not args.no_e2e:
         e2e_s, h2d, d2h = e2e_measure(gdn, w, d, ws, max(3, min(args.steps, 10)), dev)
         e2e_s = max_over_ranks(e2e_s, dist, dev)

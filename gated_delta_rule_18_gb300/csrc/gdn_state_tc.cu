@@ -322,41 +322,42 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         // ------------------------------------------------------ the MMA issuer
         bool ok = true;
         int c = 0;
+        // operand descriptors of both stages / buffers, built once: a K step
+        // of 16 advances the start address by 256 bytes, i.e. the descriptor
+        // by 16 (the 14-bit address field cannot carry: shared addresses stay
+        // below 256 KB)
+        const uint64_t dW0 = tc_sdesc(sbase + Lay::w, 128, 2048), dW1 = tc_sdesc(sbase + Lay::stage + Lay::w, 128, 2048);
+        const uint64_t dK0 = tc_sdesc(sbase + Lay::kg, 128, 1024), dK1 = tc_sdesc(sbase + Lay::stage + Lay::kg, 128, 1024);
+        const uint64_t dZ0 = tc_sdesc(sbase + Lay::z, 128, 1024), dZ1 = tc_sdesc(sbase + Lay::stage + Lay::z, 128, 1024);
+        const uint64_t dV0 = tc_sdesc(sbase + Lay::vn, 128, 1024), dV1 = tc_sdesc(sbase + Lay::vn + Lay::vn_bytes, 128, 1024);
+        const uint64_t dH = tc_sdesc(sbase + Lay::h, 128, 2048);
         for (; c < nchunks && ok; ++c) {
             const int st = c & 1;
             const uint32_t par = c & 1;
-            const uint32_t stg = sbase + st * Lay::stage;
             const uint32_t dcol = kColD + par * 64;
+            const uint64_t dW = st ? dW1 : dW0, dK = st ? dK1 : dK0, dZ = st ? dZ1 : dZ0, dV = par ? dV1 : dV0;
             // [Xw; O] = [w; qg] h once h_c is written and chunk c's operands
             // landed (this accumulator set's previous user, chunk c-2, was read
             // out before P v_new of chunk c-1 was issued, below)
             ok = wait_bar(b_st[st], (c >> 1) & 1, abort) && wait_bar(b_h, par, abort);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t hb = sbase + Lay::h;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc_mma(tmem + dcol, tc_sdesc(stg + Lay::w + ks * 256, 128, 2048), tc_sdesc(hb + ks * 256, 128, 2048),
-                       kIdescK, ks > 0);
+            for (int ks = 0; ks < 8; ++ks) tc_mma(tmem + dcol, dW + 16 * ks, dH + 16 * ks, kIdescK, ks > 0);
             tc_commit(b_a);
             // dh = kg^T v_new, then [.; O] += [0; P] v_new
             ok = wait_bar(b_vn, par, abort);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t vb = sbase + Lay::vn + par * Lay::vn_bytes;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc_mma(tmem + kColDh, tc_sdesc(stg + Lay::kg + ks * 256, 128, 1024), tc_sdesc(vb + ks * 256, 128, 1024),
-                       kIdescMN, ks > 0);
+            for (int ks = 0; ks < 4; ++ks) tc_mma(tmem + kColDh, dK + 16 * ks, dV + 16 * ks, kIdescMN, ks > 0);
             tc_commit(b_dh);
             // b_o must not run two phases ahead of the output warps: chunk
             // c-1's output has to be read out before chunk c's is committed
             if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
             if (!ok) break;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc_mma(tmem + dcol, tc_sdesc(stg + Lay::z + ks * 256, 128, 1024), tc_sdesc(vb + ks * 256, 128, 1024),
-                       kIdescK, 1);
+            for (int ks = 0; ks < 4; ++ks) tc_mma(tmem + dcol, dZ + 16 * ks, dV + 16 * ks, kIdescK, 1);
             tc_commit(b_o);
         }
         if (!ok) {
