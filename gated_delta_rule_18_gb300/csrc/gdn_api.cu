@@ -559,7 +559,7 @@ namespace {
 // of a concurrent bidirectional scan. Created on first use, never destroyed.
 struct SideStream {
     cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr, mid_main = nullptr, mid_side = nullptr;
 };
 std::mutex &side_mutex() {
     static std::mutex *m = new std::mutex();
@@ -576,6 +576,8 @@ cudaError_t side_stream(SideStream *&out) {
         if ((e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
         if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.mid_main, cudaEventDisableTiming)) != cudaSuccess) return e;
+        if ((e = cudaEventCreateWithFlags(&x.mid_side, cudaEventDisableTiming)) != cudaSuccess) return e;
     }
     out = &x;
     return cudaSuccess;
@@ -647,21 +649,37 @@ gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd
     std::lock_guard<std::mutex> lock(side_mutex());
     SideStream *side = nullptr;
     if (side_stream(side) != cudaSuccess) return GDN_ERR_CUDA;
-    auto run = [&](gdn::FwdParams &p, cudaStream_t s) -> cudaError_t {
+    // everything of a direction up to its state pass
+    auto first = [&](gdn::FwdParams &p, cudaStream_t s) -> cudaError_t {
         cudaError_t e = cudaSuccess;
         if (varlen) e = launch(KTable, s, [&] { return gdn::launch_chunk_table(p, s); });
         if (e != cudaSuccess) return e;
         if (qkd.dtype == GDN_F32)
             return launch(KFusedF32, s, [&] { return gdn::launch_fused_f32(p, L.KP, perkey, s); });
         if (L.max_chunks > 0) e = launch(KIntra, s, [&] { return gdn::launch_intra_bf16(p, perkey, s); });
-        if (e != cudaSuccess) return e;
+        return e;
+    };
+    auto second = [&](gdn::FwdParams &p, cudaStream_t s) -> cudaError_t {
+        if (qkd.dtype == GDN_F32) return cudaSuccess;
         return launch(KState, s, [&] { return gdn::launch_state_tc(p, s); });
     };
-    // fork: the reverse direction on the side stream, the forward on the caller's
+    // fork: the reverse direction on the side stream, the forward on the
+    // caller's. Each state pass waits for both directions' intra passes, so
+    // the two intra passes share the whole GPU and the two state passes (one
+    // CTA per SM each) then start together, instead of one direction's state
+    // CTAs taking SMs from the other's intra pass.
     cudaError_t e = cudaEventRecord(side->fork, stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
-    if (e == cudaSuccess) e = run(pr, side->s);
-    if (e == cudaSuccess) e = run(pf, stream);
+    if (e == cudaSuccess) e = first(pr, side->s);
+    if (e == cudaSuccess) e = first(pf, stream);
+    if (e == cudaSuccess && qkd.dtype != GDN_F32) {
+        e = cudaEventRecord(side->mid_side, side->s);
+        if (e == cudaSuccess) e = cudaEventRecord(side->mid_main, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->mid_side, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->mid_main, 0);
+    }
+    if (e == cudaSuccess) e = second(pr, side->s);
+    if (e == cudaSuccess) e = second(pf, stream);
     // join, then out += the reverse half, den += its denominator
     if (e == cudaSuccess) e = cudaEventRecord(side->join, side->s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, side->join, 0);
