@@ -20,7 +20,7 @@ from .build import LIB
 __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
            "gdn_merge", "gdn_frame_fwd", "gdn_frame_workspace_size", "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_forward", "lib",
-           "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect",
+           "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect", "gdn_set_state_tile",
            "launch_count", "kernel_names"]
 
 F32, BF16 = 0, 1
@@ -105,6 +105,8 @@ def lib():
     L.gdn_kernel_name.argtypes = [I]
     L.gdn_profile_enable.restype = None
     L.gdn_profile_enable.argtypes = [I]
+    L.gdn_set_state_tile.restype = None
+    L.gdn_set_state_tile.argtypes = [I]
     L.gdn_profile_collect.restype = I
     L.gdn_profile_collect.argtypes = [ctypes.POINTER(F), ctypes.POINTER(I), I]
     L.gdn_launch_count.restype = ctypes.c_longlong
@@ -538,6 +540,12 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
 def kernel_names() -> list[str]:
     L = lib()
     return [L.gdn_kernel_name(i).decode() for i in range(L.gdn_kernel_kinds())]
+
+
+def gdn_set_state_tile(bv: int = 0) -> None:
+    """Value columns per state-pass CTA: 0 by the grid, 64 or 128 forced
+    (see include/gdn.h)."""
+    lib().gdn_set_state_tile(int(bv))
 
 
 def profile_enable(on: bool = True) -> None:

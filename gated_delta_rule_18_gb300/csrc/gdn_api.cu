@@ -814,6 +814,8 @@ const char *gdn_kernel_name(int kind) {
     return (kind >= 0 && kind < KNumKinds) ? kKindNames[kind] : "unknown";
 }
 
+void gdn_set_state_tile(int bv) { gdn::set_state_tile(bv); }
+
 void gdn_profile_enable(int on) {
     Profiler &P = prof();
     std::lock_guard<std::mutex> g(P.mu);

@@ -335,6 +335,8 @@ cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
 cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
+// value columns per state-kernel CTA: 0 chooses by the grid, 64 or 128 force one
+void set_state_tile(int bv);
 
 // The serial step of segment-parallel state passing: per (sequence x head),
 // h_in[0] = h0 (or 0) and h_in[s+1] = M_s h_in[s] + E_s, fp32.

@@ -43,6 +43,8 @@
 // makes every role leave its loop, the kernel records GDN_DEVERR_TIMEOUT in
 // the workspace error word, drains what it issued (again bounded), frees its
 // tensor memory and returns.
+#include <atomic>
+
 #include "gdn_tc.cuh"
 
 namespace gdn {
@@ -50,9 +52,31 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kThreads = 288;  // 9 warps, see the role map above
-constexpr int kBVt = 64;  // value columns per CTA
+// BV value columns per CTA: 64 (the default), or 128 for grids with more
+// (sequence, head, 64-column tile) units than SMs, where one CTA carrying
+// both 64-column tiles of a head (N = 128 products, the head's w / qg / kg /
+// P staged once) does the two tiles' chains in about the time of one.
+template <int BV>
+struct Cfg;
+template <>
+struct Cfg<64> {
+    static constexpr int kThreads = 288;  // 9 warps
+    static constexpr int kURing = 3, kVnBuf = 2;
+    static constexpr uint32_t kTmemCols = 256;
+};
+template <>
+struct Cfg<128> {
+    static constexpr int kThreads = 384;  // 12 warps
+    // a ring of two u slots and one v_new buffer fit the 128-column tiles in
+    // shared memory: chunk c+2's u copy follows chunk c's output product,
+    // after chunk c's v_new (the slot's last reader); chunk c+1's v_new is
+    // written after its first product, whose commit covers chunk c's products
+    // that read the v_new buffer (one issuing thread, products in order)
+    static constexpr int kURing = 2, kVnBuf = 1;
+    static constexpr uint32_t kTmemCols = 512;
+};
 
+template <int BV>
 struct Lay {
     // one stage of MMA operands: w | qg | kg^T | zero block | P
     static constexpr uint32_t w = 0;
@@ -61,22 +85,19 @@ struct Lay {
     static constexpr uint32_t z = kg + kImgW;  // 64 zero rows stacked over P
     static constexpr uint32_t pm = z + kImgP;
     static constexpr uint32_t stage = pm + kImgP;
-    static constexpr uint32_t u = 2 * stage;               // ring of 3 u tiles
-    static constexpr uint32_t dec = u + 3 * kImgU;         // ring of 4 decay vectors
-    static constexpr uint32_t h = dec + 4 * kDecB;          // h as the MMA B operand (MN-major)
-    static constexpr uint32_t vn = h + 64 * kKP * 2;       // 2 x v_new as the MMA B operand (MN-major)
-    static constexpr uint32_t vn_bytes = 64 * 64 * 2;
-    static constexpr uint32_t bytes = vn + 2 * vn_bytes;
-    static constexpr uint32_t copy_bytes = 3 * kImgW + kImgP + kImgU + kDecB;
+    static constexpr uint32_t u_slot = kImgU * (BV / 64);      // BV/64 u image tiles side by side
+    static constexpr uint32_t u = 2 * stage;                    // ring of u slots
+    static constexpr uint32_t dec = u + Cfg<BV>::kURing * u_slot;  // ring of 4 decay vectors
+    static constexpr uint32_t h = dec + 4 * kDecB;              // h as the MMA B operand (MN-major)
+    static constexpr uint32_t vn = h + BV * kKP * 2;            // v_new as the MMA B operand (MN-major)
+    static constexpr uint32_t vn_bytes = 64 * BV * 2;
+    static constexpr uint32_t bytes = vn + Cfg<BV>::kVnBuf * vn_bytes;
 };
+static_assert(Lay<128>::bytes <= 226 * 1024, "shared memory of the 128-column tiles");
 
-// TMEM columns: [Xw; O] of even / odd chunks [0,64) / [64,128) (lane = row:
-// 0-63 Xw, 64-127 O), dh [128,192)
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColD = 0, kColDh = 128;
-
-constexpr uint32_t kIdescK = tc_idesc(128, 64, 0, 1);   // A K-major ([w;qg], [0;P]), B MN-major
-constexpr uint32_t kIdescMN = tc_idesc(128, 64, 1, 1);  // A = kg^T MN-major, B = v_new MN-major
+// TMEM columns: [Xw; O] of even / odd chunks [0,BV) / [BV,2BV) (lane = row:
+// 0-63 Xw, 64-127 O), dh [2BV,3BV)
+constexpr uint32_t kColD = 0;
 
 __device__ __forceinline__ uint4 pack8(const float *f) {
     uint4 u;
@@ -87,7 +108,16 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
     return u;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p) {
+template <int BV>
+__global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const FwdParams p) {
+    using Lay = gdn::Lay<BV>;
+    constexpr int kThreads = Cfg<BV>::kThreads;
+    constexpr uint32_t kTmemCols = Cfg<BV>::kTmemCols;
+    constexpr uint32_t kColDh = 2 * BV;
+    constexpr uint32_t kIdescK = tc_idesc(128, BV, 0, 1);   // A K-major ([w;qg], [0;P]), B MN-major
+    constexpr uint32_t kIdescMN = tc_idesc(128, BV, 1, 1);  // A = kg^T MN-major, B = v_new MN-major
+    constexpr int kUT = BV / 64;                            // u image tiles per CTA
+    constexpr int kOutW = BV == 64 ? 6 : 10;                // first output warp (TMEM lanes 64-127)
     extern __shared__ __align__(1024) unsigned char sm[];
     __shared__ __align__(8) uint64_t bar_stage[2], bar_ofree[2];
     __shared__ __align__(8) uint64_t bar_h, bar_vn, bar_a, bar_dh, bar_o;
@@ -99,14 +129,18 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     // the column tiles of one (sequence, head) are adjacent in launch order,
     // so they run together and all but the first read the head's operand
     // images from L2 rather than HBM
-    const int n_tiles = p.n_vt + (p.summary ? p.n_kt : 0);
+    // (the 128-column tiles serve plain forward passes only: no summary)
+    const int n_tiles = BV == 64 ? p.n_vt + (p.summary ? p.n_kt : 0) : (p.n_vt + kUT - 1) / kUT;
     const int bhx = blockIdx.x / n_tiles;
     const int s = bhx / H, hh = bhx % H;
-    const int vt = blockIdx.x % n_tiles, v0 = vt * kBVt;
+    const int vt = blockIdx.x % n_tiles, v0 = vt * BV;
     const int seg = blockIdx.z;
     // a transition tile of a summary pass: columns t0 .. t0+63 of M
-    const bool trt = p.summary && vt >= p.n_vt;
-    const int t0 = trt ? (vt - p.n_vt) * kBVt : 0;
+    const bool trt = BV == 64 && p.summary && vt >= p.n_vt;
+    const int t0 = trt ? (vt - p.n_vt) * BV : 0;
+    // u image tiles of this CTA present in the images (a 128-column CTA over
+    // an odd last tile keeps the second half of its u slots zero)
+    const int n_ut = trt ? 0 : min(kUT, p.n_vt - vt * kUT);
     if (p.cu_seqlens && *p.n_chunks < 0) return;
     SeqInfo si;
     if (!seq_info(p, s, si)) return;
@@ -120,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const uint32_t b_st[2] = {smem_u32(&bar_stage[0]), smem_u32(&bar_stage[1])};
     const uint32_t b_of[2] = {smem_u32(&bar_ofree[0]), smem_u32(&bar_ofree[1])};
     const uint32_t b_h = smem_u32(&bar_h), b_vn = smem_u32(&bar_vn), b_a = smem_u32(&bar_a);
-    const uint32_t b_dh = smem_u32(&bar_dh), b_o = smem_u32(&bar_o);
+    const uint32_t b_dh = smem_u32(&bar_dh);
+    const uint32_t b_o = smem_u32(&bar_o);
     volatile int *abort = &abort_s;
 
     if (warp == 0) {
@@ -135,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_st[1]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[0]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[1]));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(b_h));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b_h), "r"(32 * 4 * kUT));  // recurrence
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 128;" ::"r"(b_vn));  // warps 0, 1, 4, 5
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_a));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_dh));
@@ -147,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         *reinterpret_cast<uint4 *>(sm + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4 *>(sm + Lay::stage + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
     }
-    if (trt)  // u = 0 for the transition columns: the u ring stays zero
-        for (int e = tid; e < (int)(3 * kImgU / 16); e += kThreads)
+    if (n_ut < kUT)  // u = 0 for transition columns and absent tiles: those parts stay zero
+        for (int e = tid; e < (int)(Cfg<BV>::kURing * Lay::u_slot / 16); e += kThreads)
             *reinterpret_cast<uint4 *>(sm + Lay::u + 16 * e) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     tc_fence_before();
@@ -157,35 +192,27 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
     const uint32_t tmem = tmem_base_s;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // chunk c's operands: MMA operands into stage c&1, u into ring slot c%3,
+    // chunk c's operands: MMA operands into stage c&1, u into its ring slot,
     // dec into ring slot c%4, all counted on the stage's barrier.
     auto issue_stage = [&](int c) {
         const int st = c & 1;
         const uint32_t dst = sbase + st * Lay::stage;
         const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b_st[st]),
-                     "r"(Lay::copy_bytes - (trt ? kImgU : 0u))
-                     : "memory");
-        const void *src[6] = {p.w_img + gch * kImgW, p.qg_img + gch * kImgW, p.kg_img + gch * kImgW,
-                              p.p_img + gch * kImgP, p.u_img + (gch * p.n_vt + vt) * kImgU, p.dec + gch * kKP};
-        const uint32_t dsts[6] = {dst + Lay::w, dst + Lay::qg, dst + Lay::kg, dst + Lay::pm,
-                                  sbase + Lay::u + (uint32_t)(c % 3) * kImgU, sbase + Lay::dec + (uint32_t)(c % 4) * kDecB};
-        const uint32_t len[6] = {kImgW, kImgW, kImgW, kImgP, kImgU, kDecB};
-#pragma unroll
-        for (int x = 0; x < 6; ++x) {
-            if (x == 4 && trt) continue;  // transition tiles read no u
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                    dsts[x]),
-                "l"(src[x]), "r"(len[x]), "r"(b_st[st])
-                : "memory");
-        }
+        arrive_expect_tx(b_st[st], 3 * kImgW + kImgP + kDecB + (uint32_t)n_ut * kImgU);
+        bulk_g2s(dst + Lay::w, p.w_img + gch * kImgW, kImgW, b_st[st]);
+        bulk_g2s(dst + Lay::qg, p.qg_img + gch * kImgW, kImgW, b_st[st]);
+        bulk_g2s(dst + Lay::kg, p.kg_img + gch * kImgW, kImgW, b_st[st]);
+        bulk_g2s(dst + Lay::pm, p.p_img + gch * kImgP, kImgP, b_st[st]);
+        const uint32_t us = sbase + Lay::u + (uint32_t)(c % Cfg<BV>::kURing) * Lay::u_slot;
+        for (int x = 0; x < n_ut; ++x)
+            bulk_g2s(us + x * kImgU, p.u_img + (gch * p.n_vt + vt * kUT + x) * kImgU, kImgU, b_st[st]);
+        bulk_g2s(sbase + Lay::dec + (uint32_t)(c % 4) * kDecB, p.dec + gch * kKP, kDecB, b_st[st]);
     };
     // v_new = u - Xw for token row i, columns c0 .. c0+31 (warps 0,1 / 4,5)
     // token row i, columns c0 .. c0+31 of chunk c's u, read ahead of the
     // product it is combined with
     auto load_u = [&](int c, int i, int c0, uint4 (&uv)[4]) {
-        const unsigned char *urow = sm + Lay::u + (c % 3) * kImgU + img_u_off(i, c0);
+        const unsigned char *urow = sm + Lay::u + (c % Cfg<BV>::kURing) * Lay::u_slot + img_u_off(i, c0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) uv[j] = *reinterpret_cast<const uint4 *>(urow + 1024 * j);
     };
@@ -201,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
               "=r"(rr[14]), "=r"(rr[15]), "=r"(rr[16]), "=r"(rr[17]), "=r"(rr[18]), "=r"(rr[19]),
               "=r"(rr[20]), "=r"(rr[21]), "=r"(rr[22]), "=r"(rr[23]), "=r"(rr[24]), "=r"(rr[25]),
               "=r"(rr[26]), "=r"(rr[27]), "=r"(rr[28]), "=r"(rr[29]), "=r"(rr[30]), "=r"(rr[31])
-            : "r"(tmem + lane_base + kColD + par * 64 + c0));
+            : "r"(tmem + lane_base + kColD + par * BV + c0));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -216,16 +243,18 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             }
             // MN-major B operand (N = column, K = token): (col/8)*1024 + i*16
             const uint4 pv = pack8(f);
-            *reinterpret_cast<uint4 *>(sm + Lay::vn + par * Lay::vn_bytes + (c0 / 8 + j) * 1024 + i * 16) = pv;
+            *reinterpret_cast<uint4 *>(sm + Lay::vn + (Cfg<BV>::kVnBuf == 2 ? par : 0u) * Lay::vn_bytes +
+                                       (c0 / 8 + j) * 1024 + i * 16) = pv;
             if (p.vn_snap && v0 + c0 + 8 * j < V)
                 *reinterpret_cast<uint4 *>(p.vn_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * kChunk + i) * V +
                                            v0 + c0 + 8 * j) = pv;
         }
     };
 
-    if (warp < 4) {
+    if (warp < 4 * kUT) {
         // ------------------------------------------------ recurrence warps
-        const int r = tid;
+        // thread r of warp group hg keeps row r, columns 64 hg .. 64 hg + 63
+        const int r = BV == 64 ? tid : tid & 127, hc = BV == 64 ? 0 : (warp >> 2) * 64, v1 = v0 + hc;
         float h[64];
         if (p.summary) {  // E from h = 0, M from h = I
 #pragma unroll
@@ -233,11 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         } else if (p.h_in) {
             const float *src = p.h_in + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) h[c] = (r < K && v0 + c < p.Vt) ? src[v0 + c] : 0.f;
+            for (int c = 0; c < 64; ++c) h[c] = (r < K && v1 + c < p.Vt) ? src[v1 + c] : 0.f;
         } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c)
-                h[c] = (p.h0 && r < K && v0 + c < V) ? p.h0[(bh * K + r) * V + v0 + c] : 0.f;
+                h[c] = (p.h0 && r < K && v1 + c < V) ? p.h0[(bh * K + r) * V + v1 + c] : 0.f;
         }
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -245,27 +274,33 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             const uint32_t par = c & 1;
             // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16; its last
             // reader, chunk c-1's first product, finished before that chunk's dh
-            bf16 *hs = p.h_snap ? p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * V + v0 : nullptr;
+            bf16 *hs = p.h_snap ? p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * V + v1 : nullptr;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint4 hv = pack8(&h[8 * j]);
-                *reinterpret_cast<uint4 *>(sm + Lay::h + j * 2048 + r * 16) = hv;
-                if (hs && r < K && v0 + 8 * j < V) *reinterpret_cast<uint4 *>(hs + 8 * j) = hv;
+                *reinterpret_cast<uint4 *>(sm + Lay::h + (hc / 8 + j) * 2048 + r * 16) = hv;
+                if (hs && r < K && v1 + 8 * j < V) *reinterpret_cast<uint4 *>(hs + 8 * j) = hv;
             }
             fence_async_smem();
             arrive(b_h);
-            if (warp < 2) {  // v_new for token row i = tid, columns 0..31
+            if ((warp & 3) < 2) {  // v_new for token row r (TMEM lanes 0-63)
                 // Only the v_new warps wait for the stage: chunk c+2's copies
                 // into the same slot need this chunk's v_new first, so the
                 // barrier cannot run a phase ahead of them; warps 2-3 take
                 // dec after the dh product, which follows the stage.
                 ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
                 if (!ok) break;
-                uint4 uv[4];
-                load_u(c, tid, 0, uv);
+                // 64 columns: columns 0..31 (the 64-column tile: its helpers
+                // take 32..63), or this group's 64 of the 128-column tile
+                uint4 uv[4], uw[4];
+                load_u(c, r, hc, uv);
+                if (BV == 128) load_u(c, r, hc + 32, uw);
                 ok = warp_all(wait_bar(b_a, par, abort));
                 tc_fence_after();
-                vnew_half(c, tid, 0, uv);
+                if (ok) {
+                    vnew_half(c, r, hc, uv);
+                    if (BV == 128) vnew_half(c, r, hc + 32, uw);
+                }
                 fence_async_smem();
                 tc_fence_before();
                 arrive(b_vn);
@@ -278,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 float t[32];
-                tc_ld32(tmem + lane_base + kColDh + 32 * half, t);
+                tc_ld32(tmem + lane_base + kColDh + hc + 32 * half, t);
 #pragma unroll
                 for (int x = 0; x < 32; ++x) h[32 * half + x] = fmaf(d, h[32 * half + x], t[x]);
             }
@@ -295,14 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
                 float *dst = p.sum_ext + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt;
 #pragma unroll
                 for (int x = 0; x < 64; ++x)
-                    if (v0 + x < p.Vt) dst[v0 + x] = h[x];
+                    if (v1 + x < p.Vt) dst[v1 + x] = h[x];
             }
         } else if (ok && p.h_final && r < K && cb + nchunks == nall) {
 #pragma unroll
             for (int x = 0; x < 64; ++x)
-                if (v0 + x < V) p.h_final[(bh * K + r) * V + v0 + x] = h[x];
+                if (v1 + x < V) p.h_final[(bh * K + r) * V + v1 + x] = h[x];
         }
-    } else if (warp == 4 || warp == 5) {
+    } else if (BV == 64 && (warp == 4 || warp == 5)) {
         // ------------------------------------- v_new helpers (columns 32..63)
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -329,12 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
         const uint64_t dW0 = tc_sdesc(sbase + Lay::w, 128, 2048), dW1 = tc_sdesc(sbase + Lay::stage + Lay::w, 128, 2048);
         const uint64_t dK0 = tc_sdesc(sbase + Lay::kg, 128, 1024), dK1 = tc_sdesc(sbase + Lay::stage + Lay::kg, 128, 1024);
         const uint64_t dZ0 = tc_sdesc(sbase + Lay::z, 128, 1024), dZ1 = tc_sdesc(sbase + Lay::stage + Lay::z, 128, 1024);
-        const uint64_t dV0 = tc_sdesc(sbase + Lay::vn, 128, 1024), dV1 = tc_sdesc(sbase + Lay::vn + Lay::vn_bytes, 128, 1024);
+        const uint64_t dV0 = tc_sdesc(sbase + Lay::vn, 128, 1024),
+                       dV1 = tc_sdesc(sbase + Lay::vn + (Cfg<BV>::kVnBuf - 1) * Lay::vn_bytes, 128, 1024);
         const uint64_t dH = tc_sdesc(sbase + Lay::h, 128, 2048);
         for (; c < nchunks && ok; ++c) {
             const int st = c & 1;
             const uint32_t par = c & 1;
-            const uint32_t dcol = kColD + par * 64;
+            const uint32_t dcol = kColD + par * BV;
             const uint64_t dW = st ? dW1 : dW0, dK = st ? dK1 : dK0, dZ = st ? dZ1 : dZ0, dV = par ? dV1 : dV0;
             // [Xw; O] = [w; qg] h once h_c is written and chunk c's operands
             // landed (this accumulator set's previous user, chunk c-2, was read
@@ -354,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             tc_commit(b_dh);
             // b_o must not run two phases ahead of the output warps: chunk
             // c-1's output has to be read out before chunk c's is committed
+            // (this also keeps the output warps, which issue the operand
+            // copies, in step with the chain)
             if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
             if (!ok) break;
 #pragma unroll
@@ -369,10 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             if (c + 1 < nchunks) wait_bar(b_st[(c + 1) & 1], ((c + 1) >> 1) & 1, nullptr);
             if (c + 2 < nchunks) wait_bar(b_st[c & 1], ((c + 2) >> 1) & 1, nullptr);
         }
-    } else if (warp == 6 || warp == 7) {
+    } else if (warp == kOutW || warp == kOutW + 1) {
         // ------------------------------------------------ output warps (lanes 64-127)
-        const int i = tid - 192;  // token row within the chunk
-        if (tid == 192) {
+        const int i = tid - 32 * kOutW;  // token row within the chunk
+        const bool copier = i == 0;
+        if (copier) {
             if (nchunks > 0) issue_stage(0);
             if (nchunks > 1) issue_stage(1);
         }
@@ -383,80 +422,91 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
             const int Lc = min(kChunk, si.len - pos0);
             const bool wr = i < Lc && !p.summary && p.out;  // no output: summary or recompute pass
             const int tq = wr ? q_token(p.reverse, si.len, pos0 + i) : 0;
-            const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + v0;
             float *dp = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
-            const bool den_here = p.has_den && v0 <= V && V < v0 + 64;
-            // accumulating into bf16 rows: their old contents are loaded while
-            // this chunk's products are still running
-            uint4 prev[8];
-            float dprev = 0.f;
-            if (wr && p.accumulate && !p.out_f32) {
+            // 64 columns at a time
+#pragma unroll 1
+            for (int hv = 0; hv < kUT; ++hv) {
+                const int vo = v0 + 64 * hv;
+                const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + vo;
+                const bool den_here = p.has_den && vo <= V && V < vo + 64;
+                // accumulating into bf16 rows: their old contents are loaded while
+                // this chunk's products are still running
+                uint4 prev[8];
+                float dprev = 0.f;
+                if (wr && p.accumulate && !p.out_f32) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    prev[j] = (v0 + 8 * j + 8 <= V) ? *reinterpret_cast<const uint4 *>((const bf16 *)p.out + off + 8 * j)
-                                                    : make_uint4(0, 0, 0, 0);
-            }
-            if (wr && p.accumulate && den_here) dprev = *dp;
-            ok = warp_all(wait_bar(b_o, par, abort));
-            tc_fence_after();
-            // chunk c's last MMA is done: stage c&1 may take chunk c+2's MMA
-            // operands; u slot (c+2)%3 was last read by chunk c-1's v_new and
-            // dec slot (c+2)%4 by chunk c-2's h update, both long finished
-            if (tid == 192 && ok && c + 2 < nchunks) issue_stage(c + 2);
-            float t[64];
-            tc_ld64(tmem + lane_base + kColD + par * 64, t);
-            tc_fence_before();
-            arrive(b_of[c & 1]);
-            if (!ok || !wr) continue;
-            if (p.out_f32) {
-#pragma unroll
-                for (int h4 = 0; h4 < 2; ++h4) {  // per half: every load before any store
-                    float4 y[8];
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = 4 * h4 + jj;
-                        const bool in = p.accumulate && v0 + 8 * j + 8 <= V;
-                        const float4 *op = reinterpret_cast<const float4 *>((const float *)p.out + off + 8 * j);
-                        y[2 * jj] = in ? op[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-                        y[2 * jj + 1] = in ? op[1] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        const int j = 4 * h4 + jj;
-                        if (v0 + 8 * j + 8 > V) continue;
-                        float4 *op = reinterpret_cast<float4 *>((float *)p.out + off + 8 * j);
-                        const float4 y0 = y[2 * jj], y1 = y[2 * jj + 1];
-                        op[0] = make_float4(t[8 * j] + y0.x, t[8 * j + 1] + y0.y, t[8 * j + 2] + y0.z,
-                                            t[8 * j + 3] + y0.w);
-                        op[1] = make_float4(t[8 * j + 4] + y1.x, t[8 * j + 5] + y1.y, t[8 * j + 6] + y1.z,
-                                            t[8 * j + 7] + y1.w);
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        prev[j] = (vo + 8 * j + 8 <= V)
+                                      ? *reinterpret_cast<const uint4 *>((const bf16 *)p.out + off + 8 * j)
+                                      : make_uint4(0, 0, 0, 0);
                 }
-            } else {
+                if (wr && p.accumulate && den_here) dprev = *dp;
+                if (hv == 0) {
+                    ok = warp_all(wait_bar(b_o, par, abort));
+                    tc_fence_after();
+                    // chunk c's last MMA is done: stage c&1 may take chunk c+2's
+                    // MMA operands; u slot (c+2) of the ring was last read by an
+                    // earlier chunk's v_new and dec slot (c+2)%4 by chunk c-2's h
+                    // update, both finished
+                    if (copier && ok && c + 2 < nchunks) issue_stage(c + 2);
+                }
+                float t[64];
+                tc_ld64(tmem + lane_base + kColD + par * BV + 64 * hv, t);
+                if (hv == kUT - 1) {
+                    tc_fence_before();
+                    arrive(b_of[c & 1]);
+                }
+                if (!ok || !wr) continue;
+                if (p.out_f32) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (v0 + 8 * j + 8 > V) continue;
-                    float f[8];
+                    for (int h4 = 0; h4 < 2; ++h4) {  // per half: every load before any store
+                        float4 y[8];
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) f[x] = t[8 * j + x];
-                    if (p.accumulate) {
-                        const __nv_bfloat162 *y2 = reinterpret_cast<const __nv_bfloat162 *>(&prev[j]);
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = 4 * h4 + jj;
+                            const bool in = p.accumulate && vo + 8 * j + 8 <= V;
+                            const float4 *op = reinterpret_cast<const float4 *>((const float *)p.out + off + 8 * j);
+                            y[2 * jj] = in ? op[0] : make_float4(0.f, 0.f, 0.f, 0.f);
+                            y[2 * jj + 1] = in ? op[1] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float2 fy = __bfloat1622float2(y2[x]);
-                            f[2 * x] += fy.x;
-                            f[2 * x + 1] += fy.y;
+                        for (int jj = 0; jj < 4; ++jj) {
+                            const int j = 4 * h4 + jj;
+                            if (vo + 8 * j + 8 > V) continue;
+                            float4 *op = reinterpret_cast<float4 *>((float *)p.out + off + 8 * j);
+                            const float4 y0 = y[2 * jj], y1 = y[2 * jj + 1];
+                            op[0] = make_float4(t[8 * j] + y0.x, t[8 * j + 1] + y0.y, t[8 * j + 2] + y0.z,
+                                                t[8 * j + 3] + y0.w);
+                            op[1] = make_float4(t[8 * j + 4] + y1.x, t[8 * j + 5] + y1.y, t[8 * j + 6] + y1.z,
+                                                t[8 * j + 7] + y1.w);
                         }
                     }
-                    *reinterpret_cast<uint4 *>((bf16 *)p.out + off + 8 * j) = pack8(f);
-                }
-            }
-            if (den_here) {  // the ones column V sits at the start of an 8-column group
-                float dv = 0.f;
+                } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (v0 + 8 * j == V) dv = t[8 * j];
-                *dp = (p.accumulate ? dprev : 0.f) + dv;
+                    for (int j = 0; j < 8; ++j) {
+                        if (vo + 8 * j + 8 > V) continue;
+                        float f[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) f[x] = t[8 * j + x];
+                        if (p.accumulate) {
+                            const __nv_bfloat162 *y2 = reinterpret_cast<const __nv_bfloat162 *>(&prev[j]);
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                const float2 fy = __bfloat1622float2(y2[x]);
+                                f[2 * x] += fy.x;
+                                f[2 * x + 1] += fy.y;
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>((bf16 *)p.out + off + 8 * j) = pack8(f);
+                    }
+                }
+                if (den_here) {  // the ones column V sits at the start of an 8-column group
+                    float dv = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (vo + 8 * j == V) dv = t[8 * j];
+                    *dp = (p.accumulate ? dprev : 0.f) + dv;
+                }
             }
         }
     }
@@ -470,17 +520,47 @@ __global__ void __launch_bounds__(kThreads, 1) state_tc_kernel(const FwdParams p
 
 }  // namespace
 
-cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Lay::bytes);
+namespace {
+std::atomic<int> g_state_tile{0};  // 0: by the grid, else 64 or 128
+
+template <int BV>
+cudaError_t launch_bv(const FwdParams &p, int n_tiles, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Lay<BV>::bytes);
     if (e != cudaSuccess) return e;
     const int nall = (p.T + kChunk - 1) / kChunk;
     // summary 2: every segment but the last (whose summary nothing reads)
     const int nseg = p.seg_chunks ? max(1, (nall + p.seg_chunks - 1) / p.seg_chunks) - (p.summary == 2 ? 1 : 0) : 1;
     if (nseg < 1) return cudaSuccess;
-    dim3 grid(p.n_seq * p.H * (p.n_vt + (p.summary ? p.n_kt : 0)), 1, nseg);
-    state_tc_kernel<<<grid, kThreads, Lay::bytes, st>>>(p);
+    dim3 grid(p.n_seq * p.H * n_tiles, 1, nseg);
+    state_tc_kernel<BV><<<grid, Cfg<BV>::kThreads, Lay<BV>::bytes, st>>>(p);
     return cudaGetLastError();
+}
+}  // namespace
+
+void set_state_tile(int bv) { g_state_tile.store(bv == 64 || bv == 128 ? bv : 0); }
+
+cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st) {
+    // 128-column tiles: plain passes (no summary, no snapshots) over two or
+    // more 64-column tiles whose 64-column grid would not fit one wave of
+    // one CTA per SM
+    bool wide = false;
+    const int forced = g_state_tile.load();
+    if (!p.summary && !p.h_snap && p.n_vt >= 2) {
+        if (forced) {
+            wide = forced == 128;
+        } else {
+            int dev = 0, n_sm = 0;
+            cudaError_t e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+            const int64_t nall = (p.T + kChunk - 1) / kChunk;
+            const int64_t nseg = p.seg_chunks ? (nall + p.seg_chunks - 1) / p.seg_chunks : 1;
+            wide = (int64_t)p.n_seq * p.H * p.n_vt * nseg > n_sm;
+        }
+    }
+    if (wide) return launch_bv<128>(p, (p.n_vt + 1) / 2, st);
+    return launch_bv<64>(p, p.n_vt + (p.summary ? p.n_kt : 0), st);
 }
 
 }  // namespace gdn

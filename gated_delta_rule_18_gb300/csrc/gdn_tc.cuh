@@ -11,7 +11,7 @@ namespace gdn {
 // instruction descriptor, kind::f16 with bf16 A and B and an fp32 accumulator
 // (bit 4: D f32, bits 7 / 10: A / B bf16, bits 15 / 16: A / B MN-major,
 // N >> 3 at bit 17, M >> 4 at bit 24)
-constexpr uint32_t tc_idesc(int M, int N, int a_mn, int b_mn) {
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }

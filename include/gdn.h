@@ -397,6 +397,19 @@ void gdn_profile_enable(int on);
 gdn_status gdn_profile_collect(float *ms, int *launches, int n);
 long long gdn_launch_count(void);
 
+/*
+ * Value columns per CTA of the tensor-core state pass (the chunk-serial
+ * recurrence of the chunked form, hyper-parallel coverage_diff page,
+ * `chunk_gated_delta_rule_fwd_kernel_h_blockdim64`).
+ *   bv = 0 (the default) chooses by the grid: 64-column CTAs, or 128-column
+ *   CTAs (both 64-column tiles of a head in one CTA) for passes without
+ *   summaries or snapshots whose 64-column grid has more CTAs than the GPU
+ *   has SMs. bv = 64 or 128 forces one (128 only where the pass allows it);
+ *   any other value means 0. Process-wide; affects later launches. Both
+ *   compute the same recurrence (results agree to rounding order).
+ */
+void gdn_set_state_tile(int bv);
+
 #ifdef __cplusplus
 }
 #endif

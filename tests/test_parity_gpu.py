@@ -496,3 +496,32 @@ def test_repeated_long_runs_clean_and_deterministic(name):
             first = cur
         else:
             assert t.equal(cur[0], first[0]) and t.equal(cur[1], first[1])
+
+
+@pytest.fixture
+def wide_state_tiles():
+    """Force the state pass's 128-column CTAs (both 64-column tiles of a head
+    in one CTA), which the library otherwise picks only for grids wider than
+    the GPU; the same oracle comparisons then cover that kernel."""
+    import gated_delta_rule_18_gb300 as gdn
+    gdn.gdn_set_state_tile(128)
+    yield
+    gdn.gdn_set_state_tile(0)
+
+
+WIDE = ["bf16_k128_h0", "bf16_gk_v256", "bf16_varlen_h0", "bf16_k32_v96", "bf16_k112_v112", "bf16_t64"]
+
+
+@pytest.mark.parametrize("name", WIDE)
+def test_small_causal_wide_state_tiles(name, wide_state_tiles):
+    test_small_causal(name)
+
+
+def test_small_bidirectional_segmented_resume_wide_state_tiles(wide_state_tiles):
+    test_small_bidirectional_l2("bf16")       # den column: an odd last 64-column tile
+    test_small_video_rms_bidirectional()
+    for name in sorted(SEG):
+        test_small_segmented(name)             # entering states per segment (grid z)
+    test_reverse_only_varlen_gk("bf16")
+    test_split_resume_bit_exact("bf16")
+    test_zero_tokens_pass_state_through("bf16")
