@@ -246,9 +246,15 @@ def test_full_size_dense(name):
         assert e_o <= tol and e_h <= tol, (name, b, heads, e_o, e_h)
 
 
-def test_full_size_varlen():
+@pytest.mark.parametrize("tile", [0, 64])  # 0: the library's choice (128-column CTAs here)
+def test_full_size_varlen(tile):
+    import gated_delta_rule_18_gb300 as gdn
     w = workloads.build("varlen_bf16_64seq_h32d128")
-    got = run_gpu(w)
+    gdn.gdn_set_state_tile(tile)
+    try:
+        got = run_gpu(w)
+    finally:
+        gdn.gdn_set_state_tile(0)
     seqs, heads = [0, 17, 63], [3, 31]
     sw, rows = _sub_varlen(w, seqs, heads)
     ref = oracle.forward(sw)
