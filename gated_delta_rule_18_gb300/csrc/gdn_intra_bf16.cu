@@ -408,6 +408,11 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
             constexpr int kItems = kChunk * (KP / 8) / NT;
             const int n_items = (kChunk - r0) * (KP / 8);
             float fct[kItems][8];
+            // a thread's items all sit in one eight-channel group (NT is a
+            // multiple of KP / 8), so the reference row's gates load once
+            static_assert(NT % (KP / 8) == 0, "fixed channel group per thread");
+            float gr[8];
+            ld8f(sG + r * KP + (tid % (KP / 8)) * 8, gr);
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {  // 0: keys (A), 1: queries (P)
                 __syncthreads();  // the previous product has read sL
@@ -419,9 +424,8 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
                     if (e >= n_items) break;
                     const int i = r0 + e / (KP / 8), d = (e % (KP / 8)) * 8;
                     if (pass == 0) {
-                        float gi[8], gr[8];
+                        float gi[8];
                         ld8f(sG + i * KP + d, gi);
-                        ld8f(sG + r * KP + d, gr);
 #pragma unroll
                         for (int x = 0; x < 8; ++x) fct[u][x] = ex2(gi[x] - gr[x]);
                     }
