@@ -350,9 +350,12 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
             }
         }
     } else {
-        if (tid < 2 * kChunk) {  // row norms as scalars (the tiles stay raw)
-            const int r = tid & 63;
-            const bf16 *row = (tid < 64 ? sQ : sK) + r * KS;
+        // row norms as scalars (the tiles stay raw) on the upper 128 threads,
+        // alongside the channel cumsums on the lower 128
+        static_assert(!PERKEY || NT >= 2 * kChunk + KP, "norms and cumsums on separate threads");
+        if (tid >= NT - 2 * kChunk) {
+            const int t2 = tid - (NT - 2 * kChunk), r = t2 & 63;
+            const bf16 *row = (t2 < 64 ? sQ : sK) + r * KS;
             float ss = 0.f;
 #pragma unroll
             for (int d = 0; d < KP; d += 8) {
@@ -361,7 +364,7 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
 #pragma unroll
                 for (int x = 0; x < 8; ++x) ss = fmaf(f[x], f[x], ss);
             }
-            (tid < 64 ? sRq : sRk)[r] = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
+            (t2 < 64 ? sRq : sRk)[r] = p.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
         }
         if (tid < KP) {  // per-channel cumsums: thread d keeps its channel's 64 gates in registers
             static_assert(kThreads == KP, "one thread per key channel");
