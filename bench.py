@@ -117,6 +117,11 @@ def kernel_bytes(w, name):
         return f * (th * ((3 * K + V + C) * 2) + chunks * K * 4) + (n_seg - 1) * bh * K * (V + K) * 4
     if name == "seg_combine":  # (E, M) in, the entering states out
         return (n_seg - 1) * bh * K * (V + K) * 4 + n_seg * bh * K * V * 4
+    if name == "f32_prep":  # inputs in; w, qg, kg, P, u images and dec out (fp32)
+        return th * ((2 * K + w.V) * e + 4 + gate + (3 * K + C + V) * 4) + chunks * K * 4
+    if name == "f32_serial":  # the images in, the output (and h0 / h_final) out
+        return th * ((3 * K + C + V) * 4 + w.V * e) + chunks * K * 4 + \
+            (2 if w.h0 is not None else 1) * w.n_seq * w.H * w.K * w.V * 4
     if name == "fused_f32":
         return th * ((2 * K + w.V) * e + 4 + gate + w.V * e) + w.n_seq * w.H * w.K * w.V * 4
     if name == "prep_rms":

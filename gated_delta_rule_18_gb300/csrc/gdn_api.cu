@@ -16,12 +16,12 @@ using gdn::FwdParams;
 
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
-    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KNumKinds
+    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
-                                     "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum"};
+                                     "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial"};
 
 struct Profiler {
     std::mutex mu;
@@ -104,6 +104,21 @@ bool ws_layout(int B, int T, int H, int K, int V, int n_seq, int varlen, int dty
     L.seq0 = off;
     off = align_up(off + (varlen ? sizeof(int) * (size_t)(n_seq + 1) : 0));
     L.w = L.qg = L.kg = L.pm = L.u = L.dec = off;
+    if (dtype == GDN_F32 && gdn::f32_split(n_seq, H, L.Vt)) {  // fp32 images of the split path
+        const size_t hmc = (size_t)H * (size_t)mc, f = sizeof(float);
+        L.w = off;
+        off = align_up(off + hmc * gdn::kChunk * L.KP * f);
+        L.qg = off;
+        off = align_up(off + hmc * gdn::kChunk * L.KP * f);
+        L.kg = off;
+        off = align_up(off + hmc * gdn::kChunk * L.KP * f);
+        L.pm = off;
+        off = align_up(off + hmc * gdn::kChunk * gdn::kChunk * f);
+        L.u = off;
+        off = align_up(off + hmc * gdn::kChunk * gdn::f32_vp32(L.Vt) * f);
+        L.dec = off;
+        off = align_up(off + hmc * L.KP * f);
+    }
     if (dtype == GDN_BF16) {  // per-(head, chunk) operand images
         const size_t hmc = (size_t)H * (size_t)mc;
         L.w = off;
@@ -134,6 +149,18 @@ bool strides_ok(const gdn_tensor_desc &d) {
 bool dtype_ok(int t) { return t == GDN_F32 || t == GDN_BF16; }
 
 gdn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+// The fp32 path: one fused kernel, or, for grids that would leave the GPU
+// mostly idle, the chunk-parallel prep and the chunk-serial pass (the
+// workspace holds their images exactly then, see ws_layout).
+cudaError_t launch_f32(const gdn::FwdParams &p, int KP, int perkey, cudaStream_t s) {
+    if (!gdn::f32_split(p.n_seq, p.H, p.Vt))
+        return launch(KFusedF32, s, [&] { return gdn::launch_fused_f32(p, KP, perkey, s); });
+    cudaError_t e = cudaSuccess;
+    if (p.max_chunks > 0) e = launch(KF32Prep, s, [&] { return gdn::launch_f32_prep(p, KP, perkey, s); });
+    if (e != cudaSuccess) return e;
+    return launch(KF32Serial, s, [&] { return gdn::launch_f32_serial(p, KP, s); });
+}
 
 }  // namespace
 
@@ -331,7 +358,7 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     if (varlen) e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     if (qkd.dtype == GDN_F32) {
-        e = launch(KFusedF32, stream, [&] { return gdn::launch_fused_f32(p, L.KP, perkey, stream); });
+        e = launch_f32(p, L.KP, perkey, stream);
         return cuda_status(e);
     }
     if (L.max_chunks > 0) {
@@ -655,7 +682,7 @@ gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd
         if (varlen) e = launch(KTable, s, [&] { return gdn::launch_chunk_table(p, s); });
         if (e != cudaSuccess) return e;
         if (qkd.dtype == GDN_F32)
-            return launch(KFusedF32, s, [&] { return gdn::launch_fused_f32(p, L.KP, perkey, s); });
+            return launch_f32(p, L.KP, perkey, s);
         if (L.max_chunks > 0) e = launch(KIntra, s, [&] { return gdn::launch_intra_bf16(p, perkey, s); });
         return e;
     };

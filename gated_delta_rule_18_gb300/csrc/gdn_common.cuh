@@ -352,6 +352,17 @@ cudaError_t launch_bwd_dh(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_dk(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);
+// the fp32 path in two kernels (chunk-parallel prep, chunk-serial pass) for
+// problems whose fused grid would leave the GPU mostly idle
+cudaError_t launch_f32_prep(const FwdParams &p, int KP, int perkey, cudaStream_t st);
+cudaError_t launch_f32_serial(const FwdParams &p, int KP, cudaStream_t st);
+// value columns of the fp32 u image (a multiple of 32)
+__host__ __device__ __forceinline__ int f32_vp32(int vt) { return (vt + 31) / 32 * 32; }
+// the fp32 path splits when its fused grid has at most this many CTAs
+constexpr int kF32SplitMaxCtas = 32;
+__host__ __device__ __forceinline__ bool f32_split(int n_seq, int H, int vt) {
+    return (int64_t)n_seq * H * ((vt + 31) / 32) <= kF32SplitMaxCtas;
+}
 cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, void *y,
                         int64_t ysb, int64_t yst, int64_t ysh, int B, int T, int H, int D,
                         int bf16, int mode, float scale, float eps, float *inv_rms,

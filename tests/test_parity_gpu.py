@@ -45,6 +45,10 @@ SMALL = {
     "f32_k128_v256_gk": dict(B=1, T=150, H=2, K=128, V=256, dtype="f32", g_mu=None, gk_mu=4.0),
     "f32_varlen_h0": dict(B=1, T=sum(VL), H=2, K=64, V=64, dtype="f32", lengths=VL, h0_std=0.5),
     "f32_k32_v96": dict(B=1, T=97, H=3, K=32, V=96, dtype="f32"),
+    # 20 x 2 x 2 (sequence, head, 32-column tile) units: the fused fp32 kernel
+    # (the cases above split into the chunk-parallel prep and serial pass)
+    "f32_fused_b20": dict(B=20, T=130, H=2, K=64, V=64, dtype="f32", h0_std=0.5),
+    "f32_fused_gk_b12": dict(B=12, T=70, H=2, K=128, V=64, dtype="f32", g_mu=None, gk_mu=4.0),
     "bf16_dense_k64": dict(B=2, T=200, H=3, K=64, V=64),
     "bf16_k128_h0": dict(B=1, T=333, H=2, K=128, V=128, h0_std=0.5),
     "bf16_gk_v256": dict(B=1, T=190, H=2, K=128, V=256, g_mu=None, gk_mu=4.0),
