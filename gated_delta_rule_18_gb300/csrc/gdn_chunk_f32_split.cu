@@ -23,7 +23,8 @@ namespace {
 constexpr int kT = 256;  // threads per CTA
 constexpr int kBV = 32;  // value columns per tile of the serial pass
 constexpr int kBW = 128;  // right-hand-side columns per substitution pass of the prep
-constexpr int kAS = kChunk + 1, kVS = kBV + 1, kWS = kBW + 1;
+constexpr int kAS = kChunk + 1, kWS = kBW + 1;
+constexpr int kVS = kBV + 4;  // 16-byte aligned rows of h and v_new: a thread's 4 columns in one load
 
 // ---------------------------------------------------------------- prep ----
 template <int KP, bool PERKEY>
@@ -423,9 +424,8 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
                 for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = 0.f;
 #pragma unroll 4
             for (int d = 0; d < KP; ++d) {
-                float hv[4];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) hv[c4] = sH[d * kVS + 4 * nq + c4];
+                const float4 h4 = *reinterpret_cast<const float4 *>(sH + d * kVS + 4 * nq);
+                const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const float wv = sW[(ig + 32 * r) * QS + d];
@@ -451,9 +451,8 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
                 for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = 0.f;
 #pragma unroll 4
             for (int d = 0; d < KP; ++d) {
-                float hv[4];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) hv[c4] = sH[d * kVS + 4 * nq + c4];
+                const float4 h4 = *reinterpret_cast<const float4 *>(sH + d * kVS + 4 * nq);
+                const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const float qv = sQG[(ig + 32 * r) * QS + d];
@@ -463,9 +462,8 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
             }
 #pragma unroll 4
             for (int j = 0; j < kChunk; ++j) {
-                float vv[4];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) vv[c4] = sVn[j * kVS + 4 * nq + c4];
+                const float4 v4 = *reinterpret_cast<const float4 *>(sVn + j * kVS + 4 * nq);
+                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const float pj = sP[(ig + 32 * r) * PS + j];
@@ -509,9 +507,8 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
             }
 #pragma unroll 4
             for (int i = 0; i < Lc; ++i) {
-                float vv[4];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) vv[c4] = sVn[i * kVS + 4 * nq + c4];
+                const float4 v4 = *reinterpret_cast<const float4 *>(sVn + i * kVS + 4 * nq);
+                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                 for (int r = 0; r < RD; ++r) {
                     const float kf = sKG[i * QS + dg + 32 * r];
