@@ -20,7 +20,8 @@
 namespace gdn {
 namespace {
 
-constexpr int kT = 256;  // threads per CTA
+constexpr int kT = 256;   // threads per prep CTA
+constexpr int kTS = 512;  // threads per serial CTA: two halves splitting each reduction
 constexpr int kBV = 32;  // value columns per tile of the serial pass
 constexpr int kBW = 128;  // right-hand-side columns per substitution pass of the prep
 constexpr int kAS = kChunk + 1, kWS = kBW + 1;
@@ -344,13 +345,14 @@ struct SerSmem {
     static constexpr int NB = KP == 64 ? 2 : 1;
     static constexpr int vn = NB * buf;
     static constexpr int h = vn + kChunk * kVS;
-    static constexpr int total = h + KP * kVS;
+    static constexpr int part = h + KP * kVS;  // the upper half's partial sums
+    static constexpr int total = part + KP * kVS;
     static constexpr size_t bytes = sizeof(float) * total;
 };
 static_assert(SerSmem<64>::bytes <= 227 * 1024 && SerSmem<128>::bytes <= 227 * 1024, "serial shared memory");
 
 template <int KP>
-__global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int vp32) {
+__global__ void __launch_bounds__(kTS) f32_serial_kernel(const FwdParams p, int vp32) {
     using L = SerSmem<KP>;
     constexpr int QS = L::QS, PS = L::PS, US = L::US;
     extern __shared__ __align__(16) float sm[];
@@ -365,14 +367,18 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
     const int nchunks = (si.len + kChunk - 1) / kChunk;
     const int gc0 = p.cu_seqlens ? p.seq_chunk0[s] : s * ((p.T + kChunk - 1) / kChunk);
 
-    for (int e = tid; e < KP * kBV; e += kT) {  // state tile h[d][n]
+    for (int e = tid; e < KP * kBV; e += kTS) {  // state tile h[d][n]
         const int d = e / kBV, n = e % kBV, col = v0 + n;
         sH[d * kVS + n] = (p.h0 && d < K && col < V) ? p.h0[(((int64_t)s * H + hh) * K + d) * V + col] : 0.f;
     }
-    // 2 rows x 4 columns per thread for the 64 x 32 products; KP/32 key rows
-    // x 4 columns for the state update
-    const int nq = tid & 7, ig = tid >> 3, dg = tid >> 3;
+    // 2 rows x 4 columns per thread for the 64 x 32 products, KP/32 key rows
+    // x 4 columns for the state update; the two halves of the CTA (hf) take
+    // two halves of each reduction, the upper one handing its partial sums
+    // over through sPart
+    const int hf = tid >> 8, lt = tid & 255;
+    const int nq = lt & 7, ig = lt >> 3, dg = lt >> 3;
     constexpr int RD = KP / 32;
+    float *sPart = sm + L::part;
     // chunk c's operands into buffer c % NB: 16-byte asynchronous copies
     auto fetch = [&](int c) {
         float *bs = sm + (c % L::NB) * L::buf;
@@ -382,21 +388,21 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
         const float *gKg = reinterpret_cast<const float *>(p.kg_img) + gch * kChunk * KP;
         const float *gP = reinterpret_cast<const float *>(p.p_img) + gch * kChunk * kChunk;
         const float *gU = reinterpret_cast<const float *>(p.u_img) + gch * kChunk * vp32 + v0;
-        for (int e = tid; e < kChunk * KP / 4; e += kT) {
+        for (int e = tid; e < kChunk * KP / 4; e += kTS) {
             const int i = e / (KP / 4), d = (e % (KP / 4)) * 4;
             cp_async16(bs + L::w + i * QS + d, gW + i * KP + d, 16);
             cp_async16(bs + L::qg + i * QS + d, gQg + i * KP + d, 16);
             cp_async16(bs + L::kg + i * QS + d, gKg + i * KP + d, 16);
         }
-        for (int e = tid; e < kChunk * kChunk / 4; e += kT) {
+        for (int e = tid; e < kChunk * kChunk / 4; e += kTS) {
             const int i = e / (kChunk / 4), j = (e % (kChunk / 4)) * 4;
             cp_async16(bs + L::pm + i * PS + j, gP + i * kChunk + j, 16);
         }
-        for (int e = tid; e < kChunk * kBV / 4; e += kT) {
+        for (int e = tid; e < kChunk * kBV / 4; e += kTS) {
             const int i = e / (kBV / 4), n = (e % (kBV / 4)) * 4;
             cp_async16(bs + L::u + i * US + n, gU + i * vp32 + n, 16);
         }
-        for (int e = tid; e < KP / 4; e += kT) cp_async16(bs + L::dec + 4 * e, p.dec + gch * KP + 4 * e, 16);
+        for (int e = tid; e < KP / 4; e += kTS) cp_async16(bs + L::dec + 4 * e, p.dec + gch * KP + 4 * e, 16);
     };
     if (nchunks > 0) fetch(0);
     cp_async_commit();
@@ -415,15 +421,16 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
         const float *bs = sm + (c % L::NB) * L::buf;
         const float *sW = bs + L::w, *sQG = bs + L::qg, *sKG = bs + L::kg, *sP = bs + L::pm;
         const float *sU = bs + L::u, *sDec = bs + L::dec;
-        // ---- v_new = u - w h
+        // ---- v_new = u - w h: keys [hf KP/2, (hf+1) KP/2) per half
         {
             float acc[2][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < KP; ++d) {
+            const int d0 = hf * (KP / 2);
+#pragma unroll 16
+            for (int d = d0; d < d0 + KP / 2; ++d) {
                 const float4 h4 = *reinterpret_cast<const float4 *>(sH + d * kVS + 4 * nq);
                 const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
 #pragma unroll
@@ -433,80 +440,106 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
                     for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(wv, hv[c4], acc[r][c4]);
                 }
             }
+            if (hf)
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < 2; ++r)
+                    *reinterpret_cast<float4 *>(sPart + (ig + 32 * r) * kVS + 4 * nq) =
+                        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            __syncthreads();
+            if (!hf)
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int i = ig + 32 * r, n = 4 * nq + c4;
-                    sVn[i * kVS + n] = sU[i * US + n] - acc[r][c4];
+                for (int r = 0; r < 2; ++r) {
+                    const int i = ig + 32 * r;
+                    const float4 o4 = *reinterpret_cast<const float4 *>(sPart + i * kVS + 4 * nq);
+                    const float oa[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int n = 4 * nq + c4;
+                        sVn[i * kVS + n] = sU[i * US + n] - (acc[r][c4] + oa[c4]);
+                    }
                 }
         }
         __syncthreads();
-        // ---- o = qg h + P v_new (P is zero right of the diagonal)
+        // ---- o = qg h (lower half) + P v_new (upper half; P is zero right of
+        // the diagonal)
         {
             float acc[2][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = 0.f;
-#pragma unroll 4
-            for (int d = 0; d < KP; ++d) {
-                const float4 h4 = *reinterpret_cast<const float4 *>(sH + d * kVS + 4 * nq);
-                const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
+            if (!hf) {
+#pragma unroll 16
+                for (int d = 0; d < KP; ++d) {
+                    const float4 h4 = *reinterpret_cast<const float4 *>(sH + d * kVS + 4 * nq);
+                    const float hv[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float qv = sQG[(ig + 32 * r) * QS + d];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(qv, hv[c4], acc[r][c4]);
+                    }
+                }
+            } else {
+#pragma unroll 16
+                for (int j = 0; j < kChunk; ++j) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(sVn + j * kVS + 4 * nq);
+                    const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float pj = sP[(ig + 32 * r) * PS + j];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(pj, vv[c4], acc[r][c4]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+                    *reinterpret_cast<float4 *>(sPart + (ig + 32 * r) * kVS + 4 * nq) =
+                        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            }
+            __syncthreads();
+            if (!hf) {
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float qv = sQG[(ig + 32 * r) * QS + d];
+                    const int i = ig + 32 * r;
+                    if (i >= Lc) continue;
+                    const float4 o4 = *reinterpret_cast<const float4 *>(sPart + i * kVS + 4 * nq);
+                    const float oa[4] = {o4.x, o4.y, o4.z, o4.w};
+                    const int tq = q_token(p.reverse, si.len, pos0 + i);
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(qv, hv[c4], acc[r][c4]);
-                }
-            }
-#pragma unroll 4
-            for (int j = 0; j < kChunk; ++j) {
-                const float4 v4 = *reinterpret_cast<const float4 *>(sVn + j * kVS + 4 * nq);
-                const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float pj = sP[(ig + 32 * r) * PS + j];
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(pj, vv[c4], acc[r][c4]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int i = ig + 32 * r;
-                if (i >= Lc) continue;
-                const int tq = q_token(p.reverse, si.len, pos0 + i);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int col = v0 + 4 * nq + c4;
-                    const float val = acc[r][c4];
-                    if (col < V) {
-                        const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + col;
-                        if (p.out_f32) {
-                            float *o = (float *)p.out + off;
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int col = v0 + 4 * nq + c4;
+                        const float val = acc[r][c4] + oa[c4];
+                        if (col < V) {
+                            const int64_t off = si.b * p.o_sb + (int64_t)(si.tstart + tq) * p.o_st + hh * p.o_sh + col;
+                            if (p.out_f32) {
+                                float *o = (float *)p.out + off;
+                                *o = p.accumulate ? *o + val : val;
+                            } else {
+                                __nv_bfloat16 *o = (__nv_bfloat16 *)p.out + off;
+                                *o = __float2bfloat16_rn(p.accumulate ? __bfloat162float(*o) + val : val);
+                            }
+                        } else if (p.has_den && col == V) {
+                            float *o = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
                             *o = p.accumulate ? *o + val : val;
-                        } else {
-                            __nv_bfloat16 *o = (__nv_bfloat16 *)p.out + off;
-                            *o = __float2bfloat16_rn(p.accumulate ? __bfloat162float(*o) + val : val);
                         }
-                    } else if (p.has_den && col == V) {
-                        float *o = p.den + ((int64_t)si.b * H + hh) * p.T + si.tstart + tq;
-                        *o = p.accumulate ? *o + val : val;
                     }
                 }
             }
         }
-        // ---- h = dec . h + kg^T v_new
+        __syncthreads();  // sPart is rewritten below
+        // ---- h = dec . h + kg^T v_new: tokens [32 hf, 32 hf + 32) per half
         {
             float acc[RD][4];
 #pragma unroll
             for (int r = 0; r < RD; ++r) {
-                const float dd = sDec[dg + 32 * r];
+                const float dd = hf ? 0.f : sDec[dg + 32 * r];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = dd * sH[(dg + 32 * r) * kVS + 4 * nq + c4];
+                for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = hf ? 0.f : dd * sH[(dg + 32 * r) * kVS + 4 * nq + c4];
             }
-#pragma unroll 4
-            for (int i = 0; i < Lc; ++i) {
+            const int i0 = 32 * hf, i1 = min(Lc, i0 + 32);
+#pragma unroll 8
+            for (int i = i0; i < i1; ++i) {
                 const float4 v4 = *reinterpret_cast<const float4 *>(sVn + i * kVS + 4 * nq);
                 const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
@@ -516,11 +549,19 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
                     for (int c4 = 0; c4 < 4; ++c4) acc[r][c4] = fmaf(kf, vv[c4], acc[r][c4]);
                 }
             }
-            __syncthreads();  // every thread has read its h block (and the output its h) before any is rewritten
+            if (hf)
 #pragma unroll
-            for (int r = 0; r < RD; ++r)
+                for (int r = 0; r < RD; ++r)
+                    *reinterpret_cast<float4 *>(sPart + (dg + 32 * r) * kVS + 4 * nq) =
+                        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+            __syncthreads();  // the partials are in, and every read of h is done
+            if (!hf)
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) sH[(dg + 32 * r) * kVS + 4 * nq + c4] = acc[r][c4];
+                for (int r = 0; r < RD; ++r) {
+                    const float4 o4 = *reinterpret_cast<const float4 *>(sPart + (dg + 32 * r) * kVS + 4 * nq);
+                    *reinterpret_cast<float4 *>(sH + (dg + 32 * r) * kVS + 4 * nq) =
+                        make_float4(acc[r][0] + o4.x, acc[r][1] + o4.y, acc[r][2] + o4.z, acc[r][3] + o4.w);
+                }
         }
         __syncthreads();  // this buffer is refilled and v_new rewritten next
         if (L::NB == 1 && c + 1 < nchunks) fetch(c + 1);
@@ -528,7 +569,7 @@ __global__ void __launch_bounds__(kT) f32_serial_kernel(const FwdParams p, int v
     cp_async_wait<0>();
     __syncthreads();
     if (p.h_final) {
-        for (int e = tid; e < KP * kBV; e += kT) {
+        for (int e = tid; e < KP * kBV; e += kTS) {
             const int d = e / kBV, n = e % kBV, col = v0 + n;
             if (d < K && col < V) p.h_final[(((int64_t)s * H + hh) * K + d) * V + col] = sH[d * kVS + n];
         }
@@ -552,7 +593,7 @@ cudaError_t launch_serial_t(const FwdParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
     if (e != cudaSuccess) return e;
     dim3 grid(p.n_seq * p.H, (p.Vt + kBV - 1) / kBV);
-    kern<<<grid, kT, L::bytes, st>>>(p, f32_vp32(p.Vt));
+    kern<<<grid, kTS, L::bytes, st>>>(p, f32_vp32(p.Vt));
     return cudaGetLastError();
 }
 
