@@ -680,7 +680,7 @@ def main():
     if args.graph_replay > 0 and args.pass_ == "fwd":
         result["graph_replay"] = graph_replay(gdn, w, d, ws, args.graph_replay, fl, by, peaks)
     if not args.no_e2e:
-        e2e_s, h2d, d2h = e2e_measure(gdn, w, d, ws, max(3, min(args.steps, 10)), dev)
+        e2e_s, h2d, d2h = e2e_measure(gdn, w, d, ws, max(10, min(args.steps, 50)), dev)
         e2e_s = max_over_ranks(e2e_s, dist, dev)
         result["e2e"] = {"value": tokens * world / e2e_s, "unit": "tokens/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

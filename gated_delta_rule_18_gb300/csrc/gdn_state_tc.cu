@@ -11,8 +11,9 @@
 //   warps 0,1  with warps 4,5 (same TMEM lanes 0-63): v_new = u - Xw, each
 //   + 4,5      warp pair splitting a row's 64 columns in halves.
 //   warps 6-7  the output: read O for TMEM lanes 64-127 and store it; one of
-//              their threads also copies chunk c+2's operands once chunk
-//              c's last MMA is done.
+//              their threads also issues the operand copies once chunk c's
+//              last MMA is done: chunk c+3's [w; qg], u and dec, chunk
+//              c+2's kg^T and P.
 //   warp 8     lane 0 issues every tcgen05.mma and does nothing else, so it
 //              answers each hand-over at once and no v_new warp waits on
 //              its issuing.
@@ -35,9 +36,12 @@
 // the next chunk. [Xw; O] and v_new are double buffered. The intra-chunk
 // kernel stores w, qg, kg^T, P, u and dec as per-chunk images in the
 // shared-memory operand layouts, so a chunk's operands arrive by six 1-D bulk
-// async copies (cp.async.bulk), two chunks ahead (the MMA operands in two
-// stages, u in a ring of three and dec in a ring of four, so that every buffer
-// a copy overwrites was released before the copy is issued).
+// async copies (cp.async.bulk) in two rings, each with its own barriers:
+// ring A ([w; qg], u; dec in a ring of four) three chunks (two for the
+// 128-column tiles) ahead of the first product, ring B (kg^T, P) two chunks
+// ahead of the dh product, so that every buffer a copy overwrites was
+// released before the copy is issued. (With one two-slot ring for all six, a
+// chunk's first product waited ~280 cycles for its copies after h was ready.)
 //
 // Every wait is bounded: a wait that gives up raises a shared abort flag that
 // makes every role leave its loop, the kernel records GDN_DEVERR_TIMEOUT in
@@ -61,39 +65,42 @@ struct Cfg;
 template <>
 struct Cfg<64> {
     static constexpr int kThreads = 288;  // 9 warps
-    static constexpr int kURing = 3, kVnBuf = 2;
+    // [w; qg], u and dec are copied kRingA chunks ahead of their first
+    // product; kg^T and P, read later in a chunk, two chunks ahead
+    static constexpr int kRingA = 3, kVnBuf = 2;
     static constexpr uint32_t kTmemCols = 256;
 };
 template <>
 struct Cfg<128> {
     static constexpr int kThreads = 384;  // 12 warps
-    // a ring of two u slots and one v_new buffer fit the 128-column tiles in
-    // shared memory: chunk c+2's u copy follows chunk c's output product,
-    // after chunk c's v_new (the slot's last reader); chunk c+1's v_new is
-    // written after its first product, whose commit covers chunk c's products
-    // that read the v_new buffer (one issuing thread, products in order)
-    static constexpr int kURing = 2, kVnBuf = 1;
+    // rings of two [w; qg] / u slots and one v_new buffer fit the 128-column
+    // tiles in shared memory; chunk c+1's v_new is written after its first
+    // product, whose commit covers chunk c's products that read the v_new
+    // buffer (one issuing thread, products in order)
+    static constexpr int kRingA = 2, kVnBuf = 1;
     static constexpr uint32_t kTmemCols = 512;
 };
 
 template <int BV>
 struct Lay {
-    // one stage of MMA operands: w | qg | kg^T | zero block | P
+    // ring A (kRingA slots): w | qg, then ring B (two slots): kg^T | zero block | P
     static constexpr uint32_t w = 0;
     static constexpr uint32_t qg = w + kImgW;  // directly after w: [w; qg] is one M=128 operand
-    static constexpr uint32_t kg = qg + kImgW;
-    static constexpr uint32_t z = kg + kImgW;  // 64 zero rows stacked over P
+    static constexpr uint32_t a_slot = 2 * kImgW;
+    static constexpr uint32_t b_ring = Cfg<BV>::kRingA * a_slot;
+    static constexpr uint32_t kg = 0;              // within a ring B slot
+    static constexpr uint32_t z = kg + kImgW;      // 64 zero rows stacked over P
     static constexpr uint32_t pm = z + kImgP;
-    static constexpr uint32_t stage = pm + kImgP;
+    static constexpr uint32_t b_slot = pm + kImgP;
     static constexpr uint32_t u_slot = kImgU * (BV / 64);      // BV/64 u image tiles side by side
-    static constexpr uint32_t u = 2 * stage;                    // ring of u slots
-    static constexpr uint32_t dec = u + Cfg<BV>::kURing * u_slot;  // ring of 4 decay vectors
+    static constexpr uint32_t u = b_ring + 2 * b_slot;          // ring of u slots (ring A's chunks)
+    static constexpr uint32_t dec = u + Cfg<BV>::kRingA * u_slot;  // ring of 4 decay vectors
     static constexpr uint32_t h = dec + 4 * kDecB;              // h as the MMA B operand (MN-major)
     static constexpr uint32_t vn = h + BV * kKP * 2;            // v_new as the MMA B operand (MN-major)
     static constexpr uint32_t vn_bytes = 64 * BV * 2;
     static constexpr uint32_t bytes = vn + Cfg<BV>::kVnBuf * vn_bytes;
 };
-static_assert(Lay<128>::bytes <= 226 * 1024, "shared memory of the 128-column tiles");
+static_assert(Lay<64>::bytes <= 226 * 1024 && Lay<128>::bytes <= 226 * 1024, "shared memory per CTA");
 
 // TMEM columns: [Xw; O] of even / odd chunks [0,BV) / [BV,2BV) (lane = row:
 // 0-63 Xw, 64-127 O), dh [2BV,3BV)
@@ -119,7 +126,8 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     constexpr int kUT = BV / 64;                            // u image tiles per CTA
     constexpr int kOutW = BV == 64 ? 6 : 10;                // first output warp (TMEM lanes 64-127)
     extern __shared__ __align__(1024) unsigned char sm[];
-    __shared__ __align__(8) uint64_t bar_stage[2], bar_ofree[2];
+    constexpr int kRingA = Cfg<BV>::kRingA;
+    __shared__ __align__(8) uint64_t bar_ra[kRingA], bar_rb[2], bar_ofree[2];
     __shared__ __align__(8) uint64_t bar_h, bar_vn, bar_a, bar_dh, bar_o;
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     const int64_t bh = (int64_t)s * H + hh, n_bh = (int64_t)p.n_seq * H;
     const int gc0 = (p.cu_seqlens ? p.seq_chunk0[s] : s * ((p.T + kChunk - 1) / kChunk)) + cb;
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t b_st[2] = {smem_u32(&bar_stage[0]), smem_u32(&bar_stage[1])};
+    const uint32_t b_ra0 = smem_u32(&bar_ra[0]), b_rb0 = smem_u32(&bar_rb[0]);  // 8-byte barriers in a row
     const uint32_t b_of[2] = {smem_u32(&bar_ofree[0]), smem_u32(&bar_ofree[1])};
     const uint32_t b_h = smem_u32(&bar_h), b_vn = smem_u32(&bar_vn), b_a = smem_u32(&bar_a);
     const uint32_t b_dh = smem_u32(&bar_dh);
@@ -166,8 +174,9 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     }
     if (tid == 0) {
         abort_s = 0;
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_st[0]));
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_st[1]));
+        for (int x = 0; x < kRingA; ++x) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_ra0 + 8 * x));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_rb0));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(b_rb0 + 8));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[0]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 64;" ::"r"(b_of[1]));
         asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b_h), "r"(32 * 4 * kUT));  // recurrence
@@ -179,11 +188,11 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     }
     // the zero blocks stacked over P (never overwritten by the copies)
     for (int e = tid; e < (int)(kImgP / 16); e += kThreads) {
-        *reinterpret_cast<uint4 *>(sm + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(sm + Lay::stage + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + Lay::b_ring + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + Lay::b_ring + Lay::b_slot + Lay::z + 16 * e) = make_uint4(0, 0, 0, 0);
     }
     if (n_ut < kUT)  // u = 0 for transition columns and absent tiles: those parts stay zero
-        for (int e = tid; e < (int)(Cfg<BV>::kURing * Lay::u_slot / 16); e += kThreads)
+        for (int e = tid; e < (int)(kRingA * Lay::u_slot / 16); e += kThreads)
             *reinterpret_cast<uint4 *>(sm + Lay::u + 16 * e) = make_uint4(0, 0, 0, 0);
     fence_async_smem();
     tc_fence_before();
@@ -192,27 +201,36 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     const uint32_t tmem = tmem_base_s;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    // chunk c's operands: MMA operands into stage c&1, u into its ring slot,
-    // dec into ring slot c%4, all counted on the stage's barrier.
-    auto issue_stage = [&](int c) {
-        const int st = c & 1;
-        const uint32_t dst = sbase + st * Lay::stage;
+    // chunk c's operands of the first product and of v_new ([w; qg], u, dec)
+    // into ring A slot c % kRingA, counted on that slot's barrier (dec into
+    // ring slot c % 4)
+    auto issue_a = [&](int c) {
+        const uint32_t ra = (uint32_t)(c % kRingA), bar = b_ra0 + 8 * ra;
+        const uint32_t dst = sbase + ra * Lay::a_slot;
         const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
-        arrive_expect_tx(b_st[st], 3 * kImgW + kImgP + kDecB + (uint32_t)n_ut * kImgU);
-        bulk_g2s(dst + Lay::w, p.w_img + gch * kImgW, kImgW, b_st[st]);
-        bulk_g2s(dst + Lay::qg, p.qg_img + gch * kImgW, kImgW, b_st[st]);
-        bulk_g2s(dst + Lay::kg, p.kg_img + gch * kImgW, kImgW, b_st[st]);
-        bulk_g2s(dst + Lay::pm, p.p_img + gch * kImgP, kImgP, b_st[st]);
-        const uint32_t us = sbase + Lay::u + (uint32_t)(c % Cfg<BV>::kURing) * Lay::u_slot;
+        arrive_expect_tx(bar, 2 * kImgW + kDecB + (uint32_t)n_ut * kImgU);
+        bulk_g2s(dst + Lay::w, p.w_img + gch * kImgW, kImgW, bar);
+        bulk_g2s(dst + Lay::qg, p.qg_img + gch * kImgW, kImgW, bar);
+        const uint32_t us = sbase + Lay::u + ra * Lay::u_slot;
         for (int x = 0; x < n_ut; ++x)
-            bulk_g2s(us + x * kImgU, p.u_img + (gch * p.n_vt + vt * kUT + x) * kImgU, kImgU, b_st[st]);
-        bulk_g2s(sbase + Lay::dec + (uint32_t)(c % 4) * kDecB, p.dec + gch * kKP, kDecB, b_st[st]);
+            bulk_g2s(us + x * kImgU, p.u_img + (gch * p.n_vt + vt * kUT + x) * kImgU, kImgU, bar);
+        bulk_g2s(sbase + Lay::dec + (uint32_t)(c % 4) * kDecB, p.dec + gch * kKP, kDecB, bar);
+    };
+    // chunk c's operands of the dh and output products (kg^T, P) into ring B
+    // slot c & 1
+    auto issue_b = [&](int c) {
+        const uint32_t bar = b_rb0 + 8 * (c & 1);
+        const uint32_t dst = sbase + Lay::b_ring + (c & 1) * Lay::b_slot;
+        const size_t gch = (size_t)hh * p.max_chunks + gc0 + c;
+        arrive_expect_tx(bar, kImgW + kImgP);
+        bulk_g2s(dst + Lay::kg, p.kg_img + gch * kImgW, kImgW, bar);
+        bulk_g2s(dst + Lay::pm, p.p_img + gch * kImgP, kImgP, bar);
     };
     // v_new = u - Xw for token row i, columns c0 .. c0+31 (warps 0,1 / 4,5)
     // token row i, columns c0 .. c0+31 of chunk c's u, read ahead of the
     // product it is combined with
     auto load_u = [&](int c, int i, int c0, uint4 (&uv)[4]) {
-        const unsigned char *urow = sm + Lay::u + (c % Cfg<BV>::kURing) * Lay::u_slot + img_u_off(i, c0);
+        const unsigned char *urow = sm + Lay::u + (c % kRingA) * Lay::u_slot + img_u_off(i, c0);
 #pragma unroll
         for (int j = 0; j < 4; ++j) uv[j] = *reinterpret_cast<const uint4 *>(urow + 1024 * j);
     };
@@ -270,7 +288,6 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
         }
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c & 1;
             const uint32_t par = c & 1;
             // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16; its last
             // reader, chunk c-1's first product, finished before that chunk's dh
@@ -284,11 +301,11 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             fence_async_smem();
             arrive(b_h);
             if ((warp & 3) < 2) {  // v_new for token row r (TMEM lanes 0-63)
-                // Only the v_new warps wait for the stage: chunk c+2's copies
-                // into the same slot need this chunk's v_new first, so the
-                // barrier cannot run a phase ahead of them; warps 2-3 take
-                // dec after the dh product, which follows the stage.
-                ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));  // u and dec of chunk c
+                // Only the v_new warps (and the issuer) wait for ring A: chunk
+                // c+kRingA's copies into the same slot follow this chunk's
+                // v_new, so the barrier cannot run a phase ahead of them;
+                // warps 2-3 take dec after the dh product, which follows it.
+                ok = warp_all(wait_bar(b_ra0 + 8 * (c % kRingA), (c / kRingA) & 1, abort));  // u, dec of chunk c
                 if (!ok) break;
                 // 64 columns: columns 0..31 (the 64-column tile: its helpers
                 // take 32..63), or this group's 64 of the 128-column tile
@@ -341,9 +358,8 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
         // ------------------------------------- v_new helpers (columns 32..63)
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
-            const int st = c & 1;
             const uint32_t par = c & 1;
-            ok = warp_all(wait_bar(b_st[st], (c >> 1) & 1, abort));
+            ok = warp_all(wait_bar(b_ra0 + 8 * (c % kRingA), (c / kRingA) & 1, abort));
             uint4 uv[4];
             if (ok) load_u(c, tid - 128, 32, uv);
             ok = ok && warp_all(wait_bar(b_a, par, abort));
@@ -357,32 +373,37 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
         // ------------------------------------------------------ the MMA issuer
         bool ok = true;
         int c = 0;
-        // operand descriptors of both stages / buffers, built once: a K step
+        // operand descriptors of every slot / buffer, built once: a K step
         // of 16 advances the start address by 256 bytes, i.e. the descriptor
         // by 16 (the 14-bit address field cannot carry: shared addresses stay
         // below 256 KB)
-        const uint64_t dW0 = tc_sdesc(sbase + Lay::w, 128, 2048), dW1 = tc_sdesc(sbase + Lay::stage + Lay::w, 128, 2048);
-        const uint64_t dK0 = tc_sdesc(sbase + Lay::kg, 128, 1024), dK1 = tc_sdesc(sbase + Lay::stage + Lay::kg, 128, 1024);
-        const uint64_t dZ0 = tc_sdesc(sbase + Lay::z, 128, 1024), dZ1 = tc_sdesc(sbase + Lay::stage + Lay::z, 128, 1024);
+        const uint64_t dW0 = tc_sdesc(sbase + Lay::w, 128, 2048),
+                       dW1 = tc_sdesc(sbase + Lay::a_slot + Lay::w, 128, 2048),
+                       dW2 = tc_sdesc(sbase + (kRingA - 1) * Lay::a_slot + Lay::w, 128, 2048);
+        const uint32_t b1 = sbase + Lay::b_ring + Lay::b_slot;
+        const uint64_t dK0 = tc_sdesc(sbase + Lay::b_ring + Lay::kg, 128, 1024), dK1 = tc_sdesc(b1 + Lay::kg, 128, 1024);
+        const uint64_t dZ0 = tc_sdesc(sbase + Lay::b_ring + Lay::z, 128, 1024), dZ1 = tc_sdesc(b1 + Lay::z, 128, 1024);
         const uint64_t dV0 = tc_sdesc(sbase + Lay::vn, 128, 1024),
                        dV1 = tc_sdesc(sbase + Lay::vn + (Cfg<BV>::kVnBuf - 1) * Lay::vn_bytes, 128, 1024);
         const uint64_t dH = tc_sdesc(sbase + Lay::h, 128, 2048);
         for (; c < nchunks && ok; ++c) {
-            const int st = c & 1;
             const uint32_t par = c & 1;
+            const int ra = c % kRingA;
             const uint32_t dcol = kColD + par * BV;
-            const uint64_t dW = st ? dW1 : dW0, dK = st ? dK1 : dK0, dZ = st ? dZ1 : dZ0, dV = par ? dV1 : dV0;
-            // [Xw; O] = [w; qg] h once h_c is written and chunk c's operands
-            // landed (this accumulator set's previous user, chunk c-2, was read
-            // out before P v_new of chunk c-1 was issued, below)
-            ok = wait_bar(b_st[st], (c >> 1) & 1, abort) && wait_bar(b_h, par, abort);
+            const uint64_t dW = ra == 0 ? dW0 : ra == 1 ? dW1 : dW2;
+            const uint64_t dK = par ? dK1 : dK0, dZ = par ? dZ1 : dZ0, dV = par ? dV1 : dV0;
+            // [Xw; O] = [w; qg] h once h_c is written and chunk c's ring A
+            // copies landed (this accumulator set's previous user, chunk c-2,
+            // was read out before P v_new of chunk c-1 was issued, below)
+            ok = wait_bar(b_ra0 + 8 * ra, (c / kRingA) & 1, abort) && wait_bar(b_h, par, abort);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) tc_mma(tmem + dcol, dW + 16 * ks, dH + 16 * ks, kIdescK, ks > 0);
             tc_commit(b_a);
-            // dh = kg^T v_new, then [.; O] += [0; P] v_new
-            ok = wait_bar(b_vn, par, abort);
+            // dh = kg^T v_new, then [.; O] += [0; P] v_new (ring B: kg^T, P,
+            // landed long before; polled while v_new is still being formed)
+            ok = wait_bar(b_rb0 + 8 * par, (c >> 1) & 1, abort) && wait_bar(b_vn, par, abort);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
@@ -390,8 +411,8 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             tc_commit(b_dh);
             // b_o must not run two phases ahead of the output warps: chunk
             // c-1's output has to be read out before chunk c's is committed
-            // (this also keeps the output warps, which issue the operand
-            // copies, in step with the chain)
+            // (this also keeps the output warps, which issue the copies, in
+            // step with the chain)
             if (c >= 1) ok = wait_bar(b_of[(c - 1) & 1], ((c - 1) >> 1) & 1, abort);
             if (!ok) break;
 #pragma unroll
@@ -399,21 +420,25 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             tc_commit(b_o);
         }
         if (!ok) {
-            // drain what was issued: the last MMA groups and outstanding copies
+            // drain the last MMA groups (the copier drains the copies)
             *abort = 1;
             wait_bar(b_a, (uint32_t)c & 1, nullptr);
             wait_bar(b_o, (uint32_t)(c - 1) & 1, nullptr);
-            wait_bar(b_st[c & 1], (c >> 1) & 1, nullptr);
-            if (c + 1 < nchunks) wait_bar(b_st[(c + 1) & 1], ((c + 1) >> 1) & 1, nullptr);
-            if (c + 2 < nchunks) wait_bar(b_st[c & 1], ((c + 2) >> 1) & 1, nullptr);
         }
     } else if (warp == kOutW || warp == kOutW + 1) {
         // ------------------------------------------------ output warps (lanes 64-127)
         const int i = tid - 32 * kOutW;  // token row within the chunk
+        // one thread issues every copy once chunk c's last product is done:
+        // ring A for chunk c+kRingA (its slot's readers, chunk c's first
+        // product and v_new, are done), ring B for chunk c+2
         const bool copier = i == 0;
+        int a_hi = 0, b_hi = 0;  // chunks issued on rings A and B
         if (copier) {
-            if (nchunks > 0) issue_stage(0);
-            if (nchunks > 1) issue_stage(1);
+            for (; a_hi < 2 && a_hi < nchunks; ++a_hi) {
+                issue_a(a_hi);
+                if (b_hi < nchunks) issue_b(b_hi++);
+            }
+            for (; a_hi < kRingA && a_hi < nchunks; ++a_hi) issue_a(a_hi);
         }
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -444,11 +469,10 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
                 if (hv == 0) {
                     ok = warp_all(wait_bar(b_o, par, abort));
                     tc_fence_after();
-                    // chunk c's last MMA is done: stage c&1 may take chunk c+2's
-                    // MMA operands; u slot (c+2) of the ring was last read by an
-                    // earlier chunk's v_new and dec slot (c+2)%4 by chunk c-2's h
-                    // update, both finished
-                    if (copier && ok && c + 2 < nchunks) issue_stage(c + 2);
+                    if (copier && ok) {
+                        if (a_hi < nchunks) issue_a(a_hi++);  // chunk c + kRingA
+                        if (b_hi < nchunks) issue_b(b_hi++);  // chunk c + 2
+                    }
                 }
                 float t[64];
                 tc_ld64(tmem + lane_base + kColD + par * BV + 64 * hv, t);
@@ -508,6 +532,11 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
                     *dp = (p.accumulate ? dprev : 0.f) + dv;
                 }
             }
+        }
+        if (copier && !ok) {  // drain the outstanding copies
+            for (int j = max(0, a_hi - kRingA); j < a_hi; ++j)
+                wait_bar(b_ra0 + 8 * (j % kRingA), (j / kRingA) & 1, nullptr);
+            for (int j = max(0, b_hi - 2); j < b_hi; ++j) wait_bar(b_rb0 + 8 * (j & 1), (j >> 1) & 1, nullptr);
         }
     }
 
