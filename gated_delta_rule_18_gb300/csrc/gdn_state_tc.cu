@@ -115,6 +115,33 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
     return u;
 }
 
+// columns v1 .. v1+63 of one fp32 state row (n columns; columns past n read
+// as 0 and are not written), by 16-byte accesses when the row start is
+// 16-byte aligned and n a multiple of 4 (v1 is a multiple of 64)
+__device__ __forceinline__ void load_row64(float (&h)[64], const float *row, int v1, int n) {
+    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && (n & 3) == 0) {
+#pragma unroll
+        for (int x = 0; x < 64; x += 4) {
+            const float4 t = v1 + x < n ? *reinterpret_cast<const float4 *>(row + v1 + x) : make_float4(0.f, 0.f, 0.f, 0.f);
+            h[x] = t.x, h[x + 1] = t.y, h[x + 2] = t.z, h[x + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int x = 0; x < 64; ++x) h[x] = v1 + x < n ? row[v1 + x] : 0.f;
+    }
+}
+__device__ __forceinline__ void store_row64(float *row, const float (&h)[64], int v1, int n) {
+    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && (n & 3) == 0) {
+#pragma unroll
+        for (int x = 0; x < 64; x += 4)
+            if (v1 + x < n) *reinterpret_cast<float4 *>(row + v1 + x) = make_float4(h[x], h[x + 1], h[x + 2], h[x + 3]);
+    } else {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+            if (v1 + x < n) row[v1 + x] = h[x];
+    }
+}
+
 template <int BV>
 __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const FwdParams p) {
     using Lay = gdn::Lay<BV>;
@@ -277,14 +304,13 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
         if (p.summary) {  // E from h = 0, M from h = I
 #pragma unroll
             for (int c = 0; c < 64; ++c) h[c] = (trt && r < K && r == t0 + c) ? 1.f : 0.f;
-        } else if (p.h_in) {
-            const float *src = p.h_in + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) h[c] = (r < K && v1 + c < p.Vt) ? src[v1 + c] : 0.f;
+        } else if (p.h_in && r < K) {
+            load_row64(h, p.h_in + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt, v1, p.Vt);
+        } else if (p.h0 && r < K) {
+            load_row64(h, p.h0 + (bh * K + r) * V, v1, V);
         } else {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-                h[c] = (p.h0 && r < K && v1 + c < V) ? p.h0[(bh * K + r) * V + v1 + c] : 0.f;
+            for (int c = 0; c < 64; ++c) h[c] = 0.f;
         }
         bool ok = true;
         for (int c = 0; c < nchunks && ok; ++c) {
@@ -344,15 +370,10 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
                 for (int x = 0; x < 64; ++x)
                     if (t0 + x < K) dst[r * rs + (t0 + x) * cs] = h[x];
             } else {
-                float *dst = p.sum_ext + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt;
-#pragma unroll
-                for (int x = 0; x < 64; ++x)
-                    if (v1 + x < p.Vt) dst[v1 + x] = h[x];
+                store_row64(p.sum_ext + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt, h, v1, p.Vt);
             }
         } else if (ok && p.h_final && r < K && cb + nchunks == nall) {
-#pragma unroll
-            for (int x = 0; x < 64; ++x)
-                if (v1 + x < V) p.h_final[(bh * K + r) * V + v1 + x] = h[x];
+            store_row64(p.h_final + (bh * K + r) * V, h, v1, V);
         }
     } else if (BV == 64 && (warp == 4 || warp == 5)) {
         // ------------------------------------- v_new helpers (columns 32..63)

@@ -508,6 +508,33 @@ def test_repeated_long_runs_clean_and_deterministic(name):
             assert t.equal(cur[0], first[0]) and t.equal(cur[1], first[1])
 
 
+@pytest.mark.parametrize("tile", [0, 128])
+def test_state_rows_at_any_alignment(tile):
+    """The state pass moves h0 and h_final rows by 16-byte accesses where the
+    row starts allow it and element by element otherwise: h0 and h_final
+    given as views one float past an aligned start reproduce the aligned
+    run's output and final state bit for bit (both state tile widths)."""
+    import gated_delta_rule_18_gb300 as gdn
+    t = torch()
+    w = workloads.make(2, 200, 2, 128, 128, "bf16", seed=12, name="state_align", h0_std=0.5)
+    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    beta, g, h0 = f32_dev(w.beta), f32_dev(w.g), f32_dev(w.h0)
+    n = h0.numel()
+    h0_odd = t.empty(n + 1, dtype=t.float32, device=dev())[1:].view(h0.shape)
+    h0_odd.copy_(h0)
+    hf = t.empty_like(h0)
+    hf_odd = t.empty(n + 1, dtype=t.float32, device=dev())[1:].view(h0.shape)
+    assert h0_odd.data_ptr() % 16 == 4 and hf_odd.data_ptr() % 16 == 4
+    gdn.gdn_set_state_tile(tile)
+    try:
+        a = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h0=h0, h_final=hf, qk_l2norm=w.prep == "l2")
+        b = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h0=h0_odd, h_final=hf_odd, qk_l2norm=w.prep == "l2")
+        t.cuda.synchronize()
+    finally:
+        gdn.gdn_set_state_tile(0)
+    assert t.equal(a, b) and t.equal(hf, hf_odd)
+
+
 @pytest.fixture
 def wide_state_tiles():
     """Force the state pass's 128-column CTAs (both 64-column tiles of a head
