@@ -161,17 +161,23 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
     // the first kernel of a fixed-length launch clears the error word (the
     // chunk-table kernel does it for variable-length batches)
     if (!p.cu_seqlens && gid == 0 && hh == 0 && tid == 0) *p.err = 0;
-    int s, c;
+    int s, c, slot;  // slot: the chunk's image index within the head
     if (p.cu_seqlens) {
         if (gid >= *p.n_chunks) return;
         const int2 e = p.chunk_tab[gid];
         s = e.x;
         c = e.y;
+        slot = gid;
     } else {
+        // chunks in descending order over the grid, sequences next: the last
+        // CTAs write every sequence's first chunks, which the state pass
+        // reads first, so those images are still in L2 when it starts
         const int nts = (p.T + kChunk - 1) / kChunk;
-        s = gid / nts;
-        c = gid - s * nts;
-        if (s >= p.n_seq) return;
+        const int cr = gid / p.n_seq;
+        s = gid - cr * p.n_seq;
+        c = nts - 1 - cr;
+        if (c < 0) return;
+        slot = s * nts + c;
     }
     SeqInfo si;
     if (!seq_info(p, s, si)) return;
@@ -179,7 +185,7 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
     const int Lc = min(kChunk, si.len - pos0);
     if (Lc <= 0) return;
     const int K = p.K, H = p.H, V = p.V;
-    const size_t gch = (size_t)hh * p.max_chunks + gid;  // this chunk's image slot
+    const size_t gch = (size_t)hh * p.max_chunks + slot;
     const bf16 *q = (const bf16 *)p.q, *k = (const bf16 *)p.k, *v = (const bf16 *)p.v;
     const int64_t qk_base = si.b * p.qk_sb + hh * p.qk_sh;
     const int64_t v_base = si.b * p.v_sb + hh * p.v_sh;
