@@ -121,7 +121,9 @@ size_t gdn_workspace_size(int B, int T, int H, int K, int V, int n_seq,
  *   gk:   (B, T, H, K) fp32 per-key natural-log gate, or NULL.
  *   beta: (B, T, H) fp32.
  *   h0:   (n_seq, H, K, V) fp32 initial state (state at the end of a prefix,
- *         decayed by this call's first gate), or NULL for zero.
+ *         decayed by this call's first gate), or NULL for zero. h0 and
+ *         h_final may start at any 4-byte boundary; the bf16 path moves
+ *         their rows by 16-byte accesses when the start is 16-byte aligned.
  *   cu_seqlens: device int32 (n_seq + 1) offsets of packed sequences, or NULL
  *         for B dense sequences of length T (n_seq must then equal B).
  *         With cu_seqlens, B must be 1; chunks never cross sequences.
