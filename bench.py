@@ -36,6 +36,18 @@ METRIC = "GDN chunked fwd tokens/s & TFLOP/s at 1 GB300; % of roofline; vs CPU o
 DEFAULT_WORKLOAD = "causal_bf16_b4h16t4096d128"
 C = 64
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Nominal FP32 FFMA peak of the part (MEASURED_PEAKS.json has no fp32 figure):
+# 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz maximum SM clock.
+FP32_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12
+# L2 size used to decide whether inputs fit in L2 (then the timed steps are
+# each preceded by an L2 flush): 129 MB, the same number in both arms.
+L2_BYTES = 129 * 10 ** 6
+# The five workloads of the benchmark statement, reported side by side.
+CONFIGS = ["causal_f32_b1h2t256d64", "causal_bf16_b4h16t4096d128", "bidir_video_b2h16n8192d112",
+           "varlen_bf16_64seq_h32d128", "gk_bf16_b1h32t65536k128v256"]
+# the timed steps plus this much more of the same step, back to back, are
+# sampled for clocks (nvidia-smi needs a run of about a second to see it)
+CLOCK_SOAK_S = 1.5
 
 
 # ------------------------------------------------------------ work model ---
@@ -510,6 +522,158 @@ def oracle_sample(w):
 
 # ------------------------------------------------------------------ main ---
 
+def workload_input_bytes(w):
+    """Bytes of the workload's input tensors as they sit in HBM (qkv counted
+    once when q, k, v are views of it)."""
+    n = 0
+    for st in ((w.qkv,) if w.qkv is not None else (w.q, w.k, w.v)):
+        n += int(np.prod(st.shape)) * (2 if st.dtype == "bf16" else 4)
+    for a in (w.beta, w.g, w.gk, w.h0, w.g_bwd, w.beta_bwd, w.g_frame, w.cu_seqlens):
+        if a is not None:
+            n += int(np.asarray(a).size) * 4
+    if w.gate is not None:
+        n += int(np.prod(w.gate.shape)) * 2
+    return n
+
+
+def workload_tokens(w):
+    return w.B * w.T
+
+
+def config_of(w, name, world):
+    """The `config` object of the JSON line (the same in both arms) and
+    whether the timed steps are preceded by an L2 flush (inputs that fit in
+    L2)."""
+    in_bytes = workload_input_bytes(w)
+    flush = in_bytes <= L2_BYTES
+    cfg = {"workload": name, "B": w.B, "T": w.T, "H": w.H, "K": w.K, "V": w.V, "chunk": C,
+           "tokens_per_step_per_gpu": workload_tokens(w),
+           "l2": ("L2 flushed before every timed step (2 x L2 bytes written, outside the "
+                  "step's events)" if flush else "inputs larger than L2 (no flush)"),
+           "input_bytes": in_bytes, "parallelism": f"replicas x{world}"}
+    if w.segment_len is not None:
+        cfg.update(segment_len=w.segment_len, segments=seg_count(w))
+    return cfg, flush
+
+
+def path_roof(w, peaks):
+    """(FLOPs, bytes, roofline seconds, bound, compute peak TFLOP/s, its
+    source) of one step of w: bf16 workloads against the measured dense bf16
+    tensor peak, fp32 ones against the nominal FP32 FFMA peak."""
+    fl, by = path_work(w)
+    if w.dtype == "bf16":
+        pk, src = peaks["bf16_tflops"], "bf16_tflops"
+    else:
+        pk, src = FP32_TFLOPS_NOMINAL, "nominal fp32 FFMA (152 SMs x 128 lanes x 2 x 2.07 GHz)"
+    t_c, t_m = fl / (pk * 1e12), by / (peaks["hbm_gbs"] * 1e9)
+    return fl, by, max(t_c, t_m), ("hbm" if t_m >= t_c else ("tensor" if w.dtype == "bf16" else "alu")), pk, src
+
+
+def time_steps(gdn, w, d, ws, run, steps, stream, flush, scrub, prof_every):
+    """Device seconds of `steps` back-to-back steps (CUDA events on the
+    launching stream), with the library's per-launch event pairs on every
+    prof_every-th step. Inputs that fit in L2 get a write of twice the L2
+    size before every step, outside that step's own events."""
+    import torch
+    prof = lambda i: gdn.profile_enable(prof_every > 0 and i % prof_every == 0)
+    if not flush:
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(steps):
+            prof(i)
+            run(gdn, w, d, ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        sec = a.elapsed_time(b) / 1e3
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i, (ea, eb) in enumerate(evs):
+            scrub.zero_()
+            ea.record(stream)
+            prof(i)
+            run(gdn, w, d, ws)
+            eb.record(stream)
+        torch.cuda.synchronize()
+        sec = sum(ea.elapsed_time(eb) for ea, eb in evs) / 1e3
+    gdn.profile_enable(False)
+    return sec
+
+
+def dominant_roofline(w, per_kernel, prof_steps, by, peaks, peak_src, workload_name, T_override):
+    """The `roofline` object for the kernel with the largest device time:
+    achieved = the path's algorithmic bytes per launch (inputs read once,
+    outputs written once, divided over the launches of that kernel in one
+    step) / its average launch time."""
+    if not per_kernel:
+        return None
+    name, (ms_tot, n) = max(per_kernel.items(), key=lambda kv: kv[1][0])
+    avg_s = ms_tot / 1e3 / n
+    per_step = n / max(1, prof_steps)
+    alg = by / per_step
+    ach = alg / avg_s / 1e9
+    return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / peaks["hbm_gbs"],
+            "traffic": measured_traffic(name, workload_name) if T_override is None else None,
+            "algorithmic_bytes": alg,
+            "algorithmic_bytes_basis": "path minimum per launch: inputs read once, outputs "
+                                       "written once, h0 / h_final once, no intermediates",
+            "launches_per_step": per_step,
+            "kernel_image_bytes": kernel_bytes(w, name),
+            "avg_launch_us": avg_s * 1e6, "peak_source": f"{peak_src} hbm_gbs"}
+
+
+def sweep_configs(gdn, dev, stream, peaks, headline, rank, steps=10, warmup=3):
+    """Every workload of the benchmark statement timed the same way as the
+    headline (one entry per workload; the headline's own entry repeats its
+    numbers): ms per step, tokens/s, algorithmic TFLOP/s, the path roofline
+    fraction and the per-kernel times. The 256-token fp32 workload also gets
+    the fraction of a CUDA-graph replay of 64 back-to-back calls."""
+    import torch
+    out = {}
+    for name in CONFIGS:
+        if name == headline["config"]["workload"]:
+            out[name] = {k: headline[k] for k in ("ms_per_step", "value", "tflops")}
+            out[name]["tokens_per_s"] = out[name].pop("value")
+            out[name]["path_frac"] = headline["path_roofline"]["frac"]
+            out[name]["kernels_us"] = {k: v["avg_us"] for k, v in headline["kernels"].items()}
+            out[name]["steps"] = headline["steps"]
+            continue
+        w = workloads.build(name, seed=rank)
+        w = resolve_segments(gdn, w, dev)
+        d = device_inputs(w, dev)
+        ws = workspace_for(gdn, w, dev)
+        _, flush = config_of(w, name, 1)
+        scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
+        for _ in range(warmup):
+            run_step(gdn, w, d, ws)
+        torch.cuda.synchronize()
+        gdn.profile_collect()
+        sec = time_steps(gdn, w, d, ws, run_step, steps, stream, flush, scrub, 0)
+        # per-kernel times from a second run with an event pair around every launch
+        time_steps(gdn, w, d, ws, run_step, min(steps, 5), stream, flush, scrub, 1)
+        per_kernel = gdn.profile_collect()
+        step_s = sec / steps
+        fl, by, roof_t, bound, pk, src = path_roof(w, peaks)
+        e = {"ms_per_step": step_s * 1e3, "tokens_per_s": workload_tokens(w) / step_s,
+             "tflops": fl / step_s / 1e12, "path_frac": roof_t / step_s, "path_roofline_us": roof_t * 1e6,
+             "bound": bound, "compute_peak_tflops": pk, "compute_peak_source": src,
+             "kernels_us": {k: v[0] / v[1] * 1e3 for k, v in per_kernel.items()},
+             "steps": steps, "l2": "flushed before every step" if flush else "inputs larger than L2",
+             "kernel_timing": "per-launch event pairs in a separate run of the same steps"}
+        if w.dtype != "bf16":
+            g = graph_replay(gdn, w, d, ws, 64, fl, by, {**peaks, "bf16_tflops": pk})
+            e["graph_us_per_call"] = g["us_per_call"]
+            e["path_frac_graph"] = roof_t / (g["us_per_call"] * 1e-6)
+            e["graph_note"] = "64 back-to-back calls in one CUDA graph, warm L2"
+        out[name] = e
+        del d, ws, scrub
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -519,6 +683,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the side-by-side timing of every benchmark workload")
     ap.add_argument("--T", type=int, default=None,
                     help="override the token count of a dense workload (smaller profiling captures)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
@@ -563,22 +729,17 @@ def main():
             rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
         ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V), dtype=torch.uint8,
                          device=dev)
-        args.no_e2e = args.no_cpu_baseline = True
+        args.no_e2e = args.no_cpu_baseline = args.no_configs = True
 
-        def run_step(gdn, w, d, ws):  # noqa: F811 -- the timed step of this pass
+        def run(gdn, w, d, ws):  # the timed step of this pass
             return gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dout"],
                                      h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws)
     else:
         ws = workspace_for(gdn, w, dev)
-        run_step = globals()["run_step"]
+        run = run_step
     stream = torch.cuda.current_stream()
-
-    # L2 hygiene: a workload whose inputs exceed L2 needs no flush between
-    # steps; smaller ones get an L2-sized write before every timed step
-    in_bytes = sum(t.numel() * t.element_size() for t in d.values() if torch.is_tensor(t))
-    l2_bytes = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 10 ** 6
-    flush = in_bytes <= l2_bytes
-    scrub = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
+    config, flush = config_of(w, args.workload, world)
+    scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
     sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
@@ -586,7 +747,7 @@ def main():
     time.sleep(0.3)
     # the warm-up steps run right before the timed ones (no idle gap between)
     for _ in range(warmup):
-        run_step(gdn, w, d, ws)
+        run(gdn, w, d, ws)
     torch.cuda.synchronize()
     gdn.profile_collect()
     if dist:
@@ -596,79 +757,45 @@ def main():
     # the library's per-launch event pairs (the per-kernel times) are taken on
     # every PROFILE_EVERY-th timed step: an event pair waits for the kernel
     # before it to drain, which costs ~2 us per kernel boundary
-    prof = lambda i: gdn.profile_enable(i % PROFILE_EVERY == 0)
-    if not flush:
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(args.steps):
-            prof(i)
-            run_step(gdn, w, d, ws)
-        b.record(stream)
-        torch.cuda.synchronize()
-        sec = a.elapsed_time(b) / 1e3
-    else:
-        # inputs that fit in L2: write a buffer twice the L2 size before each
-        # step, outside that step's own events
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i, (ea, eb) in enumerate(evs):
-            scrub.zero_()
-            ea.record(stream)
-            prof(i)
-            run_step(gdn, w, d, ws)
-            eb.record(stream)
-        torch.cuda.synchronize()
-        sec = sum(ea.elapsed_time(eb) for ea, eb in evs) / 1e3
-    gdn.profile_enable(False)
+    sec = time_steps(gdn, w, d, ws, run, args.steps, stream, flush, scrub, PROFILE_EVERY)
     if dist:
         dist.barrier()
     launches = gdn.launch_count() - launches0
-    clocks = sampler.stop()
     per_kernel = gdn.profile_collect()
+    # the same step back to back right after the timed ones, until the sampled
+    # window is CLOCK_SOAK_S long: the clock record covers the timed steps and
+    # this run (nvidia-smi samples every 100 ms), and its step time is a
+    # cross-check of the headline
+    soak_steps, soak_sec, t0 = 0, 0.0, time.perf_counter()
+    while time.perf_counter() - t0 < CLOCK_SOAK_S and not flush:
+        n = 50
+        soak_sec += time_steps(gdn, w, d, ws, run, n, stream, False, None, 0)
+        soak_steps += n
+    clocks = sampler.stop()
+    clocks["window"] = (f"warm-up, the {args.steps} timed steps and {soak_steps} more of the same "
+                        "step back to back")
     sec = max_over_ranks(sec, dist, dev)
     ms_per_step = sec / args.steps * 1e3
-    tokens = w.B * w.T
+    tokens = workload_tokens(w)
     value = job_tokens_per_s(tokens, world, args.steps, sec)
 
-    fl, by = path_work(w)
     peaks, peak_src = load_peaks()
     step_s = sec / args.steps
-    roof_t = max(fl / (peaks["bf16_tflops"] * 1e12), by / (peaks["hbm_gbs"] * 1e9))
-
-    # dominant kernel: largest total device time in the timed region
-    dom = max(per_kernel.items(), key=lambda kv: kv[1][0]) if per_kernel else None
-    roofline = None
-    if dom:
-        name, (ms_tot, n) = dom
-        avg_s = ms_tot / 1e3 / n
-        kb = kernel_bytes(w, name)
-        ach = kb / avg_s / 1e9 if kb else None
-        roofline = {"bound": "hbm", "kernel": name, "achieved": ach, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": (ach / peaks["hbm_gbs"]) if ach else None,
-                    "traffic": measured_traffic(name, args.workload) if args.T is None else None,
-                    "algorithmic_bytes": kb, "avg_launch_us": avg_s * 1e6,
-                    "peak_source": f"{peak_src} hbm_gbs"}
+    fl, by, roof_t, bound, pk, pk_src = path_roof(w, peaks)
+    prof_steps = -(-args.steps // PROFILE_EVERY)
 
     result = {
         "metric": METRIC if args.pass_ == "fwd" else METRIC_BWD, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "K": w.K,
-                   "V": w.V, "chunk": C, "tokens_per_step_per_gpu": tokens,
-                   "l2": ("L2 flushed before every timed step (2 x L2 bytes written, outside the "
-                          "step's events)" if flush else "inputs larger than L2 (no flush)"),
-                   "input_bytes": in_bytes,
-                   "parallelism": f"replicas x{world}",
-                   **({"segment_len": w.segment_len, "segments": seg_count(w)}
-                      if w.segment_len is not None else {})},
+        "config": config,
         "tflops": fl * world / step_s / 1e12,
-        "path_roofline": {"bound": "hbm" if by / peaks["hbm_gbs"] > fl / peaks["bf16_tflops"] / 1e3
-                          else "tensor", "min_bytes": by, "flops": fl,
+        "path_roofline": {"bound": bound, "min_bytes": by, "flops": fl,
                           "roofline_ms": roof_t * 1e3, "frac": roof_t / step_s,
-                          "peak_source": peak_src},
-        "roofline": roofline,
+                          "peak_source": f"{peak_src} hbm_gbs; compute {pk_src}"},
+        "roofline": dominant_roofline(w, per_kernel, prof_steps, by, peaks, peak_src,
+                                      args.workload, args.T) if args.pass_ == "fwd" else None,
         "kernels_sampled": f"per-launch CUDA event pairs on every {PROFILE_EVERY}th timed step",
         "kernels": {k2: {"avg_us": v2[0] / v2[1] * 1e3, "launches": v2[1],
                          "share": v2[0] / max(1e-9, sum(x[0] for x in per_kernel.values()))}
@@ -677,6 +804,8 @@ def main():
         "clocks": clocks,
         "impl": "ours",
     }
+    if soak_steps:
+        result["ms_per_step_sustained"] = soak_sec / soak_steps * 1e3
     if args.graph_replay > 0 and args.pass_ == "fwd":
         result["graph_replay"] = graph_replay(gdn, w, d, ws, args.graph_replay, fl, by, peaks)
     if not args.no_e2e:
@@ -689,6 +818,11 @@ def main():
         tok_s, csec, cores, desc = oracle_sample(w)
         result["cpu_baseline"] = {"value": tok_s, "unit": "tokens/s", "cores": cores,
                                   "kind": "oracle", "sample": desc, "seconds": csec}
+    if world == 1 and not args.no_configs and args.T is None and args.segment_len is None \
+            and args.workload in CONFIGS:
+        del d, ws, scrub
+        torch.cuda.empty_cache()
+        result["configs"] = sweep_configs(gdn, dev, stream, peaks, result, rank)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -717,7 +851,7 @@ def main_reference(args, warmup, rank, world):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": wall / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload},
+        "data": "synthetic", "config": config_of(w, args.workload, world)[0],
         "impl": "reference",
         "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": desc, "value": value},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,

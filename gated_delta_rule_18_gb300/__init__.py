@@ -19,7 +19,8 @@ from .build import LIB
 
 __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
            "gdn_merge", "gdn_frame_fwd", "gdn_frame_workspace_size", "gdn_workspace_size",
-           "gdn_status_string", "gdn_last_device_error", "gdn_forward", "lib",
+           "gdn_status_string", "gdn_last_device_error", "gdn_noalloc_last_device_error",
+           "gdn_set_stall_test", "gdn_forward", "lib",
            "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect", "gdn_set_state_tile",
            "launch_count", "kernel_names"]
 
@@ -99,6 +100,10 @@ def lib():
     L.gdn_merge.argtypes = [P, TensorDesc, P, P, TensorDesc, P, TensorDesc, I, I, I, I, F, P]
     L.gdn_last_device_error.restype = I
     L.gdn_last_device_error.argtypes = [P, P, ctypes.POINTER(I)]
+    L.gdn_noalloc_last_device_error.restype = I
+    L.gdn_noalloc_last_device_error.argtypes = [P, ctypes.POINTER(I)]
+    L.gdn_set_stall_test.restype = None
+    L.gdn_set_stall_test.argtypes = [I, I]
     L.gdn_kernel_kinds.restype = I
     L.gdn_kernel_kinds.argtypes = []
     L.gdn_kernel_name.restype = ctypes.c_char_p
@@ -424,12 +429,30 @@ def gdn_frame_fwd(q, k, v, beta, g_frame, frame, out=None, den=None, h0=None, h_
 
 
 def gdn_last_device_error(workspace, stream=None) -> int:
-    """Synchronise, read and clear the device error word; returns it."""
+    """Synchronise, read and clear the device error word; returns it
+    (GDN_DEVERR_* bits: 1 malformed cu_seqlens, 2 a bounded wait gave up)."""
     w = ctypes.c_int(0)
     st = lib().gdn_last_device_error(_ptr(workspace), _stream(stream), ctypes.byref(w))
-    if st not in (0, 9):
+    if st not in (0, 7, 9):
         raise GDNError(st, "gdn_last_device_error")
     return w.value
+
+
+def gdn_noalloc_last_device_error(stream=None) -> int:
+    """gdn_last_device_error for gdn_chunk_fwd_noalloc's built-in buffer on
+    the current device; returns the word."""
+    w = ctypes.c_int(0)
+    st = lib().gdn_noalloc_last_device_error(_stream(stream), ctypes.byref(w))
+    if st not in (0, 7, 9):
+        raise GDNError(st, "gdn_noalloc_last_device_error")
+    return w.value
+
+
+def gdn_set_stall_test(cta: int = -1, limit_us: int = 1000) -> None:
+    """Testing aid of the time-out path (see include/gdn.h): block `cta` of
+    later intra-chunk and state-pass launches stalls, gives up after about
+    limit_us and reports a time-out; cta < 0 turns it off."""
+    lib().gdn_set_stall_test(int(cta), int(limit_us))
 
 
 def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,

@@ -38,6 +38,8 @@ Profiler &prof() {
     return *p;
 }
 std::atomic<long long> g_launches{0};
+// the testing aid of gdn_set_stall_test (-1: off)
+std::atomic<int> g_stall_cta{-1}, g_stall_us{1000};
 
 cudaEvent_t take_event(Profiler &P) {
     if (!P.pool.empty()) {
@@ -292,7 +294,16 @@ gdn_status fwd_setup(const void *q, const void *k, gdn_tensor_desc qkd, const vo
     p.Vt = L.Vt;
     p.max_chunks = L.max_chunks;
     p.n_vt = L.n_vt;
+    p.stall_cta = g_stall_cta.load();
+    p.stall_us = g_stall_us.load();
     return GDN_OK;
+}
+
+// The device error word describes one call: it is cleared in stream order
+// before the call's first kernel, so no kernel of the call clears it while
+// another block may already have recorded an error.
+cudaError_t clear_err(const gdn::FwdParams &p, cudaStream_t s) {
+    return cudaMemsetAsync(p.err, 0, sizeof(int), s);
 }
 
 void bind_ws(unsigned char *ws, const Ws &L, gdn::FwdParams &p) {
@@ -354,8 +365,8 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     const int perkey = gk != nullptr;
     const int varlen = cu_seqlens != nullptr;
 
-    cudaError_t e = cudaSuccess;
-    if (varlen) e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
+    cudaError_t e = clear_err(p, stream);
+    if (e == cudaSuccess && varlen) e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     if (qkd.dtype == GDN_F32) {
         e = launch_f32(p, L.KP, perkey, stream);
@@ -396,7 +407,8 @@ gdn_status gdn_chunk_fwd_seg(const void *q, const void *k, gdn_tensor_desc qkd, 
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     bind_ws(ws, L, p);
     const int perkey = gk != nullptr;
-    cudaError_t e = cudaSuccess;
+    cudaError_t e = clear_err(p, stream);
+    if (e != cudaSuccess) return GDN_ERR_CUDA;
     if (L.max_chunks > 0) {
         e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, perkey, stream); });
         if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -473,7 +485,9 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v, g
     if (!ws_ok(workspace, ws_bytes, L.total)) return GDN_ERR_WORKSPACE;
     if (T == 0) return GDN_OK;
     bind_ws(static_cast<unsigned char *>(workspace), L, p);
-    cudaError_t e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, gk != nullptr, stream); });
+    cudaError_t e = clear_err(p, stream);
+    if (e == cudaSuccess)
+        e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, gk != nullptr, stream); });
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     p.seg_chunks = S.seg_chunks;
     p.summary = 1;
@@ -555,7 +569,8 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     bind_ws(ws, L, p);
     p.h_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.h);
     p.vn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.vn);
-    cudaError_t e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, 0, stream); });
+    cudaError_t e = clear_err(p, stream);
+    if (e == cudaSuccess) e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, 0, stream); });
     if (e == cudaSuccess) e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
     if (e != cudaSuccess) return GDN_ERR_CUDA;
     gdn::BwdParams b{};
@@ -671,6 +686,7 @@ gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd
     if (st != GDN_OK) return st;
     bind_ws(ws + S.fwd, L, pf);
     bind_ws(ws + S.rev, L, pr);
+    pr.err = pf.err;  // both directions report into the word at the workspace start
     const int perkey = gk != nullptr, varlen = cu_seqlens != nullptr;
 
     std::lock_guard<std::mutex> lock(side_mutex());
@@ -695,7 +711,8 @@ gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd
     // the two intra passes share the whole GPU and the two state passes (one
     // CTA per SM each) then start together, instead of one direction's state
     // CTAs taking SMs from the other's intra pass.
-    cudaError_t e = cudaEventRecord(side->fork, stream);
+    cudaError_t e = clear_err(pf, stream);
+    if (e == cudaSuccess) e = cudaEventRecord(side->fork, stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
     if (e == cudaSuccess) e = first(pr, side->s);
     if (e == cudaSuccess) e = first(pf, stream);
@@ -842,6 +859,11 @@ const char *gdn_kernel_name(int kind) {
 }
 
 void gdn_set_state_tile(int bv) { gdn::set_state_tile(bv); }
+
+void gdn_set_stall_test(int cta, int limit_us) {
+    g_stall_us.store(limit_us > 0 ? limit_us : 1);
+    g_stall_cta.store(cta >= 0 ? cta : -1);
+}
 
 void gdn_profile_enable(int on) {
     Profiler &P = prof();

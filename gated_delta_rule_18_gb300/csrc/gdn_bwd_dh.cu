@@ -29,7 +29,6 @@ using bf16 = __nv_bfloat16;
 constexpr int kThreads = 256;
 constexpr int kL6 = 64 + 8;  // row stride of a 64-column tile
 constexpr uint32_t kStageBytes = kImgP + 3 * kImgW + kDecB;
-constexpr int kDevErrTimeout = 2;  // the error word's time-out bit
 
 struct DhStage {
     unsigned char p[kImgP];   // P image

@@ -59,7 +59,6 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
     const int s = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     const int v0 = blockIdx.y * kBVf;
     const int K = p.K, V = p.V, H = p.H;
-    if (!p.cu_seqlens && blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) *p.err = 0;
     if (p.cu_seqlens && *p.n_chunks < 0) return;  // cu_seqlens rejected on the device
     SeqInfo si;
     if (!seq_info(p, s, si)) return;

@@ -54,7 +54,6 @@ __global__ void __launch_bounds__(kT) f32_prep_kernel(const FwdParams p, int vp3
     float *sA = sm + L::a, *sT = sm + L::t, *sP = sm + L::pm, *sX = sm + L::x, *sR = sm + L::r;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hh = blockIdx.x % p.H, gid = blockIdx.x / p.H;
-    if (!p.cu_seqlens && gid == 0 && hh == 0 && tid == 0) *p.err = 0;
     int s, c;
     if (p.cu_seqlens) {
         if (gid >= *p.n_chunks) return;

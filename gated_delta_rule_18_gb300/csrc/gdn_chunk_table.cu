@@ -26,7 +26,8 @@ __global__ void __launch_bounds__(1024) chunk_table_kernel(const int32_t *__rest
     for (int s = tid; s < n_seq; s += blockDim.x)
         if (cu[s + 1] < cu[s]) bad = 1;
     __syncthreads();
-    if (tid == 0) *err = bad ? 1 : 0;  // the word describes this call only
+    // (the host clears the word on the stream before a call's first kernel)
+    if (tid == 0 && bad) atomicOr(err, 1);
     if (bad) {
         if (tid == 0) *n_chunks = -1;
         return;

@@ -66,6 +66,9 @@ struct FwdParams {
     // the state entering every chunk and the chunk's v_new, bf16, indexed
     // [head][global chunk]: h_snap (K, V) rows, vn_snap (64, V) rows.
     __nv_bfloat16 *h_snap, *vn_snap;
+    // testing aid for the bounded-wait path: block stall_cta (linear index)
+    // of the intra-chunk and state kernels stalls instead of working (-1: off)
+    int stall_cta, stall_us;
 };
 
 // Everything the backward kernels need (dense batches, scalar gate). The
@@ -228,6 +231,40 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             }
         }
     }
+}
+
+// Device error word bits (the same values as GDN_DEVERR_* in gdn.h).
+constexpr int kDevErrSeqlens = 1, kDevErrTimeout = 2;
+
+// Testing aid for the time-out path: the block whose linear index is
+// p.stall_cta waits on an mbarrier that nothing completes until its
+// p.stall_us limit runs out, records a time-out in the error word and
+// reports true, so that the kernel leaves before issuing any copy or MMA.
+// Every other block returns false at once. The decision depends only on the
+// block index, so a block's threads all take the same branch.
+static __device__ __noinline__ bool stall_test(const FwdParams &p) {
+    const int b = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+    if (p.stall_cta < 0 || b != p.stall_cta) return false;
+    __shared__ __align__(8) uint64_t never;
+    const uint32_t bar = smem_u32(&never);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        const uint64_t t0 = now_ns(), lim = (uint64_t)max(p.stall_us, 1) * 1000ull;
+        for (;;) {
+            uint32_t ok;
+            asm volatile(
+                "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+                " selp.u32 %0, 1, 0, q;\n}"
+                : "=r"(ok)
+                : "r"(bar), "r"(0u)
+                : "memory");
+            if (ok || now_ns() - t0 > lim) break;
+        }
+        atomicOr(p.err, kDevErrTimeout);
+    }
+    __syncthreads();
+    return true;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *smem) {

@@ -52,7 +52,6 @@ constexpr int kThreads = 128;
 constexpr int kBS = 24;   // bf16 row stride of a 16x16 block (A below the diagonal, T)
 constexpr int kTSet = 4 * 16 * kBS;  // one set of T's four diagonal blocks
 constexpr int kAdS = 17;  // fp32 row stride of A's diagonal blocks
-constexpr int kDevErrTimeout = 2;
 
 // Shared memory. The scalar-gate kernel copies the value tile into the q
 // tile's space once qg is written; the per-key kernel keeps it apart (its
@@ -158,9 +157,7 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
     // heads vary fastest across the grid, so CTAs resident together read the
     // same tokens of all heads (whole DRAM pages) rather than one head's rows
     const int hh = blockIdx.x % p.H, gid = blockIdx.x / p.H;
-    // the first kernel of a fixed-length launch clears the error word (the
-    // chunk-table kernel does it for variable-length batches)
-    if (!p.cu_seqlens && gid == 0 && hh == 0 && tid == 0) *p.err = 0;
+    if (stall_test(p)) return;
     int s, c, slot;  // slot: the chunk's image index within the head
     if (p.cu_seqlens) {
         if (gid >= *p.n_chunks) return;

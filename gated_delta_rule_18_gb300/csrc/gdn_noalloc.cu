@@ -48,14 +48,30 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(
     const int32_t *cu_seqlens, int n_seq, void *out, gdn_tensor_desc od, float *h_final,
     float *den_out, int B, int T, int H, int K, int V, int chunk, int reverse, int flags,
     cudaStream_t stream) {
+    // gdn_chunk_fwd's own argument checks first: given no workspace it
+    // launches nothing and returns GDN_ERR_WORKSPACE exactly when every
+    // argument check passed, so a bad argument gets the status gdn_chunk_fwd
+    // would give it
+    const gdn_status pre = gdn_chunk_fwd(q, k, qkd, v, vd, g, gk, beta, h0, cu_seqlens, n_seq, out,
+                                         od, h_final, den_out, B, T, H, K, V, chunk, reverse, flags,
+                                         nullptr, 0, stream);
+    if (pre != GDN_ERR_WORKSPACE) return pre;
     const size_t need = gdn_workspace_size(B, T, H, K, V, n_seq, cu_seqlens != nullptr,
                                            qkd.dtype, den_out != nullptr);
-    if (need == 0) return GDN_ERR_SHAPE;
-    if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
+    if (need == 0 || need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_WORKSPACE;
     void *scratch = nullptr;
     const gdn_status st = scratch_address(&scratch);
     if (st != GDN_OK) return st;
     return gdn_chunk_fwd(q, k, qkd, v, vd, g, gk, beta, h0, cu_seqlens, n_seq, out, od, h_final,
                          den_out, B, T, H, K, V, chunk, reverse, flags, scratch,
                          (size_t)GDN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// The error word sits at the start of the built-in buffer, where
+// gdn_chunk_fwd keeps it in any workspace.
+extern "C" gdn_status gdn_noalloc_last_device_error(cudaStream_t stream, int *word) {
+    void *scratch = nullptr;
+    const gdn_status st = scratch_address(&scratch);
+    if (st != GDN_OK) return st;
+    return gdn_last_device_error(scratch, stream, word);
 }

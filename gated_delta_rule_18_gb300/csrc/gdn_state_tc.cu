@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     // u image tiles of this CTA present in the images (a 128-column CTA over
     // an odd last tile keeps the second half of its u slots zero)
     const int n_ut = trt ? 0 : min(kUT, p.n_vt - vt * kUT);
+    if (stall_test(p)) return;
     if (p.cu_seqlens && *p.n_chunks < 0) return;
     SeqInfo si;
     if (!seq_info(p, s, si)) return;
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && *abort) atomicOr(p.err, 2);
+    if (tid == 0 && *abort) atomicOr(p.err, kDevErrTimeout);
     if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 

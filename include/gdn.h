@@ -166,8 +166,10 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd,
  * until the process exits). Nothing is allocated: no cudaMalloc/cudaFree and
  * no allocating library routine is called (leave gdn_profile_enable off,
  * since profiling creates CUDA events).
- *   - Problems whose gdn_workspace_size() exceeds GDN_NOALLOC_SCRATCH_BYTES
- *     are rejected with GDN_ERR_WORKSPACE before anything runs.
+ *   - Argument checks are gdn_chunk_fwd's and return its status codes.
+ *     Problems that pass them but whose gdn_workspace_size() exceeds
+ *     GDN_NOALLOC_SCRATCH_BYTES are rejected with GDN_ERR_WORKSPACE before
+ *     anything runs.
  *   - The first call on each device looks up the buffer's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
@@ -176,9 +178,9 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd,
  *     cleared between calls. Calls that overlap on the GPU (different
  *     streams, or different host threads on the same device) race on the
  *     buffer: serialise them.
- *   - The device error word of gdn_last_device_error() lives in the buffer
- *     too; it is not reachable from outside, so device-side argument errors
- *     of this entry point are not reported.
+ *   - The device error word (malformed cu_seqlens, bounded waits that gave
+ *     up) lives in the buffer too: read it with
+ *     gdn_noalloc_last_device_error() after the call.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
 gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k,
@@ -190,6 +192,15 @@ gdn_status gdn_chunk_fwd_noalloc(const void *q, const void *k,
                                  float *h_final, float *den_out, int B, int T,
                                  int H, int K, int V, int chunk, int reverse,
                                  int flags, cudaStream_t stream);
+
+/*
+ * gdn_noalloc_last_device_error -- gdn_last_device_error for the built-in
+ * buffer of gdn_chunk_fwd_noalloc on the current device: synchronise
+ * `stream`, store the error word in *word (may be NULL), clear it, and
+ * return GDN_ERR_TIMEOUT / GDN_ERR_DEVICE / GDN_OK as gdn_last_device_error
+ * does. Allocates nothing.
+ */
+gdn_status gdn_noalloc_last_device_error(cudaStream_t stream, int *word);
 
 /*
  * gdn_seg_workspace_size / gdn_chunk_fwd_seg -- gdn_chunk_fwd for dense
@@ -380,7 +391,9 @@ const char *gdn_status_string(gdn_status s);
  * that gdn_chunk_fwd keeps in `workspace`, store it in *word (GDN_DEVERR_*
  * bits, may be NULL) and clear it. Returns GDN_ERR_TIMEOUT if a bounded
  * wait gave up, GDN_ERR_DEVICE for other set bits, GDN_ERR_CUDA on a CUDA
- * failure, else GDN_OK.
+ * failure, else GDN_OK. The word describes the last call that used this
+ * workspace: every call clears it on its stream before its first kernel
+ * (both directions of gdn_chunk_fwd_bidir report into the same word).
  */
 gdn_status gdn_last_device_error(void *workspace, cudaStream_t stream,
                                  int *word);
@@ -411,6 +424,18 @@ long long gdn_launch_count(void);
  *   compute the same recurrence (results agree to rounding order).
  */
 void gdn_set_state_tile(int bv);
+
+/*
+ * Testing aid for the device-side time-out path; the pages have no
+ * counterpart. While set (cta >= 0), the block with linear index `cta` of
+ * every later intra-chunk and state-pass launch of the bf16 path waits on a
+ * barrier that nothing completes, gives up after about `limit_us`
+ * microseconds, records GDN_DEVERR_TIMEOUT in the call's error word and
+ * leaves without issuing any copy or tensor-core operation; every other
+ * block works as usual (the call's results are then incomplete).
+ * cta < 0 turns it off (the default). Process-wide; affects later launches.
+ */
+void gdn_set_stall_test(int cta, int limit_us);
 
 #ifdef __cplusplus
 }

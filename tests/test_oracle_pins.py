@@ -595,3 +595,119 @@ def test_gradients_beta0_closed_form():
     terms = e * np.einsum("tk,kv,tv->t", q, h0, dd)
     terms[-1] += e[-1] * np.sum(dhf[0, 0] * h0)
     np.testing.assert_allclose(res["dg"][0, :, 0], np.cumsum(terms[::-1])[::-1], rtol=1e-12)
+
+
+# ------------------------------------------ denominators and the forward glue ---
+# SANA `fused_gdn.py` page, `_fused_gdn_kernel`: the z state (`z_hat`, `dz`,
+# `den`) runs the same rule as the numerator with a ones value, in either
+# direction (REVERSE); `fused_bigdn_func` sums both directions of num and den.
+
+def test_orthogonal_keys_reverse_den_closed_form():
+    """Reverse denominator, mutually orthogonal keys: the reverse closed form
+    with v = 1,  den_p = sum_{j>p} beta_j (q_p . k_j) exp(g_{p+1} + ... + g_{j-1})."""
+    rng = np.random.default_rng(31)
+    T, K = 9, 11
+    k = _orth_keys(rng, T, K)
+    q = rng.standard_normal((T, K))
+    beta, g = rng.uniform(0.1, 1, T), -rng.uniform(0, 0.7, T)
+    ref = np.zeros(T)
+    for p in range(T):
+        for j in range(p + 1, T):
+            ref[p] += beta[j] * (q[p] @ k[j]) * np.exp(g[p + 1:j].sum())
+    d = oracle.den(_one(q), _one(k), _one(beta), g=_one(g), reverse=True)[0, 0]
+    np.testing.assert_allclose(d, ref, rtol=1e-12, atol=1e-12)
+    # the causal one differs (it includes the self term and earlier tokens)
+    dc = oracle.den(_one(q), _one(k), _one(beta), g=_one(g))[0, 0]
+    assert np.abs(dc - ref).max() > 1e-3
+
+
+def _frame_den_matrix(q, k, beta, gf, S, reverse):
+    """Frame-rule denominator per (batch, head) as matrix products: z is a
+    K-vector; a frame's write is z <- e^{g_f} z, z <- z + K_f^T diag(beta_f)
+    (1 - K_f z) with z the post-decay pre-frame state; den = Q_f z. Forward:
+    frame f reads frames 0..f. Reverse: frame f reads frames F-1 down to f+1,
+    each decayed by its own gate before its write (no self term)."""
+    B, T, H, K = q.shape
+    F = T // S
+    gf = np.asarray(gf, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+    out = np.zeros((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            def write(z, f):
+                rows = slice(f * S, (f + 1) * S)
+                Kf = k[b, rows, h]
+                zp = np.exp(gf[b, f, h]) * z
+                return zp + Kf.T @ (beta[b, rows, h] * (1.0 - Kf @ zp))
+            z = np.zeros(K)
+            order = range(F - 1, -1, -1) if reverse else range(F)
+            for f in order:
+                rows = slice(f * S, (f + 1) * S)
+                if not reverse:
+                    z = write(z, f)
+                out[b, h, rows] = q[b, rows, h] @ z
+                if reverse:
+                    z = write(z, f)
+    return out
+
+
+@pytest.mark.parametrize("reverse", [False, True])
+def test_frame_den_matrix_form(reverse):
+    B, F, S, H, K, V = 2, 5, 3, 2, 4, 1
+    q, k, _, beta, gf = _frame_rand(41, B, F, S, H, K, V)
+    got = oracle.frame_den(q, k, beta, gf, S, reverse=reverse)
+    want = _frame_den_matrix(q, k, beta, gf, S, reverse)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    other = _frame_den_matrix(q, k, beta, gf, S, not reverse)
+    assert np.abs(got - other).max() > 1e-3
+
+
+def _rms_relu(x, scale):
+    """Full-channel RMSNorm (eps 1e-5, weight 1) over the H*D channels of
+    each token, then ReLU, then * scale, written out in numpy."""
+    ms = (x * x).mean(axis=(2, 3), keepdims=True)
+    return np.maximum(x / np.sqrt(ms + 1e-5), 0.0) * scale
+
+
+def test_forward_glue_bidirectional_chunk_causal_merge():
+    """oracle.forward on a bidirectional workload (chunk-causal backward gates
+    and a gate for the merge) equals the pieces put together by hand: the
+    prep in numpy, the causal scan plus the reverse scan with the backward
+    gates, both denominators, and num / (den + eps) * silu(gate)."""
+    import workloads
+    w = workloads.make_video(1, 24, 2, 8, seed=3, reset_every=8, merge=True)
+    res = oracle.forward(w)
+    qn = _rms_relu(w.q.values.astype(np.float64), 1.0)
+    kn = _rms_relu(w.k.values.astype(np.float64), 8 ** -0.5)
+    v = w.v.values.astype(np.float64)
+    of, _ = oracle.scan(qn, kn, v, w.beta, g=w.g)
+    orv, _ = oracle.scan(qn, kn, v, w.beta_bwd, g=w.g_bwd, reverse=True)
+    num = of + orv
+    den = (oracle.den(qn, kn, w.beta, g=w.g)
+           + oracle.den(qn, kn, w.beta_bwd, g=w.g_bwd, reverse=True))
+    np.testing.assert_allclose(res["out"], num, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(res["den"], den, rtol=1e-12, atol=1e-12)
+    x = w.gate.values.astype(np.float64)
+    merged = num / (den.transpose(0, 2, 1)[..., None] + w.eps) * (x / (1.0 + np.exp(-x)))
+    np.testing.assert_allclose(res["merged"], merged, rtol=1e-12, atol=1e-12)
+    # the backward gates matter here: the same sum with the forward gates differs
+    orv_plain, _ = oracle.scan(qn, kn, v, w.beta, g=w.g, reverse=True)
+    assert np.abs(of + orv_plain - num).max() > 1e-3
+
+
+def test_forward_glue_frame_bidirectional():
+    """oracle.forward on a frame-causal bidirectional workload equals both
+    directions of the frame rule and both frame denominators summed, with the
+    numpy prep; each direction checked against the matrix forms."""
+    import workloads
+    w = workloads.make_video(1, 12, 2, 8, seed=4, frame=4)
+    res = oracle.forward(w)
+    qn = _rms_relu(w.q.values.astype(np.float64), 1.0)
+    kn = _rms_relu(w.k.values.astype(np.float64), 8 ** -0.5)
+    v = w.v.values.astype(np.float64)
+    of, _ = oracle.frame_scan(qn, kn, v, w.beta, w.g_frame, 4)
+    orv, _ = oracle.frame_scan(qn, kn, v, w.beta, w.g_frame, 4, reverse=True)
+    np.testing.assert_allclose(res["out"], of + orv, rtol=1e-12, atol=1e-12)
+    den = (_frame_den_matrix(qn, kn, w.beta, w.g_frame, 4, False)
+           + _frame_den_matrix(qn, kn, w.beta, w.g_frame, 4, True))
+    np.testing.assert_allclose(res["den"], den, rtol=1e-12, atol=1e-12)

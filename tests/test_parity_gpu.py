@@ -7,6 +7,7 @@ fp32 path and <= 2e-2 on the bf16 tensor-core path (fp32 state).
 Small cases span several 64-token chunks plus a ragged tail; the full-size
 workloads run exactly as the benchmark launches them and are compared on
 sampled (sequence, head) pairs the oracle computes directly."""
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -79,7 +80,7 @@ def test_small_bidirectional_l2(dtype):
 
 def test_small_video_rms_bidirectional():
     w = workloads.make_video(1, 300, 4, 112, seed=3, name="video_small")
-    _compare(w, ["out", "den"])
+    _compare(w, ["out", "den", "q_inv_rms", "k_inv_rms"])
 
 
 @pytest.mark.parametrize("reset", [64, 100])
@@ -210,6 +211,35 @@ def test_malformed_cu_seqlens_sets_device_error():
     assert gdn.gdn_last_device_error(ws) == 0
 
 
+@pytest.mark.parametrize("cta", [5, 29])
+def test_stalled_block_reports_timeout(cta):
+    """A block other than the first of the intra-chunk and state launches
+    waits on a barrier that nothing completes (the library's stall testing
+    aid) and gives up after 2 ms: the call reports GDN_ERR_TIMEOUT through the
+    error word (cleared in stream order before the call, so no block of the
+    call can erase it), the kernels return, and the next call on the same
+    workspace is clean and correct."""
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(2, 64 * 8, 2, 128, 128, "bf16", seed=11)
+    q, k, v, beta, g = to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g)
+    ws = torch.empty(gdn.gdn_workspace_size(2, 64 * 8, 2, 128, 128, 2, 0, gdn.BF16, 0),
+                     dtype=torch.uint8, device="cuda")
+    L = gdn.lib()
+    gdn.gdn_set_stall_test(cta, 2000)
+    try:
+        gdn.gdn_chunk_fwd(q, k, v, beta, g=g, qk_l2norm=True, workspace=ws)
+        word = ctypes.c_int(0)
+        st = L.gdn_last_device_error(ctypes.c_void_p(ws.data_ptr()), None, ctypes.byref(word))
+    finally:
+        gdn.gdn_set_stall_test(-1, 0)
+    assert st == 7 and word.value & 2, (st, word.value)  # GDN_ERR_TIMEOUT
+    out = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, qk_l2norm=True, workspace=ws)
+    assert gdn.gdn_last_device_error(ws) == 0
+    ref = oracle.forward(w)
+    assert rel_err(out.double().cpu().numpy(), ref["out"]) <= TOL["bf16"]
+
+
 # ------------------------------------------------------- full-size, sampled ---
 
 def _sub(w, b_idx, heads):
@@ -272,8 +302,12 @@ def test_full_size_chunkcausal_merge():
     got = run_gpu(w)
     b, heads = 0, [3, 14]
     qkv = w.qkv.take((slice(b, b + 1),)).values.astype(np.float64)
-    qn, _ = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
-    kn, _ = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    qn, q_inv = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
+    kn, k_inv = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    # the per-token inverse RMS the prep writes (fp32 arithmetic: 1e-5 is far
+    # above its rounding, far below any indexing or reduction mistake)
+    assert rel_err(got["q_inv_rms"][b:b + 1], q_inv) <= 1e-5
+    assert rel_err(got["k_inv_rms"][b:b + 1], k_inv) <= 1e-5
     qn, kn, vv = qn[:, :, heads], kn[:, :, heads], qkv[:, :, 2][:, :, heads]
     sel = lambda a: a[b:b + 1][:, :, heads]
     beta, g, bb, gb = sel(w.beta), sel(w.g), sel(w.beta_bwd), sel(w.g_bwd)
@@ -291,8 +325,12 @@ def test_full_size_frame_video():
     got = run_gpu(w)
     b, heads = 1, [2, 11]
     qkv = w.qkv.take((slice(b, b + 1),)).values.astype(np.float64)
-    qn, _ = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
-    kn, _ = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    qn, q_inv = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
+    kn, k_inv = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    # the per-token inverse RMS the prep writes (fp32 arithmetic: 1e-5 is far
+    # above its rounding, far below any indexing or reduction mistake)
+    assert rel_err(got["q_inv_rms"][b:b + 1], q_inv) <= 1e-5
+    assert rel_err(got["k_inv_rms"][b:b + 1], k_inv) <= 1e-5
     qn, kn, vv = qn[:, :, heads], kn[:, :, heads], qkv[:, :, 2][:, :, heads]
     beta, gf = w.beta[b:b + 1][:, :, heads], w.g_frame[b:b + 1][:, :, heads]
     of, _ = oracle.frame_scan(qn, kn, vv, beta, gf, w.frame)
@@ -309,8 +347,12 @@ def test_full_size_video_bidirectional():
     b, heads = 1, [0, 9]
     # full-channel RMS prep needs every head of the token; scan two heads
     qkv = w.qkv.take((slice(b, b + 1),)).values.astype(np.float64)
-    qn, _ = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
-    kn, _ = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    qn, q_inv = oracle.rmsnorm_channels(qkv[:, :, 0], 1e-5, relu=True, scale=1.0)
+    kn, k_inv = oracle.rmsnorm_channels(qkv[:, :, 1], 1e-5, relu=True, scale=w.K ** -0.5)
+    # the per-token inverse RMS the prep writes (fp32 arithmetic: 1e-5 is far
+    # above its rounding, far below any indexing or reduction mistake)
+    assert rel_err(got["q_inv_rms"][b:b + 1], q_inv) <= 1e-5
+    assert rel_err(got["k_inv_rms"][b:b + 1], k_inv) <= 1e-5
     qn, kn, vv = qn[:, :, heads], kn[:, :, heads], qkv[:, :, 2][:, :, heads]
     beta, g = w.beta[b:b + 1][:, :, heads], w.g[b:b + 1][:, :, heads]
     of, _ = oracle.scan(qn, kn, vv, beta, g=g)
