@@ -117,6 +117,9 @@ def kernel_bytes(w, name):
     chunks = th / C
     if name == "intra_bf16":
         return th * ((2 * K + w.V) * e + 4 + gate + (3 * K + V + C) * 2) + chunks * K * 4
+    if name == "fused_tc":  # one direction: q, k, v, beta, g in; o (and den) out; h0 / h_final
+        hs = 0 if w.bidirectional else (2 if w.h0 is not None else 1) * w.n_seq * w.H * w.K * w.V * 4
+        return th * ((2 * w.K + w.V) * e + 8 + w.V * e + (4 if w.bidirectional else 0)) + hs
     n_seg, bh = seg_count(w), w.n_seq * w.H
     if name == "state_tc":
         hs = (2 if w.h0 is not None else 1) * w.n_seq * w.H * w.K * w.V * 4
@@ -164,7 +167,8 @@ def kernel_bytes(w, name):
     return None
 
 
-KERNEL_SOURCES = {"intra_bf16": ["gdn_intra_bf16.cu", "gdn_common.cuh"],
+KERNEL_SOURCES = {"fused_tc": ["gdn_fused_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"],
+                  "intra_bf16": ["gdn_intra_bf16.cu", "gdn_common.cuh"],
                   "state_tc": ["gdn_state_tc.cu", "gdn_tc.cuh", "gdn_common.cuh"]}
 
 

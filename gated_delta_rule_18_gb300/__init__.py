@@ -20,7 +20,7 @@ from .build import LIB
 __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
            "gdn_merge", "gdn_frame_fwd", "gdn_frame_workspace_size", "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_noalloc_last_device_error",
-           "gdn_set_stall_test", "gdn_forward", "lib",
+           "gdn_set_stall_test", "gdn_set_fused", "gdn_forward", "lib",
            "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect", "gdn_set_state_tile",
            "launch_count", "kernel_names"]
 
@@ -104,6 +104,8 @@ def lib():
     L.gdn_noalloc_last_device_error.argtypes = [P, ctypes.POINTER(I)]
     L.gdn_set_stall_test.restype = None
     L.gdn_set_stall_test.argtypes = [I, I]
+    L.gdn_set_fused.restype = None
+    L.gdn_set_fused.argtypes = [I]
     L.gdn_kernel_kinds.restype = I
     L.gdn_kernel_kinds.argtypes = []
     L.gdn_kernel_name.restype = ctypes.c_char_p
@@ -446,6 +448,13 @@ def gdn_noalloc_last_device_error(stream=None) -> int:
     if st not in (0, 7, 9):
         raise GDNError(st, "gdn_noalloc_last_device_error")
     return w.value
+
+
+def gdn_set_fused(on: bool = True) -> None:
+    """Run the bf16 scalar-gate forward as one fused tcgen05 kernel per
+    direction (on) or as the split intra-chunk + state passes (off, the
+    default); see include/gdn.h."""
+    lib().gdn_set_fused(int(bool(on)))
 
 
 def gdn_set_stall_test(cta: int = -1, limit_us: int = 1000) -> None:

@@ -16,12 +16,13 @@ using gdn::FwdParams;
 
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
-    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KNumKinds
+    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KFused, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
-                                     "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial"};
+                                     "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial",
+                                     "fused_tc"};
 
 struct Profiler {
     std::mutex mu;
@@ -372,6 +373,9 @@ gdn_status gdn_chunk_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
         e = launch_f32(p, L.KP, perkey, stream);
         return cuda_status(e);
     }
+    gdn::FusedMaps maps;
+    if (gdn::fused_prepare(p, &maps))
+        return cuda_status(launch(KFused, stream, [&] { return gdn::launch_fused_tc(p, maps, stream); }));
     if (L.max_chunks > 0) {
         e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, perkey, stream); });
         if (e != cudaSuccess) return GDN_ERR_CUDA;
@@ -692,6 +696,10 @@ gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd
     std::lock_guard<std::mutex> lock(side_mutex());
     SideStream *side = nullptr;
     if (side_stream(side) != cudaSuccess) return GDN_ERR_CUDA;
+    // one kernel per direction where the fused path applies, else the split
+    // intra-chunk and state passes
+    gdn::FusedMaps mf, mr;
+    const bool fused = qkd.dtype == GDN_BF16 && gdn::fused_prepare(pf, &mf) && gdn::fused_prepare(pr, &mr);
     // everything of a direction up to its state pass
     auto first = [&](gdn::FwdParams &p, cudaStream_t s) -> cudaError_t {
         cudaError_t e = cudaSuccess;
@@ -699,11 +707,16 @@ gdn_status gdn_chunk_fwd_bidir(const void *q, const void *k, gdn_tensor_desc qkd
         if (e != cudaSuccess) return e;
         if (qkd.dtype == GDN_F32)
             return launch_f32(p, L.KP, perkey, s);
-        if (L.max_chunks > 0) e = launch(KIntra, s, [&] { return gdn::launch_intra_bf16(p, perkey, s); });
+        if (!fused && L.max_chunks > 0)
+            e = launch(KIntra, s, [&] { return gdn::launch_intra_bf16(p, perkey, s); });
         return e;
     };
     auto second = [&](gdn::FwdParams &p, cudaStream_t s) -> cudaError_t {
         if (qkd.dtype == GDN_F32) return cudaSuccess;
+        if (fused) {
+            const gdn::FusedMaps &m = &p == &pf ? mf : mr;
+            return launch(KFused, s, [&] { return gdn::launch_fused_tc(p, m, s); });
+        }
         return launch(KState, s, [&] { return gdn::launch_state_tc(p, s); });
     };
     // fork: the reverse direction on the side stream, the forward on the
@@ -859,6 +872,8 @@ const char *gdn_kernel_name(int kind) {
 }
 
 void gdn_set_state_tile(int bv) { gdn::set_state_tile(bv); }
+
+void gdn_set_fused(int on) { gdn::set_fused(on); }
 
 void gdn_set_stall_test(int cta, int limit_us) {
     g_stall_us.store(limit_us > 0 ? limit_us : 1);

@@ -5,6 +5,7 @@
 // bf16 mma).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -237,20 +238,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 constexpr int kDevErrSeqlens = 1, kDevErrTimeout = 2;
 
 // Testing aid for the time-out path: the block whose linear index is
-// p.stall_cta waits on an mbarrier that nothing completes until its
-// p.stall_us limit runs out, records a time-out in the error word and
-// reports true, so that the kernel leaves before issuing any copy or MMA.
-// Every other block returns false at once. The decision depends only on the
-// block index, so a block's threads all take the same branch.
-static __device__ __noinline__ bool stall_test(const FwdParams &p) {
+// stall_cta waits on an mbarrier that nothing completes until its stall_us
+// limit runs out, records a time-out in the error word and reports true, so
+// that the kernel leaves before issuing any copy or MMA. Every other block
+// returns false at once. The decision depends only on the block index, so a
+// block's threads all take the same branch. (Scalars, not the parameter
+// block, are passed: taking the address of a kernel's parameters would move
+// them to local memory.)
+static __device__ __forceinline__ bool stall_test(int stall_cta, int stall_us, int *err) {
     const int b = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
-    if (p.stall_cta < 0 || b != p.stall_cta) return false;
+    if (stall_cta < 0 || b != stall_cta) return false;
     __shared__ __align__(8) uint64_t never;
     const uint32_t bar = smem_u32(&never);
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
-        const uint64_t t0 = now_ns(), lim = (uint64_t)max(p.stall_us, 1) * 1000ull;
+        const uint64_t t0 = now_ns(), lim = (uint64_t)max(stall_us, 1) * 1000ull;
         for (;;) {
             uint32_t ok;
             asm volatile(
@@ -261,7 +264,7 @@ static __device__ __noinline__ bool stall_test(const FwdParams &p) {
                 : "memory");
             if (ok || now_ns() - t0 > lim) break;
         }
-        atomicOr(p.err, kDevErrTimeout);
+        atomicOr(err, kDevErrTimeout);
     }
     __syncthreads();
     return true;
@@ -371,6 +374,16 @@ cudaError_t launch_frame_gram(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_frame_chain(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st);
 cudaError_t launch_intra_bf16(const FwdParams &p, int perkey, cudaStream_t st);
+// The bf16 forward of one direction in one kernel (gdn_fused_tc.cu): the
+// tensor maps of q, k and v, built by fused_prepare, which returns false when
+// the call needs the split path (per-key gate, segments, summaries,
+// snapshots, layouts a tensor map cannot express, or the path switched off).
+struct FusedMaps {
+    CUtensorMap q, k, v;
+};
+bool fused_prepare(const FwdParams &p, FusedMaps *m);
+cudaError_t launch_fused_tc(const FwdParams &p, const FusedMaps &m, cudaStream_t st);
+void set_fused(int on);
 cudaError_t launch_state_tc(const FwdParams &p, cudaStream_t st);
 // value columns per state-kernel CTA: 0 chooses by the grid, 64 or 128 force one
 void set_state_tile(int bv);

@@ -127,7 +127,9 @@ __device__ __forceinline__ bool wait_copies(uint32_t bar, int *err) {
     return false;
 }
 
-template <bool PERKEY>
+// STALL: the instantiation with the stall testing aid (launched only while it
+// is on, so that the working kernel carries none of its code)
+template <bool PERKEY, bool STALL>
 __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 : 4)
     intra_kernel(const FwdParams p, int VP) {
     using L = Lay<PERKEY>;
@@ -157,7 +159,7 @@ __global__ void __launch_bounds__(PERKEY ? 2 * kThreads : kThreads, PERKEY ? 2 :
     // heads vary fastest across the grid, so CTAs resident together read the
     // same tokens of all heads (whole DRAM pages) rather than one head's rows
     const int hh = blockIdx.x % p.H, gid = blockIdx.x / p.H;
-    if (stall_test(p)) return;
+    if (STALL && stall_test(p.stall_cta, p.stall_us, p.err)) return;
     int s, c, slot;  // slot: the chunk's image index within the head
     if (p.cu_seqlens) {
         if (gid >= *p.n_chunks) return;
@@ -685,7 +687,7 @@ cudaError_t launch_t(const FwdParams &p, cudaStream_t st) {
     using L = Lay<PERKEY>;
     const int VP = p.n_vt * 64;
     const size_t bytes = L::bytes(VP);
-    auto kern = intra_kernel<PERKEY>;
+    auto kern = p.stall_cta >= 0 ? intra_kernel<PERKEY, true> : intra_kernel<PERKEY, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
     // the whole shared-memory carveout, so that 4 (scalar) / 2 (per-key) CTAs fit per SM

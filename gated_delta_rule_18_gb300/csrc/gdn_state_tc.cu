@@ -142,7 +142,9 @@ __device__ __forceinline__ void store_row64(float *row, const float (&h)[64], in
     }
 }
 
-template <int BV>
+// STALL: the instantiation with the stall testing aid (launched only while it
+// is on, so that the working kernel carries none of its code)
+template <int BV, bool STALL>
 __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const FwdParams p) {
     using Lay = gdn::Lay<BV>;
     constexpr int kThreads = Cfg<BV>::kThreads;
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
     // u image tiles of this CTA present in the images (a 128-column CTA over
     // an odd last tile keeps the second half of its u slots zero)
     const int n_ut = trt ? 0 : min(kUT, p.n_vt - vt * kUT);
-    if (stall_test(p)) return;
+    if (STALL && stall_test(p.stall_cta, p.stall_us, p.err)) return;
     if (p.cu_seqlens && *p.n_chunks < 0) return;
     SeqInfo si;
     if (!seq_info(p, s, si)) return;
@@ -576,15 +578,15 @@ std::atomic<int> g_state_tile{0};  // 0: by the grid, else 64 or 128
 
 template <int BV>
 cudaError_t launch_bv(const FwdParams &p, int n_tiles, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(state_tc_kernel<BV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Lay<BV>::bytes);
+    auto kern = p.stall_cta >= 0 ? state_tc_kernel<BV, true> : state_tc_kernel<BV, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay<BV>::bytes);
     if (e != cudaSuccess) return e;
     const int nall = (p.T + kChunk - 1) / kChunk;
     // summary 2: every segment but the last (whose summary nothing reads)
     const int nseg = p.seg_chunks ? max(1, (nall + p.seg_chunks - 1) / p.seg_chunks) - (p.summary == 2 ? 1 : 0) : 1;
     if (nseg < 1) return cudaSuccess;
     dim3 grid(p.n_seq * p.H * n_tiles, 1, nseg);
-    state_tc_kernel<BV><<<grid, Cfg<BV>::kThreads, Lay<BV>::bytes, st>>>(p);
+    kern<<<grid, Cfg<BV>::kThreads, Lay<BV>::bytes, st>>>(p);
     return cudaGetLastError();
 }
 }  // namespace

@@ -426,6 +426,22 @@ long long gdn_launch_count(void);
 void gdn_set_state_tile(int bv);
 
 /*
+ * Path of the bf16 forward with a scalar gate. on = 0 (the default) runs the
+ * split path: an intra-chunk pass writing per-chunk operand images, then the
+ * chunk-serial state pass. on = 1 runs each scan direction as one kernel in
+ * which the intra-chunk WY factors are formed on the tensor cores (tcgen05,
+ * TMA-loaded tiles) inside the state pass's CTAs and never leave the SM; it
+ * falls back to the split path where it does not apply (per-key gates,
+ * segment-parallel passes, summaries, gradient snapshots, layouts a TMA
+ * tensor map cannot express). Both compute the same recurrence; results
+ * agree to rounding order. On GB300 the fused kernel is correct but slower
+ * than the split path (every value-tile CTA of a head repeats the head's
+ * intra-chunk work, and that work per chunk exceeds the chain's step), so it
+ * is not the default. Process-wide; affects later launches.
+ */
+void gdn_set_fused(int on);
+
+/*
  * Testing aid for the device-side time-out path; the pages have no
  * counterpart. While set (cta >= 0), the block with linear index `cta` of
  * every later intra-chunk and state-pass launch of the bf16 path waits on a

@@ -71,6 +71,41 @@ def test_small_causal(name):
     _compare(w)
 
 
+@pytest.fixture
+def fused_path():
+    """Run the bf16 scalar-gate forward as the fused kernel (one tcgen05
+    kernel per direction, intra-chunk factors formed in the state pass's
+    CTAs; the library runs the split passes by default), so the same oracle
+    comparisons cover both paths."""
+    import gated_delta_rule_18_gb300 as gdn
+    gdn.gdn_set_fused(True)
+    yield
+    gdn.gdn_set_fused(False)
+
+
+FUSED = ["bf16_dense_k64", "bf16_k128_h0", "bf16_varlen_h0", "bf16_k32_v96", "bf16_k112_v112",
+         "bf16_t1", "bf16_t64", "bf16_gk_v256"]
+
+
+@pytest.mark.parametrize("name", FUSED)
+def test_small_causal_fused_path(name, fused_path):
+    test_small_causal(name)  # (the per-key case falls back to the split path)
+
+
+def test_small_bidirectional_fused_path(fused_path):
+    test_small_bidirectional_l2("bf16")      # den column in a value tile of its own
+    test_small_video_rms_bidirectional()     # K = V = 112, den in the second tile
+    test_small_chunkcausal_merge(100)        # backward gates of -inf: the per-entry form
+    test_full_reset_and_frozen_state("bf16")  # g = -inf: the per-entry form
+    test_split_resume_bit_exact("bf16")
+    test_zero_tokens_pass_state_through("bf16")
+
+
+def test_full_size_dense_fused_path(fused_path):
+    test_full_size_dense("causal_bf16_b4h16t4096d128")
+    test_full_size_video_bidirectional()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_small_bidirectional_l2(dtype):
     w = workloads.make(2, 170, 2, 64, 64, dtype, seed=2, name="bidir_small")
@@ -211,14 +246,15 @@ def test_malformed_cu_seqlens_sets_device_error():
     assert gdn.gdn_last_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("cta", [5, 29])
-def test_stalled_block_reports_timeout(cta):
-    """A block other than the first of the intra-chunk and state launches
-    waits on a barrier that nothing completes (the library's stall testing
-    aid) and gives up after 2 ms: the call reports GDN_ERR_TIMEOUT through the
-    error word (cleared in stream order before the call, so no block of the
-    call can erase it), the kernels return, and the next call on the same
-    workspace is clean and correct."""
+@pytest.mark.parametrize("cta,fused", [(5, True), (5, False), (29, False)])
+def test_stalled_block_reports_timeout(cta, fused):
+    """A block other than the first (of the fused kernel, or of the split
+    path's intra-chunk and state launches) waits on a barrier that nothing
+    completes (the library's stall testing aid) and gives up after 2 ms: the
+    call reports GDN_ERR_TIMEOUT through the error word (cleared in stream
+    order before the call, so no block of the call can erase it), the
+    kernels return, and the next call on the same workspace is clean and
+    correct."""
     import gated_delta_rule_18_gb300 as gdn
     import torch
     w = workloads.make(2, 64 * 8, 2, 128, 128, "bf16", seed=11)
@@ -226,16 +262,20 @@ def test_stalled_block_reports_timeout(cta):
     ws = torch.empty(gdn.gdn_workspace_size(2, 64 * 8, 2, 128, 128, 2, 0, gdn.BF16, 0),
                      dtype=torch.uint8, device="cuda")
     L = gdn.lib()
+    gdn.gdn_set_fused(fused)
     gdn.gdn_set_stall_test(cta, 2000)
     try:
         gdn.gdn_chunk_fwd(q, k, v, beta, g=g, qk_l2norm=True, workspace=ws)
         word = ctypes.c_int(0)
         st = L.gdn_last_device_error(ctypes.c_void_p(ws.data_ptr()), None, ctypes.byref(word))
+        gdn.gdn_set_stall_test(-1, 0)
+        out = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, qk_l2norm=True, workspace=ws)
+        clean = gdn.gdn_last_device_error(ws)
     finally:
         gdn.gdn_set_stall_test(-1, 0)
+        gdn.gdn_set_fused(False)
     assert st == 7 and word.value & 2, (st, word.value)  # GDN_ERR_TIMEOUT
-    out = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, qk_l2norm=True, workspace=ws)
-    assert gdn.gdn_last_device_error(ws) == 0
+    assert clean == 0
     ref = oracle.forward(w)
     assert rel_err(out.double().cpu().numpy(), ref["out"]) <= TOL["bf16"]
 
@@ -280,15 +320,19 @@ def test_full_size_dense(name):
         assert e_o <= tol and e_h <= tol, (name, b, heads, e_o, e_h)
 
 
-@pytest.mark.parametrize("tile", [0, 64])  # 0: the library's choice (128-column CTAs here)
-def test_full_size_varlen(tile):
+# fused: one kernel per direction (the default); split 0: the split path with
+# the library's state tile (128-column CTAs here); split 64: 64-column CTAs
+@pytest.mark.parametrize("fused,tile", [(True, 0), (False, 0), (False, 64)])
+def test_full_size_varlen(fused, tile):
     import gated_delta_rule_18_gb300 as gdn
     w = workloads.build("varlen_bf16_64seq_h32d128")
     gdn.gdn_set_state_tile(tile)
+    gdn.gdn_set_fused(fused)
     try:
         got = run_gpu(w)
     finally:
         gdn.gdn_set_state_tile(0)
+        gdn.gdn_set_fused(False)
     seqs, heads = [0, 17, 63], [3, 31]
     sw, rows = _sub_varlen(w, seqs, heads)
     ref = oracle.forward(sw)
@@ -550,12 +594,13 @@ def test_repeated_long_runs_clean_and_deterministic(name):
             assert t.equal(cur[0], first[0]) and t.equal(cur[1], first[1])
 
 
-@pytest.mark.parametrize("tile", [0, 128])
-def test_state_rows_at_any_alignment(tile):
+@pytest.mark.parametrize("fused,tile", [(True, 0), (False, 64), (False, 128)])
+def test_state_rows_at_any_alignment(fused, tile):
     """The state pass moves h0 and h_final rows by 16-byte accesses where the
     row starts allow it and element by element otherwise: h0 and h_final
     given as views one float past an aligned start reproduce the aligned
-    run's output and final state bit for bit (both state tile widths)."""
+    run's output and final state bit for bit (the fused kernel and both
+    state tile widths of the split path)."""
     import gated_delta_rule_18_gb300 as gdn
     t = torch()
     w = workloads.make(2, 200, 2, 128, 128, "bf16", seed=12, name="state_align", h0_std=0.5)
@@ -568,12 +613,14 @@ def test_state_rows_at_any_alignment(tile):
     hf_odd = t.empty(n + 1, dtype=t.float32, device=dev())[1:].view(h0.shape)
     assert h0_odd.data_ptr() % 16 == 4 and hf_odd.data_ptr() % 16 == 4
     gdn.gdn_set_state_tile(tile)
+    gdn.gdn_set_fused(fused)
     try:
         a = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h0=h0, h_final=hf, qk_l2norm=w.prep == "l2")
         b = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h0=h0_odd, h_final=hf_odd, qk_l2norm=w.prep == "l2")
         t.cuda.synchronize()
     finally:
         gdn.gdn_set_state_tile(0)
+        gdn.gdn_set_fused(False)
     assert t.equal(a, b) and t.equal(hf, hf_odd)
 
 
