@@ -159,6 +159,15 @@ def _stream(stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _state_shape(n_seq, H, K, V, den, **states):
+    """State tensors are (n_seq, H, K, V), with the denominator's z column
+    (V + 1) when den is given; the library cannot see a buffer's size."""
+    want = (n_seq, H, K, V + (1 if den is not None else 0))
+    for name, t in states.items():
+        if t is not None and tuple(t.shape) != want:
+            raise ValueError(f"{name} must have shape {want}, got {tuple(t.shape)}")
+
+
 def _f32(t, name):
     torch = _torch()
     if t is None:
@@ -196,7 +205,8 @@ def gdn_chunk_fwd(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None, out=
     """One direction of the chunked scan (see include/gdn.h).
 
     q, k: (B, T, H, K); v: (B, T, H, V); beta, g: (B, T, H) fp32;
-    gk: (B, T, H, K) fp32; h0/h_final: (n_seq, H, K, V) fp32;
+    gk: (B, T, H, K) fp32; h0/h_final: (n_seq, H, K, V) fp32, or
+    (n_seq, H, K, V + 1) with `den` (column V: the denominator's z state);
     cu_seqlens: int32 device tensor (n_seq + 1) with B == 1;
     den: (B, H, T) fp32. Missing `out` / `workspace` are allocated with
     torch. Returns out."""
@@ -209,6 +219,7 @@ def gdn_chunk_fwd(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None, out=
     for name, t in (("beta", beta), ("g", g), ("gk", gk), ("h0", h0), ("h_final", h_final),
                     ("den", den)):
         _f32(t, name)
+    _state_shape(n_seq, H, K, V, den, h0=h0, h_final=h_final)
     if out is None:
         out = torch.empty((B, T, H, V), dtype=out_dtype or q.dtype, device=q.device)
     dt = _dtype_code(q)
@@ -216,9 +227,12 @@ def gdn_chunk_fwd(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None, out=
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     flags = (ACCUMULATE if accumulate else 0) | (QK_L2NORM if qk_l2norm else 0)
+    # an empty den (T = 0) may have no address; any non-NULL pointer tells
+    # the library that the state carries the z column (nothing is written)
+    den_p = _ptr(workspace) if den is not None and den.numel() == 0 else _ptr(den)
     st = lib().gdn_chunk_fwd(
         _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta),
-        _ptr(h0), _ptr(cu_seqlens), n_seq, _ptr(out), _desc(out), _ptr(h_final), _ptr(den),
+        _ptr(h0), _ptr(cu_seqlens), n_seq, _ptr(out), _desc(out), _ptr(h_final), den_p,
         B, T, H, K, V, 64, int(bool(reverse)), flags, _ptr(workspace),
         workspace.numel(), _stream(stream))
     if st != 0:
@@ -248,6 +262,7 @@ def gdn_chunk_fwd_seg(q, k, v, beta, segment_len, g=None, gk=None, h0=None, out=
     for name, t in (("beta", beta), ("g", g), ("gk", gk), ("h0", h0), ("h_final", h_final),
                     ("den", den)):
         _f32(t, name)
+    _state_shape(B, H, K, V, den, h0=h0, h_final=h_final)
     if out is None:
         out = torch.empty((B, T, H, V), dtype=out_dtype or q.dtype, device=q.device)
     need = gdn_seg_workspace_size(B, T, H, K, V, den is not None, segment_len)
@@ -372,6 +387,7 @@ def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqle
     B, T, H, K = q.shape
     V = v.shape[3]
     n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    _state_shape(n_seq, H, K, V, den, h0=h0, h_final=h_final)
     flags = (ACCUMULATE if accumulate else 0) | (QK_L2NORM if qk_l2norm else 0)
     st = lib().gdn_chunk_fwd_noalloc(
         _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta),
@@ -415,6 +431,7 @@ def gdn_frame_fwd(q, k, v, beta, g_frame, frame, out=None, den=None, h0=None, h_
     for name, t in (("beta", beta), ("g_frame", g_frame), ("h0", h0), ("h_final", h_final),
                     ("den", den)):
         _f32(t, name)
+    _state_shape(B, H, K, V, den, h0=h0, h_final=h_final)
     if out is None:
         out = torch.empty((B, T, H, V), dtype=out_dtype or q.dtype, device=q.device)
     need = gdn_frame_workspace_size(B, T, H, K, V, frame, den is not None)
@@ -484,6 +501,10 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
     segment_len: segment-parallel state passing (gdn_chunk_fwd_seg; dense
     bf16 inputs) with segments of this many tokens, or "auto" for
     gdn_seg_choose's pick on this device.
+    h0 / with_final_state: the causal direction's state in and out,
+    (n_seq, H, K, V); bidirectional, (n_seq, H, K, V + 1) with the
+    denominator's z state in column V (the reverse direction starts from
+    zero at the end of the call, as on the pages).
     Returns a dict with "out" and, as requested, "h_final" / "den" /
     "merged" / "q_inv_rms" / "k_inv_rms"."""
     torch = _torch()
@@ -523,6 +544,8 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
             if hf is not None:
                 res["h_final"] = hf
             return res
+        if h0 is not None or with_final_state:
+            raise ValueError("the bidirectional frame-causal form carries no state")
         den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
         res["out"] = gdn_frame_fwd(q, k, v, beta, g_frame, frame, den=den, direction=2,
                                    workspace=workspace, stream=stream)
@@ -550,7 +573,10 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
             res["h_final"] = hf
         return res
     den = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
-    if not segment_len and not ({"q", "k", "v", "gk"} & set(bw)) and not (gk is not None and "g" in bw):
+    hf = (torch.empty((n_seq, H, K, v.shape[3] + 1), dtype=torch.float32, device=q.device)
+          if with_final_state else None)
+    if (h0 is None and hf is None and not segment_len and not ({"q", "k", "v", "gk"} & set(bw))
+            and not (gk is not None and "g" in bw)):
         # both directions at once, the reverse on the library's second stream
         out = gdn_chunk_fwd_bidir(q, k, v, beta, g=g, gk=gk, g_bwd=bw.get("g"),
                                   beta_bwd=bw.get("beta"), cu_seqlens=cu_seqlens, den=den,
@@ -560,10 +586,12 @@ def gdn_forward(q, k, v, beta, g=None, gk=None, h0=None, cu_seqlens=None,
                                                               cu_seqlens is not None,
                                                               _dtype_code(q), True) else None)
     else:
-        out = scan(q, k, v, beta, g, gk, den=den)
+        out = scan(q, k, v, beta, g, gk, den=den, h0=h0, h_final=hf)
         scan(bw.get("q", q), bw.get("k", k), bw.get("v", v), bw.get("beta", beta), bw.get("g", g),
              bw.get("gk", gk), den=den, out=out, reverse=True, accumulate=True)
     res["out"], res["den"] = out, den
+    if hf is not None:
+        res["h_final"] = hf
     if merge:
         res["merged"] = gdn_merge(out, den, gate=gate, eps=eps, stream=stream)
     return res

@@ -249,7 +249,6 @@ gdn_status fwd_setup(const void *q, const void *k, gdn_tensor_desc qkd, const vo
     if (!varlen && n_seq != B) return GDN_ERR_SHAPE;
     if (reverse != 0 && reverse != 1) return GDN_ERR_SHAPE;
     if (reverse && (h0 || h_final)) return GDN_ERR_UNSUPPORTED;
-    if (den_out && (h0 || h_final)) return GDN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return GDN_ERR_LAYOUT;  // (NULL counts as aligned)
     if (!strides_ok(qkd) || !strides_ok(vd) || !strides_ok(od)) return GDN_ERR_LAYOUT;

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
     for (int e = tid; e < KP * kBVf; e += kThreadsF) {
         const int d = e / kBVf, n = e % kBVf, col = v0 + n;
         float x = 0.f;
-        if (p.h0 && d < K && col < V) x = p.h0[(((int64_t)s * H + hh) * K + d) * V + col];
+        if (p.h0 && d < K && col < p.Vt) x = p.h0[(((int64_t)s * H + hh) * K + d) * p.Vt + col];
         sH[d * VS + n] = x;
     }
 
@@ -484,8 +484,8 @@ __global__ void __launch_bounds__(kThreadsF) fused_f32_kernel(const FwdParams p)
     if (p.h_final) {
         for (int e = tid; e < KP * kBVf; e += kThreadsF) {
             const int d = e / kBVf, n = e % kBVf, col = v0 + n;
-            if (d < K && col < V)
-                p.h_final[(((int64_t)s * H + hh) * K + d) * V + col] = sH[d * VS + n];
+            if (d < K && col < p.Vt)
+                p.h_final[(((int64_t)s * H + hh) * K + d) * p.Vt + col] = sH[d * VS + n];
         }
     }
 }

@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kTS) f32_serial_kernel(const FwdParams p, int 
 
     for (int e = tid; e < KP * kBV; e += kTS) {  // state tile h[d][n]
         const int d = e / kBV, n = e % kBV, col = v0 + n;
-        sH[d * kVS + n] = (p.h0 && d < K && col < V) ? p.h0[(((int64_t)s * H + hh) * K + d) * V + col] : 0.f;
+        sH[d * kVS + n] = (p.h0 && d < K && col < p.Vt) ? p.h0[(((int64_t)s * H + hh) * K + d) * p.Vt + col] : 0.f;
     }
     // 2 rows x 4 columns per thread for the 64 x 32 products, KP/32 key rows
     // x 4 columns for the state update; the two halves of the CTA (hf) take
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(kTS) f32_serial_kernel(const FwdParams p, int 
     if (p.h_final) {
         for (int e = tid; e < KP * kBV; e += kTS) {
             const int d = e / kBV, n = e % kBV, col = v0 + n;
-            if (d < K && col < V) p.h_final[(((int64_t)s * H + hh) * K + d) * V + col] = sH[d * kVS + n];
+            if (d < K && col < p.Vt) p.h_final[(((int64_t)s * H + hh) * K + d) * p.Vt + col] = sH[d * kVS + n];
         }
     }
 }

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(256, 1) frame_chain_kernel(const FrameParams p
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int r = r0 + i, j = j0 + c0 + c;
-                acc[i][c] = (!rev && p.h0 && r < K && j < p.V) ? p.h0[(((int64_t)b * p.H + h) * K + r) * p.V + j] : 0.f;
+                acc[i][c] = (!rev && p.h0 && r < K && j < p.Vt) ? p.h0[(((int64_t)b * p.H + h) * K + r) * p.Vt + j] : 0.f;
             }
         for (int i = 0; i < F; ++i) {
             const int of = rev ? F - 1 - i : i;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(256, 1) frame_chain_kernel(const FrameParams p
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int r = r0 + x, j = j0 + c0 + c;
-                    if (r < K && j < p.V) p.h_final[(((int64_t)b * p.H + h) * K + r) * p.V + j] = acc[x][c];
+                    if (r < K && j < p.Vt) p.h_final[(((int64_t)b * p.H + h) * K + r) * p.Vt + j] = acc[x][c];
                 }
         }
     };

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) seg_combine_kernel(const SegParams p
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = r0 + i;
-        acc[i] = (p.h0 && r < K && jc < p.V) ? p.h0[(bh * K + r) * p.V + jc] : 0.f;
+        acc[i] = (p.h0 && r < K && jc < Vt) ? p.h0[(bh * K + r) * Vt + jc] : 0.f;
     }
     for (int s = 0;; ++s) {
         // h_in[s]: to global and to the shared tile

@@ -121,23 +121,29 @@ size_t gdn_workspace_size(int B, int T, int H, int K, int V, int n_seq,
  *   gk:   (B, T, H, K) fp32 per-key natural-log gate, or NULL.
  *   beta: (B, T, H) fp32.
  *   h0:   (n_seq, H, K, V) fp32 initial state (state at the end of a prefix,
- *         decayed by this call's first gate), or NULL for zero. h0 and
+ *         decayed by this call's first gate), or NULL for zero. With den_out
+ *         the state is (n_seq, H, K, V + 1): column V is the denominator's
+ *         z state (SANA `fused_gdn.py` page, `_fused_gdn_kernel`,
+ *         init_state_z / the final z), the state of the same scan over
+ *         v = 1, so that a stream split into calls carries both. h0 and
  *         h_final may start at any 4-byte boundary; the bf16 path moves
  *         their rows by 16-byte accesses when the start is 16-byte aligned.
  *   cu_seqlens: device int32 (n_seq + 1) offsets of packed sequences, or NULL
  *         for B dense sequences of length T (n_seq must then equal B).
  *         With cu_seqlens, B must be 1; chunks never cross sequences.
  *   out:  (B, T, H, V), descriptor od, dtype GDN_F32 or GDN_BF16.
- *   h_final: (n_seq, H, K, V) fp32 state after the last token, or NULL.
+ *   h_final: (n_seq, H, K, V) fp32 state after the last token (V + 1
+ *         columns with den_out, as h0), or NULL.
  *   den_out: (B, H, T) fp32 denominator (the same scan with v = 1, SANA
- *         `fused_gdn.py` page, z state), or NULL.
+ *         `fused_gdn.py` page, z state), or NULL. With T = 0 any non-NULL
+ *         pointer selects the (V + 1)-column state; nothing is written.
  *   chunk: must be 64. K <= 128 (a multiple of 8), V (+1 with den_out) <= 256.
  *   reverse: 0 causal; 1 anti-causal flip-and-shift scan (SANA
  *         `fused_cam_gdn.py` page, `_flip_and_shift` and
  *         `_torch_cam_scan_reference`): o_t reads tokens t+1 .. end, token
  *         t+1's gate decays the state before its write, and no token reads
  *         itself. reverse with h0 or h_final -> GDN_ERR_UNSUPPORTED, as on
- *         the pages; den_out with h0 or h_final -> GDN_ERR_UNSUPPORTED.
+ *         the pages.
  *   flags: GDN_ACCUMULATE, GDN_QK_L2NORM.
  *   workspace: >= gdn_workspace_size() bytes, 256-byte aligned.
  */
@@ -369,7 +375,8 @@ gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den,
  *   q, k: (B, T, H, K) bf16 (prepared: gdn_prep); v: (B, T, H, V) bf16;
  *   g_frame: (B, T / frame, H) fp32 log decays (floored at -30);
  *   beta: (B, T, H) fp32; out: (B, T, H, V) bf16 or fp32; den_out: (B, H, T)
- *   fp32 or NULL; h0 / h_final: (B, H, K, V) fp32, direction 0 only.
+ *   fp32 or NULL; h0 / h_final: (B, H, K, V) fp32 (V + 1 columns with
+ *   den_out, column V the z state, as for gdn_chunk_fwd), direction 0 only.
  *   frame a multiple of 64 dividing T; K <= 128, V <= 256, both multiples
  *   of 8. flags: GDN_ACCUMULATE adds into out / den_out.
  * Workspace: gdn_frame_workspace_size() bytes (with_den as for the call).

@@ -149,15 +149,19 @@ def frame_den(q, k, beta, g_frame, frame, reverse=False, threads=None):
 
 
 def den(q, k, beta, g=None, gk=None, cu_seqlens=None, reverse=False,
-        threads=None):
+        threads=None, z0=None, with_state=False):
     """Denominator scan: the same recurrence with V = 1 and v = 1
-    (SANA `fused_gdn.py` page, `_fused_gdn_kernel` z-state). Returns
-    (B, H, T) float64."""
+    (SANA `fused_gdn.py` page, `_fused_gdn_kernel` z-state). z0: the z
+    state (n_seq, H, K) the scan starts from (init_state_z), or None for
+    zero. Returns (B, H, T) float64, and with with_state also the final z
+    state (n_seq, H, K)."""
     B, T, H, _ = np.shape(q)
     ones = np.ones((B, T, H, 1), dtype=np.float64)
-    out, _ = scan(q, k, ones, beta, g=g, gk=gk, cu_seqlens=cu_seqlens,
-                  reverse=reverse, threads=threads)
-    return np.ascontiguousarray(out[..., 0].transpose(0, 2, 1))
+    h0 = None if z0 is None else np.asarray(z0, dtype=np.float64)[..., None]
+    out, zf = scan(q, k, ones, beta, g=g, gk=gk, h0=h0, cu_seqlens=cu_seqlens,
+                   reverse=reverse, threads=threads)
+    d = np.ascontiguousarray(out[..., 0].transpose(0, 2, 1))
+    return (d, np.ascontiguousarray(zf[..., 0])) if with_state else d
 
 
 def state_summary(k, v, beta, segment_len, g=None, gk=None, threads=None):

@@ -109,7 +109,6 @@ def fwd(L, **kw):
     (dict(qkd=TensorDesc(gdn.BF16, 0, 128 * 2 * 64, 2 * 64 + 4, 64)), LAYOUT),
     (dict(g=ctypes.c_void_p(A + 2)), LAYOUT),
     (dict(reverse=1, h0=P(10)), UNSUP), (dict(reverse=1, hf=P(10)), UNSUP),
-    (dict(den=P(8), h0=P(10)), UNSUP),
     (dict(flags=0x80), UNSUP),
 ])
 def test_chunk_fwd_rejects_on_host(L, kw, code):

@@ -621,6 +621,62 @@ def test_orthogonal_keys_reverse_den_closed_form():
     assert np.abs(dc - ref).max() > 1e-3
 
 
+
+# the z state carried in and out of a call (`_fused_gdn_kernel`'s
+# init_state_z and its final z): z is a K-vector with
+#   z_t = e^{g_t} (I - beta_t k_t k_t^T) z_{t-1} + beta_t k_t,  den_t = q_t . z_t
+# (the rule's state with a single ones column; the matrix is symmetric)
+
+def test_den_z_state_matrix_recurrence():
+    rng = np.random.default_rng(33)
+    B, T, H, K = 2, 8, 3, 5
+    q, k = rng.standard_normal((B, T, H, K)), rng.standard_normal((B, T, H, K)) * 0.5
+    beta, g = rng.uniform(0, 1, (B, T, H)), -rng.uniform(0, 0.6, (B, T, H))
+    z0 = rng.standard_normal((B, H, K))
+    want = np.zeros((B, H, T))
+    zf = np.zeros((B, H, K))
+    for b in range(B):
+        for h in range(H):
+            z = z0[b, h].copy()
+            for t in range(T):
+                kt = k[b, t, h]
+                z = np.exp(g[b, t, h]) * (np.eye(K) - beta[b, t, h] * np.outer(kt, kt)) @ z + beta[b, t, h] * kt
+                want[b, h, t] = q[b, t, h] @ z
+            zf[b, h] = z
+    got, got_zf = oracle.den(q, k, beta, g=g, z0=z0, with_state=True)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got_zf, zf, rtol=1e-12, atol=1e-12)
+
+
+def test_den_z_state_beta_zero_closed_form():
+    """beta = 0: nothing is written, z_t = exp(sum_{s<=t} gk_s) * z0
+    elementwise (per-key gate), den_t = q_t . z_t."""
+    rng = np.random.default_rng(34)
+    T, K = 6, 4
+    q = rng.standard_normal((T, K))
+    gk = -rng.uniform(0, 0.5, (T, K))
+    z0 = rng.standard_normal(K)
+    zt = np.exp(np.cumsum(gk, axis=0)) * z0
+    d, zf = oracle.den(_one(q), _one(rng.standard_normal((T, K))), _one(np.zeros(T)), gk=_one(gk),
+                       z0=z0[None, None], with_state=True)
+    np.testing.assert_allclose(d[0, 0], np.einsum("tk,tk->t", q, zt), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(zf[0, 0], zt[-1], rtol=1e-13, atol=1e-13)
+
+
+def test_den_z_state_split_resume():
+    """A stream split into two calls, the second starting from the first's
+    final z, gives the unsplit denominator and final z."""
+    rng = np.random.default_rng(35)
+    T, K, t0 = 30, 6, 13
+    q, k = rng.standard_normal((T, K)), rng.standard_normal((T, K)) * 0.4
+    beta, g = rng.uniform(0, 1, T), -rng.uniform(0, 0.4, T)
+    full, zf = oracle.den(_one(q), _one(k), _one(beta), g=_one(g), with_state=True)
+    pre, zp = oracle.den(_one(q[:t0]), _one(k[:t0]), _one(beta[:t0]), g=_one(g[:t0]), with_state=True)
+    suf, zs = oracle.den(_one(q[t0:]), _one(k[t0:]), _one(beta[t0:]), g=_one(g[t0:]), z0=zp,
+                         with_state=True)
+    np.testing.assert_array_equal(full, np.concatenate([pre, suf], axis=2))
+    np.testing.assert_array_equal(zf, zs)
+
 def _frame_den_matrix(q, k, beta, gf, S, reverse):
     """Frame-rule denominator per (batch, head) as matrix products: z is a
     K-vector; a frame's write is z <- e^{g_f} z, z <- z + K_f^T diag(beta_f)

@@ -651,3 +651,120 @@ def test_small_bidirectional_segmented_resume_wide_state_tiles(wide_state_tiles)
     test_reverse_only_varlen_gk("bf16")
     test_split_resume_bit_exact("bf16")
     test_zero_tokens_pass_state_through("bf16")
+
+
+# ---- the denominator's z state carried in and out (SANA `fused_gdn.py` page,
+# `_fused_gdn_kernel`: init_state_z / the final z): with den, h0 and h_final
+# are (n_seq, H, K, V + 1) and column V is z, the state of the scan over v = 1
+
+def _den_state_ref(w, h0a, reverse=False):
+    """Oracle: the scan over [v, 1] from [h0, z0]; (out, den, h_final)."""
+    qn, kn = oracle.l2norm(w.q.values), oracle.l2norm(w.k.values)
+    va = np.concatenate([w.v.values, np.ones(w.v.values.shape[:-1] + (1,))], axis=-1)
+    oa, hfa = oracle.scan(qn, kn, va, w.beta, g=w.g, gk=w.gk, h0=h0a, cu_seqlens=w.cu_seqlens,
+                          reverse=reverse)
+    return oa[..., :-1], np.ascontiguousarray(oa[..., -1].transpose(0, 2, 1)), hfa
+
+
+DEN_STATE = {
+    "bf16_dense_v64": (dict(B=2, T=200, H=2, K=64, V=64, dtype="bf16"), False),
+    "bf16_varlen_gk": (dict(B=1, T=1 + 64 + 130 + 7, H=2, K=128, V=128, dtype="bf16",
+                            lengths=[1, 64, 130, 0, 7], g_mu=None, gk_mu=3.0), False),
+    "bf16_dense_fused": (dict(B=2, T=200, H=2, K=128, V=112, dtype="bf16"), True),
+    "f32_split": (dict(B=1, T=256, H=2, K=64, V=64, dtype="f32"), False),
+    "f32_fused_b20": (dict(B=20, T=130, H=2, K=64, V=64, dtype="f32"), False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DEN_STATE))
+def test_den_with_state_io(name):
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    spec, fused = DEN_STATE[name]
+    spec = dict(spec)
+    B, T, H, K, V, dt = (spec.pop(x) for x in ("B", "T", "H", "K", "V", "dtype"))
+    w = workloads.make(B, T, H, K, V, dt, seed=51, **spec)
+    h0a = workloads._normal_f32(52, "h0", w.n_seq * H * K * (V + 1), 0.0, 0.3).reshape(
+        w.n_seq, H, K, V + 1)
+    out_r, den_r, hf_r = _den_state_ref(w, h0a)
+    hf = torch.full((w.n_seq, H, K, V + 1), float("nan"), device="cuda")
+    den = torch.full((B, H, T), float("nan"), device="cuda")
+    gdn.gdn_set_fused(fused)
+    try:
+        out = gdn.gdn_chunk_fwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta),
+                                g=f32_dev(w.g), gk=f32_dev(w.gk), h0=f32_dev(h0a),
+                                cu_seqlens=i32_dev(w.cu_seqlens), h_final=hf, den=den,
+                                qk_l2norm=True)
+        torch.cuda.synchronize()
+    finally:
+        gdn.gdn_set_fused(False)
+    errs = {k: rel_err(a.double().cpu().numpy(), b)
+            for k, a, b in (("out", out, out_r), ("den", den, den_r), ("h_final", hf, hf_r))}
+    assert all(e <= TOL[dt] for e in errs.values()), (name, errs)
+
+
+def test_den_state_split_resume_and_wrong_shape():
+    """Two calls carrying [h, z] give the one-call num, den and final state
+    bit for bit; a state without the z column is refused on the host."""
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(1, 320, 2, 64, 64, "bf16", seed=53)
+    q, k, v = to_dev(w.q), to_dev(w.k), to_dev(w.v)
+    beta, g = f32_dev(w.beta), f32_dev(w.g)
+    hf = torch.empty((1, 2, 64, 65), device="cuda")
+    den = torch.empty((1, 2, 320), device="cuda")
+    full = gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h_final=hf, den=den, qk_l2norm=True)
+    t0 = 128
+    h1, h2 = torch.empty_like(hf), torch.empty_like(hf)
+    d1, d2 = torch.empty((1, 2, t0), device="cuda"), torch.empty((1, 2, 320 - t0), device="cuda")
+    a = gdn.gdn_chunk_fwd(q[:, :t0], k[:, :t0], v[:, :t0], beta[:, :t0].contiguous(),
+                          g=g[:, :t0].contiguous(), h_final=h1, den=d1, qk_l2norm=True)
+    b = gdn.gdn_chunk_fwd(q[:, t0:], k[:, t0:], v[:, t0:], beta[:, t0:].contiguous(),
+                          g=g[:, t0:].contiguous(), h0=h1, h_final=h2, den=d2, qk_l2norm=True)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.cat([a, b], 1), full)
+    assert torch.equal(torch.cat([d1, d2], 2), den)
+    assert torch.equal(h2, hf)
+    with pytest.raises(ValueError):
+        gdn.gdn_chunk_fwd(q, k, v, beta, g=g, h0=torch.zeros((1, 2, 64, 64), device="cuda"),
+                          den=den, qk_l2norm=True)
+
+
+def test_den_state_zero_tokens_and_segments():
+    """T = 0 passes [h, z] through; the segment-parallel pass carries it."""
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w0 = workloads.make(2, 0, 2, 64, 64, "bf16", seed=54)
+    h0a = workloads._normal_f32(55, "h0", 2 * 2 * 64 * 65, 0.0, 0.5).reshape(2, 2, 64, 65)
+    hf = torch.full((2, 2, 64, 65), float("nan"), device="cuda")
+    gdn.gdn_chunk_fwd(to_dev(w0.q), to_dev(w0.k), to_dev(w0.v), f32_dev(w0.beta), g=f32_dev(w0.g),
+                      h0=f32_dev(h0a), h_final=hf, den=torch.empty((2, 2, 0), device="cuda"))
+    torch.cuda.synchronize()
+    assert np.array_equal(hf.cpu().numpy(), h0a)
+    w = workloads.make(1, 700, 2, 128, 128, "bf16", seed=56)
+    h0b = workloads._normal_f32(57, "h0", 2 * 128 * 129, 0.0, 0.3).reshape(1, 2, 128, 129)
+    out_r, den_r, hf_r = _den_state_ref(w, h0b)
+    hf = torch.full((1, 2, 128, 129), float("nan"), device="cuda")
+    den = torch.full((1, 2, 700), float("nan"), device="cuda")
+    out = gdn.gdn_chunk_fwd_seg(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), 192,
+                                g=f32_dev(w.g), h0=f32_dev(h0b), h_final=hf, den=den,
+                                qk_l2norm=True)
+    torch.cuda.synchronize()
+    for a, b in ((out, out_r), (den, den_r), (hf, hf_r)):
+        assert rel_err(a.double().cpu().numpy(), b) <= TOL["bf16"]
+
+
+def test_bidirectional_forward_carries_den_state():
+    """gdn_forward(bidirectional, h0, with_final_state): the causal direction
+    runs from [h0, z0] and returns its [h, z]; the reverse starts from zero."""
+    import gated_delta_rule_18_gb300 as gdn
+    import torch
+    w = workloads.make(2, 170, 2, 64, 64, "bf16", seed=58)
+    h0a = workloads._normal_f32(59, "h0", 2 * 2 * 64 * 65, 0.0, 0.3).reshape(2, 2, 64, 65)
+    of, df, hf_r = _den_state_ref(w, h0a)
+    orv, drv, _ = _den_state_ref(w, None, reverse=True)
+    res = gdn.gdn_forward(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), g=f32_dev(w.g),
+                          h0=f32_dev(h0a), bidirectional=True, with_final_state=True)
+    torch.cuda.synchronize()
+    for key, ref in (("out", of + orv), ("den", df + drv), ("h_final", hf_r)):
+        assert rel_err(res[key].double().cpu().numpy(), ref) <= TOL["bf16"], key
