@@ -696,6 +696,9 @@ def main():
                          "of a dense causal workload instead of the forward")
     ap.add_argument("--graph-replay", type=int, default=0,
                     help="also time N back-to-back calls captured in one CUDA graph (forward pass)")
+    ap.add_argument("--fused", action="store_true",
+                    help="run the bf16 scalar-gate forward as the single fused kernel "
+                         "(gdn_set_fused; the split passes are the default)")
     ap.add_argument("--segment-len", type=int, default=None,
                     help="segment-parallel state passing with this many tokens per segment "
                          "(0: one pass per sequence); default: the workload's own setting")
@@ -720,29 +723,33 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
+    gdn.gdn_set_fused(args.fused)
     w = workloads.build(args.workload, seed=rank, T=args.T)  # each replica its own data
     if args.segment_len is not None:
         w = dataclasses.replace(w, segment_len=args.segment_len or None)
     w = resolve_segments(gdn, w, dev)
     d = device_inputs(w, dev)
     if args.pass_ == "bwd":
-        if w.dtype != "bf16" or w.bidirectional or w.gk is not None or w.cu_seqlens is not None \
-                or w.frame > 1:
-            raise SystemExit("--pass bwd takes a dense causal bf16 workload with a scalar gate")
+        if w.dtype != "bf16" or w.bidirectional or w.gk is not None or w.frame > 1:
+            raise SystemExit("--pass bwd takes a causal bf16 workload with a scalar gate")
         d["dout"] = torch.from_numpy(workloads.stored_normal(
             rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
-        ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V), dtype=torch.uint8,
+        ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq,
+                                                    w.cu_seqlens is not None), dtype=torch.uint8,
                          device=dev)
         args.no_e2e = args.no_cpu_baseline = args.no_configs = True
 
         def run(gdn, w, d, ws):  # the timed step of this pass
             return gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dout"],
-                                     h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws)
+                                     h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws,
+                                     cu_seqlens=d.get("cu_seqlens"))
     else:
         ws = workspace_for(gdn, w, dev)
         run = run_step
     stream = torch.cuda.current_stream()
     config, flush = config_of(w, args.workload, world)
+    if args.fused:
+        config = dict(config, path="fused single-kernel forward (opt-in)")
     scrub = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
     sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ

@@ -292,6 +292,7 @@ gdn_status fwd_setup(const void *q, const void *k, gdn_tensor_desc qkd, const vo
     p.l2norm = (flags & GDN_QK_L2NORM) ? 1 : 0;
     p.has_den = den_out != nullptr;
     p.Vt = L.Vt;
+    p.h_ld = L.Vt;
     p.max_chunks = L.max_chunks;
     p.n_vt = L.n_vt;
     p.stall_cta = g_stall_cta.load();
@@ -507,19 +508,25 @@ namespace {
 // backward sections after the forward workspace: bf16 snapshots of the state
 // entering each chunk, v_new, the state gradient at each chunk's end, dv_new
 struct BwdWs {
-    size_t h, vn, dh, dvn, total;
+    size_t h, vn, dh, dvn, dkp, dgp, total;
 };
-bool bwd_layout(const Ws &L, int H, int K, int V, BwdWs &S) {
+// after the forward's workspace L (of one value range of at most 128
+// columns): the snapshots of that range, then bwd_dq's shares of dk and dG
+bool bwd_layout(const Ws &L, int B, int T, int H, int K, int Vp, BwdWs &S) {
     const size_t hc = (size_t)H * L.max_chunks;
     size_t off = L.total;
     S.h = off;
-    off = align_up(off + hc * K * V * 2);
+    off = align_up(off + hc * K * Vp * 2);
     S.vn = off;
-    off = align_up(off + hc * gdn::kChunk * V * 2);
+    off = align_up(off + hc * gdn::kChunk * Vp * 2);
     S.dh = off;
-    off = align_up(off + hc * K * V * 2);
+    off = align_up(off + hc * K * Vp * 2);
     S.dvn = off;
-    off = align_up(off + hc * gdn::kChunk * V * 2);
+    off = align_up(off + hc * gdn::kChunk * Vp * 2);
+    S.dkp = off;
+    off = align_up(off + (size_t)B * T * H * K * 4);
+    S.dgp = off;
+    off = align_up(off + (size_t)B * T * H * 4);
     S.total = off;
     return true;
 }
@@ -527,72 +534,101 @@ bool bwd_layout(const Ws &L, int H, int K, int V, BwdWs &S) {
 
 extern "C" {
 
-size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V) {
+size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq, int varlen,
+                              int perkey) {
     Ws L;
     BwdWs S;
-    if (V > 128 || !ws_layout(B, T, H, K, V, B, 0, GDN_BF16, 0, L)) return 0;
-    bwd_layout(L, H, K, V, S);
+    if (perkey || V < 1 || V > 256) return 0;
+    const int Vp = V > 128 ? 128 : V;
+    if (!ws_layout(B, T, H, K, Vp, n_seq, varlen, GDN_BF16, 0, L)) return 0;
+    bwd_layout(L, B, T, H, K, Vp, S);
     return S.total;
 }
 
 gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
-                         gdn_tensor_desc vd, const float *g, const float *beta, const float *h0,
-                         const void *dout, gdn_tensor_desc dod, const float *dh_final, float *dq,
-                         float *dk, float *dv, float *dbeta, float *dg, float *dh0, int B, int T,
-                         int H, int K, int V, int chunk, int reverse, int flags, void *workspace,
+                         gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
+                         const float *h0, const int32_t *cu_seqlens, int n_seq, const void *dout,
+                         gdn_tensor_desc dod, const float *dh_final, float *dq, float *dk,
+                         float *dv, float *dbeta, float *dg, float *dh0, int B, int T, int H, int K,
+                         int V, int chunk, int reverse, int flags, void *workspace,
                          size_t ws_bytes, cudaStream_t stream) {
     if (T > 0 && (!dout || !dq || !dk || !dv || !dbeta || !dg)) return GDN_ERR_NULL;
     if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16 || (T > 0 && dod.dtype != GDN_BF16))
         return GDN_ERR_DTYPE;
     if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;
+    if (gk) return GDN_ERR_UNSUPPORTED;
     if (reverse && (h0 || dh_final || dh0)) return GDN_ERR_UNSUPPORTED;
-    if (V > 128) return GDN_ERR_SHAPE;
+    if (V < 1 || V > 256 || V % 8 != 0) return GDN_ERR_SHAPE;
     if (!aligned16(dout) || !strides_ok(dod)) return GDN_ERR_LAYOUT;
     for (const void *f : {(const void *)dq, (const void *)dk, (const void *)dv, (const void *)dbeta,
                           (const void *)dg, (const void *)dh0, (const void *)dh_final})
         if (f && (reinterpret_cast<uintptr_t>(f) & 7)) return GDN_ERR_LAYOUT;
+    // The value columns of the state evolve independently given k, beta and
+    // g, so the gradient is formed over ranges of at most 128 columns: dv
+    // and dh0 per range, dq, dk, dbeta and dg summed over the ranges.
+    const int Vp = V > 128 ? 128 : V;
     Ws L;
     gdn::FwdParams p;
-    // the forward recompute: no outputs, the snapshots instead
-    gdn_status st = fwd_setup(q, k, qkd, v, vd, g, nullptr, beta, h0, nullptr, B, nullptr,
+    // the forward recompute of the first range: no outputs, the snapshots instead
+    gdn_status st = fwd_setup(q, k, qkd, v, vd, g, gk, beta, h0, cu_seqlens, n_seq, nullptr,
                               gdn_tensor_desc{GDN_BF16, 0, 0, 0, 0}, nullptr, nullptr, B, T, H, K,
-                              V, chunk, reverse, flags, false, L, p);
+                              Vp, chunk, reverse, flags, false, L, p);
     if (st != GDN_OK) return st;
     BwdWs S;
-    bwd_layout(L, H, K, V, S);
+    bwd_layout(L, B, T, H, K, Vp, S);
     if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
     if (T == 0) {  // dL/dh0 = dL/dh_final
         if (!dh0) return GDN_OK;
-        const size_t n = (size_t)B * H * K * V * sizeof(float);
+        const size_t n = (size_t)n_seq * H * K * V * sizeof(float);
         cudaError_t e = dh_final ? cudaMemcpyAsync(dh0, dh_final, n, cudaMemcpyDeviceToDevice, stream)
                                  : cudaMemsetAsync(dh0, 0, n, stream);
         return cuda_status(e);
     }
     unsigned char *ws = static_cast<unsigned char *>(workspace);
-    bind_ws(ws, L, p);
-    p.h_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.h);
-    p.vn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.vn);
-    cudaError_t e = clear_err(p, stream);
-    if (e == cudaSuccess) e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, 0, stream); });
-    if (e == cudaSuccess) e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
-    if (e != cudaSuccess) return GDN_ERR_CUDA;
-    gdn::BwdParams b{};
-    b.q = q, b.k = k, b.v = v, b.dout = dout;
-    b.qk_sb = qkd.stride_b, b.qk_st = qkd.stride_t, b.qk_sh = qkd.stride_h;
-    b.v_sb = vd.stride_b, b.v_st = vd.stride_t, b.v_sh = vd.stride_h;
-    b.do_sb = dod.stride_b, b.do_st = dod.stride_t, b.do_sh = dod.stride_h;
-    b.g = g, b.beta = beta, b.dh_final = dh_final;
-    b.dq = dq, b.dk = dk, b.dv = dv, b.dbeta = dbeta, b.dg = dg, b.dh0 = dh0;
-    b.B = B, b.T = T, b.H = H, b.K = K, b.V = V, b.reverse = reverse, b.l2norm = p.l2norm;
-    b.max_chunks = L.max_chunks;
-    b.w_img = p.w_img, b.qg_img = p.qg_img, b.kg_img = p.kg_img, b.p_img = p.p_img, b.dec = p.dec;
-    b.h_snap = p.h_snap, b.vn_snap = p.vn_snap;
-    b.dh_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dh);
-    b.dvn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dvn);
-    b.err = p.err;
-    e = launch(KBwdDh, stream, [&] { return gdn::launch_bwd_dh(b, stream); });
-    if (e == cudaSuccess) e = launch(KBwdDq, stream, [&] { return gdn::launch_bwd_dq(b, stream); });
-    if (e == cudaSuccess) e = launch(KBwdDk, stream, [&] { return gdn::launch_bwd_dk(b, stream); });
+    cudaError_t e = cudaSuccess;
+    for (int v_off = 0; v_off < V && e == cudaSuccess; v_off += 128) {
+        const int Vh = V - v_off < 128 ? V - v_off : 128;
+        const __nv_bfloat16 *vr = static_cast<const __nv_bfloat16 *>(v) + v_off;
+        if (v_off > 0) {  // the same checks passed for the first range
+            st = fwd_setup(q, k, qkd, vr, vd, g, gk, beta, h0 ? h0 + v_off : nullptr, cu_seqlens,
+                           n_seq, nullptr, gdn_tensor_desc{GDN_BF16, 0, 0, 0, 0}, nullptr, nullptr,
+                           B, T, H, K, Vh, chunk, reverse, flags, false, L, p);
+            if (st != GDN_OK) return st;
+        }
+        p.h_ld = V;  // h0 rows keep all V columns
+        bind_ws(ws, L, p);
+        p.h_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.h);
+        p.vn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.vn);
+        if (v_off == 0) e = clear_err(p, stream);
+        if (e == cudaSuccess && cu_seqlens)
+            e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
+        if (e == cudaSuccess) e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, 0, stream); });
+        if (e == cudaSuccess) e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
+        if (e != cudaSuccess) return GDN_ERR_CUDA;
+        gdn::BwdParams b{};
+        b.q = q, b.k = k, b.v = vr, b.dout = static_cast<const __nv_bfloat16 *>(dout) + v_off;
+        b.qk_sb = qkd.stride_b, b.qk_st = qkd.stride_t, b.qk_sh = qkd.stride_h;
+        b.v_sb = vd.stride_b, b.v_st = vd.stride_t, b.v_sh = vd.stride_h;
+        b.do_sb = dod.stride_b, b.do_st = dod.stride_t, b.do_sh = dod.stride_h;
+        b.g = g, b.beta = beta, b.dh_final = dh_final ? dh_final + v_off : nullptr;
+        b.dq = dq, b.dk = dk, b.dv = dv + v_off, b.dbeta = dbeta, b.dg = dg;
+        b.dh0 = dh0 ? dh0 + v_off : nullptr;
+        b.B = B, b.T = T, b.H = H, b.K = K, b.V = Vh, b.reverse = reverse, b.l2norm = p.l2norm;
+        b.max_chunks = L.max_chunks;
+        b.cu_seqlens = cu_seqlens, b.n_seq = n_seq;
+        b.n_chunks = p.n_chunks, b.chunk_tab = p.chunk_tab, b.seq_chunk0 = p.seq_chunk0;
+        b.vfull = V, b.v_off = v_off, b.acc = v_off > 0;
+        b.dk_part = reinterpret_cast<float *>(ws + S.dkp);
+        b.dg_part = reinterpret_cast<float *>(ws + S.dgp);
+        b.w_img = p.w_img, b.qg_img = p.qg_img, b.kg_img = p.kg_img, b.p_img = p.p_img, b.dec = p.dec;
+        b.h_snap = p.h_snap, b.vn_snap = p.vn_snap;
+        b.dh_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dh);
+        b.dvn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dvn);
+        b.err = p.err;
+        e = launch(KBwdDh, stream, [&] { return gdn::launch_bwd_dh(b, stream); });
+        if (e == cudaSuccess) e = launch(KBwdDq, stream, [&] { return gdn::launch_bwd_dq(b, stream); });
+        if (e == cudaSuccess) e = launch(KBwdDk, stream, [&] { return gdn::launch_bwd_dk(b, stream); });
+    }
     return cuda_status(e);
 }
 

@@ -52,8 +52,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
     const int g8 = lane >> 2, t4 = lane & 3;
     const int s = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     const int v0 = blockIdx.y * 64;
-    const int K = p.K, V = p.V, T = p.T;
+    const int K = p.K, V = p.V;
+    if (p.cu_seqlens && *p.n_chunks < 0) return;  // a bad cu_seqlens: nothing was recomputed
+    // the sequence: its tokens at flat rows b * T + tstart + t, its chunks at
+    // global chunk slots c0 .. c0 + nts - 1
+    const int b = p.cu_seqlens ? 0 : s, tstart = p.cu_seqlens ? p.cu_seqlens[s] : 0;
+    const int T = p.cu_seqlens ? p.cu_seqlens[s + 1] - tstart : p.T;
     const int nts = (T + kChunk - 1) / kChunk;
+    const int c0 = p.cu_seqlens ? p.seq_chunk0[s] : s * nts;
     const bf16 *dout = (const bf16 *)p.dout;
     const uint32_t bar[2] = {smem_u32(&bars[0]), smem_u32(&bars[1])};
     if (tid == 0) {
@@ -64,7 +70,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
     __syncthreads();
 
     // step `it` handles chunk nts - 1 - it in stage it & 1
-    auto gch_of = [&](int it) { return (int64_t)hh * p.max_chunks + (int64_t)s * nts + (nts - 1 - it); };
+    auto gch_of = [&](int it) { return (int64_t)hh * p.max_chunks + c0 + (nts - 1 - it); };
     auto stage = [&](int it) {
         DhStage &S = sm.st[it & 1];
         const int c = nts - 1 - it;
@@ -83,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
             const int i = e >> 3, c8 = (e & 7) * 8, col = v0 + c8;
             const bool in = i < Lc && col < V;
             const int tq = in ? q_token(p.reverse, T, pos0 + i) : 0;
-            const bf16 *src = in ? dout + s * p.do_sb + (int64_t)tq * p.do_st + hh * p.do_sh + col : dout;
+            const bf16 *src = in ? dout + b * p.do_sb + (int64_t)(tstart + tq) * p.do_st + hh * p.do_sh + col : dout;
             cp_async16(S.dout + i * kL6 + c8, src, in ? 16 : 0);
         }
         cp_async_commit();
@@ -96,8 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int r = 16 * warp + g8 + 8 * (e >> 1), col = v0 + 8 * n + 2 * t4 + (e & 1);
-            acc[n][e] = (p.dh_final && r < K && col < V) ? p.dh_final[(((int64_t)s * p.H + hh) * K + r) * V + col]
-                                                         : 0.f;
+            acc[n][e] = (p.dh_final && r < K && col < V)
+                            ? p.dh_final[(((int64_t)s * p.H + hh) * K + r) * p.vfull + col]
+                            : 0.f;
         }
     if (nts > 0) stage(0);
     bool ok = true;
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = 16 * warp + g8 + 8 * (e >> 1), col = v0 + 8 * n + 2 * t4 + (e & 1);
-                if (r < K && col < V) p.dh0[(((int64_t)s * p.H + hh) * K + r) * V + col] = acc[n][e];
+                if (r < K && col < V) p.dh0[(((int64_t)s * p.H + hh) * K + r) * p.vfull + col] = acc[n][e];
             }
     }
 }
@@ -235,7 +242,7 @@ cudaError_t launch_bwd_dh(const BwdParams &p, cudaStream_t st) {
     const int bytes = (int)sizeof(DhSmem);
     cudaError_t e = cudaFuncSetAttribute(bwd_dh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    bwd_dh_kernel<<<dim3(p.B * p.H, (p.V + 63) / 64), kThreads, bytes, st>>>(p);
+    bwd_dh_kernel<<<dim3(p.n_seq * p.H, (p.V + 63) / 64), kThreads, bytes, st>>>(p);
     return cudaGetLastError();
 }
 

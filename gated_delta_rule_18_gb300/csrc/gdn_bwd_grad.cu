@@ -46,20 +46,31 @@ constexpr int kPS = kChunk + 1;  // fp32 64 x 64 row stride
 
 __device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
 
-// common per-chunk addressing
+// common per-chunk addressing: chunk c of sequence s (s < 0: no chunk in
+// this slot), its tokens at flat rows row0 + t (row0 = b * T + tstart)
 struct ChunkCtx {
-    int s, hh, c, pos0, Lc;
+    int s, hh, c, pos0, Lc, len, b, tstart;
+    int64_t row0;
     int64_t gch;  // [head][global chunk] image / snapshot slot
 };
 __device__ __forceinline__ ChunkCtx chunk_ctx(const BwdParams &p) {
     ChunkCtx x;
-    const int nts = (p.T + kChunk - 1) / kChunk;
     x.hh = blockIdx.x % p.H;
     const int gid = blockIdx.x / p.H;
-    x.s = gid / nts;
-    x.c = gid - x.s * nts;
+    x.s = -1;
+    if (p.cu_seqlens) {  // the forward's chunk table (a bad cu_seqlens leaves it empty)
+        if (gid >= *p.n_chunks) return x;
+        const int2 e = p.chunk_tab[gid];
+        x.s = e.x, x.c = e.y;
+        x.b = 0, x.tstart = p.cu_seqlens[x.s], x.len = p.cu_seqlens[x.s + 1] - x.tstart;
+    } else {
+        const int nts = (p.T + kChunk - 1) / kChunk;
+        x.s = gid / nts, x.c = gid - x.s * nts;
+        x.b = x.s, x.tstart = 0, x.len = p.T;
+    }
     x.pos0 = x.c * kChunk;
-    x.Lc = min(kChunk, p.T - x.pos0);
+    x.Lc = min(kChunk, x.len - x.pos0);
+    x.row0 = (int64_t)x.b * p.T + x.tstart;
     x.gch = (int64_t)x.hh * p.max_chunks + gid;
     return x;
 }
@@ -144,8 +155,8 @@ __device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_ou
 __device__ __forceinline__ void gates(const BwdParams &p, const ChunkCtx &x, float *sG, float *sB, float *graw) {
     const int tid = threadIdx.x;
     if (tid < kChunk) {
-        const int tk = tid < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + tid) : -1;
-        const int64_t row = ((int64_t)x.s * p.T + tk) * p.H + x.hh;
+        const int tk = tid < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + tid) : -1;
+        const int64_t row = (x.row0 + tk) * p.H + x.hh;
         const float g = tk >= 0 ? p.g[row] : 0.f;
         graw[tid] = g;
         sG[tid] = tk >= 0 ? fmaxf(g, kLogGateMin) : 0.f;
@@ -179,23 +190,25 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
     const ChunkCtx x = chunk_ctx(p);
-    if (x.s >= p.B) return;
+    if (x.s < 0) return;
     const int K = p.K, V = p.V, kq = round16(K), kv = round16(V);
     const bf16 *q = (const bf16 *)p.q, *k = (const bf16 *)p.k, *dout = (const bf16 *)p.dout;
 
     load_rows(sm.q, kLK, kChunk, K, [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
-        return q + x.s * p.qk_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.qk_st + x.hh * p.qk_sh;
+        return q + x.b * p.qk_sb + (int64_t)(x.tstart + q_token(p.reverse, x.len, x.pos0 + i)) * p.qk_st +
+               x.hh * p.qk_sh;
     });
     load_rows(sm.k, kLK, kChunk, K, [&](int i) -> const bf16 * {
-        const int tk = i < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + i) : -1;
+        const int tk = i < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + i) : -1;
         if (tk < 0) return nullptr;
-        return k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
+        return k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
     cp_async_commit();  // q and k first: the norms and Q K^T start while the rest lands
     load_rows(sm.dout, kLK, kChunk, V, [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
-        return dout + x.s * p.do_sb + (int64_t)q_token(p.reverse, p.T, x.pos0 + i) * p.do_st + x.hh * p.do_sh;
+        return dout + x.b * p.do_sb + (int64_t)(x.tstart + q_token(p.reverse, x.len, x.pos0 + i)) * p.do_st +
+               x.hh * p.do_sh;
     });
     load_rows(sm.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.vn_snap + (x.gch * kChunk + i) * V;
@@ -296,8 +309,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
     for (int hf = 0; hf < 2; ++hf) {
         const int i = m0 + g8 + 8 * hf;
         if (i >= x.Lc) continue;
-        const int tq = q_token(p.reverse, p.T, x.pos0 + i);
-        float *dst = p.dq + (((int64_t)x.s * p.T + tq) * p.H + x.hh) * K;
+        const int tq = q_token(p.reverse, x.len, x.pos0 + i);
+        float *dst = p.dq + ((x.row0 + tq) * p.H + x.hh) * K;
         const float r = sm.rq[i], dot = sm.row[i];
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
@@ -307,6 +320,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
             o.x = p.l2norm ? r * (dq[n][2 * hf] - __bfloat162float(sm.q[i * kLK + d]) * dot) : dq[n][2 * hf];
             o.y = p.l2norm ? r * (dq[n][2 * hf + 1] - __bfloat162float(sm.q[i * kLK + d + 1]) * dot)
                            : dq[n][2 * hf + 1];
+            if (p.acc) {
+                const float2 a = *reinterpret_cast<const float2 *>(dst + d);
+                o.x += a.x, o.y += a.y;
+            }
             *reinterpret_cast<float2 *>(dst + d) = o;
         }
     }
@@ -318,9 +335,9 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int j = m0 + g8 + 8 * hf;
-            const int tk = j < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + j) : -1;
+            const int tk = j < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + j) : -1;
             if (tk < 0) continue;
-            float *dst = p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K;
+            float *dst = p.dk_part + ((x.row0 + tk) * p.H + x.hh) * K;
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
                 const int d = nk0 + 8 * n + 2 * t4;
@@ -330,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
     }
     __syncthreads();
     if (tid < x.Lc) {  // this kernel's share of dG, at the kv rows (bwd_dk adds the rest)
-        const int tk = kv_token(p.reverse, p.T, x.pos0 + tid);
-        if (tk >= 0) p.dg[((int64_t)x.s * p.T + tk) * p.H + x.hh] = sm.dG[tid];
+        const int tk = kv_token(p.reverse, x.len, x.pos0 + tid);
+        if (tk >= 0) p.dg_part[(x.row0 + tk) * p.H + x.hh] = sm.dG[tid];
     }
 }
 
@@ -365,19 +382,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, t4 = lane & 3;
     const ChunkCtx x = chunk_ctx(p);
-    if (x.s >= p.B) return;
+    if (x.s < 0) return;
     const int K = p.K, V = p.V, kq = round16(K), kv = round16(V);
     const bf16 *k = (const bf16 *)p.k, *v = (const bf16 *)p.v;
-    auto kv_row = [&](int i) { return i < x.Lc ? kv_token(p.reverse, p.T, x.pos0 + i) : -1; };
+    auto kv_row = [&](int i) { return i < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + i) : -1; };
 
     load_rows(sm.k, kLK, kChunk, K, [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
-        return tk < 0 ? nullptr : k + x.s * p.qk_sb + (int64_t)tk * p.qk_st + x.hh * p.qk_sh;
+        return tk < 0 ? nullptr : k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
     cp_async_commit();  // k first: the norms and K K^T start while the rest lands
     load_rows(sm.v, kLK, kChunk, V, [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
-        return tk < 0 ? nullptr : v + x.s * p.v_sb + (int64_t)tk * p.v_st + x.hh * p.v_sh;
+        return tk < 0 ? nullptr : v + x.b * p.v_sb + (int64_t)(x.tstart + tk) * p.v_st + x.hh * p.v_sh;
     });
     load_rows(sm.dvn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.dvn_snap + (x.gch * kChunk + i) * V;
@@ -398,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         const int tk = kv_row(m0 + g8 + 8 * hf);
-        const float *src = tk >= 0 ? p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K : nullptr;
+        const float *src = tk >= 0 ? p.dk_part + ((x.row0 + tk) * p.H + x.hh) * K : nullptr;
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
             const int d = nk0 + 8 * n + 2 * t4;
@@ -707,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         for (int hf = 0; hf < 2; ++hf) {
             const int i = m0 + g8 + 8 * hf;
             const int tk = kv_row(i);
-            float *dst = tk >= 0 ? p.dv + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * V : nullptr;
+            float *dst = tk >= 0 ? p.dv + ((x.row0 + tk) * p.H + x.hh) * p.vfull : nullptr;
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
                 const int c = nk0 + 8 * n + 2 * t4;
@@ -733,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         const int i = m0 + g8 + 8 * hf;
         const int tk = kv_row(i);
         if (tk < 0) continue;
-        float *dst = p.dk + (((int64_t)x.s * p.T + tk) * p.H + x.hh) * K;
+        float *dst = p.dk + ((x.row0 + tk) * p.H + x.hh) * K;
         const float r = sm.rk[i], dot = sm.row[i];
 #pragma unroll
         for (int n = 0; n < 8; ++n) {
@@ -743,14 +760,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             o.x = p.l2norm ? r * (dk[n][2 * hf] - __bfloat162float(sm.k[i * kLK + d]) * dot) : dk[n][2 * hf];
             o.y = p.l2norm ? r * (dk[n][2 * hf + 1] - __bfloat162float(sm.k[i * kLK + d + 1]) * dot)
                            : dk[n][2 * hf + 1];
+            if (p.acc) {
+                const float2 a = *reinterpret_cast<const float2 *>(dst + d);
+                o.x += a.x, o.y += a.y;
+            }
             *reinterpret_cast<float2 *>(dst + d) = o;
         }
     }
     // the reverse scan never reads token 0's key and value: zero gradients
     if (p.reverse && x.c == 0) {
-        const int64_t row = (int64_t)x.s * p.T * p.H + x.hh;
+        const int64_t row = x.row0 * p.H + x.hh;
         for (int e = tid; e < K; e += kThreads) p.dk[row * K + e] = 0.f;
-        for (int e = tid; e < V; e += kThreads) p.dv[row * V + e] = 0.f;
+        for (int e = tid; e < V; e += kThreads) p.dv[row * p.vfull + e] = 0.f;
         if (tid == 0) p.dbeta[row] = p.dg[row] = 0.f;
     }
     // dbeta, and dg = suffix sums of dG within the chunk (G is the running sum of g)
@@ -758,8 +779,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         float d0 = 0.f, d1 = 0.f;
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
         const int t0 = kv_row(i0), t1 = kv_row(i1);
-        if (t0 >= 0) d0 = sm.dG[i0] + p.dg[((int64_t)x.s * p.T + t0) * p.H + x.hh];
-        if (t1 >= 0) d1 = sm.dG[i1] + p.dg[((int64_t)x.s * p.T + t1) * p.H + x.hh];
+        if (t0 >= 0) d0 = sm.dG[i0] + p.dg_part[(x.row0 + t0) * p.H + x.hh];
+        if (t1 >= 0) d1 = sm.dG[i1] + p.dg_part[(x.row0 + t1) * p.H + x.hh];
         if (i0 == last) d0 += sm.gc;
         if (i1 == last) d1 += sm.gc;
         // suffix sum over lanes of the pair sums
@@ -770,15 +791,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             if (lane + o < 32) incl += y;
         }
         const float s1 = incl - d0, s0 = incl;  // dg at i1 and at i0
+        // (a later value range adds to the earlier ranges' sums)
         if (t0 >= 0) {
-            const int64_t row = ((int64_t)x.s * p.T + t0) * p.H + x.hh;
-            p.dg[row] = sm.graw[i0] < kLogGateMin ? 0.f : s0;
-            p.dbeta[row] = sm.dB[i0];
+            const int64_t row = (x.row0 + t0) * p.H + x.hh;
+            const float dg0 = sm.graw[i0] < kLogGateMin ? 0.f : s0;
+            p.dg[row] = p.acc ? p.dg[row] + dg0 : dg0;
+            p.dbeta[row] = p.acc ? p.dbeta[row] + sm.dB[i0] : sm.dB[i0];
         }
         if (t1 >= 0) {
-            const int64_t row = ((int64_t)x.s * p.T + t1) * p.H + x.hh;
-            p.dg[row] = sm.graw[i1] < kLogGateMin ? 0.f : s1;
-            p.dbeta[row] = sm.dB[i1];
+            const int64_t row = (x.row0 + t1) * p.H + x.hh;
+            const float dg1 = sm.graw[i1] < kLogGateMin ? 0.f : s1;
+            p.dg[row] = p.acc ? p.dg[row] + dg1 : dg1;
+            p.dbeta[row] = p.acc ? p.dbeta[row] + sm.dB[i1] : sm.dB[i1];
         }
     }
 }
@@ -787,8 +811,7 @@ template <class Kern>
 cudaError_t launch_grid(Kern kern, int bytes, const BwdParams &p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    const int nts = (p.T + kChunk - 1) / kChunk;
-    kern<<<p.B * nts * p.H, kThreads, bytes, st>>>(p);
+    kern<<<p.max_chunks * p.H, kThreads, bytes, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -39,6 +39,8 @@ struct FwdParams {
     int B, T, H, K, V, n_seq;
     int reverse, accumulate, l2norm, has_den;
     int Vt;  // V + has_den: value columns carried by the scan
+    int h_ld;  // row stride (floats) of h0 / h_final in the bf16 state pass: Vt, or the
+               // full width when a backward pass recomputes one value-column range
     // workspace
     int *err;         // device error word
     int *n_chunks;    // number of valid chunk-table entries (varlen)
@@ -83,7 +85,17 @@ struct BwdParams {
     const float *g, *beta, *dh_final;
     float *dq, *dk, *dv, *dbeta, *dg, *dh0;
     int B, T, H, K, V, reverse, l2norm;
-    int max_chunks;  // chunks per head: B * ceil(T / 64)
+    int max_chunks;  // chunk slots per head (the forward's)
+    // variable-length batches: the forward's chunk table (B == 1)
+    const int32_t *cu_seqlens;
+    const int *n_chunks, *seq_chunk0;
+    const int2 *chunk_tab;
+    int n_seq;
+    // one pass covers value columns [v_off, v_off + V) of vfull: dout, v, dv,
+    // dh_final and dh0 point at column v_off and keep rows of vfull columns
+    int vfull, v_off;
+    int acc;                 // add dq, dk, dbeta, dg into the outputs (a later value range)
+    float *dk_part, *dg_part;  // bwd_dq's shares of dk and dG, read by bwd_dk (workspace)
     // the forward's per-chunk operand images and snapshots (workspace)
     const unsigned char *w_img, *qg_img, *kg_img, *p_img;
     const float *dec;

@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = tid;
         float h[64];
         if (p.h0 && r < K) {
-            load_row64(h, p.h0 + (bh * K + r) * p.Vt, v0, p.Vt);
+            load_row64(h, p.h0 + (bh * K + r) * p.h_ld, v0, p.Vt);
         } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c) h[c] = 0.f;
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
         }
         if (ok && warp >= 2 && nchunks > 0) ok = output(nchunks - 1, tid - 64);
-        if (ok && p.h_final && r < K) store_row64(p.h_final + (bh * K + r) * p.Vt, h, v0, p.Vt);
+        if (ok && p.h_final && r < K) store_row64(p.h_final + (bh * K + r) * p.h_ld, h, v0, p.Vt);
     } else if (warp == 4 || warp == 5) {
         // ------------------------------------- v_new helpers (columns 32..63)
         const int i = tid - 128;

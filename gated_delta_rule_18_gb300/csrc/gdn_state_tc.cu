@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
         } else if (p.h_in && r < K) {
             load_row64(h, p.h_in + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt, v1, p.Vt);
         } else if (p.h0 && r < K) {
-            load_row64(h, p.h0 + (bh * K + r) * p.Vt, v1, p.Vt);
+            load_row64(h, p.h0 + (bh * K + r) * p.h_ld, v1, p.Vt);
         } else {
 #pragma unroll
             for (int c = 0; c < 64; ++c) h[c] = 0.f;
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
                 store_row64(p.sum_ext + (((int64_t)seg * n_bh + bh) * K + r) * p.Vt, h, v1, p.Vt);
             }
         } else if (ok && p.h_final && r < K && cb + nchunks == nall) {
-            store_row64(p.h_final + (bh * K + r) * p.Vt, h, v1, p.Vt);
+            store_row64(p.h_final + (bh * K + r) * p.h_ld, h, v1, p.Vt);
         }
     } else if (BV == 64 && (warp == 4 || warp == 5)) {
         // ------------------------------------- v_new helpers (columns 32..63)

@@ -273,34 +273,42 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
 
 /*
  * gdn_bwd_workspace_size / gdn_chunk_bwd -- gradients of one direction of
- * the chunked scan (gdn_chunk_fwd's bf16 path, dense batches, scalar gate)
- * for the loss L = sum(dout . o) + sum(dh_final . h_final): the reverse-time
- * chunked state gradient of the hyper-parallel coverage_diff page
- * (`chunk_gated_delta_rule_bwd_dhu`) and the per-chunk input gradients of the
- * WY form (`chunk_bwd_dqkwg`, `prepare_wy_repr_bwd` on the same page; the
- * per-step rules of the SANA `fused_cam_gdn.py` page's `_cam_scan_bwd_kernel`
- * at one token per frame). The forward is recomputed first (its per-chunk
- * operands and the state entering every chunk are kept in the workspace).
- *   q, k, v, g, beta, h0, reverse, flags: as for gdn_chunk_fwd (bf16 q/k/v,
- *     cu_seqlens and gk not offered); flags: GDN_QK_L2NORM (the gradients
- *     are then with respect to the raw q and k).
+ * the chunked scan (gdn_chunk_fwd's bf16 path, scalar gate) for the loss
+ * L = sum(dout . o) + sum(dh_final . h_final): the reverse-time chunked state
+ * gradient of the hyper-parallel coverage_diff page
+ * (`chunk_gated_delta_rule_bwd_dhu`, with its varlen offsets) and the
+ * per-chunk input gradients of the WY form (`chunk_bwd_dqkwg`,
+ * `prepare_wy_repr_bwd` on the same page; the per-step rules of the SANA
+ * `fused_cam_gdn.py` page's `_cam_scan_bwd_kernel` at one token per frame).
+ * The forward is recomputed first (its per-chunk operands and the state
+ * entering every chunk are kept in the workspace). The value columns of the
+ * state evolve independently given k, beta and g, so V > 128 runs as two
+ * ranges of columns: dv and dh0 per range, dq, dk, dbeta and dg summed.
+ *   q, k, v, g, beta, h0, cu_seqlens, n_seq, reverse, flags: as for
+ *     gdn_chunk_fwd (bf16 q/k/v); flags: GDN_QK_L2NORM (the gradients are
+ *     then with respect to the raw q and k). gk: must be NULL
+ *     (GDN_ERR_UNSUPPORTED otherwise).
  *   dout: (B, T, H, V) bf16 upstream gradient of o, descriptor dod.
- *   dh_final: (B, H, K, V) fp32 upstream gradient of h_final, or NULL (0).
+ *   dh_final: (n_seq, H, K, V) fp32 upstream gradient of h_final, or NULL (0).
  *   dq, dk: (B, T, H, K); dv: (B, T, H, V); dbeta, dg: (B, T, H); dh0:
- *     (B, H, K, V) or NULL -- fp32, contiguous, 8-byte aligned. dg is 0 where
- *     g is below the -30 floor the forward applies.
- *   K <= 128 and V <= 128, both multiples of 8. reverse with h0, dh_final or
+ *     (n_seq, H, K, V) or NULL -- fp32, contiguous, 8-byte aligned. dg is 0
+ *     where g is below the -30 floor the forward applies.
+ *   K <= 128 and V <= 256, both multiples of 8. reverse with h0, dh_final or
  *   dh0 -> GDN_ERR_UNSUPPORTED.
- *   workspace: >= gdn_bwd_workspace_size() bytes, 256-byte aligned.
+ *   workspace: >= gdn_bwd_workspace_size(B, T, H, K, V, n_seq, varlen,
+ *   perkey) bytes (0 for an unsupported shape), 256-byte aligned.
  */
-size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V);
+size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq,
+                              int varlen, int perkey);
 gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd,
                          const void *v, gdn_tensor_desc vd, const float *g,
-                         const float *beta, const float *h0, const void *dout,
-                         gdn_tensor_desc dod, const float *dh_final, float *dq,
-                         float *dk, float *dv, float *dbeta, float *dg,
-                         float *dh0, int B, int T, int H, int K, int V,
-                         int chunk, int reverse, int flags, void *workspace,
+                         const float *gk, const float *beta, const float *h0,
+                         const int32_t *cu_seqlens, int n_seq,
+                         const void *dout, gdn_tensor_desc dod,
+                         const float *dh_final, float *dq, float *dk,
+                         float *dv, float *dbeta, float *dg, float *dh0,
+                         int B, int T, int H, int K, int V, int chunk,
+                         int reverse, int flags, void *workspace,
                          size_t ws_bytes, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */

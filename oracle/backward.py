@@ -58,6 +58,8 @@ def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6)
         d = beta[:, t][:, :, None] * (v[:, t] - pred)                      # correct
         return S + k[:, t][:, :, :, None] * d[:, :, None, :]               # write
 
+    if T == 0:
+        return torch.zeros(B, 0, H, V, dtype=torch.float64), S
     if not reverse:
         for t in range(T):
             S = write(S, t)
@@ -70,24 +72,41 @@ def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6)
 
 
 def scan_grad(q, k, v, beta, g, do, h0=None, dh_final=None, reverse=False, l2norm=False,
-              eps=1e-6):
+              eps=1e-6, cu_seqlens=None):
     """Gradients of L = sum(do * o) + sum(dh_final * h_final) with respect to
     q, k, v, beta, g and h0 (raw q, k when l2norm). Returns a dict of float64
     numpy arrays: dq, dk, dv, dbeta, dg, dh0 (dh0 also when h0 is None: the
-    gradient at a zero initial state), and the forward o, h_final."""
+    gradient at a zero initial state), and the forward o, h_final.
+    cu_seqlens (B == 1): packed sequences, each its own recurrence from
+    h0[s]; h0, dh_final and dh0 are then (n_seq, H, K, V)."""
     torch = _torch()
     B, T, H, K = np.shape(q)
     V = np.shape(v)[-1]
+    if cu_seqlens is None:
+        spans = [(b, 0, T) for b in range(B)]
+    else:
+        assert B == 1
+        cu = [int(x) for x in cu_seqlens]
+        spans = [(0, cu[s], cu[s + 1]) for s in range(len(cu) - 1)]
+    n = len(spans)
     tq, tk, tv, tb, tg = map(_t, (q, k, v, beta, g))
-    th0 = _t(np.zeros((B, H, K, V)) if h0 is None else h0)
-    o, hf = scan_torch(tq, tk, tv, tb, tg, th0, reverse=reverse, l2norm=l2norm, eps=eps)
+    th0 = _t(np.zeros((n, H, K, V)) if h0 is None else h0)
+    outs, finals = [], []
+    for s, (b, a, e) in enumerate(spans):
+        sl = (slice(b, b + 1), slice(a, e))
+        o_s, hf_s = scan_torch(tq[sl], tk[sl], tv[sl], tb[sl], tg[sl], th0[s:s + 1],
+                               reverse=reverse, l2norm=l2norm, eps=eps)
+        outs.append(o_s)
+        finals.append(hf_s)
+    o = torch.cat(outs, dim=1) if cu_seqlens is not None else torch.cat(outs, dim=0)
+    hf = torch.cat(finals, dim=0)
     loss = (o * torch.tensor(np.asarray(do, dtype=np.float64))).sum()
     if dh_final is not None:
         loss = loss + (hf * torch.tensor(np.asarray(dh_final, dtype=np.float64))).sum()
     grads = torch.autograd.grad(loss, (tq, tk, tv, tb, tg, th0), allow_unused=True)
     names = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
     shapes = (tq.shape, tk.shape, tv.shape, tb.shape, tg.shape, th0.shape)
-    res = {n: (np.zeros(s) if gr is None else gr.detach().numpy())
-           for n, gr, s in zip(names, grads, shapes)}
+    res = {n_: (np.zeros(s_) if gr is None else gr.detach().numpy())
+           for n_, gr, s_ in zip(names, grads, shapes)}
     res["o"], res["h_final"] = o.detach().numpy(), hf.detach().numpy()
     return res

@@ -198,22 +198,27 @@ def test_seg_fwd_and_summary_reject_on_host(L):
 def test_chunk_bwd_rejects_on_host(L):
     d16, d32 = desc(gdn.BF16, 1, 128, 2, 64), desc(gdn.F32, 1, 128, 2, 64)
 
-    def bw(q=P(0), qkd=d16, dod=d16, h0=None, dhf=None, dh0=P(16), dq=P(10), V=64, T=128,
+    def bw(q=P(0), qkd=d16, dod=d16, gk=None, h0=None, dhf=None, dh0=P(16), dq=P(10), V=64, T=128,
            reverse=0, flags=0, wsb=1 << 30):
-        return L.gdn_chunk_bwd(q, P(1), qkd, P(2), d16, P(3), P(4), h0, P(5), dod, dhf, dq, P(11),
-                               P(12), P(13), P(14), dh0, 1, T, 2, 64, V, 64, reverse, flags, P(9),
-                               wsb, None)
+        return L.gdn_chunk_bwd(q, P(1), qkd, P(2), d16, P(3), gk, P(4), h0, None, 1, P(5), dod, dhf,
+                               dq, P(11), P(12), P(13), P(14), dh0, 1, T, 2, 64, V, 64, reverse,
+                               flags, P(9), wsb, None)
     assert bw(dq=None) == NULL
     assert bw(qkd=d32) == DTYPE                # bf16 inputs only
     assert bw(dod=d32) == DTYPE
-    assert bw(V=256) == SHAPE                  # V <= 128
+    assert bw(V=264) == SHAPE                  # V <= 256
+    assert bw(V=60) == SHAPE                   # a multiple of 8
+    assert bw(gk=P(7)) == UNSUP                # per-key gates: not built
     assert bw(reverse=1) == UNSUP              # dh0 asked of a reverse scan
     assert bw(flags=GDN_ACCUMULATE_FLAG) == UNSUP
     assert bw(dq=ctypes.c_void_p(A + 4)) == LAYOUT
     assert bw(wsb=1024) == WS
     assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 64) > gdn.gdn_workspace_size(
         1, 128, 2, 64, 64, 1, 0, gdn.BF16, 0)
-    assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 256) == 0
+    # V = 256 runs as two 128-column ranges over one range's workspace
+    assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 256) == gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 128)
+    assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 264) == 0
+    assert gdn.gdn_bwd_workspace_size(1, 300, 2, 64, 64, 3, True) > 0
 
 
 def test_bidir_rejects_on_host(L):

@@ -574,6 +574,41 @@ def test_gradients_match_central_differences(reverse, l2norm):
         np.testing.assert_allclose(res[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
 
 
+def test_gradients_varlen_match_central_differences():
+    """Packed sequences (one empty, one of one token), each from its own h0:
+    the autograd gradients against central differences of the C oracle's
+    variable-length forward, on every input coordinate."""
+    from oracle import backward
+    lens = [3, 0, 1, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, H, K, V, n = int(cu[-1]), 2, 3, 2, len(lens)
+    rng = np.random.default_rng(48)
+    x = dict(q=rng.standard_normal((1, T, H, K)), k=rng.standard_normal((1, T, H, K)) / np.sqrt(K),
+             v=rng.standard_normal((1, T, H, V)), beta=rng.uniform(0.2, 0.9, (1, T, H)),
+             g=-rng.uniform(0.05, 0.6, (1, T, H)), h0=rng.standard_normal((n, H, K, V)))
+    do, dhf = rng.standard_normal((1, T, H, V)), rng.standard_normal((n, H, K, V))
+
+    def loss(y):
+        q, k = oracle.l2norm(y["q"]), oracle.l2norm(y["k"])
+        o, hf = oracle.scan(q, k, y["v"], y["beta"], g=y["g"], h0=y["h0"], cu_seqlens=cu, threads=1)
+        return float(np.sum(do * o) + np.sum(dhf * hf))
+    res = backward.scan_grad(x["q"], x["k"], x["v"], x["beta"], x["g"], do, h0=x["h0"],
+                             dh_final=dhf, l2norm=True, cu_seqlens=cu)
+    eps = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"), ("g", "dg"),
+                        ("h0", "dh0")):
+        fd = np.zeros_like(x[name])
+        for ix in np.ndindex(x[name].shape):
+            xp = {n_: a.copy() for n_, a in x.items()}
+            xm = {n_: a.copy() for n_, a in x.items()}
+            xp[name][ix] += eps
+            xm[name][ix] -= eps
+            fd[ix] = (loss(xp) - loss(xm)) / (2 * eps)
+        np.testing.assert_allclose(res[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
+    # the empty sequence passes its final-state gradient straight through
+    np.testing.assert_array_equal(res["dh0"][1], dhf[1])
+
+
 def test_gradients_beta0_closed_form():
     """beta = 0: o_t = e^{G_t} h0^T q_t and h_final = e^{G_T} h0 with G the
     running sum of g, so dq_t = e^{G_t} h0 do_t, dh0 = sum_t e^{G_t} q_t do_t^T

@@ -474,6 +474,13 @@ BWD = {
     "k32_v96": dict(B=1, T=97, H=3, K=32, V=96),
     "t64": dict(B=1, T=64, H=2, K=128, V=128, h0_std=0.5),
     "t1": dict(B=2, T=1, H=2, K=64, V=64, h0_std=0.5),
+    # V > 128: two ranges of value columns, dq / dk / dbeta / dg summed
+    "v256_h0": dict(B=1, T=150, H=2, K=64, V=256, h0_std=0.5),
+    "v192_k128": dict(B=2, T=100, H=2, K=128, V=192, h0_std=0.5),
+    # packed sequences (an empty one, one token, ragged tails), each its own h0
+    "varlen_h0": dict(B=1, T=1 + 64 + 130 + 70, H=2, K=64, V=64, h0_std=0.5,
+                      lengths=[1, 64, 130, 0, 70]),
+    "varlen_v256": dict(B=1, T=70 + 129, H=2, K=128, V=256, h0_std=0.5, lengths=[70, 129]),
 }
 
 
@@ -482,13 +489,14 @@ def _bwd_compare(w, reverse=False, seed=21):
     from oracle import backward
     rng = np.random.default_rng(seed)
     dout = workloads.stored_normal(seed, "dout", (w.B, w.T, w.H, w.V), "bf16")
-    dhf = None if reverse else rng.standard_normal((w.B, w.H, w.K, w.V)).astype(np.float32)
+    dhf = None if reverse else rng.standard_normal((w.n_seq, w.H, w.K, w.V)).astype(np.float32)
     h0 = None if reverse else w.h0
     ref = backward.scan_grad(w.q.values, w.k.values, w.v.values, w.beta, w.g, dout.values,
-                             h0=h0, dh_final=dhf, reverse=reverse, l2norm=True)
+                             h0=h0, dh_final=dhf, reverse=reverse, l2norm=True,
+                             cu_seqlens=w.cu_seqlens)
     got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
                             to_dev(dout), h0=f32_dev(h0), dh_final=f32_dev(dhf), reverse=reverse,
-                            qk_l2norm=True)
+                            qk_l2norm=True, cu_seqlens=i32_dev(w.cu_seqlens))
     torch().cuda.synchronize()
     errs = {n: rel_err(got[n].double().cpu().numpy(), ref[n]) for n in got}
     assert all(e <= 1.5e-2 for e in errs.values()), (w.name, errs)
@@ -504,6 +512,58 @@ def test_small_backward(name):
 def test_small_backward_reverse():
     w = workloads.make(1, 64 * 3 + 9, 2, 64, 64, seed=18, name="bwd_reverse")
     _bwd_compare(w, reverse=True)
+
+
+def test_small_backward_reverse_varlen_v256():
+    lens = [65, 1, 0, 100]
+    w = workloads.make(1, sum(lens), 2, 64, 256, seed=19, lengths=lens, name="bwd_reverse_varlen")
+    _bwd_compare(w, reverse=True)
+
+
+def test_full_size_backward_varlen():
+    """the 64-sequence, 32-head, K = V = 128 variable-length workload with its
+    h0: gradients of every sequence and head on the GPU, two (sequence, head)
+    pairs against the oracle"""
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    w = workloads.build("varlen_bf16_64seq_h32d128")
+    dout = workloads.stored_normal(6, "dout", (w.B, w.T, w.H, w.V), "bf16")
+    got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(dout), h0=f32_dev(w.h0), qk_l2norm=True,
+                            cu_seqlens=i32_dev(w.cu_seqlens))
+    torch().cuda.synchronize()
+    got = {n: t.double().cpu().numpy() for n, t in got.items()}
+    cu = w.cu_seqlens
+    lens = np.diff(cu)
+    for s, h in ((int(np.argmin(lens)), 5), (int(np.argsort(lens)[len(lens) // 2]), 30)):
+        a, e = int(cu[s]), int(cu[s + 1])
+        sel = (slice(0, 1), slice(a, e), slice(h, h + 1))
+        ref = backward.scan_grad(w.q.values[sel], w.k.values[sel], w.v.values[sel], w.beta[sel],
+                                 w.g[sel], dout.values[sel], h0=w.h0[s:s + 1, h:h + 1], l2norm=True)
+        errs = {n: rel_err(got[n][sel], ref[n]) for n in ("dq", "dk", "dv", "dbeta", "dg")}
+        errs["dh0"] = rel_err(got["dh0"][s:s + 1, h:h + 1], ref["dh0"])
+        assert all(e_ <= 1.5e-2 for e_ in errs.values()), (s, h, int(lens[s]), errs)
+
+
+def test_full_size_backward_v256():
+    """K = 128, V = 256 and 32 heads (the per-key workload's widths, with a
+    scalar gate) over 8,192 tokens (the oracle's autograd keeps every step's
+    state): one head against the oracle"""
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    w = workloads.make(1, 8192, 32, 128, 256, seed=27, g_mu=3.0, name="bwd_v256_full")
+    dout = workloads.stored_normal(7, "dout", (w.B, w.T, w.H, w.V), "bf16")
+    got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(dout), qk_l2norm=True)
+    torch().cuda.synchronize()
+    h = 17
+    sel = (slice(0, 1), slice(None), slice(h, h + 1))
+    got = {n: t[sel[:t.dim()]].double().cpu().numpy() if n != "dh0" else t[:, h:h + 1].double().cpu().numpy()
+           for n, t in got.items()}
+    ref = backward.scan_grad(w.q.values[sel], w.k.values[sel], w.v.values[sel], w.beta[sel],
+                             w.g[sel], dout.values[sel], l2norm=True)
+    errs = {n: rel_err(got[n], ref[n]) for n in ("dq", "dk", "dv", "dbeta", "dg", "dh0")}
+    assert all(e_ <= 1.5e-2 for e_ in errs.values()), errs
 
 
 def test_full_size_backward():
