@@ -39,9 +39,11 @@ def _l2(x, eps):
     return x / (x * x).sum(-1, keepdim=True).add(eps).sqrt()
 
 
-def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6):
+def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6, gk=None):
     """The token recurrence on torch float64 tensors (differentiable).
-    q, k (B, T, H, K); v (B, T, H, V); beta, g (B, T, H); h0 (B, H, K, V).
+    q, k (B, T, H, K); v (B, T, H, V); beta, g (B, T, H) or, per key, gk
+    (B, T, H, K) with g None (the coverage_diff page's USE_GK: the decay
+    scales the state's key rows); h0 (B, H, K, V).
     Returns (o (B, T, H, V), h_final (B, H, K, V)); reverse: the
     flip-and-shift scan (position p reads tokens p+1 .. T-1, R_{T-1} = 0)."""
     torch = _torch()
@@ -53,7 +55,10 @@ def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6)
     outs = [None] * T
 
     def write(S, t):
-        S = torch.exp(g[:, t])[:, :, None, None] * S                     # decay
+        if gk is not None:
+            S = torch.exp(gk[:, t])[:, :, :, None] * S                     # per-key decay
+        else:
+            S = torch.exp(g[:, t])[:, :, None, None] * S                   # decay
         pred = torch.einsum("bhkv,bhk->bhv", S, k[:, t])                   # S^T k
         d = beta[:, t][:, :, None] * (v[:, t] - pred)                      # correct
         return S + k[:, t][:, :, :, None] * d[:, :, None, :]               # write
@@ -72,11 +77,12 @@ def scan_torch(q, k, v, beta, g, h0=None, reverse=False, l2norm=False, eps=1e-6)
 
 
 def scan_grad(q, k, v, beta, g, do, h0=None, dh_final=None, reverse=False, l2norm=False,
-              eps=1e-6, cu_seqlens=None):
+              eps=1e-6, cu_seqlens=None, gk=None):
     """Gradients of L = sum(do * o) + sum(dh_final * h_final) with respect to
     q, k, v, beta, g and h0 (raw q, k when l2norm). Returns a dict of float64
     numpy arrays: dq, dk, dv, dbeta, dg, dh0 (dh0 also when h0 is None: the
-    gradient at a zero initial state), and the forward o, h_final.
+    gradient at a zero initial state), and the forward o, h_final. With a
+    per-key gate gk (g None), dg is dL/dgk (B, T, H, K).
     cu_seqlens (B == 1): packed sequences, each its own recurrence from
     h0[s]; h0, dh_final and dh0 are then (n_seq, H, K, V)."""
     torch = _torch()
@@ -89,13 +95,15 @@ def scan_grad(q, k, v, beta, g, do, h0=None, dh_final=None, reverse=False, l2nor
         cu = [int(x) for x in cu_seqlens]
         spans = [(0, cu[s], cu[s + 1]) for s in range(len(cu) - 1)]
     n = len(spans)
-    tq, tk, tv, tb, tg = map(_t, (q, k, v, beta, g))
+    tq, tk, tv, tb, tg = map(_t, (q, k, v, beta, g if gk is None else gk))
     th0 = _t(np.zeros((n, H, K, V)) if h0 is None else h0)
     outs, finals = [], []
     for s, (b, a, e) in enumerate(spans):
         sl = (slice(b, b + 1), slice(a, e))
-        o_s, hf_s = scan_torch(tq[sl], tk[sl], tv[sl], tb[sl], tg[sl], th0[s:s + 1],
-                               reverse=reverse, l2norm=l2norm, eps=eps)
+        gs = tg[sl]
+        o_s, hf_s = scan_torch(tq[sl], tk[sl], tv[sl], tb[sl], None if gk is not None else gs,
+                               th0[s:s + 1], reverse=reverse, l2norm=l2norm, eps=eps,
+                               gk=gs if gk is not None else None)
         outs.append(o_s)
         finals.append(hf_s)
     o = torch.cat(outs, dim=1) if cu_seqlens is not None else torch.cat(outs, dim=0)

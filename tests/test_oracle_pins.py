@@ -609,6 +609,38 @@ def test_gradients_varlen_match_central_differences():
     np.testing.assert_array_equal(res["dh0"][1], dhf[1])
 
 
+def test_gradients_per_key_gate_match_central_differences():
+    """Per-key gates (the state's key rows decay separately), with L2 prep,
+    h0 and dh_final: autograd against central differences of the C oracle."""
+    from oracle import backward
+    x, do, dhf = _fd_case(49, 1, 5, 2, 3, 2)
+    gk = -np.random.default_rng(50).uniform(0.05, 0.8, (1, 5, 2, 3))
+
+    def loss(y, gk_):
+        q, k = oracle.l2norm(y["q"]), oracle.l2norm(y["k"])
+        o, hf = oracle.scan(q, k, y["v"], y["beta"], gk=gk_, h0=y["h0"], threads=1)
+        return float(np.sum(do * o) + np.sum(dhf * hf))
+    res = backward.scan_grad(x["q"], x["k"], x["v"], x["beta"], None, do, h0=x["h0"],
+                             dh_final=dhf, l2norm=True, gk=gk)
+    eps = 1e-6
+    fd = np.zeros_like(gk)
+    for ix in np.ndindex(gk.shape):
+        gp, gm = gk.copy(), gk.copy()
+        gp[ix] += eps
+        gm[ix] -= eps
+        fd[ix] = (loss(x, gp) - loss(x, gm)) / (2 * eps)
+    np.testing.assert_allclose(res["dg"], fd, rtol=1e-6, atol=1e-8, err_msg="dgk")
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"), ("h0", "dh0")):
+        fd = np.zeros_like(x[name])
+        for ix in np.ndindex(x[name].shape):
+            xp = {n_: a.copy() for n_, a in x.items()}
+            xm = {n_: a.copy() for n_, a in x.items()}
+            xp[name][ix] += eps
+            xm[name][ix] -= eps
+            fd[ix] = (loss(xp, gk) - loss(xm, gk)) / (2 * eps)
+        np.testing.assert_allclose(res[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
+
+
 def test_gradients_beta0_closed_form():
     """beta = 0: o_t = e^{G_t} h0^T q_t and h_final = e^{G_T} h0 with G the
     running sum of g, so dq_t = e^{G_t} h0 do_t, dh0 = sum_t e^{G_t} q_t do_t^T
