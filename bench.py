@@ -730,19 +730,19 @@ def main():
     w = resolve_segments(gdn, w, dev)
     d = device_inputs(w, dev)
     if args.pass_ == "bwd":
-        if w.dtype != "bf16" or w.bidirectional or w.gk is not None or w.frame > 1:
-            raise SystemExit("--pass bwd takes a causal bf16 workload with a scalar gate")
+        if w.dtype != "bf16" or w.bidirectional or w.frame > 1:
+            raise SystemExit("--pass bwd takes a causal bf16 workload")
         d["dout"] = torch.from_numpy(workloads.stored_normal(
             rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
         ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq,
-                                                    w.cu_seqlens is not None), dtype=torch.uint8,
-                         device=dev)
+                                                    w.cu_seqlens is not None, w.gk is not None),
+                         dtype=torch.uint8, device=dev)
         args.no_e2e = args.no_cpu_baseline = args.no_configs = True
 
         def run(gdn, w, d, ws):  # the timed step of this pass
             return gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dout"],
                                      h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws,
-                                     cu_seqlens=d.get("cu_seqlens"))
+                                     cu_seqlens=d.get("cu_seqlens"), gk=d.get("gk"))
     else:
         ws = workspace_for(gdn, w, dev)
         run = run_step

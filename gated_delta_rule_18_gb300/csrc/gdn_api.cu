@@ -512,7 +512,7 @@ struct BwdWs {
 };
 // after the forward's workspace L (of one value range of at most 128
 // columns): the snapshots of that range, then bwd_dq's shares of dk and dG
-bool bwd_layout(const Ws &L, int B, int T, int H, int K, int Vp, BwdWs &S) {
+bool bwd_layout(const Ws &L, int B, int T, int H, int K, int Vp, int perkey, BwdWs &S) {
     const size_t hc = (size_t)H * L.max_chunks;
     size_t off = L.total;
     S.h = off;
@@ -526,7 +526,7 @@ bool bwd_layout(const Ws &L, int B, int T, int H, int K, int Vp, BwdWs &S) {
     S.dkp = off;
     off = align_up(off + (size_t)B * T * H * K * 4);
     S.dgp = off;
-    off = align_up(off + (size_t)B * T * H * 4);
+    off = align_up(off + (size_t)B * T * H * (perkey ? K : 1) * 4);  // dG per key with gk
     S.total = off;
     return true;
 }
@@ -538,10 +538,10 @@ size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq, int 
                               int perkey) {
     Ws L;
     BwdWs S;
-    if (perkey || V < 1 || V > 256) return 0;
+    if (V < 1 || V > 256) return 0;
     const int Vp = V > 128 ? 128 : V;
     if (!ws_layout(B, T, H, K, Vp, n_seq, varlen, GDN_BF16, 0, L)) return 0;
-    bwd_layout(L, B, T, H, K, Vp, S);
+    bwd_layout(L, B, T, H, K, Vp, perkey != 0, S);
     return S.total;
 }
 
@@ -556,7 +556,6 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16 || (T > 0 && dod.dtype != GDN_BF16))
         return GDN_ERR_DTYPE;
     if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;
-    if (gk) return GDN_ERR_UNSUPPORTED;
     if (reverse && (h0 || dh_final || dh0)) return GDN_ERR_UNSUPPORTED;
     if (V < 1 || V > 256 || V % 8 != 0) return GDN_ERR_SHAPE;
     if (!aligned16(dout) || !strides_ok(dod)) return GDN_ERR_LAYOUT;
@@ -575,7 +574,8 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
                               Vp, chunk, reverse, flags, false, L, p);
     if (st != GDN_OK) return st;
     BwdWs S;
-    bwd_layout(L, B, T, H, K, Vp, S);
+    const int perkey = gk != nullptr;
+    bwd_layout(L, B, T, H, K, Vp, perkey, S);
     if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
     if (T == 0) {  // dL/dh0 = dL/dh_final
         if (!dh0) return GDN_OK;
@@ -602,7 +602,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
         if (v_off == 0) e = clear_err(p, stream);
         if (e == cudaSuccess && cu_seqlens)
             e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
-        if (e == cudaSuccess) e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, 0, stream); });
+        if (e == cudaSuccess) e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, perkey, stream); });
         if (e == cudaSuccess) e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         gdn::BwdParams b{};
@@ -610,7 +610,7 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
         b.qk_sb = qkd.stride_b, b.qk_st = qkd.stride_t, b.qk_sh = qkd.stride_h;
         b.v_sb = vd.stride_b, b.v_st = vd.stride_t, b.v_sh = vd.stride_h;
         b.do_sb = dod.stride_b, b.do_st = dod.stride_t, b.do_sh = dod.stride_h;
-        b.g = g, b.beta = beta, b.dh_final = dh_final ? dh_final + v_off : nullptr;
+        b.g = g, b.gk = gk, b.beta = beta, b.dh_final = dh_final ? dh_final + v_off : nullptr;
         b.dq = dq, b.dk = dk, b.dv = dv + v_off, b.dbeta = dbeta, b.dg = dg;
         b.dh0 = dh0 ? dh0 + v_off : nullptr;
         b.B = B, b.T = T, b.H = H, b.K = K, b.V = Vh, b.reverse = reverse, b.l2norm = p.l2norm;
@@ -626,8 +626,10 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
         b.dvn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.dvn);
         b.err = p.err;
         e = launch(KBwdDh, stream, [&] { return gdn::launch_bwd_dh(b, stream); });
-        if (e == cudaSuccess) e = launch(KBwdDq, stream, [&] { return gdn::launch_bwd_dq(b, stream); });
-        if (e == cudaSuccess) e = launch(KBwdDk, stream, [&] { return gdn::launch_bwd_dk(b, stream); });
+        if (e == cudaSuccess)
+            e = launch(KBwdDq, stream, [&] { return perkey ? gdn::launch_bwd_dq_gk(b, stream) : gdn::launch_bwd_dq(b, stream); });
+        if (e == cudaSuccess)
+            e = launch(KBwdDk, stream, [&] { return perkey ? gdn::launch_bwd_dk_gk(b, stream) : gdn::launch_bwd_dk(b, stream); });
     }
     return cuda_status(e);
 }

@@ -82,7 +82,7 @@ struct BwdParams {
     int64_t qk_sb, qk_st, qk_sh;
     int64_t v_sb, v_st, v_sh;
     int64_t do_sb, do_st, do_sh;
-    const float *g, *beta, *dh_final;
+    const float *g, *gk, *beta, *dh_final;  // gk: per-key gates (then dg is (B, T, H, K))
     float *dq, *dk, *dv, *dbeta, *dg, *dh0;
     int B, T, H, K, V, reverse, l2norm;
     int max_chunks;  // chunk slots per head (the forward's)
@@ -413,6 +413,8 @@ cudaError_t launch_seg_combine(const SegParams &p, cudaStream_t st);
 cudaError_t launch_bwd_dh(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_bwd_dk(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_dq_gk(const BwdParams &p, cudaStream_t st);
+cudaError_t launch_bwd_dk_gk(const BwdParams &p, cudaStream_t st);
 cudaError_t launch_fused_f32(const FwdParams &p, int KP, int perkey, cudaStream_t st);
 // the fp32 path in two kernels (chunk-parallel prep, chunk-serial pass) for
 // problems whose fused grid would leave the GPU mostly idle

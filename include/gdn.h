@@ -273,7 +273,7 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
 
 /*
  * gdn_bwd_workspace_size / gdn_chunk_bwd -- gradients of one direction of
- * the chunked scan (gdn_chunk_fwd's bf16 path, scalar gate) for the loss
+ * the chunked scan (gdn_chunk_fwd's bf16 path) for the loss
  * L = sum(dout . o) + sum(dh_final . h_final): the reverse-time chunked state
  * gradient of the hyper-parallel coverage_diff page
  * (`chunk_gated_delta_rule_bwd_dhu`, with its varlen offsets) and the
@@ -286,11 +286,14 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
  * ranges of columns: dv and dh0 per range, dq, dk, dbeta and dg summed.
  *   q, k, v, g, beta, h0, cu_seqlens, n_seq, reverse, flags: as for
  *     gdn_chunk_fwd (bf16 q/k/v); flags: GDN_QK_L2NORM (the gradients are
- *     then with respect to the raw q and k). gk: must be NULL
- *     (GDN_ERR_UNSUPPORTED otherwise).
+ *     then with respect to the raw q and k). With gk (per-key gates, g
+ *     NULL) dg is dL/dgk, (B, T, H, K): the chunk products that carry
+ *     e^{G_i - G_j} per key are split about 16-row block middles, as in the
+ *     forward, and dgk is 0 where the forward floors gk at -10.
  *   dout: (B, T, H, V) bf16 upstream gradient of o, descriptor dod.
  *   dh_final: (n_seq, H, K, V) fp32 upstream gradient of h_final, or NULL (0).
- *   dq, dk: (B, T, H, K); dv: (B, T, H, V); dbeta, dg: (B, T, H); dh0:
+ *   dq, dk: (B, T, H, K); dv: (B, T, H, V); dbeta, dg: (B, T, H) (dg
+ *     (B, T, H, K) with gk); dh0:
  *     (n_seq, H, K, V) or NULL -- fp32, contiguous, 8-byte aligned. dg is 0
  *     where g is below the -30 floor the forward applies.
  *   K <= 128 and V <= 256, both multiples of 8. reverse with h0, dh_final or

@@ -208,7 +208,7 @@ def test_chunk_bwd_rejects_on_host(L):
     assert bw(dod=d32) == DTYPE
     assert bw(V=264) == SHAPE                  # V <= 256
     assert bw(V=60) == SHAPE                   # a multiple of 8
-    assert bw(gk=P(7)) == UNSUP                # per-key gates: not built
+    assert bw(gk=P(7)) == UNSUP                # g and gk both given
     assert bw(reverse=1) == UNSUP              # dh0 asked of a reverse scan
     assert bw(flags=GDN_ACCUMULATE_FLAG) == UNSUP
     assert bw(dq=ctypes.c_void_p(A + 4)) == LAYOUT
