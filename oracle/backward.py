@@ -118,3 +118,78 @@ def scan_grad(q, k, v, beta, g, do, h0=None, dh_final=None, reverse=False, l2nor
            for n_, gr, s_ in zip(names, grads, shapes)}
     res["o"], res["h_final"] = o.detach().numpy(), hf.detach().numpy()
     return res
+
+
+def frame_scan_torch(q, k, v, beta, g_frame, frame, h0=None, reverse=False):
+    """The frame-causal rule on torch float64 tensors (differentiable), as
+    the C oracle's frame scan: per frame f of `frame` tokens, S_pre =
+    e^{g_f} S, then S = S_pre + sum_t beta_t k_t (v_t - S_pre^T k_t)^T, and
+    every token of the frame reads the post-frame state. Reverse: frame f
+    reads the state built from frames F-1 .. f+1 (each decayed by its own g
+    before its write), the last frame the zero state. q, k (B, T, H, K);
+    v (B, T, H, V); beta (B, T, H); g_frame (B, T // frame, H), floored at
+    -30 as the forward does; h0 (B, H, K, V). Returns (o, h_final)."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    F = T // frame
+    S = torch.zeros(B, H, K, V, dtype=torch.float64) if h0 is None else h0
+    g = torch.clamp(g_frame, min=-30.0)
+
+    def absorb(S, f):
+        sl = slice(f * frame, (f + 1) * frame)
+        Sp = torch.exp(g[:, f])[:, :, None, None] * S
+        kf, vf, bf = k[:, sl], v[:, sl], beta[:, sl]                      # (B, S, H, .)
+        pred = torch.einsum("bhkv,bshk->bshv", Sp, kf)
+        err = bf[..., None] * (vf - pred)
+        return Sp + torch.einsum("bshk,bshv->bhkv", kf, err)
+
+    def emit(S, f):
+        sl = slice(f * frame, (f + 1) * frame)
+        return torch.einsum("bhkv,bshk->bshv", S, q[:, sl])
+
+    outs = [None] * F
+    for i in range(F):
+        if not reverse:
+            S = absorb(S, i)
+            outs[i] = emit(S, i)
+        else:
+            if i > 0:
+                S = absorb(S, F - i)
+            outs[F - 1 - i] = emit(S, F - 1 - i)
+    if F == 0:
+        return torch.zeros(B, 0, H, V, dtype=torch.float64), S
+    return torch.cat(outs, dim=1), S
+
+
+def frame_grad(q, k, v, beta, g_frame, frame, do, dden=None, h0=None, dh_final=None, direction=0):
+    """Gradients of L = sum(do . o) + sum(dden . den) + sum(dh_final . h_final)
+    for the frame-causal rule with q, k as given (no prep): direction 0
+    causal (with h0 / h_final), 1 reverse, 2 both summed (o and den are the
+    sums of the two directions). den is the same rule with a ones value.
+    Returns float64 numpy dq, dk, dv, dbeta, dg_frame and, for direction 0,
+    dh0."""
+    torch = _torch()
+    B, T, H, K = np.shape(q)
+    V = np.shape(v)[-1]
+    tq, tk, tv, tb, tg = map(_t, (q, k, v, beta, g_frame))
+    th0 = _t(np.zeros((B, H, K, V)) if h0 is None else h0)
+    loss = 0.0
+    for rev in ([False], [True], [False, True])[direction]:
+        o, hf = frame_scan_torch(tq, tk, tv, tb, tg, frame, h0=None if rev else th0, reverse=rev)
+        loss = loss + (o * torch.tensor(np.asarray(do, dtype=np.float64))).sum()
+        if dden is not None:
+            ones = torch.ones(B, T, H, 1, dtype=torch.float64)
+            z0 = None if rev else torch.zeros(B, H, K, 1, dtype=torch.float64)
+            d, _ = frame_scan_torch(tq, tk, ones, tb, tg, frame, h0=z0, reverse=rev)
+            loss = loss + (d[..., 0].permute(0, 2, 1) * torch.tensor(np.asarray(dden, dtype=np.float64))).sum()
+        if not rev and dh_final is not None:
+            loss = loss + (hf * torch.tensor(np.asarray(dh_final, dtype=np.float64))).sum()
+    grads = torch.autograd.grad(loss, (tq, tk, tv, tb, tg, th0), allow_unused=True)
+    names = ("dq", "dk", "dv", "dbeta", "dg_frame", "dh0")
+    shapes = (tq.shape, tk.shape, tv.shape, tb.shape, tg.shape, th0.shape)
+    res = {n_: (np.zeros(s_) if gr is None else gr.detach().numpy())
+           for n_, gr, s_ in zip(names, grads, shapes)}
+    if direction != 0:
+        res.pop("dh0")
+    return res

@@ -641,6 +641,53 @@ def test_gradients_per_key_gate_match_central_differences():
         np.testing.assert_allclose(res[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
 
 
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_frame_gradients_match_central_differences(direction):
+    """Frame-causal rule (frames of 2 tokens) with the denominator's upstream
+    gradient, and h0 / dh_final in the causal direction: autograd of the
+    frame loop against central differences of the C oracle's frame scan."""
+    from oracle import backward
+    rng = np.random.default_rng(60 + direction)
+    B, F, S, H, K, V = 1, 3, 2, 2, 3, 2
+    T = F * S
+    x = dict(q=rng.standard_normal((B, T, H, K)), k=rng.standard_normal((B, T, H, K)) / 2,
+             v=rng.standard_normal((B, T, H, V)), beta=rng.uniform(0.2, 0.9, (B, T, H)),
+             g=-rng.uniform(0.1, 0.6, (B, F, H)), h0=rng.standard_normal((B, H, K, V)))
+    do, dden = rng.standard_normal((B, T, H, V)), rng.standard_normal((B, H, T))
+    dhf = rng.standard_normal((B, H, K, V))
+    state = direction == 0
+
+    def loss(y):
+        tot = 0.0
+        for rev in ([False], [True], [False, True])[direction]:
+            o, hf = oracle.frame_scan(y["q"], y["k"], y["v"], y["beta"], y["g"], S,
+                                      h0=y["h0"] if state else None, reverse=rev, threads=1)
+            d = oracle.frame_den(y["q"], y["k"], y["beta"], y["g"], S, reverse=rev, threads=1)
+            tot += float(np.sum(do * o) + np.sum(dden * d))
+            if state:
+                tot += float(np.sum(dhf * hf))
+        return tot
+    res = backward.frame_grad(x["q"], x["k"], x["v"], x["beta"], x["g"], S, do, dden=dden,
+                              h0=x["h0"] if state else None, dh_final=dhf if state else None,
+                              direction=direction)
+    eps = 1e-6
+    names = [("q", "dq"), ("k", "dk"), ("v", "dv"), ("beta", "dbeta"), ("g", "dg_frame")]
+    if state:
+        names.append(("h0", "dh0"))
+    for name, gname in names:
+        fd = np.zeros_like(x[name])
+        for ix in np.ndindex(x[name].shape):
+            xp = {n_: a.copy() for n_, a in x.items()}
+            xm = {n_: a.copy() for n_, a in x.items()}
+            xp[name][ix] += eps
+            xm[name][ix] -= eps
+            fd[ix] = (loss(xp) - loss(xm)) / (2 * eps)
+        np.testing.assert_allclose(res[gname], fd, rtol=1e-6, atol=1e-8, err_msg=gname)
+    if direction == 1:  # the reverse scan never reads frame 0's keys and values
+        np.testing.assert_array_equal(res["dv"][:, :S], 0.0)
+        np.testing.assert_array_equal(res["dg_frame"][:, 0], 0.0)
+
+
 def test_gradients_beta0_closed_form():
     """beta = 0: o_t = e^{G_t} h0^T q_t and h_final = e^{G_T} h0 with G the
     running sum of g, so dq_t = e^{G_t} h0 do_t, dh0 = sum_t e^{G_t} q_t do_t^T
