@@ -730,19 +730,38 @@ def main():
     w = resolve_segments(gdn, w, dev)
     d = device_inputs(w, dev)
     if args.pass_ == "bwd":
-        if w.dtype != "bf16" or w.bidirectional or w.frame > 1:
-            raise SystemExit("--pass bwd takes a causal bf16 workload")
+        if w.dtype != "bf16" or (w.bidirectional and w.frame == 1):
+            raise SystemExit("--pass bwd takes a causal bf16 workload or a frame-causal one")
         d["dout"] = torch.from_numpy(workloads.stored_normal(
             rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
-        ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq,
-                                                    w.cu_seqlens is not None, w.gk is not None),
-                         dtype=torch.uint8, device=dev)
         args.no_e2e = args.no_cpu_baseline = args.no_configs = True
+        if w.frame > 1:  # the frame-causal rule: prep recompute, then gdn_frame_bwd
+            d["dden"] = torch.from_numpy(np.random.default_rng(rank).standard_normal(
+                (w.B, w.H, w.T)).astype(np.float32)).to(dev) if w.bidirectional else None
+            ws = torch.empty(gdn.gdn_frame_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, w.frame,
+                                                              w.bidirectional),
+                             dtype=torch.uint8, device=dev)
 
-        def run(gdn, w, d, ws):  # the timed step of this pass
-            return gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dout"],
-                                     h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws,
-                                     cu_seqlens=d.get("cu_seqlens"), gk=d.get("gk"))
+            def run(gdn, w, d, ws):  # the timed step of this pass
+                if w.prep == "rms_relu":
+                    q = gdn.gdn_prep(d["q"], mode=gdn.PREP_RMS | gdn.PREP_RELU, scale=1.0, eps=1e-5)
+                    k = gdn.gdn_prep(d["k"], mode=gdn.PREP_RMS | gdn.PREP_RELU, scale=w.K ** -0.5,
+                                     eps=1e-5)
+                else:
+                    q = gdn.gdn_prep(d["q"], mode=gdn.PREP_L2)
+                    k = gdn.gdn_prep(d["k"], mode=gdn.PREP_L2)
+                return gdn.gdn_frame_bwd(q, k, d["v"], d["beta"], d["g_frame"], w.frame, d["dout"],
+                                         dden=d["dden"], h0=None if w.bidirectional else d["h0"],
+                                         direction=2 if w.bidirectional else 0, workspace=ws)
+        else:
+            ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq,
+                                                        w.cu_seqlens is not None, w.gk is not None),
+                             dtype=torch.uint8, device=dev)
+
+            def run(gdn, w, d, ws):  # the timed step of this pass
+                return gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["dout"],
+                                         h0=d["h0"], qk_l2norm=w.prep == "l2", workspace=ws,
+                                         cu_seqlens=d.get("cu_seqlens"), gk=d.get("gk"))
     else:
         ws = workspace_for(gdn, w, dev)
         run = run_step

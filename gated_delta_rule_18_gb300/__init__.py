@@ -91,6 +91,11 @@ def lib():
     L.gdn_chunk_bwd.restype = I
     L.gdn_chunk_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P, TensorDesc,
                                 P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+    L.gdn_frame_bwd_workspace_size.restype = ctypes.c_size_t
+    L.gdn_frame_bwd_workspace_size.argtypes = [I] * 7
+    L.gdn_frame_bwd.restype = I
+    L.gdn_frame_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, TensorDesc, P, P, P, P,
+                                P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
     L.gdn_bidir_workspace_size.restype = ctypes.c_size_t
     L.gdn_bidir_workspace_size.argtypes = [I] * 9
     L.gdn_chunk_fwd_bidir.restype = I
@@ -403,6 +408,46 @@ def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqle
     if st != 0:
         raise GDNError(st, "gdn_chunk_fwd_noalloc")
     return out
+
+
+def gdn_frame_bwd_workspace_size(B, T, H, K, V, frame, with_den) -> int:
+    return int(lib().gdn_frame_bwd_workspace_size(B, T, H, K, V, frame, int(bool(with_den))))
+
+
+def gdn_frame_bwd(q, k, v, beta, g_frame, frame, dout, dden=None, h0=None, dh_final=None,
+                  direction=0, with_dh0=None, workspace=None, stream=None):
+    """Gradients of the frame-causal rule (see include/gdn.h) for
+    L = sum(dout * o) + sum(dden * den) + sum(dh_final * h_final), with
+    respect to q and k as gdn_frame_fwd takes them. Returns a dict of fp32
+    tensors dq, dk, dv, dbeta, dg_frame and, for direction 0 (unless
+    with_dh0=False), dh0 (V + 1 columns with dden)."""
+    torch = _torch()
+    B, T, H, K = q.shape
+    V = v.shape[3]
+    for name, t in (("beta", beta), ("g_frame", g_frame), ("dden", dden), ("h0", h0),
+                    ("dh_final", dh_final)):
+        _f32(t, name)
+    _state_shape(B, H, K, V, dden, h0=h0, dh_final=dh_final)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    res = {"dq": torch.empty((B, T, H, K), **f32), "dk": torch.empty((B, T, H, K), **f32),
+           "dv": torch.empty((B, T, H, V), **f32), "dbeta": torch.empty((B, T, H), **f32),
+           "dg_frame": torch.empty((B, T // frame, H), **f32)}
+    if with_dh0 is None:
+        with_dh0 = direction == 0
+    if with_dh0:
+        res["dh0"] = torch.empty((B, H, K, V + (dden is not None)), **f32)
+    need = gdn_frame_bwd_workspace_size(B, T, H, K, V, frame, dden is not None)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().gdn_frame_bwd(
+        _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g_frame), _ptr(beta), _ptr(h0),
+        _ptr(dout), _desc(dout), _ptr(dden), _ptr(dh_final), _ptr(res["dq"]), _ptr(res["dk"]),
+        _ptr(res["dv"]), _ptr(res["dbeta"]), _ptr(res["dg_frame"]), _ptr(res.get("dh0")),
+        B, T, H, K, V, int(frame), int(direction), 0, _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_frame_bwd")
+    return res
 
 
 def gdn_merge(num, den, gate=None, eps=1e-6, out=None, out_dtype=None, stream=None):

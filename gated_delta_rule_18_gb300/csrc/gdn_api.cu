@@ -7,6 +7,7 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_frame_bwd.cuh"
 
 namespace {
 
@@ -16,13 +17,14 @@ using gdn::FwdParams;
 
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
-    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KFused, KNumKinds
+    KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KFused,
+    KFrameXt, KFrameLam, KFrameTok, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
                                      "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial",
-                                     "fused_tc"};
+                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad"};
 
 struct Profiler {
     std::mutex mu;
@@ -887,6 +889,116 @@ gdn_status gdn_frame_fwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     cudaError_t e = launch(KFrameGram, stream, [&] { return gdn::launch_frame_gram(p, stream); });
     if (e == cudaSuccess) e = launch(KFrameChain, stream, [&] { return gdn::launch_frame_chain(p, stream); });
     if (e == cudaSuccess) e = launch(KFrameOut, stream, [&] { return gdn::launch_frame_out(p, stream); });
+    return cuda_status(e);
+}
+
+namespace {
+struct FrameBwdWs {
+    FrameWs fwd;  // A_f, B_f and direction 0's read states
+    size_t sread1, cmat, lam, dgp, total;
+};
+bool frame_bwd_ws(int B, int T, int H, int K, int V, int frame, int with_den, FrameBwdWs &L) {
+    if (!frame_ws(B, T, H, K, V, frame, with_den, L.fwd)) return false;
+    const size_t F = (size_t)(T / frame), bh = (size_t)B * H, Vt = (size_t)V + (with_den ? 1 : 0);
+    const size_t Vs = (Vt + 7) / 8 * 8, st = bh * F * K * Vs * 4;
+    size_t off = align_up(L.fwd.total);
+    L.sread1 = off;
+    off = align_up(off + st);
+    L.cmat = off;
+    off = align_up(off + st);
+    L.lam = off;
+    off = align_up(off + st);
+    L.dgp = off;
+    off = align_up(off + bh * F * ((Vt + gdn::kFrameBwdCT - 1) / gdn::kFrameBwdCT) * 4);
+    L.total = off;
+    return true;
+}
+}  // namespace
+
+size_t gdn_frame_bwd_workspace_size(int B, int T, int H, int K, int V, int frame, int with_den) {
+    FrameBwdWs L;
+    if (V + (with_den ? 1 : 0) > 128) return 0;
+    return frame_bwd_ws(B, T, H, K, V, frame, with_den, L) ? L.total : 0;
+}
+
+gdn_status gdn_frame_bwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                         gdn_tensor_desc vd, const float *g_frame, const float *beta, const float *h0,
+                         const void *dout, gdn_tensor_desc dod, const float *dden,
+                         const float *dh_final, float *dq, float *dk, float *dv, float *dbeta,
+                         float *dg_frame, float *dh0, int B, int T, int H, int K, int V, int frame,
+                         int direction, int flags, void *workspace, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (B < 1 || T < 0 || H < 1 || K < 1 || V < 1) return GDN_ERR_SHAPE;
+    if (direction < 0 || direction > 2 || flags != 0) return GDN_ERR_UNSUPPORTED;
+    if ((h0 || dh_final || dh0) && direction != 0) return GDN_ERR_UNSUPPORTED;
+    if (T > 0 && (!q || !k || !v || !g_frame || !beta || !dout || !dq || !dk || !dv || !dbeta || !dg_frame))
+        return GDN_ERR_NULL;
+    if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16 || dod.dtype != GDN_BF16) return GDN_ERR_DTYPE;
+    const int Vt = V + (dden ? 1 : 0);
+    if (K % 8 != 0 || V % 8 != 0 || K > 128 || Vt > 128) return GDN_ERR_SHAPE;
+    if (frame < gdn::kChunk || frame % gdn::kChunk != 0 || T % frame != 0) return GDN_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !strides_ok(qkd) ||
+        !strides_ok(vd) || !strides_ok(dod))
+        return GDN_ERR_LAYOUT;
+    for (const void *f : {(const void *)dq, (const void *)dk, (const void *)dv, (const void *)dbeta,
+                          (const void *)dg_frame, (const void *)dh0, (const void *)dh_final,
+                          (const void *)h0, (const void *)dden, (const void *)g_frame, (const void *)beta})
+        if (f && (reinterpret_cast<uintptr_t>(f) & 7)) return GDN_ERR_LAYOUT;
+    FrameBwdWs L;
+    if (!frame_bwd_ws(B, T, H, K, V, frame, dden != nullptr, L)) return GDN_ERR_SHAPE;
+    if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
+    if (T == 0) {  // dL/dh0 = dL/dh_final
+        if (!dh0) return GDN_OK;
+        const size_t n = (size_t)B * H * K * Vt * sizeof(float);
+        return cuda_status(dh_final ? cudaMemcpyAsync(dh0, dh_final, n, cudaMemcpyDeviceToDevice, stream)
+                                    : cudaMemsetAsync(dh0, 0, n, stream));
+    }
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    // the forward's A_f, B_f and the read states of each direction
+    gdn::FrameParams p{};
+    p.q = q, p.k = k, p.v = v;
+    p.qk_sb = qkd.stride_b, p.qk_st = qkd.stride_t, p.qk_sh = qkd.stride_h;
+    p.v_sb = vd.stride_b, p.v_st = vd.stride_t, p.v_sh = vd.stride_h;
+    p.beta = beta, p.g_frame = g_frame;
+    p.B = B, p.T = T, p.H = H, p.K = K, p.V = V, p.Vt = Vt;
+    p.Vs = (Vt + 7) / 8 * 8;
+    p.F = T / frame, p.frame = frame;
+    p.has_den = dden != nullptr;
+    p.amat = reinterpret_cast<float *>(ws + L.fwd.amat);
+    p.bmat = reinterpret_cast<float *>(ws + L.fwd.bmat);
+    float *sread[2] = {reinterpret_cast<float *>(ws + L.fwd.sout), reinterpret_cast<float *>(ws + L.sread1)};
+    cudaError_t e = launch(KFrameGram, stream, [&] { return gdn::launch_frame_gram(p, stream); });
+    gdn::FrameBwdParams b{};
+    b.q = q, b.k = k, b.v = v, b.dout = dout;
+    b.qk_sb = qkd.stride_b, b.qk_st = qkd.stride_t, b.qk_sh = qkd.stride_h;
+    b.v_sb = vd.stride_b, b.v_st = vd.stride_t, b.v_sh = vd.stride_h;
+    b.do_sb = dod.stride_b, b.do_st = dod.stride_t, b.do_sh = dod.stride_h;
+    b.beta = beta, b.g_frame = g_frame, b.h0 = h0, b.dden = dden, b.dh_final = dh_final;
+    b.dq = dq, b.dk = dk, b.dv = dv, b.dbeta = dbeta, b.dg_frame = dg_frame, b.dh0 = dh0;
+    b.B = B, b.T = T, b.H = H, b.K = K, b.V = V, b.Vt = Vt, b.Vs = p.Vs, b.F = p.F, b.frame = frame;
+    b.tok_group = 1;  // the largest of 4, 3, 2 chunks dividing the frame's
+    for (int g = 4; g > 1; --g)
+        if ((frame / gdn::kChunk) % g == 0) {
+            b.tok_group = g;
+            break;
+        }
+    b.amat = p.amat;
+    b.cmat = reinterpret_cast<float *>(ws + L.cmat);
+    b.lam = reinterpret_cast<float *>(ws + L.lam);
+    b.dgp = reinterpret_cast<float *>(ws + L.dgp);
+    // Q_f^T [dO_f | dden_f] serves both directions
+    if (e == cudaSuccess) e = launch(KFrameXt, stream, [&] { return gdn::launch_frame_xt(b, stream); });
+    int pass = 0;
+    for (int d = 0; d < 2 && e == cudaSuccess; ++d) {
+        if (direction != 2 && direction != d) continue;
+        p.direction = d;
+        p.sout = sread[d];
+        p.h0 = d == 0 ? h0 : nullptr;
+        e = launch(KFrameChain, stream, [&] { return gdn::launch_frame_chain(p, stream); });
+        b.direction = d, b.acc = pass++ > 0, b.sread = sread[d];
+        if (e == cudaSuccess) e = launch(KFrameLam, stream, [&] { return gdn::launch_frame_lam(b, stream); });
+        if (e == cudaSuccess) e = launch(KFrameTok, stream, [&] { return gdn::launch_frame_tokgrad(b, stream); });
+    }
     return cuda_status(e);
 }
 

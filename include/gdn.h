@@ -314,6 +314,39 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd,
                          int reverse, int flags, void *workspace,
                          size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * gdn_frame_bwd_workspace_size / gdn_frame_bwd -- gradients of the
+ * frame-causal rule of gdn_frame_fwd (SANA `fused_gdn.py` page,
+ * `_fused_gdn_bwd_kernel`; SANA `fused_cam_gdn.py` page, `_cam_scan_bwd_kernel`)
+ * for L = sum(dout . o) + sum(dden . den) + sum(dh_final . h_final), with
+ * respect to q and k as gdn_frame_fwd takes them (prepared), v, beta,
+ * g_frame and h0. The forward's per-frame matrices and states are
+ * recomputed first; then, per direction, a reverse chain over the frames
+ * forms the state gradient after every frame's write and the per-token
+ * gradients follow from it in parallel.
+ *   q, k, v, g_frame, beta, h0, frame, direction: as for gdn_frame_fwd
+ *     (direction 2: both directions summed); h0 (B, H, K, V), or V + 1
+ *     columns with dden, direction 0 only.
+ *   dout: (B, T, H, V) bf16, descriptor dod. dden: (B, H, T) fp32 upstream
+ *     gradient of den, or NULL (no denominator). dh_final: like h0, or NULL.
+ *   dq, dk: (B, T, H, K); dv: (B, T, H, V); dbeta: (B, T, H); dg_frame:
+ *     (B, T / frame, H); dh0: like h0, or NULL -- fp32, contiguous, 8-byte
+ *     aligned. dg_frame is 0 where g_frame is below the -30 floor.
+ *   K <= 128 and V (+1 with dden) <= 128; K and V multiples of 8. flags: 0.
+ *   workspace: >= gdn_frame_bwd_workspace_size() bytes (0: unsupported
+ *   shape), 256-byte aligned.
+ */
+size_t gdn_frame_bwd_workspace_size(int B, int T, int H, int K, int V, int frame,
+                                    int with_den);
+gdn_status gdn_frame_bwd(const void *q, const void *k, gdn_tensor_desc qkd,
+                         const void *v, gdn_tensor_desc vd, const float *g_frame,
+                         const float *beta, const float *h0, const void *dout,
+                         gdn_tensor_desc dod, const float *dden,
+                         const float *dh_final, float *dq, float *dk, float *dv,
+                         float *dbeta, float *dg_frame, float *dh0, int B, int T,
+                         int H, int K, int V, int frame, int direction, int flags,
+                         void *workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 /*
  * gdn_bidir_workspace_size / gdn_chunk_fwd_bidir -- both directions of the

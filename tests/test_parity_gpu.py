@@ -881,3 +881,77 @@ def test_backward_gk_full_size_clean_and_deterministic():
     for n in a:
         assert t.isfinite(a[n]).all(), n
         assert t.equal(a[n], b[n]), n
+
+
+# ---- gradients of the frame-causal rule (gdn_frame_bwd) against the frame
+# loop's fp64 autograd; q and k are passed prepared (L2-normalised, bf16)
+
+FRAME_BWD = {
+    "causal_h0_k64": dict(B=1, T=256, H=2, K=64, V=64, frame=64, direction=0, den=False, state=True),
+    "causal_den_h0": dict(B=2, T=256, H=2, K=64, V=56, frame=128, direction=0, den=True, state=True),
+    "reverse_k128": dict(B=1, T=384, H=2, K=128, V=128, frame=64, direction=1, den=False, state=False),
+    "both_den_video": dict(B=1, T=512, H=3, K=112, V=112, frame=128, direction=2, den=True, state=False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FRAME_BWD))
+def test_frame_backward(name):
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    t = torch()
+    c = FRAME_BWD[name]
+    B, T, H, K, V, S = c["B"], c["T"], c["H"], c["K"], c["V"], c["frame"]
+    w = workloads.make(B, T, H, K, V, "bf16", seed=71, name="frame_bwd_" + name)
+    # prepared q, k: the L2-normalised rows rounded to bf16, for both sides
+    qn = t.from_numpy(oracle.l2norm(w.q.values)).to(dev()).to(t.bfloat16)
+    kn = t.from_numpy(oracle.l2norm(w.k.values)).to(dev()).to(t.bfloat16)
+    gf = workloads.log_sigmoid_normal(72, "g_frame", (B, T // S, H), 2.0)
+    rng = np.random.default_rng(73)
+    dout = workloads.stored_normal(74, "dout", (B, T, H, V), "bf16")
+    Vt = V + c["den"]
+    dden = rng.standard_normal((B, H, T)).astype(np.float32) if c["den"] else None
+    h0 = (rng.standard_normal((B, H, K, Vt)) * 0.3).astype(np.float32) if c["state"] else None
+    dhf = rng.standard_normal((B, H, K, Vt)).astype(np.float32) if c["state"] else None
+    got = gdn.gdn_frame_bwd(qn, kn, to_dev(w.v), f32_dev(w.beta), f32_dev(gf), S, to_dev(dout),
+                            dden=f32_dev(dden), h0=f32_dev(h0), dh_final=f32_dev(dhf),
+                            direction=c["direction"])
+    t.cuda.synchronize()
+    qv, kv = qn.double().cpu().numpy(), kn.double().cpu().numpy()
+    if c["den"] and c["state"]:
+        # the state carries the ones column: run the oracle on [v | 1]
+        va = np.concatenate([w.v.values, np.ones((B, T, H, 1))], axis=-1)
+        da = np.concatenate([dout.values, dden.transpose(0, 2, 1)[..., None].astype(np.float64)], axis=-1)
+        ref = backward.frame_grad(qv, kv, va, w.beta, gf, S, da, h0=h0, dh_final=dhf, direction=0)
+        ref["dv"] = ref["dv"][..., :V]
+    else:
+        ref = backward.frame_grad(qv, kv, w.v.values, w.beta, gf, S, dout.values, dden=dden,
+                                  h0=h0, dh_final=dhf, direction=c["direction"])
+    errs = {n: rel_err(got[n].double().cpu().numpy(), ref[n]) for n in ref}
+    assert set(got) == set(ref), (sorted(got), sorted(ref))
+    assert all(e <= 1.5e-2 for e in errs.values()), (name, errs)
+
+
+def test_frame_backward_full_size_video():
+    """the frame-causal video workload (2 x 8 frames of 1,024 tokens, 16
+    heads, K = V = 112, both directions with the denominator): q, k prepared
+    on the GPU, gradients of every head, two heads against the oracle"""
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    t = torch()
+    w = workloads.build("frame_video_b2h16f8s1024d112")
+    qkv = to_dev(w.qkv)
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    qn = gdn.gdn_prep(q, mode=gdn.PREP_RMS | gdn.PREP_RELU, scale=1.0, eps=1e-5)
+    kn = gdn.gdn_prep(k, mode=gdn.PREP_RMS | gdn.PREP_RELU, scale=w.K ** -0.5, eps=1e-5)
+    dout = workloads.stored_normal(75, "dout", (w.B, w.T, w.H, w.V), "bf16")
+    dden = np.random.default_rng(76).standard_normal((w.B, w.H, w.T)).astype(np.float32)
+    got = gdn.gdn_frame_bwd(qn, kn, v, f32_dev(w.beta), f32_dev(w.g_frame), w.frame, to_dev(dout),
+                            dden=f32_dev(dden), direction=2)
+    t.cuda.synchronize()
+    qv, kv, vv = (x.double().cpu().numpy() for x in (qn, kn, v))
+    for b, h in ((0, 2), (1, 13)):
+        sel = (slice(b, b + 1), slice(None), slice(h, h + 1))
+        ref = backward.frame_grad(qv[sel], kv[sel], vv[sel], w.beta[sel], w.g_frame[sel], w.frame,
+                                  dout.values[sel], dden=dden[b:b + 1, h:h + 1], direction=2)
+        errs = {n: rel_err(got[n][sel].double().cpu().numpy(), ref[n]) for n in ref}
+        assert all(e <= 1.5e-2 for e in errs.values()), (b, h, errs)
