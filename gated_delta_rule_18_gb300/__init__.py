@@ -21,7 +21,7 @@ __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
            "gdn_merge", "gdn_frame_fwd", "gdn_frame_workspace_size", "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_noalloc_last_device_error",
            "gdn_set_stall_test", "gdn_set_fused", "gdn_forward", "lib",
-           "PREP_L2", "PREP_RMS", "PREP_RELU", "profile_enable", "profile_collect", "gdn_set_state_tile",
+           "PREP_L2", "PREP_RMS", "PREP_RELU", "gdn_prep_bwd", "gdn_frame_bwd", "profile_enable", "profile_collect", "gdn_set_state_tile",
            "launch_count", "kernel_names"]
 
 F32, BF16 = 0, 1
@@ -91,6 +91,8 @@ def lib():
     L.gdn_chunk_bwd.restype = I
     L.gdn_chunk_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P, TensorDesc,
                                 P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+    L.gdn_prep_bwd.restype = I
+    L.gdn_prep_bwd.argtypes = [P, TensorDesc, P, P, I, I, I, I, I, ctypes.c_float, ctypes.c_float, P]
     L.gdn_frame_bwd_workspace_size.restype = ctypes.c_size_t
     L.gdn_frame_bwd_workspace_size.argtypes = [I] * 7
     L.gdn_frame_bwd.restype = I
@@ -408,6 +410,21 @@ def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqle
     if st != 0:
         raise GDNError(st, "gdn_chunk_fwd_noalloc")
     return out
+
+
+def gdn_prep_bwd(x, dy, mode=PREP_L2, scale=1.0, eps=1e-6, dx=None, stream=None):
+    """The gradient of gdn_prep (see include/gdn.h): dx = dL/dx for dy =
+    dL/dy, x the forward's input (B, T, H, D), dy fp32. Returns dx (fp32)."""
+    torch = _torch()
+    B, T, H, D = x.shape
+    _f32(dy, "dy")
+    if dx is None:
+        dx = torch.empty((B, T, H, D), dtype=torch.float32, device=x.device)
+    st = lib().gdn_prep_bwd(_ptr(x), _desc(x), _ptr(dy), _ptr(dx), B, T, H, D, int(mode),
+                            float(scale), float(eps), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_prep_bwd")
+    return dx
 
 
 def gdn_frame_bwd_workspace_size(B, T, H, K, V, frame, with_den) -> int:

@@ -9,6 +9,12 @@
 #include "gdn_common.cuh"
 #include "gdn_frame_bwd.cuh"
 
+namespace gdn {
+cudaError_t launch_prep_bwd(const void *x, int64_t xsb, int64_t xst, int64_t xsh, const float *dy,
+                            float *dx, int B, int T, int H, int D, int bf16, int mode, float scale,
+                            float eps, cudaStream_t st);
+}
+
 namespace {
 
 using gdn::FwdParams;
@@ -18,13 +24,13 @@ using gdn::FwdParams;
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
     KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KFused,
-    KFrameXt, KFrameLam, KFrameTok, KNumKinds
+    KFrameXt, KFrameLam, KFrameTok, KPrepBwd, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
                                      "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial",
-                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad"};
+                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad", "prep_bwd"};
 
 struct Profiler {
     std::mutex mu;
@@ -216,6 +222,27 @@ gdn_status gdn_prep(const void *x, gdn_tensor_desc xd, void *y, gdn_tensor_desc 
         return gdn::launch_prep(x, xd.stride_b, xd.stride_t, xd.stride_h, y, yd.stride_b,
                                 yd.stride_t, yd.stride_h, B, T, H, D, xd.dtype == GDN_BF16, mode,
                                 scale, eps, base == GDN_PREP_RMS ? inv_rms : nullptr, stream);
+    }));
+}
+
+gdn_status gdn_prep_bwd(const void *x, gdn_tensor_desc xd, const float *dy, float *dx, int B,
+                        int T, int H, int D, int mode, float scale, float eps,
+                        cudaStream_t stream) {
+    if (T > 0 && (!x || !dy || !dx)) return GDN_ERR_NULL;
+    if (B < 1 || T < 0 || H < 1 || D < 1) return GDN_ERR_SHAPE;
+    if (!dtype_ok(xd.dtype)) return GDN_ERR_DTYPE;
+    const int base = mode & 0xF;
+    if ((mode & ~0x1F) != 0 || (base != GDN_PREP_L2 && base != GDN_PREP_RMS))
+        return GDN_ERR_UNSUPPORTED;
+    if (D % (16 / elem_size(xd.dtype)) != 0) return GDN_ERR_SHAPE;
+    if (base == GDN_PREP_L2 && D > 256) return GDN_ERR_SHAPE;
+    if (base == GDN_PREP_RMS && (int64_t)H * D > 16384) return GDN_ERR_SHAPE;
+    if (!aligned16(x) || !strides_ok(xd)) return GDN_ERR_LAYOUT;
+    if ((reinterpret_cast<uintptr_t>(dy) & 3) || (reinterpret_cast<uintptr_t>(dx) & 3)) return GDN_ERR_LAYOUT;
+    if (T == 0) return GDN_OK;
+    return cuda_status(launch(KPrepBwd, stream, [&] {
+        return gdn::launch_prep_bwd(x, xd.stride_b, xd.stride_t, xd.stride_h, dy, dx, B, T, H, D,
+                                    xd.dtype == GDN_BF16, mode, scale, eps, stream);
     }));
 }
 

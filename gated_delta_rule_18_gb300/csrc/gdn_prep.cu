@@ -150,6 +150,61 @@ __global__ void __launch_bounds__(256) prep_rms_kernel(const T *__restrict__ x, 
     }
 }
 
+// Backward of y = relu?(x * inv) * scale: with dt = scale * dy (zero where
+// the ReLU cut, i.e. where x <= 0) and inv = (m sum x^2 + eps)^{-1/2} (m = 1
+// for the per-(token, head) L2 form, 1 / (H D) for the full-channel RMS
+// form), dx = inv dt - x inv^3 m sum(dt x). One warp per row, two passes
+// (the second reads the row again from L1/L2); dy and dx fp32 contiguous.
+template <typename T>
+__global__ void __launch_bounds__(256) prep_bwd_kernel(const T *__restrict__ x, int64_t xsb, int64_t xst,
+                                                       int64_t xsh, const float *__restrict__ dy,
+                                                       float *__restrict__ dx, int B, int T_, int H, int D,
+                                                       int rms, int relu, float scale, float eps) {
+    constexpr int N = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t rows = rms ? (int64_t)B * T_ : (int64_t)B * T_ * H;
+    if (row >= rows) return;
+    const int heads = rms ? H : 1;                 // heads in this row
+    const int64_t tok = rms ? row : row / H;       // flat token b * T + t
+    const int h0 = rms ? 0 : (int)(row % H);
+    const int b = (int)(tok / T_), t = (int)(tok % T_);
+    const int per = D / N;                         // vectors per head
+    const float m = rms ? 1.f / (float)(H * D) : 1.f;
+    float ss = 0.f, sd = 0.f;
+    for (int e = lane; e < heads * per; e += 32) {
+        const int hh = h0 + e / per, d0 = (e % per) * N;
+        float xf[N], gf[N];
+        unpack<T>(*reinterpret_cast<const uint4 *>(x + b * xsb + (int64_t)t * xst + hh * xsh + d0), xf);
+        const float *g = dy + ((tok * H + hh) * D + d0);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            gf[i] = (relu && xf[i] <= 0.f) ? 0.f : scale * g[i];
+            ss = fmaf(xf[i], xf[i], ss);
+            sd = fmaf(gf[i], xf[i], sd);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        sd += __shfl_xor_sync(0xffffffffu, sd, o);
+    }
+    const float inv = rsqrtf(m * ss + eps);
+    const float c = inv * inv * inv * m * sd;
+    for (int e = lane; e < heads * per; e += 32) {
+        const int hh = h0 + e / per, d0 = (e % per) * N;
+        float xf[N];
+        unpack<T>(*reinterpret_cast<const uint4 *>(x + b * xsb + (int64_t)t * xst + hh * xsh + d0), xf);
+        const float *g = dy + ((tok * H + hh) * D + d0);
+        float *o = dx + ((tok * H + hh) * D + d0);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float dt = (relu && xf[i] <= 0.f) ? 0.f : scale * g[i];
+            o[i] = inv * dt - xf[i] * c;
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, void *y,
@@ -185,4 +240,24 @@ cudaError_t launch_prep(const void *x, int64_t xsb, int64_t xst, int64_t xsh, vo
     return cudaGetLastError();
 }
 
+}  // namespace gdn
+
+namespace gdn {
+cudaError_t launch_prep_bwd(const void *x, int64_t xsb, int64_t xst, int64_t xsh, const float *dy,
+                            float *dx, int B, int T, int H, int D, int bf16, int mode, float scale,
+                            float eps, cudaStream_t st) {
+    const int relu = (mode & 0x10) ? 1 : 0;
+    const int rms = mode & 0x1;
+    const int64_t rows = rms ? (int64_t)B * T : (int64_t)B * T * H;
+    if (rows == 0) return cudaSuccess;
+    const int wpb = 8;
+    const unsigned grid = (unsigned)((rows + wpb - 1) / wpb);
+    if (bf16)
+        prep_bwd_kernel<__nv_bfloat16><<<grid, 32 * wpb, 0, st>>>((const __nv_bfloat16 *)x, xsb, xst, xsh, dy, dx,
+                                                                  B, T, H, D, rms, relu, scale, eps);
+    else
+        prep_bwd_kernel<float><<<grid, 32 * wpb, 0, st>>>((const float *)x, xsb, xst, xsh, dy, dx, B, T, H, D,
+                                                          rms, relu, scale, eps);
+    return cudaGetLastError();
+}
 }  // namespace gdn

@@ -103,6 +103,19 @@ gdn_status gdn_prep(const void *x, gdn_tensor_desc xd, void *y,
                     cudaStream_t stream);
 
 /*
+ * gdn_prep_bwd -- the gradient of gdn_prep: dx = dL/dx for an upstream dy =
+ * dL/dy, with the same mode, scale and eps (the backward of the pages'
+ * RMSNorm / L2 normalisation, ReLU and k_scale). With t = x inv (inv the
+ * normalisation factor of x's row), dt = scale dy where the ReLU passed,
+ * dx = inv dt - x inv^3 m sum_row(dt x), m = 1 (L2) or 1 / (H D) (RMS).
+ *   x: (B, T, H, D), descriptor xd (the forward's input); dy, dx: (B, T, H,
+ *   D) fp32, contiguous, 4-byte aligned. Limits as for gdn_prep.
+ */
+gdn_status gdn_prep_bwd(const void *x, gdn_tensor_desc xd, const float *dy,
+                        float *dx, int B, int T, int H, int D, int mode,
+                        float scale, float eps, cudaStream_t stream);
+
+/*
  * gdn_workspace_size -- bytes of scratch gdn_chunk_fwd needs for this shape.
  *   varlen != 0: B must be 1 and T is the packed token count.
  *   with_den != 0: the call will also compute the denominator.

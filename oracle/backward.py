@@ -193,3 +193,25 @@ def frame_grad(q, k, v, beta, g_frame, frame, do, dden=None, h0=None, dh_final=N
     if direction != 0:
         res.pop("dh0")
     return res
+
+
+def prep_grad(x, dy, rms=False, relu=False, scale=1.0, eps=None):
+    """Gradient dL/dx of the q/k preparation y = relu?(normalised x) * scale
+    for an upstream dy: rms=False normalises per (token, head) over D
+    (x / sqrt(sum x^2 + eps), eps 1e-6 by default), rms=True over the H*D
+    channels of a token (x / sqrt(sum x^2 / (H D) + eps), eps 1e-5; the SANA
+    `fused_gdn.py` page's full-channel RMSNorm). x, dy (B, T, H, D)."""
+    torch = _torch()
+    tx = _t(x)
+    if rms:
+        B, T, H, D = tx.shape
+        flat = tx.reshape(B, T, H * D)
+        inv = 1.0 / torch.sqrt((flat * flat).mean(-1, keepdim=True) + (1e-5 if eps is None else eps))
+        y = (flat * inv).reshape(B, T, H, D)
+    else:
+        y = _l2(tx, 1e-6 if eps is None else eps)
+    if relu:
+        y = torch.clamp(y, min=0.0)
+    y = y * scale
+    (g,) = torch.autograd.grad((y * torch.tensor(np.asarray(dy, dtype=np.float64))).sum(), (tx,))
+    return g.detach().numpy()

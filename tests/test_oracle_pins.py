@@ -688,6 +688,33 @@ def test_frame_gradients_match_central_differences(direction):
         np.testing.assert_array_equal(res["dg_frame"][:, 0], 0.0)
 
 
+@pytest.mark.parametrize("rms,relu,scale", [(False, False, 1.0), (False, True, 0.5), (True, True, 0.3),
+                                             (True, False, 1.0)])
+def test_prep_gradients_match_central_differences(rms, relu, scale):
+    """The q/k preparation's gradient against central differences of the C
+    oracle's L2 and full-channel RMS normalisations."""
+    from oracle import backward
+    rng = np.random.default_rng(70 + 2 * rms + relu)
+    x = rng.standard_normal((1, 3, 2, 4))
+    dy = rng.standard_normal(x.shape)
+
+    def f(z):
+        if rms:
+            y, _ = oracle.rmsnorm_channels(z, 1e-5, relu=relu, scale=scale)
+        else:
+            y = oracle.l2norm(z)
+            y = (np.maximum(y, 0.0) if relu else y) * scale
+        return float(np.sum(y * dy))
+    got = backward.prep_grad(x, dy, rms=rms, relu=relu, scale=scale)
+    fd = np.zeros_like(x)
+    for ix in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[ix] += 1e-6
+        xm[ix] -= 1e-6
+        fd[ix] = (f(xp) - f(xm)) / 2e-6
+    np.testing.assert_allclose(got, fd, rtol=1e-6, atol=1e-8)
+
+
 def test_gradients_beta0_closed_form():
     """beta = 0: o_t = e^{G_t} h0^T q_t and h_final = e^{G_T} h0 with G the
     running sum of g, so dq_t = e^{G_t} h0 do_t, dh0 = sum_t e^{G_t} q_t do_t^T

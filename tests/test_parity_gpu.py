@@ -955,3 +955,28 @@ def test_frame_backward_full_size_video():
                                   dout.values[sel], dden=dden[b:b + 1, h:h + 1], direction=2)
         errs = {n: rel_err(got[n][sel].double().cpu().numpy(), ref[n]) for n in ref}
         assert all(e <= 1.5e-2 for e in errs.values()), (b, h, errs)
+
+
+@pytest.mark.parametrize("dtype,mode,scale", [("bf16", "l2", 1.0), ("f32", "l2_relu", 0.5),
+                                              ("bf16", "rms_relu", 112 ** -0.5), ("f32", "rms", 1.0)])
+def test_prep_backward(dtype, mode, scale):
+    """gdn_prep_bwd against the fp64 autograd of the preparation (an
+    interleaved qkv view for the bf16 cases, as the video workload passes q)"""
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    t = torch()
+    B, T, H, D = 2, 77, 4, 112 if dtype == "bf16" else 64
+    rng = np.random.default_rng(81)
+    x64 = rng.standard_normal((B, T, 3, H, D))
+    tdt = t.bfloat16 if dtype == "bf16" else t.float32
+    xall = t.from_numpy(x64).to(dev()).to(tdt)
+    x = xall[:, :, 0]  # strided view
+    dy = rng.standard_normal((B, T, H, D)).astype(np.float32)
+    flags = {"l2": gdn.PREP_L2, "l2_relu": gdn.PREP_L2 | gdn.PREP_RELU, "rms": gdn.PREP_RMS,
+             "rms_relu": gdn.PREP_RMS | gdn.PREP_RELU}[mode]
+    eps = 1e-5 if mode.startswith("rms") else 1e-6
+    got = gdn.gdn_prep_bwd(x, f32_dev(dy), mode=flags, scale=scale, eps=eps)
+    t.cuda.synchronize()
+    ref = backward.prep_grad(x.double().cpu().numpy(), dy, rms=mode.startswith("rms"),
+                             relu=mode.endswith("relu"), scale=scale, eps=eps)
+    assert rel_err(got.double().cpu().numpy(), ref) <= 1e-5
