@@ -21,7 +21,7 @@ __all__ = ["GDNError", "gdn_prep", "gdn_chunk_fwd", "gdn_chunk_fwd_noalloc",
            "gdn_merge", "gdn_frame_fwd", "gdn_frame_workspace_size", "gdn_workspace_size",
            "gdn_status_string", "gdn_last_device_error", "gdn_noalloc_last_device_error",
            "gdn_set_stall_test", "gdn_set_fused", "gdn_forward", "lib",
-           "PREP_L2", "PREP_RMS", "PREP_RELU", "gdn_prep_bwd", "gdn_frame_bwd", "profile_enable", "profile_collect", "gdn_set_state_tile",
+           "PREP_L2", "PREP_RMS", "PREP_RELU", "gdn_prep_bwd", "gdn_frame_bwd", "gdn_merge_bwd", "profile_enable", "profile_collect", "gdn_set_state_tile",
            "launch_count", "kernel_names"]
 
 F32, BF16 = 0, 1
@@ -91,6 +91,9 @@ def lib():
     L.gdn_chunk_bwd.restype = I
     L.gdn_chunk_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P, TensorDesc,
                                 P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+    L.gdn_merge_bwd.restype = I
+    L.gdn_merge_bwd.argtypes = [P, TensorDesc, P, P, TensorDesc, P, P, P, P, I, I, I, I,
+                                ctypes.c_float, P]
     L.gdn_prep_bwd.restype = I
     L.gdn_prep_bwd.argtypes = [P, TensorDesc, P, P, I, I, I, I, I, ctypes.c_float, ctypes.c_float, P]
     L.gdn_frame_bwd_workspace_size.restype = ctypes.c_size_t
@@ -410,6 +413,26 @@ def gdn_chunk_fwd_noalloc(q, k, v, beta, out, g=None, gk=None, h0=None, cu_seqle
     if st != 0:
         raise GDNError(st, "gdn_chunk_fwd_noalloc")
     return out
+
+
+def gdn_merge_bwd(num, den, dout, gate=None, eps=1e-6, stream=None):
+    """The gradient of gdn_merge (see include/gdn.h) for dout = dL/dout
+    (fp32): returns dnum, dden and, with a gate, dgate (fp32)."""
+    torch = _torch()
+    B, T, H, V = num.shape
+    for name, t in (("den", den), ("dout", dout)):
+        _f32(t, name)
+    f32 = dict(dtype=torch.float32, device=num.device)
+    res = {"dnum": torch.empty((B, T, H, V), **f32), "dden": torch.empty((B, H, T), **f32)}
+    if gate is not None:
+        res["dgate"] = torch.empty((B, T, H, V), **f32)
+    gd = _desc(gate) if gate is not None else TensorDesc(_dtype_code(num), 0, 0, 0, 0)
+    st = lib().gdn_merge_bwd(_ptr(num), _desc(num), _ptr(den), _ptr(gate), gd, _ptr(dout),
+                             _ptr(res["dnum"]), _ptr(res["dden"]), _ptr(res.get("dgate")),
+                             B, T, H, V, float(eps), _stream(stream))
+    if st != 0:
+        raise GDNError(st, "gdn_merge_bwd")
+    return res
 
 
 def gdn_prep_bwd(x, dy, mode=PREP_L2, scale=1.0, eps=1e-6, dx=None, stream=None):

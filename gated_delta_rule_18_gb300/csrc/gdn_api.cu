@@ -13,6 +13,10 @@ namespace gdn {
 cudaError_t launch_prep_bwd(const void *x, int64_t xsb, int64_t xst, int64_t xsh, const float *dy,
                             float *dx, int B, int T, int H, int D, int bf16, int mode, float scale,
                             float eps, cudaStream_t st);
+cudaError_t launch_merge_bwd(const void *num, int64_t n_sb, int64_t n_st, int64_t n_sh, int bf16,
+                             const float *den, const void *gate, int64_t g_sb, int64_t g_st, int64_t g_sh,
+                             const float *dout, float *dnum, float *dden, float *dgate, int B, int T,
+                             int H, int V, float eps, cudaStream_t st);
 }
 
 namespace {
@@ -24,13 +28,13 @@ using gdn::FwdParams;
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
     KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KFused,
-    KFrameXt, KFrameLam, KFrameTok, KPrepBwd, KNumKinds
+    KFrameXt, KFrameLam, KFrameTok, KPrepBwd, KMergeBwd, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
                                      "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial",
-                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad", "prep_bwd"};
+                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad", "prep_bwd", "merge_bwd"};
 
 struct Profiler {
     std::mutex mu;
@@ -844,6 +848,29 @@ gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den, cons
     m.num_bf16 = nd.dtype == GDN_BF16;
     m.out_bf16 = od.dtype == GDN_BF16;
     return cuda_status(launch(KMerge, stream, [&] { return gdn::launch_merge(m, stream); }));
+}
+
+gdn_status gdn_merge_bwd(const void *num, gdn_tensor_desc nd, const float *den, const void *gate,
+                         gdn_tensor_desc gd, const float *dout, float *dnum, float *dden,
+                         float *dgate, int B, int T, int H, int V, float eps,
+                         cudaStream_t stream) {
+    if (B < 1 || T < 0 || H < 1 || V < 1 || V > 1024) return GDN_ERR_SHAPE;
+    if (T > 0 && (!num || !den || !dout || !dnum || !dden)) return GDN_ERR_NULL;
+    if (!dtype_ok(nd.dtype) || (gate && gd.dtype != nd.dtype)) return GDN_ERR_DTYPE;
+    if (!(eps >= 0.f)) return GDN_ERR_SHAPE;
+    if (gate && !dgate) return GDN_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(num) % elem_size(nd.dtype) ||
+        (gate && reinterpret_cast<uintptr_t>(gate) % elem_size(gd.dtype)))
+        return GDN_ERR_LAYOUT;
+    for (const void *f : {(const void *)den, (const void *)dout, (const void *)dnum, (const void *)dden,
+                          (const void *)dgate})
+        if (f && (reinterpret_cast<uintptr_t>(f) & 3)) return GDN_ERR_LAYOUT;
+    if (T == 0) return GDN_OK;
+    return cuda_status(launch(KMergeBwd, stream, [&] {
+        return gdn::launch_merge_bwd(num, nd.stride_b, nd.stride_t, nd.stride_h, nd.dtype == GDN_BF16, den,
+                                     gate, gd.stride_b, gd.stride_t, gd.stride_h, dout, dnum, dden,
+                                     gate ? dgate : nullptr, B, T, H, V, eps, stream);
+    }));
 }
 
 namespace {

@@ -153,3 +153,74 @@ cudaError_t launch_merge(const MergeParams &m, cudaStream_t st) {
 }
 
 }  // namespace gdn
+
+// ------------------------------------------------------------ backward ---
+// Gradients of out = num / (den + eps) * s, s = silu(gate) (or 1), for an
+// upstream dout: with r = 1 / (den + eps),
+//   dnum = dout s r,  dden = -sum_v dout num s r^2,
+//   dgate = dout num r silu'(gate),  silu'(x) = sig(x) (1 + x (1 - sig(x))).
+// One warp per (b, t, h) row of V values (dden summed by the warp, in a
+// fixed order); num and gate through their strides, dout and the outputs
+// fp32 contiguous.
+namespace gdn {
+namespace {
+template <typename T>
+__device__ __forceinline__ float ld_f(const T *p) {
+    if constexpr (sizeof(T) == 4) return *p;
+    else return __bfloat162float(*p);
+}
+template <typename T>
+__global__ void __launch_bounds__(256) merge_bwd_kernel(const T *num, int64_t n_sb, int64_t n_st, int64_t n_sh,
+                                                        const float *den, const T *gate, int64_t g_sb,
+                                                        int64_t g_st, int64_t g_sh, const float *dout,
+                                                        float *dnum, float *dden, float *dgate, int B, int T_,
+                                                        int H, int V, float eps) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= (int64_t)B * T_ * H) return;
+    const int h = (int)(row % H);
+    const int64_t tok = row / H;
+    const int b = (int)(tok / T_), t = (int)(tok % T_);
+    const int64_t di = ((int64_t)b * H + h) * T_ + t;
+    const float r = 1.f / (den[di] + eps);
+    const T *nrow = num + b * n_sb + (int64_t)t * n_st + h * n_sh;
+    const T *grow = gate ? gate + b * g_sb + (int64_t)t * g_st + h * g_sh : nullptr;
+    const float *orow = dout + row * V;
+    float acc = 0.f;
+    for (int c = lane; c < V; c += 32) {
+        const float n = ld_f(nrow + c), go = orow[c];
+        float s = 1.f, ds = 0.f;
+        if (grow) {
+            const float x = ld_f(grow + c);
+            const float sg = 1.f / (1.f + __expf(-x));
+            s = x * sg;
+            ds = sg * (1.f + x * (1.f - sg));
+        }
+        dnum[row * V + c] = go * s * r;
+        if (dgate) dgate[row * V + c] = go * n * r * ds;
+        acc = fmaf(go * n, s, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) dden[di] = -acc * r * r;
+}
+}  // namespace
+
+cudaError_t launch_merge_bwd(const void *num, int64_t n_sb, int64_t n_st, int64_t n_sh, int bf16,
+                             const float *den, const void *gate, int64_t g_sb, int64_t g_st, int64_t g_sh,
+                             const float *dout, float *dnum, float *dden, float *dgate, int B, int T,
+                             int H, int V, float eps, cudaStream_t st) {
+    const int64_t rows = (int64_t)B * T * H;
+    if (rows == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    if (bf16)
+        merge_bwd_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            (const __nv_bfloat16 *)num, n_sb, n_st, n_sh, den, (const __nv_bfloat16 *)gate, g_sb, g_st, g_sh,
+            dout, dnum, dden, dgate, B, T, H, V, eps);
+    else
+        merge_bwd_kernel<float><<<grid, 256, 0, st>>>((const float *)num, n_sb, n_st, n_sh, den,
+                                                      (const float *)gate, g_sb, g_st, g_sh, dout, dnum,
+                                                      dden, dgate, B, T, H, V, eps);
+    return cudaGetLastError();
+}
+}  // namespace gdn

@@ -419,6 +419,20 @@ gdn_status gdn_merge(const void *num, gdn_tensor_desc nd, const float *den,
                      cudaStream_t stream);
 
 /*
+ * gdn_merge_bwd -- the gradient of gdn_merge for an upstream dout: with
+ * r = 1 / (den + eps) and s = silu(gate) (or 1),
+ *   dnum = dout s r,  dden = -sum_v dout num s r^2,
+ *   dgate = dout num r silu'(gate),  silu'(x) = sig(x) (1 + x (1 - sig(x))).
+ *   num, gate: as for gdn_merge (gate NULL: no dgate); den: (B, H, T) fp32;
+ *   dout, dnum, dgate: (B, T, H, V) fp32 contiguous; dden: (B, H, T) fp32.
+ *   V <= 1024; eps >= 0.
+ */
+gdn_status gdn_merge_bwd(const void *num, gdn_tensor_desc nd, const float *den,
+                         const void *gate, gdn_tensor_desc gd, const float *dout,
+                         float *dnum, float *dden, float *dgate, int B, int T,
+                         int H, int V, float eps, cudaStream_t stream);
+
+/*
  * gdn_frame_workspace_size / gdn_frame_fwd -- the frame-causal form of the
  * rule (SANA `fused_gdn.py` page, `_fused_gdn_kernel` with S tokens per frame;
  * SANA `fused_cam_gdn.py` page, `_cam_scan_kernel`): per (sequence, head),

@@ -215,3 +215,23 @@ def prep_grad(x, dy, rms=False, relu=False, scale=1.0, eps=None):
     y = y * scale
     (g,) = torch.autograd.grad((y * torch.tensor(np.asarray(dy, dtype=np.float64))).sum(), (tx,))
     return g.detach().numpy()
+
+
+def merge_grad(num, den, dout, gate=None, eps=1e-6):
+    """Gradients of L = sum(dout . out) for the bidirectional merge out =
+    num / (den + eps) * silu(gate) (SANA `fused_gdn.py` page,
+    `fused_bigdn_func` / `_fused_bidi_merge_kernel`): returns dnum
+    (B, T, H, V), dden (B, H, T) and, with a gate, dgate."""
+    torch = _torch()
+    tn, td = _t(num), _t(den)
+    out = tn / (td.permute(0, 2, 1)[..., None] + eps)
+    ins = [tn, td]
+    if gate is not None:
+        tg = _t(gate)
+        out = out * (tg * torch.sigmoid(tg))
+        ins.append(tg)
+    grads = torch.autograd.grad((out * torch.tensor(np.asarray(dout, dtype=np.float64))).sum(), ins)
+    res = {"dnum": grads[0].detach().numpy(), "dden": grads[1].detach().numpy()}
+    if gate is not None:
+        res["dgate"] = grads[2].detach().numpy()
+    return res

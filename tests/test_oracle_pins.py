@@ -715,6 +715,33 @@ def test_prep_gradients_match_central_differences(rms, relu, scale):
     np.testing.assert_allclose(got, fd, rtol=1e-6, atol=1e-8)
 
 
+@pytest.mark.parametrize("with_gate", [False, True])
+def test_merge_gradients_match_central_differences(with_gate):
+    """The merge's gradients against central differences of oracle.merge."""
+    from oracle import backward
+    rng = np.random.default_rng(90 + with_gate)
+    num = rng.standard_normal((1, 3, 2, 4))
+    den = rng.uniform(0.2, 2.0, (1, 2, 3))
+    gate = rng.standard_normal(num.shape) * 2 if with_gate else None
+    dout = rng.standard_normal(num.shape)
+    res = backward.merge_grad(num, den, dout, gate=gate, eps=1e-3)
+    x = {"num": num, "den": den}
+    if with_gate:
+        x["gate"] = gate
+
+    def f(y):
+        return float(np.sum(dout * oracle.merge(y["num"], y["den"], gate=y.get("gate"), eps=1e-3)))
+    for name in x:
+        fd = np.zeros_like(x[name])
+        for ix in np.ndindex(x[name].shape):
+            xp = {n_: a.copy() for n_, a in x.items()}
+            xm = {n_: a.copy() for n_, a in x.items()}
+            xp[name][ix] += 1e-6
+            xm[name][ix] -= 1e-6
+            fd[ix] = (f(xp) - f(xm)) / 2e-6
+        np.testing.assert_allclose(res["d" + name], fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
 def test_gradients_beta0_closed_form():
     """beta = 0: o_t = e^{G_t} h0^T q_t and h_final = e^{G_T} h0 with G the
     running sum of g, so dq_t = e^{G_t} h0 do_t, dh0 = sum_t e^{G_t} q_t do_t^T

@@ -980,3 +980,26 @@ def test_prep_backward(dtype, mode, scale):
     ref = backward.prep_grad(x.double().cpu().numpy(), dy, rms=mode.startswith("rms"),
                              relu=mode.endswith("relu"), scale=scale, eps=eps)
     assert rel_err(got.double().cpu().numpy(), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype,with_gate", [("bf16", True), ("f32", False), ("f32", True)])
+def test_merge_backward(dtype, with_gate):
+    """gdn_merge_bwd against the fp64 autograd of the merge"""
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    t = torch()
+    rng = np.random.default_rng(91)
+    B, T, H, V = 2, 37, 3, 112
+    tdt = {"bf16": t.bfloat16, "f32": t.float32}[dtype]
+    wide = t.from_numpy(rng.standard_normal((B, T, 2 * H, V))).to(dev()).to(tdt)
+    num = wide[:, :, ::2]
+    den = t.from_numpy(rng.uniform(0.05, 3.0, (B, H, T))).float().to(dev())
+    gate = t.from_numpy(rng.standard_normal((B, T, H, V)) * 3).to(dev()).to(tdt) if with_gate else None
+    dout = rng.standard_normal((B, T, H, V)).astype(np.float32)
+    got = gdn.gdn_merge_bwd(num, den, f32_dev(dout), gate=gate, eps=1e-3)
+    t.cuda.synchronize()
+    ref = backward.merge_grad(num.double().cpu().numpy(), den.double().cpu().numpy(), dout,
+                              gate=None if gate is None else gate.double().cpu().numpy(), eps=1e-3)
+    assert set(got) == set(ref)
+    for n in ref:
+        assert rel_err(got[n].double().cpu().numpy(), ref[n]) <= 1e-5, n
