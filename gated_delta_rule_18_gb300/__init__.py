@@ -87,10 +87,10 @@ def lib():
     L.gdn_state_summary.argtypes = [P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, I, I, I, I, I,
                                     I, I, P, ctypes.c_size_t, P]
     L.gdn_bwd_workspace_size.restype = ctypes.c_size_t
-    L.gdn_bwd_workspace_size.argtypes = [I] * 8
+    L.gdn_bwd_workspace_size.argtypes = [I] * 9
     L.gdn_chunk_bwd.restype = I
     L.gdn_chunk_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P, TensorDesc,
-                                P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
+                                P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
     L.gdn_merge_bwd.restype = I
     L.gdn_merge_bwd.argtypes = [P, TensorDesc, P, P, TensorDesc, P, P, P, P, I, I, I, I,
                                 ctypes.c_float, P]
@@ -315,18 +315,21 @@ def gdn_state_summary(k, v, beta, segment_len, g=None, gk=None, with_transition=
     return ext, tr
 
 
-def gdn_bwd_workspace_size(B, T, H, K, V, n_seq=None, varlen=False, perkey=False) -> int:
+def gdn_bwd_workspace_size(B, T, H, K, V, n_seq=None, varlen=False, perkey=False,
+                           with_den=False) -> int:
     return int(lib().gdn_bwd_workspace_size(B, T, H, K, V, B if n_seq is None else n_seq,
-                                            int(bool(varlen)), int(bool(perkey))))
+                                            int(bool(varlen)), int(bool(perkey)),
+                                            int(bool(with_den))))
 
 
 def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
                   qk_l2norm=False, with_dh0=None, workspace=None, stream=None, gk=None,
-                  cu_seqlens=None):
+                  cu_seqlens=None, dden=None):
     """Gradients of one direction of the scan for L = sum(dout * o) +
     sum(dh_final * h_final) (see include/gdn.h). q, k (B, T, H, K), v and
     dout (B, T, H, V) bf16; beta, g (B, T, H), h0 / dh_final (n_seq, H, K,
-    V) fp32; cu_seqlens: int32 (n_seq + 1) with B == 1. Returns a dict of
+    V) fp32 (V + 1 columns with dden, the denominator's upstream gradient
+    (B, H, T)); cu_seqlens: int32 (n_seq + 1) with B == 1. Returns a dict of
     fp32 tensors dq, dk, dv, dbeta, dg and, unless reverse (or
     with_dh0=False), dh0."""
     torch = _torch()
@@ -335,9 +338,10 @@ def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
     n_seq = B if cu_seqlens is None else cu_seqlens.numel() - 1
     if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_contiguous()):
         raise GDNError(3, "cu_seqlens must be a contiguous int32 tensor")
-    for name, t in (("beta", beta), ("g", g), ("gk", gk), ("h0", h0), ("dh_final", dh_final)):
+    for name, t in (("beta", beta), ("g", g), ("gk", gk), ("h0", h0), ("dh_final", dh_final),
+                    ("dden", dden)):
         _f32(t, name)
-    _state_shape(n_seq, H, K, V, None, h0=h0, dh_final=dh_final)
+    _state_shape(n_seq, H, K, V, dden, h0=h0, dh_final=dh_final)
     f32 = dict(dtype=torch.float32, device=q.device)
     res = {"dq": torch.empty((B, T, H, K), **f32), "dk": torch.empty((B, T, H, K), **f32),
            "dv": torch.empty((B, T, H, V), **f32), "dbeta": torch.empty((B, T, H), **f32),
@@ -345,13 +349,14 @@ def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
     if with_dh0 is None:
         with_dh0 = not reverse
     if with_dh0:
-        res["dh0"] = torch.empty((n_seq, H, K, V), **f32)
-    need = gdn_bwd_workspace_size(B, T, H, K, V, n_seq, cu_seqlens is not None, gk is not None)
+        res["dh0"] = torch.empty((n_seq, H, K, V + (dden is not None)), **f32)
+    need = gdn_bwd_workspace_size(B, T, H, K, V, n_seq, cu_seqlens is not None, gk is not None,
+                                  dden is not None)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     st = lib().gdn_chunk_bwd(
         _ptr(q), _ptr(k), _desc(q), _ptr(v), _desc(v), _ptr(g), _ptr(gk), _ptr(beta), _ptr(h0),
-        _ptr(cu_seqlens), n_seq, _ptr(dout), _desc(dout), _ptr(dh_final), _ptr(res["dq"]),
+        _ptr(cu_seqlens), n_seq, _ptr(dout), _desc(dout), _ptr(dden), _ptr(dh_final), _ptr(res["dq"]),
         _ptr(res["dk"]), _ptr(res["dv"]), _ptr(res["dbeta"]), _ptr(res["dg"]),
         _ptr(res.get("dh0")), B, T, H, K, V, 64, int(bool(reverse)),
         QK_L2NORM if qk_l2norm else 0, _ptr(workspace), workspace.numel(), _stream(stream))

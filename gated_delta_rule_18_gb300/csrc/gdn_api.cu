@@ -326,6 +326,7 @@ gdn_status fwd_setup(const void *q, const void *k, gdn_tensor_desc qkd, const vo
     p.has_den = den_out != nullptr;
     p.Vt = L.Vt;
     p.h_ld = L.Vt;
+    p.snap_ld = (L.Vt + 7) / 8 * 8;
     p.max_chunks = L.max_chunks;
     p.n_vt = L.n_vt;
     p.stall_cta = g_stall_cta.load();
@@ -547,6 +548,7 @@ struct BwdWs {
 // columns): the snapshots of that range, then bwd_dq's shares of dk and dG
 bool bwd_layout(const Ws &L, int B, int T, int H, int K, int Vp, int perkey, BwdWs &S) {
     const size_t hc = (size_t)H * L.max_chunks;
+    Vp = (Vp + 7) / 8 * 8;  // the snapshots' 16-byte rows
     size_t off = L.total;
     S.h = off;
     off = align_up(off + hc * K * Vp * 2);
@@ -567,23 +569,55 @@ bool bwd_layout(const Ws &L, int B, int T, int H, int K, int Vp, int perkey, Bwd
 
 extern "C" {
 
+}  // extern "C"
+
+namespace {
+// The value columns of a backward pass in ranges of at most 128 (the state
+// columns evolve independently); with the denominator the last range also
+// carries the ones column, so it keeps at most 120 value columns.
+struct BwdRange {
+    int off, w, den;
+};
+int bwd_ranges(int V, int den, BwdRange (&r)[4]) {
+    int n = 0, off = 0, rem = V;
+    const int cap_last = den ? 120 : 128;
+    while (rem > cap_last && n < 3) {
+        const int take = rem - 8 < 128 ? rem - 8 : 128;
+        r[n++] = {off, take, 0};
+        off += take, rem -= take;
+    }
+    r[n++] = {off, rem, den};
+    return n;
+}
+size_t bwd_ws_total(int B, int T, int H, int K, int V, int n_seq, int varlen, int perkey, int den) {
+    BwdRange r[4];
+    const int n = bwd_ranges(V, den, r);
+    size_t tot = 0;
+    for (int i = 0; i < n; ++i) {
+        Ws L;
+        BwdWs S;
+        if (!ws_layout(B, T, H, K, r[i].w, n_seq, varlen, GDN_BF16, r[i].den, L)) return 0;
+        bwd_layout(L, B, T, H, K, r[i].w + r[i].den, perkey, S);
+        if (S.total > tot) tot = S.total;
+    }
+    return tot;
+}
+}  // namespace
+
+extern "C" {
+
 size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq, int varlen,
-                              int perkey) {
-    Ws L;
-    BwdWs S;
+                              int perkey, int with_den) {
     if (V < 1 || V > 256) return 0;
-    const int Vp = V > 128 ? 128 : V;
-    if (!ws_layout(B, T, H, K, Vp, n_seq, varlen, GDN_BF16, 0, L)) return 0;
-    bwd_layout(L, B, T, H, K, Vp, perkey != 0, S);
-    return S.total;
+    return bwd_ws_total(B, T, H, K, V, n_seq, varlen, perkey != 0, with_den != 0);
 }
 
 gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
                          gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
                          const float *h0, const int32_t *cu_seqlens, int n_seq, const void *dout,
-                         gdn_tensor_desc dod, const float *dh_final, float *dq, float *dk,
-                         float *dv, float *dbeta, float *dg, float *dh0, int B, int T, int H, int K,
-                         int V, int chunk, int reverse, int flags, void *workspace,
+                         gdn_tensor_desc dod, const float *dden, const float *dh_final, float *dq,
+                         float *dk, float *dv, float *dbeta, float *dg, float *dh0, int B, int T,
+                         int H, int K, int V, int chunk, int reverse, int flags, void *workspace,
                          size_t ws_bytes, cudaStream_t stream) {
     if (T > 0 && (!dout || !dq || !dk || !dv || !dbeta || !dg)) return GDN_ERR_NULL;
     if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16 || (T > 0 && dod.dtype != GDN_BF16))
@@ -595,62 +629,76 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
     for (const void *f : {(const void *)dq, (const void *)dk, (const void *)dv, (const void *)dbeta,
                           (const void *)dg, (const void *)dh0, (const void *)dh_final})
         if (f && (reinterpret_cast<uintptr_t>(f) & 7)) return GDN_ERR_LAYOUT;
+    if (dden && (reinterpret_cast<uintptr_t>(dden) & 3)) return GDN_ERR_LAYOUT;
+    const int den = dden != nullptr;
+    const int Vs = V + den;  // columns of h0, h_final, dh0, dh_final
     // The value columns of the state evolve independently given k, beta and
     // g, so the gradient is formed over ranges of at most 128 columns: dv
     // and dh0 per range, dq, dk, dbeta and dg summed over the ranges.
-    const int Vp = V > 128 ? 128 : V;
+    BwdRange rg[4];
+    const int nrg = bwd_ranges(V, den, rg);
     Ws L;
     gdn::FwdParams p;
-    // the forward recompute of the first range: no outputs, the snapshots instead
-    gdn_status st = fwd_setup(q, k, qkd, v, vd, g, gk, beta, h0, cu_seqlens, n_seq, nullptr,
-                              gdn_tensor_desc{GDN_BF16, 0, 0, 0, 0}, nullptr, nullptr, B, T, H, K,
-                              Vp, chunk, reverse, flags, false, L, p);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    // the forward recompute of a range: no outputs, the snapshots instead (a
+    // range with the ones column is run as with a denominator, which it then
+    // never writes)
+    auto setup = [&](const BwdRange &r) {
+        return fwd_setup(q, k, qkd, static_cast<const __nv_bfloat16 *>(v) + r.off, vd, g, gk, beta,
+                         h0 ? h0 + r.off : nullptr, cu_seqlens, n_seq, nullptr,
+                         gdn_tensor_desc{GDN_BF16, 0, 0, 0, 0}, nullptr,
+                         r.den ? reinterpret_cast<float *>(ws ? ws : reinterpret_cast<unsigned char *>(16))
+                               : nullptr,
+                         B, T, H, K, r.w, chunk, reverse, flags, false, L, p);
+    };
+    gdn_status st = setup(rg[0]);
     if (st != GDN_OK) return st;
-    BwdWs S;
     const int perkey = gk != nullptr;
-    bwd_layout(L, B, T, H, K, Vp, perkey, S);
-    if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
+    const size_t need = bwd_ws_total(B, T, H, K, V, n_seq, cu_seqlens != nullptr, perkey, den);
+    if (need == 0) return GDN_ERR_SHAPE;
+    if (!ws_ok(workspace, ws_bytes, need)) return GDN_ERR_WORKSPACE;
     if (T == 0) {  // dL/dh0 = dL/dh_final
         if (!dh0) return GDN_OK;
-        const size_t n = (size_t)n_seq * H * K * V * sizeof(float);
+        const size_t n = (size_t)n_seq * H * K * Vs * sizeof(float);
         cudaError_t e = dh_final ? cudaMemcpyAsync(dh0, dh_final, n, cudaMemcpyDeviceToDevice, stream)
                                  : cudaMemsetAsync(dh0, 0, n, stream);
         return cuda_status(e);
     }
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
     cudaError_t e = cudaSuccess;
-    for (int v_off = 0; v_off < V && e == cudaSuccess; v_off += 128) {
-        const int Vh = V - v_off < 128 ? V - v_off : 128;
-        const __nv_bfloat16 *vr = static_cast<const __nv_bfloat16 *>(v) + v_off;
-        if (v_off > 0) {  // the same checks passed for the first range
-            st = fwd_setup(q, k, qkd, vr, vd, g, gk, beta, h0 ? h0 + v_off : nullptr, cu_seqlens,
-                           n_seq, nullptr, gdn_tensor_desc{GDN_BF16, 0, 0, 0, 0}, nullptr, nullptr,
-                           B, T, H, K, Vh, chunk, reverse, flags, false, L, p);
+    for (int ri = 0; ri < nrg && e == cudaSuccess; ++ri) {
+        const BwdRange &r = rg[ri];
+        if (ri > 0) {  // the same checks passed for the first range
+            st = setup(r);
             if (st != GDN_OK) return st;
         }
-        p.h_ld = V;  // h0 rows keep all V columns
+        BwdWs S;
+        bwd_layout(L, B, T, H, K, r.w + r.den, perkey, S);
+        p.h_ld = Vs;  // h0 rows keep all the state's columns
         bind_ws(ws, L, p);
         p.h_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.h);
         p.vn_snap = reinterpret_cast<__nv_bfloat16 *>(ws + S.vn);
-        if (v_off == 0) e = clear_err(p, stream);
+        if (ri == 0) e = clear_err(p, stream);
         if (e == cudaSuccess && cu_seqlens)
             e = launch(KTable, stream, [&] { return gdn::launch_chunk_table(p, stream); });
         if (e == cudaSuccess) e = launch(KIntra, stream, [&] { return gdn::launch_intra_bf16(p, perkey, stream); });
         if (e == cudaSuccess) e = launch(KState, stream, [&] { return gdn::launch_state_tc(p, stream); });
         if (e != cudaSuccess) return GDN_ERR_CUDA;
         gdn::BwdParams b{};
-        b.q = q, b.k = k, b.v = vr, b.dout = static_cast<const __nv_bfloat16 *>(dout) + v_off;
+        b.q = q, b.k = k, b.v = static_cast<const __nv_bfloat16 *>(v) + r.off;
+        b.dout = static_cast<const __nv_bfloat16 *>(dout) + r.off;
         b.qk_sb = qkd.stride_b, b.qk_st = qkd.stride_t, b.qk_sh = qkd.stride_h;
         b.v_sb = vd.stride_b, b.v_st = vd.stride_t, b.v_sh = vd.stride_h;
         b.do_sb = dod.stride_b, b.do_st = dod.stride_t, b.do_sh = dod.stride_h;
-        b.g = g, b.gk = gk, b.beta = beta, b.dh_final = dh_final ? dh_final + v_off : nullptr;
-        b.dq = dq, b.dk = dk, b.dv = dv + v_off, b.dbeta = dbeta, b.dg = dg;
-        b.dh0 = dh0 ? dh0 + v_off : nullptr;
-        b.B = B, b.T = T, b.H = H, b.K = K, b.V = Vh, b.reverse = reverse, b.l2norm = p.l2norm;
+        b.g = g, b.gk = gk, b.beta = beta, b.dh_final = dh_final ? dh_final + r.off : nullptr;
+        b.dq = dq, b.dk = dk, b.dv = dv + r.off, b.dbeta = dbeta, b.dg = dg;
+        b.dh0 = dh0 ? dh0 + r.off : nullptr;
+        b.B = B, b.T = T, b.H = H, b.K = K, b.V = r.w + r.den, b.reverse = reverse, b.l2norm = p.l2norm;
         b.max_chunks = L.max_chunks;
         b.cu_seqlens = cu_seqlens, b.n_seq = n_seq;
         b.n_chunks = p.n_chunks, b.chunk_tab = p.chunk_tab, b.seq_chunk0 = p.seq_chunk0;
-        b.vfull = V, b.v_off = v_off, b.acc = v_off > 0;
+        b.vfull = Vs, b.v_off = r.off, b.dv_ld = V, b.acc = ri > 0;
+        b.dden = dden, b.den_col = r.den ? r.w : -1;
+        b.snap_ld = (r.w + r.den + 7) / 8 * 8;
         b.dk_part = reinterpret_cast<float *>(ws + S.dkp);
         b.dg_part = reinterpret_cast<float *>(ws + S.dgp);
         b.w_img = p.w_img, b.qg_img = p.qg_img, b.kg_img = p.kg_img, b.p_img = p.p_img, b.dec = p.dec;

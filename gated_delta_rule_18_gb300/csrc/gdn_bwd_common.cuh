@@ -122,6 +122,26 @@ __device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_ou
     }
 }
 
+// The denominator's column of a range that carries it: dden into the dout
+// tile (query rows), and the ones value into the value tile (key rows). Rows
+// 0 .. 63 by threads 0 .. 63; a barrier must follow before the tiles are read.
+__device__ __forceinline__ void fill_den_dout(const BwdParams &p, const ChunkCtx &x, bf16 *dout, int ld) {
+    const int i = threadIdx.x;
+    if (p.den_col < 0 || i >= kChunk) return;
+    float d = 0.f;
+    if (i < x.Lc)
+        d = p.dden[((int64_t)x.b * p.H + x.hh) * p.T + x.tstart + q_token(p.reverse, x.len, x.pos0 + i)];
+    dout[i * ld + p.den_col] = __float2bfloat16_rn(d);
+}
+__device__ __forceinline__ void fill_den_v(const BwdParams &p, const ChunkCtx &x, bf16 *vt, int ld) {
+    const int i = threadIdx.x;
+    if (p.den_col < 0 || i >= kChunk) return;
+    const int tk = i < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + i) : -1;
+    vt[i * ld + p.den_col] = __float2bfloat16_rn(tk >= 0 ? 1.f : 0.f);
+}
+// value columns of this range that come from v / dout (the rest: the ones column)
+__device__ __forceinline__ int value_cols(const BwdParams &p) { return p.den_col >= 0 ? p.den_col : p.V; }
+
 // T = (I + A)^{-1} with A_ij = beta_i kkg_ij (i > j; kkg fp32 with row
 // stride kPS), by 16 x 16 blocks as in the forward's solve: diagonal
 // inverses T_II in fp32 by forward substitution, B_IM = -T_II A_IM, then

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
         const int pos0 = c * kChunk, Lc = min(kChunk, T - pos0);
         for (int e = tid; e < kChunk * 8; e += kThreads) {  // do: 64 rows x 8 pieces
             const int i = e >> 3, c8 = (e & 7) * 8, col = v0 + c8;
-            const bool in = i < Lc && col < V;
+            const bool in = i < Lc && col < (p.den_col >= 0 ? p.den_col : V);
             const int tq = in ? q_token(p.reverse, T, pos0 + i) : 0;
             const bf16 *src = in ? dout + b * p.do_sb + (int64_t)(tstart + tq) * p.do_st + hh * p.do_sh + col : dout;
             cp_async16(S.dout + i * kL6 + c8, src, in ? 16 : 0);
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
     bool ok = true;
     int it = 0;
     for (; it < nts; ++it) {
-        const DhStage &S = sm.st[it & 1];
+        DhStage &S = sm.st[it & 1];
         if (it + 1 < nts) {
             stage(it + 1);
             cp_async_wait<1>();
@@ -118,6 +118,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
             cp_async_wait<0>();
         }
         ok = wait_bar(bar[it & 1], (it >> 1) & 1, nullptr);
+        // the denominator's column of the do tile: dden (the barrier below
+        // precedes its readers)
+        if (p.den_col >= v0 && p.den_col < v0 + 64 && tid < kChunk) {
+            const int c = nts - 1 - it, pos0 = c * kChunk, Lc = min(kChunk, T - pos0);
+            float dd = 0.f;
+            if (tid < Lc) dd = p.dden[((int64_t)b * p.H + hh) * p.T + tstart + q_token(p.reverse, T, pos0 + tid)];
+            S.dout[tid * kL6 + (p.den_col - v0)] = __float2bfloat16_rn(dd);
+        }
         // dh' to the B-operand tile
 #pragma unroll
         for (int n = 0; n < 8; ++n)
@@ -128,11 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
         if (__syncthreads_or(!ok)) break;
         const int64_t gch = gch_of(it);
         {  // its snapshot, 16-byte pieces
-            bf16 *snap = p.dh_snap + gch * K * V + v0;
+            bf16 *snap = p.dh_snap + gch * K * p.snap_ld + v0;
             for (int e = tid; e < kKP * 8; e += kThreads) {
                 const int r = e >> 3, c8 = (e & 7) * 8;
                 if (r < K && v0 + c8 < V)
-                    *reinterpret_cast<uint4 *>(snap + (int64_t)r * V + c8) =
+                    *reinterpret_cast<uint4 *>(snap + (int64_t)r * p.snap_ld + c8) =
                         *reinterpret_cast<const uint4 *>(sm.dh + r * kL6 + c8);
             }
         }
@@ -175,13 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
         }
         __syncthreads();
         {  // dv_new's snapshot (the tile holds -dv_new: flip the sign bits)
-            bf16 *vsnap = p.dvn_snap + gch * kChunk * V + v0;
+            bf16 *vsnap = p.dvn_snap + gch * kChunk * p.snap_ld + v0;
             for (int e = tid; e < kChunk * 8; e += kThreads) {
                 const int i = e >> 3, c8 = (e & 7) * 8;
                 if (v0 + c8 < V) {
                     uint4 u = *reinterpret_cast<const uint4 *>(sm.dvn + i * kL6 + c8);
                     u.x ^= 0x80008000u, u.y ^= 0x80008000u, u.z ^= 0x80008000u, u.w ^= 0x80008000u;
-                    *reinterpret_cast<uint4 *>(vsnap + (int64_t)i * V + c8) = u;
+                    *reinterpret_cast<uint4 *>(vsnap + (int64_t)i * p.snap_ld + c8) = u;
                 }
             }
         }

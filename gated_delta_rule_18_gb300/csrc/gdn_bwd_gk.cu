@@ -230,16 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
         return tk < 0 ? nullptr : k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
     cp_async_commit();
-    load_rows(sm.dout, kLK, kChunk, V, [&](int i) -> const bf16 * {
+    load_rows(sm.dout, kLK, kChunk, value_cols(p), [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
         return dout + x.b * p.do_sb + (int64_t)(x.tstart + q_token(p.reverse, x.len, x.pos0 + i)) * p.do_st +
                x.hh * p.do_sh;
     });
     load_rows(sm.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
-        return p.vn_snap + (x.gch * kChunk + i) * V;
+        return p.vn_snap + (x.gch * kChunk + i) * p.snap_ld;
     });
     load_rows(sm.h, kLK, kKP, V, [&](int r) -> const bf16 * {
-        return r < K ? p.h_snap + (x.gch * K + r) * V : nullptr;
+        return r < K ? p.h_snap + (x.gch * K + r) * p.snap_ld : nullptr;
     });
     cp_async_commit();
     if (tid < kChunk) sm.row[tid] = 0.f;
@@ -249,6 +249,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
     norm_rows(sm.q, kLK, kq, sm.rq, p.l2norm);
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
     cp_async_wait<0>();
+    __syncthreads();
+    fill_den_dout(p, x, sm.dout, kLK);
     __syncthreads();
 
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
@@ -389,21 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
         return tk < 0 ? nullptr : k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
     cp_async_commit();
-    load_rows(sm.v, kLK, kChunk, V, [&](int i) -> const bf16 * {
+    load_rows(sm.v, kLK, kChunk, value_cols(p), [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : v + x.b * p.v_sb + (int64_t)(x.tstart + tk) * p.v_st + x.hh * p.v_sh;
     });
     load_rows(sm.dvn, kLK, kChunk, V, [&](int i) -> const bf16 * {
-        return p.dvn_snap + (x.gch * kChunk + i) * V;
+        return p.dvn_snap + (x.gch * kChunk + i) * p.snap_ld;
     });
     load_rows(sm.u.a.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
-        return p.vn_snap + (x.gch * kChunk + i) * V;
+        return p.vn_snap + (x.gch * kChunk + i) * p.snap_ld;
     });
     load_rows(sm.u.a.h, kLK, kKP, V, [&](int r) -> const bf16 * {
-        return r < K ? p.h_snap + (x.gch * K + r) * V : nullptr;
+        return r < K ? p.h_snap + (x.gch * K + r) * p.snap_ld : nullptr;
     });
     load_rows(sm.u.a.dh, kLK, kKP, V, [&](int r) -> const bf16 * {
-        return r < K ? p.dh_snap + (x.gch * K + r) * V : nullptr;
+        return r < K ? p.dh_snap + (x.gch * K + r) * p.snap_ld : nullptr;
     });
     cp_async_commit();
     if (tid < kChunk) {
@@ -422,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
     __syncthreads();
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
     cp_async_wait<0>();
+    __syncthreads();
+    fill_den_v(p, x, sm.v, kLK);
     __syncthreads();
     const int last = x.Lc - 1;
     const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
@@ -656,12 +660,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
         for (int hf = 0; hf < 2; ++hf) {
             const int i = m0 + g8 + 8 * hf;
             const int tk = kv_row(i);
-            float *dst = tk >= 0 ? p.dv + ((x.row0 + tk) * p.H + x.hh) * p.vfull : nullptr;
+            float *dst = tk >= 0 ? p.dv + ((x.row0 + tk) * p.H + x.hh) * p.dv_ld : nullptr;
 #pragma unroll
             for (int n = 0; n < 8; ++n) {
                 const int c = nk0 + 8 * n + 2 * t4;
                 part[hf] += bu[n][2 * hf] * tile_at(sm.v, i, c) + bu[n][2 * hf + 1] * tile_at(sm.v, i, c + 1);
-                if (dst && c < V)
+                if (dst && c < value_cols(p))
                     *reinterpret_cast<float2 *>(dst + c) =
                         make_float2(sm.beta[i] * bu[n][2 * hf], sm.beta[i] * bu[n][2 * hf + 1]);
             }
@@ -708,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
     if (p.reverse && x.c == 0) {
         const int64_t row = x.row0 * p.H + x.hh;
         for (int e = tid; e < K; e += kThreads) p.dk[row * K + e] = p.dg[row * K + e] = 0.f;
-        for (int e = tid; e < V; e += kThreads) p.dv[row * p.vfull + e] = 0.f;
+        for (int e = tid; e < value_cols(p); e += kThreads) p.dv[row * p.dv_ld + e] = 0.f;
         if (tid == 0) p.dbeta[row] = 0.f;
     }
     // dbeta, and dgk = suffix sums of dG within the chunk, one key per thread

@@ -39,6 +39,7 @@ struct FwdParams {
     int B, T, H, K, V, n_seq;
     int reverse, accumulate, l2norm, has_den;
     int Vt;  // V + has_den: value columns carried by the scan
+    int snap_ld;  // row stride of the h / v_new snapshots: Vt rounded up to 8 (16-byte rows)
     int h_ld;  // row stride (floats) of h0 / h_final in the bf16 state pass: Vt, or the
                // full width when a backward pass recomputes one value-column range
     // workspace
@@ -94,7 +95,13 @@ struct BwdParams {
     // one pass covers value columns [v_off, v_off + V) of vfull: dout, v, dv,
     // dh_final and dh0 point at column v_off and keep rows of vfull columns
     int vfull, v_off;
+    int dv_ld;  // row stride of dv (the value columns, without the denominator's)
+    int snap_ld;  // row stride of the snapshots: V rounded up to 8 (16-byte rows)
     int acc;                 // add dq, dk, dbeta, dg into the outputs (a later value range)
+    // the denominator: its upstream gradient (B, H, T), and the column of this
+    // range that carries the ones value (-1: none; then V = the value columns)
+    const float *dden;
+    int den_col;
     float *dk_part, *dg_part;  // bwd_dq's shares of dk and dG, read by bwd_dk (workspace)
     // the forward's per-chunk operand images and snapshots (workspace)
     const unsigned char *w_img, *qg_img, *kg_img, *p_img;

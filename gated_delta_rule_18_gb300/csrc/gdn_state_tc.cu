@@ -293,8 +293,9 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             const uint4 pv = pack8(f);
             *reinterpret_cast<uint4 *>(sm + Lay::vn + (Cfg<BV>::kVnBuf == 2 ? par : 0u) * Lay::vn_bytes +
                                        (c0 / 8 + j) * 1024 + i * 16) = pv;
-            if (p.vn_snap && v0 + c0 + 8 * j < V)
-                *reinterpret_cast<uint4 *>(p.vn_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * kChunk + i) * V +
+            if (p.vn_snap && v0 + c0 + 8 * j < p.Vt)  // (the ones column's too)
+                *reinterpret_cast<uint4 *>(p.vn_snap +
+                                           (((int64_t)hh * p.max_chunks + gc0 + c) * kChunk + i) * p.snap_ld +
                                            v0 + c0 + 8 * j) = pv;
         }
     };
@@ -320,12 +321,13 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             const uint32_t par = c & 1;
             // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16; its last
             // reader, chunk c-1's first product, finished before that chunk's dh
-            bf16 *hs = p.h_snap ? p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * V + v1 : nullptr;
+            bf16 *hs = p.h_snap ? p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * p.snap_ld + v1
+                                : nullptr;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint4 hv = pack8(&h[8 * j]);
                 *reinterpret_cast<uint4 *>(sm + Lay::h + (hc / 8 + j) * 2048 + r * 16) = hv;
-                if (hs && r < K && v1 + 8 * j < V) *reinterpret_cast<uint4 *>(hs + 8 * j) = hv;
+                if (hs && r < K && v1 + 8 * j < p.Vt) *reinterpret_cast<uint4 *>(hs + 8 * j) = hv;
             }
             fence_async_smem();
             arrive(b_h);

@@ -304,6 +304,10 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
  *     e^{G_i - G_j} per key are split about 16-row block middles, as in the
  *     forward, and dgk is 0 where the forward floors gk at -10.
  *   dout: (B, T, H, V) bf16 upstream gradient of o, descriptor dod.
+ *   dden: (B, H, T) fp32 upstream gradient of den_out (the same scan over
+ *     v = 1), or NULL when the loss does not involve den. With dden the state
+ *     carries the ones column: h0, dh_final and dh0 are then (n_seq, H, K,
+ *     V + 1), as for gdn_chunk_fwd with den_out.
  *   dh_final: (n_seq, H, K, V) fp32 upstream gradient of h_final, or NULL (0).
  *   dq, dk: (B, T, H, K); dv: (B, T, H, V); dbeta, dg: (B, T, H) (dg
  *     (B, T, H, K) with gk); dh0:
@@ -312,16 +316,17 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
  *   K <= 128 and V <= 256, both multiples of 8. reverse with h0, dh_final or
  *   dh0 -> GDN_ERR_UNSUPPORTED.
  *   workspace: >= gdn_bwd_workspace_size(B, T, H, K, V, n_seq, varlen,
- *   perkey) bytes (0 for an unsupported shape), 256-byte aligned.
+ *   perkey, with_den) bytes (0 for an unsupported shape), 256-byte aligned.
  */
 size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq,
-                              int varlen, int perkey);
+                              int varlen, int perkey, int with_den);
 gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd,
                          const void *v, gdn_tensor_desc vd, const float *g,
                          const float *gk, const float *beta, const float *h0,
                          const int32_t *cu_seqlens, int n_seq,
                          const void *dout, gdn_tensor_desc dod,
-                         const float *dh_final, float *dq, float *dk,
+                         const float *dden, const float *dh_final,
+                         float *dq, float *dk,
                          float *dv, float *dbeta, float *dg, float *dh0,
                          int B, int T, int H, int K, int V, int chunk,
                          int reverse, int flags, void *workspace,

@@ -200,8 +200,8 @@ def test_chunk_bwd_rejects_on_host(L):
 
     def bw(q=P(0), qkd=d16, dod=d16, gk=None, h0=None, dhf=None, dh0=P(16), dq=P(10), V=64, T=128,
            reverse=0, flags=0, wsb=1 << 30):
-        return L.gdn_chunk_bwd(q, P(1), qkd, P(2), d16, P(3), gk, P(4), h0, None, 1, P(5), dod, dhf,
-                               dq, P(11), P(12), P(13), P(14), dh0, 1, T, 2, 64, V, 64, reverse,
+        return L.gdn_chunk_bwd(q, P(1), qkd, P(2), d16, P(3), gk, P(4), h0, None, 1, P(5), dod, None,
+                               dhf, dq, P(11), P(12), P(13), P(14), dh0, 1, T, 2, 64, V, 64, reverse,
                                flags, P(9), wsb, None)
     assert bw(dq=None) == NULL
     assert bw(qkd=d32) == DTYPE                # bf16 inputs only
@@ -219,6 +219,8 @@ def test_chunk_bwd_rejects_on_host(L):
     assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 256) == gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 128)
     assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 264) == 0
     assert gdn.gdn_bwd_workspace_size(1, 300, 2, 64, 64, 3, True) > 0
+    # the denominator's column: V = 128 runs as ranges of 120 and 8 + the ones column
+    assert gdn.gdn_bwd_workspace_size(1, 128, 2, 64, 128, with_den=True) > 0
 
 
 def test_bidir_rejects_on_host(L):

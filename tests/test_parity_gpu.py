@@ -1003,3 +1003,43 @@ def test_merge_backward(dtype, with_gate):
     assert set(got) == set(ref)
     for n in ref:
         assert rel_err(got[n].double().cpu().numpy(), ref[n]) <= 1e-5, n
+
+
+# ---- the token rule's backward with the denominator's upstream gradient: the
+# oracle runs on [v | 1] with [dO | dden] (the ones column's dv dropped)
+
+DEN_BWD = {
+    "causal_h0_v64": (dict(B=2, T=200, H=2, K=64, V=64, h0_std=0.5), False),
+    "reverse_v64": (dict(B=1, T=150, H=2, K=64, V=64), True),
+    "v128_gk_varlen": (dict(B=1, T=1 + 64 + 130, H=2, K=128, V=128, h0_std=0.5, g_mu=None, gk_mu=3.0,
+                            lengths=[1, 64, 130]), False),
+    "v256_h0": (dict(B=1, T=190, H=2, K=64, V=256, h0_std=0.5), False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DEN_BWD))
+def test_backward_with_den(name):
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    spec, reverse = DEN_BWD[name]
+    spec = dict(spec)
+    h0_std = spec.pop("h0_std", None)
+    w = workloads.make(**spec, seed=95, name="bwd_den_" + name)
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    rng = np.random.default_rng(96)
+    dout = workloads.stored_normal(97, "dout", (B, T, H, V), "bf16")
+    dden = rng.standard_normal((B, H, T)).astype(np.float32)
+    h0 = None if reverse or h0_std is None else (rng.standard_normal((w.n_seq, H, K, V + 1)) * h0_std).astype(np.float32)
+    dhf = None if reverse else rng.standard_normal((w.n_seq, H, K, V + 1)).astype(np.float32)
+    va = np.concatenate([w.v.values, np.ones((B, T, H, 1))], axis=-1)
+    da = np.concatenate([dout.values, dden.transpose(0, 2, 1)[..., None].astype(np.float64)], axis=-1)
+    ref = backward.scan_grad(w.q.values, w.k.values, va, w.beta, w.g, da, h0=h0, dh_final=dhf,
+                             reverse=reverse, l2norm=True, cu_seqlens=w.cu_seqlens, gk=w.gk)
+    ref["dv"] = ref["dv"][..., :V]
+    got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(dout), h0=f32_dev(h0), dh_final=f32_dev(dhf), reverse=reverse,
+                            qk_l2norm=True, cu_seqlens=i32_dev(w.cu_seqlens), gk=f32_dev(w.gk),
+                            dden=f32_dev(dden))
+    torch().cuda.synchronize()
+    errs = {n: rel_err(got[n].double().cpu().numpy(), ref[n]) for n in got}
+    assert all(e <= 1.5e-2 for e in errs.values()), (name, errs)
