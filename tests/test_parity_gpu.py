@@ -1043,3 +1043,78 @@ def test_backward_with_den(name):
     torch().cuda.synchronize()
     errs = {n: rel_err(got[n].double().cpu().numpy(), ref[n]) for n in got}
     assert all(e <= 1.5e-2 for e in errs.values()), (name, errs)
+
+
+# ---- the torch.autograd wrappers, against the oracles composed the same way
+
+@pytest.mark.parametrize("gate_kind", ["scalar", "perkey"])
+def test_autograd_chunk_gated_delta_rule(gate_kind):
+    from gated_delta_rule_18_gb300.autograd import chunk_gated_delta_rule
+    from oracle import backward
+    t = torch()
+    spec = dict(h0_std=0.5) if gate_kind == "scalar" else dict(h0_std=0.5, g_mu=None, gk_mu=3.0)
+    w = workloads.make(2, 150, 2, 64, 64, "bf16", seed=101, **spec)
+    q, k, v = (to_dev(x).requires_grad_() for x in (w.q, w.k, w.v))
+    beta = f32_dev(w.beta).requires_grad_()
+    gate = f32_dev(w.g if gate_kind == "scalar" else w.gk).requires_grad_()
+    h0 = f32_dev(w.h0).requires_grad_()
+    o, hf = chunk_gated_delta_rule(q, k, v, beta, g=gate if gate_kind == "scalar" else None,
+                                   gk=gate if gate_kind == "perkey" else None, initial_state=h0,
+                                   output_final_state=True)
+    rng = np.random.default_rng(102)
+    do = workloads.stored_normal(103, "dout", tuple(o.shape), "bf16")
+    dhf = rng.standard_normal(tuple(hf.shape)).astype(np.float32)
+    loss = (o.float() * to_dev(do).float()).sum() + (hf * f32_dev(dhf)).sum()
+    grads = t.autograd.grad(loss, (q, k, v, beta, gate, h0))
+    ref = backward.scan_grad(w.q.values, w.k.values, w.v.values, w.beta, w.g, do.values, h0=w.h0,
+                             dh_final=dhf, l2norm=True, gk=w.gk)
+    for name, gr in zip(("dq", "dk", "dv", "dbeta", "dg", "dh0"), grads):
+        assert rel_err(gr.double().cpu().numpy(), ref[name]) <= 1.5e-2, name
+
+
+def test_autograd_bidirectional_merge():
+    """the bidirectional form with the chunk-causal reverse gates, den and a
+    gate: the merged output's gradients. q and k are non-negative, as after
+    the pages' ReLU, so den stays positive and the merge well conditioned."""
+    from gated_delta_rule_18_gb300.autograd import bidirectional_gated_delta_rule
+    from oracle import backward
+    t = torch()
+    B, T, H, K, V = 1, 200, 2, 64, 64
+    w = workloads.make(B, T, H, K, V, "bf16", seed=104)
+    g_bwd = w.g.copy()
+    g_bwd[:, ::64] = -np.inf                                  # a reset every 64 tokens
+    beta_bwd = w.beta.copy()
+    beta_bwd[:, ::64] = 0.0
+    rng = np.random.default_rng(105)
+    gate64 = rng.standard_normal((B, T, H, V)) * 2
+    gate = t.from_numpy(gate64).to(dev()).to(t.bfloat16)
+    q, k = (to_dev(x).abs().requires_grad_() for x in (w.q, w.k))
+    v = to_dev(w.v).requires_grad_()
+    beta, g = f32_dev(w.beta).requires_grad_(), f32_dev(w.g).requires_grad_()
+    gb, bb = f32_dev(g_bwd).requires_grad_(), f32_dev(beta_bwd).requires_grad_()
+    gate.requires_grad_()
+    out = bidirectional_gated_delta_rule(q, k, v, beta, g, g_bwd=gb, beta_bwd=bb, gate=gate, eps=1e-3)
+    dout = workloads.stored_normal(106, "dout", (B, T, H, V), "bf16")
+    loss = (out.float() * to_dev(dout).float()).sum()
+    grads = t.autograd.grad(loss, (q, k, v, beta, g, gb, bb, gate))
+    # the oracle composed: forward and reverse scans on [v | 1], merge, then
+    # the merge's gradient fed back through both scans
+    qa, ka = np.abs(w.q.values), np.abs(w.k.values)
+    qn, kn = oracle.l2norm(qa), oracle.l2norm(ka)
+    va = np.concatenate([w.v.values, np.ones((B, T, H, 1))], axis=-1)
+    of, _ = oracle.scan(qn, kn, va, w.beta, g=w.g)
+    orv, _ = oracle.scan(qn, kn, va, beta_bwd, g=g_bwd, reverse=True)
+    num = (of + orv)[..., :V]
+    den = np.ascontiguousarray((of + orv)[..., V].transpose(0, 2, 1))
+    assert den.min() > 0.05, den.min()  # a well-conditioned merge
+    gq = t.from_numpy(gate64).to(t.bfloat16).double().numpy()
+    m = backward.merge_grad(num, den, dout.values, gate=gq, eps=1e-3)
+    da = np.concatenate([m["dnum"], m["dden"].transpose(0, 2, 1)[..., None]], axis=-1)
+    rf = backward.scan_grad(qa, ka, va, w.beta, w.g, da, l2norm=True)
+    rr = backward.scan_grad(qa, ka, va, beta_bwd, g_bwd, da, reverse=True, l2norm=True)
+    want = {"dq": rf["dq"] + rr["dq"], "dk": rf["dk"] + rr["dk"],
+            "dv": (rf["dv"] + rr["dv"])[..., :V], "dbeta": rf["dbeta"], "dg": rf["dg"],
+            "dg_bwd": rr["dg"], "dbeta_bwd": rr["dbeta"], "dgate": m["dgate"]}
+    for name, gr in zip(("dq", "dk", "dv", "dbeta", "dg", "dg_bwd", "dbeta_bwd", "dgate"), grads):
+        got = np.nan_to_num(gr.double().cpu().numpy())
+        assert rel_err(got, np.nan_to_num(want[name])) <= 1.5e-2, name
