@@ -59,11 +59,13 @@ __device__ __forceinline__ void load_rows(bf16 *dst, int ld, int rows, int ncol,
     }
 }
 
-// row sums of a warp's 16 x 32 fragment set c (see gdn_mma.cuh) added into
+// row sums of a warp's 16 x 32 fragment set c (see gdn_mma.cuh) stored into
 // row_dst[m0 ..], and column sums times col_sign into col_dst[n0 ..]: the
-// gate-gradient terms of entries that depend on G_i - G_j
-__device__ __forceinline__ void rowcol_add(const float (&c)[4][4], int m0, int n0, float *row_dst,
-                                           float *col_dst, float col_sign) {
+// gate-gradient terms of entries that depend on G_i - G_j. Every row and
+// column has one writer per warp, so the caller's slots are summed in a
+// fixed order (bit-reproducible runs).
+__device__ __forceinline__ void rowcol_store(const float (&c)[4][4], int m0, int n0, float *row_dst,
+                                             float *col_dst, float col_sign) {
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -72,7 +74,7 @@ __device__ __forceinline__ void rowcol_add(const float (&c)[4][4], int m0, int n
         for (int n = 0; n < 4; ++n) r += c[n][2 * hf] + c[n][2 * hf + 1];
         r += __shfl_xor_sync(0xffffffffu, r, 1);
         r += __shfl_xor_sync(0xffffffffu, r, 2);
-        if (t4 == 0 && r != 0.f) atomicAdd(row_dst + m0 + g8 + 8 * hf, r);
+        if (t4 == 0) row_dst[m0 + g8 + 8 * hf] = r;
     }
 #pragma unroll
     for (int n = 0; n < 4; ++n)
@@ -82,7 +84,7 @@ __device__ __forceinline__ void rowcol_add(const float (&c)[4][4], int m0, int n
             v += __shfl_xor_sync(0xffffffffu, v, 4);
             v += __shfl_xor_sync(0xffffffffu, v, 8);
             v += __shfl_xor_sync(0xffffffffu, v, 16);
-            if (g8 == 0 && v != 0.f) atomicAdd(col_dst + n0 + 8 * n + 2 * t4 + b, col_sign * v);
+            if (g8 == 0) col_dst[n0 + 8 * n + 2 * t4 + b] = col_sign * v;
         }
 }
 

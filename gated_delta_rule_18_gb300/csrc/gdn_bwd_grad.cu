@@ -67,7 +67,10 @@ __device__ __forceinline__ void gates(const BwdParams &p, const ChunkCtx &x, flo
 struct DqSmem {
     bf16 q[kChunk * kLK], k[kChunk * kLK], dout[kChunk * kLK], vn[kChunk * kLK];
     bf16 h[kKP * kLK];  // (M_P takes the v_new tile's space once dP is formed)
-    float G[kChunk], graw[kChunk], rq[kChunk], rk[kChunk], dG[kChunk], row[kChunk];
+    float G[kChunk], graw[kChunk], rq[kChunk], rk[kChunk], row[kChunk];
+    // dG's pieces, one slot per contributing warp (summed in a fixed order):
+    // P's row sums by column half, its column sums by row block, qg's by key half
+    float dGs[8][kChunk];
 };
 
 __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) {
@@ -103,7 +106,8 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
         return r < K ? p.h_snap + (x.gch * K + r) * p.snap_ld : nullptr;
     });
     cp_async_commit();
-    if (tid < kChunk) sm.dG[tid] = sm.row[tid] = 0.f;
+    for (int e = tid; e < 8 * kChunk; e += kThreads) (&sm.dGs[0][0])[e] = 0.f;
+    if (tid < kChunk) sm.row[tid] = 0.f;
     gates(p, x, sm.G, nullptr, sm.graw);
     cp_async_wait<1>();
     __syncthreads();
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
                 }
                 *reinterpret_cast<uint32_t *>(sm.vn + i * kL6 + n0 + 8 * n + 2 * t4) = pack_bf16(mpv[0], mpv[1]);
             }
-        rowcol_add(ct, m0, n0, sm.dG, sm.dG, -1.f);
+        rowcol_store(ct, m0, n0, sm.dGs[warp >> 2], sm.dGs[2 + (warp & 3)], -1.f);
     }
     __syncthreads();
 
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
             float v = part[hf];
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
-            if (t4 == 0 && m0 + g8 + 8 * hf < x.Lc) atomicAdd(&sm.dG[m0 + g8 + 8 * hf], v);
+            if (t4 == 0) sm.dGs[6 + (warp >> 2)][m0 + g8 + 8 * hf] = m0 + g8 + 8 * hf < x.Lc ? v : 0.f;
         }
         warp_gemm(dq, Tile{sm.vn, kL6}, false, Tile{sm.k, kLK}, true, m0, nk0, kChunk, lane);
     }
@@ -236,7 +240,10 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
     __syncthreads();
     if (tid < x.Lc) {  // this kernel's share of dG, at the kv rows (bwd_dk adds the rest)
         const int tk = kv_token(p.reverse, x.len, x.pos0 + tid);
-        if (tk >= 0) p.dg_part[(x.row0 + tk) * p.H + x.hh] = sm.dG[tid];
+        float dGv = 0.f;
+#pragma unroll
+        for (int x8 = 0; x8 < 8; ++x8) dGv += sm.dGs[x8][tid];
+        if (tk >= 0) p.dg_part[(x.row0 + tk) * p.H + x.hh] = dGv;
     }
 }
 
@@ -260,8 +267,12 @@ struct DkSmem {
         DkP2 b;
     } u;
     float kkg[kChunk * kPS];  // (K^ K^T . Gamma), strictly lower
-    float G[kChunk], graw[kChunk], beta[kChunk], rk[kChunk], dG[kChunk], dB[kChunk], row[kChunk];
-    float gc;  // dL/dG_C
+    float G[kChunk], graw[kChunk], beta[kChunk], rk[kChunk], row[kChunk];
+    // dG's, dbeta's and dG_C's pieces, one slot per contributing warp (summed in
+    // a fixed order): dG: kg (by key half), A's rows (column half), A's
+    // columns (row block), X_w (key half); dbeta: A (column half), X_w, u (key
+    // half); dG_C: the decay per warp, kg per key half and row
+    float dGs[10][kChunk], dBs[6][kChunk], gck[2][kChunk], gcs[kThreads / 32];
 };
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) {
@@ -310,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             pdk[hf][n] = (src && d < K) ? *reinterpret_cast<const float2 *>(src + d) : make_float2(0.f, 0.f);
         }
     }
-    if (tid < kChunk) sm.dG[tid] = sm.dB[tid] = sm.row[tid] = 0.f;
-    if (tid == 0) sm.gc = 0.f;
+    for (int e = tid; e < 10 * kChunk; e += kThreads) (&sm.dGs[0][0])[e] = 0.f;
+    for (int e = tid; e < 6 * kChunk; e += kThreads) (&sm.dBs[0][0])[e] = 0.f;
+    if (tid < kChunk) sm.row[tid] = sm.gck[0][tid] = sm.gck[1][tid] = 0.f;
     gates(p, x, sm.G, sm.beta, sm.graw);
     cp_async_wait<1>();
     __syncthreads();
@@ -352,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0) atomicAdd(&sm.gc, acc * __expf(GC));
+        if (lane == 0) sm.gcs[warp] = acc * __expf(GC);
     }
     __syncthreads();
 
@@ -385,9 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             float s = part[hf];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t4 == 0 && s != 0.f) {  // kg_i = e^{G_C - G_i} k^_i
-                atomicAdd(&sm.dG[m0 + g8 + 8 * hf], -s);
-                atomicAdd(&sm.gc, s);
+            if (t4 == 0) {  // kg_i = e^{G_C - G_i} k^_i
+                sm.dGs[warp >> 2][m0 + g8 + 8 * hf] = -s;
+                sm.gck[warp >> 2][m0 + g8 + 8 * hf] = s;
             }
         }
     }
@@ -485,9 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             float s = pb[hf];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t4 == 0 && s != 0.f) atomicAdd(&sm.dB[m0 + g8 + 8 * hf], s);
+            if (t4 == 0) sm.dBs[warp >> 2][m0 + g8 + 8 * hf] = s;
         }
-        rowcol_add(ct, m0, n0, sm.dG, sm.dG, -1.f);
+        rowcol_store(ct, m0, n0, sm.dGs[2 + (warp >> 2)], sm.dGs[4 + (warp & 3)], -1.f);
     }
     __syncthreads();
     // dk^ += dS K^ + beta e^{G} . (T^T dw)
@@ -511,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             const int i = m0 + g8 + 8 * hf;
-            if (t4 == 0 && i < x.Lc && s != 0.f) {
-                atomicAdd(&sm.dB[i], egr[hf] * s);
-                atomicAdd(&sm.dG[i], sm.beta[i] * egr[hf] * s);
+            if (t4 == 0) {
+                sm.dBs[2 + (warp >> 2)][i] = i < x.Lc ? egr[hf] * s : 0.f;
+                sm.dGs[8 + (warp >> 2)][i] = i < x.Lc ? sm.beta[i] * egr[hf] * s : 0.f;
             }
         }
     }
@@ -566,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             float s = part[hf];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t4 == 0 && s != 0.f) atomicAdd(&sm.dB[m0 + g8 + 8 * hf], s);
+            if (t4 == 0) sm.dBs[4 + (warp >> 2)][m0 + g8 + 8 * hf] = s;
         }
     }
     __syncthreads();
@@ -605,10 +617,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         float d0 = 0.f, d1 = 0.f;
         const int i0 = 2 * lane, i1 = 2 * lane + 1;
         const int t0 = kv_row(i0), t1 = kv_row(i1);
-        if (t0 >= 0) d0 = sm.dG[i0] + p.dg_part[(x.row0 + t0) * p.H + x.hh];
-        if (t1 >= 0) d1 = sm.dG[i1] + p.dg_part[(x.row0 + t1) * p.H + x.hh];
-        if (i0 == last) d0 += sm.gc;
-        if (i1 == last) d1 += sm.gc;
+        float dG0 = 0.f, dG1 = 0.f, dB0 = 0.f, dB1 = 0.f;
+#pragma unroll
+        for (int x10 = 0; x10 < 10; ++x10) dG0 += sm.dGs[x10][i0], dG1 += sm.dGs[x10][i1];
+#pragma unroll
+        for (int x6 = 0; x6 < 6; ++x6) dB0 += sm.dBs[x6][i0], dB1 += sm.dBs[x6][i1];
+        // dG_C: the decay's pieces and the kg terms of every row (a fixed reduction tree)
+        const float gc = warp_sum((lane < kThreads / 32 ? sm.gcs[lane] : 0.f) + sm.gck[0][i0] + sm.gck[0][i1] +
+                                  sm.gck[1][i0] + sm.gck[1][i1]);
+        if (t0 >= 0) d0 = dG0 + p.dg_part[(x.row0 + t0) * p.H + x.hh];
+        if (t1 >= 0) d1 = dG1 + p.dg_part[(x.row0 + t1) * p.H + x.hh];
+        if (i0 == last) d0 += gc;
+        if (i1 == last) d1 += gc;
         // suffix sum over lanes of the pair sums
         float incl = d0 + d1;
 #pragma unroll
@@ -622,13 +642,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             const int64_t row = (x.row0 + t0) * p.H + x.hh;
             const float dg0 = sm.graw[i0] < kLogGateMin ? 0.f : s0;
             p.dg[row] = p.acc ? p.dg[row] + dg0 : dg0;
-            p.dbeta[row] = p.acc ? p.dbeta[row] + sm.dB[i0] : sm.dB[i0];
+            p.dbeta[row] = p.acc ? p.dbeta[row] + dB0 : dB0;
         }
         if (t1 >= 0) {
             const int64_t row = (x.row0 + t1) * p.H + x.hh;
             const float dg1 = sm.graw[i1] < kLogGateMin ? 0.f : s1;
             p.dg[row] = p.acc ? p.dg[row] + dg1 : dg1;
-            p.dbeta[row] = p.acc ? p.dbeta[row] + sm.dB[i1] : sm.dB[i1];
+            p.dbeta[row] = p.acc ? p.dbeta[row] + dB1 : dB1;
         }
     }
 }

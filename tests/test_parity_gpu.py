@@ -1118,3 +1118,24 @@ def test_autograd_bidirectional_merge():
     for name, gr in zip(("dq", "dk", "dv", "dbeta", "dg", "dg_bwd", "dbeta_bwd", "dgate"), grads):
         got = np.nan_to_num(gr.double().cpu().numpy())
         assert rel_err(got, np.nan_to_num(want[name])) <= 1.5e-2, name
+
+
+def test_backward_bit_reproducible():
+    """the scalar-gate backward on the 4 x 4096-token, 16-head workload with
+    h0, dh_final and the denominator: two runs give bit-identical gradients
+    (every cross-warp sum has a fixed order)"""
+    import gated_delta_rule_18_gb300 as gdn
+    t = torch()
+    w = workloads.build("causal_bf16_b4h16t4096d128")
+    rng = np.random.default_rng(111)
+    dout = to_dev(workloads.stored_normal(112, "dout", (w.B, w.T, w.H, w.V), "bf16"))
+    dden = f32_dev(rng.standard_normal((w.B, w.H, w.T)).astype(np.float32))
+    h0 = f32_dev((rng.standard_normal((w.B, w.H, w.K, w.V + 1)) * 0.1).astype(np.float32))
+    dhf = f32_dev(rng.standard_normal((w.B, w.H, w.K, w.V + 1)).astype(np.float32))
+    args = (to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g), dout)
+    a = gdn.gdn_chunk_bwd(*args, h0=h0, dh_final=dhf, dden=dden, qk_l2norm=True)
+    b = gdn.gdn_chunk_bwd(*args, h0=h0, dh_final=dhf, dden=dden, qk_l2norm=True)
+    t.cuda.synchronize()
+    for n in a:
+        assert t.isfinite(a[n]).all(), n
+        assert t.equal(a[n], b[n]), n
