@@ -1139,3 +1139,46 @@ def test_backward_bit_reproducible():
     for n in a:
         assert t.isfinite(a[n]).all(), n
         assert t.equal(a[n], b[n]), n
+
+
+def test_autograd_frame_video():
+    """the SANA video form end to end (RMS/ReLU prep, both frame-causal
+    directions with den, gated merge) on a small interleaved-qkv case: all
+    input gradients against the oracles composed the same way"""
+    from gated_delta_rule_18_gb300.autograd import frame_video_gated_delta_rule
+    from oracle import backward
+    t = torch()
+    B, T, H, D, S = 1, 256, 2, 64, 64
+    rng = np.random.default_rng(121)
+    qkv = t.from_numpy(rng.standard_normal((B, T, 3, H, D))).to(dev()).to(t.bfloat16)
+    q, k, v = (qkv[:, :, i].detach().requires_grad_() for i in range(3))
+    # small betas: a frame's update I - K^T diag(beta) K stays contractive
+    # (sum_t beta_t |k_t|^2 < 1 over 64 tokens), so den stays positive
+    beta64 = 0.03 / (1.0 + np.exp(-rng.standard_normal((B, T, H))))
+    gf64 = workloads.log_sigmoid_normal(122, "g_frame", (B, T // S, H), 2.0)
+    gate64 = rng.standard_normal((B, T, H, D))
+    beta, gf = f32_dev(beta64).requires_grad_(), f32_dev(gf64).requires_grad_()
+    gate = t.from_numpy(gate64).to(dev()).to(t.bfloat16).requires_grad_()
+    out = frame_video_gated_delta_rule(q, k, v, beta, gf, S, gate=gate, eps=1e-3)
+    dout = workloads.stored_normal(123, "dout", (B, T, H, D), "bf16")
+    loss = (out.float() * to_dev(dout).float()).sum()
+    grads = t.autograd.grad(loss, (q, k, v, beta, gf, gate))
+    # oracles: prep, frame scans on [v | 1], merge; then the chain backwards
+    qv, kv, vv = (x.detach().double().cpu().numpy() for x in (q, k, v))
+    b32 = np.asarray(beta64, np.float32).astype(np.float64)
+    g32 = np.asarray(gf64, np.float32).astype(np.float64)
+    qn, _ = oracle.rmsnorm_channels(qv, 1e-5, relu=True, scale=1.0)
+    kn, _ = oracle.rmsnorm_channels(kv, 1e-5, relu=True, scale=D ** -0.5)
+    va = np.concatenate([vv, np.ones((B, T, H, 1))], axis=-1)
+    of, _ = oracle.frame_scan(qn, kn, va, b32, g32, S)
+    orv, _ = oracle.frame_scan(qn, kn, va, b32, g32, S, reverse=True)
+    num, den = (of + orv)[..., :D], np.ascontiguousarray((of + orv)[..., D].transpose(0, 2, 1))
+    assert den.min() > 0.05, den.min()
+    gq = gate.detach().double().cpu().numpy()
+    m = backward.merge_grad(num, den, dout.values, gate=gq, eps=1e-3)
+    f = backward.frame_grad(qn, kn, vv, b32, g32, S, m["dnum"], dden=m["dden"], direction=2)
+    want = {"dq": backward.prep_grad(qv, f["dq"], rms=True, relu=True, scale=1.0),
+            "dk": backward.prep_grad(kv, f["dk"], rms=True, relu=True, scale=D ** -0.5),
+            "dv": f["dv"], "dbeta": f["dbeta"], "dg_frame": f["dg_frame"], "dgate": m["dgate"]}
+    for name, gr in zip(("dq", "dk", "dv", "dbeta", "dg_frame", "dgate"), grads):
+        assert rel_err(gr.double().cpu().numpy(), want[name]) <= 1.5e-2, name
