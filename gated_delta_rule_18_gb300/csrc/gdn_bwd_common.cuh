@@ -47,37 +47,38 @@ __device__ __forceinline__ ChunkCtx chunk_ctx(const BwdParams &p) {
 }
 
 // 16-byte pieces of a (rows x ncol) bf16 block into a row-major 128-column
-// tile: thread t copies piece t % 16 of rows t / 16, t / 16 + 16, ...; rows
-// with no source (row_ptr NULL) and columns >= ncol are zero-filled
-template <class RowPtr>
+// tile: thread t copies piece t % 16 of rows t / 16, t / 16 + NT / 16, ...;
+// rows with no source (row_ptr NULL) and columns >= ncol are zero-filled
+template <int NT = kThreads, class RowPtr>
 __device__ __forceinline__ void load_rows(bf16 *dst, int ld, int rows, int ncol, RowPtr row_ptr) {
     const int c8 = (threadIdx.x & 15) * 8;
-    for (int i = threadIdx.x >> 4; i < rows; i += kThreads / 16) {
+    for (int i = threadIdx.x >> 4; i < rows; i += NT / 16) {
         const bf16 *src = row_ptr(i);
         const bool in = src != nullptr && c8 < ncol;
         cp_async16(dst + i * ld + c8, in ? src + c8 : dst, in ? 16 : 0);
     }
 }
 
-// row sums of a warp's 16 x 32 fragment set c (see gdn_mma.cuh) stored into
-// row_dst[m0 ..], and column sums times col_sign into col_dst[n0 ..]: the
-// gate-gradient terms of entries that depend on G_i - G_j. Every row and
+// row sums of a warp's 16 x (8 NF) fragment set c (see gdn_mma.cuh) stored
+// into row_dst[m0 ..], and column sums times col_sign into col_dst[n0 ..]:
+// the gate-gradient terms of entries that depend on G_i - G_j. Every row and
 // column has one writer per warp, so the caller's slots are summed in a
 // fixed order (bit-reproducible runs).
-__device__ __forceinline__ void rowcol_store(const float (&c)[4][4], int m0, int n0, float *row_dst,
+template <int NF>
+__device__ __forceinline__ void rowcol_store(const float (&c)[NF][4], int m0, int n0, float *row_dst,
                                              float *col_dst, float col_sign) {
     const int lane = threadIdx.x & 31, g8 = lane >> 2, t4 = lane & 3;
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         float r = 0.f;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) r += c[n][2 * hf] + c[n][2 * hf + 1];
+        for (int n = 0; n < NF; ++n) r += c[n][2 * hf] + c[n][2 * hf + 1];
         r += __shfl_xor_sync(0xffffffffu, r, 1);
         r += __shfl_xor_sync(0xffffffffu, r, 2);
         if (t4 == 0) row_dst[m0 + g8 + 8 * hf] = r;
     }
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < NF; ++n)
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
             float v = c[n][b] + c[n][2 + b];
@@ -89,10 +90,11 @@ __device__ __forceinline__ void rowcol_store(const float (&c)[4][4], int m0, int
 }
 
 // L2 norms of 64 rows of a tile (1 when not normalising), then the rows
-// scaled in place (bf16)
+// scaled in place (bf16); NT threads call it (threads past 256 only scale)
+template <int NT = kThreads>
 __device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_out, bool l2) {
     const int tid = threadIdx.x;
-    {  // four threads per row, each a quarter of the columns
+    if (tid < 4 * kChunk) {  // four threads per row, each a quarter of the columns (whole warps)
         const int row = tid >> 2, q4 = tid & 3;
         float ss = 0.f;
         for (int d = 8 * q4; d < ncol; d += 32) {
@@ -110,7 +112,7 @@ __device__ __forceinline__ void norm_rows(bf16 *t, int ld, int ncol, float *r_ou
     }
     __syncthreads();
     if (!l2) return;
-    for (int e = tid; e < kChunk * (ncol / 8); e += kThreads) {
+    for (int e = tid; e < kChunk * (ncol / 8); e += NT) {
         const int i = e / (ncol / 8), d = (e % (ncol / 8)) * 8;
         uint4 u = *reinterpret_cast<const uint4 *>(t + i * ld + d);
         __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
@@ -150,11 +152,12 @@ __device__ __forceinline__ int value_cols(const BwdParams &p) { return p.den_col
 // block row I of T is sum_{M<I} B_IM (block row M) next to T_II (bf16
 // products, fp32 sums). T goes to sTb (bf16, row stride kL6); sAb and sBb
 // (same shape) hold A and the B_IM meanwhile. Every thread of the CTA calls
-// it; it ends with a barrier.
+// it (NT threads); it ends with a barrier.
+template <int NT = kThreads>
 __device__ __forceinline__ void solve_t(const float *kkg, const float *beta, bf16 *sTb, bf16 *sAb,
                                         bf16 *sBb) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, t4 = lane & 3;
-    for (int e = tid; e < kChunk * 32; e += kThreads) {
+    for (int e = tid; e < kChunk * 32; e += NT) {
         const int i = e >> 5, j = (e & 31) * 2;
         const float a0 = j < i ? beta[i] * kkg[i * kPS + j] : 0.f;
         const float a1 = j + 1 < i ? beta[i] * kkg[i * kPS + j + 1] : 0.f;

@@ -47,27 +47,58 @@
 namespace gdn {
 namespace {
 
-// per-key in-chunk cumulative log gates of the kv rows (floored as in the
-// forward; rows without a token and keys >= K stay 0), fp32 [64][kKP]
-__device__ __forceinline__ void gates_gk(const BwdParams &p, const ChunkCtx &x, float *G) {
+// row stride of the fp32 gate tile: the fragment epilogues read it as float2
+// pairs at 8 rows x 4 column pairs, conflict-free at this stride
+constexpr int kGS = kKP + 8;
+
+// G at (row i, keys d, d + 1), d even
+__device__ __forceinline__ float2 g2(const float *G, int i, int d) {
+    return *reinterpret_cast<const float2 *>(G + i * kGS + d);
+}
+// G at (row i, keys d .. d + 7), d a multiple of 8
+__device__ __forceinline__ void g8v(const float *G, int i, int d, float *f) {
+    const float4 a = *reinterpret_cast<const float4 *>(G + i * kGS + d);
+    const float4 b = *reinterpret_cast<const float4 *>(G + i * kGS + d + 4);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+}
+
+// the raw per-key log gates of the kv rows into G (fp32, row stride kGS),
+// by 16-byte async copies in the caller's commit group: keys 64 hf .. 64 hf
+// + 63 (256 bytes a row) per half; rows without a token and keys >= K are
+// zero-filled
+__device__ __forceinline__ void gates_gk_load(const BwdParams &p, const ChunkCtx &x, float *G) {
     const int K = p.K;
-    for (int e = threadIdx.x; e < kChunk * kKP; e += kThreads) {
-        const int i = e / kKP, d = e % kKP;
-        const int tk = i < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + i) : -1;
-        float g = 0.f;
-        if (tk >= 0 && d < K) g = fmaxf(p.gk[((x.row0 + tk) * p.H + x.hh) * K + d], kLogGateMinPerKeyTC);
-        G[e] = g;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int k0 = 64 * hf;
+        load_rows(reinterpret_cast<bf16 *>(G + k0), 2 * kGS, kChunk, 2 * max(0, min(64, K - k0)),
+                  [&](int i) -> const bf16 * {
+                      const int tk = i < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + i) : -1;
+                      return tk < 0 ? nullptr
+                                    : reinterpret_cast<const bf16 *>(p.gk + ((x.row0 + tk) * p.H + x.hh) * K + k0);
+                  });
     }
-    __syncthreads();
+}
+// once those copies have landed (and a barrier): the floor of the forward,
+// then the in-chunk cumulative sums, one key per thread; ends with a barrier
+__device__ __forceinline__ void gates_gk_cumsum(float *G) {
     if (threadIdx.x < kKP) {
         float run = 0.f;
         for (int i = 0; i < kChunk; ++i) {
-            run += G[i * kKP + threadIdx.x];
-            G[i * kKP + threadIdx.x] = run;
+            run += fmaxf(G[i * kGS + threadIdx.x], kLogGateMinPerKeyTC);  // zero rows stay 0
+            G[i * kGS + threadIdx.x] = run;
         }
     }
     __syncthreads();
 }
+
+// Items of a 64 x kKP per-key tile by thread: key d = tid % kKP, rows
+// tid / kKP + (kThreads / kKP) u for u < kTileItems. Loops over them are
+// unrolled with every global load issued before the first use, so a
+// thread's loads are in flight together.
+constexpr int kRowStep = kThreads / kKP;
+constexpr int kTileItems = kChunk / kRowStep;
+static_assert(kThreads % kKP == 0, "whole rows of keys per pass");
 
 // scr row j = Y_j . e^{c (G_j - G_r(j))}, r(j) the middle row of j's 16-row
 // block (c = -1: the left product's operand, c = +1: the right's); columns
@@ -82,11 +113,14 @@ __device__ __forceinline__ void scaled_rows(bf16 *scr, const bf16 *Y, const floa
         }
         uint4 u = *reinterpret_cast<const uint4 *>(Y + j * kLK + d);
         __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
+        float gj[8], gr[8];
+        g8v(G, j, d, gj);
+        g8v(G, r, d, gr);
 #pragma unroll
         for (int x2 = 0; x2 < 4; ++x2) {
             const float2 f = __bfloat1622float2(h2[x2]);
-            const float e0 = __expf(c * (G[j * kKP + d + 2 * x2] - G[r * kKP + d + 2 * x2]));
-            const float e1 = __expf(c * (G[j * kKP + d + 2 * x2 + 1] - G[r * kKP + d + 2 * x2 + 1]));
+            const float e0 = __expf(c * (gj[2 * x2] - gr[2 * x2]));
+            const float e1 = __expf(c * (gj[2 * x2 + 1] - gr[2 * x2 + 1]));
             h2[x2] = __floats2bfloat162_rn(f.x * e0, f.y * e1);
         }
         *reinterpret_cast<uint4 *>(scr + j * kLK + d) = u;
@@ -109,12 +143,16 @@ __device__ __forceinline__ void gated_left(float (&out)[8][4], const bf16 *M, co
             warp_gemm(c, Tile{M + 16 * J, kL6}, false, Tile{scr + 16 * J * kLK, kLK}, true, m0, nk0, 16, lane);
             const int r = 16 * J + 8;
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
+            for (int n = 0; n < 8; ++n) {
+                const int d = nk0 + 8 * n + 2 * t4;
+                const float2 gr = g2(G, r, d);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = m0 + g8 + 8 * (e >> 1), d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                    out[n][e] = fmaf(c[n][e], __expf(G[i * kKP + d] - G[r * kKP + d]), out[n][e]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float2 gi = g2(G, m0 + g8 + 8 * hf, d);
+                    out[n][2 * hf] = fmaf(c[n][2 * hf], __expf(gi.x - gr.x), out[n][2 * hf]);
+                    out[n][2 * hf + 1] = fmaf(c[n][2 * hf + 1], __expf(gi.y - gr.y), out[n][2 * hf + 1]);
                 }
+            }
         }
     }
     __syncthreads();
@@ -134,12 +172,16 @@ __device__ __forceinline__ void gated_right(float (&out)[8][4], const bf16 *M, c
             warp_gemm(c, Tile{M + 16 * I * kL6, kL6}, true, Tile{scr + 16 * I * kLK, kLK}, true, m0, nk0, 16, lane);
             const int r = 16 * I + 8;
 #pragma unroll
-            for (int n = 0; n < 8; ++n)
+            for (int n = 0; n < 8; ++n) {
+                const int d = nk0 + 8 * n + 2 * t4;
+                const float2 gr = g2(G, r, d);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = m0 + g8 + 8 * (e >> 1), d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                    out[n][e] = fmaf(c[n][e], __expf(G[r * kKP + d] - G[j * kKP + d]), out[n][e]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float2 gj = g2(G, m0 + g8 + 8 * hf, d);
+                    out[n][2 * hf] = fmaf(c[n][2 * hf], __expf(gr.x - gj.x), out[n][2 * hf]);
+                    out[n][2 * hf + 1] = fmaf(c[n][2 * hf + 1], __expf(gr.y - gj.y), out[n][2 * hf + 1]);
                 }
+            }
         }
     }
     __syncthreads();
@@ -205,7 +247,7 @@ struct GkDqSmem {
     bf16 h[kKP * kLK];
     bf16 mp[kChunk * kL6];   // dP, lower including the diagonal
     bf16 scr[kChunk * kLK];  // the gated products' scaled operand
-    float G[kChunk * kKP];
+    float G[kChunk * kGS];
     float rq[kChunk], rk[kChunk], row[kChunk];
 };
 
@@ -229,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
+    gates_gk_load(p, x, sm.G);
     cp_async_commit();
     load_rows(sm.dout, kLK, kChunk, value_cols(p), [&](int i) -> const bf16 * {
         if (i >= x.Lc) return nullptr;
@@ -243,9 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
     });
     cp_async_commit();
     if (tid < kChunk) sm.row[tid] = 0.f;
-    gates_gk(p, x, sm.G);
     cp_async_wait<1>();
     __syncthreads();
+    gates_gk_cumsum(sm.G);
     norm_rows(sm.q, kLK, kq, sm.rq, p.l2norm);
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
     cp_async_wait<0>();
@@ -277,10 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
 #pragma unroll
         for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = m0 + g8 + 8 * (e >> 1), d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                dq[n][e] *= __expf(sm.G[i * kKP + d]);
-                dG[n][e] = dq[n][e] * tile_at(sm.q, i, d);
+            for (int hf = 0; hf < 2; ++hf) {
+                const int i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4;
+                const float2 gi = g2(sm.G, i, d);
+                dq[n][2 * hf] *= __expf(gi.x);
+                dq[n][2 * hf + 1] *= __expf(gi.y);
+                dG[n][2 * hf] = dq[n][2 * hf] * tile_at(sm.q, i, d);
+                dG[n][2 * hf + 1] = dq[n][2 * hf + 1] * tile_at(sm.q, i, d + 1);
             }
     }
     {  // left(dP; K^)
@@ -366,7 +412,7 @@ struct GkDkSmem {
         GkDkP1 a;
         GkDkP2 b;
     } u;
-    float G[kChunk * kKP];
+    float G[kChunk * kGS];
     float kkg[kChunk * kPS];  // Gam[K^, K^], strictly lower
     float beta[kChunk], rk[kChunk], row[kChunk];
     // dbeta's and the last row's dG pieces, one slot per contributing warp,
@@ -390,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
+    gates_gk_load(p, x, sm.G);
     cp_async_commit();
     load_rows(sm.v, kLK, kChunk, value_cols(p), [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
@@ -418,10 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
     if (tid < kKP)
 #pragma unroll
         for (int x5 = 0; x5 < 5; ++x5) sm.gcp[x5][tid] = 0.f;
-    __syncthreads();
-    gates_gk(p, x, sm.G);
     cp_async_wait<1>();
     __syncthreads();
+    gates_gk_cumsum(sm.G);
     norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
     cp_async_wait<0>();
     __syncthreads();
@@ -444,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
                 acc = fmaf(a.x, b.x, fmaf(a.y, b.y, acc));
             }
         }
-        sm.gcp[0][d] = acc * __expf(sm.G[last * kKP + d]);
+        sm.gcp[0][d] = acc * __expf(sm.G[last * kGS + d]);
     }
     float dk[8][4], dG[8][4];
     acc_zero(dk);
@@ -454,15 +500,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
         acc_zero(c);
         warp_gemm(c, Tile{sm.u.a.vn, kLK}, false, Tile{sm.u.a.dh, kLK}, false, m0, nk0, kv, lane);
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < 8; ++n) {
+            const int d0 = nk0 + 8 * n + 2 * t4;
+            const float2 gl = g2(sm.G, last, d0);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = m0 + g8 + 8 * (e >> 1), d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                const float f = i < x.Lc ? __expf(sm.G[last * kKP + d] - sm.G[i * kKP + d]) : 0.f;
-                dk[n][e] = f * c[n][e];
-                c[n][e] = f * tile_at(sm.k, i, d) * c[n][e];  // Kc . dKc
-                dG[n][e] = -c[n][e];
+            for (int hf = 0; hf < 2; ++hf) {
+                const int i = m0 + g8 + 8 * hf;
+                const float2 gi = g2(sm.G, i, d0);
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const int e = 2 * hf + b;
+                    const float f = i < x.Lc ? __expf((b ? gl.y : gl.x) - (b ? gi.y : gi.x)) : 0.f;
+                    dk[n][e] = f * c[n][e];
+                    c[n][e] = f * tile_at(sm.k, i, d0 + b) * c[n][e];  // Kc . dKc
+                    dG[n][e] = -c[n][e];
+                }
             }
+        }
         frag_colsum_store(c, nk0, sm.gcp[1 + (warp & 3)]);
     }
     if (nk0 < kq) {  // dw = -(dv_new h^T)
@@ -495,12 +549,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
             if (i >= 16 * J) {
                 u = *reinterpret_cast<const uint4 *>(sm.k + i * kLK + d);
                 __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
+                float gi[8], gr[8];
+                g8v(sm.G, i, d, gi);
+                g8v(sm.G, r, d, gr);
 #pragma unroll
                 for (int x2 = 0; x2 < 4; ++x2) {
                     const float2 f = __bfloat1622float2(h2[x2]);
-                    h2[x2] = __floats2bfloat162_rn(
-                        f.x * __expf(sm.G[i * kKP + d + 2 * x2] - sm.G[r * kKP + d + 2 * x2]),
-                        f.y * __expf(sm.G[i * kKP + d + 2 * x2 + 1] - sm.G[r * kKP + d + 2 * x2 + 1]));
+                    h2[x2] = __floats2bfloat162_rn(f.x * __expf(gi[2 * x2] - gr[2 * x2]),
+                                                   f.y * __expf(gi[2 * x2 + 1] - gr[2 * x2 + 1]));
                 }
             }
             *reinterpret_cast<uint4 *>(sm.u.b.xw + i * kLK + d) = u;
@@ -529,11 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
         const int i = e >> 4, d = (e & 15) * 8;
         uint4 u = *reinterpret_cast<const uint4 *>(sm.k + i * kLK + d);
         __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&u);
+        float gi[8];
+        g8v(sm.G, i, d, gi);
+        const float bi = sm.beta[i];
 #pragma unroll
         for (int x2 = 0; x2 < 4; ++x2) {
             const float2 kk = __bfloat1622float2(h2[x2]);
-            h2[x2] = __floats2bfloat162_rn(sm.beta[i] * __expf(sm.G[i * kKP + d + 2 * x2]) * kk.x,
-                                           sm.beta[i] * __expf(sm.G[i * kKP + d + 2 * x2 + 1]) * kk.y);
+            h2[x2] = __floats2bfloat162_rn(bi * __expf(gi[2 * x2]) * kk.x, bi * __expf(gi[2 * x2 + 1]) * kk.y);
         }
         *reinterpret_cast<uint4 *>(sm.u.b.xw + i * kLK + d) = u;
     }
@@ -623,12 +681,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
 #pragma unroll
         for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
-                const float kp = __expf(sm.G[i * kKP + d]) * tile_at(sm.k, i, d);
-                part[hf] += bw[n][e] * kp;
-                dk[n][e] = fmaf(sm.beta[i] * __expf(sm.G[i * kKP + d]), bw[n][e], dk[n][e]);
-                dG[n][e] = fmaf(sm.beta[i] * kp, bw[n][e], dG[n][e]);
+            for (int hf = 0; hf < 2; ++hf) {
+                const int i = m0 + g8 + 8 * hf, d0 = nk0 + 8 * n + 2 * t4;
+                const float2 gi = g2(sm.G, i, d0);
+                const float bi = sm.beta[i];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    const int e = 2 * hf + b;
+                    const float eg = __expf(b ? gi.y : gi.x);
+                    const float kp = eg * tile_at(sm.k, i, d0 + b);
+                    part[hf] += bw[n][e] * kp;
+                    dk[n][e] = fmaf(bi * eg, bw[n][e], dk[n][e]);
+                    dG[n][e] = fmaf(bi * kp, bw[n][e], dG[n][e]);
+                }
             }
         rowsum_store(part, m0, sm.dBp[2 + (warp >> 2)]);
     }
@@ -726,23 +791,58 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
             p.dbeta[row] = p.acc ? p.dbeta[row] + db : db;
         }
     }
+    // (1) every term of dG_i: bwd_dq_gk's share and the last row's terms;
+    // whether the forward floored gk there (its derivative is then 0). The
+    // global loads are coalesced over keys and independent of one another.
+    unsigned char *floored = reinterpret_cast<unsigned char *>(sm.u.b.scr);  // [64][kKP]
+    const int dk0 = tid % kKP, ir = tid / kKP;
+    {
+        float part[kTileItems], graw[kTileItems];
+#pragma unroll
+        for (int u = 0; u < kTileItems; ++u) {
+            const int i = ir + kRowStep * u, tk = kv_row(i);
+            part[u] = graw[u] = 0.f;
+            if (tk >= 0 && dk0 < K) {
+                const int64_t row = ((x.row0 + tk) * p.H + x.hh) * K + dk0;
+                part[u] = p.dg_part[row];
+                graw[u] = p.gk[row];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kTileItems; ++u) {
+            const int i = ir + kRowStep * u, tk = kv_row(i);
+            if (i >= x.Lc || dk0 >= K) continue;
+            float t = sm.u.b.dGs[i * kKP + dk0] + part[u];
+            if (i == last)
+#pragma unroll
+                for (int x5 = 0; x5 < 5; ++x5) t += sm.gcp[x5][dk0];
+            sm.u.b.dGs[i * kKP + dk0] = t;
+            floored[i * kKP + dk0] = tk >= 0 && graw[u] < kLogGateMinPerKeyTC;
+        }
+    }
+    __syncthreads();
+    // (2) suffix sums within the chunk, one key per thread, in shared memory
     for (int d = tid; d < K; d += kThreads) {
         float run = 0.f;
         for (int i = x.Lc - 1; i >= 0; --i) {
-            const int tk = kv_row(i);
-            float t = sm.u.b.dGs[i * kKP + d];
-            if (i == last)
+            run += sm.u.b.dGs[i * kKP + d];
+            sm.u.b.dGs[i * kKP + d] = floored[i * kKP + d] ? 0.f : run;
+        }
+    }
+    __syncthreads();
+    // (3) the stores (a later value range adds to the earlier ranges' sums)
+    {
+        float prev[kTileItems];
 #pragma unroll
-                for (int x5 = 0; x5 < 5; ++x5) t += sm.gcp[x5][d];
-            if (tk < 0) {
-                run += t;
-                continue;
-            }
-            const int64_t row = ((x.row0 + tk) * p.H + x.hh) * K + d;
-            run += t + p.dg_part[row];
-            // d/dgk of the floored gate is 0 where the forward floored it
-            const float gval = p.gk[row] < kLogGateMinPerKeyTC ? 0.f : run;
-            p.dg[row] = p.acc ? p.dg[row] + gval : gval;
+        for (int u = 0; u < kTileItems; ++u) {
+            const int i = ir + kRowStep * u, tk = kv_row(i);
+            prev[u] = (p.acc && tk >= 0 && dk0 < K) ? p.dg[((x.row0 + tk) * p.H + x.hh) * K + dk0] : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kTileItems; ++u) {
+            const int i = ir + kRowStep * u, tk = kv_row(i);
+            if (tk < 0 || dk0 >= K) continue;
+            p.dg[((x.row0 + tk) * p.H + x.hh) * K + dk0] = prev[u] + sm.u.b.dGs[i * kKP + dk0];
         }
     }
 }

@@ -31,7 +31,7 @@
 //   bwd_dk  dk (adding that partial), dv, dbeta, dg (adding bwd_dq's dG).
 // Products run on mma.sync (bf16 operands, fp32 accumulate); T = (I + A)^{-1}
 // is formed by blocks (fp32 diagonal inverses, bf16 block products). 8 warps
-// per CTA.
+// per CTA for bwd_dq, 16 for bwd_dk (4 row blocks x 4 column groups).
 #include "gdn_bwd_common.cuh"
 
 namespace gdn {
@@ -260,25 +260,32 @@ struct DkP2 {  // afterwards
     bf16 z[kChunk * kL6];
     bf16 ms[kChunk * kL6];
 };
+// NW warps: 4 row blocks of 16 times NQ = NW / 4 column groups
+template <int NW>
 struct DkSmem {
+    static constexpr int NQ = NW / 4;
     bf16 k[kChunk * kLK], v[kChunk * kLK], dvn[kChunk * kLK], dw[kChunk * kLK];
     union {
         DkP1 a;
         DkP2 b;
     } u;
     float kkg[kChunk * kPS];  // (K^ K^T . Gamma), strictly lower
-    float G[kChunk], graw[kChunk], beta[kChunk], rk[kChunk], row[kChunk];
+    float G[kChunk], graw[kChunk], beta[kChunk], rk[kChunk];
     // dG's, dbeta's and dG_C's pieces, one slot per contributing warp (summed in
-    // a fixed order): dG: kg (by key half), A's rows (column half), A's
-    // columns (row block), X_w (key half); dbeta: A (column half), X_w, u (key
-    // half); dG_C: the decay per warp, kg per key half and row
-    float dGs[10][kChunk], dBs[6][kChunk], gck[2][kChunk], gcs[kThreads / 32];
+    // a fixed order): dG: kg (by column group), A's rows (column group), A's
+    // columns (row block), X_w (column group); dbeta: A, X_w, u (column
+    // group); dG_C: the decay per warp, kg per column group and row; the
+    // normalisation's row dot dk^ . k^ per column group
+    float dGs[3 * NQ + 4][kChunk], dBs[3 * NQ][kChunk], gck[NQ][kChunk], gcs[NW], rowp[NQ][kChunk];
 };
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) {
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, 1) bwd_dk_kernel(const BwdParams p) {
+    constexpr int NT = NW * 32, NQ = NW / 4;
+    constexpr int F64 = 8 / NQ, FK = 16 / NQ;  // 8-column fragments per warp: 64- and 128-wide outputs
     extern __shared__ __align__(16) unsigned char smraw[];
-    DkSmem &sm = *reinterpret_cast<DkSmem *>(smraw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    DkSmem<NW> &sm = *reinterpret_cast<DkSmem<NW> *>(smraw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, hq = warp >> 2;
     const int g8 = lane >> 2, t4 = lane & 3;
     const ChunkCtx x = chunk_ctx(p);
     if (x.s < 0) return;
@@ -286,58 +293,58 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     const bf16 *k = (const bf16 *)p.k, *v = (const bf16 *)p.v;
     auto kv_row = [&](int i) { return i < x.Lc ? kv_token(p.reverse, x.len, x.pos0 + i) : -1; };
 
-    load_rows(sm.k, kLK, kChunk, K, [&](int i) -> const bf16 * {
+    load_rows<NT>(sm.k, kLK, kChunk, K, [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : k + x.b * p.qk_sb + (int64_t)(x.tstart + tk) * p.qk_st + x.hh * p.qk_sh;
     });
     cp_async_commit();  // k first: the norms and K K^T start while the rest lands
-    load_rows(sm.v, kLK, kChunk, value_cols(p), [&](int i) -> const bf16 * {
+    load_rows<NT>(sm.v, kLK, kChunk, value_cols(p), [&](int i) -> const bf16 * {
         const int tk = kv_row(i);
         return tk < 0 ? nullptr : v + x.b * p.v_sb + (int64_t)(x.tstart + tk) * p.v_st + x.hh * p.v_sh;
     });
-    load_rows(sm.dvn, kLK, kChunk, V, [&](int i) -> const bf16 * {
+    load_rows<NT>(sm.dvn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.dvn_snap + (x.gch * kChunk + i) * p.snap_ld;
     });
-    load_rows(sm.u.a.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
+    load_rows<NT>(sm.u.a.vn, kLK, kChunk, V, [&](int i) -> const bf16 * {
         return p.vn_snap + (x.gch * kChunk + i) * p.snap_ld;
     });
-    load_rows(sm.u.a.h, kLK, kKP, V, [&](int r) -> const bf16 * {
+    load_rows<NT>(sm.u.a.h, kLK, kKP, V, [&](int r) -> const bf16 * {
         return r < K ? p.h_snap + (x.gch * K + r) * p.snap_ld : nullptr;
     });
-    load_rows(sm.u.a.dh, kLK, kKP, V, [&](int r) -> const bf16 * {
+    load_rows<NT>(sm.u.a.dh, kLK, kKP, V, [&](int r) -> const bf16 * {
         return r < K ? p.dh_snap + (x.gch * K + r) * p.snap_ld : nullptr;
     });
     cp_async_commit();
-    const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2), nk0 = 64 * (warp >> 2);
+    const int m0 = 16 * (warp & 3), n0 = (64 / NQ) * hq, nk0 = (128 / NQ) * hq;
     // bwd_dq's M_P^T Q^ for this thread's dk fragment, loaded now (added at the end)
-    float2 pdk[2][8];
+    float2 pdk[2][FK];
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         const int tk = kv_row(m0 + g8 + 8 * hf);
         const float *src = tk >= 0 ? p.dk_part + ((x.row0 + tk) * p.H + x.hh) * K : nullptr;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
+        for (int n = 0; n < FK; ++n) {
             const int d = nk0 + 8 * n + 2 * t4;
             pdk[hf][n] = (src && d < K) ? *reinterpret_cast<const float2 *>(src + d) : make_float2(0.f, 0.f);
         }
     }
-    for (int e = tid; e < 10 * kChunk; e += kThreads) (&sm.dGs[0][0])[e] = 0.f;
-    for (int e = tid; e < 6 * kChunk; e += kThreads) (&sm.dBs[0][0])[e] = 0.f;
-    if (tid < kChunk) sm.row[tid] = sm.gck[0][tid] = sm.gck[1][tid] = 0.f;
+    for (int e = tid; e < (3 * NQ + 4) * kChunk; e += NT) (&sm.dGs[0][0])[e] = 0.f;
+    for (int e = tid; e < 3 * NQ * kChunk; e += NT) (&sm.dBs[0][0])[e] = 0.f;
+    for (int e = tid; e < NQ * kChunk; e += NT) (&sm.gck[0][0])[e] = (&sm.rowp[0][0])[e] = 0.f;
     gates(p, x, sm.G, sm.beta, sm.graw);
     cp_async_wait<1>();
     __syncthreads();
-    norm_rows(sm.k, kLK, kq, sm.rk, p.l2norm);
+    norm_rows<NT>(sm.k, kLK, kq, sm.rk, p.l2norm);
     const int last = x.Lc - 1;
     const float GC = sm.G[last];
     __syncthreads();
     // S . Gamma, strictly lower
     {
-        float sk[4][4];
+        float sk[F64][4];
         acc_zero(sk);
         warp_gemm(sk, Tile{sm.k, kLK}, false, Tile{sm.k, kLK}, false, m0, n0, kq, lane);
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int n = 0; n < F64; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int i = m0 + g8 + 8 * (e >> 1), j = n0 + 8 * n + 2 * t4 + (e & 1);
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     // e^{G_C} h . dh'  (dG_C of the state decay), 8 columns per step
     {
         float acc = 0.f;
-        for (int e = tid; e < K * (kv / 8); e += kThreads) {
+        for (int e = tid; e < K * (kv / 8); e += NT) {
             const int r = e / (kv / 8), c8 = (e % (kv / 8)) * 8;
             const uint4 ua = *reinterpret_cast<const uint4 *>(sm.u.a.h + r * kLK + c8);
             const uint4 ub = *reinterpret_cast<const uint4 *>(sm.u.a.dh + r * kLK + c8);
@@ -378,13 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         ecr[hf] = i < x.Lc ? __expf(GC - sm.G[i]) : 0.f;
     }
     // dk^ starts with the kg term: e^{G_C - G} . (v_new dh'^T)
-    float dk[8][4];
+    float dk[FK][4];
     {
         acc_zero(dk);
         warp_gemm(dk, Tile{sm.u.a.vn, kLK}, false, Tile{sm.u.a.dh, kLK}, false, m0, nk0, kv, lane);
         float part[2] = {0.f, 0.f};
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < FK; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
@@ -398,18 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             if (t4 == 0) {  // kg_i = e^{G_C - G_i} k^_i
-                sm.dGs[warp >> 2][m0 + g8 + 8 * hf] = -s;
-                sm.gck[warp >> 2][m0 + g8 + 8 * hf] = s;
+                sm.dGs[hq][m0 + g8 + 8 * hf] = -s;
+                sm.gck[hq][m0 + g8 + 8 * hf] = s;
             }
         }
     }
     // dw = -v_new' ... = -(dv_new h^T)
     {
-        float dw[8][4];
+        float dw[FK][4];
         acc_zero(dw);
         warp_gemm(dw, Tile{sm.dvn, kLK}, false, Tile{sm.u.a.h, kLK}, false, m0, nk0, kv, lane);
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < FK; ++n)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
                 *reinterpret_cast<uint32_t *>(sm.dw + (m0 + g8 + 8 * hf) * kLK + nk0 + 8 * n + 2 * t4) =
@@ -420,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     // T = (I + A)^{-1}, A_ij = beta_i (S . Gamma)_ij (i > j); A and the
     // solve's B_IM take the Y and Z tiles' space until those are formed
     bf16 *sTb = sm.u.b.tb;
-    solve_t(sm.kkg, sm.beta, sTb, sm.u.b.y, sm.u.b.z);
+    solve_t<NT>(sm.kkg, sm.beta, sTb, sm.u.b.y, sm.u.b.z);
     // X_w = beta e^{G} . K^
-    for (int e = tid; e < kChunk * (kKP / 8); e += kThreads) {
+    for (int e = tid; e < kChunk * (kKP / 8); e += NT) {
         const int i = e >> 4, d = (e & 15) * 8;
         const float f = sm.beta[i] * __expf(sm.G[i]);
         uint4 u = *reinterpret_cast<const uint4 *>(sm.k + i * kLK + d);
@@ -438,16 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     const Tile tT{sm.u.b.tb, kL6};
     // Y = dv_new (beta . V)^T + dw X_w^T
     {
-        float y[4][4];
+        float y[F64][4];
         acc_zero(y);
         warp_gemm(y, Tile{sm.dvn, kLK}, false, Tile{sm.v, kLK}, false, m0, n0, kv, lane);
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int n = 0; n < F64; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) y[n][e] *= sm.beta[n0 + 8 * n + 2 * t4 + (e & 1)];
         warp_gemm(y, Tile{sm.dw, kLK}, false, Tile{sm.u.b.xw, kLK}, false, m0, n0, kq, lane);
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int n = 0; n < F64; ++n)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
                 *reinterpret_cast<uint32_t *>(sm.u.b.y + (m0 + g8 + 8 * hf) * kL6 + n0 + 8 * n + 2 * t4) =
@@ -456,11 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     __syncthreads();
     // Z = Y T^T
     {
-        float z[4][4];
+        float z[F64][4];
         acc_zero(z);
         warp_gemm(z, Tile{sm.u.b.y, kL6}, false, tT, false, m0, n0, kChunk, lane);
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int n = 0; n < F64; ++n)
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
                 *reinterpret_cast<uint32_t *>(sm.u.b.z + (m0 + g8 + 8 * hf) * kL6 + n0 + 8 * n + 2 * t4) =
@@ -469,13 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     __syncthreads();
     // dA = -T^T Z (strictly lower): dbeta, dG, and dS = M_A + M_A^T
     {
-        float a[4][4];
+        float a[F64][4];
         acc_zero(a);
         warp_gemm(a, tT, true, Tile{sm.u.b.z, kL6}, true, m0, n0, kChunk, lane);
         float pb[2] = {0.f, 0.f};
-        float ct[4][4];  // dA_ij A_ij: d/dG_i of A_ij is A_ij, d/dG_j is -A_ij
+        float ct[F64][4];  // dA_ij A_ij: d/dG_i of A_ij is A_ij, d/dG_j is -A_ij
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+        for (int n = 0; n < F64; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, j = n0 + 8 * n + 2 * t4 + (e & 1);
@@ -497,20 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             float s = pb[hf];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t4 == 0) sm.dBs[warp >> 2][m0 + g8 + 8 * hf] = s;
+            if (t4 == 0) sm.dBs[hq][m0 + g8 + 8 * hf] = s;
         }
-        rowcol_store(ct, m0, n0, sm.dGs[2 + (warp >> 2)], sm.dGs[4 + (warp & 3)], -1.f);
+        rowcol_store(ct, m0, n0, sm.dGs[NQ + hq], sm.dGs[2 * NQ + (warp & 3)], -1.f);
     }
     __syncthreads();
     // dk^ += dS K^ + beta e^{G} . (T^T dw)
     warp_gemm(dk, Tile{sm.u.b.ms, kL6}, false, Tile{sm.k, kLK}, true, m0, nk0, kChunk, lane);
     {
-        float bw[8][4];
+        float bw[FK][4];
         acc_zero(bw);
         warp_gemm(bw, tT, true, Tile{sm.dw, kLK}, true, m0, nk0, kChunk, lane);
         float part[2] = {0.f, 0.f};
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < FK; ++n)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int hf = e >> 1, i = m0 + g8 + 8 * hf, d = nk0 + 8 * n + 2 * t4 + (e & 1);
@@ -524,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             s += __shfl_xor_sync(0xffffffffu, s, 2);
             const int i = m0 + g8 + 8 * hf;
             if (t4 == 0) {
-                sm.dBs[2 + (warp >> 2)][i] = i < x.Lc ? egr[hf] * s : 0.f;
-                sm.dGs[8 + (warp >> 2)][i] = i < x.Lc ? sm.beta[i] * egr[hf] * s : 0.f;
+                sm.dBs[NQ + hq][i] = i < x.Lc ? egr[hf] * s : 0.f;
+                sm.dGs[2 * NQ + 4 + hq][i] = i < x.Lc ? sm.beta[i] * egr[hf] * s : 0.f;
             }
         }
     }
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         for (int hf = 0; hf < 2; ++hf) {
             const int i = m0 + g8 + 8 * hf;
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
+            for (int n = 0; n < FK; ++n) {
                 const int d = nk0 + 8 * n + 2 * t4;
                 dk[n][2 * hf] += pdk[hf][n].x;
                 dk[n][2 * hf + 1] += pdk[hf][n].y;
@@ -549,12 +556,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             float s = part[hf];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t4 == 0) atomicAdd(&sm.row[m0 + g8 + 8 * hf], s);
+            if (t4 == 0) sm.rowp[hq][m0 + g8 + 8 * hf] = s;
         }
     }
     // dB_u = T^T dv_new: dv and the beta term of u
     {
-        float bu[8][4];
+        float bu[FK][4];
         acc_zero(bu);
         warp_gemm(bu, tT, true, Tile{sm.dvn, kLK}, true, m0, nk0, kChunk, lane);
         float part[2] = {0.f, 0.f};
@@ -564,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             const int tk = kv_row(i);
             float *dst = tk >= 0 ? p.dv + ((x.row0 + tk) * p.H + x.hh) * p.dv_ld : nullptr;
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
+            for (int n = 0; n < FK; ++n) {
                 const int c = nk0 + 8 * n + 2 * t4;
                 part[hf] += bu[n][2 * hf] * __bfloat162float(sm.v[i * kLK + c]) +
                             bu[n][2 * hf + 1] * __bfloat162float(sm.v[i * kLK + c + 1]);
@@ -578,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
             float s = part[hf];
             s += __shfl_xor_sync(0xffffffffu, s, 1);
             s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if (t4 == 0) sm.dBs[4 + (warp >> 2)][m0 + g8 + 8 * hf] = s;
+            if (t4 == 0) sm.dBs[2 * NQ + hq][m0 + g8 + 8 * hf] = s;
         }
     }
     __syncthreads();
@@ -589,9 +596,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         const int tk = kv_row(i);
         if (tk < 0) continue;
         float *dst = p.dk + ((x.row0 + tk) * p.H + x.hh) * K;
-        const float r = sm.rk[i], dot = sm.row[i];
+        float dot = 0.f;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
+        for (int q = 0; q < NQ; ++q) dot += sm.rowp[q][i];
+        const float r = sm.rk[i];
+#pragma unroll
+        for (int n = 0; n < FK; ++n) {
             const int d = nk0 + 8 * n + 2 * t4;
             if (d >= K) continue;
             float2 o;
@@ -608,8 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
     // the reverse scan never reads token 0's key and value: zero gradients
     if (p.reverse && x.c == 0) {
         const int64_t row = x.row0 * p.H + x.hh;
-        for (int e = tid; e < K; e += kThreads) p.dk[row * K + e] = 0.f;
-        for (int e = tid; e < value_cols(p); e += kThreads) p.dv[row * p.dv_ld + e] = 0.f;
+        for (int e = tid; e < K; e += NT) p.dk[row * K + e] = 0.f;
+        for (int e = tid; e < value_cols(p); e += NT) p.dv[row * p.dv_ld + e] = 0.f;
         if (tid == 0) p.dbeta[row] = p.dg[row] = 0.f;
     }
     // dbeta, and dg = suffix sums of dG within the chunk (G is the running sum of g)
@@ -619,12 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
         const int t0 = kv_row(i0), t1 = kv_row(i1);
         float dG0 = 0.f, dG1 = 0.f, dB0 = 0.f, dB1 = 0.f;
 #pragma unroll
-        for (int x10 = 0; x10 < 10; ++x10) dG0 += sm.dGs[x10][i0], dG1 += sm.dGs[x10][i1];
+        for (int sl = 0; sl < 3 * NQ + 4; ++sl) dG0 += sm.dGs[sl][i0], dG1 += sm.dGs[sl][i1];
 #pragma unroll
-        for (int x6 = 0; x6 < 6; ++x6) dB0 += sm.dBs[x6][i0], dB1 += sm.dBs[x6][i1];
+        for (int sl = 0; sl < 3 * NQ; ++sl) dB0 += sm.dBs[sl][i0], dB1 += sm.dBs[sl][i1];
         // dG_C: the decay's pieces and the kg terms of every row (a fixed reduction tree)
-        const float gc = warp_sum((lane < kThreads / 32 ? sm.gcs[lane] : 0.f) + sm.gck[0][i0] + sm.gck[0][i1] +
-                                  sm.gck[1][i0] + sm.gck[1][i1]);
+        float gl = lane < NW ? sm.gcs[lane] : 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) gl += sm.gck[q][i0] + sm.gck[q][i1];
+        const float gc = warp_sum(gl);
         if (t0 >= 0) d0 = dG0 + p.dg_part[(x.row0 + t0) * p.H + x.hh];
         if (t1 >= 0) d1 = dG1 + p.dg_part[(x.row0 + t1) * p.H + x.hh];
         if (i0 == last) d0 += gc;
@@ -654,10 +666,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_kernel(const BwdParams p) 
 }
 
 template <class Kern>
-cudaError_t launch_grid(Kern kern, int bytes, const BwdParams &p, cudaStream_t st) {
+cudaError_t launch_grid(Kern kern, int bytes, const BwdParams &p, cudaStream_t st, int threads = kThreads) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    kern<<<p.max_chunks * p.H, kThreads, bytes, st>>>(p);
+    kern<<<p.max_chunks * p.H, threads, bytes, st>>>(p);
     return cudaGetLastError();
 }
 
@@ -670,7 +682,9 @@ cudaError_t launch_bwd_dq(const BwdParams &p, cudaStream_t st) {
     return launch_grid(bwd_dq_kernel, (int)sizeof(DqSmem), p, st);
 }
 cudaError_t launch_bwd_dk(const BwdParams &p, cudaStream_t st) {
-    return launch_grid(bwd_dk_kernel, (int)sizeof(DkSmem), p, st);
+    // 16 warps: half the fragment work per warp of an 8-warp CTA, at one CTA
+    // per SM either way (shared memory)
+    return launch_grid(bwd_dk_kernel<16>, (int)sizeof(DkSmem<16>), p, st, 16 * 32);
 }
 
 }  // namespace gdn
