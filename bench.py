@@ -693,7 +693,8 @@ def main():
                     help="override the token count of a dense workload (smaller profiling captures)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="bwd: time the gradients (gdn_chunk_bwd, forward recompute included) "
-                         "of a dense causal workload instead of the forward")
+                         "of a causal workload (bf16 or fp32), or gdn_frame_bwd of a frame-causal "
+                         "one, instead of the forward")
     ap.add_argument("--graph-replay", type=int, default=0,
                     help="also time N back-to-back calls captured in one CUDA graph (forward pass)")
     ap.add_argument("--fused", action="store_true",
@@ -730,10 +731,14 @@ def main():
     w = resolve_segments(gdn, w, dev)
     d = device_inputs(w, dev)
     if args.pass_ == "bwd":
-        if w.dtype != "bf16" or (w.bidirectional and w.frame == 1):
-            raise SystemExit("--pass bwd takes a causal bf16 workload or a frame-causal one")
-        d["dout"] = torch.from_numpy(workloads.stored_normal(
-            rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        if w.bidirectional and w.frame == 1:
+            raise SystemExit("--pass bwd takes a causal workload (bf16 or fp32) or a frame-causal one")
+        if w.dtype == "bf16":
+            d["dout"] = torch.from_numpy(workloads.stored_normal(
+                rank, "dout", (w.B, w.T, w.H, w.V), "bf16").bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        else:  # the fp32 path's backward takes an fp32 upstream gradient
+            d["dout"] = torch.from_numpy(workloads.stored_normal(
+                rank, "dout", (w.B, w.T, w.H, w.V), "f32").values).to(dev)
         args.no_e2e = args.no_cpu_baseline = args.no_configs = True
         if w.frame > 1:  # the frame-causal rule: prep recompute, then gdn_frame_bwd
             d["dden"] = torch.from_numpy(np.random.default_rng(rank).standard_normal(
@@ -755,7 +760,8 @@ def main():
                                          direction=2 if w.bidirectional else 0, workspace=ws)
         else:
             ws = torch.empty(gdn.gdn_bwd_workspace_size(w.B, w.T, w.H, w.K, w.V, w.n_seq,
-                                                        w.cu_seqlens is not None, w.gk is not None),
+                                                        w.cu_seqlens is not None, w.gk is not None,
+                                                        fp32=w.dtype == "f32"),
                              dtype=torch.uint8, device=dev)
 
             def run(gdn, w, d, ws):  # the timed step of this pass

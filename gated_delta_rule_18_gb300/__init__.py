@@ -88,6 +88,8 @@ def lib():
                                     I, I, P, ctypes.c_size_t, P]
     L.gdn_bwd_workspace_size.restype = ctypes.c_size_t
     L.gdn_bwd_workspace_size.argtypes = [I] * 9
+    L.gdn_bwd_f32_workspace_size.restype = ctypes.c_size_t
+    L.gdn_bwd_f32_workspace_size.argtypes = [I] * 9
     L.gdn_chunk_bwd.restype = I
     L.gdn_chunk_bwd.argtypes = [P, P, TensorDesc, P, TensorDesc, P, P, P, P, P, I, P, TensorDesc,
                                 P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, P, ctypes.c_size_t, P]
@@ -316,10 +318,10 @@ def gdn_state_summary(k, v, beta, segment_len, g=None, gk=None, with_transition=
 
 
 def gdn_bwd_workspace_size(B, T, H, K, V, n_seq=None, varlen=False, perkey=False,
-                           with_den=False) -> int:
-    return int(lib().gdn_bwd_workspace_size(B, T, H, K, V, B if n_seq is None else n_seq,
-                                            int(bool(varlen)), int(bool(perkey)),
-                                            int(bool(with_den))))
+                           with_den=False, fp32=False) -> int:
+    fn = lib().gdn_bwd_f32_workspace_size if fp32 else lib().gdn_bwd_workspace_size
+    return int(fn(B, T, H, K, V, B if n_seq is None else n_seq, int(bool(varlen)), int(bool(perkey)),
+                  int(bool(with_den))))
 
 
 def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
@@ -327,7 +329,8 @@ def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
                   cu_seqlens=None, dden=None):
     """Gradients of one direction of the scan for L = sum(dout * o) +
     sum(dh_final * h_final) (see include/gdn.h). q, k (B, T, H, K), v and
-    dout (B, T, H, V) bf16; beta, g (B, T, H), h0 / dh_final (n_seq, H, K,
+    dout (B, T, H, V), all bf16 (the chunked tensor-core backward) or all
+    fp32 (the fp32 token recurrence in reverse); beta, g (B, T, H), h0 / dh_final (n_seq, H, K,
     V) fp32 (V + 1 columns with dden, the denominator's upstream gradient
     (B, H, T)); cu_seqlens: int32 (n_seq + 1) with B == 1. Returns a dict of
     fp32 tensors dq, dk, dv, dbeta, dg and, unless reverse (or
@@ -351,7 +354,7 @@ def gdn_chunk_bwd(q, k, v, beta, g, dout, h0=None, dh_final=None, reverse=False,
     if with_dh0:
         res["dh0"] = torch.empty((n_seq, H, K, V + (dden is not None)), **f32)
     need = gdn_bwd_workspace_size(B, T, H, K, V, n_seq, cu_seqlens is not None, gk is not None,
-                                  dden is not None)
+                                  dden is not None, fp32=q.dtype == torch.float32)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     st = lib().gdn_chunk_bwd(

@@ -7,6 +7,7 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_bwd_f32.cuh"
 #include "gdn_frame_bwd.cuh"
 
 namespace gdn {
@@ -28,13 +29,14 @@ using gdn::FwdParams;
 enum Kind {
     KPrepL2 = 0, KPrepRms, KTable, KIntra, KState, KFusedF32, KMerge, KFrameGram, KFrameChain,
     KFrameOut, KSegSummary, KSegCombine, KBwdDh, KBwdDq, KBwdDk, KSum, KF32Prep, KF32Serial, KFused,
-    KFrameXt, KFrameLam, KFrameTok, KPrepBwd, KMergeBwd, KNumKinds
+    KFrameXt, KFrameLam, KFrameTok, KPrepBwd, KMergeBwd, KBwdF32Scan, KBwdF32Reduce, KNumKinds
 };
 const char *kKindNames[KNumKinds] = {"prep_l2",  "prep_rms", "chunk_table", "intra_bf16",
                                      "state_tc", "fused_f32", "merge",      "frame_gram",
                                      "frame_chain", "frame_out", "seg_summary", "seg_combine",
                                      "bwd_dh", "bwd_dq", "bwd_dk", "dir_sum", "f32_prep", "f32_serial",
-                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad", "prep_bwd", "merge_bwd"};
+                                     "fused_tc", "frame_xt", "frame_lam", "frame_tokgrad", "prep_bwd", "merge_bwd",
+                                     "bwd_f32_scan", "bwd_f32_reduce"};
 
 struct Profiler {
     std::mutex mu;
@@ -602,6 +604,95 @@ size_t bwd_ws_total(int B, int T, int H, int K, int V, int n_seq, int varlen, in
     }
     return tot;
 }
+
+// The fp32 backward's workspace: the error word, the state checkpoints (one
+// per kF32BwdGroup positions, per head and 16-column range; a packed
+// sequence s starts at slot c_s / 16 + s, which never overlaps the one
+// before), and the per-range parts of dq^, dk^ (dgk) and of dbeta, dg.
+struct F32BwdWs {
+    size_t err, ck, pk, ps, total;
+    int n_range;
+    int64_t ck_groups;
+};
+bool f32_bwd_layout(int B, int T, int H, int K, int V, int n_seq, int varlen, int perkey, int den,
+                    F32BwdWs &S) {
+    if (B < 0 || T < 0 || H < 1 || K < 1 || K > gdn::kF32BwdKP || V < 1 || V > 256) return false;
+    if (varlen ? (B != 1 || n_seq < 1) : n_seq != B) return false;
+    const int Vs = V + (den ? 1 : 0);
+    S.n_range = (Vs + gdn::kF32BwdCols - 1) / gdn::kF32BwdCols;
+    S.ck_groups = varlen ? (int64_t)T / gdn::kF32BwdGroup + n_seq
+                         : (int64_t)n_seq * ((T + gdn::kF32BwdGroup - 1) / gdn::kF32BwdGroup);
+    const size_t rows = (size_t)B * T * H;
+    size_t off = 0;
+    S.err = off;
+    off = align_up(off + 2 * sizeof(int));
+    S.ck = off;
+    off = align_up(off + (size_t)H * S.n_range * S.ck_groups * gdn::kF32BwdState * sizeof(float));
+    S.pk = off;
+    off = align_up(off + (size_t)S.n_range * rows * (perkey ? 3 : 2) * K * sizeof(float));
+    S.ps = off;
+    off = align_up(off + (size_t)S.n_range * rows * 2 * sizeof(float));
+    S.total = off;
+    return true;
+}
+
+// gdn_chunk_bwd for fp32 q, k, v and dout (the token recurrence in reverse
+// time, gdn_bwd_f32.cu); the same arguments and checks as the bf16 path
+gdn_status chunk_bwd_f32(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
+                         gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
+                         const float *h0, const int32_t *cu_seqlens, int n_seq, const void *dout,
+                         gdn_tensor_desc dod, const float *dden, const float *dh_final, float *dq,
+                         float *dk, float *dv, float *dbeta, float *dg, float *dh0, int B, int T,
+                         int H, int K, int V, int chunk, int reverse, int flags, void *workspace,
+                         size_t ws_bytes, cudaStream_t stream) {
+    if (vd.dtype != GDN_F32 || (T > 0 && dod.dtype != GDN_F32)) return GDN_ERR_DTYPE;
+    if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;
+    if (reverse && (h0 || dh_final || dh0)) return GDN_ERR_UNSUPPORTED;
+    if (g && gk) return GDN_ERR_UNSUPPORTED;
+    if (chunk != gdn::kChunk) return GDN_ERR_SHAPE;
+    if (T > 0 && (!q || !k || !v || !beta || (!g && !gk))) return GDN_ERR_NULL;
+    const int den = dden != nullptr;
+    F32BwdWs S;
+    if (!f32_bwd_layout(B, T, H, K, V, n_seq, cu_seqlens != nullptr, gk != nullptr, den, S))
+        return GDN_ERR_SHAPE;
+    for (const gdn_tensor_desc *d : {&qkd, &vd, &dod})
+        if (d->stride_b < 0 || d->stride_t < 0 || d->stride_h < 0) return GDN_ERR_LAYOUT;
+    for (const void *f : {q, k, v, dout, (const void *)g, (const void *)gk, (const void *)beta,
+                          (const void *)h0, (const void *)dden, (const void *)dh_final, (const void *)dq,
+                          (const void *)dk, (const void *)dv, (const void *)dbeta, (const void *)dg,
+                          (const void *)dh0})
+        if (f && (reinterpret_cast<uintptr_t>(f) & 3)) return GDN_ERR_LAYOUT;
+    if (!ws_ok(workspace, ws_bytes, S.total)) return GDN_ERR_WORKSPACE;
+    const int Vs = V + den;
+    if (T == 0) {  // dL/dh0 = dL/dh_final
+        if (!dh0) return GDN_OK;
+        const size_t n = (size_t)n_seq * H * K * Vs * sizeof(float);
+        cudaError_t e = dh_final ? cudaMemcpyAsync(dh0, dh_final, n, cudaMemcpyDeviceToDevice, stream)
+                                 : cudaMemsetAsync(dh0, 0, n, stream);
+        return cuda_status(e);
+    }
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    gdn::F32BwdParams p{};
+    p.q = static_cast<const float *>(q), p.k = static_cast<const float *>(k);
+    p.v = static_cast<const float *>(v), p.dout = static_cast<const float *>(dout);
+    p.qk_sb = qkd.stride_b, p.qk_st = qkd.stride_t, p.qk_sh = qkd.stride_h;
+    p.v_sb = vd.stride_b, p.v_st = vd.stride_t, p.v_sh = vd.stride_h;
+    p.do_sb = dod.stride_b, p.do_st = dod.stride_t, p.do_sh = dod.stride_h;
+    p.beta = beta, p.g = g, p.gk = gk, p.h0 = h0, p.dh_final = dh_final, p.dden = dden;
+    p.cu_seqlens = cu_seqlens;
+    p.dv = dv, p.dh0 = dh0, p.dq = dq, p.dk = dk, p.dbeta = dbeta, p.dg = dg;
+    p.err = reinterpret_cast<int *>(ws + S.err);
+    p.ckpt = reinterpret_cast<float *>(ws + S.ck);
+    p.part_k = reinterpret_cast<float *>(ws + S.pk);
+    p.part_s = reinterpret_cast<float *>(ws + S.ps);
+    p.B = B, p.T = T, p.H = H, p.K = K, p.V = V, p.Vs = Vs, p.n_seq = n_seq, p.n_range = S.n_range;
+    p.reverse = reverse, p.l2norm = (flags & GDN_QK_L2NORM) != 0, p.ck_groups = S.ck_groups;
+    cudaError_t e = cudaMemsetAsync(p.err, 0, sizeof(int), stream);
+    if (e == cudaSuccess) e = launch(KBwdF32Scan, stream, [&] { return gdn::launch_bwd_f32_scan(p, stream); });
+    if (e == cudaSuccess)
+        e = launch(KBwdF32Reduce, stream, [&] { return gdn::launch_bwd_f32_reduce(p, stream); });
+    return cuda_status(e);
+}
 }  // namespace
 
 extern "C" {
@@ -612,6 +703,13 @@ size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq, int 
     return bwd_ws_total(B, T, H, K, V, n_seq, varlen, perkey != 0, with_den != 0);
 }
 
+size_t gdn_bwd_f32_workspace_size(int B, int T, int H, int K, int V, int n_seq, int varlen,
+                                  int perkey, int with_den) {
+    F32BwdWs S;
+    if (!f32_bwd_layout(B, T, H, K, V, n_seq, varlen != 0, perkey != 0, with_den != 0, S)) return 0;
+    return S.total;
+}
+
 gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, const void *v,
                          gdn_tensor_desc vd, const float *g, const float *gk, const float *beta,
                          const float *h0, const int32_t *cu_seqlens, int n_seq, const void *dout,
@@ -620,6 +718,10 @@ gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd, cons
                          int H, int K, int V, int chunk, int reverse, int flags, void *workspace,
                          size_t ws_bytes, cudaStream_t stream) {
     if (T > 0 && (!dout || !dq || !dk || !dv || !dbeta || !dg)) return GDN_ERR_NULL;
+    if (qkd.dtype == GDN_F32)
+        return chunk_bwd_f32(q, k, qkd, v, vd, g, gk, beta, h0, cu_seqlens, n_seq, dout, dod, dden,
+                             dh_final, dq, dk, dv, dbeta, dg, dh0, B, T, H, K, V, chunk, reverse, flags,
+                             workspace, ws_bytes, stream);
     if (qkd.dtype != GDN_BF16 || vd.dtype != GDN_BF16 || (T > 0 && dod.dtype != GDN_BF16))
         return GDN_ERR_DTYPE;
     if ((flags & ~GDN_QK_L2NORM) != 0) return GDN_ERR_UNSUPPORTED;

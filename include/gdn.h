@@ -286,7 +286,7 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
 
 /*
  * gdn_bwd_workspace_size / gdn_chunk_bwd -- gradients of one direction of
- * the chunked scan (gdn_chunk_fwd's bf16 path) for the loss
+ * the chunked scan (gdn_chunk_fwd's bf16 path; fp32 below) for the loss
  * L = sum(dout . o) + sum(dh_final . h_final): the reverse-time chunked state
  * gradient of the hyper-parallel coverage_diff page
  * (`chunk_gated_delta_rule_bwd_dhu`, with its varlen offsets) and the
@@ -317,9 +317,29 @@ gdn_status gdn_state_summary(const void *k, gdn_tensor_desc kd, const void *v,
  *   dh0 -> GDN_ERR_UNSUPPORTED.
  *   workspace: >= gdn_bwd_workspace_size(B, T, H, K, V, n_seq, varlen,
  *   perkey, with_den) bytes (0 for an unsupported shape), 256-byte aligned.
+ *
+ * fp32 (qkd, vd and dod GDN_F32, the dtype of gdn_chunk_fwd's fp32 path):
+ * the same arguments, loss and outputs, computed by the token recurrence in
+ * reverse time in IEEE fp32 on CUDA cores. Per position, with P the decayed
+ * state before it and r = v - P^T k the correction: dh += q do^T,
+ * dq = h' do, dv = beta dh^T k, dbeta = r . (dh^T k), dk = beta dh r -
+ * P dv, dg = sum((dh - k dv^T) . P), and the state gradient carries back as
+ * e^{g} (dh - k dv^T) (the SANA `fused_cam_gdn.py` page's
+ * `_cam_scan_bwd_kernel` rules). The state is checkpointed every 16
+ * positions and each group of 16 recomputed before it is walked back. Any
+ * K <= 128 and V <= 256; any non-negative strides; pointers 4-byte aligned;
+ * gates floored at -30 as in the fp32 forward (g and gk: 0 gradient there).
+ * A malformed cu_seqlens leaves that sequence's outputs unwritten and sets
+ * GDN_DEVERR_SEQLENS in the word gdn_last_device_error() reads.
+ *   workspace: >= gdn_bwd_f32_workspace_size(B, T, H, K, V, n_seq, varlen,
+ *   perkey, with_den) bytes (0 for an unsupported shape), 256-byte aligned:
+ *   checkpoints of (T / 16 + n_seq) x 2,048 floats per head and 16 state
+ *   columns, and per-16-column partial sums of dq, dk (dgk), dbeta and dg.
  */
 size_t gdn_bwd_workspace_size(int B, int T, int H, int K, int V, int n_seq,
                               int varlen, int perkey, int with_den);
+size_t gdn_bwd_f32_workspace_size(int B, int T, int H, int K, int V, int n_seq,
+                                  int varlen, int perkey, int with_den);
 gdn_status gdn_chunk_bwd(const void *q, const void *k, gdn_tensor_desc qkd,
                          const void *v, gdn_tensor_desc vd, const float *g,
                          const float *gk, const float *beta, const float *h0,

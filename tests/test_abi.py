@@ -198,14 +198,30 @@ def test_seg_fwd_and_summary_reject_on_host(L):
 def test_chunk_bwd_rejects_on_host(L):
     d16, d32 = desc(gdn.BF16, 1, 128, 2, 64), desc(gdn.F32, 1, 128, 2, 64)
 
-    def bw(q=P(0), qkd=d16, dod=d16, gk=None, h0=None, dhf=None, dh0=P(16), dq=P(10), V=64, T=128,
-           reverse=0, flags=0, wsb=1 << 30):
-        return L.gdn_chunk_bwd(q, P(1), qkd, P(2), d16, P(3), gk, P(4), h0, None, 1, P(5), dod, None,
-                               dhf, dq, P(11), P(12), P(13), P(14), dh0, 1, T, 2, 64, V, 64, reverse,
+    def bw(q=P(0), qkd=d16, vd=d16, dod=d16, gk=None, h0=None, dhf=None, dh0=P(16), dq=P(10), V=64,
+           T=128, K=64, reverse=0, flags=0, wsb=1 << 30):
+        return L.gdn_chunk_bwd(q, P(1), qkd, P(2), vd, P(3), gk, P(4), h0, None, 1, P(5), dod, None,
+                               dhf, dq, P(11), P(12), P(13), P(14), dh0, 1, T, 2, K, V, 64, reverse,
                                flags, P(9), wsb, None)
     assert bw(dq=None) == NULL
-    assert bw(qkd=d32) == DTYPE                # bf16 inputs only
+    assert bw(qkd=d32) == DTYPE                # fp32 q / k with bf16 v
     assert bw(dod=d32) == DTYPE
+    # the fp32 path (fp32 q, k, v and dout): its own shape and layout checks
+    f32 = dict(qkd=d32, vd=d32, dod=d32)
+    assert bw(vd=d16, dod=d32, qkd=d32) == DTYPE
+    assert bw(dod=d16, qkd=d32, vd=d32) == DTYPE
+    assert bw(K=129, **f32) == SHAPE           # K <= 128
+    assert bw(V=264, **f32) == SHAPE
+    assert bw(gk=P(7), **f32) == UNSUP
+    assert bw(reverse=1, **f32) == UNSUP
+    assert bw(dq=ctypes.c_void_p(A + 2), **f32) == LAYOUT   # 4-byte aligned fp32
+    assert bw(wsb=1024, **f32) == WS
+    assert bw(T=0, dh0=None, **f32) == OK      # nothing to do
+    assert gdn.gdn_bwd_workspace_size(1, 256, 2, 64, 64, fp32=True) > 0
+    assert gdn.gdn_bwd_workspace_size(1, 256, 2, 129, 64, fp32=True) == 0
+    assert gdn.gdn_bwd_workspace_size(2, 256, 2, 64, 64, 3, True, fp32=True) == 0   # packed: B == 1
+    # any V: ragged 16-column ranges, the ones column in the last
+    assert gdn.gdn_bwd_workspace_size(1, 100, 2, 48, 40, with_den=True, fp32=True) > 0
     assert bw(V=264) == SHAPE                  # V <= 256
     assert bw(V=60) == SHAPE                   # a multiple of 8
     assert bw(gk=P(7)) == UNSUP                # g and gk both given

@@ -1045,6 +1045,82 @@ def test_backward_with_den(name):
     assert all(e <= 1.5e-2 for e in errs.values()), (name, errs)
 
 
+# ---- the fp32 backward (the token recurrence in reverse, fp32 on CUDA
+# cores) against the fp64 oracle at the fp32 path's bound
+
+F32_BWD = {
+    # the 256-token fp32 problem (B=1, H=2, K=V=64) with h0 and dh_final
+    "t256_k64_h0": dict(B=1, T=256, H=2, K=64, V=64, h0_std=0.5),
+    # 64 independent problems of that shape
+    "b64_t256_k64": dict(B=64, T=256, H=2, K=64, V=64, h0_std=0.5),
+    "reverse": dict(B=2, T=100, H=2, K=64, V=48, reverse=True),
+    "no_l2": dict(B=1, T=90, H=2, K=64, V=64, h0_std=0.5, l2=False),
+    # nine 16-column ranges (the last one ragged), K at its largest
+    "k128_v136": dict(B=1, T=77, H=2, K=128, V=136, h0_std=0.5),
+    # per-key gates over packed sequences (one token, an empty one, ragged groups)
+    "gk_varlen_k48_v40": dict(B=1, T=68, H=3, K=48, V=40, h0_std=0.5, g_mu=None, gk_mu=1.0,
+                              lengths=[1, 17, 0, 50]),
+    # the denominator's ones column (its own range when V is a multiple of 16)
+    "den_h0": dict(B=2, T=70, H=2, K=64, V=64, h0_std=0.5, den=True),
+    "den_reverse_gk": dict(B=1, T=90, H=2, K=32, V=24, g_mu=None, gk_mu=2.0, reverse=True, den=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(F32_BWD))
+def test_small_backward_fp32(name):
+    import gated_delta_rule_18_gb300 as gdn
+    from oracle import backward
+    spec = dict(F32_BWD[name])
+    reverse, den, l2 = spec.pop("reverse", False), spec.pop("den", False), spec.pop("l2", True)
+    h0_std = spec.pop("h0_std", None)
+    w = workloads.make(**spec, dtype="f32", seed=111, name="bwd_f32_" + name)
+    if not l2:  # unnormalised rows of norm ~1 (|k|^2 ~ K would make the recurrence blow up)
+        w = dataclasses.replace(w, q=workloads.Stored("f32", (w.q.values / 8).astype(np.float32)),
+                                k=workloads.Stored("f32", (w.k.values / 8).astype(np.float32)))
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    Vs = V + den
+    rng = np.random.default_rng(112)
+    dout = workloads.stored_normal(113, "dout", (B, T, H, V), "f32")
+    dden = rng.standard_normal((B, H, T)).astype(np.float32) if den else None
+    h0 = None if reverse or h0_std is None else (rng.standard_normal((w.n_seq, H, K, Vs)) * h0_std).astype(np.float32)
+    dhf = None if reverse else rng.standard_normal((w.n_seq, H, K, Vs)).astype(np.float32)
+    va, da = w.v.values, dout.values
+    if den:
+        va = np.concatenate([va, np.ones((B, T, H, 1))], axis=-1)
+        da = np.concatenate([da, dden.transpose(0, 2, 1)[..., None].astype(np.float64)], axis=-1)
+    ref = backward.scan_grad(w.q.values, w.k.values, va, w.beta, w.g, da, h0=h0, dh_final=dhf,
+                             reverse=reverse, l2norm=l2, cu_seqlens=w.cu_seqlens, gk=w.gk)
+    ref["dv"] = ref["dv"][..., :V]
+    got = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(dout), h0=f32_dev(h0), dh_final=f32_dev(dhf), reverse=reverse,
+                            qk_l2norm=l2, cu_seqlens=i32_dev(w.cu_seqlens), gk=f32_dev(w.gk),
+                            dden=f32_dev(dden))
+    torch().cuda.synchronize()
+    errs = {n: rel_err(got[n].double().cpu().numpy(), ref[n]) for n in got}
+    assert all(e <= TOL["f32"] for e in errs.values()), (name, errs)
+
+
+def test_backward_fp32_reproducible_and_malformed_seqlens():
+    """two runs agree bit for bit (the column ranges are summed in a fixed
+    order); a cu_seqlens that does not end at T is reported in the error
+    word, with the call itself returning GDN_OK"""
+    import gated_delta_rule_18_gb300 as gdn
+    w = workloads.make(1, 120, 2, 64, 40, dtype="f32", seed=114, g_mu=None, gk_mu=2.0,
+                       lengths=[50, 70])
+    dout = workloads.stored_normal(115, "dout", (1, 120, 2, 40), "f32")
+    args = (to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), None, to_dev(dout))
+    a = gdn.gdn_chunk_bwd(*args, qk_l2norm=True, cu_seqlens=i32_dev(w.cu_seqlens), gk=f32_dev(w.gk))
+    b = gdn.gdn_chunk_bwd(*args, qk_l2norm=True, cu_seqlens=i32_dev(w.cu_seqlens), gk=f32_dev(w.gk))
+    torch().cuda.synchronize()
+    for n in a:
+        assert torch().equal(a[n], b[n]), n
+    bad = i32_dev(np.array([0, 50, 119], dtype=np.int32))
+    need = gdn.gdn_bwd_workspace_size(1, 120, 2, 64, 40, 2, True, True, fp32=True)
+    ws = torch().zeros(need, dtype=torch().uint8, device=dev())
+    gdn.gdn_chunk_bwd(*args, qk_l2norm=True, cu_seqlens=bad, gk=f32_dev(w.gk), workspace=ws)
+    assert gdn.gdn_last_device_error(ws) & 1
+
+
 # ---- the torch.autograd wrappers, against the oracles composed the same way
 
 @pytest.mark.parametrize("gate_kind", ["scalar", "perkey"])
