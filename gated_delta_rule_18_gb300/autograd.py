@@ -6,8 +6,9 @@ gdn_merge_bwd, gdn_prep_bwd).
 Nothing here computes on its own: the wrappers marshal tensors and sum the
 two directions' gradients.
 
-The gradient kernels take the upstream gradient of the output in bf16 (the
-inputs' precision); an fp32 upstream gradient is rounded to bf16 first.
+The gradient kernels take the upstream gradient of the output in the
+inputs' precision: for bf16 inputs an fp32 upstream gradient is rounded to
+bf16 first; fp32 inputs (the fp32 path) keep it in fp32.
 """
 from __future__ import annotations
 
@@ -38,7 +39,8 @@ class _ChunkGDR(torch.autograd.Function):
     def backward(ctx, do, dhf):
         q, k, v, beta, g, gk, h0, cu_seqlens = ctx.saved_tensors
         want_h0 = h0 is not None and ctx.needs_input_grad[6]
-        res = gdn_chunk_bwd(q, k, v, beta, g, _bf16(do), h0=h0,
+        do = do.float().contiguous() if q.dtype == torch.float32 else _bf16(do)
+        res = gdn_chunk_bwd(q, k, v, beta, g, do, h0=h0,
                             dh_final=None if dhf is None else dhf.float().contiguous(),
                             reverse=ctx.reverse, qk_l2norm=ctx.qk_l2norm, with_dh0=want_h0,
                             gk=gk, cu_seqlens=cu_seqlens)
@@ -53,7 +55,8 @@ def chunk_gated_delta_rule(q, k, v, beta, g=None, gk=None, initial_state=None,
                            use_qk_l2norm=True):
     """One direction of the chunked gated delta rule, differentiable in q, k,
     v, beta, g (or the per-key gk) and initial_state. Shapes and meanings as
-    gdn_chunk_fwd: q, k (B, T, H, K), v (B, T, H, V) bf16; beta, g (B, T, H)
+    gdn_chunk_fwd: q, k (B, T, H, K), v (B, T, H, V) bf16 (or all fp32: the
+    fp32 path and its backward); beta, g (B, T, H)
     fp32; gk (B, T, H, K) fp32; initial_state (n_seq, H, K, V) fp32;
     cu_seqlens int32 (n_seq + 1) with B == 1. use_qk_l2norm normalises q and
     k per (token, head) inside the kernels. Returns (o, final_state or None)."""

@@ -1148,6 +1148,26 @@ def test_autograd_chunk_gated_delta_rule(gate_kind):
         assert rel_err(gr.double().cpu().numpy(), ref[name]) <= 1.5e-2, name
 
 
+def test_autograd_chunk_gated_delta_rule_fp32():
+    """fp32 inputs: the fp32 forward and the fp32 backward, at the fp32 bound"""
+    from gated_delta_rule_18_gb300.autograd import chunk_gated_delta_rule
+    from oracle import backward
+    t = torch()
+    w = workloads.make(1, 256, 2, 64, 64, "f32", seed=105, h0_std=0.5)
+    q, k, v = (to_dev(x).requires_grad_() for x in (w.q, w.k, w.v))
+    beta, g, h0 = (f32_dev(x).requires_grad_() for x in (w.beta, w.g, w.h0))
+    o, hf = chunk_gated_delta_rule(q, k, v, beta, g=g, initial_state=h0, output_final_state=True)
+    rng = np.random.default_rng(106)
+    do = rng.standard_normal(tuple(o.shape)).astype(np.float32)
+    dhf = rng.standard_normal(tuple(hf.shape)).astype(np.float32)
+    loss = (o * f32_dev(do)).sum() + (hf * f32_dev(dhf)).sum()
+    grads = t.autograd.grad(loss, (q, k, v, beta, g, h0))
+    ref = backward.scan_grad(w.q.values, w.k.values, w.v.values, w.beta, w.g, do, h0=w.h0,
+                             dh_final=dhf, l2norm=True)
+    for name, gr in zip(("dq", "dk", "dv", "dbeta", "dg", "dh0"), grads):
+        assert rel_err(gr.double().cpu().numpy(), ref[name]) <= TOL["f32"], name
+
+
 def test_autograd_bidirectional_merge():
     """the bidirectional form with the chunk-causal reverse gates, den and a
     gate: the merged output's gradients. q and k are non-negative, as after
