@@ -1,55 +1,75 @@
-// gdn_bwd_dh.cu -- the serial part of the backward: the state gradient walked
-// back over the chunks (hyper-parallel coverage_diff page,
+// gdn_bwd_dh.cu -- the serial part of the backward on the fifth-generation
+// tensor cores (tcgen05, accumulators in TMEM): the state gradient walked back
+// over the chunks (hyper-parallel coverage_diff page,
 // `chunk_gated_delta_rule_bwd_dhu`: dh accumulates q do^T and - w dv each
 // chunk and is decayed by the chunk's e^{g_last}; dv gains k dh).
 //
 // The forward per chunk (state h entering it, G the in-chunk cumulative gate):
-//   v_new = u - w h,   o = qg h + P v_new,   h' = e^{G_C} h + kg^T v_new
-// with qg = e^{G} q, kg = e^{G_C - G} k. For the loss gradient dh' at the
-// chunk's end and do of its outputs, reverse mode gives
-//   dv_new = P^T do + kg dh'                   (the chunk's dL/dv_new)
-//   dh     = e^{G_C} dh' + qg^T do - w^T dv_new (dL/dh, handed to chunk c-1)
-// One CTA (8 warps) per (sequence, head, 64-column value tile) walks the
-// chunks last to first; dh (128 keys x 64 columns, fp32) lives in the warps'
-// mma accumulators, warp w holding keys 16w .. 16w+15. The forward's P, qg,
-// kg and w images and decay arrive one chunk ahead by one bulk async copy
-// each onto an mbarrier and are read by ldmatrix in their stored (core
-// block) layout; the do tile comes by cp.async. Per chunk the kernel stores
-// dh' and dv_new (bf16, 16-byte stores from shared memory) for the
-// chunk-parallel gradient kernels. Every wait is bounded (about 0.5 s); a
-// wait that gives up marks the error word and the CTA leaves after its
-// copies in flight have landed (again bounded).
+//   v_new = u - w h,   o = qg h + P v_new,   h' = e^{G_C} h + kg^T v_new.
+// For the loss gradient dh' at the chunk's end and do of its outputs:
+//   dv_new = P^T do + kg dh'                     M = 64 tokens, N = 64 columns
+//   dh     = e^{G_C} dh' + qg^T do - w^T dv_new   M = 128 keys
+// The forward's per-chunk images serve as the transposed operands: P^T, qg^T
+// and w^T are the P, qg and w images read MN-major, kg is the kg^T image
+// read K-major.
+//
+// One CTA per (sequence, head, 64-column tile) walks the chunks last to
+// first, warp-specialised (9 warps):
+//   warps 0-3  the recurrence: thread d keeps row d of dh (64 fp32) in
+//              registers, writes dh' as the bf16 B operand of kg dh' (and its
+//              snapshot) and applies dh = dec . dh' + [qg^T do - w^T dv_new]
+//              read from TMEM; while they wait for those products they copy
+//              the do tiles (cp.async) two chunks ahead and store the
+//              previous chunk's dv_new snapshot from TMEM.
+//   warps 4-7  dv_new: read from TMEM (M = 64 layout: rows 16q .. 16q+15 at
+//              lanes 32q ..), written negated as the B operand of w^T dv_new.
+//   warp 8     lane 0 issues every MMA and the images' bulk copies.
+// Per chunk the do-only products (P^T do, qg^T do) are issued as soon as the
+// chunk's operands have landed, ahead of dh'; what is left on the chain is
+// dh' -> 8 MMAs -> dv_new -> 4 MMAs -> dh. Operands arrive in three slots,
+// two chunks ahead; the TMEM accumulators are double buffered.
+//
+// Every wait is bounded: a wait that gives up raises a shared abort flag that
+// makes every role leave its loop; the kernel records GDN_DEVERR_TIMEOUT,
+// drains what it issued (again bounded), frees its tensor memory and returns.
 #include "gdn_mma.cuh"
+#include "gdn_tc.cuh"
 
 namespace gdn {
 namespace {
 
 using bf16 = __nv_bfloat16;
 
-constexpr int kThreads = 256;
-constexpr int kL6 = 64 + 8;  // row stride of a 64-column tile
-constexpr uint32_t kStageBytes = kImgP + 3 * kImgW + kDecB;
+constexpr int kThreadsTc = 288;  // 9 warps
+constexpr int kNS = 3;           // operand slots
+// one slot: qg | w | kg^T | P | do (64 x 64, MN-major B) | dec
+constexpr uint32_t kOffQg = 0, kOffW = kImgW, kOffKg = 2 * kImgW, kOffP = 3 * kImgW;
+constexpr uint32_t kOffDo = kOffP + kImgP, kOffDec = kOffDo + 64 * 64 * 2;
+constexpr uint32_t kSlot = 65 * 1024;
+static_assert(kOffDec + kDecB <= kSlot, "slot layout");
+constexpr uint32_t kOffDh = kNS * kSlot;               // dh' (128 keys x 64 columns, MN-major B)
+constexpr uint32_t kOffDvn = kOffDh + kKP * 64 * 2;     // -dv_new (64 tokens x 64 columns, MN-major B)
+constexpr uint32_t kBytesTc = kOffDvn + 64 * 64 * 2;
+static_assert(kBytesTc <= 226 * 1024, "shared memory per CTA");
+// TMEM columns: dv_new of even / odd chunks at 0 / 64 (M = 64 layout), dh's
+// products at 128 / 192 (lane = key)
+constexpr uint32_t kTmemCols = 256, kColDv = 0, kColDh = 128;
 
-struct DhStage {
-    unsigned char p[kImgP];   // P image
-    unsigned char qg[kImgW];  // qg image
-    unsigned char kd[kImgW];  // kg^T image
-    unsigned char w[kImgW];   // w image
-    float dec[kKP];
-    bf16 dout[kChunk * kL6];  // do [i][col]
-};
-struct DhSmem {
-    DhStage st[2];
-    bf16 dh[kKP * kL6];       // dh' [d][col] (B operand)
-    bf16 dvn[kChunk * kL6];   // -dv_new [i][col] (B operand)
-};
+__device__ __forceinline__ uint4 pack8(const float *f) {
+    uint4 u;
+    u.x = pack_bf16(f[0], f[1]);
+    u.y = pack_bf16(f[2], f[3]);
+    u.z = pack_bf16(f[4], f[5]);
+    u.w = pack_bf16(f[6], f[7]);
+    return u;
+}
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) {
-    extern __shared__ __align__(128) unsigned char smraw[];
-    DhSmem &sm = *reinterpret_cast<DhSmem *>(smraw);
-    __shared__ __align__(8) uint64_t bars[2];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g8 = lane >> 2, t4 = lane & 3;
+__global__ void __launch_bounds__(kThreadsTc, 1) bwd_dh_kernel(const BwdParams p) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ __align__(8) uint64_t bar_full[kNS], bar_dvd[2], bar_dhd[2], bar_dhr, bar_dvr;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x / p.H, hh = blockIdx.x % p.H;
     const int v0 = blockIdx.y * 64;
     const int K = p.K, V = p.V;
@@ -60,197 +80,258 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dh_kernel(const BwdParams p) 
     const int T = p.cu_seqlens ? p.cu_seqlens[s + 1] - tstart : p.T;
     const int nts = (T + kChunk - 1) / kChunk;
     const int c0 = p.cu_seqlens ? p.seq_chunk0[s] : s * nts;
+    const int vcols = p.den_col >= 0 ? p.den_col : V;  // columns from do (the rest: the ones column)
     const bf16 *dout = (const bf16 *)p.dout;
-    const uint32_t bar[2] = {smem_u32(&bars[0]), smem_u32(&bars[1])};
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t b_full = smem_u32(&bar_full[0]), b_dvd = smem_u32(&bar_dvd[0]), b_dhd = smem_u32(&bar_dhd[0]);
+    const uint32_t b_dhr = smem_u32(&bar_dhr), b_dvr = smem_u32(&bar_dvr);
+    volatile int *abort = &abort_s;
+
+    if (warp == 0) tc_alloc(&tmem_base_s, kTmemCols);
     if (tid == 0) {
-        mbar_init(bar[0], 1);
-        mbar_init(bar[1], 1);
+        abort_s = 0;
+        // a slot fills by the issuer's bulk copies (one arrival with their
+        // bytes) and the do tile's 128 copying threads
+        for (int x = 0; x < kNS; ++x) mbar_init(b_full + 8 * x, 129);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(b_dvd + 8 * x, 1);
+            mbar_init(b_dhd + 8 * x, 1);
+        }
+        mbar_init(b_dhr, 128);
+        mbar_init(b_dvr, 128);
         fence_mbar_init();
     }
+    tc_fence_before();
     __syncthreads();
-
-    // step `it` handles chunk nts - 1 - it in stage it & 1
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // step `it` handles chunk nts - 1 - it, in slot it % kNS
     auto gch_of = [&](int it) { return (int64_t)hh * p.max_chunks + c0 + (nts - 1 - it); };
-    auto stage = [&](int it) {
-        DhStage &S = sm.st[it & 1];
-        const int c = nts - 1 - it;
-        const int64_t gch = gch_of(it);
-        if (tid == 0) {
-            fence_async_smem();  // earlier generic reads of this stage come first
-            arrive_expect_tx(bar[it & 1], kStageBytes);
-            bulk_g2s(smem_u32(S.p), p.p_img + gch * kImgP, kImgP, bar[it & 1]);
-            bulk_g2s(smem_u32(S.qg), p.qg_img + gch * kImgW, kImgW, bar[it & 1]);
-            bulk_g2s(smem_u32(S.kd), p.kg_img + gch * kImgW, kImgW, bar[it & 1]);
-            bulk_g2s(smem_u32(S.w), p.w_img + gch * kImgW, kImgW, bar[it & 1]);
-            bulk_g2s(smem_u32(S.dec), p.dec + gch * kKP, kDecB, bar[it & 1]);
+    // (the do tiles are copied by the recurrence warps, in the time they
+    // wait for dh's products)
+    // chunk it's do tile into its slot: 64 tokens x 8 pieces of 16 bytes,
+    // MN-major B ((col/8)*1024 + i*16); one cp.async group
+    auto load_do = [&](int it) {
+        const int c = nts - 1 - it, pos0 = c * kChunk, Lc = min(kChunk, T - pos0);
+        unsigned char *dst = sm + (it % kNS) * kSlot + kOffDo;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+        const int e = (tid & 127) + 128 * j, i = e >> 3, pc = e & 7, col = 8 * pc;
+        unsigned char *dp = dst + pc * 1024 + i * 16;
+        if (p.den_col == v0 + col) {  // the ones column's piece: dden, then zeros
+            float dd = 0.f;
+            if (i < Lc)
+            dd = p.dden[((int64_t)b * p.H + hh) * p.T + tstart + q_token(p.reverse, T, pos0 + i)];
+            *reinterpret_cast<uint4 *>(dp) = make_uint4(pack_bf16(dd, 0.f), 0u, 0u, 0u);
+            continue;
         }
-        const int pos0 = c * kChunk, Lc = min(kChunk, T - pos0);
-        for (int e = tid; e < kChunk * 8; e += kThreads) {  // do: 64 rows x 8 pieces
-            const int i = e >> 3, c8 = (e & 7) * 8, col = v0 + c8;
-            const bool in = i < Lc && col < (p.den_col >= 0 ? p.den_col : V);
-            const int tq = in ? q_token(p.reverse, T, pos0 + i) : 0;
-            const bf16 *src = in ? dout + b * p.do_sb + (int64_t)(tstart + tq) * p.do_st + hh * p.do_sh + col : dout;
-            cp_async16(S.dout + i * kL6 + c8, src, in ? 16 : 0);
+        const bool in = i < Lc && v0 + col < vcols;
+        const bf16 *src = in ? dout + b * p.do_sb + (int64_t)(tstart + q_token(p.reverse, T, pos0 + i)) * p.do_st +
+                       hh * p.do_sh + v0 + col
+                     : dout;
+        cp_async16(dp, src, in ? 16 : 0);
         }
         cp_async_commit();
     };
+    // the do tile of chunk j has landed: make it visible to the tensor
+    // cores and count it on the slot's barrier (newer: groups issued after)
+    auto publish = [&](int j, bool newer) {
+        if (newer) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        fence_async_smem();
+        arrive(b_full + 8 * (j % kNS));
+    };
 
-    // dh' at the sequence end: dh_final (or 0); warp w holds keys 16w..16w+15
-    float acc[8][4];
+    if (warp < 4) {
+        // ------------------------------------------------ recurrence warps
+        const int d = tid;
+        float h[64];
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+        for (int c = 0; c < 64; ++c)
+            h[c] = (p.dh_final && d < K && v0 + c < V)
+                       ? p.dh_final[(((int64_t)s * p.H + hh) * K + d) * p.vfull + v0 + c]
+                       : 0.f;
+        // chunk j's dv_new (TMEM, M = 64 layout: token row 16 q + l at lane
+        // 32 q + l, l < 16) to its snapshot, by this warp's lanes 0-15; here
+        // rather than in the dv_new warps, whose proxy fence would otherwise
+        // wait for these global stores
+        auto dvn_snapshot = [&](int j) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int r = 16 * warp + g8 + 8 * (e >> 1), col = v0 + 8 * n + 2 * t4 + (e & 1);
-            acc[n][e] = (p.dh_final && r < K && col < V)
-                            ? p.dh_final[(((int64_t)s * p.H + hh) * K + r) * p.vfull + col]
-                            : 0.f;
-        }
-    if (nts > 0) stage(0);
-    bool ok = true;
-    int it = 0;
-    for (; it < nts; ++it) {
-        DhStage &S = sm.st[it & 1];
-        if (it + 1 < nts) {
-            stage(it + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        ok = wait_bar(bar[it & 1], (it >> 1) & 1, nullptr);
-        // the denominator's column of the do tile: dden (the barrier below
-        // precedes its readers)
-        if (p.den_col >= v0 && p.den_col < v0 + 64 && tid < kChunk) {
-            const int c = nts - 1 - it, pos0 = c * kChunk, Lc = min(kChunk, T - pos0);
-            float dd = 0.f;
-            if (tid < Lc) dd = p.dden[((int64_t)b * p.H + hh) * p.T + tstart + q_token(p.reverse, T, pos0 + tid)];
-            S.dout[tid * kL6 + (p.den_col - v0)] = __float2bfloat16_rn(dd);
-        }
-        // dh' to the B-operand tile
+            for (int half = 0; half < 2; ++half) {
+                float v[32];
+                tc_ld32(tmem + lane_base + kColDv + 64 * (j & 1) + 32 * half, v);
+                if (lane < 16) {
+                    const int i = 16 * warp + lane;
+                    bf16 *vs = p.dvn_snap + (gch_of(j) * kChunk + i) * p.snap_ld + v0 + 32 * half;
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-                *reinterpret_cast<uint32_t *>(sm.dh + (16 * warp + g8 + 8 * hf) * kL6 + 8 * n + 2 * t4) =
-                    pack_bf16(acc[n][2 * hf], acc[n][2 * hf + 1]);
-        if (__syncthreads_or(!ok)) break;
-        const int64_t gch = gch_of(it);
-        {  // its snapshot, 16-byte pieces
-            bf16 *snap = p.dh_snap + gch * K * p.snap_ld + v0;
-            for (int e = tid; e < kKP * 8; e += kThreads) {
-                const int r = e >> 3, c8 = (e & 7) * 8;
-                if (r < K && v0 + c8 < V)
-                    *reinterpret_cast<uint4 *>(snap + (int64_t)r * p.snap_ld + c8) =
-                        *reinterpret_cast<const uint4 *>(sm.dh + r * kL6 + c8);
-            }
-        }
-        // dv_new = P^T do + kg dh'  (64 tokens x 64 columns; warp: 16 rows x 32 columns)
-        {
-            float a2[4][4];
-            acc_zero(a2);
-            const int m0 = 16 * (warp & 3), n0 = 32 * (warp >> 2);
-            const Tile tdo{S.dout, kL6}, tdh{sm.dh, kL6};
-#pragma unroll
-            for (int k0 = 0; k0 < kChunk; k0 += 16) {  // P^T: stored [i][j], read transposed
-                uint32_t a[4];
-                ldsm_x4_t(a, S.p + img_p_off(k0 + (lane & 7) + ((lane >> 4) << 3), m0 + ((lane >> 3) & 1) * 8));
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t b[4];
-                    frag_b2(b, tdo, true, n0 + 16 * np, k0, lane);
-                    mma_bf16(a2[2 * np], a, b[0], b[1]);
-                    mma_bf16(a2[2 * np + 1], a, b[2], b[3]);
+                    for (int x = 0; x < 4; ++x)
+                        if (v0 + 32 * half + 8 * x < V) *reinterpret_cast<uint4 *>(vs + 8 * x) = pack8(&v[8 * x]);
                 }
             }
+            tc_fence_before();
+        };
+        if (nts > 0) load_do(0);
+        if (nts > 1) load_do(1);
+        if (nts > 0) publish(0, nts > 1);
+        bool ok = true;
+        for (int it = 0; it < nts && ok; ++it) {
+            const int sl = it % kNS;
+            // the slot's decay (the slot is refilled only after this chunk's
+            // products, which wait for the arrival below)
+            ok = warp_all(wait_bar(b_full + 8 * sl, (it / kNS) & 1, abort));
+            if (!ok) break;
+            const float dec = reinterpret_cast<const float *>(sm + sl * kSlot + kOffDec)[d];
+            // dh' -> the MN-major B operand ((col/8)*2048 + d*16; its last
+            // reader, chunk it-1's kg dh', finished before that chunk's dh),
+            // handed over before its snapshot is stored (a proxy fence after
+            // the global stores would wait for them)
 #pragma unroll
-            for (int k0 = 0; k0 < kKP; k0 += 16) {  // kg: [j][d] pieces of the kg^T image
-                uint32_t a[4];
-                ldsm_x4(a, S.kd + img_kt_off(m0 + (lane & 15), k0 + (lane >> 4) * 8));
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(sm + kOffDh + j * 2048 + d * 16) = pack8(&h[8 * j]);
+            fence_async_smem();
+            arrive(b_dhr);
+            // chunk it-1's dv_new snapshot from its TMEM buffer (chunk it+1's
+            // products overwrite that buffer only after the publish below)
+            if (it >= 1) dvn_snapshot(it - 1);
+            // chunk it+2's do tile (its slot was chunk it-1's, whose products
+            // are done), then chunk it+1's, copied a chunk ago, is published
+            if (it + 2 < nts) load_do(it + 2);
+            if (it + 1 < nts) publish(it + 1, it + 2 < nts);
+            if (d < K) {
+                bf16 *hs = p.dh_snap + (gch_of(it) * K + d) * p.snap_ld + v0;
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t b[4];
-                    frag_b2(b, tdh, true, n0 + 16 * np, k0, lane);
-                    mma_bf16(a2[2 * np], a, b[0], b[1]);
-                    mma_bf16(a2[2 * np + 1], a, b[2], b[3]);
+                for (int j = 0; j < 8; ++j)
+                    if (v0 + 8 * j < V) *reinterpret_cast<uint4 *>(hs + 8 * j) = pack8(&h[8 * j]);
+            }
+            ok = warp_all(wait_bar(b_dhd + 8 * (it & 1), (it >> 1) & 1, abort));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float t[32];
+                tc_ld32(tmem + lane_base + kColDh + 64 * (it & 1) + 32 * half, t);
+#pragma unroll
+                for (int x = 0; x < 32; ++x) h[32 * half + x] = fmaf(dec, h[32 * half + x], t[x]);
+            }
+            tc_fence_before();
+        }
+        if (ok && nts > 0) dvn_snapshot(nts - 1);
+        cp_async_wait<0>();  // no copy outlives the CTA
+        if (ok && p.dh0 && d < K) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+                if (v0 + c < V) p.dh0[(((int64_t)s * p.H + hh) * K + d) * p.vfull + v0 + c] = h[c];
+        }
+    } else if (warp < 8) {
+        // ------------------------------------------------ dv_new (warps 4-7)
+        const int q4 = warp & 3;
+        bool ok = true;
+        for (int it = 0; it < nts && ok; ++it) {
+            ok = warp_all(wait_bar(b_dvd + 8 * (it & 1), (it >> 1) & 1, abort));
+            tc_fence_after();
+            float v[64];
+            if (ok) {
+                tc_ld64(tmem + lane_base + kColDv + 64 * (it & 1), v);
+                if (lane < 16) {  // token row i of the M = 64 accumulator: -dv_new
+                    const int i = 16 * q4 + lane;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 u = pack8(&v[8 * j]);
+                        u.x ^= 0x80008000u, u.y ^= 0x80008000u, u.z ^= 0x80008000u, u.w ^= 0x80008000u;
+                        *reinterpret_cast<uint4 *>(sm + kOffDvn + j * 1024 + i * 16) = u;
+                    }
                 }
             }
-#pragma unroll
-            for (int n = 0; n < 4; ++n)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-                    *reinterpret_cast<uint32_t *>(sm.dvn + (m0 + g8 + 8 * hf) * kL6 + n0 + 8 * n + 2 * t4) =
-                        pack_bf16(-a2[n][2 * hf], -a2[n][2 * hf + 1]);
+            fence_async_smem();
+            tc_fence_before();
+            arrive(b_dvr);
         }
-        __syncthreads();
-        {  // dv_new's snapshot (the tile holds -dv_new: flip the sign bits)
-            bf16 *vsnap = p.dvn_snap + gch * kChunk * p.snap_ld + v0;
-            for (int e = tid; e < kChunk * 8; e += kThreads) {
-                const int i = e >> 3, c8 = (e & 7) * 8;
-                if (v0 + c8 < V) {
-                    uint4 u = *reinterpret_cast<const uint4 *>(sm.dvn + i * kL6 + c8);
-                    u.x ^= 0x80008000u, u.y ^= 0x80008000u, u.z ^= 0x80008000u, u.w ^= 0x80008000u;
-                    *reinterpret_cast<uint4 *>(vsnap + (int64_t)i * p.snap_ld + c8) = u;
-                }
-            }
+    } else if (tid == 8 * 32) {
+        // ------------------------------------------------------ the MMA issuer
+        auto issue_imgs = [&](int it) {
+            const uint32_t slot = sbase + (uint32_t)(it % kNS) * kSlot, bar = b_full + 8 * (it % kNS);
+            const int64_t gch = gch_of(it);
+            arrive_expect_tx(bar, 3 * kImgW + kImgP + kDecB);
+            bulk_g2s(slot + kOffQg, p.qg_img + gch * kImgW, kImgW, bar);
+            bulk_g2s(slot + kOffW, p.w_img + gch * kImgW, kImgW, bar);
+            bulk_g2s(slot + kOffKg, p.kg_img + gch * kImgW, kImgW, bar);
+            bulk_g2s(slot + kOffP, p.p_img + gch * kImgP, kImgP, bar);
+            bulk_g2s(slot + kOffDec, p.dec + gch * kKP, kDecB, bar);
+        };
+        // instruction descriptors: P^T do (A MN-major), kg dh' (A K-major),
+        // qg^T do and w^T dv_new (M = 128, A MN-major); B always MN-major
+        constexpr uint32_t kIdPd = tc_idesc(64, 64, 1, 1), kIdKg = tc_idesc(64, 64, 0, 1);
+        constexpr uint32_t kIdDh = tc_idesc(128, 64, 1, 1);
+        // B descriptors (lbo: core stride along K, sbo: along N); a K step of
+        // 16 advances them by 256 bytes
+        const uint64_t dDh = tc_sdesc(sbase + kOffDh, 128, 2048), dDv = tc_sdesc(sbase + kOffDvn, 128, 1024);
+        int issued = min(nts, kNS);
+        for (int j = 0; j < issued; ++j) issue_imgs(j);
+        bool ok = true;
+        int it = 0;
+        for (; it < nts && ok; ++it) {
+            const int sl = it % kNS;
+            const uint32_t bb = (uint32_t)(it & 1);
+            const uint32_t slot = sbase + (uint32_t)sl * kSlot;
+            // A descriptors: P^T (K = token i: cores 1024 apart, M = j: 128),
+            // qg^T / w^T (K = i: 2048, M = key: 128), kg (K = key: 1024, M = i: 128)
+            const uint64_t dP = tc_sdesc(slot + kOffP, 1024, 128), dQ = tc_sdesc(slot + kOffQg, 2048, 128);
+            const uint64_t dW = tc_sdesc(slot + kOffW, 2048, 128), dK = tc_sdesc(slot + kOffKg, 1024, 128);
+            const uint64_t dO = tc_sdesc(slot + kOffDo, 128, 1024);
+            const uint32_t tdv = tmem + kColDv + 64 * bb, tdh = tmem + kColDh + 64 * bb;
+            ok = wait_bar(b_full + 8 * sl, (it / kNS) & 1, abort);
+            if (!ok) break;
+            tc_fence_after();
+            // the do-only products (the accumulators' previous readers,
+            // chunk it-2's, were done before chunk it-1's dh' arrived)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc_mma(tdv, dP + 128 * ks, dO + 16 * ks, kIdPd, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc_mma(tdh, dQ + 256 * ks, dO + 16 * ks, kIdDh, ks > 0);
+            ok = wait_bar(b_dhr, (uint32_t)it & 1, abort);
+            if (!ok) break;
+            tc_fence_after();
+            // chunk it+2's images into chunk it-1's slot (dh' of chunk it
+            // follows that chunk's last product)
+            if (it >= 1 && issued < nts) issue_imgs(issued++);
+            // dv_new += kg dh' (K = 128 keys)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) tc_mma(tdv, dK + 128 * ks, dDh + 16 * ks, kIdKg, 1);
+            tc_commit(b_dvd + 8 * bb);
+            ok = wait_bar(b_dvr, (uint32_t)it & 1, abort);
+            if (!ok) break;
+            tc_fence_after();
+            // dh += w^T (-dv_new) (K = 64 tokens)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc_mma(tdh, dW + 256 * ks, dDv + 16 * ks, kIdDh, 1);
+            tc_commit(b_dhd + 8 * bb);
         }
-        // dh = e^{G_C} dh' + qg^T do - w^T dv_new
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const float d = S.dec[16 * warp + g8 + 8 * hf];
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                acc[n][2 * hf] *= d;
-                acc[n][2 * hf + 1] *= d;
-            }
+        if (!ok) {
+            // drain: one more commit covers every MMA issued so far; its
+            // barrier (chunk it's dv_new barrier) completes the phase of
+            // parity (it / 2) & 1 at the latest with it. Then the bulk copies
+            // of the chunks not yet consumed land (bounded waits).
+            *abort = 1;
+            tc_commit(b_dvd + 8 * (uint32_t)(it & 1));
+            wait_bar(b_dvd + 8 * (uint32_t)(it & 1), (uint32_t)(it >> 1) & 1, nullptr);
+            for (int j = it; j < issued; ++j) wait_bar(b_full + 8 * (j % kNS), (j / kNS) & 1, nullptr);
         }
-        {
-            const Tile tdo{S.dout, kL6}, tdv{sm.dvn, kL6};
-            const int m0 = 16 * warp;
-#pragma unroll
-            for (int k0 = 0; k0 < kChunk; k0 += 16) {  // qg^T and w^T: stored [i][d], read transposed
-                uint32_t aq[4], aw[4];
-                ldsm_x4_t(aq, S.qg + img_w_off(k0 + (lane & 7) + ((lane >> 4) << 3), m0 + ((lane >> 3) & 1) * 8));
-                ldsm_x4_t(aw, S.w + img_w_off(k0 + (lane & 7) + ((lane >> 4) << 3), m0 + ((lane >> 3) & 1) * 8));
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    uint32_t b[4], bv[4];
-                    frag_b2(b, tdo, true, 16 * np, k0, lane);
-                    frag_b2(bv, tdv, true, 16 * np, k0, lane);
-                    mma_bf16(acc[2 * np], aq, b[0], b[1]);
-                    mma_bf16(acc[2 * np + 1], aq, b[2], b[3]);
-                    mma_bf16(acc[2 * np], aw, bv[0], bv[1]);
-                    mma_bf16(acc[2 * np + 1], aw, bv[2], bv[3]);
-                }
-            }
-        }
-        __syncthreads();  // stage it & 1, dh and dvn are rewritten next
     }
-    if (!ok) {
-        // a copy wait gave up: record it, let the copies in flight land, leave
-        if (tid == 0) atomicOr(p.err, kDevErrTimeout);
-        cp_async_wait<0>();
-        wait_bar(bar[it & 1], (it >> 1) & 1, nullptr);
-        if (it + 1 < nts) wait_bar(bar[(it + 1) & 1], ((it + 1) >> 1) & 1, nullptr);
-        return;
-    }
-    if (p.dh0) {
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int r = 16 * warp + g8 + 8 * (e >> 1), col = v0 + 8 * n + 2 * t4 + (e & 1);
-                if (r < K && col < V) p.dh0[(((int64_t)s * p.H + hh) * K + r) * p.vfull + col] = acc[n][e];
-            }
-    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && *abort) atomicOr(p.err, kDevErrTimeout);
+    if (warp == 0) tc_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dh(const BwdParams &p, cudaStream_t st) {
-    const int bytes = (int)sizeof(DhSmem);
-    cudaError_t e = cudaFuncSetAttribute(bwd_dh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaError_t e = cudaFuncSetAttribute(bwd_dh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBytesTc);
     if (e != cudaSuccess) return e;
-    bwd_dh_kernel<<<dim3(p.n_seq * p.H, (p.V + 63) / 64), kThreads, bytes, st>>>(p);
+    bwd_dh_kernel<<<dim3(p.n_seq * p.H, (p.V + 63) / 64), kThreadsTc, kBytesTc, st>>>(p);
     return cudaGetLastError();
 }
 

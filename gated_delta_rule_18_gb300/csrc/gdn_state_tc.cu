@@ -264,7 +264,9 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
 #pragma unroll
         for (int j = 0; j < 4; ++j) uv[j] = *reinterpret_cast<const uint4 *>(urow + 1024 * j);
     };
-    auto vnew_half = [&](int c, int i, int c0, const uint4 (&uvs)[4]) {
+    // (the packed values also go to keep[], for the snapshot the caller
+    // stores after its hand-over)
+    auto vnew_half = [&](int c, int i, int c0, const uint4 (&uvs)[4], uint4 (&keep)[4]) {
         const uint32_t par = c & 1;
         uint32_t rr[32];
         asm volatile(
@@ -293,11 +295,18 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             const uint4 pv = pack8(f);
             *reinterpret_cast<uint4 *>(sm + Lay::vn + (Cfg<BV>::kVnBuf == 2 ? par : 0u) * Lay::vn_bytes +
                                        (c0 / 8 + j) * 1024 + i * 16) = pv;
-            if (p.vn_snap && v0 + c0 + 8 * j < p.Vt)  // (the ones column's too)
-                *reinterpret_cast<uint4 *>(p.vn_snap +
-                                           (((int64_t)hh * p.max_chunks + gc0 + c) * kChunk + i) * p.snap_ld +
-                                           v0 + c0 + 8 * j) = pv;
+            keep[j] = pv;
         }
+    };
+    // v_new's snapshot (the ones column's too), stored after the hand-over: a
+    // proxy fence after global stores would wait for them
+    auto vnew_snapshot = [&](int c, int i, int c0, const uint4 (&keep)[4]) {
+        if (!p.vn_snap) return;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (v0 + c0 + 8 * j < p.Vt)
+                *reinterpret_cast<uint4 *>(p.vn_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * kChunk + i) * p.snap_ld +
+                                           v0 + c0 + 8 * j) = keep[j];
     };
 
     if (warp < 4 * kUT) {
@@ -321,16 +330,19 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
             const uint32_t par = c & 1;
             // h (bf16) -> MN-major B operand: (col/8)*2048 + r*16; its last
             // reader, chunk c-1's first product, finished before that chunk's dh
-            bf16 *hs = p.h_snap ? p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * p.snap_ld + v1
-                                : nullptr;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 hv = pack8(&h[8 * j]);
-                *reinterpret_cast<uint4 *>(sm + Lay::h + (hc / 8 + j) * 2048 + r * 16) = hv;
-                if (hs && r < K && v1 + 8 * j < p.Vt) *reinterpret_cast<uint4 *>(hs + 8 * j) = hv;
-            }
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(sm + Lay::h + (hc / 8 + j) * 2048 + r * 16) = pack8(&h[8 * j]);
             fence_async_smem();
             arrive(b_h);
+            // its snapshot after the hand-over (a proxy fence after global
+            // stores would wait for them)
+            if (p.h_snap && r < K) {
+                bf16 *hs = p.h_snap + (((int64_t)hh * p.max_chunks + gc0 + c) * K + r) * p.snap_ld + v1;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (v1 + 8 * j < p.Vt) *reinterpret_cast<uint4 *>(hs + 8 * j) = pack8(&h[8 * j]);
+            }
             if ((warp & 3) < 2) {  // v_new for token row r (TMEM lanes 0-63)
                 // Only the v_new warps (and the issuer) wait for ring A: chunk
                 // c+kRingA's copies into the same slot follow this chunk's
@@ -340,19 +352,20 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
                 if (!ok) break;
                 // 64 columns: columns 0..31 (the 64-column tile: its helpers
                 // take 32..63), or this group's 64 of the 128-column tile
-                uint4 uv[4], uw[4];
+                uint4 uv[4], uw[4], kv[4], kw[4];
                 load_u(c, r, hc, uv);
                 if (BV == 128) load_u(c, r, hc + 32, uw);
                 ok = warp_all(wait_bar(b_a, par, abort));
                 tc_fence_after();
                 if (ok) {
-                    vnew_half(c, r, hc, uv);
-                    if (BV == 128) vnew_half(c, r, hc + 32, uw);
+                    vnew_half(c, r, hc, uv, kv);
+                    if (BV == 128) vnew_half(c, r, hc + 32, uw, kw);
                 }
                 fence_async_smem();
                 tc_fence_before();
                 arrive(b_vn);
                 if (!ok) break;
+                if (BV == 64) vnew_snapshot(c, r, hc, kv);  // (128-column tiles run without snapshots)
             }
             ok = warp_all(wait_bar(b_dh, par, abort));
             if (!ok) break;
@@ -386,14 +399,15 @@ __global__ void __launch_bounds__(Cfg<BV>::kThreads, 1) state_tc_kernel(const Fw
         for (int c = 0; c < nchunks && ok; ++c) {
             const uint32_t par = c & 1;
             ok = warp_all(wait_bar(b_ra0 + 8 * (c % kRingA), (c / kRingA) & 1, abort));
-            uint4 uv[4];
+            uint4 uv[4], kv[4];
             if (ok) load_u(c, tid - 128, 32, uv);
             ok = ok && warp_all(wait_bar(b_a, par, abort));
             tc_fence_after();
-            if (ok) vnew_half(c, tid - 128, 32, uv);
+            if (ok) vnew_half(c, tid - 128, 32, uv, kv);
             fence_async_smem();
             tc_fence_before();
             arrive(b_vn);
+            if (ok) vnew_snapshot(c, tid - 128, 32, kv);
         }
     } else if (tid == 8 * 32) {
         // ------------------------------------------------------ the MMA issuer
