@@ -167,18 +167,28 @@ __global__ void __launch_bounds__(kThreads, 1) frame_lam_kernel(const FrameBwdPa
     if (nsteps > 0) lam_stage_a(p, sm, (nsteps - 1) & 1, (int64_t)bh * F + write_frame(d, F, nsteps - 1));
     for (int cs = nsteps - 1; cs >= 0; --cs) {
         const int w = write_frame(d, F, cs), rf = read_frame(d, F, cs);
-        // Lam = C_r + carry, to the workspace and the shared tile
+        // Lam = C_r + carry, to the workspace and the shared tile (every C
+        // value is loaded before the first store: a load after a store to
+        // Lam could not be moved above it, and each would wait its own
+        // round trip)
         const float *C = p.cmat + ((int64_t)bh * F + rf) * K * Vs;
         float *L = p.lam + ((int64_t)bh * F + w) * K * Vs;
+        float cin[4][4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int r = r0 + x, j = j0 + c0 + c;
+                cin[x][c] = (r < K && j < Vs) ? C[(int64_t)r * Vs + j] : 0.f;
+            }
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
             const int r = r0 + x;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const int j = j0 + c0 + c;
-                const bool in = r < K && j < Vs;
-                carry[x][c] += in ? C[(int64_t)r * Vs + j] : 0.f;
-                if (in) L[(int64_t)r * Vs + j] = carry[x][c];
+                carry[x][c] += cin[x][c];
+                if (r < K && j < Vs) L[(int64_t)r * Vs + j] = carry[x][c];
             }
             *reinterpret_cast<float4 *>(sm.s + r * kFrameBwdCT + c0) =
                 make_float4(carry[x][0], carry[x][1], carry[x][2], carry[x][3]);
