@@ -254,7 +254,17 @@ __global__ void __launch_bounds__(256, 1) frame_chain_kernel(const FrameParams p
                     for (int c = 0; c < 4; ++c) acc[x][c] = fmaf(dec, acc[x][c], bv[x][c]);
                 __syncthreads();  // the tile and this buffer are rewritten next
             }
-            // the state frame `of` reads, summed over the directions
+            // the state frame `of` reads, summed over the directions (the
+            // forward run's values all loaded before the first store)
+            float prev[4][4];
+            const bool add = rev && p.direction == 2;
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int r = r0 + x, j = j0 + c0 + c;
+                    prev[x][c] = (add && r < K && j < Vt) ? p.sout[(((int64_t)bh * F + of) * K + r) * p.Vs + j] : 0.f;
+                }
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
                 const int r = r0 + x;
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(256, 1) frame_chain_kernel(const FrameParams p
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int j = j0 + c0 + c;
-                    if (j < Vt) dst[j] = (rev && p.direction == 2) ? dst[j] + acc[x][c] : acc[x][c];
+                    if (j < Vt) dst[j] = prev[x][c] + acc[x][c];
                 }
             }
         }
