@@ -292,13 +292,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1) bwd_dh_kernel(const BwdParams p
             ok = wait_bar(b_dhr, (uint32_t)it & 1, abort);
             if (!ok) break;
             tc_fence_after();
-            // chunk it+2's images into chunk it-1's slot (dh' of chunk it
-            // follows that chunk's last product)
-            if (it >= 1 && issued < nts) issue_imgs(issued++);
             // dv_new += kg dh' (K = 128 keys)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) tc_mma(tdv, dK + 128 * ks, dDh + 16 * ks, kIdKg, 1);
             tc_commit(b_dvd + 8 * bb);
+            // chunk it+2's images into chunk it-1's slot (dh' of chunk it
+            // followed that chunk's last product), while dv_new is read out
+            if (it >= 1 && issued < nts) issue_imgs(issued++);
             ok = wait_bar(b_dvr, (uint32_t)it & 1, abort);
             if (!ok) break;
             tc_fence_after();
