@@ -1100,6 +1100,17 @@ def test_small_backward_fp32(name):
     assert all(e <= TOL["f32"] for e in errs.values()), (name, errs)
 
 
+def test_backward_fp32_empty_sequence():
+    """T = 0 on the fp32 path: dh0 = dh_final, and the token outputs are empty"""
+    import gated_delta_rule_18_gb300 as gdn
+    w = workloads.make(2, 0, 2, 64, 48, dtype="f32", seed=116, h0_std=0.5)
+    res = gdn.gdn_chunk_bwd(to_dev(w.q), to_dev(w.k), to_dev(w.v), f32_dev(w.beta), f32_dev(w.g),
+                            to_dev(w.v), h0=f32_dev(w.h0), dh_final=f32_dev(w.h0))
+    torch().cuda.synchronize()
+    assert np.array_equal(res["dh0"].cpu().numpy(), w.h0)
+    assert res["dq"].numel() == 0 and res["dv"].numel() == 0
+
+
 def test_backward_fp32_reproducible_and_malformed_seqlens():
     """two runs agree bit for bit (the column ranges are summed in a fixed
     order); a cu_seqlens that does not end at T is reported in the error
