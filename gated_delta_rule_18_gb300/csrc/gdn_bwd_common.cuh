@@ -146,6 +146,28 @@ __device__ __forceinline__ void fill_den_v(const BwdParams &p, const ChunkCtx &x
 // value columns of this range that come from v / dout (the rest: the ones column)
 __device__ __forceinline__ int value_cols(const BwdParams &p) { return p.den_col >= 0 ? p.den_col : p.V; }
 
+// The per-key sums (dq or dk, (B*T, H, K) fp32) that an earlier value range
+// left at this thread's fragment positions: chunk rows r0 and r0 + 8, keys
+// k0 + 8n + 2 (lane & 3), n < NF. Zero on the first range, where `on` is
+// false, past K, or where tok_of(row) < 0. All loads go out together, ahead
+// of the stores that add them: a load placed after a store through the same
+// pointer would otherwise wait for the one before it.
+template <int NF, class TokOf>
+__device__ __forceinline__ void acc_rows_load(float2 (&prev)[2][NF], const BwdParams &p, const ChunkCtx &x,
+                                              const float *base, int r0, int k0, bool on, TokOf tok_of) {
+    const int t4 = threadIdx.x & 3;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int tk = p.acc && on ? tok_of(r0 + 8 * hf) : -1;
+        const float *src = tk >= 0 ? base + ((x.row0 + tk) * p.H + x.hh) * p.K : nullptr;
+#pragma unroll
+        for (int n = 0; n < NF; ++n) {
+            const int d = k0 + 8 * n + 2 * t4;
+            prev[hf][n] = src && d < p.K ? *reinterpret_cast<const float2 *>(src + d) : make_float2(0.f, 0.f);
+        }
+    }
+}
+
 // T = (I + A)^{-1} with A_ij = beta_i kkg_ij (i > j; kkg fp32 with row
 // stride kPS), by 16 x 16 blocks as in the forward's solve: diagonal
 // inverses T_II in fp32 by forward substitution, B_IM = -T_II A_IM, then

@@ -344,6 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
     }
     // through the normalisation: dq = (dq^ - q^ (q^ . dq^)) / |q|
     if (nk0 < kq) frag_rowdot_add(dq, sm.q, m0, nk0, sm.row);
+    // an earlier value range's dq, read before any store so that the loads
+    // do not wait one after another behind the stores
+    float2 prev[2][8];
+    acc_rows_load(prev, p, x, p.dq, m0 + g8, nk0, nk0 < kq, [&](int i) {
+        return i < x.Lc ? q_token(p.reverse, x.len, x.pos0 + i) : -1;
+    });
     __syncthreads();
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -359,10 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_gk_kernel(const BwdParams 
             float2 o;
             o.x = p.l2norm ? r * (dq[n][2 * hf] - tile_at(sm.q, i, d) * dot) : dq[n][2 * hf];
             o.y = p.l2norm ? r * (dq[n][2 * hf + 1] - tile_at(sm.q, i, d + 1) * dot) : dq[n][2 * hf + 1];
-            if (p.acc) {
-                const float2 a = *reinterpret_cast<const float2 *>(dst + d);
-                o.x += a.x, o.y += a.y;
-            }
+            if (p.acc) o.x += prev[hf][n].x, o.y += prev[hf][n].y;
             *reinterpret_cast<float2 *>(dst + d) = o;
         }
     }
@@ -751,26 +754,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dk_gk_kernel(const BwdParams 
             }
     }
     __syncthreads();
-    // dk out
+    // dk out (an earlier value range's dk read first, as for dq)
+    {
+        float2 prev[2][8];
+        acc_rows_load(prev, p, x, p.dk, m0 + g8, nk0, nk0 < kq, kv_row);
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        const int i = m0 + g8 + 8 * hf;
-        const int tk = kv_row(i);
-        if (tk < 0 || nk0 >= kq) continue;
-        float *dst = p.dk + ((x.row0 + tk) * p.H + x.hh) * K;
-        const float r = sm.rk[i], dot = sm.row[i];
+        for (int hf = 0; hf < 2; ++hf) {
+            const int i = m0 + g8 + 8 * hf;
+            const int tk = kv_row(i);
+            if (tk < 0 || nk0 >= kq) continue;
+            float *dst = p.dk + ((x.row0 + tk) * p.H + x.hh) * K;
+            const float r = sm.rk[i], dot = sm.row[i];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int d = nk0 + 8 * n + 2 * t4;
-            if (d >= K) continue;
-            float2 o;
-            o.x = p.l2norm ? r * (dk[n][2 * hf] - tile_at(sm.k, i, d) * dot) : dk[n][2 * hf];
-            o.y = p.l2norm ? r * (dk[n][2 * hf + 1] - tile_at(sm.k, i, d + 1) * dot) : dk[n][2 * hf + 1];
-            if (p.acc) {
-                const float2 a = *reinterpret_cast<const float2 *>(dst + d);
-                o.x += a.x, o.y += a.y;
+            for (int n = 0; n < 8; ++n) {
+                const int d = nk0 + 8 * n + 2 * t4;
+                if (d >= K) continue;
+                float2 o;
+                o.x = p.l2norm ? r * (dk[n][2 * hf] - tile_at(sm.k, i, d) * dot) : dk[n][2 * hf];
+                o.y = p.l2norm ? r * (dk[n][2 * hf + 1] - tile_at(sm.k, i, d + 1) * dot) : dk[n][2 * hf + 1];
+                if (p.acc) o.x += prev[hf][n].x, o.y += prev[hf][n].y;
+                *reinterpret_cast<float2 *>(dst + d) = o;
             }
-            *reinterpret_cast<float2 *>(dst + d) = o;
         }
     }
     // the reverse scan never reads token 0's key and value: zero gradients

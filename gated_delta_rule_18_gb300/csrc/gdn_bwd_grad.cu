@@ -196,6 +196,11 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
             if (t4 == 0) atomicAdd(&sm.row[m0 + g8 + 8 * hf], v);
         }
     }
+    // an earlier value range's dq, read before any store (the loads then overlap)
+    float2 prev[2][8];
+    acc_rows_load(prev, p, x, p.dq, m0 + g8, nk0, true, [&](int i) {
+        return i < x.Lc ? q_token(p.reverse, x.len, x.pos0 + i) : -1;
+    });
     __syncthreads();
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
@@ -212,10 +217,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_dq_kernel(const BwdParams p) 
             o.x = p.l2norm ? r * (dq[n][2 * hf] - __bfloat162float(sm.q[i * kLK + d]) * dot) : dq[n][2 * hf];
             o.y = p.l2norm ? r * (dq[n][2 * hf + 1] - __bfloat162float(sm.q[i * kLK + d + 1]) * dot)
                            : dq[n][2 * hf + 1];
-            if (p.acc) {
-                const float2 a = *reinterpret_cast<const float2 *>(dst + d);
-                o.x += a.x, o.y += a.y;
-            }
+            if (p.acc) o.x += prev[hf][n].x, o.y += prev[hf][n].y;
             *reinterpret_cast<float2 *>(dst + d) = o;
         }
     }
@@ -589,7 +591,9 @@ __global__ void __launch_bounds__(NW * 32, 1) bwd_dk_kernel(const BwdParams p) {
         }
     }
     __syncthreads();
-    // dk out
+    // dk out (an earlier value range's dk read first, as for dq)
+    float2 prev[2][FK];
+    acc_rows_load(prev, p, x, p.dk, m0 + g8, nk0, true, kv_row);
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
         const int i = m0 + g8 + 8 * hf;
@@ -608,10 +612,7 @@ __global__ void __launch_bounds__(NW * 32, 1) bwd_dk_kernel(const BwdParams p) {
             o.x = p.l2norm ? r * (dk[n][2 * hf] - __bfloat162float(sm.k[i * kLK + d]) * dot) : dk[n][2 * hf];
             o.y = p.l2norm ? r * (dk[n][2 * hf + 1] - __bfloat162float(sm.k[i * kLK + d + 1]) * dot)
                            : dk[n][2 * hf + 1];
-            if (p.acc) {
-                const float2 a = *reinterpret_cast<const float2 *>(dst + d);
-                o.x += a.x, o.y += a.y;
-            }
+            if (p.acc) o.x += prev[hf][n].x, o.y += prev[hf][n].y;
             *reinterpret_cast<float2 *>(dst + d) = o;
         }
     }
@@ -637,8 +638,14 @@ __global__ void __launch_bounds__(NW * 32, 1) bwd_dk_kernel(const BwdParams p) {
 #pragma unroll
         for (int q = 0; q < NQ; ++q) gl += sm.gck[q][i0] + sm.gck[q][i1];
         const float gc = warp_sum(gl);
-        if (t0 >= 0) d0 = dG0 + p.dg_part[(x.row0 + t0) * p.H + x.hh];
-        if (t1 >= 0) d1 = dG1 + p.dg_part[(x.row0 + t1) * p.H + x.hh];
+        const int64_t row0 = (x.row0 + t0) * p.H + x.hh, row1 = (x.row0 + t1) * p.H + x.hh;
+        if (t0 >= 0) d0 = dG0 + p.dg_part[row0];
+        if (t1 >= 0) d1 = dG1 + p.dg_part[row1];
+        // a later value range adds to the earlier ranges' sums: read them
+        // here, before the stores below
+        float pg0 = 0.f, pb0 = 0.f, pg1 = 0.f, pb1 = 0.f;
+        if (p.acc && t0 >= 0) pg0 = p.dg[row0], pb0 = p.dbeta[row0];
+        if (p.acc && t1 >= 0) pg1 = p.dg[row1], pb1 = p.dbeta[row1];
         if (i0 == last) d0 += gc;
         if (i1 == last) d1 += gc;
         // suffix sum over lanes of the pair sums
@@ -649,18 +656,15 @@ __global__ void __launch_bounds__(NW * 32, 1) bwd_dk_kernel(const BwdParams p) {
             if (lane + o < 32) incl += y;
         }
         const float s1 = incl - d0, s0 = incl;  // dg at i1 and at i0
-        // (a later value range adds to the earlier ranges' sums)
         if (t0 >= 0) {
-            const int64_t row = (x.row0 + t0) * p.H + x.hh;
             const float dg0 = sm.graw[i0] < kLogGateMin ? 0.f : s0;
-            p.dg[row] = p.acc ? p.dg[row] + dg0 : dg0;
-            p.dbeta[row] = p.acc ? p.dbeta[row] + dB0 : dB0;
+            p.dg[row0] = p.acc ? pg0 + dg0 : dg0;
+            p.dbeta[row0] = p.acc ? pb0 + dB0 : dB0;
         }
         if (t1 >= 0) {
-            const int64_t row = (x.row0 + t1) * p.H + x.hh;
             const float dg1 = sm.graw[i1] < kLogGateMin ? 0.f : s1;
-            p.dg[row] = p.acc ? p.dg[row] + dg1 : dg1;
-            p.dbeta[row] = p.acc ? p.dbeta[row] + dB1 : dB1;
+            p.dg[row1] = p.acc ? pg1 + dg1 : dg1;
+            p.dbeta[row1] = p.acc ? pb1 + dB1 : dB1;
         }
     }
 }
