@@ -292,31 +292,41 @@ __global__ void __launch_bounds__(256, 1) frame_chain_kernel(const FrameParams p
 }
 
 // ----------------------------------------------------------------- out ---
-// One CTA (8 warps) per (sequence x head, 64-token chunk, 128 value columns):
-// the chunk's q rows (cp.async) and its frame's state, converted to bf16
-// from 16-byte fp32 loads; warp w computes tokens 16 (w & 3) .. + 15 of
-// column half w >> 2.
+// One CTA (8 warps) per (sequence x head, up to kOutChunks consecutive
+// 64-token chunks of one frame, 128 value columns). The frame's state is
+// converted to bf16 once per CTA, from 16-byte fp32 loads; the chunks' q rows
+// stream through two cp.async buffers, the next chunk's copy in flight while
+// the current one is multiplied and stored. Warp w computes tokens
+// 16 (w & 3) .. + 15 of column half w >> 2.
+constexpr int kOutChunks = 4;
 struct OutSmem {
-    bf16 q[kChunk * kKS];   // [token][key]
-    bf16 st[kKP * kXB];     // state block, [key][column]
+    bf16 q[2][kChunk * kKS];  // [token][key], two chunks
+    bf16 st[kKP * kXB];       // state block, [key][column]
 };
 __global__ void __launch_bounds__(256) frame_out_kernel(const FrameParams p) {
     extern __shared__ __align__(16) unsigned char smraw[];
     OutSmem &sm = *reinterpret_cast<OutSmem *>(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.x / p.H, h = blockIdx.x % p.H, c = blockIdx.y, cb = blockIdx.z;
+    const int b = blockIdx.x / p.H, h = blockIdx.x % p.H, cb = blockIdx.z;
     const int K = p.K, V = p.V, Vt = p.Vt;
-    const int64_t t0 = (int64_t)c * kChunk;
-    const int f = (int)(t0 / p.frame);
+    // chunks per frame, CTAs per frame; this CTA's frame and chunks
+    const int cpf = p.frame / kChunk, gpf = (cpf + kOutChunks - 1) / kOutChunks;
+    const int f = blockIdx.y / gpf;
+    const int c_begin = f * cpf + (blockIdx.y % gpf) * kOutChunks;
+    const int n_ch = min(kOutChunks, (f + 1) * cpf - c_begin);
     const int col0 = cb * 128;
     const bf16 *qp = (const bf16 *)p.q;
-    for (int e = tid; e < kChunk * (kKP / 8); e += 256) {
-        const int i = e >> 4, d = (e & 15) * 8;
-        const bool in = d < K;
-        cp_async16(sm.q + i * kKS + d, in ? qp + b * p.qk_sb + (t0 + i) * p.qk_st + h * p.qk_sh + d : qp,
-                   in ? 16 : 0);
-    }
-    cp_async_commit();
+    auto load_q = [&](int c, bf16 *dst) {
+        const int64_t t0 = (int64_t)c * kChunk;
+        for (int e = tid; e < kChunk * (kKP / 8); e += 256) {
+            const int i = e >> 4, d = (e & 15) * 8;
+            const bool in = d < K;
+            cp_async16(dst + i * kKS + d, in ? qp + b * p.qk_sb + (t0 + i) * p.qk_st + h * p.qk_sh + d : qp,
+                       in ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    load_q(c_begin, sm.q[0]);
     const float *S = p.sout + ((int64_t)blockIdx.x * p.F + f) * K * p.Vs;
 #pragma unroll 4
     for (int e = tid; e < kKP * 32; e += 256) {  // 4 columns per step
@@ -328,54 +338,64 @@ __global__ void __launch_bounds__(256) frame_out_kernel(const FrameParams p) {
         if (j + 3 >= Vt) v4.w = 0.f;
         *reinterpret_cast<uint2 *>(sm.st + rr * kXB + cc) = make_uint2(pack_bf16(v4.x, v4.y), pack_bf16(v4.z, v4.w));
     }
-    cp_async_wait<0>();
-    __syncthreads();
     const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);
-    float acc[8][4];
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < kKP / 16; ++ks) {
-        uint32_t a[4];
-        ldsm_x4(a, sm.q + (m0 + (lane & 15)) * kKS + ks * 16 + (lane >> 4) * 8);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            uint32_t bb[4];
-            ldsm_x4_t(bb, sm.st + (ks * 16 + (lane & 15)) * kXB + n0 + 16 * np + (lane >> 4) * 8);
-            mma_bf16(acc[2 * np], a, bb[0], bb[1]);
-            mma_bf16(acc[2 * np + 1], a, bb[2], bb[3]);
-        }
-    }
     const int g8 = lane >> 2, t4 = lane & 3;
+    for (int it = 0; it < n_ch; ++it) {
+        if (it + 1 < n_ch) {
+            load_q(c_begin + it + 1, sm.q[(it + 1) & 1]);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const bf16 *qs = sm.q[it & 1];
+        const int64_t t0 = (int64_t)(c_begin + it) * kChunk;
+        float acc[8][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < 8; ++n)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int64_t t = t0 + m0 + g8 + 8 * hf;
-            const int j = col0 + n0 + 8 * n + 2 * t4;
-            const float o0 = acc[n][2 * hf], o1 = acc[n][2 * hf + 1];
-            if (j + 1 < V) {  // both columns are values (V is a multiple of 8)
-                const int64_t off = b * p.o_sb + t * p.o_st + h * p.o_sh + j;
-                if (p.out_f32) {
-                    float *op = (float *)p.out + off;
-                    op[0] = p.accumulate ? op[0] + o0 : o0;
-                    op[1] = p.accumulate ? op[1] + o1 : o1;
-                } else {
-                    bf16 *op = (bf16 *)p.out + off;
-                    float y0 = o0, y1 = o1;
-                    if (p.accumulate) {
-                        y0 += __bfloat162float(op[0]);
-                        y1 += __bfloat162float(op[1]);
-                    }
-                    *reinterpret_cast<uint32_t *>(op) = pack_bf16(y0, y1);
-                }
-            } else if (p.has_den && j == V) {
-                float *dp = p.den + ((int64_t)b * p.H + h) * p.T + t;
-                *dp = p.accumulate ? *dp + o0 : o0;
+            for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < kKP / 16; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(a, qs + (m0 + (lane & 15)) * kKS + ks * 16 + (lane >> 4) * 8);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                uint32_t bb[4];
+                ldsm_x4_t(bb, sm.st + (ks * 16 + (lane & 15)) * kXB + n0 + 16 * np + (lane >> 4) * 8);
+                mma_bf16(acc[2 * np], a, bb[0], bb[1]);
+                mma_bf16(acc[2 * np + 1], a, bb[2], bb[3]);
             }
         }
+#pragma unroll
+        for (int n = 0; n < 8; ++n)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int64_t t = t0 + m0 + g8 + 8 * hf;
+                const int j = col0 + n0 + 8 * n + 2 * t4;
+                const float o0 = acc[n][2 * hf], o1 = acc[n][2 * hf + 1];
+                if (j + 1 < V) {  // both columns are values (V is a multiple of 8)
+                    const int64_t off = b * p.o_sb + t * p.o_st + h * p.o_sh + j;
+                    if (p.out_f32) {
+                        float *op = (float *)p.out + off;
+                        op[0] = p.accumulate ? op[0] + o0 : o0;
+                        op[1] = p.accumulate ? op[1] + o1 : o1;
+                    } else {
+                        bf16 *op = (bf16 *)p.out + off;
+                        float y0 = o0, y1 = o1;
+                        if (p.accumulate) {
+                            y0 += __bfloat162float(op[0]);
+                            y1 += __bfloat162float(op[1]);
+                        }
+                        *reinterpret_cast<uint32_t *>(op) = pack_bf16(y0, y1);
+                    }
+                } else if (p.has_den && j == V) {
+                    float *dp = p.den + ((int64_t)b * p.H + h) * p.T + t;
+                    *dp = p.accumulate ? *dp + o0 : o0;
+                }
+            }
+        __syncthreads();  // every warp is done with this q buffer before it is refilled
+    }
 }
 
 }  // namespace
@@ -399,7 +419,8 @@ cudaError_t launch_frame_out(const FrameParams &p, cudaStream_t st) {
     const int bytes = (int)sizeof(OutSmem);
     cudaError_t e = cudaFuncSetAttribute(frame_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    frame_out_kernel<<<dim3(p.B * p.H, p.T / kChunk, (p.Vt + 127) / 128), 256, bytes, st>>>(p);
+    const int gpf = (p.frame / kChunk + kOutChunks - 1) / kOutChunks;  // CTAs per frame
+    frame_out_kernel<<<dim3(p.B * p.H, p.F * gpf, (p.Vt + 127) / 128), 256, bytes, st>>>(p);
     return cudaGetLastError();
 }
 
