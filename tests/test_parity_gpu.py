@@ -127,10 +127,12 @@ def test_small_chunkcausal_merge(reset):
     _compare(w, ["out", "den", "merged"])
 
 
-@pytest.mark.parametrize("frame", [64, 192])
-def test_small_frame_bidirectional(frame):
-    # frame-causal form: frames share the pre-frame state; both directions + den
-    w = workloads.make_video(1, 576, 4, 112, seed=6, name="frame_small", frame=frame)
+@pytest.mark.parametrize("T,frame", [(576, 64), (576, 192), (640, 320)])
+def test_small_frame_bidirectional(T, frame):
+    # frame-causal form: frames share the pre-frame state; both directions + den.
+    # Frames of 1, 3 and 5 chunks: the output kernel takes up to four chunks of
+    # a frame per CTA, so 5 gives one CTA of four and one of a single chunk.
+    w = workloads.make_video(1, T, 4, 112, seed=6, name="frame_small", frame=frame)
     _compare(w, ["out", "den"])
 
 
