@@ -258,22 +258,40 @@ struct TokSmem {
     float dbp[2][kChunk];  // dbeta per column half (summed in order)
 };
 // fp32 (K x Vt-or-more, row stride ld) state -> bf16 [key][column] tile,
-// zero past K rows and Vt columns (or everywhere for a null state)
+// zero past K rows and Vt columns (or everywhere for a null state). A
+// thread's 16 reads go out in batches of kStBatch before their shared-memory
+// stores, so their latencies overlap instead of adding up.
+constexpr int kStPer = kKP * (kKP / 4) / kThreads;  // float4 groups per thread
+constexpr int kStBatch = 8;
+static_assert(kStPer % kStBatch == 0, "state tile batches");
 __device__ __forceinline__ void state_tile(bf16 *dst, const float *src, int ld, int K, int Vt) {
-    for (int e = threadIdx.x; e < kKP * (kKP / 4); e += kThreads) {
-        const int r = e / (kKP / 4), c = (e % (kKP / 4)) * 4;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (src && r < K) {
-            if ((ld & 3) == 0 && c + 4 <= Vt) {
-                const float4 f4 = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + c);
-                v[0] = f4.x, v[1] = f4.y, v[2] = f4.z, v[3] = f4.w;
-            } else {
+    const bool vec = (ld & 3) == 0;
 #pragma unroll
-                for (int x = 0; x < 4; ++x)
-                    if (c + x < Vt) v[x] = src[(int64_t)r * ld + c + x];
+    for (int b0 = 0; b0 < kStPer; b0 += kStBatch) {
+        float v[kStBatch][4];
+#pragma unroll
+        for (int u = 0; u < kStBatch; ++u) {
+            const int e = threadIdx.x + (b0 + u) * kThreads;
+            const int r = e / (kKP / 4), c = (e % (kKP / 4)) * 4;
+            v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
+            if (src && r < K) {
+                if (vec && c + 4 <= Vt) {
+                    const float4 f4 = *reinterpret_cast<const float4 *>(src + (int64_t)r * ld + c);
+                    v[u][0] = f4.x, v[u][1] = f4.y, v[u][2] = f4.z, v[u][3] = f4.w;
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        if (c + x < Vt) v[u][x] = src[(int64_t)r * ld + c + x];
+                }
             }
         }
-        *reinterpret_cast<uint2 *>(dst + r * kKS + c) = make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
+#pragma unroll
+        for (int u = 0; u < kStBatch; ++u) {
+            const int e = threadIdx.x + (b0 + u) * kThreads;
+            const int r = e / (kKP / 4), c = (e % (kKP / 4)) * 4;
+            *reinterpret_cast<uint2 *>(dst + r * kKS + c) =
+                make_uint2(pack_bf16(v[u][0], v[u][1]), pack_bf16(v[u][2], v[u][3]));
+        }
     }
 }
 
