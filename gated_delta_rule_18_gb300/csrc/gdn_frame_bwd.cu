@@ -51,7 +51,9 @@ struct XtSmem {
     XtStage st[2];
 };
 
-__global__ void __launch_bounds__(kThreads, 1) frame_xt_kernel(const FrameBwdParams p) {
+// Two CTAs per SM (at most 128 registers a thread): a grid of (sequence x
+// head, frame) CTAs, 256 on the video shape, is then resident in one wave.
+__global__ void __launch_bounds__(kThreads, 2) frame_xt_kernel(const FrameBwdParams p) {
     extern __shared__ __align__(16) unsigned char smraw[];
     XtSmem &sm = *reinterpret_cast<XtSmem *>(smraw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
