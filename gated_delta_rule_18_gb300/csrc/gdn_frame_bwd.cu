@@ -361,33 +361,22 @@ __global__ void __launch_bounds__(kThreads, 1) frame_tokgrad_kernel(const FrameB
                 *reinterpret_cast<uint32_t *>(sm.e + i * kKS + c) = pack_bf16(e0, e1);
                 *reinterpret_cast<uint32_t *>(sm.u + i * kKS + c) = pack_bf16(uf[n][2 * hf], uf[n][2 * hf + 1]);
             }
-        // dv = beta U (the second direction adds to the first's): a batch's
-        // previous values are all loaded before its stores, so those loads
-        // overlap instead of waiting one after another
+        // dv = beta U; the second direction adds to the first's with
+        // reductions that return nothing (no load waits; one add per
+        // element, so the sum does not depend on timing)
 #pragma unroll
-        for (int nb = 0; nb < 8; nb += 4) {
-            float2 prev[4][2];
+        for (int n = 0; n < 8; ++n)
 #pragma unroll
-            for (int nn = 0; nn < 4; ++nn)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int i = m0 + g8 + 8 * hf, c = n0 + 8 * (nb + nn) + 2 * t4;
-                    prev[nn][hf] = (p.acc && c < V)
-                                       ? *reinterpret_cast<const float2 *>(
-                                             p.dv + ((((int64_t)b * p.T + t0 + i) * p.H + h) * V + c))
-                                       : make_float2(0.f, 0.f);
-                }
-#pragma unroll
-            for (int nn = 0; nn < 4; ++nn)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int n = nb + nn, i = m0 + g8 + 8 * hf, c = n0 + 8 * n + 2 * t4;
-                    if (c >= V) continue;
-                    *reinterpret_cast<float2 *>(p.dv + ((((int64_t)b * p.T + t0 + i) * p.H + h) * V + c)) =
-                        make_float2(prev[nn][hf].x + sm.beta[i] * uf[n][2 * hf],
-                                    prev[nn][hf].y + sm.beta[i] * uf[n][2 * hf + 1]);
-                }
-        }
+            for (int hf = 0; hf < 2; ++hf) {
+                const int i = m0 + g8 + 8 * hf, c = n0 + 8 * n + 2 * t4;
+                if (c >= V) continue;
+                float2 *dst = reinterpret_cast<float2 *>(p.dv + ((((int64_t)b * p.T + t0 + i) * p.H + h) * V + c));
+                const float2 val = make_float2(sm.beta[i] * uf[n][2 * hf], sm.beta[i] * uf[n][2 * hf + 1]);
+                if (p.acc)
+                    atomicAdd(dst, val);
+                else
+                    *dst = val;
+            }
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             float s = pb[hf];
@@ -419,29 +408,24 @@ __global__ void __launch_bounds__(kThreads, 1) frame_tokgrad_kernel(const FrameB
 #pragma unroll
             for (int e = 0; e < 4; ++e) dk[n][e] = sm.beta[m0 + g8 + 8 * (e >> 1)] * (dk[n][e] - dec * c2[n][e]);
     }
-    if (nk0 < kq) {  // (batches of previous values loaded before their stores, as for dv)
+    if (nk0 < kq) {  // (the second direction adds by reductions, as for dv)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
             const int i = m0 + g8 + 8 * hf;
             const int64_t row = (((int64_t)b * p.T + t0 + i) * p.H + h) * K;
 #pragma unroll
-            for (int nb = 0; nb < 8; nb += 4) {
-                float2 aq[4], ak[4];
-#pragma unroll
-                for (int nn = 0; nn < 4; ++nn) {
-                    const int c = nk0 + 8 * (nb + nn) + 2 * t4;
-                    const bool in = p.acc && c < K;
-                    aq[nn] = in ? *reinterpret_cast<const float2 *>(p.dq + row + c) : make_float2(0.f, 0.f);
-                    ak[nn] = in ? *reinterpret_cast<const float2 *>(p.dk + row + c) : make_float2(0.f, 0.f);
-                }
-#pragma unroll
-                for (int nn = 0; nn < 4; ++nn) {
-                    const int n = nb + nn, c = nk0 + 8 * n + 2 * t4;
-                    if (c >= K) continue;
-                    *reinterpret_cast<float2 *>(p.dq + row + c) =
-                        make_float2(aq[nn].x + dq[n][2 * hf], aq[nn].y + dq[n][2 * hf + 1]);
-                    *reinterpret_cast<float2 *>(p.dk + row + c) =
-                        make_float2(ak[nn].x + dk[n][2 * hf], ak[nn].y + dk[n][2 * hf + 1]);
+            for (int n = 0; n < 8; ++n) {
+                const int c = nk0 + 8 * n + 2 * t4;
+                if (c >= K) continue;
+                float2 *oq = reinterpret_cast<float2 *>(p.dq + row + c), *ok = reinterpret_cast<float2 *>(p.dk + row + c);
+                const float2 vq = make_float2(dq[n][2 * hf], dq[n][2 * hf + 1]);
+                const float2 vk = make_float2(dk[n][2 * hf], dk[n][2 * hf + 1]);
+                if (p.acc) {
+                    atomicAdd(oq, vq);
+                    atomicAdd(ok, vk);
+                } else {
+                    *oq = vq;
+                    *ok = vk;
                 }
             }
         }
@@ -449,7 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1) frame_tokgrad_kernel(const FrameB
     if (tid < kChunk) {
         const int64_t row = ((int64_t)b * p.T + t0 + tid) * p.H + h;
         const float db = wr ? sm.dbp[0][tid] + sm.dbp[1][tid] : 0.f;
-        p.dbeta[row] = p.acc ? p.dbeta[row] + db : db;
+        if (p.acc)
+            atomicAdd(p.dbeta + row, db);
+        else
+            p.dbeta[row] = db;
     }
     // dg_frame from the chain's parts, once per frame (its first chunk)
     if (tid == 0 && t0 % p.frame == 0) {
