@@ -19,18 +19,21 @@
 //   dk_t = beta_t (Lam e_t - P_f u_t)  (P_f = e^{g_f} S_prev, as predicted from),
 //   dg_f = e^{g_f} sum(A_f Lam . S_prev),  dS_prev = e^{g_f} A_f Lam (dh0),
 // and per token of the reading frame dq_t = R_f [do_t | dden_t].
-// Three kernels per direction:
+// Three kernels (frame_xt once, the other two per direction):
 //   frame_xt      per (sequence x head, frame): C_f = Q_f^T [dO_f | dden_f]
-//                 over the frame's chunks on tensor cores (mma.sync)
+//                 over the frame's chunks on tensor cores (mma.sync); both
+//                 directions read it
 //   frame_lam     per (sequence x head, 32-column tile): the fp32 chain of
 //                 Lam over the writes in reverse order, A_f applied from
 //                 shared memory (copied in one step ahead); the dg_f parts
 //                 of its tile; dh0
-//   frame_tokgrad per (sequence x head, 64-token chunk): U = K Lam, E = X -
-//                 K P, dv, dbeta, dk = beta (E Lam^T - U P^T), dq = [dO |
-//                 dden] R^T on tensor cores, and dg_frame from the parts
+//   frame_tokgrad per (sequence x head, 1 to 4 chunks of one frame): U = K
+//                 Lam, E = X - K P, dv, dbeta, dk = beta (E Lam^T - U P^T),
+//                 dq = [dO | dden] R^T on tensor cores, and dg_frame from
+//                 the parts
 // The two directions of a bidirectional pass run one after the other, the
-// second adding into the outputs.
+// second adding into the first's outputs (reductions for the per-token
+// gradients).
 #include "gdn_frame_bwd.cuh"
 #include "gdn_mma.cuh"
 
