@@ -20,8 +20,8 @@
 //                S_f = A_f (e^{g_f} S_{f-1}) + B_f forward and / or reverse
 //                (the next A_f copied in while the current one is applied),
 //                the states each frame's outputs read summed over directions
-//   frame_out    per (sequence, head, 64-token chunk, 128-column block):
-//                O = Q S_f on tensor cores; the ones column gives den
+//   frame_out    per (sequence, head, up to 4 chunks of one frame, 128-column
+//                block): O = Q S_f on tensor cores; the ones column gives den
 #include "gdn_common.cuh"
 
 namespace gdn {
