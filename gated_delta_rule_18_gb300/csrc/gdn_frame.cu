@@ -30,12 +30,6 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kKS = kKP + 8;  // bf16 row stride of a 128-key tile
-constexpr int kXS = 64 + 8;   // bf16 row stride of a 64-column tile
-
-__device__ __forceinline__ const bf16 *row_ptr(const void *base, int64_t sb, int64_t st, int64_t sh, int b,
-                                               int64_t t, int h) {
-    return (const bf16 *)base + b * sb + t * st + h * sh;
-}
 
 // ---------------------------------------------------------------- gram ---
 // One CTA (8 warps) per (sequence x head, frame, 128-column block of
